@@ -1,0 +1,213 @@
+"""fp64 CPU oracle for the causal differential-attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The product library never loads it and shares no code with it.
+
+The arithmetic lives in ``diffattn_oracle.c`` (plain loops in double
+precision); this module compiles it with gcc, loads it with ctypes and
+converts numpy / torch arrays to contiguous float64.
+
+Citations (page titles as printed):
+  * "Differential Transformer V2" -- pseudo-code ``DiffAttnV1`` and
+    ``DiffAttnV2`` (lam_init schedule, lambda re-parameterisation, rmsnorm,
+    (1 - lam_init) scale, paired heads ``attn[:,0::2] - sigmoid(lam)*attn[:,1::2]``,
+    GQA groups contiguous, decoding is memory-bound).
+  * "How best to implement a differential transformer?" (nanoGPT issue 567) --
+    ``RMSNorm(2*head_dim, eps=1e-5, elementwise_affine=False)``, causal mask,
+    1/sqrt(head_dim) score scale, head pairing (2h, 2h+1).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` (closed forms,
+library attention routines, invariants, brute force); none is parity-unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "diffattn_oracle.c")
+_LIB = os.path.join(_HERE, "_liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/_liboracle.so`` (gcc, -O2, no fast-math)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            dp = ctypes.POINTER(ctypes.c_double)
+            i64p = ctypes.POINTER(ctypes.c_int64)
+            lib.oracle_lambda_init.restype = ctypes.c_double
+            lib.oracle_lambda_init.argtypes = [ctypes.c_int]
+            lib.oracle_lambda_full.restype = ctypes.c_double
+            lib.oracle_lambda_full.argtypes = [dp, dp, dp, dp, ctypes.c_int, ctypes.c_double]
+            lib.oracle_rmsnorm.restype = None
+            lib.oracle_rmsnorm.argtypes = [dp, ctypes.c_int, ctypes.c_double, dp]
+            lib.oracle_v1_fwd.restype = ctypes.c_int
+            lib.oracle_v1_fwd.argtypes = [dp] * 9 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64, dp, ctypes.c_int]
+            lib.oracle_v2_fwd.restype = ctypes.c_int
+            lib.oracle_v2_fwd.argtypes = [dp] * 4 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64, dp, ctypes.c_int]
+            lib.oracle_v2_decode.restype = ctypes.c_int
+            lib.oracle_v2_decode.argtypes = ([dp] * 4 + [ctypes.c_int, ctypes.c_int64] + [ctypes.c_int] * 3
+                                             + [i64p, ctypes.c_int64, dp, ctypes.c_int])
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _f64(x) -> np.ndarray:
+    """Any numpy array or CPU torch tensor (fp32/bf16/fp64) -> contiguous float64."""
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _rows(rows):
+    if rows is None:
+        return None, None, 0
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    return r, r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), r.size
+
+
+def lambda_init(layer_index: int) -> float:
+    """lam_init = 0.8 - 0.6 exp(-0.3 layer_index) ("Differential Transformer V2", DiffAttnV1)."""
+    return _load().oracle_lambda_init(int(layer_index))
+
+
+def lambda_full(lq1, lk1, lq2, lk2, layer_index: int) -> float:
+    """lam = exp(sum(lq1*lk1)) - exp(sum(lq2*lk2)) + lam_init ("Differential Transformer V2")."""
+    a = [_f64(x) for x in (lq1, lk1, lq2, lk2)]
+    return _load().oracle_lambda_full(*[_ptr(x) for x in a], a[0].size, lambda_init(layer_index))
+
+
+def rmsnorm(x, eps: float = 1e-5) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) over the last axis, no affine weight (nanoGPT issue 567, subln)."""
+    x = _f64(x)
+    flat = x.reshape(-1, x.shape[-1])
+    out = np.empty_like(flat)
+    lib = _load()
+    for r in range(flat.shape[0]):
+        lib.oracle_rmsnorm(_ptr(flat[r]), flat.shape[1], float(eps), _ptr(out[r]))
+    return out.reshape(x.shape)
+
+
+def v1_fwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, layer_index: int,
+           rows=None, nthreads: int | None = None) -> np.ndarray:
+    """DIFF V1 causal forward ("Differential Transformer V2", DiffAttnV1).
+
+    q1, q2, k1, k2: (B, T, H, d); v: (B, T, H, 2d); lambda vectors: (d,).
+    rows=None returns (B, T, H, 2d); otherwise ``rows`` holds flat ids
+    (b*T + t)*H + h and the result is (len(rows), 2d).
+    """
+    q1, q2, k1, k2, v = (_f64(x) for x in (q1, q2, k1, k2, v))
+    lq1, lk1, lq2, lk2 = (_f64(x) for x in (lq1, lk1, lq2, lk2))
+    B, T, H, d = q1.shape
+    assert v.shape == (B, T, H, 2 * d), v.shape
+    for x in (q2, k1, k2):
+        assert x.shape == (B, T, H, d)
+    r, rp, n = _rows(rows)
+    out = np.empty(((n if r is not None else B * T * H), 2 * d), dtype=np.float64)
+    rc = _load().oracle_v1_fwd(_ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
+                               _ptr(lq1), _ptr(lk1), _ptr(lq2), _ptr(lk2),
+                               B, T, H, d, int(layer_index), rp, n, _ptr(out),
+                               nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_v1_fwd failed ({rc})")
+    return out if r is not None else out.reshape(B, T, H, 2 * d)
+
+
+def v2_fwd(q, k, v, lam, rows=None, nthreads: int | None = None) -> np.ndarray:
+    """DIFF V2 causal prefill ("Differential Transformer V2", DiffAttnV2).
+
+    q: (B, T, Hq, D); k, v: (B, T, Hkv, D); lam: (B, T, Hq/2) logits.
+    rows=None returns (B, T, Hq/2, D); otherwise flat ids (b*T + t)*(Hq/2) + i.
+    """
+    q, k, v, lam = (_f64(x) for x in (q, k, v, lam))
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    assert Hq % 2 == 0 and Hq % Hkv == 0 and (Hq // Hkv) % 2 == 0
+    assert k.shape == (B, T, Hkv, D) and v.shape == (B, T, Hkv, D)
+    assert lam.shape == (B, T, Hq // 2)
+    r, rp, n = _rows(rows)
+    out = np.empty(((n if r is not None else B * T * (Hq // 2)), D), dtype=np.float64)
+    rc = _load().oracle_v2_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(lam), B, T, Hq, Hkv, D,
+                               rp, n, _ptr(out), nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_v2_fwd failed ({rc})")
+    return out if r is not None else out.reshape(B, T, Hq // 2, D)
+
+
+def v2_decode(q, k_cache, v_cache, lam, rows=None, nthreads: int | None = None) -> np.ndarray:
+    """DIFF V2 single-token decode against an L-row KV cache.
+
+    q: (B, Hq, D); caches: (B, L, Hkv, D); lam: (B, Hq/2).
+    rows=None returns (B, Hq/2, D); otherwise flat ids b*(Hq/2) + i.
+    """
+    q, k, v, lam = (_f64(x) for x in (q, k_cache, v_cache, lam))
+    B, Hq, D = q.shape
+    L, Hkv = k.shape[1], k.shape[2]
+    assert Hq % Hkv == 0 and (Hq // Hkv) % 2 == 0
+    assert k.shape == (B, L, Hkv, D) and v.shape == (B, L, Hkv, D)
+    assert lam.shape == (B, Hq // 2)
+    r, rp, n = _rows(rows)
+    out = np.empty(((n if r is not None else B * (Hq // 2)), D), dtype=np.float64)
+    rc = _load().oracle_v2_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(lam), B, L, Hq, Hkv, D,
+                                  rp, n, _ptr(out), nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_v2_decode failed ({rc})")
+    return out if r is not None else out.reshape(B, Hq // 2, D)
+
+
+def decode_gather(q, k_cache, v_cache, lam, rows):
+    """Copy only the cache slices that the listed decode rows read.
+
+    The decode oracle for row (b, i) touches k/v[b, :, g] with g = 2i/G.  For
+    very large caches this returns small contiguous inputs (one batch entry,
+    one kv head per listed row) and the row ids that address them, so that
+    sampled rows can be checked without converting the whole cache to fp64.
+    """
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    G = Hq // Hkv
+    P = Hq // 2
+    out = []
+    for rid in np.asarray(rows, dtype=np.int64).reshape(-1):
+        b, i = int(rid) // P, int(rid) % P
+        g = (2 * i) // G
+        qs = q[b:b + 1, g * G:(g + 1) * G]               # (1, G, D)
+        ks = k_cache[b:b + 1, :, g:g + 1]                 # (1, L, 1, D)
+        vs = v_cache[b:b + 1, :, g:g + 1]
+        ls = lam[b:b + 1, g * G // 2:(g + 1) * G // 2]    # (1, G/2)
+        local = i - g * G // 2
+        out.append((qs, ks, vs, ls, local))
+    return out
