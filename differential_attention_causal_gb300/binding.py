@@ -1,0 +1,191 @@
+"""ctypes binding over libdiffattn.so (the C ABI in include/diffattn.h).
+
+Argument marshalling only: every step of the differential-attention forward
+runs in the library's CUDA kernels.  torch is used for device memory and the
+current CUDA stream.  If the library is missing this module raises at first
+use -- there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdiffattn.so")
+
+DA_F32, DA_BF16 = 0, 1
+STATUS = {
+    0: "DA_OK", 1: "DA_ERR_NULL_PTR", 2: "DA_ERR_BAD_SHAPE", 3: "DA_ERR_UNSUPPORTED_DIM",
+    4: "DA_ERR_BAD_GROUP", 5: "DA_ERR_MISALIGNED", 6: "DA_ERR_WORKSPACE_TOO_SMALL",
+    7: "DA_ERR_CUDA", 8: "DA_ERR_BAD_DTYPE", 9: "DA_ERR_DEVICE_TIMEOUT",
+}
+_lock = threading.Lock()
+_lib = None
+
+
+class DiffAttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}: {status_string(code)}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdiffattn.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} not found: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, fp, i32, i64 = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+            L.diffattn_v1_fwd.restype = i32
+            L.diffattn_v1_fwd.argtypes = ([vp] * 5 + [fp] * 4 + [vp] + [i32] * 5 + [i64] * 12 + [i32, vp])
+            L.diffattn_v2_fwd.restype = i32
+            L.diffattn_v2_fwd.argtypes = [vp, vp, vp, fp, vp] + [i32] * 5 + [i32, vp]
+            L.diffattn_v2_decode_workspace_size.restype = ctypes.c_size_t
+            L.diffattn_v2_decode_workspace_size.argtypes = [i32] * 6
+            L.diffattn_v2_decode.restype = i32
+            L.diffattn_v2_decode.argtypes = ([vp, vp, vp, fp, vp, vp, ctypes.c_size_t] + [i32] * 5 + [i32, vp])
+            L.diffattn_status_string.restype = ctypes.c_char_p
+            L.diffattn_status_string.argtypes = [i32]
+            L.diffattn_device_error.restype = i32
+            L.diffattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.diffattn_last_launch_count.restype = i32
+            L.diffattn_last_launch_count.argtypes = []
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().diffattn_status_string(int(code)).decode()
+
+
+def last_launch_count() -> int:
+    """Kernel launches enqueued by the last successful call on this thread."""
+    return lib().diffattn_last_launch_count()
+
+
+def device_error() -> int:
+    """Synchronise, then read and clear the device error word (0 = no kernel gave up)."""
+    code = ctypes.c_uint32(0)
+    rc = lib().diffattn_device_error(ctypes.byref(code))
+    if rc not in (0, 9):
+        raise DiffAttnError("diffattn_device_error", rc)
+    return int(code.value)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DA_BF16
+    if t.dtype == torch.float32:
+        return DA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+
+
+def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise DiffAttnError(fn, rc)
+
+
+def v1_fwd(q1, q2, k1, k2, v, lam_q1, lam_k1, lam_q2, lam_k2, layer_index: int,
+           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """DIFF V1 causal forward ("Differential Transformer V2", DiffAttnV1).
+
+    q1, q2, k1, k2: (B, T, H, d) CUDA tensors with the last dim contiguous
+    (strided views such as q[:, :, 0::2] of an interleaved (B, T, 2H, d)
+    tensor are passed as is); q1/q2 and k1/k2 must share strides.
+    v: (B, T, H, 2d).  lam_*: fp32 (d,).  Returns out (B, T, H, 2d).
+    """
+    for n, t in (("q1", q1), ("q2", q2), ("k1", k1), ("k2", k2), ("v", v)):
+        _cuda(t, n)
+    B, T, H, d = q1.shape
+    if out is None:
+        out = torch.empty((B, T, H, 2 * d), dtype=q1.dtype, device=q1.device)
+    if q1.stride() != q2.stride() or k1.stride() != k2.stride():
+        raise ValueError("q1/q2 and k1/k2 must share strides")
+    for t in (q1, k1, v, out):
+        if t.stride(-1) != 1:
+            raise ValueError("head dimension must be contiguous")
+    lams = [x.contiguous() for x in (lam_q1, lam_k1, lam_q2, lam_k2)]
+    for x in lams:
+        if x.dtype != torch.float32 or not x.is_cuda or x.numel() != d:
+            raise ValueError("lambda vectors must be fp32 CUDA tensors of length d")
+    dt = _dtype_code(q1)
+    qs, ks, vs, os_ = q1.stride(), k1.stride(), v.stride(), out.stride()
+    rc = lib().diffattn_v1_fwd(
+        q1.data_ptr(), q2.data_ptr(), k1.data_ptr(), k2.data_ptr(), v.data_ptr(),
+        *[x.data_ptr() for x in lams], out.data_ptr(),
+        B, T, H, d, int(layer_index),
+        qs[0], qs[1], qs[2], ks[0], ks[1], ks[2], vs[0], vs[1], vs[2], os_[0], os_[1], os_[2],
+        dt, _stream(stream))
+    _check("diffattn_v1_fwd", rc)
+    return out
+
+
+def v2_fwd(q, k, v, lam, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """DIFF V2 causal prefill ("Differential Transformer V2", DiffAttnV2).
+
+    q: (B, T, Hq, D), k, v: (B, T, Hkv, D), lam: (B, T, Hq/2) fp32 logits,
+    all contiguous CUDA tensors.  Returns out (B, T, Hq/2, D).
+    """
+    for n, t in (("q", q), ("k", k), ("v", v), ("lam", lam)):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if lam.dtype != torch.float32:
+        raise ValueError("lam must be fp32")
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty((B, T, Hq // 2, D), dtype=q.dtype, device=q.device)
+    rc = lib().diffattn_v2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), out.data_ptr(),
+                               B, T, Hq, Hkv, D, _dtype_code(q), _stream(stream))
+    _check("diffattn_v2_fwd", rc)
+    return out
+
+
+def decode_workspace_size(B: int, L: int, Hq: int, Hkv: int, D: int, dtype=torch.bfloat16) -> int:
+    code = DA_BF16 if dtype == torch.bfloat16 else DA_F32
+    return int(lib().diffattn_v2_decode_workspace_size(B, L, Hq, Hkv, D, code))
+
+
+def v2_decode(q, k_cache, v_cache, lam, out: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """DIFF V2 single-token decode against a KV cache.
+
+    q: (B, Hq, D); k_cache, v_cache: (B, L, Hkv, D); lam: (B, Hq/2) fp32.
+    workspace: optional uint8 CUDA tensor of at least decode_workspace_size()
+    bytes (allocated here with torch when omitted).  Returns out (B, Hq/2, D).
+    """
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("lam", lam)):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, Hq, D = q.shape
+    L, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq // 2, D), dtype=q.dtype, device=q.device)
+    need = decode_workspace_size(B, L, Hq, Hkv, D, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = lib().diffattn_v2_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), lam.data_ptr(),
+                                  out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                  B, L, Hq, Hkv, D, _dtype_code(q), _stream(stream))
+    _check("diffattn_v2_decode", rc)
+    return out

@@ -1,0 +1,307 @@
+// da_api.cu -- the C ABI of libdiffattn.so (declared in include/diffattn.h).
+//
+// Host side only: argument checks (nothing is enqueued when one fails), TMA
+// tensor-map encoding, the device error word, and the launch of the kernels
+// in k_prefill.cu (tcgen05 prefill), k_decode.cu (split-KV decode) and
+// k_simt.cu (fp32).  The library allocates no memory.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "da_internal.h"
+#include "diffattn.h"
+
+namespace da {
+
+// Sticky device error word, set by bounded waits that give up.
+__device__ uint32_t g_err_word;
+
+namespace {
+
+thread_local int t_last_launches = 0;
+
+std::mutex g_mu;
+uint32_t *g_err_ptr[64];   // per-device address of g_err_word
+int g_num_sms[64];
+
+// Address of this device's error word (looked up once per device, with that
+// device current).
+bool device_state(uint32_t **err, int *num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess || !p) return false;
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            return false;
+        g_err_ptr[dev] = static_cast<uint32_t *>(p);
+        g_num_sms[dev] = n;
+    }
+    *err = g_err_ptr[dev];
+    if (num_sms) *num_sms = g_num_sms[dev];
+    return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_ok(int64_t s, int esize) { return s > 0 && ((s * esize) % 16) == 0 && s < (int64_t(1) << 36); }
+
+da_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DA_OK : DA_ERR_CUDA; }
+
+}  // namespace
+
+bool encode_map_4d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t d1, uint64_t d2, uint64_t d3,
+                   int64_t s1, int64_t s2, int64_t s3, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {inner, d1, d2, d3};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(s1) * 2, static_cast<cuuint64_t>(s2) * 2,
+                             static_cast<cuuint64_t>(s3) * 2};
+    cuuint32_t box[4] = {64, 1, box_rows, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    std::memset(m, 0, sizeof(*m));
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace da
+
+using namespace da;
+
+extern "C" {
+
+const char *diffattn_status_string(da_status s) {
+    switch (s) {
+        case DA_OK: return "ok";
+        case DA_ERR_NULL_PTR: return "a required pointer is NULL";
+        case DA_ERR_BAD_SHAPE: return "a size is out of range";
+        case DA_ERR_UNSUPPORTED_DIM: return "head dimension not supported for this dtype";
+        case DA_ERR_BAD_GROUP: return "Hq must be a multiple of Hkv with an even group size (<= 8 for bf16 decode)";
+        case DA_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+        case DA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case DA_ERR_CUDA: return "CUDA error";
+        case DA_ERR_BAD_DTYPE: return "unknown dtype";
+        case DA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (device error word set)";
+    }
+    return "unknown status";
+}
+
+int diffattn_last_launch_count(void) { return t_last_launches; }
+
+da_status diffattn_device_error(uint32_t *code) {
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
+    if (v != 0 && cudaMemset(err, 0, sizeof(v)) != cudaSuccess) return DA_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
+    if (code) *code = v;
+    return v ? DA_ERR_DEVICE_TIMEOUT : DA_OK;
+}
+
+da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const void *k2, const void *v,
+                          const float *lam_q1, const float *lam_k1, const float *lam_q2, const float *lam_k2,
+                          void *out, int B, int T, int H, int d, int layer_index,
+                          int64_t q_sb, int64_t q_st, int64_t q_sh, int64_t k_sb, int64_t k_st, int64_t k_sh,
+                          int64_t v_sb, int64_t v_st, int64_t v_sh, int64_t o_sb, int64_t o_st, int64_t o_sh,
+                          da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q1 || !q2 || !k1 || !k2 || !v || !lam_q1 || !lam_k1 || !lam_q2 || !lam_k2 || !out)
+        return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
+    const int es = dtype == DA_BF16 ? 2 : 4;
+    if (dtype == DA_BF16 ? !prefill_supported(d, 2 * d, false) : (d != 32 && d != 64 && d != 128))
+        return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q1, q2, k1, k2, v, static_cast<const void *>(out)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    for (int64_t s : {q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh, o_sb, o_st, o_sh})
+        if (!stride_ok(s, es)) return DA_ERR_MISALIGNED;
+    uint32_t *err = nullptr;
+    int nsm = 0;
+    if (!device_state(&err, &nsm)) return DA_ERR_CUDA;
+    t_last_launches = 0;
+    if (dtype == DA_F32) {
+        SimtParams p{};
+        p.q1 = static_cast<const float *>(q1); p.q2 = static_cast<const float *>(q2);
+        p.k1 = static_cast<const float *>(k1); p.k2 = static_cast<const float *>(k2);
+        p.v = static_cast<const float *>(v);
+        p.q_sb = q_sb; p.q_st = q_st; p.q_sh = q_sh;
+        p.k_sb = k_sb; p.k_st = k_st; p.k_sh = k_sh;
+        p.v_sb = v_sb; p.v_st = v_st; p.v_sh = v_sh;
+        p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
+        p.out = static_cast<float *>(out);
+        p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+        p.layer_index = layer_index;
+        p.B = B; p.Tq = T; p.Lk = T; p.H = H; p.G = 1; p.mode = 1;
+        p.err = err;
+        const da_status st = cuda_status(launch_simt(p, d, 2 * d, stream));
+        if (st == DA_OK) t_last_launches = 1;
+        return st;
+    }
+    PrefillMaps m;
+    const uint64_t uT = static_cast<uint64_t>(T), uH = static_cast<uint64_t>(H), uB = static_cast<uint64_t>(B);
+    if (!encode_map_4d(&m.q1, q1, d, uH, uT, uB, q_sh, q_st, q_sb, 128) ||
+        !encode_map_4d(&m.q2, q2, d, uH, uT, uB, q_sh, q_st, q_sb, 128) ||
+        !encode_map_4d(&m.k1, k1, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
+        !encode_map_4d(&m.k2, k2, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
+        !encode_map_4d(&m.v, v, 2 * d, uH, uT, uB, v_sh, v_st, v_sb, 128))
+        return DA_ERR_CUDA;
+    PrefillParams p{};
+    p.out = out; p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
+    p.lam = nullptr;
+    p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+    p.layer_index = layer_index;
+    p.B = B; p.T = T; p.H = H; p.G = 1;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
+    p.err = err;
+    const da_status st = cuda_status(launch_prefill(m, p, d, 2 * d, false, stream));
+    if (st == DA_OK) t_last_launches = 1;
+    return st;
+}
+
+da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const float *lam, void *out, int B, int T,
+                          int Hq, int Hkv, int D, da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q || !k || !v || !lam || !out) return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || Hq < 2 || Hkv < 1) return DA_ERR_BAD_SHAPE;
+    if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
+    if (D != 64 && D != 128) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q, k, v, static_cast<const void *>(out)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    const int P = Hq / 2, G = Hq / Hkv;
+    t_last_launches = 0;
+    if (dtype == DA_F32) {
+        SimtParams p{};
+        p.q1 = p.q2 = static_cast<const float *>(q);
+        p.k1 = p.k2 = static_cast<const float *>(k);
+        p.v = static_cast<const float *>(v);
+        p.q_sh = D; p.q_st = static_cast<int64_t>(Hq) * D; p.q_sb = p.q_st * T;
+        p.k_sh = D; p.k_st = static_cast<int64_t>(Hkv) * D; p.k_sb = p.k_st * T;
+        p.v_sh = p.k_sh; p.v_st = p.k_st; p.v_sb = p.k_sb;
+        p.o_sh = D; p.o_st = static_cast<int64_t>(P) * D; p.o_sb = p.o_st * T;
+        p.out = static_cast<float *>(out);
+        p.lam = lam; p.lam_st = P; p.lam_sb = static_cast<int64_t>(P) * T;
+        p.B = B; p.Tq = T; p.Lk = T; p.H = P; p.G = G; p.mode = 2;
+        p.err = err;
+        const da_status st = cuda_status(launch_simt(p, D, D, stream));
+        if (st == DA_OK) t_last_launches = 1;
+        return st;
+    }
+    PrefillMaps m;
+    const uint64_t uT = static_cast<uint64_t>(T), uB = static_cast<uint64_t>(B);
+    const int64_t qst = static_cast<int64_t>(Hq) * D, kst = static_cast<int64_t>(Hkv) * D;
+    if (!encode_map_4d(&m.q1, q, D, Hq, uT, uB, D, qst, qst * T, 128) ||
+        !encode_map_4d(&m.k1, k, D, Hkv, uT, uB, D, kst, kst * T, 128) ||
+        !encode_map_4d(&m.v, v, D, Hkv, uT, uB, D, kst, kst * T, 128))
+        return DA_ERR_CUDA;
+    m.q2 = m.q1;
+    m.k2 = m.k1;
+    PrefillParams p{};
+    p.out = out;
+    p.o_sh = D; p.o_st = static_cast<int64_t>(P) * D; p.o_sb = p.o_st * T;
+    p.lam = lam;
+    p.B = B; p.T = T; p.H = P; p.G = G;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.err = err;
+    const da_status st = cuda_status(launch_prefill(m, p, D, D, true, stream));
+    if (st == DA_OK) t_last_launches = 1;
+    return st;
+}
+
+size_t diffattn_v2_decode_workspace_size(int B, int L, int Hq, int Hkv, int D, da_dtype dtype) {
+    if (dtype == DA_F32) return 0;
+    if (dtype != DA_BF16 || Hkv < 1 || Hq % Hkv != 0) return 0;
+    uint32_t *err = nullptr;
+    int nsm = 0;
+    if (!device_state(&err, &nsm)) return 0;
+    int grid, max_seg, spb;
+    int64_t units;
+    size_t ws = 0;
+    if (!decode_plan(B, L, Hq, Hkv, D, nsm, &grid, &max_seg, &units, &spb, &ws)) return 0;
+    return ws;
+}
+
+da_status diffattn_v2_decode(const void *q, const void *k_cache, const void *v_cache, const float *lam, void *out,
+                             void *workspace, size_t workspace_bytes, int B, int L, int Hq, int Hkv, int D,
+                             da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q || !k_cache || !v_cache || !lam || !out) return DA_ERR_NULL_PTR;
+    if (B < 1 || L < 1 || Hq < 2 || Hkv < 1) return DA_ERR_BAD_SHAPE;
+    if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
+    if (D != 64 && D != 128) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q, k_cache, v_cache, static_cast<const void *>(out)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    uint32_t *err = nullptr;
+    int nsm = 0;
+    if (!device_state(&err, &nsm)) return DA_ERR_CUDA;
+    const int P = Hq / 2, G = Hq / Hkv;
+    t_last_launches = 0;
+    if (dtype == DA_F32) {
+        SimtParams p{};
+        p.q1 = p.q2 = static_cast<const float *>(q);
+        p.k1 = p.k2 = static_cast<const float *>(k_cache);
+        p.v = static_cast<const float *>(v_cache);
+        p.q_sh = D; p.q_st = 0; p.q_sb = static_cast<int64_t>(Hq) * D;
+        p.k_sh = D; p.k_st = static_cast<int64_t>(Hkv) * D; p.k_sb = p.k_st * L;
+        p.v_sh = p.k_sh; p.v_st = p.k_st; p.v_sb = p.k_sb;
+        p.o_sh = D; p.o_st = 0; p.o_sb = static_cast<int64_t>(P) * D;
+        p.out = static_cast<float *>(out);
+        p.lam = lam; p.lam_st = 0; p.lam_sb = P;
+        p.B = B; p.Tq = 1; p.Lk = L; p.H = P; p.G = G; p.mode = 2;
+        p.err = err;
+        const da_status st = cuda_status(launch_simt(p, D, D, stream));
+        if (st == DA_OK) t_last_launches = 1;
+        return st;
+    }
+    if (G > 8) return DA_ERR_BAD_GROUP;
+    int grid, max_seg, spb;
+    int64_t units;
+    size_t need = 0;
+    if (!decode_plan(B, L, Hq, Hkv, D, nsm, &grid, &max_seg, &units, &spb, &need)) return DA_ERR_BAD_SHAPE;
+    if (!workspace) return DA_ERR_NULL_PTR;
+    if (!aligned16(workspace)) return DA_ERR_MISALIGNED;
+    if (workspace_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
+    DecodeMaps m;
+    const int64_t st_row = static_cast<int64_t>(Hkv) * D;
+    if (!encode_map_4d(&m.k, k_cache, D, Hkv, static_cast<uint64_t>(L), B, D, st_row, st_row * L,
+                       kDecodeKeysPerUnit) ||
+        !encode_map_4d(&m.v, v_cache, D, Hkv, static_cast<uint64_t>(L), B, D, st_row, st_row * L,
+                       kDecodeKeysPerUnit))
+        return DA_ERR_CUDA;
+    DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.lam = lam;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.ws = static_cast<float *>(workspace);
+    p.B = B; p.L = L; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.D = D;
+    p.grid = grid; p.max_seg = max_seg; p.units = units; p.spb = spb;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.err = err;
+    const da_status st = cuda_status(launch_decode(m, p, stream));
+    if (st == DA_OK) t_last_launches = 2;
+    return st;
+}
+
+}  // extern "C"

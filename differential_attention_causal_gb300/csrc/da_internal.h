@@ -1,0 +1,81 @@
+// da_internal.h -- parameter blocks and launchers shared between the C-ABI
+// host code (da_api.cu) and the kernel translation units.  Not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace da {
+
+// ---------------------------------------------------------------- SIMT fp32
+// One warp per output row.  mode 1 = DIFF V1, mode 2 = DIFF V2 (prefill or
+// decode).  Query t attends keys 0 .. t + (Lk - Tq): Lk == Tq is the causal
+// prefill, Tq == 1 is decode against Lk cached rows.
+struct SimtParams {
+    const float *q1, *q2, *k1, *k2, *v;
+    int64_t q_sb, q_st, q_sh;
+    int64_t k_sb, k_st, k_sh;
+    int64_t v_sb, v_st, v_sh;
+    int64_t o_sb, o_st, o_sh;
+    float *out;
+    const float *lam;              // V2 logits at lam[b*lam_sb + t*lam_st + i]
+    int64_t lam_sb, lam_st;
+    const float *lq1, *lk1, *lq2, *lk2;
+    int layer_index;
+    int B, Tq, Lk, H, G, mode;
+    uint32_t *err;
+};
+cudaError_t launch_simt(const SimtParams &p, int dqk, int dv, cudaStream_t s);
+
+// ------------------------------------------------------- tcgen05 prefill
+// V1: H diff heads; tensor maps over q1, q2, k1, k2, v.
+// V2: H = Hq/2 pairs; tq1 == tq2 over q, tk1 == tk2 over k, G = Hq/Hkv.
+struct PrefillParams {
+    void *out;
+    int64_t o_sb, o_st, o_sh;      // elements
+    const float *lam;              // V2 logits (B, T, H) contiguous
+    const float *lq1, *lk1, *lq2, *lk2;
+    int layer_index;
+    int B, T, H, G;
+    float scale_log2;              // log2(e) / sqrt(dqk)
+    uint32_t *err;
+};
+struct PrefillMaps {
+    CUtensorMap q1, q2, k1, k2, v;
+};
+// dqk/dv in {64/128 (V1), 128/256 (V1 two-pass), 64/64, 128/128 (V2)}
+cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
+                           cudaStream_t s);
+bool prefill_supported(int dqk, int dv, bool v2);
+
+// --------------------------------------------------------------- decode
+struct DecodeParams {
+    const __nv_bfloat16 *q;        // (B, Hq, D)
+    const float *lam;              // (B, Hq/2)
+    __nv_bfloat16 *out;            // (B, Hq/2, D)
+    float *ws;                     // workspace (partials)
+    int B, L, Hq, Hkv, G, D;
+    int grid;                      // CTAs of the split kernel
+    int max_seg;                   // partial slots per CTA
+    int64_t units;                 // B * Hkv * ceil(L / 64)
+    int spb;                       // 64-key units per (b, kv head)
+    float scale_log2;
+    uint32_t *err;
+};
+struct DecodeMaps {
+    CUtensorMap k, v;
+};
+// Sizes the decode plan on the current device.  Returns false on bad sizes.
+bool decode_plan(int B, int L, int Hq, int Hkv, int D, int num_sms, int *grid, int *max_seg,
+                 int64_t *units, int *spb, size_t *ws_bytes);
+cudaError_t launch_decode(const DecodeMaps &m, const DecodeParams &p, cudaStream_t s);
+constexpr int kDecodeKeysPerUnit = 64;
+
+// Tensor-map helper (da_api.cu): 4-D bf16 map over (inner, d1, d2, d3) with
+// element strides s1, s2, s3, box (64, 1, box_rows, 1), 128-byte swizzle.
+bool encode_map_4d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t d1, uint64_t d2,
+                   uint64_t d3, int64_t s1, int64_t s2, int64_t s3, uint32_t box_rows);
+
+}  // namespace da

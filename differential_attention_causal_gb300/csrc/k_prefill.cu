@@ -1,0 +1,415 @@
+// k_prefill.cu -- fused causal differential-attention prefill on tcgen05
+// tensor cores (bf16 in, fp32 accumulate), DIFF V1 and DIFF V2.
+//
+// "Differential Transformer V2": DiffAttnV1 computes two causal attentions
+// attn_b = softmax(Q_b K_b^T / sqrt(d)) V over one shared V (2d wide) and
+// returns RMSNorm(attn1 - lam attn2) (1 - lam_init); DiffAttnV2 runs one GQA
+// attention whose even / odd query heads of a group share K and V and returns
+// attn[:,0::2] - sigmoid(lam) attn[:,1::2].  Both are the same shape of work:
+// two branches (Q1,K1) and (Q2,K2) against one V, combined per row at the end.
+//
+// One CTA = 128 query rows of one diff head (V1) or one head pair (V2).
+//   warp 0      TMA producer: Q1, Q2 once; then K (K1 and K2 for V1) and V
+//               tiles of 128 keys into a 2-stage ring, causal tiles only.
+//   warp 1      TMEM owner and single-thread MMA issuer.
+//   warps 4-7   softmax for branch 1 (thread = query row = TMEM lane)
+//   warps 8-11  softmax for branch 2
+// TMEM (512 columns): S1 | S2 (128 fp32 columns each) | O1 | O2 (DV each).
+// Per KV tile j the MMA warp issues   PV1(j-1) S1(j) ... PV2(j-1) S2(j):
+//   S_b = Q_b K_b^T      (SS MMA, K-major operands, 128-byte swizzle)
+//   P_b (bf16) is written by the softmax threads over the first 64 columns
+//   of S_b, and O_b += P_b V is a TS MMA (A = P from TMEM, B = V MN-major).
+// While branch 1's threads exponentiate, the tensor core runs branch 2's
+// products and vice versa.  The online softmax keeps a per-row reference
+// max and rescales O only when the running max grows by more than 2^8; P
+// stays below 2^8 and the final division by l uses the same reference, so
+// the result is exact up to rounding.
+// Epilogue (same kernel): x = O1/l1 - c O2/l2 with c = lam (V1) or
+// sigmoid(lam[b,t,pair]) (V2); V1 then applies RMSNorm over the DV channels
+// (eps 1e-5) and the (1 - lam_init) scale; bf16 rows are stored directly.
+#include "da_common.cuh"
+#include "da_internal.h"
+
+namespace da {
+namespace {
+
+template <int DQK, int DV, bool V2>
+struct PreCfg {
+    static constexpr int BM = 128, BN = 128;
+    static constexpr int STAGES = 2;
+    static constexpr int QB = DQK / 64;                // 64-column boxes per Q/K tile
+    static constexpr int VB = DV / 64;
+    static constexpr int BOX = 128 * 128;              // bytes of one 128-row x 64-col box
+    static constexpr int Q_TILE = QB * BOX;
+    static constexpr int K_TILE = QB * BOX;
+    static constexpr int V_TILE = VB * BOX;
+    static constexpr int NK = V2 ? 1 : 2;              // K tiles per stage
+    static constexpr int STAGE = NK * K_TILE + V_TILE;
+    static constexpr int OFF_Q1 = 0;
+    static constexpr int OFF_Q2 = Q_TILE;
+    static constexpr int OFF_ST = 2 * Q_TILE;
+    static constexpr int OFF_X = OFF_ST + STAGES * STAGE;   // 4 x 128 floats exchange
+    static constexpr int OFF_BAR = OFF_X + 4 * 128 * 4;
+    // q, kfull[S], vfull[S], empty[S], s[2], p[2], o[2], drain
+    static constexpr int NBAR = 1 + 3 * STAGES + 7;
+    static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_TSLOT + 16 + 1024;      // + alignment slack
+    static constexpr int COL_S1 = 0, COL_S2 = BN, COL_O1 = 2 * BN, COL_O2 = 2 * BN + DV;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
+    static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, true);
+    static_assert(COL_O2 + DV <= 512, "TMEM budget");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t *err, bool ok) {
+    if (ok) ok = mbar_wait(bar, parity, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+template <int DQK, int DV, bool V2>
+__global__ void __launch_bounds__(384, 1)
+    prefill_onepass(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
+                    const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
+                    const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
+    using C = PreCfg<DQK, DV, V2>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // heaviest (last) query tiles first
+    const int n_qt = (p.T + C::BM - 1) / C::BM;
+    const int per_qt = p.H * p.B;
+    const int qt = n_qt - 1 - static_cast<int>(blockIdx.x) / per_qt;
+    const int rest = static_cast<int>(blockIdx.x) % per_qt;
+    const int h = rest % p.H, b = rest / p.H;
+    const int q0 = qt * C::BM;
+    const int n_kv = qt + 1;   // causal: key tiles 0..qt (BN == BM)
+    const int hq1 = V2 ? 2 * h : h, hq2 = V2 ? 2 * h + 1 : h;
+    const int hk = V2 ? (2 * h) / p.G : h;
+
+    const uint32_t bar_q = sbase + C::OFF_BAR;
+    const uint32_t bar_kf = bar_q + 8;
+    const uint32_t bar_vf = bar_kf + 8 * C::STAGES;
+    const uint32_t bar_em = bar_vf + 8 * C::STAGES;
+    const uint32_t bar_s = bar_em + 8 * C::STAGES;    // [2]
+    const uint32_t bar_p = bar_s + 16;                // [2]
+    const uint32_t bar_o = bar_p + 16;                // [2]
+    const uint32_t bar_dr = bar_o + 16;
+    const uint32_t tslot = sbase + C::OFF_TSLOT;
+    const uint32_t sQ1 = sbase + C::OFF_Q1, sQ2 = sbase + C::OFF_Q2;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar_kf + 8 * s, 1);
+            mbar_init(bar_vf + 8 * s, 1);
+            mbar_init(bar_em + 8 * s, 1);
+        }
+        for (int br = 0; br < 2; ++br) {
+            mbar_init(bar_s + 8 * br, 1);
+            mbar_init(bar_p + 8 * br, 128);
+            mbar_init(bar_o + 8 * br, 1);
+        }
+        mbar_init(bar_dr, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::OFF_TSLOT);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            prefetch_tmap(&tq1);
+            prefetch_tmap(&tk1);
+            prefetch_tmap(&tv);
+            if (!V2) {
+                prefetch_tmap(&tq2);
+                prefetch_tmap(&tk2);
+            }
+            mbar_arrive_expect_tx(bar_q, 2 * C::Q_TILE);
+#pragma unroll
+            for (int c = 0; c < C::QB; ++c) {
+                tma_load_4d(sQ1 + c * C::BOX, &tq1, bar_q, 64 * c, hq1, q0, b);
+                tma_load_4d(sQ2 + c * C::BOX, &tq2, bar_q, 64 * c, hq2, q0, b);
+            }
+            int j = 0;
+            for (; j < n_kv; ++j) {
+                const int st = j % C::STAGES;
+                if (j >= C::STAGES &&
+                    !mbar_wait(bar_em + 8 * st, static_cast<uint32_t>((j / C::STAGES - 1) & 1), p.err))
+                    break;
+                const uint32_t sk1 = sbase + C::OFF_ST + st * C::STAGE;
+                const uint32_t sk2 = sk1 + C::K_TILE;
+                const uint32_t sv = sk1 + C::NK * C::K_TILE;
+                mbar_arrive_expect_tx(bar_kf + 8 * st, C::NK * C::K_TILE);
+#pragma unroll
+                for (int c = 0; c < C::QB; ++c) {
+                    tma_load_4d(sk1 + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
+                    if (!V2) tma_load_4d(sk2 + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
+                }
+                mbar_arrive_expect_tx(bar_vf + 8 * st, C::V_TILE);
+#pragma unroll
+                for (int c = 0; c < C::VB; ++c)
+                    tma_load_4d(sv + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b);
+            }
+            // leave no copy in flight
+            mbar_wait(bar_q, 0, p.err);
+            for (int k = (j > C::STAGES ? j - C::STAGES : 0); k < j; ++k) {
+                mbar_wait(bar_kf + 8 * (k % C::STAGES), static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
+                mbar_wait(bar_vf + 8 * (k % C::STAGES), static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            auto stage_k1 = [&](int st) { return sbase + C::OFF_ST + st * C::STAGE; };
+            auto stage_k2 = [&](int st) { return sbase + C::OFF_ST + st * C::STAGE + (V2 ? 0 : C::K_TILE); };
+            auto stage_v = [&](int st) { return sbase + C::OFF_ST + st * C::STAGE + C::NK * C::K_TILE; };
+            auto issue_qk = [&](uint32_t dcol, uint32_t sq, uint32_t sk) {
+#pragma unroll
+                for (int ks = 0; ks < DQK / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::BOX + (ks & 3) * 32;
+                    mma_ss(tmem + dcol, sdesc_sw128(sq + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024),
+                           C::IDESC_QK, ks > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](uint32_t dcol, uint32_t pcol, uint32_t sv, bool acc) {
+#pragma unroll
+                for (int ks = 0; ks < C::BN / 16; ++ks)
+                    mma_ts(tmem + dcol, tmem + pcol + ks * 8, sdesc_sw128(sv + ks * 2048, C::BOX, 1024),
+                           C::IDESC_PV, (acc || ks > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kf, 0, p.err);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(C::COL_S1, sQ1, stage_k1(0));
+                mma_commit(bar_s);
+                issue_qk(C::COL_S2, sQ2, stage_k2(0));
+                mma_commit(bar_s + 8);
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int st = j % C::STAGES;
+                const uint32_t ph = static_cast<uint32_t>((j / C::STAGES) & 1);
+                ok = mbar_wait(bar_vf + 8 * st, ph, p.err) && mbar_wait(bar_p, j & 1, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(C::COL_O1, C::COL_S1, stage_v(st), j > 0);
+                const bool more = j + 1 < n_kv;
+                const int st1 = (j + 1) % C::STAGES;
+                if (more) {
+                    ok = mbar_wait(bar_kf + 8 * st1, static_cast<uint32_t>(((j + 1) / C::STAGES) & 1), p.err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(C::COL_S1, sQ1, stage_k1(st1));
+                    mma_commit(bar_s);
+                } else {
+                    mma_commit(bar_o);
+                }
+                ok = mbar_wait(bar_p + 8, j & 1, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(C::COL_O2, C::COL_S2, stage_v(st), j > 0);
+                mma_commit(bar_em + 8 * st);
+                if (more) {
+                    issue_qk(C::COL_S2, sQ2, stage_k2(st1));
+                    mma_commit(bar_s + 8);
+                } else {
+                    mma_commit(bar_o + 8);
+                }
+            }
+            // no MMA may be in flight when TMEM is released
+            mma_commit(bar_dr);
+            mbar_wait(bar_dr, 0, p.err);
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------------------- softmax
+        const int br = (warp - 4) >> 2;
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (br ? C::COL_S2 : C::COL_S1);
+        const uint32_t tO = tmem + lane_off + (br ? C::COL_O2 : C::COL_O1);
+        const uint32_t my_s = bar_s + 8 * br, my_p = bar_p + 8 * br, my_o = bar_o + 8 * br;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            ok = warp_wait(my_s, j & 1, p.err, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t s[C::BN];
+            tmem_ld32(tS + 0, s);
+            tmem_ld32(tS + 32, s + 32);
+            tmem_ld32(tS + 64, s + 64);
+            tmem_ld32(tS + 96, s + 96);
+            tmem_wait_ld();
+            const bool diag = (j == qt);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < C::BN; ++c) {
+                float x = __uint_as_float(s[c]) * p.scale_log2;
+                if (diag && c > row) x = -INFINITY;
+                s[c] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
+            }
+            const float m_new = fmaxf(m_ref, mx);
+            float alpha = 1.f;
+            const bool resc = m_new > m_ref + 8.f;
+            if (resc) {
+                alpha = ex2(m_ref - m_new);
+                l *= alpha;
+                m_ref = m_new;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                // O_b is quiescent: PV_b(j-1) completed before S_b(j) was signalled.
+#pragma unroll 1
+                for (int c0 = 0; c0 < DV; c0 += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + c0, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+                    tmem_st32(tO + c0, ov);
+                }
+                tmem_wait_st();
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < C::BN / 2; ++c) {
+                const float p0 = ex2(__uint_as_float(s[2 * c]) - m_ref);
+                const float p1 = ex2(__uint_as_float(s[2 * c + 1]) - m_ref);
+                rs += p0 + p1;
+                s[c] = pack_bf16(p0, p1);
+            }
+            l += rs;
+            tmem_st32(tS + 0, s);
+            tmem_st32(tS + 32, s + 32);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(my_p);
+        }
+
+        // ------------------------------------------------------- epilogue
+        ok = warp_wait(my_o, 0, p.err, ok);
+        tc_fence_after();
+        float *xch = reinterpret_cast<float *>(smem + C::OFF_X);
+        xch[br * 128 + row] = l;
+        named_bar_sync(1, 256);
+        const float l1 = xch[row], l2 = xch[128 + row];
+        const int t = q0 + row;
+        float lam_init = 0.f, c2;
+        if (V2) {
+            const float lg = (t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
+            c2 = 1.f / (1.f + __expf(-lg)) / l2;
+        } else {
+            float d1 = 0.f, d2 = 0.f;
+            for (int c = lane; c < DQK; c += 32) {
+                d1 = fmaf(p.lq1[c], p.lk1[c], d1);
+                d2 = fmaf(p.lq2[c], p.lk2[c], d2);
+            }
+            d1 = warp_sum(d1);
+            d2 = warp_sum(d2);
+            lam_init = 0.8f - 0.6f * expf(-0.3f * static_cast<float>(p.layer_index));
+            const float lam = expf(d1) - expf(d2) + lam_init;
+            c2 = lam / l2;
+        }
+        const float c1 = 1.f / l1;
+        constexpr int HALF = DV / 2;
+        const int col0 = br * HALF;
+        float x[HALF];
+        float ss = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < HALF; cc += 32) {
+            uint32_t a[32], bb[32];
+            tmem_ld32(tmem + lane_off + C::COL_O1 + col0 + cc, a);
+            tmem_ld32(tmem + lane_off + C::COL_O2 + col0 + cc, bb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float v = __uint_as_float(a[k]) * c1 - __uint_as_float(bb[k]) * c2;
+                x[cc + k] = v;
+                ss = fmaf(v, v, ss);
+            }
+        }
+        if (!V2) {
+            xch[256 + br * 128 + row] = ss;
+            named_bar_sync(1, 256);
+            const float ms = (xch[256 + row] + xch[384 + row]) * (1.f / static_cast<float>(DV));
+            const float r = (1.f - lam_init) * rsqrtf(ms + 1e-5f);
+#pragma unroll
+            for (int k = 0; k < HALF; ++k) x[k] *= r;
+        }
+        if (ok && t < p.T) {
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + static_cast<int64_t>(b) * p.o_sb +
+                                 static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh + col0;
+#pragma unroll
+            for (int k = 0; k < HALF; k += 8) {
+                uint4 v;
+                v.x = pack_bf16(x[k], x[k + 1]);
+                v.y = pack_bf16(x[k + 2], x[k + 3]);
+                v.z = pack_bf16(x[k + 4], x[k + 5]);
+                v.w = pack_bf16(x[k + 6], x[k + 7]);
+                *reinterpret_cast<uint4 *>(dst + k) = v;
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int DQK, int DV, bool V2>
+cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
+    using C = PreCfg<DQK, DV, V2>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static unsigned long long attr_done = 0;   // one bit per device
+    if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
+    }
+    const int n_qt = (p.T + C::BM - 1) / C::BM;
+    const long long grid = static_cast<long long>(n_qt) * p.H * p.B;
+    if (grid < 1 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    prefill_onepass<DQK, DV, V2><<<static_cast<unsigned>(grid), 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_supported(int dqk, int dv, bool v2) {
+    if (v2) return (dqk == 128 && dv == 128) || (dqk == 64 && dv == 64);
+    return dqk == 64 && dv == 128;
+}
+
+cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
+                           cudaStream_t s) {
+    if (v2 && dqk == 128 && dv == 128) return launch_t<128, 128, true>(m, p, s);
+    if (v2 && dqk == 64 && dv == 64) return launch_t<64, 64, true>(m, p, s);
+    if (!v2 && dqk == 64 && dv == 128) return launch_t<64, 128, false>(m, p, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace da

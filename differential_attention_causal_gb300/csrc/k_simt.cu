@@ -1,0 +1,140 @@
+// k_simt.cu -- fp32 differential attention on CUDA cores (dtype DA_F32).
+//
+// "Differential Transformer V2", DiffAttnV1 / DiffAttnV2: both branches are
+// plain causal softmax attentions; V1 combines them as
+// RMSNorm(a1 - lam a2) (1 - lam_init), V2 as a1 - sigmoid(lam) a2.
+//
+// One warp owns one output row.  Lanes split the head dimension; every key
+// costs one warp-wide dot-product reduction per branch and an exact online
+// softmax update (running max m, running sum l, rescaled accumulator).  This
+// path exists for fp32 accuracy (the tf32 tensor-core rate would not hold a
+// 1e-4 bound after the RMSNorm) and for the small fp32 workloads; it is not
+// the throughput path.
+#include "da_common.cuh"
+#include "da_internal.h"
+
+namespace da {
+namespace {
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
+    constexpr int NQ = DQK / 32;   // q/k elements per lane
+    constexpr int NV = DV / 32;    // v/out elements per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+    const int64_t nrows = static_cast<int64_t>(p.B) * p.Tq * p.H;
+    if (row >= nrows) return;
+    if (ld_volatile_u32(p.err) != 0) {   // an earlier kernel gave up: do not compute
+        if (lane == 0) atomicOr(p.err, kErrAborted);
+        return;
+    }
+    const int h = static_cast<int>(row % p.H);
+    const int t = static_cast<int>((row / p.H) % p.Tq);
+    const int b = static_cast<int>(row / (static_cast<int64_t>(p.H) * p.Tq));
+
+    // Head selection: V1 diff head h reads q1/k1 and q2/k2 at head h and v at
+    // head h; V2 pair h reads query heads 2h (kept) and 2h+1 (subtracted) and
+    // kv head 2h / G (heads of one GQA group are contiguous).
+    int hq1, hq2, hk;
+    if (p.mode == 1) { hq1 = h; hq2 = h; hk = h; }
+    else { hq1 = 2 * h; hq2 = 2 * h + 1; hk = (2 * h) / p.G; }
+
+    const float *q1 = p.q1 + b * p.q_sb + t * p.q_st + hq1 * p.q_sh;
+    const float *q2 = p.q2 + b * p.q_sb + t * p.q_st + hq2 * p.q_sh;
+    const float *k1 = p.k1 + b * p.k_sb + hk * p.k_sh;
+    const float *k2 = p.k2 + b * p.k_sb + hk * p.k_sh;
+    const float *vv = p.v + b * p.v_sb + hk * p.v_sh;
+
+    float qa[NQ], qb[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) { qa[i] = q1[lane + 32 * i]; qb[i] = q2[lane + 32 * i]; }
+    const float scale = rsqrtf(static_cast<float>(DQK));
+    float m1 = -INFINITY, m2 = -INFINITY, l1 = 0.f, l2 = 0.f;
+    float o1[NV], o2[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) { o1[i] = 0.f; o2[i] = 0.f; }
+
+    const int nkeys = t + (p.Lk - p.Tq) + 1;   // keys 0 .. t + (Lk - Tq)
+    for (int j = 0; j < nkeys; ++j) {
+        const float *kj1 = k1 + j * p.k_st;
+        const float *kj2 = k2 + j * p.k_st;
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int i = 0; i < NQ; ++i) {
+            s1 = fmaf(qa[i], kj1[lane + 32 * i], s1);
+            s2 = fmaf(qb[i], kj2[lane + 32 * i], s2);
+        }
+        s1 = warp_sum(s1) * scale;
+        s2 = warp_sum(s2) * scale;
+        const float n1 = fmaxf(m1, s1), n2 = fmaxf(m2, s2);
+        const float a1 = expf(m1 - n1), a2 = expf(m2 - n2);   // 0 on the first key
+        const float p1 = expf(s1 - n1), p2 = expf(s2 - n2);
+        l1 = l1 * a1 + p1;
+        l2 = l2 * a2 + p2;
+        m1 = n1;
+        m2 = n2;
+        const float *vj = vv + j * p.v_st;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const float x = vj[lane + 32 * i];
+            o1[i] = fmaf(p1, x, o1[i] * a1);
+            o2[i] = fmaf(p2, x, o2[i] * a2);
+        }
+    }
+
+    float *out = p.out + b * p.o_sb + t * p.o_st + h * p.o_sh;
+    if (p.mode == 1) {
+        // lam = exp(lq1 . lk1) - exp(lq2 . lk2) + lam_init ; lam_init = 0.8 - 0.6 exp(-0.3 layer)
+        float d1 = 0.f, d2 = 0.f;
+        for (int c = lane; c < DQK; c += 32) {
+            d1 = fmaf(p.lq1[c], p.lk1[c], d1);
+            d2 = fmaf(p.lq2[c], p.lk2[c], d2);
+        }
+        d1 = warp_sum(d1);
+        d2 = warp_sum(d2);
+        const float lam_init = 0.8f - 0.6f * expf(-0.3f * static_cast<float>(p.layer_index));
+        const float lam = expf(d1) - expf(d2) + lam_init;
+        const float i1 = 1.f / l1, i2 = lam / l2;
+        float x[NV], ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            x[i] = o1[i] * i1 - o2[i] * i2;
+            ss = fmaf(x[i], x[i], ss);
+        }
+        ss = warp_sum(ss);
+        // RMSNorm over the DV channels, eps 1e-5, no weight; then (1 - lam_init)
+        const float r = (1.f - lam_init) / sqrtf(ss / static_cast<float>(DV) + 1e-5f);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) out[lane + 32 * i] = x[i] * r;
+    } else {
+        const float lg = p.lam[b * p.lam_sb + t * p.lam_st + h];
+        const float sg = 1.f / (1.f + expf(-lg));
+        const float i1 = 1.f / l1, i2 = sg / l2;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) out[lane + 32 * i] = o1[i] * i1 - o2[i] * i2;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_simt(const SimtParams &p, int dqk, int dv, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(p.B) * p.Tq * p.H;
+    const int64_t blocks = (rows + 3) / 4;
+    if (blocks <= 0 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(128);
+    if (dqk == 32 && dv == 64) simt_fwd<32, 64><<<grid, block, 0, s>>>(p);
+    else if (dqk == 64 && dv == 128) simt_fwd<64, 128><<<grid, block, 0, s>>>(p);
+    else if (dqk == 128 && dv == 256) simt_fwd<128, 256><<<grid, block, 0, s>>>(p);
+    else if (dqk == 64 && dv == 64) simt_fwd<64, 64><<<grid, block, 0, s>>>(p);
+    else if (dqk == 128 && dv == 128) simt_fwd<128, 128><<<grid, block, 0, s>>>(p);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace da

@@ -1,0 +1,143 @@
+/*
+ * diffattn.h -- C ABI of libdiffattn.so: causal differential-attention forward
+ * on one GB300 (sm_103a).
+ *
+ * Operations (page titles as printed on the pages):
+ *   diffattn_v1_fwd     "Differential Transformer V2", pseudo-code DiffAttnV1:
+ *                       out = (1 - lam_init) * RMSNorm(softmax(Q1 K1^T / sqrt(d)) V
+ *                                                     - lam * softmax(Q2 K2^T / sqrt(d)) V)
+ *                       lam_init = 0.8 - 0.6 exp(-0.3 layer_index)
+ *                       lam = exp(sum(lam_q1*lam_k1)) - exp(sum(lam_q2*lam_k2)) + lam_init
+ *                       RMSNorm over the 2d channels of each (token, diff head),
+ *                       eps = 1e-5, no weight ("How best to implement a
+ *                       differential transformer?", first CausalSelfAttention, subln).
+ *   diffattn_v2_fwd     same page, pseudo-code DiffAttnV2: one causal GQA attention
+ *                       over Hq query heads, then out = attn[:, 0::2]
+ *                       - sigmoid(lam) * attn[:, 1::2] (heads of one GQA group are
+ *                       contiguous, so heads 2i and 2i+1 share kv head 2i/(Hq/Hkv)).
+ *   diffattn_v2_decode  same page, the decoding remark after DiffAttnV2: the V2
+ *                       operation for one new query token per sequence against an
+ *                       L-row KV cache (the token attends all L rows).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates and frees nothing and keeps no per-call state; it may be called
+ *     concurrently on different streams.
+ *   - The head dimension of every tensor is contiguous (stride 1).  Base pointers
+ *     must be 16-byte aligned and every other stride, in bytes, a multiple of 16.
+ *   - Softmax scale is fixed at 1/sqrt(d) (d = query/key head dim); causal mask
+ *     j <= i with queries and keys aligned at position 0 (prefill).
+ *   - dtype DA_BF16: bf16 q/k/v/out; softmax, lambda, norm and gate math in
+ *     fp32; prefill runs on the tcgen05 tensor-core kernels, decode on the
+ *     split-KV tensor-core kernel.  dtype DA_F32: fp32 everywhere on CUDA cores.
+ *     Lambda vectors and lambda logits are fp32 for both dtypes.
+ *   - `out` must not overlap any input.
+ *   - Arguments are checked on the host before anything is enqueued; on any
+ *     error the call returns a non-zero da_status and enqueues nothing.  A CUDA
+ *     launch error is returned as DA_ERR_CUDA.  Work is asynchronous on
+ *     `stream` (NULL = legacy default stream).
+ *   - Device-side waits are bounded: a kernel that gives up waiting records a
+ *     code in a device error word and returns; read it with
+ *     diffattn_device_error().
+ */
+#ifndef DIFFATTN_H
+#define DIFFATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DA_OK = 0,
+    DA_ERR_NULL_PTR = 1,          /* a required pointer is NULL                        */
+    DA_ERR_BAD_SHAPE = 2,         /* a size is < 1 or too large                         */
+    DA_ERR_UNSUPPORTED_DIM = 3,   /* head dim not supported for this dtype             */
+    DA_ERR_BAD_GROUP = 4,         /* Hq % Hkv != 0, Hq/Hkv odd, or too large for dtype  */
+    DA_ERR_MISALIGNED = 5,        /* pointer or stride breaks the 16-byte rule, or the  */
+                                  /* head dimension is not contiguous                   */
+    DA_ERR_WORKSPACE_TOO_SMALL = 6,
+    DA_ERR_CUDA = 7,              /* CUDA runtime / driver error                        */
+    DA_ERR_BAD_DTYPE = 8,
+    DA_ERR_DEVICE_TIMEOUT = 9     /* reported by diffattn_device_error()               */
+} da_status;
+
+typedef enum { DA_F32 = 0, DA_BF16 = 1 } da_dtype;
+
+/* DIFF V1 causal forward.
+ *   q1, q2, k1, k2 : (B, T, H, d) tensors given by base pointer + element strides
+ *                    (q_sb, q_st, q_sh) shared by q1 and q2, (k_sb, k_st, k_sh)
+ *                    shared by k1 and k2.  The nanoGPT-issue layout -- one
+ *                    interleaved (B, T, 2H, d) tensor, q1 = heads 0::2,
+ *                    q2 = heads 1::2 -- is q1 = q, q2 = q + d, q_sh = 2d,
+ *                    q_st = 2Hd, q_sb = 2HdT.
+ *   v              : (B, T, H, 2d), strides (v_sb, v_st, v_sh).
+ *   lam_q1 .. lam_k2 : fp32 device vectors of length d.
+ *   out            : (B, T, H, 2d), strides (o_sb, o_st, o_sh), dtype as inputs.
+ *   layer_index    : >= 0, used as given (0-based) in lam_init.
+ *   Supported: DA_BF16 with d in {64, 128};  DA_F32 with d in {32, 64, 128}.
+ */
+da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const void *k2,
+                          const void *v,
+                          const float *lam_q1, const float *lam_k1,
+                          const float *lam_q2, const float *lam_k2,
+                          void *out,
+                          int B, int T, int H, int d, int layer_index,
+                          int64_t q_sb, int64_t q_st, int64_t q_sh,
+                          int64_t k_sb, int64_t k_st, int64_t k_sh,
+                          int64_t v_sb, int64_t v_st, int64_t v_sh,
+                          int64_t o_sb, int64_t o_st, int64_t o_sh,
+                          da_dtype dtype, cudaStream_t stream);
+
+/* DIFF V2 causal prefill (contiguous tensors).
+ *   q   : (B, T, Hq, D)        Hq even; G = Hq / Hkv must be an even integer
+ *   k, v: (B, T, Hkv, D)
+ *   lam : (B, T, Hq/2) fp32 lambda logits, one per token and output head
+ *   out : (B, T, Hq/2, D), dtype as inputs
+ *   Supported: D in {64, 128} for both dtypes.
+ */
+da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const float *lam,
+                          void *out, int B, int T, int Hq, int Hkv, int D,
+                          da_dtype dtype, cudaStream_t stream);
+
+/* Bytes of device scratch that diffattn_v2_decode needs for these sizes on the
+ * current device (depends on its SM count).  Returns 0 for invalid sizes. */
+size_t diffattn_v2_decode_workspace_size(int B, int L, int Hq, int Hkv, int D, da_dtype dtype);
+
+/* DIFF V2 decode: one new query token per sequence against a KV cache.
+ *   q           : (B, Hq, D)            G = Hq / Hkv even, G <= 8 for DA_BF16
+ *   k_cache, v_cache : (B, L, Hkv, D)   rows 0..L-1 all valid (the new token's
+ *                                        own K/V already written at row L-1)
+ *   lam         : (B, Hq/2) fp32 lambda logits
+ *   out         : (B, Hq/2, D)
+ *   workspace   : device scratch of at least diffattn_v2_decode_workspace_size()
+ *                 bytes, 256-byte aligned, owned by the caller; contents on entry
+ *                 are ignored and on exit undefined.  Calls that share one
+ *                 workspace must be ordered on the GPU (same stream).
+ *   Supported: D in {64, 128}.
+ */
+da_status diffattn_v2_decode(const void *q, const void *k_cache, const void *v_cache,
+                             const float *lam, void *out, void *workspace,
+                             size_t workspace_bytes, int B, int L, int Hq, int Hkv, int D,
+                             da_dtype dtype, cudaStream_t stream);
+
+/* Static string for a status code (never NULL). */
+const char *diffattn_status_string(da_status s);
+
+/* Synchronises the current device, reads and clears the device error word that
+ * the kernels set when a bounded wait gives up.  *code receives the raw word
+ * (0 = no error).  Returns DA_OK if the word was 0, DA_ERR_DEVICE_TIMEOUT if a
+ * kernel recorded a give-up, DA_ERR_CUDA if the read itself failed. */
+da_status diffattn_device_error(uint32_t *code);
+
+/* Number of kernel launches the last successful call on this host thread
+ * enqueued (launch accounting for benchmarks). */
+int diffattn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DIFFATTN_H */
