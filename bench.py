@@ -1,0 +1,454 @@
+#!/usr/bin/env python3
+"""Benchmark of the causal differential-attention forward on GB300.
+
+One step = one fused DIFF V1 forward (lambda, both causal attentions, the
+combine, RMSNorm and the (1 - lam_init) scale -- every step of the V1 path)
+over the workload B=4, T=2048, 16 diff heads, d=64, dv=128, layer_index=12,
+bf16 inputs drawn N(0,1) with a seeded generator.  The line also carries, as
+auxiliary measurements, DIFF V2 prefill (B=8, T=4096, Hq=32, Hkv=8, D=128,
+TFLOP/s) and DIFF V2 decode (B=64, L=32768, Hq=64, Hkv=8, D=128, HBM GB/s).
+
+Usage:
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own batch of the same workload
+(seed + rank), no collective on the data path; timing is max over ranks.
+--impl reference times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from differential_attention_causal_gb300 import inputs  # noqa: E402
+
+HEADLINE = "v1_bf16_B4_T2048_H16_d64"
+METRIC = "fused diff-attn fwd TFLOP/s (% bf16 TC peak); V2 decode HBM GB/s (% peak)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM traffic per launch from an ncu capture, valid only for the kernel source
+# it was taken on (sha256 of the .cu file, first 16 hex digits).
+TRAFFIC_RECORDS: dict = {}
+
+
+# ----------------------------------------------------------------- helpers
+
+def v1_flops(s) -> float:
+    """Algorithmic FLOPs of one DIFF V1 forward: per causal (query, key) pair
+    2d (S1) + 2d (S2) + 2*2d (P1 V) + 2*2d (P2 V) = 12d; pairs = T(T+1)/2."""
+    return float(s.B) * s.H * s.T * (s.T + 1) / 2 * 12 * s.d
+
+
+def v2_flops(s) -> float:
+    """DIFF V2 prefill: per query head and causal pair 2D (QK) + 2D (PV)."""
+    return float(s.B) * s.Hq * s.T * (s.T + 1) / 2 * 4 * s.D
+
+
+def decode_bytes(s) -> int:
+    """Bytes one decode must move: K and V caches once, q, lam, out."""
+    return (2 * s.B * s.L * s.Hkv * s.D * 2 + s.B * s.Hq * s.D * 2
+            + s.B * (s.Hq // 2) * 4 + s.B * (s.Hq // 2) * s.D * 2)
+
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def src_sha(rel: str) -> str:
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled in the background."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 100):
+        self.index, self.period = index, period_ms
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+            time.sleep(0.5)
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        busy = [x for x in sm if smax and x > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def time_steps(step, steps: int, flush: torch.Tensor | None):
+    """Per-step device time (ms) with CUDA events on the current stream; the
+    L2 flush (if any) runs between steps, outside the events."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        if flush is not None:
+            flush.add_(1)
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+# ------------------------------------------------------------- our arm
+
+def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
+    from differential_attention_causal_gb300 import binding
+    import torch.distributed as dist
+
+    peaks, peak_kind = load_peaks()
+    s = inputs.WORKLOADS[HEADLINE]
+    x = inputs.make_v1(s, seed=args.seed + rank, device=dev)
+    out = torch.empty((s.B, s.T, s.H, 2 * s.d), dtype=torch.bfloat16, device=dev)
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        binding.v1_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"],
+                       x["lam_k2"], s.layer_index, out=out)
+
+    for _ in range(args.warmup):
+        flush.add_(1)
+        step()
+    torch.cuda.synchronize()
+    launches_per_step = binding.last_launch_count()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    times = time_steps(step, args.steps, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if binding.device_error():
+        raise RuntimeError("a kernel reported a device-side wait timeout")
+    flops = v1_flops(s)
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    avg_ms = sum(times) / len(times)
+    achieved = flops / (avg_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    tr = TRAFFIC_RECORDS.get("prefill_v1_d64")
+    traffic = tr["bytes_per_launch"] if tr and tr["src_sha"] == src_sha(
+        "differential_attention_causal_gb300/csrc/k_prefill.cu") else None
+
+    # end to end through the public call with host buffers: pinned H2D of the
+    # step's inputs, the forward, D2H of the result, all inside the events.
+    host = {k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()
+            if k in ("q", "k", "v", "lam_q1", "lam_k1", "lam_q2", "lam_k2")}
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    dl = [torch.empty_like(x[n]) for n in ("lam_q1", "lam_k1", "lam_q2", "lam_k2")]
+
+    def e2e_step():
+        dq.copy_(host["q"], non_blocking=True)
+        dk.copy_(host["k"], non_blocking=True)
+        dv.copy_(host["v"], non_blocking=True)
+        for d_, n in zip(dl, ("lam_q1", "lam_k1", "lam_q2", "lam_k2")):
+            d_.copy_(host[n], non_blocking=True)
+        binding.v1_fwd(dq[:, :, 0::2], dq[:, :, 1::2], dk[:, :, 0::2], dk[:, :, 1::2], dv, *dl,
+                       s.layer_index, out=out)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(5, min(args.steps, 50))
+    et = time_steps(e2e_step, e2e_steps, flush)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in host)
+    d2h = hout.numel() * hout.element_size()
+    e2e_ms = sum(et) / len(et)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    aux = {} if args.no_aux else run_aux(args, dev, peaks, peak_kind, binding)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.1) lambda vectors; seed + rank per rank)",
+        "config": {"workload": HEADLINE, "B": s.B, "T": s.T, "H": s.H, "d": s.d, "dv": 2 * s.d,
+                   "layer_index": s.layer_index, "causal": True,
+                   "l2": "256 MiB buffer written between timed steps (flush)",
+                   "flop_count": "12d per causal pair (two QK, two PV)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": f"bf16 dense burst ({peak_kind})", "kernel": "prefill_onepass<64,128,V1>"},
+        "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if aux:
+        line["aux"] = aux
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x, s, budget_s=args.cpu_seconds)
+    return line
+
+
+def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
+    aux = {}
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # DIFF V2 prefill
+    s = inputs.WORKLOADS["v2_bf16_B8_T4096_Hq32_Hkv8_D128"]
+    x = inputs.make_v2(s, seed=args.seed, device=dev)
+    out = torch.empty((s.B, s.T, s.Hq // 2, s.D), dtype=torch.bfloat16, device=dev)
+    f = lambda: binding.v2_fwd(x["q"], x["k"], x["v"], x["lam"], out=out)  # noqa: E731
+    for _ in range(3):
+        f()
+    t = time_steps(f, 10, flush)
+    ms = sum(t) / len(t)
+    tf = v2_flops(s) / (ms * 1e-3) / 1e12
+    aux["v2_prefill"] = {"workload": "v2_bf16_B8_T4096_Hq32_Hkv8_D128", "ms": round(ms, 4),
+                         "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                         "tokens_per_s": round(s.B * s.T / (ms * 1e-3)), "peak_kind": peak_kind}
+    del x, out
+    # DIFF V2 decode (8.6 GB cache >> L2: no flush needed)
+    s = inputs.WORKLOADS["v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128"]
+    x = inputs.make_decode(s, seed=args.seed, device=dev)
+    out = torch.empty((s.B, s.Hq // 2, s.D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(binding.decode_workspace_size(s.B, s.L, s.Hq, s.Hkv, s.D), dtype=torch.uint8, device=dev)
+    f = lambda: binding.v2_decode(x["q"], x["k_cache"], x["v_cache"], x["lam"], out=out, workspace=ws)  # noqa
+    for _ in range(3):
+        f()
+    t = time_steps(f, 20, None)
+    ms = sum(t) / len(t)
+    gbs = decode_bytes(s) / (ms * 1e-3) / 1e9
+    aux["v2_decode"] = {"workload": "v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128", "ms": round(ms, 4),
+                        "GB/s": round(gbs, 1), "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                        "frac_8TBs": round(gbs / 8000.0, 4), "tokens_per_s": round(s.B / (ms * 1e-3)),
+                        "launches": 2, "peak_kind": peak_kind}
+    del x, out, ws
+    torch.cuda.empty_cache()
+    if binding.device_error():
+        raise RuntimeError("a kernel reported a device-side wait timeout")
+    return aux
+
+
+# ------------------------------------------------------ the oracle (CPU)
+
+def _oracle_inputs(x) -> dict:
+    """fp64 contiguous host copies of the V1 inputs (done once, outside any timing)."""
+    import numpy as np
+    out = {}
+    for k in ("q1", "q2", "k1", "k2", "v", "lam_q1", "lam_k1", "lam_q2", "lam_k2"):
+        out[k] = np.ascontiguousarray(x[k].detach().to("cpu").double().numpy())
+    return out
+
+
+def _oracle_rows_time(x_cpu, s, rows) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.v1_fwd(x_cpu["q1"], x_cpu["q2"], x_cpu["k1"], x_cpu["k2"], x_cpu["v"], x_cpu["lam_q1"],
+                  x_cpu["lam_k1"], x_cpu["lam_q2"], x_cpu["lam_k2"], s.layer_index, rows=rows)
+    return time.perf_counter() - t0
+
+
+def _rows_flops(rows, s) -> float:
+    import numpy as np
+    t = (np.asarray(rows) // s.H) % s.T
+    return float(((t + 1) * 12 * s.d).sum())
+
+
+def cpu_baseline(x, s, budget_s: float = 15.0, seed: int = 0) -> dict:
+    """Time the fp64 oracle on a bounded random sample of the headline rows."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    x_cpu = _oracle_inputs(x)
+    rng = np.random.default_rng(seed)
+    nall = s.B * s.T * s.H
+    probe = rng.choice(nall, size=min(512, nall), replace=False)
+    dt = _oracle_rows_time(x_cpu, s, probe)
+    per_row = dt / len(probe)          # random rows: their mean cost is the workload's mean
+    n = int(min(nall, max(len(probe), budget_s / max(per_row, 1e-9))))
+    rows = rng.choice(nall, size=n, replace=False)
+    dt = _oracle_rows_time(x_cpu, s, rows)
+    val = _rows_flops(rows, s) / dt / 1e12
+    return {"value": val, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"{n} of {nall} output rows (b, t, head) of {HEADLINE}, uniform without replacement; "
+                      f"{dt:.1f} s wall; value = algorithmic 12d-per-pair FLOPs of the sample / wall time"}
+
+
+def run_reference(args, rank: int, world: int) -> dict | None:
+    """The oracle as the reference arm: fp64 plain C on the host cores."""
+    import numpy as np
+    import oracle
+    if rank != 0:
+        return None
+    oracle.build()
+    s = inputs.WORKLOADS[HEADLINE]
+    x = _oracle_inputs(inputs.make_v1(s, seed=args.seed, device="cpu"))
+    nall = s.B * s.T * s.H
+    rng = np.random.default_rng(args.seed)
+    probe = rng.choice(nall, size=256, replace=False)
+    dt = _oracle_rows_time(x, s, probe)
+    per_row = dt / len(probe)
+    budget = max(0.05, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    n = int(max(16, min(nall, budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        _oracle_rows_time(x, s, rng.choice(nall, size=n, replace=False))
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        rows = rng.choice(nall, size=n, replace=False)
+        tot_t += _oracle_rows_time(x, s, rows)
+        tot_f += _rows_flops(rows, s)
+    val = tot_f / tot_t / 1e12
+    sample = (f"each step: {n} of {nall} random output rows of {HEADLINE}; value = algorithmic "
+              f"12d-per-pair FLOPs of the rows / wall time")
+    return {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEADLINE, "B": s.B, "T": s.T, "H": s.H, "d": s.d, "dv": 2 * s.d,
+                   "layer_index": s.layer_index},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------ single cases (profiling)
+
+CASES = {
+    "v1": ("v1", "v1_bf16_B4_T2048_H16_d64"),
+    "v2": ("v2", "v2_bf16_B8_T4096_Hq32_Hkv8_D128"),
+    "decode": ("decode", "v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128"),
+    # the decode workload with 8 of its 64 sequences: 1.07 GB of cache, small
+    # enough for multi-pass profiler captures, still far larger than L2
+    "decode_b8": ("decode", None),
+}
+
+
+def run_case(name: str, launches: int):
+    from differential_attention_causal_gb300 import binding
+    kind, wl = CASES[name]
+    dev = torch.device("cuda", 0)
+    s = inputs.WORKLOADS[wl] if wl else inputs.DecodeShape(8, 32768, 64, 8, 128, "bf16")
+    x = inputs.make(s, seed=0, device=dev)
+    if kind == "v1":
+        f = lambda: binding.v1_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"],  # noqa
+                                   x["lam_q2"], x["lam_k2"], s.layer_index)
+    elif kind == "v2":
+        f = lambda: binding.v2_fwd(x["q"], x["k"], x["v"], x["lam"])  # noqa: E731
+    else:
+        f = lambda: binding.v2_decode(x["q"], x["k_cache"], x["v_cache"], x["lam"])  # noqa: E731
+    for _ in range(launches):
+        f()
+    torch.cuda.synchronize()
+    if binding.device_error():
+        raise RuntimeError("a kernel reported a device-side wait timeout")
+    print(json.dumps({"case": name, "launches": launches, "ok": True}))
+
+
+# -------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-aux", action="store_true", help="skip the V2 prefill / decode measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--case", choices=sorted(CASES), default=None,
+                    help="run one kernel case --launches times and exit (for profilers)")
+    ap.add_argument("--launches", type=int, default=3)
+    args = ap.parse_args()
+    if args.case:
+        run_case(args.case, args.launches)
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch.distributed as dist
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=dev)
+    try:
+        line = run_ours(args, rank, world, dev)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
