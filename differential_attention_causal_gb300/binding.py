@@ -20,7 +20,7 @@ DA_F32, DA_BF16 = 0, 1
 STATUS = {
     0: "DA_OK", 1: "DA_ERR_NULL_PTR", 2: "DA_ERR_BAD_SHAPE", 3: "DA_ERR_UNSUPPORTED_DIM",
     4: "DA_ERR_BAD_GROUP", 5: "DA_ERR_MISALIGNED", 6: "DA_ERR_WORKSPACE_TOO_SMALL",
-    7: "DA_ERR_CUDA", 8: "DA_ERR_BAD_DTYPE", 9: "DA_ERR_DEVICE_TIMEOUT",
+    7: "DA_ERR_CUDA", 8: "DA_ERR_BAD_DTYPE", 9: "DA_ERR_DEVICE_TIMEOUT", 10: "DA_ERR_SCRATCH_LIMIT",
 }
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +51,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v2_decode_workspace_size.argtypes = [i32] * 6
             L.diffattn_v2_decode.restype = i32
             L.diffattn_v2_decode.argtypes = ([vp, vp, vp, fp, vp, vp, ctypes.c_size_t] + [i32] * 5 + [i32, vp])
+            L.diffattn_v2_decode_noalloc.restype = i32
+            L.diffattn_v2_decode_noalloc.argtypes = [vp, vp, vp, fp, vp] + [i32] * 5 + [i32, vp]
             L.diffattn_status_string.restype = ctypes.c_char_p
             L.diffattn_status_string.argtypes = [i32]
             L.diffattn_device_error.restype = i32
@@ -188,4 +190,26 @@ def v2_decode(q, k_cache, v_cache, lam, out: torch.Tensor | None = None,
                                   out.data_ptr(), workspace.data_ptr(), workspace.numel(),
                                   B, L, Hq, Hkv, D, _dtype_code(q), _stream(stream))
     _check("diffattn_v2_decode", rc)
+    return out
+
+
+def v2_decode_noalloc(q, k_cache, v_cache, lam, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """DIFF V2 decode through ``diffattn_v2_decode_noalloc``: no workspace, no
+    allocation inside the library (its split-KV partials use the library's
+    static 8 MiB device buffer).  For callers that may not allocate device
+    memory; ``out`` may be passed in so that this wrapper allocates nothing
+    either.  Calls that overlap on the GPU share that buffer and must be
+    ordered.  Raises DiffAttnError (DA_ERR_SCRATCH_LIMIT) when the sizes need
+    more scratch than the buffer holds."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("lam", lam)):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, Hq, D = q.shape
+    L, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq // 2, D), dtype=q.dtype, device=q.device)
+    rc = lib().diffattn_v2_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), lam.data_ptr(),
+                                          out.data_ptr(), B, L, Hq, Hkv, D, _dtype_code(q), _stream(stream))
+    _check("diffattn_v2_decode_noalloc", rc)
     return out

@@ -101,6 +101,9 @@ const char *diffattn_status_string(da_status s) {
         case DA_ERR_CUDA: return "CUDA error";
         case DA_ERR_BAD_DTYPE: return "unknown dtype";
         case DA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (device error word set)";
+        case DA_ERR_SCRATCH_LIMIT:
+            return "sizes need more decode scratch than the library's static 8 MiB buffer; "
+                   "use diffattn_v2_decode with a workspace";
     }
     return "unknown status";
 }
@@ -305,3 +308,56 @@ da_status diffattn_v2_decode(const void *q, const void *k_cache, const void *v_c
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without allocation: the split-KV partials go to a buffer the library
+// owns, so a caller that may not allocate device memory passes only inputs
+// and outputs.  The buffer is a file-scope __device__ array; in host code its
+// name is only a stand-in, so its device address is looked up per device with
+// cudaGetSymbolAddress and that address is what the kernels receive.
+namespace da {
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64];
+
+// Device address of this device's copy of g_noalloc_scratch; looked up on
+// the first call per device, with that device current.
+bool noalloc_scratch(void **p) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || !a) return false;
+        g_scratch_ptr[dev] = a;
+    }
+    *p = g_scratch_ptr[dev];
+    return true;
+}
+}  // namespace
+}  // namespace da
+
+extern "C" da_status diffattn_v2_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                                const float *lam, void *out, int B, int L, int Hq, int Hkv,
+                                                int D, da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q || !k_cache || !v_cache || !lam || !out) return DA_ERR_NULL_PTR;
+    if (dtype == DA_F32)   // the fp32 kernel uses no scratch
+        return diffattn_v2_decode(q, k_cache, v_cache, lam, out, nullptr, 0, B, L, Hq, Hkv, D, dtype, stream);
+    uint32_t *err = nullptr;
+    int nsm = 0;
+    int grid, max_seg, spb;
+    int64_t units;
+    size_t need = 0;
+    if (B >= 1 && L >= 1 && Hq >= 2 && Hkv >= 1 && Hq % Hkv == 0 && device_state(&err, &nsm) &&
+        decode_plan(B, L, Hq, Hkv, D, nsm, &grid, &max_seg, &units, &spb, &need) &&
+        need > kNoAllocScratchBytes)
+        return DA_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    if (!noalloc_scratch(&scratch)) return DA_ERR_CUDA;
+    return diffattn_v2_decode(q, k_cache, v_cache, lam, out, scratch, kNoAllocScratchBytes, B, L, Hq, Hkv, D,
+                              dtype, stream);
+}

@@ -62,7 +62,9 @@ typedef enum {
     DA_ERR_WORKSPACE_TOO_SMALL = 6,
     DA_ERR_CUDA = 7,              /* CUDA runtime / driver error                        */
     DA_ERR_BAD_DTYPE = 8,
-    DA_ERR_DEVICE_TIMEOUT = 9     /* reported by diffattn_device_error()               */
+    DA_ERR_DEVICE_TIMEOUT = 9,    /* reported by diffattn_device_error()               */
+    DA_ERR_SCRATCH_LIMIT = 10     /* the call needs more scratch than the library's     */
+                                  /* static buffer holds (diffattn_v2_decode_noalloc)  */
 } da_status;
 
 typedef enum { DA_F32 = 0, DA_BF16 = 1 } da_dtype;
@@ -123,6 +125,33 @@ da_status diffattn_v2_decode(const void *q, const void *k_cache, const void *v_c
                              const float *lam, void *out, void *workspace,
                              size_t workspace_bytes, int B, int L, int Hq, int Hkv, int D,
                              da_dtype dtype, cudaStream_t stream);
+
+/* DIFF V2 decode that allocates nothing and takes no workspace.
+ *   The paper has no counterpart: this exists for callers that are not
+ *   allowed to allocate device memory themselves -- for example a host
+ *   framework that owns every byte of device memory through its own pool and
+ *   hands this library only inputs and outputs, or a decode loop that cannot
+ *   afford the device-wide synchronisation a cudaMalloc may cause.
+ *   Same operation, arguments, layouts and limits as diffattn_v2_decode, minus
+ *   the workspace.  The split-KV partials live instead in one static device
+ *   buffer of 8 MiB inside the library; every GPU that loads the library
+ *   holds that buffer until the process exits.
+ *   - Sizes whose partials need more than 8 MiB (see
+ *     diffattn_v2_decode_workspace_size) return DA_ERR_SCRATCH_LIMIT with
+ *     nothing enqueued; the workspace entry point has no such limit.
+ *   - The first call on each device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one buffer and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero (each call writes every partial it
+ *     reads back), but calls that overlap on the GPU -- on different streams,
+ *     or from different host threads -- race on it: order them.
+ *   - dtype DA_F32 needs no scratch and runs the same fp32 kernel as
+ *     diffattn_v2_decode.
+ */
+da_status diffattn_v2_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                     const float *lam, void *out, int B, int L, int Hq, int Hkv,
+                                     int D, da_dtype dtype, cudaStream_t stream);
 
 /* Static string for a status code (never NULL). */
 const char *diffattn_status_string(da_status s);
