@@ -9,13 +9,16 @@
 // two branches (Q1,K1) and (Q2,K2) against one V, combined per row at the end.
 //
 // One CTA = 128 query rows of one diff head (V1) or one head pair (V2).
-//   warp 0      TMA producer: Q1, Q2 once; then K (K1 and K2 for V1) and V
-//               tiles of 128 keys into a 2-stage ring, causal tiles only.
+//   warp 0      TMA producer: Q1, Q2 once; then K tiles (K1 and K2 for V1)
+//               into a KS-deep ring and V tiles into a VS-deep ring, causal
+//               tiles only, in the order the MMAs consume them.
 //   warp 1      TMEM owner and single-thread MMA issuer.
+//   warp 2      V1: the lambda scalar (lam_init and the two exp terms) into
+//               shared memory while the main loop runs.
 //   warps 4-7   softmax for branch 1 (thread = query row = TMEM lane)
 //   warps 8-11  softmax for branch 2
 // TMEM (512 columns): S1 | S2 (128 fp32 columns each) | O1 | O2 (DV each).
-// Per KV tile j the MMA warp issues   PV1(j-1) S1(j) ... PV2(j-1) S2(j):
+// Per KV tile j the MMA warp issues   PV1(j) S1(j+1) ... PV2(j) S2(j+1):
 //   S_b = Q_b K_b^T      (SS MMA, K-major operands, 128-byte swizzle)
 //   P_b (bf16) is written by the softmax threads over the first 64 columns
 //   of S_b, and O_b += P_b V is a TS MMA (A = P from TMEM, B = V MN-major).
@@ -36,30 +39,40 @@ namespace {
 template <int DQK, int DV, bool V2>
 struct PreCfg {
     static constexpr int BM = 128, BN = 128;
-    static constexpr int STAGES = 2;
     static constexpr int QB = DQK / 64;                // 64-column boxes per Q/K tile
     static constexpr int VB = DV / 64;
     static constexpr int BOX = 128 * 128;              // bytes of one 128-row x 64-col box
     static constexpr int Q_TILE = QB * BOX;
     static constexpr int K_TILE = QB * BOX;
-    static constexpr int V_TILE = VB * BOX;
-    static constexpr int NK = V2 ? 1 : 2;              // K tiles per stage
-    static constexpr int STAGE = NK * K_TILE + V_TILE;
+    static constexpr int NK = V2 ? 1 : 2;              // K tiles per key block (K1, K2)
+    static constexpr int K_SLOT = NK * K_TILE;
+    static constexpr int V_SLOT = VB * BOX;
+    // ring depths: as deep as 227 KB of shared memory allows
+    static constexpr int KS = 3;
+    static constexpr int VS = (2 * Q_TILE + KS * K_SLOT + 3 * V_SLOT <= 224 * 1024) ? 3 : 2;
     static constexpr int OFF_Q1 = 0;
     static constexpr int OFF_Q2 = Q_TILE;
-    static constexpr int OFF_ST = 2 * Q_TILE;
-    static constexpr int OFF_X = OFF_ST + STAGES * STAGE;   // 4 x 128 floats exchange
-    static constexpr int OFF_BAR = OFF_X + 4 * 128 * 4;
-    // q, kfull[S], vfull[S], empty[S], s[2], p[2], o[2], drain
-    static constexpr int NBAR = 1 + 3 * STAGES + 7;
-    static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_TSLOT + 16 + 1024;      // + alignment slack
+    static constexpr int OFF_K = 2 * Q_TILE;
+    static constexpr int OFF_V = OFF_K + KS * K_SLOT;
+    static constexpr int OFF_X = OFF_Q1;                      // epilogue exchange reuses Q1
+    static constexpr int OFF_BAR = OFF_V + VS * V_SLOT;
+    // q, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s[2], p[2][2], o[2], drain, lam
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 10;
+    static constexpr int OFF_LAM = OFF_BAR + NBAR * 8;        // 2 floats
+    static constexpr int OFF_TSLOT = OFF_LAM + 8;
+    static constexpr int SMEM = OFF_TSLOT + 8 + 1024;         // + alignment slack
     static constexpr int COL_S1 = 0, COL_S2 = BN, COL_O1 = 2 * BN, COL_O2 = 2 * BN + DV;
     static constexpr uint32_t TMEM_COLS = 512;
+    // registers per thread after the split: warps 0-3 (producer, MMA,
+    // lambda, idle) give up registers, the two softmax warpgroups take them
+    static constexpr uint32_t REGS_LOW = 56, REGS_HIGH = 208;
+    static constexpr bool REG_SPLIT = !V2;                    // measured: helps V1, costs V2
+    static constexpr int REGS_NEEDED_AT_LAUNCH = (128 * REGS_LOW + 256 * REGS_HIGH + 383) / 384;
     static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, true);
     static_assert(COL_O2 + DV <= 512, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(4 * 128 * 4 <= Q_TILE, "exchange area fits in the Q1 tile");
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t *err, bool ok) {
@@ -71,6 +84,42 @@ __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
+}
+
+// Row max of 128 raw scores with eight independent chains of 3-input max.
+__device__ __forceinline__ float row_max128(const uint32_t *s) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+#pragma unroll
+    for (int k = 16; k < 128; k += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = fmax3(a[i], __uint_as_float(s[k + 2 * i]), __uint_as_float(s[k + 2 * i + 1]));
+    }
+    return fmaxf(fmax3(a[0], a[1], a[2]), fmax3(fmax3(a[3], a[4], a[5]), a[6], a[7]));
+}
+
+// p = 2^(s*scale - m) for 64 scores, in place as 32 packed bf16 pairs in
+// s[0..31]; returns the fp32 sum of the 64 values.
+__device__ __forceinline__ float exp_pack64(uint32_t *s, float scale, float m) {
+    const float2 sc2 = make_float2(scale, scale);
+    const float2 nm2 = make_float2(-m, -m);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const float2 x =
+            __ffma2_rn(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sc2, nm2);
+        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+        switch (c & 3) {
+            case 0: acc0 = __fadd2_rn(acc0, pp); break;
+            case 1: acc1 = __fadd2_rn(acc1, pp); break;
+            case 2: acc2 = __fadd2_rn(acc2, pp); break;
+            default: acc3 = __fadd2_rn(acc3, pp); break;
+        }
+        s[c] = pack_bf16(pp.x, pp.y);
+    }
+    const float2 t = __fadd2_rn(__fadd2_rn(acc0, acc1), __fadd2_rn(acc2, acc3));
+    return t.x + t.y;
 }
 
 template <int DQK, int DV, bool V2>
@@ -97,29 +146,37 @@ __global__ void __launch_bounds__(384, 1)
     const int hk = V2 ? (2 * h) / p.G : h;
 
     const uint32_t bar_q = sbase + C::OFF_BAR;
-    const uint32_t bar_kf = bar_q + 8;
-    const uint32_t bar_vf = bar_kf + 8 * C::STAGES;
-    const uint32_t bar_em = bar_vf + 8 * C::STAGES;
-    const uint32_t bar_s = bar_em + 8 * C::STAGES;    // [2]
-    const uint32_t bar_p = bar_s + 16;                // [2]
-    const uint32_t bar_o = bar_p + 16;                // [2]
+    const uint32_t bar_kf = bar_q + 8;                 // [KS]
+    const uint32_t bar_ke = bar_kf + 8 * C::KS;        // [KS]
+    const uint32_t bar_vf = bar_ke + 8 * C::KS;        // [VS]
+    const uint32_t bar_ve = bar_vf + 8 * C::VS;        // [VS]
+    const uint32_t bar_s = bar_ve + 8 * C::VS;         // [2]
+    const uint32_t bar_p = bar_s + 16;                 // [2 branches][2 halves]
+    const uint32_t bar_o = bar_p + 32;                 // [2]
     const uint32_t bar_dr = bar_o + 16;
+    const uint32_t bar_lam = bar_dr + 8;
     const uint32_t tslot = sbase + C::OFF_TSLOT;
     const uint32_t sQ1 = sbase + C::OFF_Q1, sQ2 = sbase + C::OFF_Q2;
+    float *lam_smem = reinterpret_cast<float *>(smem + C::OFF_LAM);
 
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < C::KS; ++s) {
             mbar_init(bar_kf + 8 * s, 1);
+            mbar_init(bar_ke + 8 * s, 1);
+        }
+        for (int s = 0; s < C::VS; ++s) {
             mbar_init(bar_vf + 8 * s, 1);
-            mbar_init(bar_em + 8 * s, 1);
+            mbar_init(bar_ve + 8 * s, 1);
         }
         for (int br = 0; br < 2; ++br) {
             mbar_init(bar_s + 8 * br, 1);
-            mbar_init(bar_p + 8 * br, 128);
+            mbar_init(bar_p + 16 * br, 4);     // keys 0-63 of P: one arrival per softmax warp
+            mbar_init(bar_p + 16 * br + 8, 4); // keys 64-127
             mbar_init(bar_o + 8 * br, 1);
         }
         mbar_init(bar_dr, 1);
+        mbar_init(bar_lam, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -133,6 +190,7 @@ __global__ void __launch_bounds__(384, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
+        if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
         if (lane == 0) {
             prefetch_tmap(&tq1);
             prefetch_tmap(&tk1);
@@ -147,87 +205,122 @@ __global__ void __launch_bounds__(384, 1)
                 tma_load_4d(sQ1 + c * C::BOX, &tq1, bar_q, 64 * c, hq1, q0, b);
                 tma_load_4d(sQ2 + c * C::BOX, &tq2, bar_q, 64 * c, hq2, q0, b);
             }
-            int j = 0;
-            for (; j < n_kv; ++j) {
-                const int st = j % C::STAGES;
-                if (j >= C::STAGES &&
-                    !mbar_wait(bar_em + 8 * st, static_cast<uint32_t>((j / C::STAGES - 1) & 1), p.err))
-                    break;
-                const uint32_t sk1 = sbase + C::OFF_ST + st * C::STAGE;
-                const uint32_t sk2 = sk1 + C::K_TILE;
-                const uint32_t sv = sk1 + C::NK * C::K_TILE;
-                mbar_arrive_expect_tx(bar_kf + 8 * st, C::NK * C::K_TILE);
+            auto load_k = [&](int j) -> bool {
+                const int st = j % C::KS;
+                if (j >= C::KS &&
+                    !mbar_wait(bar_ke + 8 * st, static_cast<uint32_t>((j / C::KS - 1) & 1), p.err))
+                    return false;
+                const uint32_t dst = sbase + C::OFF_K + st * C::K_SLOT;
+                mbar_arrive_expect_tx(bar_kf + 8 * st, C::K_SLOT);
 #pragma unroll
                 for (int c = 0; c < C::QB; ++c) {
-                    tma_load_4d(sk1 + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
-                    if (!V2) tma_load_4d(sk2 + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
+                    tma_load_4d(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
+                    if (!V2)
+                        tma_load_4d(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
                 }
-                mbar_arrive_expect_tx(bar_vf + 8 * st, C::V_TILE);
+                return true;
+            };
+            auto load_v = [&](int j) -> bool {
+                const int st = j % C::VS;
+                if (j >= C::VS &&
+                    !mbar_wait(bar_ve + 8 * st, static_cast<uint32_t>((j / C::VS - 1) & 1), p.err))
+                    return false;
+                const uint32_t dst = sbase + C::OFF_V + st * C::V_SLOT;
+                mbar_arrive_expect_tx(bar_vf + 8 * st, C::V_SLOT);
 #pragma unroll
                 for (int c = 0; c < C::VB; ++c)
-                    tma_load_4d(sv + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b);
+                    tma_load_4d(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b);
+                return true;
+            };
+            // consumption order: K0, (V_j, K_j+1) ...
+            int nk = load_k(0) ? 1 : 0, nv = 0;
+            for (int j = 0; nk == j + 1 && j < n_kv; ++j) {
+                if (!load_v(j)) break;
+                nv = j + 1;
+                if (j + 1 < n_kv) {
+                    if (!load_k(j + 1)) break;
+                    nk = j + 2;
+                }
             }
             // leave no copy in flight
             mbar_wait(bar_q, 0, p.err);
-            for (int k = (j > C::STAGES ? j - C::STAGES : 0); k < j; ++k) {
-                mbar_wait(bar_kf + 8 * (k % C::STAGES), static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
-                mbar_wait(bar_vf + 8 * (k % C::STAGES), static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
-            }
+            for (int k = (nk > C::KS ? nk - C::KS : 0); k < nk; ++k)
+                mbar_wait(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
+            for (int k = (nv > C::VS ? nv - C::VS : 0); k < nv; ++k)
+                mbar_wait(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
+        if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
         if (lane == 0) {
-            auto stage_k1 = [&](int st) { return sbase + C::OFF_ST + st * C::STAGE; };
-            auto stage_k2 = [&](int st) { return sbase + C::OFF_ST + st * C::STAGE + (V2 ? 0 : C::K_TILE); };
-            auto stage_v = [&](int st) { return sbase + C::OFF_ST + st * C::STAGE + C::NK * C::K_TILE; };
+            auto k1_at = [&](int j) { return sbase + C::OFF_K + (j % C::KS) * C::K_SLOT; };
+            auto k2_at = [&](int j) { return k1_at(j) + (V2 ? 0 : C::K_TILE); };
+            auto v_at = [&](int j) { return sbase + C::OFF_V + (j % C::VS) * C::V_SLOT; };
+            // Descriptors are built once; a K step only moves the start
+            // address field (bits 0-13, in 16-byte units), which never
+            // carries for shared-memory addresses.
             auto issue_qk = [&](uint32_t dcol, uint32_t sq, uint32_t sk) {
+                const uint64_t da = sdesc_sw128(sq, 16, 1024), db = sdesc_sw128(sk, 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < DQK / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::BOX + (ks & 3) * 32;
-                    mma_ss(tmem + dcol, sdesc_sw128(sq + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024),
-                           C::IDESC_QK, ks > 0 ? 1u : 0u);
+                    const uint32_t off = ((ks >> 2) * C::BOX + (ks & 3) * 32) >> 4;
+                    mma_ss(tmem + dcol, da + off, db + off, C::IDESC_QK, ks > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](uint32_t dcol, uint32_t pcol, uint32_t sv, bool acc) {
+            // O += P V over one half of the key tile (64 keys = 4 K-steps).
+            auto issue_pv_half = [&](uint32_t dcol, uint32_t pcol, uint32_t sv, int half, bool acc) {
+                const uint64_t dv = sdesc_sw128(sv, C::BOX, 1024);
 #pragma unroll
-                for (int ks = 0; ks < C::BN / 16; ++ks)
-                    mma_ts(tmem + dcol, tmem + pcol + ks * 8, sdesc_sw128(sv + ks * 2048, C::BOX, 1024),
-                           C::IDESC_PV, (acc || ks > 0) ? 1u : 0u);
+                for (int k = 0; k < C::BN / 32; ++k) {
+                    const int ks = half * (C::BN / 32) + k;
+                    mma_ts(tmem + dcol, tmem + pcol + ks * 8, dv + ((ks * 2048) >> 4), C::IDESC_PV,
+                           (acc || ks > 0) ? 1u : 0u);
+                }
             };
             bool ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kf, 0, p.err);
             if (ok) {
                 tc_fence_after();
-                issue_qk(C::COL_S1, sQ1, stage_k1(0));
+                issue_qk(C::COL_S1, sQ1, k1_at(0));
                 mma_commit(bar_s);
-                issue_qk(C::COL_S2, sQ2, stage_k2(0));
+                issue_qk(C::COL_S2, sQ2, k2_at(0));
                 mma_commit(bar_s + 8);
+                mma_commit(bar_ke);
             }
             for (int j = 0; ok && j < n_kv; ++j) {
-                const int st = j % C::STAGES;
-                const uint32_t ph = static_cast<uint32_t>((j / C::STAGES) & 1);
-                ok = mbar_wait(bar_vf + 8 * st, ph, p.err) && mbar_wait(bar_p, j & 1, p.err);
+                const uint32_t pj = static_cast<uint32_t>(j & 1);
+                ok = mbar_wait(bar_vf + 8 * (j % C::VS), static_cast<uint32_t>((j / C::VS) & 1), p.err) &&
+                     mbar_wait(bar_p, pj, p.err);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(C::COL_O1, C::COL_S1, stage_v(st), j > 0);
+                issue_pv_half(C::COL_O1, C::COL_S1, v_at(j), 0, j > 0);
+                ok = mbar_wait(bar_p + 8, pj, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv_half(C::COL_O1, C::COL_S1, v_at(j), 1, j > 0);
                 const bool more = j + 1 < n_kv;
-                const int st1 = (j + 1) % C::STAGES;
                 if (more) {
-                    ok = mbar_wait(bar_kf + 8 * st1, static_cast<uint32_t>(((j + 1) / C::STAGES) & 1), p.err);
+                    ok = mbar_wait(bar_kf + 8 * ((j + 1) % C::KS), static_cast<uint32_t>(((j + 1) / C::KS) & 1),
+                                   p.err);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk(C::COL_S1, sQ1, stage_k1(st1));
+                    issue_qk(C::COL_S1, sQ1, k1_at(j + 1));
                     mma_commit(bar_s);
                 } else {
                     mma_commit(bar_o);
                 }
-                ok = mbar_wait(bar_p + 8, j & 1, p.err);
+                ok = mbar_wait(bar_p + 16, pj, p.err);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(C::COL_O2, C::COL_S2, stage_v(st), j > 0);
-                mma_commit(bar_em + 8 * st);
+                issue_pv_half(C::COL_O2, C::COL_S2, v_at(j), 0, j > 0);
+                ok = mbar_wait(bar_p + 24, pj, p.err);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv_half(C::COL_O2, C::COL_S2, v_at(j), 1, j > 0);
+                mma_commit(bar_ve + 8 * (j % C::VS));
                 if (more) {
-                    issue_qk(C::COL_S2, sQ2, stage_k2(st1));
+                    issue_qk(C::COL_S2, sQ2, k2_at(j + 1));
                     mma_commit(bar_s + 8);
+                    mma_commit(bar_ke + 8 * ((j + 1) % C::KS));
                 } else {
                     mma_commit(bar_o + 8);
                 }
@@ -236,15 +329,41 @@ __global__ void __launch_bounds__(384, 1)
             mma_commit(bar_dr);
             mbar_wait(bar_dr, 0, p.err);
         }
-    } else if (warp >= 4) {
+    } else if (warp == 2) {
+        // ------------------------------------------------- lambda (V1 only)
+        if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
+        if (!V2) {
+            // lam_init = 0.8 - 0.6 exp(-0.3 layer); lam = exp(lq1.lk1) - exp(lq2.lk2) + lam_init
+            float d1 = 0.f, d2 = 0.f;
+            for (int c = lane; c < DQK; c += 32) {
+                d1 = fmaf(p.lq1[c], p.lk1[c], d1);
+                d2 = fmaf(p.lq2[c], p.lk2[c], d2);
+            }
+            d1 = warp_sum(d1);
+            d2 = warp_sum(d2);
+            if (lane == 0) {
+                const float lam_init = 0.8f - 0.6f * expf(-0.3f * static_cast<float>(p.layer_index));
+                lam_smem[0] = expf(d1) - expf(d2) + lam_init;
+                lam_smem[1] = lam_init;
+                mbar_arrive(bar_lam);
+            }
+        }
+    } else if (warp == 3) {
+        if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
+    } else {
         // -------------------------------------------------------- softmax
+        if (C::REG_SPLIT) regs_increase<C::REGS_HIGH>();
         const int br = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
+        const int t = q0 + row;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + (br ? C::COL_S2 : C::COL_S1);
         const uint32_t tO = tmem + lane_off + (br ? C::COL_O2 : C::COL_O1);
-        const uint32_t my_s = bar_s + 8 * br, my_p = bar_p + 8 * br, my_o = bar_o + 8 * br;
+        const uint32_t my_s = bar_s + 8 * br, my_p = bar_p + 16 * br, my_o = bar_o + 8 * br;
+        // V2 gate logit of this row, fetched now and used in the epilogue
+        const float lg = (V2 && t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
+        const float sl2 = p.scale_log2;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
@@ -257,16 +376,12 @@ __global__ void __launch_bounds__(384, 1)
             tmem_ld32(tS + 64, s + 64);
             tmem_ld32(tS + 96, s + 96);
             tmem_wait_ld();
-            const bool diag = (j == qt);
-            float mx = -INFINITY;
+            if (j == qt) {   // diagonal tile: keys past this row are masked
 #pragma unroll
-            for (int c = 0; c < C::BN; ++c) {
-                float x = __uint_as_float(s[c]) * p.scale_log2;
-                if (diag && c > row) x = -INFINITY;
-                s[c] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int c = 0; c < C::BN; ++c)
+                    if (c > row) s[c] = 0xff800000u;   // -inf
             }
-            const float m_new = fmaxf(m_ref, mx);
+            const float m_new = fmaxf(m_ref, row_max128(s) * sl2);
             float alpha = 1.f;
             const bool resc = m_new > m_ref + 8.f;
             if (resc) {
@@ -287,45 +402,36 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 tmem_wait_st();
             }
-            float rs = 0.f;
-#pragma unroll
-            for (int c = 0; c < C::BN / 2; ++c) {
-                const float p0 = ex2(__uint_as_float(s[2 * c]) - m_ref);
-                const float p1 = ex2(__uint_as_float(s[2 * c + 1]) - m_ref);
-                rs += p0 + p1;
-                s[c] = pack_bf16(p0, p1);
-            }
-            l += rs;
+            // P in two halves: the tensor core starts O += P V on keys 0-63
+            // while keys 64-127 are still being exponentiated.
+            l += exp_pack64(s, sl2, m_ref);
             tmem_st32(tS + 0, s);
-            tmem_st32(tS + 32, s + 32);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(my_p);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(my_p);
+            l += exp_pack64(s + 64, sl2, m_ref);
+            tmem_st32(tS + 32, s + 64);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(my_p + 8);
         }
 
         // ------------------------------------------------------- epilogue
         ok = warp_wait(my_o, 0, p.err, ok);
+        if (!V2) ok = warp_wait(bar_lam, 0, p.err, ok);
         tc_fence_after();
-        float *xch = reinterpret_cast<float *>(smem + C::OFF_X);
+        float *xch = reinterpret_cast<float *>(smem + C::OFF_X);   // Q1 tile is free now
         xch[br * 128 + row] = l;
         named_bar_sync(1, 256);
         const float l1 = xch[row], l2 = xch[128 + row];
-        const int t = q0 + row;
         float lam_init = 0.f, c2;
         if (V2) {
-            const float lg = (t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
             c2 = 1.f / (1.f + __expf(-lg)) / l2;
         } else {
-            float d1 = 0.f, d2 = 0.f;
-            for (int c = lane; c < DQK; c += 32) {
-                d1 = fmaf(p.lq1[c], p.lk1[c], d1);
-                d2 = fmaf(p.lq2[c], p.lk2[c], d2);
-            }
-            d1 = warp_sum(d1);
-            d2 = warp_sum(d2);
-            lam_init = 0.8f - 0.6f * expf(-0.3f * static_cast<float>(p.layer_index));
-            const float lam = expf(d1) - expf(d2) + lam_init;
-            c2 = lam / l2;
+            lam_init = lam_smem[1];
+            c2 = lam_smem[0] / l2;
         }
         const float c1 = 1.f / l1;
         constexpr int HALF = DV / 2;
@@ -385,8 +491,15 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
     cudaGetDevice(&dev);
     static unsigned long long attr_done = 0;   // one bit per device
     if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        // The register split inside the kernel must fit in what the launch
+        // grants (384 threads x registers per thread), or its increase would
+        // never complete: refuse to launch otherwise.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_onepass<DQK, DV, V2>);
+        if (e != cudaSuccess) return e;
+        if (C::REG_SPLIT && fa.numRegs < C::REGS_NEEDED_AT_LAUNCH) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 C::SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
