@@ -6,7 +6,8 @@ combine, RMSNorm and the (1 - lam_init) scale -- every step of the V1 path)
 over the workload B=4, T=2048, 16 diff heads, d=64, dv=128, layer_index=12,
 bf16 inputs drawn N(0,1) with a seeded generator.  The line also carries, as
 auxiliary measurements, DIFF V2 prefill (B=8, T=4096, Hq=32, Hkv=8, D=128,
-TFLOP/s) and DIFF V2 decode (B=64, L=32768, Hq=64, Hkv=8, D=128, HBM GB/s).
+TFLOP/s), long-context DIFF V1 (B=1, T=32768, 12 heads, d=128, TFLOP/s) and
+DIFF V2 decode (B=64, L=32768, Hq=64, Hkv=8, D=128, HBM GB/s).
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -266,6 +267,22 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                          "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
                          "tokens_per_s": round(s.B * s.T / (ms * 1e-3)), "peak_kind": peak_kind}
     del x, out
+    # DIFF V1 long context, d = 128 / dv = 256 (two-pass kernel)
+    s = inputs.WORKLOADS["v1_bf16_B1_T32768_H12_d128"]
+    x = inputs.make_v1(s, seed=args.seed, device=dev)
+    out = torch.empty((s.B, s.T, s.H, 2 * s.d), dtype=torch.bfloat16, device=dev)
+    f = lambda: binding.v1_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"],  # noqa
+                               x["lam_q2"], x["lam_k2"], s.layer_index, out=out)
+    for _ in range(3):
+        f()
+    t = time_steps(f, 5, flush)
+    ms = sum(t) / len(t)
+    tf = v1_flops(s) / (ms * 1e-3) / 1e12
+    aux["v1_long"] = {"workload": "v1_bf16_B1_T32768_H12_d128", "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                      "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                      "tokens_per_s": round(s.B * s.T / (ms * 1e-3)), "kernel": "prefill_v1_twopass<128>",
+                      "peak_kind": peak_kind}
+    del x, out
     # DIFF V2 decode (8.6 GB cache >> L2: no flush needed)
     s = inputs.WORKLOADS["v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128"]
     x = inputs.make_decode(s, seed=args.seed, device=dev)
@@ -375,6 +392,7 @@ def run_reference(args, rank: int, world: int) -> dict | None:
 
 CASES = {
     "v1": ("v1", "v1_bf16_B4_T2048_H16_d64"),
+    "v1_long": ("v1", "v1_bf16_B1_T32768_H12_d128"),
     "v2": ("v2", "v2_bf16_B8_T4096_Hq32_Hkv8_D128"),
     "decode": ("decode", "v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128"),
     # the decode workload with 8 of its 64 sequences: 1.07 GB of cache, small

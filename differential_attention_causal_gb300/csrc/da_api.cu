@@ -133,7 +133,10 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
         return DA_ERR_NULL_PTR;
     if (B < 1 || T < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
     const int es = dtype == DA_BF16 ? 2 : 4;
-    if (dtype == DA_BF16 ? !prefill_supported(d, 2 * d, false) : (d != 32 && d != 64 && d != 128))
+    // bf16: d = 64 runs the one-pass kernel, d = 128 (dv = 256: two fp32
+    // accumulators would not fit in TMEM next to S) the two-pass kernel
+    const bool twopass = dtype == DA_BF16 && d == 128;
+    if (dtype == DA_BF16 ? !(twopass || prefill_supported(d, 2 * d, false)) : (d != 32 && d != 64 && d != 128))
         return DA_ERR_UNSUPPORTED_DIM;
     for (const void *ptr : {q1, q2, k1, k2, v, static_cast<const void *>(out)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
@@ -167,7 +170,8 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
         !encode_map_4d(&m.q2, q2, d, uH, uT, uB, q_sh, q_st, q_sb, 128) ||
         !encode_map_4d(&m.k1, k1, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
         !encode_map_4d(&m.k2, k2, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
-        !encode_map_4d(&m.v, v, 2 * d, uH, uT, uB, v_sh, v_st, v_sb, 128))
+        !encode_map_4d(&m.v, v, 2 * d, uH, uT, uB, v_sh, v_st, v_sb,
+                       twopass ? static_cast<uint32_t>(prefill_v1_twopass_v_rows(d)) : 128u))
         return DA_ERR_CUDA;
     PrefillParams p{};
     p.out = out; p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
@@ -177,7 +181,8 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
     p.B = B; p.T = T; p.H = H; p.G = 1;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
     p.err = err;
-    const da_status st = cuda_status(launch_prefill(m, p, d, 2 * d, false, stream));
+    const da_status st = cuda_status(twopass ? launch_prefill_v1_twopass(m, p, d, stream)
+                                             : launch_prefill(m, p, d, 2 * d, false, stream));
     if (st == DA_OK) t_last_launches = 1;
     return st;
 }

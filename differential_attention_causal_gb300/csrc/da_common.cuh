@@ -88,6 +88,19 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Warp-uniform bounded wait: every lane waits, the result is the AND over the
+// warp (so warp-collective tcgen05 instructions that follow stay uniform).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t *err, bool ok) {
+    if (ok) ok = mbar_wait(bar, parity, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -291,6 +304,19 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
+// Row max of 128 raw scores with eight independent chains of 3-input max.
+__device__ __forceinline__ float row_max128(const uint32_t *s) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+#pragma unroll
+    for (int k = 16; k < 128; k += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = fmax3(a[i], __uint_as_float(s[k + 2 * i]), __uint_as_float(s[k + 2 * i + 1]));
+    }
+    return fmaxf(fmax3(a[0], a[1], a[2]), fmax3(fmax3(a[3], a[4], a[5]), a[6], a[7]));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);

@@ -49,6 +49,11 @@ struct PrefillMaps {
 cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
                            cudaStream_t s);
 bool prefill_supported(int dqk, int dv, bool v2);
+// DIFF V1 in two passes over the keys (row statistics, then one combined PV);
+// dqk in {64, 128}, dv = 2 dqk.  The V tensor map's box has
+// prefill_v1_twopass_v_rows(dqk) rows (the Q/K maps 128).
+cudaError_t launch_prefill_v1_twopass(const PrefillMaps &m, const PrefillParams &p, int dqk, cudaStream_t s);
+int prefill_v1_twopass_v_rows(int dqk);
 
 // --------------------------------------------------------------- decode
 struct DecodeParams {

@@ -47,11 +47,6 @@ struct DecCfg {
     static constexpr int SLOT = 8 * D + 16;            // floats per partial slot
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t *err, bool ok) {
-    if (ok) ok = mbar_wait(bar, parity, err);
-    return __all_sync(0xffffffffu, ok);
-}
-
 template <int D>
 __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     decode_split(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,

@@ -75,30 +75,6 @@ struct PreCfg {
     static_assert(4 * 128 * 4 <= Q_TILE, "exchange area fits in the Q1 tile");
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t *err, bool ok) {
-    if (ok) ok = mbar_wait(bar, parity, err);
-    return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-// Row max of 128 raw scores with eight independent chains of 3-input max.
-__device__ __forceinline__ float row_max128(const uint32_t *s) {
-    float a[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
-#pragma unroll
-    for (int k = 16; k < 128; k += 16) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = fmax3(a[i], __uint_as_float(s[k + 2 * i]), __uint_as_float(s[k + 2 * i + 1]));
-    }
-    return fmaxf(fmax3(a[0], a[1], a[2]), fmax3(fmax3(a[3], a[4], a[5]), a[6], a[7]));
-}
-
 // p = 2^(s*scale - m) for 64 scores, in place as 32 packed bf16 pairs in
 // s[0..31]; returns the fp32 sum of the 64 values.
 __device__ __forceinline__ float exp_pack64(uint32_t *s, float scale, float m) {

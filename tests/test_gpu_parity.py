@@ -125,6 +125,30 @@ def test_v1_bf16_full_workload_sampled():
     assert_parity(y.reshape(-1, 2 * s.d)[torch.from_numpy(rows).cuda()], ref, "bf16")
 
 
+@pytest.mark.parametrize("B,T,H,layer", [(2, 300, 2, 27), (1, 1, 1, 0), (1, 128, 2, 5), (1, 129, 1, 5),
+                                         (1, 520, 3, 27)])
+def test_v1_bf16_d128_two_pass(B, T, H, layer):
+    """d = 128, dv = 256: the two-pass kernel (row statistics, then one combined PV)."""
+    s = inputs.V1Shape(B, T, H, 128, layer, "bf16")
+    x = inputs.make_v1(s, seed=7 * T + H)
+    y = run_v1(to_dev(x), layer)
+    assert_parity(y, oracle_v1(x, layer), "bf16")
+
+
+def test_v1_bf16_d128_full_workload_sampled():
+    """B=1, T=32768, 12 diff heads, d=128, dv=256, layer_index=27, seed 0: sampled rows."""
+    s = inputs.WORKLOADS["v1_bf16_B1_T32768_H12_d128"]
+    x = inputs.make_v1(s, seed=0)
+    y = run_v1(to_dev(x), s.layer_index)
+    rng = np.random.default_rng(5)
+    ts = [0, 1, 127, 128, 16383, 32766, 32767]
+    rows = [(t * s.H + h) for h in range(s.H) for t in ts]
+    rows += list(rng.integers(0, s.T * s.H, 120))
+    rows = np.array(rows, dtype=np.int64)
+    ref = oracle_v1(x, s.layer_index, rows=rows)
+    assert_parity(y.reshape(-1, 2 * s.d)[torch.from_numpy(rows).cuda()], ref, "bf16")
+
+
 # ------------------------------------------------------------------- DIFF V2
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,D", [(2, 200, 8, 2, 128), (1, 129, 4, 2, 128), (1, 1, 8, 4, 128),
