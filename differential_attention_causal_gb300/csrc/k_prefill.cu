@@ -8,8 +8,13 @@
 // attn[:,0::2] - sigmoid(lam) attn[:,1::2].  Both are the same shape of work:
 // two branches (Q1,K1) and (Q2,K2) against one V, combined per row at the end.
 //
-// One CTA = 128 query rows of one diff head (V1) or one head pair (V2).
-//   warp 0      TMA producer: Q1, Q2 once; then K tiles (K1 and K2 for V1)
+// Work tile = 128 query rows of one diff head (V1) or one head pair (V2).
+// The kernel is persistent: one CTA per SM walks a snake-ordered list of work
+// tiles, heaviest (most key tiles) first, so that every CTA gets the same
+// amount of causal work and one tile's epilogue overlaps the next tile's
+// loads and first products.
+//   warp 0      TMA producer: Q1, Q2 per work tile (as soon as the previous
+//               tile's last QK has been issued); K tiles (K1 and K2 for V1)
 //               into a KS-deep ring and V tiles into a VS-deep ring, causal
 //               tiles only, in the order the MMAs consume them.
 //   warp 1      TMEM owner and single-thread MMA issuer.
@@ -47,17 +52,20 @@ struct PreCfg {
     static constexpr int NK = V2 ? 1 : 2;              // K tiles per key block (K1, K2)
     static constexpr int K_SLOT = NK * K_TILE;
     static constexpr int V_SLOT = VB * BOX;
-    // ring depths: as deep as 227 KB of shared memory allows
-    static constexpr int KS = 3;
-    static constexpr int VS = (2 * Q_TILE + KS * K_SLOT + 3 * V_SLOT <= 224 * 1024) ? 3 : 2;
+    static constexpr int XCH_FLOATS = V2 ? 256 : 512;  // l (and for V1 the RMS partials) per row
+    // Ring depths.  V(j) is needed one K-tile later than K(j) is freed, so
+    // with shared memory for only five slots the V ring gets the third one.
+    static constexpr bool ROOMY = 2 * Q_TILE + 3 * (K_SLOT + V_SLOT) + XCH_FLOATS * 4 + 2048 <= 232448;
+    static constexpr int KS = ROOMY ? 3 : (V2 ? 3 : 2);
+    static constexpr int VS = ROOMY ? 3 : (V2 ? 2 : 3);
     static constexpr int OFF_Q1 = 0;
     static constexpr int OFF_Q2 = Q_TILE;
     static constexpr int OFF_K = 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + KS * K_SLOT;
-    static constexpr int OFF_X = OFF_Q1;                      // epilogue exchange reuses Q1
-    static constexpr int OFF_BAR = OFF_V + VS * V_SLOT;
-    // q, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s[2], p[2][2], o[2], drain, lam
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 10;
+    static constexpr int OFF_X = OFF_V + VS * V_SLOT;
+    static constexpr int OFF_BAR = OFF_X + XCH_FLOATS * 4;
+    // qfull, qfree, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s[2], p[2][2], o[2], odrain, drain, lam
+    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 3;
     static constexpr int OFF_LAM = OFF_BAR + NBAR * 8;        // 2 floats
     static constexpr int OFF_TSLOT = OFF_LAM + 8;
     static constexpr int SMEM = OFF_TSLOT + 8 + 1024;         // + alignment slack
@@ -65,14 +73,13 @@ struct PreCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     // registers per thread after the split: warps 0-3 (producer, MMA,
     // lambda, idle) give up registers, the two softmax warpgroups take them
-    static constexpr uint32_t REGS_LOW = 56, REGS_HIGH = 208;
+    static constexpr uint32_t REGS_LOW = 88, REGS_HIGH = 192;
     static constexpr bool REG_SPLIT = !V2;                    // measured: helps V1, costs V2
     static constexpr int REGS_NEEDED_AT_LAUNCH = (128 * REGS_LOW + 256 * REGS_HIGH + 383) / 384;
     static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, true);
     static_assert(COL_O2 + DV <= 512, "TMEM budget");
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(4 * 128 * 4 <= Q_TILE, "exchange area fits in the Q1 tile");
 };
 
 // p = 2^(s*scale - m) for 64 scores, in place as 32 packed bf16 pairs in
@@ -98,6 +105,15 @@ __device__ __forceinline__ float exp_pack64(uint32_t *s, float scale, float m) {
     return t.x + t.y;
 }
 
+// Number of the k-th work tile of CTA c when G CTAs walk NT tiles in snake
+// order (c, 2G-1-c, 2G+c, ...): consecutive rounds go in opposite directions,
+// so with tiles sorted by decreasing weight every CTA's total is within one
+// tile of the others.  Returns -1 past the end.
+__device__ __forceinline__ int snake_tile(int k, int c, int G, int NT) {
+    const int w = k * G + ((k & 1) ? (G - 1 - c) : c);
+    return w < NT ? w : -1;
+}
+
 template <int DQK, int DV, bool V2>
 __global__ void __launch_bounds__(384, 1)
     prefill_onepass(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
@@ -110,33 +126,31 @@ __global__ void __launch_bounds__(384, 1)
     uint8_t *smem = smem_raw + (sbase - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // heaviest (last) query tiles first
+    // work tiles: index w -> query tile n_qt-1-w/(H*B) (heaviest first), head, batch
     const int n_qt = (p.T + C::BM - 1) / C::BM;
     const int per_qt = p.H * p.B;
-    const int qt = n_qt - 1 - static_cast<int>(blockIdx.x) / per_qt;
-    const int rest = static_cast<int>(blockIdx.x) % per_qt;
-    const int h = rest % p.H, b = rest / p.H;
-    const int q0 = qt * C::BM;
-    const int n_kv = qt + 1;   // causal: key tiles 0..qt (BN == BM)
-    const int hq1 = V2 ? 2 * h : h, hq2 = V2 ? 2 * h + 1 : h;
-    const int hk = V2 ? (2 * h) / p.G : h;
+    const int NT = n_qt * per_qt;
+    const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
 
-    const uint32_t bar_q = sbase + C::OFF_BAR;
-    const uint32_t bar_kf = bar_q + 8;                 // [KS]
+    const uint32_t bar_qf = sbase + C::OFF_BAR;
+    const uint32_t bar_qe = bar_qf + 8;                // Q tiles free (last QK of a tile issued)
+    const uint32_t bar_kf = bar_qe + 8;                // [KS]
     const uint32_t bar_ke = bar_kf + 8 * C::KS;        // [KS]
     const uint32_t bar_vf = bar_ke + 8 * C::KS;        // [VS]
     const uint32_t bar_ve = bar_vf + 8 * C::VS;        // [VS]
     const uint32_t bar_s = bar_ve + 8 * C::VS;         // [2]
     const uint32_t bar_p = bar_s + 16;                 // [2 branches][2 halves]
     const uint32_t bar_o = bar_p + 32;                 // [2]
-    const uint32_t bar_dr = bar_o + 16;
+    const uint32_t bar_od = bar_o + 16;                // O read by the epilogue (8 warps)
+    const uint32_t bar_dr = bar_od + 8;
     const uint32_t bar_lam = bar_dr + 8;
     const uint32_t tslot = sbase + C::OFF_TSLOT;
     const uint32_t sQ1 = sbase + C::OFF_Q1, sQ2 = sbase + C::OFF_Q2;
     float *lam_smem = reinterpret_cast<float *>(smem + C::OFF_LAM);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar_q, 1);
+        mbar_init(bar_qf, 1);
+        mbar_init(bar_qe, 1);
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(bar_kf + 8 * s, 1);
             mbar_init(bar_ke + 8 * s, 1);
@@ -151,6 +165,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(bar_p + 16 * br + 8, 4); // keys 64-127
             mbar_init(bar_o + 8 * br, 1);
         }
+        mbar_init(bar_od, 8);
         mbar_init(bar_dr, 1);
         mbar_init(bar_lam, 1);
         fence_mbar_init();
@@ -175,16 +190,12 @@ __global__ void __launch_bounds__(384, 1)
                 prefetch_tmap(&tq2);
                 prefetch_tmap(&tk2);
             }
-            mbar_arrive_expect_tx(bar_q, 2 * C::Q_TILE);
-#pragma unroll
-            for (int c = 0; c < C::QB; ++c) {
-                tma_load_4d(sQ1 + c * C::BOX, &tq1, bar_q, 64 * c, hq1, q0, b);
-                tma_load_4d(sQ2 + c * C::BOX, &tq2, bar_q, 64 * c, hq2, q0, b);
-            }
-            auto load_k = [&](int j) -> bool {
-                const int st = j % C::KS;
-                if (j >= C::KS &&
-                    !mbar_wait(bar_ke + 8 * st, static_cast<uint32_t>((j / C::KS - 1) & 1), p.err))
+            int kc = 0, vc = 0, tc = 0;   // ring and tile counters (the MMA warp keeps the same)
+            bool ok = true;
+            auto load_k = [&](int j, int hk, int b) -> bool {
+                const int st = kc % C::KS;
+                if (kc >= C::KS &&
+                    !mbar_wait(bar_ke + 8 * st, static_cast<uint32_t>((kc / C::KS - 1) & 1), p.err))
                     return false;
                 const uint32_t dst = sbase + C::OFF_K + st * C::K_SLOT;
                 mbar_arrive_expect_tx(bar_kf + 8 * st, C::K_SLOT);
@@ -194,46 +205,58 @@ __global__ void __launch_bounds__(384, 1)
                     if (!V2)
                         tma_load_4d(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
                 }
+                ++kc;
                 return true;
             };
-            auto load_v = [&](int j) -> bool {
-                const int st = j % C::VS;
-                if (j >= C::VS &&
-                    !mbar_wait(bar_ve + 8 * st, static_cast<uint32_t>((j / C::VS - 1) & 1), p.err))
+            auto load_v = [&](int j, int hk, int b) -> bool {
+                const int st = vc % C::VS;
+                if (vc >= C::VS &&
+                    !mbar_wait(bar_ve + 8 * st, static_cast<uint32_t>((vc / C::VS - 1) & 1), p.err))
                     return false;
                 const uint32_t dst = sbase + C::OFF_V + st * C::V_SLOT;
                 mbar_arrive_expect_tx(bar_vf + 8 * st, C::V_SLOT);
 #pragma unroll
                 for (int c = 0; c < C::VB; ++c)
                     tma_load_4d(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b);
+                ++vc;
                 return true;
             };
-            // consumption order: K0, (V_j, K_j+1) ...
-            int nk = load_k(0) ? 1 : 0, nv = 0;
-            for (int j = 0; nk == j + 1 && j < n_kv; ++j) {
-                if (!load_v(j)) break;
-                nv = j + 1;
-                if (j + 1 < n_kv) {
-                    if (!load_k(j + 1)) break;
-                    nk = j + 2;
+            for (int k = 0; ok; ++k) {
+                const int w = snake_tile(k, cta, G, NT);
+                if (w < 0) break;
+                const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
+                const int h = rest % p.H, b = rest / p.H, n_kv = qt + 1;
+                const int hq1 = V2 ? 2 * h : h, hq2 = V2 ? 2 * h + 1 : h;
+                const int hk = V2 ? (2 * h) / p.G : h;
+                // Q of this tile once the previous tile's last QK has been issued
+                if (tc > 0 && !mbar_wait(bar_qe, static_cast<uint32_t>((tc - 1) & 1), p.err)) break;
+                mbar_arrive_expect_tx(bar_qf, 2 * C::Q_TILE);
+#pragma unroll
+                for (int c = 0; c < C::QB; ++c) {
+                    tma_load_4d(sQ1 + c * C::BOX, &tq1, bar_qf, 64 * c, hq1, qt * C::BM, b);
+                    tma_load_4d(sQ2 + c * C::BOX, &tq2, bar_qf, 64 * c, hq2, qt * C::BM, b);
+                }
+                ++tc;
+                // consumption order: K0, (V_j, K_j+1) ...
+                ok = load_k(0, hk, b);
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    ok = load_v(j, hk, b);
+                    if (ok && j + 1 < n_kv) ok = load_k(j + 1, hk, b);
                 }
             }
             // leave no copy in flight
-            mbar_wait(bar_q, 0, p.err);
-            for (int k = (nk > C::KS ? nk - C::KS : 0); k < nk; ++k)
+            if (tc > 0) mbar_wait(bar_qf, static_cast<uint32_t>((tc - 1) & 1), p.err);
+            for (int k = (kc > C::KS ? kc - C::KS : 0); k < kc; ++k)
                 mbar_wait(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
-            for (int k = (nv > C::VS ? nv - C::VS : 0); k < nv; ++k)
+            for (int k = (vc > C::VS ? vc - C::VS : 0); k < vc; ++k)
                 mbar_wait(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
         if (lane == 0) {
-            auto k1_at = [&](int j) { return sbase + C::OFF_K + (j % C::KS) * C::K_SLOT; };
-            auto k2_at = [&](int j) { return k1_at(j) + (V2 ? 0 : C::K_TILE); };
-            auto v_at = [&](int j) { return sbase + C::OFF_V + (j % C::VS) * C::V_SLOT; };
-            // Descriptors are built once; a K step only moves the start
-            // address field (bits 0-13, in 16-byte units), which never
+            // Descriptors are built once per operand; a K step only moves the
+            // start address field (bits 0-13, in 16-byte units), which never
             // carries for shared-memory addresses.
             auto issue_qk = [&](uint32_t dcol, uint32_t sq, uint32_t sk) {
                 const uint64_t da = sdesc_sw128(sq, 16, 1024), db = sdesc_sw128(sk, 16, 1024);
@@ -253,53 +276,73 @@ __global__ void __launch_bounds__(384, 1)
                            (acc || ks > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kf, 0, p.err);
-            if (ok) {
+            int kc = 0, vc = 0, tc = 0, it = 0;
+            bool ok = true;
+            auto k1_at = [&]() { return sbase + C::OFF_K + (kc % C::KS) * C::K_SLOT; };
+            auto k2_at = [&]() { return k1_at() + (V2 ? 0 : C::K_TILE); };
+            auto wait_k = [&]() {
+                return mbar_wait(bar_kf + 8 * (kc % C::KS), static_cast<uint32_t>((kc / C::KS) & 1), p.err);
+            };
+            for (int k = 0; ok; ++k) {
+                const int w = snake_tile(k, cta, G, NT);
+                if (w < 0) break;
+                const int n_kv = n_qt - w / per_qt;
+                ok = mbar_wait(bar_qf, static_cast<uint32_t>(tc & 1), p.err) && wait_k();
+                if (!ok) break;
                 tc_fence_after();
-                issue_qk(C::COL_S1, sQ1, k1_at(0));
+                issue_qk(C::COL_S1, sQ1, k1_at());
                 mma_commit(bar_s);
-                issue_qk(C::COL_S2, sQ2, k2_at(0));
+                issue_qk(C::COL_S2, sQ2, k2_at());
                 mma_commit(bar_s + 8);
-                mma_commit(bar_ke);
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const uint32_t pj = static_cast<uint32_t>(j & 1);
-                ok = mbar_wait(bar_vf + 8 * (j % C::VS), static_cast<uint32_t>((j / C::VS) & 1), p.err) &&
-                     mbar_wait(bar_p, pj, p.err);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv_half(C::COL_O1, C::COL_S1, v_at(j), 0, j > 0);
-                ok = mbar_wait(bar_p + 8, pj, p.err);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv_half(C::COL_O1, C::COL_S1, v_at(j), 1, j > 0);
-                const bool more = j + 1 < n_kv;
-                if (more) {
-                    ok = mbar_wait(bar_kf + 8 * ((j + 1) % C::KS), static_cast<uint32_t>(((j + 1) / C::KS) & 1),
-                                   p.err);
+                mma_commit(bar_ke + 8 * (kc % C::KS));
+                ++kc;
+                if (n_kv == 1) mma_commit(bar_qe);
+                for (int j = 0; ok && j < n_kv; ++j, ++it) {
+                    const uint32_t pj = static_cast<uint32_t>(it & 1);
+                    const int vst = vc % C::VS;
+                    const uint32_t sv = sbase + C::OFF_V + vst * C::V_SLOT;
+                    ok = mbar_wait(bar_vf + 8 * vst, static_cast<uint32_t>((vc / C::VS) & 1), p.err) &&
+                         mbar_wait(bar_p, pj, p.err);
+                    // the first PV of a tile overwrites O: the previous epilogue must have read it
+                    if (ok && j == 0 && tc > 0) ok = mbar_wait(bar_od, static_cast<uint32_t>((tc - 1) & 1), p.err);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk(C::COL_S1, sQ1, k1_at(j + 1));
-                    mma_commit(bar_s);
-                } else {
-                    mma_commit(bar_o);
+                    issue_pv_half(C::COL_O1, C::COL_S1, sv, 0, j > 0);
+                    ok = mbar_wait(bar_p + 8, pj, p.err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv_half(C::COL_O1, C::COL_S1, sv, 1, j > 0);
+                    const bool more = j + 1 < n_kv;
+                    if (more) {
+                        ok = wait_k();
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_qk(C::COL_S1, sQ1, k1_at());
+                        mma_commit(bar_s);
+                    } else {
+                        mma_commit(bar_o);
+                    }
+                    ok = mbar_wait(bar_p + 16, pj, p.err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv_half(C::COL_O2, C::COL_S2, sv, 0, j > 0);
+                    ok = mbar_wait(bar_p + 24, pj, p.err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv_half(C::COL_O2, C::COL_S2, sv, 1, j > 0);
+                    mma_commit(bar_ve + 8 * vst);
+                    ++vc;
+                    if (more) {
+                        issue_qk(C::COL_S2, sQ2, k2_at());
+                        mma_commit(bar_s + 8);
+                        mma_commit(bar_ke + 8 * (kc % C::KS));
+                        ++kc;
+                        if (j + 2 == n_kv) mma_commit(bar_qe);   // last QK of the tile issued
+                    } else {
+                        mma_commit(bar_o + 8);
+                    }
                 }
-                ok = mbar_wait(bar_p + 16, pj, p.err);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv_half(C::COL_O2, C::COL_S2, v_at(j), 0, j > 0);
-                ok = mbar_wait(bar_p + 24, pj, p.err);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv_half(C::COL_O2, C::COL_S2, v_at(j), 1, j > 0);
-                mma_commit(bar_ve + 8 * (j % C::VS));
-                if (more) {
-                    issue_qk(C::COL_S2, sQ2, k2_at(j + 1));
-                    mma_commit(bar_s + 8);
-                    mma_commit(bar_ke + 8 * ((j + 1) % C::KS));
-                } else {
-                    mma_commit(bar_o + 8);
-                }
+                ++tc;
             }
             // no MMA may be in flight when TMEM is released
             mma_commit(bar_dr);
@@ -332,120 +375,133 @@ __global__ void __launch_bounds__(384, 1)
         const int br = (warp - 4) >> 2;
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
-        const int t = q0 + row;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + lane_off + (br ? C::COL_S2 : C::COL_S1);
         const uint32_t tO = tmem + lane_off + (br ? C::COL_O2 : C::COL_O1);
         const uint32_t my_s = bar_s + 8 * br, my_p = bar_p + 16 * br, my_o = bar_o + 8 * br;
-        // V2 gate logit of this row, fetched now and used in the epilogue
-        const float lg = (V2 && t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
         const float sl2 = p.scale_log2;
-        float m_ref = -INFINITY, l = 0.f;
+        float *xch = reinterpret_cast<float *>(smem + C::OFF_X);
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            ok = warp_wait(my_s, j & 1, p.err, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t s[C::BN];
-            tmem_ld32(tS + 0, s);
-            tmem_ld32(tS + 32, s + 32);
-            tmem_ld32(tS + 64, s + 64);
-            tmem_ld32(tS + 96, s + 96);
-            tmem_wait_ld();
-            if (j == qt) {   // diagonal tile: keys past this row are masked
-#pragma unroll
-                for (int c = 0; c < C::BN; ++c)
-                    if (c > row) s[c] = 0xff800000u;   // -inf
-            }
-            const float m_new = fmaxf(m_ref, row_max128(s) * sl2);
-            float alpha = 1.f;
-            const bool resc = m_new > m_ref + 8.f;
-            if (resc) {
-                alpha = ex2(m_ref - m_new);
-                l *= alpha;
-                m_ref = m_new;
-            }
-            if (j > 0 && __any_sync(0xffffffffu, resc)) {
-                // O_b is quiescent: PV_b(j-1) completed before S_b(j) was signalled.
-#pragma unroll 1
-                for (int c0 = 0; c0 < DV; c0 += 32) {
-                    uint32_t ov[32];
-                    tmem_ld32(tO + c0, ov);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
-                    tmem_st32(tO + c0, ov);
-                }
-                tmem_wait_st();
-            }
-            // P in two halves: the tensor core starts O += P V on keys 0-63
-            // while keys 64-127 are still being exponentiated.
-            l += exp_pack64(s, sl2, m_ref);
-            tmem_st32(tS + 0, s);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(my_p);
-            l += exp_pack64(s + 64, sl2, m_ref);
-            tmem_st32(tS + 32, s + 64);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(my_p + 8);
-        }
-
-        // ------------------------------------------------------- epilogue
-        ok = warp_wait(my_o, 0, p.err, ok);
-        if (!V2) ok = warp_wait(bar_lam, 0, p.err, ok);
-        tc_fence_after();
-        float *xch = reinterpret_cast<float *>(smem + C::OFF_X);   // Q1 tile is free now
-        xch[br * 128 + row] = l;
-        named_bar_sync(1, 256);
-        const float l1 = xch[row], l2 = xch[128 + row];
-        float lam_init = 0.f, c2;
-        if (V2) {
-            c2 = 1.f / (1.f + __expf(-lg)) / l2;
-        } else {
-            lam_init = lam_smem[1];
-            c2 = lam_smem[0] / l2;
-        }
-        const float c1 = 1.f / l1;
-        constexpr int HALF = DV / 2;
-        const int col0 = br * HALF;
-        float x[HALF];
-        float ss = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < HALF; cc += 32) {
-            uint32_t a[32], bb[32];
-            tmem_ld32(tmem + lane_off + C::COL_O1 + col0 + cc, a);
-            tmem_ld32(tmem + lane_off + C::COL_O2 + col0 + cc, bb);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const float v = __uint_as_float(a[k]) * c1 - __uint_as_float(bb[k]) * c2;
-                x[cc + k] = v;
-                ss = fmaf(v, v, ss);
-            }
-        }
+        float lam = 0.f, lam_init = 0.f;
         if (!V2) {
-            xch[256 + br * 128 + row] = ss;
-            named_bar_sync(1, 256);
-            const float ms = (xch[256 + row] + xch[384 + row]) * (1.f / static_cast<float>(DV));
-            const float r = (1.f - lam_init) * rsqrtf(ms + 1e-5f);
-#pragma unroll
-            for (int k = 0; k < HALF; ++k) x[k] *= r;
+            ok = warp_wait(bar_lam, 0, p.err, ok);
+            lam = lam_smem[0];
+            lam_init = lam_smem[1];
         }
-        if (ok && t < p.T) {
-            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + static_cast<int64_t>(b) * p.o_sb +
-                                 static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh + col0;
+        int it = 0;
+        // Every softmax warp walks the same tile list and reaches the same
+        // named barriers, also after an error (then it skips waits and work).
+        for (int k = 0;; ++k) {
+            const int w = snake_tile(k, cta, G, NT);
+            if (w < 0) break;
+            const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
+            const int h = rest % p.H, b = rest / p.H, n_kv = qt + 1;
+            const int t = qt * C::BM + row;
+            // V2 gate logit of this row, fetched now and used in the epilogue
+            const float lg = (V2 && t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < n_kv; ++j, ++it) {
+                ok = warp_wait(my_s, static_cast<uint32_t>(it & 1), p.err, ok);
+                if (!ok) continue;
+                tc_fence_after();
+                uint32_t s[C::BN];
+                tmem_ld32(tS + 0, s);
+                tmem_ld32(tS + 32, s + 32);
+                tmem_ld32(tS + 64, s + 64);
+                tmem_ld32(tS + 96, s + 96);
+                tmem_wait_ld();
+                if (j == qt) {   // diagonal tile: keys past this row are masked
 #pragma unroll
-            for (int k = 0; k < HALF; k += 8) {
-                uint4 v;
-                v.x = pack_bf16(x[k], x[k + 1]);
-                v.y = pack_bf16(x[k + 2], x[k + 3]);
-                v.z = pack_bf16(x[k + 4], x[k + 5]);
-                v.w = pack_bf16(x[k + 6], x[k + 7]);
-                *reinterpret_cast<uint4 *>(dst + k) = v;
+                    for (int c = 0; c < C::BN; ++c)
+                        if (c > row) s[c] = 0xff800000u;   // -inf
+                }
+                const float m_new = fmaxf(m_ref, row_max128(s) * sl2);
+                float alpha = 1.f;
+                const bool resc = m_new > m_ref + 8.f;
+                if (resc) {
+                    alpha = ex2(m_ref - m_new);
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                    // O_b is quiescent: PV_b(j-1) completed before S_b(j) was signalled.
+#pragma unroll 1
+                    for (int c0 = 0; c0 < DV; c0 += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + c0, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int kk = 0; kk < 32; ++kk) ov[kk] = __float_as_uint(__uint_as_float(ov[kk]) * alpha);
+                        tmem_st32(tO + c0, ov);
+                    }
+                    tmem_wait_st();
+                }
+                // P in two halves: the tensor core starts O += P V on keys 0-63
+                // while keys 64-127 are still being exponentiated.
+                l += exp_pack64(s, sl2, m_ref);
+                tmem_st32(tS + 0, s);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(my_p);
+                l += exp_pack64(s + 64, sl2, m_ref);
+                tmem_st32(tS + 32, s + 64);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(my_p + 8);
+            }
+
+            // --------------------------------------------------- epilogue
+            ok = warp_wait(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
+            tc_fence_after();
+            xch[br * 128 + row] = l;
+            named_bar_sync(1, 256);   // both branches' final O are complete past this point
+            tc_fence_after();
+            const float l1 = xch[row], l2 = xch[128 + row];
+            const float c2 = V2 ? 1.f / (1.f + __expf(-lg)) / l2 : lam / l2;
+            const float c1 = 1.f / l1;
+            constexpr int HALF = DV / 2;
+            const int col0 = br * HALF;
+            float x[HALF];
+            float ss = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < HALF; cc += 32) {
+                uint32_t a[32], bb[32];
+                tmem_ld32(tmem + lane_off + C::COL_O1 + col0 + cc, a);
+                tmem_ld32(tmem + lane_off + C::COL_O2 + col0 + cc, bb);
+                tmem_wait_ld();
+#pragma unroll
+                for (int kk = 0; kk < 32; ++kk) {
+                    const float v = __uint_as_float(a[kk]) * c1 - __uint_as_float(bb[kk]) * c2;
+                    x[cc + kk] = v;
+                    ss = fmaf(v, v, ss);
+                }
+            }
+            // O has been read: the next tile's first PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_od);
+            if (!V2) {
+                xch[256 + br * 128 + row] = ss;
+                named_bar_sync(1, 256);
+                const float ms = (xch[256 + row] + xch[384 + row]) * (1.f / static_cast<float>(DV));
+                const float r = (1.f - lam_init) * rsqrtf(ms + 1e-5f);
+#pragma unroll
+                for (int kk = 0; kk < HALF; ++kk) x[kk] *= r;
+            }
+            if (ok && t < p.T) {
+                __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + static_cast<int64_t>(b) * p.o_sb +
+                                     static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh + col0;
+#pragma unroll
+                for (int kk = 0; kk < HALF; kk += 8) {
+                    uint4 v;
+                    v.x = pack_bf16(x[kk], x[kk + 1]);
+                    v.y = pack_bf16(x[kk + 2], x[kk + 3]);
+                    v.z = pack_bf16(x[kk + 4], x[kk + 5]);
+                    v.w = pack_bf16(x[kk + 6], x[kk + 7]);
+                    *reinterpret_cast<uint4 *>(dst + kk) = v;
+                }
             }
         }
     }
@@ -480,9 +536,19 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
     }
     const int n_qt = (p.T + C::BM - 1) / C::BM;
-    const long long grid = static_cast<long long>(n_qt) * p.H * p.B;
-    if (grid < 1 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    prefill_onepass<DQK, DV, V2><<<static_cast<unsigned>(grid), 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, p);
+    const long long tiles = static_cast<long long>(n_qt) * p.H * p.B;
+    if (tiles < 1 || tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // persistent: one CTA per SM (shared memory and TMEM allow no more)
+    static int num_sms[64];
+    if (dev < 64 && num_sms[dev] == 0) {
+        int nsm = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess || nsm < 1) return e != cudaSuccess ? e : cudaErrorInvalidValue;
+        num_sms[dev] = nsm;
+    }
+    const int sms = dev < 64 ? num_sms[dev] : 1;
+    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
+    prefill_onepass<DQK, DV, V2><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, p);
     return cudaGetLastError();
 }
 
