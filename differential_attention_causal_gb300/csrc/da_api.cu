@@ -171,7 +171,8 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
         !encode_map_4d(&m.k1, k1, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
         !encode_map_4d(&m.k2, k2, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
         !encode_map_4d(&m.v, v, 2 * d, uH, uT, uB, v_sh, v_st, v_sb,
-                       twopass ? static_cast<uint32_t>(prefill_v1_twopass_v_rows(d)) : 128u))
+                       twopass ? static_cast<uint32_t>(prefill_v1_twopass_v_rows(d)) : 128u) ||
+        !encode_map_4d(&m.out, out, 2 * d, uH, uT, uB, o_sh, o_st, o_sb, 128))
         return DA_ERR_CUDA;
     PrefillParams p{};
     p.out = out; p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
@@ -222,7 +223,8 @@ da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const flo
     const int64_t qst = static_cast<int64_t>(Hq) * D, kst = static_cast<int64_t>(Hkv) * D;
     if (!encode_map_4d(&m.q1, q, D, Hq, uT, uB, D, qst, qst * T, 128) ||
         !encode_map_4d(&m.k1, k, D, Hkv, uT, uB, D, kst, kst * T, 128) ||
-        !encode_map_4d(&m.v, v, D, Hkv, uT, uB, D, kst, kst * T, 128))
+        !encode_map_4d(&m.v, v, D, Hkv, uT, uB, D, kst, kst * T, 128) ||
+        !encode_map_4d(&m.out, out, D, P, uT, uB, D, static_cast<int64_t>(P) * D, static_cast<int64_t>(P) * D * T, 128))
         return DA_ERR_CUDA;
     m.q2 = m.q1;
     m.k2 = m.k1;

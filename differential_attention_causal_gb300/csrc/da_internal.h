@@ -44,6 +44,7 @@ struct PrefillParams {
 };
 struct PrefillMaps {
     CUtensorMap q1, q2, k1, k2, v;
+    CUtensorMap out;   // one-pass kernel: output tile stores (box 64 x 1 x 128 x 1)
 };
 // dqk/dv in {64/128 (V1), 128/256 (V1 two-pass), 64/64, 128/128 (V2)}
 cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,

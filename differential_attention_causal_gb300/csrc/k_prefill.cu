@@ -34,7 +34,8 @@
 // the result is exact up to rounding.
 // Epilogue (same kernel): x = O1/l1 - c O2/l2 with c = lam (V1) or
 // sigmoid(lam[b,t,pair]) (V2); V1 then applies RMSNorm over the DV channels
-// (eps 1e-5) and the (1 - lam_init) scale; bf16 rows are stored directly.
+// (eps 1e-5) and the (1 - lam_init) scale; the bf16 tile is staged in shared
+// memory and written with TMA stores.
 #include "da_common.cuh"
 #include "da_internal.h"
 
@@ -52,18 +53,21 @@ struct PreCfg {
     static constexpr int NK = V2 ? 1 : 2;              // K tiles per key block (K1, K2)
     static constexpr int K_SLOT = NK * K_TILE;
     static constexpr int V_SLOT = VB * BOX;
-    static constexpr int XCH_FLOATS = V2 ? 256 : 512;  // l (and for V1 the RMS partials) per row
+    static constexpr int OUT_TILE = VB * BOX;          // bf16 output tile staged for TMA stores
     // Ring depths.  V(j) is needed one K-tile later than K(j) is freed, so
-    // with shared memory for only five slots the V ring gets the third one.
-    static constexpr bool ROOMY = 2 * Q_TILE + 3 * (K_SLOT + V_SLOT) + XCH_FLOATS * 4 + 2048 <= 232448;
-    static constexpr int KS = ROOMY ? 3 : (V2 ? 3 : 2);
+    // when shared memory is short the V ring keeps the deeper ring (V1).
+    static constexpr bool ROOMY = 2 * Q_TILE + 3 * (K_SLOT + V_SLOT) + OUT_TILE + 2048 <= 232448;
+    static constexpr int KS = ROOMY ? 3 : 2;
     static constexpr int VS = ROOMY ? 3 : (V2 ? 2 : 3);
     static constexpr int OFF_Q1 = 0;
     static constexpr int OFF_Q2 = Q_TILE;
     static constexpr int OFF_K = 2 * Q_TILE;
     static constexpr int OFF_V = OFF_K + KS * K_SLOT;
-    static constexpr int OFF_X = OFF_V + VS * V_SLOT;
-    static constexpr int OFF_BAR = OFF_X + XCH_FLOATS * 4;
+    static constexpr int OFF_OUT = OFF_V + VS * V_SLOT;
+    // epilogue exchange of l (and for V1 the RMS partials): the first 2 KB of
+    // the output staging tile, used before the tile is written
+    static constexpr int OFF_X = OFF_OUT;
+    static constexpr int OFF_BAR = OFF_OUT + OUT_TILE;
     // qfull, qfree, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s[2], p[2][2], o[2], odrain, drain, lam
     static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 3;
     static constexpr int OFF_LAM = OFF_BAR + NBAR * 8;        // 2 floats
@@ -118,7 +122,8 @@ template <int DQK, int DV, bool V2>
 __global__ void __launch_bounds__(384, 1)
     prefill_onepass(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
                     const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
-                    const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tout,
+                    const PrefillParams p) {
     using C = PreCfg<DQK, DV, V2>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(384, 1)
             if (w < 0) break;
             const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
             const int h = rest % p.H, b = rest / p.H, n_kv = qt + 1;
-            const int t = qt * C::BM + row;
+            const int t = qt * C::BM + row;   // query token of this thread's row
             // V2 gate logit of this row, fetched now and used in the epilogue
             const float lg = (V2 && t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
             float m_ref = -INFINITY, l = 0.f;
@@ -490,23 +495,37 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int kk = 0; kk < HALF; ++kk) x[kk] *= r;
             }
-            if (ok && t < p.T) {
-                __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + static_cast<int64_t>(b) * p.o_sb +
-                                     static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh + col0;
+            named_bar_sync(1, 256);   // exchange area read: the staging tile may be written
+            // Stage the bf16 row in the 128-byte-swizzled layout of the output
+            // map's 128 x 64 boxes, then one thread stores the tile with TMA
+            // (rows past T are clipped by the map's bounds).
 #pragma unroll
-                for (int kk = 0; kk < HALF; kk += 8) {
-                    uint4 v;
-                    v.x = pack_bf16(x[kk], x[kk + 1]);
-                    v.y = pack_bf16(x[kk + 2], x[kk + 3]);
-                    v.z = pack_bf16(x[kk + 4], x[kk + 5]);
-                    v.w = pack_bf16(x[kk + 6], x[kk + 7]);
-                    *reinterpret_cast<uint4 *>(dst + kk) = v;
+            for (int kk = 0; kk < HALF; kk += 8) {
+                const int col = col0 + kk, ch = (col & 63) >> 3;
+                uint4 v;
+                v.x = pack_bf16(x[kk], x[kk + 1]);
+                v.y = pack_bf16(x[kk + 2], x[kk + 3]);
+                v.z = pack_bf16(x[kk + 4], x[kk + 5]);
+                v.w = pack_bf16(x[kk + 6], x[kk + 7]);
+                *reinterpret_cast<uint4 *>(smem + C::OFF_OUT + (col >> 6) * C::BOX + row * 128 +
+                                           ((ch ^ (row & 7)) << 4)) = v;
+            }
+            fence_async_smem();
+            named_bar_sync(1, 256);
+            if (warp == 4 && lane == 0) {
+                if (ok) {
+#pragma unroll
+                    for (int bx = 0; bx < C::VB; ++bx)
+                        tma_store_4d(&tout, sbase + C::OFF_OUT + bx * C::BOX, 64 * bx, h, qt * C::BM, b);
+                    bulk_commit();
                 }
+                bulk_wait_read_all();   // staging tile (and exchange area) reusable
             }
         }
     }
 
     // ------------------------------------------------------------ teardown
+    if (warp == 4 && lane == 0) bulk_wait_all();   // output stores complete before exit
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -548,7 +567,7 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
     }
     const int sms = dev < 64 ? num_sms[dev] : 1;
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    prefill_onepass<DQK, DV, V2><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, p);
+    prefill_onepass<DQK, DV, V2><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, m.out, p);
     return cudaGetLastError();
 }
 
