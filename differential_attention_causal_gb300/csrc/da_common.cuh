@@ -291,30 +291,6 @@ __device__ __forceinline__ float ex2(float x) {   // 2^x, hardware approximation
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// 2^x for a pair of inputs on the FMA pipe (no MUFU).  Range reduction
-// x = n + f with n = rint(x), f in [-1/2, 1/2] (Cody and Waite); 2^f from the
-// cubic fitted by csrc/gen_exp2_poly.py (Lawson minimax on the relative error,
-// max relative error 7.5e-5, far below the 2^-9 of the bf16 rounding the
-// probabilities go through); 2^n is added to the exponent field.  Inputs are
-// clamped below at -125 so the result stays a normal number (or tiny); valid
-// for x <= 127.  Adding 1.5 * 2^23 rounds x to an integer held in the low
-// mantissa bits of the sum, which also supplies n for the exponent step.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    constexpr float kC0 = 0.99992806f, kC1 = 0.69326097f, kC2 = 0.24261114f, kC3 = 0.05517167f;
-    constexpr float kRound = 12582912.0f;
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
-    const float2 n = __fadd2_rn(t, make_float2(-kRound, -kRound));
-    const float2 f = __ffma2_rn(n, make_float2(-1.f, -1.f), x);
-    float2 q = __ffma2_rn(make_float2(kC3, kC3), f, make_float2(kC2, kC2));
-    q = __ffma2_rn(q, f, make_float2(kC1, kC1));
-    q = __ffma2_rn(q, f, make_float2(kC0, kC0));
-    const uint32_t rx = (__float_as_uint(t.x) << 23) + __float_as_uint(q.x);
-    const uint32_t ry = (__float_as_uint(t.y) << 23) + __float_as_uint(q.y);
-    return make_float2(__uint_as_float(rx), __uint_as_float(ry));
-}
-
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
