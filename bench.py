@@ -135,6 +135,27 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step: float, steps: int, world: int, max_ms: float, scale: float = 1e12) -> float:
+    """Whole-job rate: every rank processes its own batch (weak scaling), so the
+    work done is units_per_step * steps * world in the slowest rank's time."""
+    return units_per_step * steps * world / (max_ms * 1e-3) / scale
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own batch of the workload."""
+    return seed + rank
+
+
 def time_steps(step, steps: int, flush: torch.Tensor | None):
     """Per-step device time (ms) with CUDA events on the current stream; the
     L2 flush (if any) runs between steps, outside the events."""
@@ -157,7 +178,7 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
 
     peaks, peak_kind = load_peaks()
     s = inputs.WORKLOADS[HEADLINE]
-    x = inputs.make_v1(s, seed=args.seed + rank, device=dev)
+    x = inputs.make_v1(s, seed=rank_seed(args.seed, rank), device=dev)
     out = torch.empty((s.B, s.T, s.H, 2 * s.d), dtype=torch.bfloat16, device=dev)
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -180,15 +201,11 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times), world, dev)
     if binding.device_error():
         raise RuntimeError("a kernel reported a device-side wait timeout")
     flops = v1_flops(s)
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops, args.steps, world, total_ms)
     avg_ms = sum(times) / len(times)
     achieved = flops / (avg_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
@@ -221,12 +238,8 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
     et = time_steps(e2e_step, e2e_steps, flush)
     h2d = sum(host[n].numel() * host[n].element_size() for n in host)
     d2h = hout.numel() * hout.element_size()
-    e2e_ms = sum(et) / len(et)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = flops * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(sum(et) / len(et), world, dev)
+    e2e_val = job_throughput(flops, 1, world, e2e_ms)
 
     aux = {} if args.no_aux else run_aux(args, dev, peaks, peak_kind, binding)
 
