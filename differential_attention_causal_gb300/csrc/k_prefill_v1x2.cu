@@ -23,7 +23,8 @@
 // puts O in [0, dv) and S1, S2 after it.  With d = 64 (dv = 128) P has two
 // buffers of its own, so the next tile's S1, S2 are computed as soon as this
 // tile's have been read; with d = 128 (dv = 256) P is written over the part of
-// S1 its own warpgroup has already read and the next S follows the PV.
+// S1 its own warpgroup has already read, so the next S2 is computed before
+// the PV and only the next S1 follows it.
 // With dv = 256 a key tile of V is 64 KB, so V streams in 32-key items.
 //
 // Executed work per causal (query, key) pair: 2d (S1) + 2d (S2) in each pass
@@ -228,8 +229,10 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) ok = load_tile_k(0);
             for (int j = 0; ok && j < n; ++j) {
                 if (C::BIG) {
+                    // K2 of the next tile first: its S2 is computed before this tile's PV
+                    if (j + 1 < n) ok = load_k(j + 1, 1);
                     for (int it = 0; ok && it < C::V_ITEMS; ++it) ok = load_v(j, it);
-                    if (ok && j + 1 < n) ok = load_tile_k(j + 1);
+                    if (ok && j + 1 < n) ok = load_k(j + 1, 0);
                 } else {
                     if (j + 1 < n) ok = load_tile_k(j + 1);
                     if (ok) ok = load_v(j, 0);
@@ -280,6 +283,16 @@ __global__ void __launch_bounds__(384, 1)
                 ++ki;
                 return true;
             };
+            // one QK from the next K ring item (d = 128: items hold K1 or K2)
+            auto qk_one = [&](uint32_t col, uint32_t sq, uint32_t bar) {
+                if (!wait_k()) return false;
+                tc_fence_after();
+                issue_qk(col, sq, k_at());
+                if (bar) mma_commit(bar);
+                mma_commit(bar_ke + 8 * (ki % C::KS));
+                ++ki;
+                return true;
+            };
             // O += P V over V item `item` of tile j (keys item*V_ROWS ..); a P half
             // (64 keys) is waited for before its first K step.
             auto pv_item = [&](int j, int item) {
@@ -314,8 +327,12 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) ok = qk_pair(C::COL_S1, C::COL_S2, 0, bar_sbf);
             for (int j = 0; ok && j < n; ++j) {
                 if (C::BIG) {
+                    // P(j) lies over S1 only: S2 of the next tile goes first, once
+                    // this tile's S has been read, then the PV, then S1.
+                    if (j + 1 < n)
+                        ok = mbar_wait(bar_sbe, static_cast<uint32_t>(j & 1), p.err) && qk_one(C::COL_S2, sQ2, 0);
                     for (int it = 0; ok && it < C::V_ITEMS; ++it) ok = pv_item(j, it);
-                    if (ok && j + 1 < n) ok = qk_pair(C::COL_S1, C::COL_S2, 0, bar_sbf);
+                    if (ok && j + 1 < n) ok = qk_one(C::COL_S1, sQ1, bar_sbf);
                 } else {
                     if (j + 1 < n) {
                         ok = mbar_wait(bar_sbe, static_cast<uint32_t>(j & 1), p.err) &&
@@ -404,11 +421,9 @@ __global__ void __launch_bounds__(384, 1)
             tmem_ld32(tmem + lane_off + C::COL_S2 + 64 * br, s + 64);
             tmem_ld32(tmem + lane_off + C::COL_S2 + 64 * br + 32, s + 96);
             tmem_wait_ld();
-            if (!C::BIG) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_sbe);
-            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_sbe);   // this tile's S has been read
             if (j == qt) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
