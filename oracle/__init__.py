@@ -69,7 +69,10 @@ def _load():
             lib.oracle_v2_fwd.argtypes = [dp] * 4 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64, dp, ctypes.c_int]
             lib.oracle_v2_decode.restype = ctypes.c_int
             lib.oracle_v2_decode.argtypes = ([dp] * 4 + [ctypes.c_int, ctypes.c_int64] + [ctypes.c_int] * 3
-                                             + [i64p, ctypes.c_int64, dp, ctypes.c_int])
+                                             + [i64p, i64p, ctypes.c_int64, dp, ctypes.c_int])
+            lib.oracle_v1_decode.restype = ctypes.c_int
+            lib.oracle_v1_decode.argtypes = ([dp] * 9 + [ctypes.c_int, ctypes.c_int64] + [ctypes.c_int] * 3
+                                             + [i64p, i64p, ctypes.c_int64, dp, ctypes.c_int])
             _lib = lib
     return _lib
 
@@ -167,10 +170,19 @@ def v2_fwd(q, k, v, lam, rows=None, nthreads: int | None = None) -> np.ndarray:
     return out if r is not None else out.reshape(B, T, Hq // 2, D)
 
 
-def v2_decode(q, k_cache, v_cache, lam, rows=None, nthreads: int | None = None) -> np.ndarray:
+def _lens(lens, B, L):
+    if lens is None:
+        return None, None
+    a = np.ascontiguousarray(np.asarray(lens.cpu() if hasattr(lens, "cpu") else lens, dtype=np.int64).reshape(-1))
+    assert a.shape == (B,) and (a >= 1).all() and (a <= L).all(), "lens must hold B values in 1..L"
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+def v2_decode(q, k_cache, v_cache, lam, rows=None, nthreads: int | None = None, lens=None) -> np.ndarray:
     """DIFF V2 single-token decode against an L-row KV cache.
 
-    q: (B, Hq, D); caches: (B, L, Hkv, D); lam: (B, Hq/2).
+    q: (B, Hq, D); caches: (B, L, Hkv, D); lam: (B, Hq/2); lens: optional
+    (B,) rows attended per sequence (default all L).
     rows=None returns (B, Hq/2, D); otherwise flat ids b*(Hq/2) + i.
     """
     q, k, v, lam = (_f64(x) for x in (q, k_cache, v_cache, lam))
@@ -179,13 +191,40 @@ def v2_decode(q, k_cache, v_cache, lam, rows=None, nthreads: int | None = None) 
     assert Hq % Hkv == 0 and (Hq // Hkv) % 2 == 0
     assert k.shape == (B, L, Hkv, D) and v.shape == (B, L, Hkv, D)
     assert lam.shape == (B, Hq // 2)
+    la, lp = _lens(lens, B, L)
     r, rp, n = _rows(rows)
     out = np.empty(((n if r is not None else B * (Hq // 2)), D), dtype=np.float64)
     rc = _load().oracle_v2_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(lam), B, L, Hq, Hkv, D,
-                                  rp, n, _ptr(out), nthreads or default_threads())
+                                  lp, rp, n, _ptr(out), nthreads or default_threads())
     if rc:
         raise RuntimeError(f"oracle_v2_decode failed ({rc})")
     return out if r is not None else out.reshape(B, Hq // 2, D)
+
+
+def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, lq1, lk1, lq2, lk2, layer_index: int,
+              rows=None, nthreads: int | None = None, lens=None) -> np.ndarray:
+    """DIFF V1 single-token decode (the DiffAttnV1 operation for one new token
+    against L cached rows; "Differential Transformer V2", DiffAttnV1).
+
+    q1, q2: (B, H, d); k1, k2: (B, L, H, d); v: (B, L, H, 2d); lambda vectors (d,);
+    lens: optional (B,) rows attended per sequence.  rows=None returns (B, H, 2d),
+    otherwise flat ids b*H + h.
+    """
+    q1, q2, k1, k2, v = (_f64(x) for x in (q1, q2, k1_cache, k2_cache, v_cache))
+    lq1, lk1, lq2, lk2 = (_f64(x) for x in (lq1, lk1, lq2, lk2))
+    B, H, d = q1.shape
+    L = k1.shape[1]
+    assert q2.shape == (B, H, d) and k1.shape == (B, L, H, d) and k2.shape == (B, L, H, d)
+    assert v.shape == (B, L, H, 2 * d)
+    la, lp = _lens(lens, B, L)
+    r, rp, n = _rows(rows)
+    out = np.empty(((n if r is not None else B * H), 2 * d), dtype=np.float64)
+    rc = _load().oracle_v1_decode(_ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v), _ptr(lq1), _ptr(lk1),
+                                  _ptr(lq2), _ptr(lk2), B, L, H, d, int(layer_index), lp, rp, n, _ptr(out),
+                                  nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_v1_decode failed ({rc})")
+    return out if r is not None else out.reshape(B, H, 2 * d)
 
 
 def decode_gather(q, k_cache, v_cache, lam, rows):

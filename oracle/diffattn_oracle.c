@@ -109,6 +109,7 @@ typedef struct {
     double lam_full, lam_init;
     int B, T, H, dqk, dv, Hkv, G;
     int64_t L;
+    const int64_t *lens;      /* decode: cached rows per sequence, or NULL for L */
     const int64_t *rows;      /* nrows row ids, or NULL for all */
     int64_t nrows;
     double *out;
@@ -117,6 +118,19 @@ typedef struct {
 
 /* V1 row id r = (b*T + t)*H + h.  Layouts (contiguous):
  *   q1,q2,k1,k2 (B,T,H,d); v (B,T,H,2d); out row = 2d doubles. */
+/* DiffAttnV1 after the two attentions: x = a1 - lam*a2, RMSNorm over the
+ * 2d channels (no affine weight), times (1 - lam_init). */
+static void v1_combine(const job_t *J, const double *a1, const double *a2,
+                       double *x, double *y)
+{
+    const int dv = J->dv;
+    for (int c = 0; c < dv; ++c)
+        x[c] = a1[c] - J->lam_full * a2[c];
+    oracle_rmsnorm(x, dv, 1e-5, y);
+    for (int c = 0; c < dv; ++c)
+        y[c] *= (1.0 - J->lam_init);
+}
+
 static void v1_row(const job_t *J, int64_t r, double *scores, double *a1,
                    double *a2, double *x, double *y)
 {
@@ -135,11 +149,7 @@ static void v1_row(const job_t *J, int64_t r, double *scores, double *a1,
     /* causal: keys 0..t */
     attend_row(q1, k1, qk_row, v, v_row, (int64_t)t + 1, d, dv, scale, scores, a1);
     attend_row(q2, k2, qk_row, v, v_row, (int64_t)t + 1, d, dv, scale, scores, a2);
-    for (int c = 0; c < dv; ++c)
-        x[c] = a1[c] - J->lam_full * a2[c];
-    oracle_rmsnorm(x, dv, 1e-5, y);
-    for (int c = 0; c < dv; ++c)
-        y[c] *= (1.0 - J->lam_init);
+    v1_combine(J, a1, a2, x, y);
 }
 
 /* V2 prefill row id r = (b*T + t)*P + i, P = H (pairs).  Layouts:
@@ -176,15 +186,16 @@ static void dec_row(const job_t *J, int64_t r, double *scores, double *a1,
 {
     const int P = J->H, D = J->dqk, Hkv = J->Hkv, G = J->G;
     const int Hq = 2 * P;
-    const int64_t L = J->L;
+    const int64_t Lc = J->L;   /* rows allocated per sequence */
     const int i = (int)(r % P);
     const int b = (int)(r / P);
+    const int64_t L = J->lens ? J->lens[b] : Lc;   /* rows this sequence attends */
     const int he = 2 * i, ho = 2 * i + 1;
     const int g = he / G;
     const double *qe = J->q1 + ((int64_t)b * Hq + he) * D;
     const double *qo = J->q1 + ((int64_t)b * Hq + ho) * D;
-    const double *k = J->k1 + ((int64_t)b * L * Hkv + g) * D;
-    const double *v = J->v + ((int64_t)b * L * Hkv + g) * D;
+    const double *k = J->k1 + ((int64_t)b * Lc * Hkv + g) * D;
+    const double *v = J->v + ((int64_t)b * Lc * Hkv + g) * D;
     const int64_t kv_row = (int64_t)Hkv * D;
     const double scale = 1.0 / sqrt((double)D);
     attend_row(qe, k, kv_row, v, kv_row, L, D, D, scale, scores, a1);
@@ -195,10 +206,32 @@ static void dec_row(const job_t *J, int64_t r, double *scores, double *a1,
         y[c] = a1[c] - sg * a2[c];
 }
 
+/* V1 decode row id r = b*H + h.  Layouts:
+ *   q1, q2 (B,H,d); k1, k2 caches (B,L,H,d); v cache (B,L,H,2d); out row 2d.
+ * The new token attends cached rows 0 .. len_b - 1 of both branches. */
+static void v1dec_row(const job_t *J, int64_t r, double *scores, double *a1,
+                      double *a2, double *x, double *y)
+{
+    const int H = J->H, d = J->dqk, dv = J->dv;
+    const int64_t Lc = J->L;
+    const int h = (int)(r % H);
+    const int b = (int)(r / H);
+    const int64_t L = J->lens ? J->lens[b] : Lc;
+    const double *q1 = J->q1 + ((int64_t)b * H + h) * d;
+    const double *q2 = J->q2 + ((int64_t)b * H + h) * d;
+    const double *k1 = J->k1 + ((int64_t)b * Lc * H + h) * d;
+    const double *k2 = J->k2 + ((int64_t)b * Lc * H + h) * d;
+    const double *v = J->v + ((int64_t)b * Lc * H + h) * dv;
+    const double scale = 1.0 / sqrt((double)d);
+    attend_row(q1, k1, (int64_t)H * d, v, (int64_t)H * dv, L, d, dv, scale, scores, a1);
+    attend_row(q2, k2, (int64_t)H * d, v, (int64_t)H * dv, L, d, dv, scale, scores, a2);
+    v1_combine(J, a1, a2, x, y);
+}
+
 static void *worker(void *arg)
 {
     const job_t *J = (const job_t *)arg;
-    const int64_t nkeys = (J->kind == 3) ? J->L : (int64_t)J->T;
+    const int64_t nkeys = (J->kind >= 3) ? J->L : (int64_t)J->T;
     const int dv = J->dv;
     double *scores = (double *)malloc(sizeof(double) * (size_t)(nkeys > 0 ? nkeys : 1));
     double *buf = (double *)malloc(sizeof(double) * (size_t)dv * 4);
@@ -215,8 +248,10 @@ static void *worker(void *arg)
             v1_row(J, r, scores, a1, a2, x, y);
         else if (J->kind == 2)
             v2_row(J, r, scores, a1, a2, y);
-        else
+        else if (J->kind == 3)
             dec_row(J, r, scores, a1, a2, y);
+        else
+            v1dec_row(J, r, scores, a1, a2, x, y);
     }
     free(scores);
     free(buf);
@@ -294,20 +329,47 @@ int oracle_v2_fwd(const double *q, const double *k, const double *v,
 }
 
 /* DIFF V2 decode: one query token per sequence against an L-row cache.
+ * lens: rows attended per sequence (each in 1..L), or NULL for all L.
  * rows: ids b*(Hq/2)+i, or NULL for all.  out: nrows x D. */
 int oracle_v2_decode(const double *q, const double *k, const double *v,
                      const double *lam, int B, int64_t L, int Hq, int Hkv,
-                     int D, const int64_t *rows, int64_t nrows, double *out,
-                     int nthreads)
+                     int D, const int64_t *lens, const int64_t *rows,
+                     int64_t nrows, double *out, int nthreads)
 {
     job_t J;
     memset(&J, 0, sizeof(J));
     J.kind = 3;
+    J.lens = lens;
     J.q1 = q; J.k1 = k; J.v = v; J.lam = lam;
     J.B = B; J.L = L; J.H = Hq / 2; J.dqk = D; J.dv = D;
     J.Hkv = Hkv; J.G = Hq / Hkv;
     J.rows = rows;
     J.nrows = rows ? nrows : (int64_t)B * (Hq / 2);
+    J.out = out;
+    return run_jobs(&J, nthreads);
+}
+
+/* DIFF V1 decode: the V1 operation for one new query token per sequence
+ * against L cached rows (its own K/V included).  q1, q2 (B,H,d); k1, k2
+ * (B,L,H,d); v (B,L,H,2d); lens rows attended per sequence or NULL for L.
+ * rows: ids b*H+h, or NULL for all.  out: nrows x 2d. */
+int oracle_v1_decode(const double *q1, const double *q2, const double *k1,
+                     const double *k2, const double *v, const double *lq1,
+                     const double *lk1, const double *lq2, const double *lk2,
+                     int B, int64_t L, int H, int d, int layer_index,
+                     const int64_t *lens, const int64_t *rows, int64_t nrows,
+                     double *out, int nthreads)
+{
+    job_t J;
+    memset(&J, 0, sizeof(J));
+    J.kind = 4;
+    J.lens = lens;
+    J.q1 = q1; J.q2 = q2; J.k1 = k1; J.k2 = k2; J.v = v;
+    J.B = B; J.L = L; J.H = H; J.dqk = d; J.dv = 2 * d;
+    J.lam_init = oracle_lambda_init(layer_index);
+    J.lam_full = oracle_lambda_full(lq1, lk1, lq2, lk2, d, J.lam_init);
+    J.rows = rows;
+    J.nrows = rows ? nrows : (int64_t)B * H;
     J.out = out;
     return run_jobs(&J, nthreads);
 }

@@ -36,9 +36,18 @@ MUTANTS = {
                            "const int g = he % Hkv;"),
     "V2 sigmoid sign": ("    const double lg = J->lam[((int64_t)b * T + t) * P + i];\n    const double sg = 1.0 / (1.0 + exp(-lg));",
                         "    const double lg = J->lam[((int64_t)b * T + t) * P + i];\n    const double sg = 1.0 / (1.0 + exp(lg));"),
+    "decode lengths ignored": ("const int64_t L = J->lens ? J->lens[b] : Lc;   /* rows this sequence attends */",
+                               "const int64_t L = Lc;"),
+    "V2 decode cache stride from the length": ("const double *k = J->k1 + ((int64_t)b * Lc * Hkv + g) * D;",
+                                               "const double *k = J->k1 + ((int64_t)b * L * Hkv + g) * D;"),
+    "V1 decode branch 2 reads k1": ("attend_row(q2, k2, (int64_t)H * d,", "attend_row(q2, k1, (int64_t)H * d,"),
     "decode drops the last cache row": ("attend_row(qe, k, kv_row, v, kv_row, L, D, D, scale, scores, a1);",
                                         "attend_row(qe, k, kv_row, v, kv_row, L - 1, D, D, scale, scores, a1);"),
 }
+
+# mutants whose text stands at more than one site (every site is mutated:
+# the same mistake made in the prefill and the decode of one variant)
+SITES = {"scale 1/sqrt(2d) in V1": 2}
 
 # pin checks that take only the oracle (parametrised ones get one case each)
 CHECKS = [
@@ -53,13 +62,15 @@ CHECKS = [
     lambda o: pins.test_v2_matches_library_gqa(o, 2, 29, 8, 2, 8),
     pins.test_v2_sigmoid_zero_gives_even_head_attention,
     pins.test_decode_matches_library_and_last_prefill_row,
+    pins.test_v1_decode_matches_library_and_last_prefill_row,
+    pins.test_decode_lengths_read_only_each_sequence_rows,
     pins.test_causality_future_rows_do_not_matter,
 ]
 
 
 def _load_mutant(name, old, new, tmp_path):
     src = open(os.path.join(ORACLE_DIR, "diffattn_oracle.c")).read()
-    assert src.count(old) == 1, f"mutation site not unique / missing: {name}"
+    assert src.count(old) == SITES.get(name, 1), f"mutation site count changed: {name}"
     c_path = tmp_path / "oracle_mut.c"
     c_path.write_text(src.replace(old, new))
     spec = importlib.util.spec_from_file_location(f"oracle_mutant_{abs(hash(name))}",

@@ -284,6 +284,85 @@ def test_decode_matches_library_and_last_prefill_row(oracle):
     np.testing.assert_allclose(got, ref.numpy(), rtol=1e-10, atol=1e-12)
 
 
+def _v1_decode_library(q1, q2, k1, k2, v, lam, lam_init, lens):
+    """V1 decode by library calls, one sequence at a time: the new token's two
+    softmax attentions over the first len_b cached rows (torch fp64 SDPA, no
+    mask), lambda combination, library RMSNorm, times (1 - lam_init)."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    out = []
+    for b, n in enumerate(lens):
+        kk1 = t(k1[b, :n]).permute(1, 0, 2)          # (H,n,d)
+        kk2 = t(k2[b, :n]).permute(1, 0, 2)
+        vv = t(v[b, :n]).permute(1, 0, 2)            # (H,n,2d)
+        a1 = F.scaled_dot_product_attention(t(q1[b]).unsqueeze(1), kk1, vv)[:, 0]
+        a2 = F.scaled_dot_product_attention(t(q2[b]).unsqueeze(1), kk2, vv)[:, 0]
+        out.append(F.rms_norm(a1 - lam * a2, (v.shape[-1],), eps=1e-5) * (1 - lam_init))
+    return torch.stack(out).numpy()
+
+
+def test_v1_decode_matches_library_and_last_prefill_row(oracle):
+    B, L, H, d, layer = 2, 33, 3, 8, 5
+    q1f, q2f, k1, k2 = rng_arrays(64, *[(B, L, H, d)] * 4)
+    (v,) = rng_arrays(65, (B, L, H, 2 * d))
+    lv = rng_arrays(66, *[(d,)] * 4, std=0.5)
+    got = oracle.v1_decode(q1f[:, -1], q2f[:, -1], k1, k2, v, *lv, layer)
+    # (a) the last row of a causal V1 prefill over the same L rows
+    pre = oracle.v1_fwd(q1f, q2f, k1, k2, v, *lv, layer)
+    np.testing.assert_allclose(got, pre[:, -1], rtol=1e-12, atol=1e-14)
+    # (b) library attention of one query over all L keys
+    lam_init, lam = oracle.lambda_init(layer), oracle.lambda_full(*lv, layer)
+    ref = _v1_decode_library(q1f[:, -1], q2f[:, -1], k1, k2, v, lam, lam_init, [L] * B)
+    np.testing.assert_allclose(got, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_decode_lengths_read_only_each_sequence_rows(oracle):
+    """Per-sequence cache lengths: rows past len_b are never read (they hold
+    NaN here), and each sequence matches library attention over its prefix."""
+    B, L, Hq, Hkv, D = 3, 40, 8, 2, 8
+    lens = np.array([40, 17, 1])
+    q, = rng_arrays(67, (B, Hq, D))
+    k, v = rng_arrays(68, (B, L, Hkv, D), (B, L, Hkv, D))
+    (lam,) = rng_arrays(69, (B, Hq // 2))
+    for b, n in enumerate(lens):
+        k[b, n:] = np.nan
+        v[b, n:] = np.nan
+    got = oracle.v2_decode(q, k, v, lam, lens=lens)
+    assert np.isfinite(got).all()
+    G = Hq // Hkv
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    for b, n in enumerate(lens):
+        kk = t(k[b, :n]).permute(1, 0, 2).repeat_interleave(G, 0)
+        vv = t(v[b, :n]).permute(1, 0, 2).repeat_interleave(G, 0)
+        a = F.scaled_dot_product_attention(t(q[b]).unsqueeze(1), kk, vv)[:, 0]
+        ref = a[0::2] - torch.sigmoid(t(lam[b])).unsqueeze(-1) * a[1::2]
+        np.testing.assert_allclose(got[b], ref.numpy(), rtol=1e-10, atol=1e-12)
+    # a single cached row: both heads of a pair return that row's value
+    g_of_pair = (2 * np.arange(Hq // 2)) // G
+    one = (1 - 1 / (1 + np.exp(-lam[2])))[:, None] * v[2, 0, g_of_pair]
+    np.testing.assert_allclose(got[2], one, rtol=1e-13, atol=1e-15)
+
+    H, d, layer = 2, 4, 3
+    q1, q2 = rng_arrays(70, (B, H, d), (B, H, d))
+    k1, k2 = rng_arrays(71, (B, L, H, d), (B, L, H, d))
+    (vv,) = rng_arrays(72, (B, L, H, 2 * d))
+    lv = rng_arrays(73, *[(d,)] * 4, std=0.5)
+    for b, n in enumerate(lens):
+        k1[b, n:] = np.nan
+        k2[b, n:] = np.nan
+        vv[b, n:] = np.nan
+    got1 = oracle.v1_decode(q1, q2, k1, k2, vv, *lv, layer, lens=lens)
+    assert np.isfinite(got1).all()
+    lam_init, lamf = oracle.lambda_init(layer), oracle.lambda_full(*lv, layer)
+    ref1 = _v1_decode_library(q1, q2, k1, k2, vv, lamf, lam_init, lens)
+    np.testing.assert_allclose(got1, ref1, rtol=1e-10, atol=1e-12)
+    # a single cached row: x = (1 - lam) v0, so the output is v0 / rms(v0)
+    # (sign of 1 - lam) times (1 - lam_init), up to the eps inside the root
+    v0 = vv[2, 0]
+    x = (1 - lamf) * v0
+    closed = x / np.sqrt((x * x).mean(-1, keepdims=True) + 1e-5) * (1 - lam_init)
+    np.testing.assert_allclose(got1[2], closed, rtol=1e-12, atol=1e-14)
+
+
 # ------------------------------------------------------------ invariants ---
 
 def test_causality_future_rows_do_not_matter(oracle):
