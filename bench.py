@@ -6,8 +6,10 @@ combine, RMSNorm and the (1 - lam_init) scale -- every step of the V1 path)
 over the workload B=4, T=2048, 16 diff heads, d=64, dv=128, layer_index=12,
 bf16 inputs drawn N(0,1) with a seeded generator.  The line also carries, as
 auxiliary measurements, DIFF V2 prefill (B=8, T=4096, Hq=32, Hkv=8, D=128,
-TFLOP/s), long-context DIFF V1 (B=1, T=32768, 12 heads, d=128, TFLOP/s) and
-DIFF V2 decode (B=64, L=32768, Hq=64, Hkv=8, D=128, HBM GB/s).
+TFLOP/s), long-context DIFF V1 (B=1, T=32768, 12 heads, d=128, TFLOP/s),
+DIFF V2 decode (B=64, L=32768, Hq=64, Hkv=8, D=128, HBM GB/s), the same decode
+with per-sequence cache lengths uniform on 1..L, and DIFF V1 decode (B=32,
+L=16384, 12 heads, d=128, HBM GB/s).
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -65,6 +67,22 @@ def decode_bytes(s) -> int:
     """Bytes one decode must move: K and V caches once, q, lam, out."""
     return (2 * s.B * s.L * s.Hkv * s.D * 2 + s.B * s.Hq * s.D * 2
             + s.B * (s.Hq // 2) * 4 + s.B * (s.Hq // 2) * s.D * 2)
+
+
+def decode_varlen_bytes(s, lens) -> int:
+    """Bytes a decode with per-sequence lengths must move: each sequence's
+    first len_b cache rows of K and V, q, lam, out and the lengths."""
+    rows = int(sum(int(n) for n in lens))
+    return (2 * rows * s.Hkv * s.D * 2 + s.B * s.Hq * s.D * 2
+            + s.B * (s.Hq // 2) * 4 + s.B * (s.Hq // 2) * s.D * 2 + s.B * 4)
+
+
+def v1_decode_bytes(s, lens=None) -> int:
+    """Bytes one DIFF V1 decode must move: k1, k2 (d) and v (2d) cache rows
+    attended, q1, q2, out (2d) and the four lambda vectors."""
+    rows = s.B * s.L if lens is None else int(sum(int(n) for n in lens))
+    return (rows * s.H * 4 * s.d * 2 + 2 * s.B * s.H * s.d * 2 + s.B * s.H * 2 * s.d * 2
+            + 4 * s.d * 4 + (0 if lens is None else s.B * 4))
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -316,6 +334,44 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                         "launches": 2, "peak_kind": peak_kind}
     del x, out, ws
     torch.cuda.empty_cache()
+    # DIFF V2 decode, per-sequence lengths uniform on 1..L (the same cache allocation)
+    s = inputs.WORKLOADS["v2_decode_varlen_bf16_B64_L32768_Hq64_Hkv8_D128"]
+    x = inputs.make_decode(s, seed=args.seed, device=dev)
+    out = torch.empty((s.B, s.Hq // 2, s.D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(binding.decode_workspace_size(s.B, s.L, s.Hq, s.Hkv, s.D), dtype=torch.uint8, device=dev)
+    f = lambda: binding.v2_decode_varlen(x["q"], x["k_cache"], x["v_cache"], x["lam"], x["cache_lens"],  # noqa
+                                         out=out, workspace=ws)
+    for _ in range(3):
+        f()
+    t = time_steps(f, 20, flush)
+    ms = sum(t) / len(t)
+    lens = x["cache_lens"].cpu().tolist()
+    gbs = decode_varlen_bytes(s, lens) / (ms * 1e-3) / 1e9
+    aux["v2_decode_varlen"] = {"workload": "v2_decode_varlen_bf16_B64_L32768_Hq64_Hkv8_D128", "ms": round(ms, 4),
+                               "cached_rows": int(sum(lens)), "GB/s": round(gbs, 1),
+                               "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                               "tokens_per_s": round(s.B / (ms * 1e-3)), "launches": 3, "l2_flush": True,
+                               "peak_kind": peak_kind}
+    del x, out, ws
+    torch.cuda.empty_cache()
+    # DIFF V1 decode, d = 128 (6.4 GB of k1, k2, v cache >> L2)
+    s = inputs.WORKLOADS["v1_decode_bf16_B32_L16384_H12_d128"]
+    x = inputs.make_v1_decode(s, seed=args.seed, device=dev)
+    out = torch.empty((s.B, s.H, 2 * s.d), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(binding.v1_decode_workspace_size(s.B, s.L, s.H, s.d), dtype=torch.uint8, device=dev)
+    f = lambda: binding.v1_decode(x["q1"], x["q2"], x["k1_cache"], x["k2_cache"], x["v_cache"],  # noqa
+                                  x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"], s.layer_index,
+                                  out=out, workspace=ws)
+    for _ in range(3):
+        f()
+    t = time_steps(f, 20, None)
+    ms = sum(t) / len(t)
+    gbs = v1_decode_bytes(s) / (ms * 1e-3) / 1e9
+    aux["v1_decode"] = {"workload": "v1_decode_bf16_B32_L16384_H12_d128", "ms": round(ms, 4),
+                        "GB/s": round(gbs, 1), "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                        "tokens_per_s": round(s.B / (ms * 1e-3)), "launches": 2, "peak_kind": peak_kind}
+    del x, out, ws
+    torch.cuda.empty_cache()
     if binding.device_error():
         raise RuntimeError("a kernel reported a device-side wait timeout")
     return aux
@@ -414,6 +470,8 @@ CASES = {
     # the decode workload with 8 of its 64 sequences: 1.07 GB of cache, small
     # enough for multi-pass profiler captures, still far larger than L2
     "decode_b8": ("decode", None),
+    "decode_varlen": ("decode_varlen", "v2_decode_varlen_bf16_B64_L32768_Hq64_Hkv8_D128"),
+    "v1_decode": ("v1_decode", "v1_decode_bf16_B32_L16384_H12_d128"),
 }
 
 
@@ -428,6 +486,12 @@ def run_case(name: str, launches: int):
                                    x["lam_q2"], x["lam_k2"], s.layer_index)
     elif kind == "v2":
         f = lambda: binding.v2_fwd(x["q"], x["k"], x["v"], x["lam"])  # noqa: E731
+    elif kind == "decode_varlen":
+        f = lambda: binding.v2_decode_varlen(x["q"], x["k_cache"], x["v_cache"], x["lam"],  # noqa: E731
+                                             x["cache_lens"])
+    elif kind == "v1_decode":
+        f = lambda: binding.v1_decode(x["q1"], x["q2"], x["k1_cache"], x["k2_cache"], x["v_cache"],  # noqa
+                                      x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"], s.layer_index)
     else:
         f = lambda: binding.v2_decode(x["q"], x["k_cache"], x["v_cache"], x["lam"])  # noqa: E731
     for _ in range(launches):

@@ -53,6 +53,14 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v2_decode.argtypes = ([vp, vp, vp, fp, vp, vp, ctypes.c_size_t] + [i32] * 5 + [i32, vp])
             L.diffattn_v2_decode_noalloc.restype = i32
             L.diffattn_v2_decode_noalloc.argtypes = [vp, vp, vp, fp, vp] + [i32] * 5 + [i32, vp]
+            L.diffattn_v2_decode_varlen.restype = i32
+            L.diffattn_v2_decode_varlen.argtypes = ([vp, vp, vp, fp, vp, vp, vp, ctypes.c_size_t] + [i32] * 5
+                                                    + [i32, vp])
+            L.diffattn_v1_decode_workspace_size.restype = ctypes.c_size_t
+            L.diffattn_v1_decode_workspace_size.argtypes = [i32] * 5
+            L.diffattn_v1_decode.restype = i32
+            L.diffattn_v1_decode.argtypes = ([vp] * 5 + [fp] * 4 + [vp, vp, vp, ctypes.c_size_t] + [i32] * 5
+                                             + [i32, vp])
             L.diffattn_status_string.restype = ctypes.c_char_p
             L.diffattn_status_string.argtypes = [i32]
             L.diffattn_device_error.restype = i32
@@ -76,7 +84,7 @@ def device_error() -> int:
     """Synchronise, then read and clear the device error word (0 = no kernel gave up)."""
     code = ctypes.c_uint32(0)
     rc = lib().diffattn_device_error(ctypes.byref(code))
-    if rc not in (0, 9):
+    if rc not in (0, 9, 11):
         raise DiffAttnError("diffattn_device_error", rc)
     return int(code.value)
 
@@ -212,4 +220,82 @@ def v2_decode_noalloc(q, k_cache, v_cache, lam, out: torch.Tensor | None = None,
     rc = lib().diffattn_v2_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), lam.data_ptr(),
                                           out.data_ptr(), B, L, Hq, Hkv, D, _dtype_code(q), _stream(stream))
     _check("diffattn_v2_decode_noalloc", rc)
+    return out
+
+
+def _lens_arg(cache_lens, B: int, device) -> torch.Tensor:
+    if not isinstance(cache_lens, torch.Tensor) or not cache_lens.is_cuda:
+        raise ValueError("cache_lens must be a CUDA tensor")
+    if cache_lens.dtype != torch.int32 or cache_lens.numel() != B or not cache_lens.is_contiguous():
+        raise ValueError("cache_lens must be a contiguous int32 tensor of B lengths")
+    return cache_lens
+
+
+def v2_decode_varlen(q, k_cache, v_cache, lam, cache_lens, out: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """DIFF V2 decode with a cache length per sequence: sequence b attends
+    cache rows 0 .. cache_lens[b]-1.  cache_lens: int32 CUDA tensor (B,), each
+    in 1..L (a length out of range is clamped and reported by device_error()).
+    Other arguments as v2_decode."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("lam", lam)):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, Hq, D = q.shape
+    L, Hkv = k_cache.shape[1], k_cache.shape[2]
+    _lens_arg(cache_lens, B, q.device)
+    if out is None:
+        out = torch.empty((B, Hq // 2, D), dtype=q.dtype, device=q.device)
+    need = decode_workspace_size(B, L, Hq, Hkv, D, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = lib().diffattn_v2_decode_varlen(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), lam.data_ptr(),
+                                         cache_lens.data_ptr(), out.data_ptr(), workspace.data_ptr(),
+                                         workspace.numel(), B, L, Hq, Hkv, D, _dtype_code(q), _stream(stream))
+    _check("diffattn_v2_decode_varlen", rc)
+    return out
+
+
+def v1_decode_workspace_size(B: int, L: int, H: int, d: int, dtype=torch.bfloat16) -> int:
+    code = DA_BF16 if dtype == torch.bfloat16 else DA_F32
+    return int(lib().diffattn_v1_decode_workspace_size(B, L, H, d, code))
+
+
+def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, lam_q1, lam_k1, lam_q2, lam_k2, layer_index: int,
+              cache_lens=None, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """DIFF V1 single-token decode ("Differential Transformer V2", DiffAttnV1
+    for one new token per sequence).
+
+    q1, q2: (B, H, d); k1_cache, k2_cache: (B, L, H, d); v_cache: (B, L, H, 2d),
+    all contiguous CUDA tensors; lam_*: fp32 (d,); cache_lens: optional int32
+    CUDA tensor (B,) of rows attended per sequence (default all L).
+    Returns out (B, H, 2d).
+    """
+    for n, t in (("q1", q1), ("q2", q2), ("k1_cache", k1_cache), ("k2_cache", k2_cache), ("v_cache", v_cache)):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, H, d = q1.shape
+    L = k1_cache.shape[1]
+    lams = [x.contiguous() for x in (lam_q1, lam_k1, lam_q2, lam_k2)]
+    for x in lams:
+        if x.dtype != torch.float32 or not x.is_cuda or x.numel() != d:
+            raise ValueError("lambda vectors must be fp32 CUDA tensors of length d")
+    lens_ptr = None
+    if cache_lens is not None:
+        lens_ptr = _lens_arg(cache_lens, B, q1.device).data_ptr()
+    if out is None:
+        out = torch.empty((B, H, 2 * d), dtype=q1.dtype, device=q1.device)
+    ws_ptr, ws_bytes = None, 0
+    if q1.dtype == torch.bfloat16:
+        need = v1_decode_workspace_size(B, L, H, d, q1.dtype)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q1.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    rc = lib().diffattn_v1_decode(q1.data_ptr(), q2.data_ptr(), k1_cache.data_ptr(), k2_cache.data_ptr(),
+                                  v_cache.data_ptr(), *[x.data_ptr() for x in lams], lens_ptr, out.data_ptr(),
+                                  ws_ptr, ws_bytes, B, L, H, d, int(layer_index), _dtype_code(q1),
+                                  _stream(stream))
+    _check("diffattn_v1_decode", rc)
     return out

@@ -104,6 +104,7 @@ const char *diffattn_status_string(da_status s) {
         case DA_ERR_SCRATCH_LIMIT:
             return "sizes need more decode scratch than the library's static 8 MiB buffer; "
                    "use diffattn_v2_decode with a workspace";
+        case DA_ERR_BAD_LENGTH: return "a decode cache length was outside 1..L and was clamped";
     }
     return "unknown status";
 }
@@ -119,6 +120,7 @@ da_status diffattn_device_error(uint32_t *code) {
     if (v != 0 && cudaMemset(err, 0, sizeof(v)) != cudaSuccess) return DA_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
     if (code) *code = v;
+    if (v == kErrBadLength) return DA_ERR_BAD_LENGTH;
     return v ? DA_ERR_DEVICE_TIMEOUT : DA_OK;
 }
 
@@ -243,19 +245,60 @@ da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const flo
 size_t diffattn_v2_decode_workspace_size(int B, int L, int Hq, int Hkv, int D, da_dtype dtype) {
     if (dtype == DA_F32) return 0;
     if (dtype != DA_BF16 || Hkv < 1 || Hq % Hkv != 0) return 0;
+    if (D != 64 && D != 128) return 0;
     uint32_t *err = nullptr;
     int nsm = 0;
     if (!device_state(&err, &nsm)) return 0;
-    int grid, max_seg, spb;
+    int grid, spb;
     int64_t units;
-    size_t ws = 0;
-    if (!decode_plan(B, L, Hq, Hkv, D, nsm, &grid, &max_seg, &units, &spb, &ws)) return 0;
+    size_t cum = 0, ws = 0;
+    // sized for per-sequence lengths, which also covers the all-L call
+    if (!decode_plan(B, L, Hkv, D, nsm, true, &grid, &units, &spb, &cum, &ws)) return 0;
     return ws;
 }
 
-da_status diffattn_v2_decode(const void *q, const void *k_cache, const void *v_cache, const float *lam, void *out,
-                             void *workspace, size_t workspace_bytes, int B, int L, int Hq, int Hkv, int D,
-                             da_dtype dtype, cudaStream_t stream) {
+size_t diffattn_v1_decode_workspace_size(int B, int L, int H, int d, da_dtype dtype) {
+    if (dtype != DA_BF16 || (d != 64 && d != 128)) return 0;
+    uint32_t *err = nullptr;
+    int nsm = 0;
+    if (!device_state(&err, &nsm)) return 0;
+    int grid, spb;
+    int64_t units;
+    size_t cum = 0, ws = 0;
+    if (!decode_plan(B, L, H, 2 * d, nsm, true, &grid, &units, &spb, &cum, &ws)) return 0;
+    return ws;
+}
+
+}  // extern "C"
+
+namespace {
+
+// bf16 split-KV decode shared by the V2 and V1 entry points (arguments
+// already checked): plan, tensor maps, workspace split, launch.
+da_status decode_bf16(bool v1, const DecodeMaps &m, DecodeParams p, const int32_t *lens, void *workspace,
+                      size_t workspace_bytes, int nsm, cudaStream_t stream) {
+    int grid, spb;
+    int64_t units;
+    size_t cum = 0, need = 0;
+    if (!decode_plan(p.B, p.L, p.Hkv, p.D, nsm, lens != nullptr, &grid, &units, &spb, &cum, &need))
+        return DA_ERR_BAD_SHAPE;
+    if (!workspace) return DA_ERR_NULL_PTR;
+    if (!aligned16(workspace)) return DA_ERR_MISALIGNED;
+    if (workspace_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
+    p.lens = lens;
+    p.cum = lens ? static_cast<int64_t *>(workspace) : nullptr;
+    p.ws = reinterpret_cast<float *>(static_cast<char *>(workspace) + cum);
+    p.grid = grid;
+    p.units = units;
+    p.spb = spb;
+    const da_status st = cuda_status(launch_decode(m, p, v1, stream));
+    if (st == DA_OK) t_last_launches = lens ? 3 : 2;
+    return st;
+}
+
+da_status v2_decode_impl(const void *q, const void *k_cache, const void *v_cache, const float *lam,
+                         const int32_t *lens, void *out, void *workspace, size_t workspace_bytes, int B, int L,
+                         int Hq, int Hkv, int D, da_dtype dtype, cudaStream_t stream) {
     if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
     if (!q || !k_cache || !v_cache || !lam || !out) return DA_ERR_NULL_PTR;
     if (B < 1 || L < 1 || Hq < 2 || Hkv < 1) return DA_ERR_BAD_SHAPE;
@@ -280,19 +323,13 @@ da_status diffattn_v2_decode(const void *q, const void *k_cache, const void *v_c
         p.out = static_cast<float *>(out);
         p.lam = lam; p.lam_st = 0; p.lam_sb = P;
         p.B = B; p.Tq = 1; p.Lk = L; p.H = P; p.G = G; p.mode = 2;
+        p.lens = lens;
         p.err = err;
         const da_status st = cuda_status(launch_simt(p, D, D, stream));
         if (st == DA_OK) t_last_launches = 1;
         return st;
     }
     if (G > 8) return DA_ERR_BAD_GROUP;
-    int grid, max_seg, spb;
-    int64_t units;
-    size_t need = 0;
-    if (!decode_plan(B, L, Hq, Hkv, D, nsm, &grid, &max_seg, &units, &spb, &need)) return DA_ERR_BAD_SHAPE;
-    if (!workspace) return DA_ERR_NULL_PTR;
-    if (!aligned16(workspace)) return DA_ERR_MISALIGNED;
-    if (workspace_bytes < need) return DA_ERR_WORKSPACE_TOO_SMALL;
     DecodeMaps m;
     const int64_t st_row = static_cast<int64_t>(Hkv) * D;
     if (!encode_map_4d(&m.k, k_cache, D, Hkv, static_cast<uint64_t>(L), B, D, st_row, st_row * L,
@@ -300,18 +337,93 @@ da_status diffattn_v2_decode(const void *q, const void *k_cache, const void *v_c
         !encode_map_4d(&m.v, v_cache, D, Hkv, static_cast<uint64_t>(L), B, D, st_row, st_row * L,
                        kDecodeKeysPerUnit))
         return DA_ERR_CUDA;
+    m.k2 = m.k;
     DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.lam = lam;
     p.out = static_cast<__nv_bfloat16 *>(out);
-    p.ws = static_cast<float *>(workspace);
     p.B = B; p.L = L; p.Hq = Hq; p.Hkv = Hkv; p.G = G; p.D = D;
-    p.grid = grid; p.max_seg = max_seg; p.units = units; p.spb = spb;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     p.err = err;
-    const da_status st = cuda_status(launch_decode(m, p, stream));
-    if (st == DA_OK) t_last_launches = 2;
-    return st;
+    return decode_bf16(false, m, p, lens, workspace, workspace_bytes, nsm, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+da_status diffattn_v2_decode(const void *q, const void *k_cache, const void *v_cache, const float *lam, void *out,
+                             void *workspace, size_t workspace_bytes, int B, int L, int Hq, int Hkv, int D,
+                             da_dtype dtype, cudaStream_t stream) {
+    return v2_decode_impl(q, k_cache, v_cache, lam, nullptr, out, workspace, workspace_bytes, B, L, Hq, Hkv, D,
+                          dtype, stream);
+}
+
+da_status diffattn_v2_decode_varlen(const void *q, const void *k_cache, const void *v_cache, const float *lam,
+                                    const int32_t *cache_lens, void *out, void *workspace, size_t workspace_bytes,
+                                    int B, int L, int Hq, int Hkv, int D, da_dtype dtype, cudaStream_t stream) {
+    if (!cache_lens) return DA_ERR_NULL_PTR;
+    if ((reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return DA_ERR_MISALIGNED;
+    return v2_decode_impl(q, k_cache, v_cache, lam, cache_lens, out, workspace, workspace_bytes, B, L, Hq, Hkv,
+                          D, dtype, stream);
+}
+
+da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cache, const void *k2_cache,
+                             const void *v_cache, const float *lam_q1, const float *lam_k1, const float *lam_q2,
+                             const float *lam_k2, const int32_t *cache_lens, void *out, void *workspace,
+                             size_t workspace_bytes, int B, int L, int H, int d, int layer_index, da_dtype dtype,
+                             cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q1 || !q2 || !k1_cache || !k2_cache || !v_cache || !lam_q1 || !lam_k1 || !lam_q2 || !lam_k2 || !out)
+        return DA_ERR_NULL_PTR;
+    if (B < 1 || L < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
+    if (dtype == DA_BF16 ? (d != 64 && d != 128) : (d != 32 && d != 64 && d != 128))
+        return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q1, q2, k1_cache, k2_cache, v_cache, static_cast<const void *>(out)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    if (cache_lens && (reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return DA_ERR_MISALIGNED;
+    uint32_t *err = nullptr;
+    int nsm = 0;
+    if (!device_state(&err, &nsm)) return DA_ERR_CUDA;
+    t_last_launches = 0;
+    const int dv = 2 * d;
+    if (dtype == DA_F32) {
+        SimtParams p{};
+        p.q1 = static_cast<const float *>(q1);
+        p.q2 = static_cast<const float *>(q2);
+        p.k1 = static_cast<const float *>(k1_cache);
+        p.k2 = static_cast<const float *>(k2_cache);
+        p.v = static_cast<const float *>(v_cache);
+        p.q_sh = d; p.q_st = 0; p.q_sb = static_cast<int64_t>(H) * d;
+        p.k_sh = d; p.k_st = static_cast<int64_t>(H) * d; p.k_sb = p.k_st * L;
+        p.v_sh = dv; p.v_st = static_cast<int64_t>(H) * dv; p.v_sb = p.v_st * L;
+        p.o_sh = dv; p.o_st = 0; p.o_sb = static_cast<int64_t>(H) * dv;
+        p.out = static_cast<float *>(out);
+        p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+        p.layer_index = layer_index;
+        p.B = B; p.Tq = 1; p.Lk = L; p.H = H; p.G = 1; p.mode = 1;
+        p.lens = cache_lens;
+        p.err = err;
+        const da_status st = cuda_status(launch_simt(p, d, dv, stream));
+        if (st == DA_OK) t_last_launches = 1;
+        return st;
+    }
+    DecodeMaps m;
+    const int64_t kr = static_cast<int64_t>(H) * d, vr = static_cast<int64_t>(H) * dv;
+    if (!encode_map_4d(&m.k, k1_cache, d, H, static_cast<uint64_t>(L), B, d, kr, kr * L, kDecodeKeysPerUnit) ||
+        !encode_map_4d(&m.k2, k2_cache, d, H, static_cast<uint64_t>(L), B, d, kr, kr * L, kDecodeKeysPerUnit) ||
+        !encode_map_4d(&m.v, v_cache, dv, H, static_cast<uint64_t>(L), B, dv, vr, vr * L, kDecodeKeysPerUnit))
+        return DA_ERR_CUDA;
+    DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q1);
+    p.q2 = static_cast<const __nv_bfloat16 *>(q2);
+    p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+    p.layer_index = layer_index;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.B = B; p.L = L; p.Hq = H; p.Hkv = H; p.G = 2; p.D = dv;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
+    p.err = err;
+    return decode_bf16(true, m, p, cache_lens, workspace, workspace_bytes, nsm, stream);
 }
 
 }  // extern "C"
@@ -356,11 +468,11 @@ extern "C" da_status diffattn_v2_decode_noalloc(const void *q, const void *k_cac
         return diffattn_v2_decode(q, k_cache, v_cache, lam, out, nullptr, 0, B, L, Hq, Hkv, D, dtype, stream);
     uint32_t *err = nullptr;
     int nsm = 0;
-    int grid, max_seg, spb;
+    int grid, spb;
     int64_t units;
-    size_t need = 0;
-    if (B >= 1 && L >= 1 && Hq >= 2 && Hkv >= 1 && Hq % Hkv == 0 && device_state(&err, &nsm) &&
-        decode_plan(B, L, Hq, Hkv, D, nsm, &grid, &max_seg, &units, &spb, &need) &&
+    size_t cum = 0, need = 0;
+    if (B >= 1 && L >= 1 && Hq >= 2 && Hkv >= 1 && Hq % Hkv == 0 && (D == 64 || D == 128) &&
+        device_state(&err, &nsm) && decode_plan(B, L, Hkv, D, nsm, false, &grid, &units, &spb, &cum, &need) &&
         need > kNoAllocScratchBytes)
         return DA_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;

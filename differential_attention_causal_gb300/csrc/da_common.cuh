@@ -14,15 +14,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "da_internal.h"
+
 namespace da {
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s of global time
 
-// Bits of the device error word.
-enum : uint32_t {
-    kErrWaitTimeout = 1u,      // a bounded mbarrier wait gave up
-    kErrAborted = 2u,          // a kernel saw an earlier error and returned early
-};
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -67,14 +64,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Wait for the phase with the given parity to complete.  Returns false after
 // recording kErrWaitTimeout if it does not within kWaitTimeoutNs, or false at
-// once if the error word is already non-zero (another CTA gave up).
+// once if the error word already holds a fatal bit (another CTA gave up).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
-            if (ld_volatile_u32(err) != 0) return false;
+            if ((ld_volatile_u32(err) & kErrFatal) != 0) return false;
             if (global_timer_ns() - t0 > kWaitTimeoutNs) {
                 atomicOr(err, kErrWaitTimeout);
                 return false;

@@ -9,6 +9,14 @@
 
 namespace da {
 
+// Bits of the device error word.
+enum : uint32_t {
+    kErrWaitTimeout = 1u,      // a bounded mbarrier wait gave up
+    kErrAborted = 2u,          // a kernel saw an earlier error and returned early
+    kErrBadLength = 4u,        // a decode cache length outside 1 .. L (clamped)
+    kErrFatal = kErrWaitTimeout | kErrAborted,   // bits after which kernels stop waiting
+};
+
 // ---------------------------------------------------------------- SIMT fp32
 // One warp per output row.  mode 1 = DIFF V1, mode 2 = DIFF V2 (prefill or
 // decode).  Query t attends keys 0 .. t + (Lk - Tq): Lk == Tq is the causal
@@ -25,6 +33,7 @@ struct SimtParams {
     const float *lq1, *lk1, *lq2, *lk2;
     int layer_index;
     int B, Tq, Lk, H, G, mode;
+    const int *lens;               // decode (Tq == 1): keys per sequence, or NULL
     uint32_t *err;
 };
 cudaError_t launch_simt(const SimtParams &p, int dqk, int dv, cudaStream_t s);
@@ -57,26 +66,38 @@ cudaError_t launch_prefill_v1_twopass(const PrefillMaps &m, const PrefillParams 
 int prefill_v1_twopass_v_rows(int dqk);
 
 // --------------------------------------------------------------- decode
+// One kernel family serves three decodes:
+//   V2      : kv head g of sequence b feeds the G query heads g*G .. g*G+G-1;
+//   V1      : "kv head" = diff head h; the two score columns are q1 . k1 and
+//             q2 . k2 (K tile = k1 channels, then k2 channels), V is 2d wide;
+// and either with every sequence attending all L cached rows (lens == NULL)
+// or sequence b attending rows 0 .. lens[b]-1.
 struct DecodeParams {
-    const __nv_bfloat16 *q;        // (B, Hq, D)
-    const float *lam;              // (B, Hq/2)
-    __nv_bfloat16 *out;            // (B, Hq/2, D)
-    float *ws;                     // workspace (partials)
-    int B, L, Hq, Hkv, G, D;
+    const __nv_bfloat16 *q;        // V2: (B, Hq, D).  V1: q1 (B, H, d)
+    const __nv_bfloat16 *q2;       // V1: q2 (B, H, d)
+    const float *lam;              // V2 logits (B, Hq/2)
+    const float *lq1, *lk1, *lq2, *lk2;   // V1 lambda vectors (d)
+    int layer_index;               // V1
+    __nv_bfloat16 *out;            // V2: (B, Hq/2, D).  V1: (B, H, 2d)
+    float *ws;                     // partial slots: B * Hkv + grid - 1
+    const int *lens;               // per-sequence rows (B), or NULL for all L
+    int64_t *cum;                  // lens != NULL: units before sequence b (B + 1)
+    int B, L, Hq, Hkv, G, D;       // V1: Hq = Hkv = H, G = 2, D = 2d
     int grid;                      // CTAs of the split kernel
-    int max_seg;                   // partial slots per CTA
-    int64_t units;                 // B * Hkv * ceil(L / 64)
-    int spb;                       // 64-key units per (b, kv head)
-    float scale_log2;
+    int64_t units;                 // lens == NULL: B * Hkv * spb
+    int spb;                       // 64-key units per (b, kv head) at L rows
+    float scale_log2;              // log2(e) / sqrt(q/k head dim)
     uint32_t *err;
 };
 struct DecodeMaps {
-    CUtensorMap k, v;
+    CUtensorMap k, k2, v;          // k2: V1 only (k1 in k)
 };
 // Sizes the decode plan on the current device.  Returns false on bad sizes.
-bool decode_plan(int B, int L, int Hq, int Hkv, int D, int num_sms, int *grid, int *max_seg,
-                 int64_t *units, int *spb, size_t *ws_bytes);
-cudaError_t launch_decode(const DecodeMaps &m, const DecodeParams &p, cudaStream_t s);
+// ws_bytes covers the partial slots and, for per-sequence lengths, the unit
+// prefix (which sits first, cum_bytes long).
+bool decode_plan(int B, int L, int Hkv, int D, int num_sms, bool varlen, int *grid, int64_t *units,
+                 int *spb, size_t *cum_bytes, size_t *ws_bytes);
+cudaError_t launch_decode(const DecodeMaps &m, const DecodeParams &p, bool v1, cudaStream_t s);
 constexpr int kDecodeKeysPerUnit = 64;
 
 // Tensor-map helper (da_api.cu): 4-D bf16 map over (inner, d1, d2, d3) with

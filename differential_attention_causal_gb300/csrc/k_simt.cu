@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const int64_t nrows = static_cast<int64_t>(p.B) * p.Tq * p.H;
     if (row >= nrows) return;
-    if (ld_volatile_u32(p.err) != 0) {   // an earlier kernel gave up: do not compute
+    if ((ld_volatile_u32(p.err) & kErrFatal) != 0) {   // an earlier kernel gave up: do not compute
         if (lane == 0) atomicOr(p.err, kErrAborted);
         return;
     }
@@ -60,7 +60,18 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
 #pragma unroll
     for (int i = 0; i < NV; ++i) { o1[i] = 0.f; o2[i] = 0.f; }
 
-    const int nkeys = t + (p.Lk - p.Tq) + 1;   // keys 0 .. t + (Lk - Tq)
+    // keys 0 .. t + (Lk - Tq), or for decode with per-sequence lengths the
+    // first lens[b] cached rows (clamped into 1 .. Lk)
+    int nkeys = t + (p.Lk - p.Tq) + 1;
+    if (p.lens) {
+        const int n = p.lens[b];
+        if (n < 1 || n > p.Lk) {
+            if (lane == 0) atomicOr(p.err, kErrBadLength);
+            nkeys = n < 1 ? 1 : p.Lk;
+        } else {
+            nkeys = n;
+        }
+    }
     for (int j = 0; j < nkeys; ++j) {
         const float *kj1 = k1 + j * p.k_st;
         const float *kj2 = k2 + j * p.k_st;

@@ -19,6 +19,13 @@ Recipe (shapes follow the workloads named in ``WORKLOADS``):
 V1 q and k are drawn as one interleaved (B, T, 2H, d) tensor each, as the
 nanoGPT issue lays them out; q1 = q[:, :, 0::2], q2 = q[:, :, 1::2] (and the
 same for k) are strided views.  v is (B, T, H, 2d).
+
+Decode inputs: V2 q (B, Hq, D) and caches (B, L, Hkv, D); V1 q1, q2 (B, H, d),
+caches k1, k2 (B, L, H, d) and v (B, L, H, 2d), drawn in that order, each
+contiguous (a cache is written one row per token, so the two branches' keys
+live in separate arrays).  With per-sequence lengths the lengths are drawn
+last, uniform on 1 .. L (torch.randint); cache rows past a sequence's length
+are drawn like the rest, so they hold ordinary values that must not count.
 """
 from __future__ import annotations
 
@@ -53,13 +60,28 @@ class V2Shape:
 
 @dataclass(frozen=True)
 class DecodeShape:
-    """DIFF V2 decode: one new query token per sequence, L cached rows."""
+    """DIFF V2 decode: one new query token per sequence, L cached rows
+    (varlen: sequence b attends its first lens[b] rows)."""
     B: int
     L: int
     Hq: int
     Hkv: int
     D: int
     dtype: str = "bf16"
+    varlen: bool = False
+
+
+@dataclass(frozen=True)
+class V1DecodeShape:
+    """DIFF V1 decode: one new query token per sequence, L cached rows of k1,
+    k2 (head dim d) and v (2d) per diff head."""
+    B: int
+    L: int
+    H: int
+    d: int
+    layer_index: int
+    dtype: str = "bf16"
+    varlen: bool = False
 
 
 # The five workloads, named by what they are.
@@ -69,6 +91,9 @@ WORKLOADS = {
     "v2_bf16_B8_T4096_Hq32_Hkv8_D128": V2Shape(8, 4096, 32, 8, 128, "bf16"),
     "v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128": DecodeShape(64, 32768, 64, 8, 128, "bf16"),
     "v1_bf16_B1_T32768_H12_d128": V1Shape(1, 32768, 12, 128, 27, "bf16"),
+    # decode beyond the five: per-sequence lengths, and DIFF V1 decode
+    "v2_decode_varlen_bf16_B64_L32768_Hq64_Hkv8_D128": DecodeShape(64, 32768, 64, 8, 128, "bf16", True),
+    "v1_decode_bf16_B32_L16384_H12_d128": V1DecodeShape(32, 16384, 12, 128, 27, "bf16"),
 }
 
 
@@ -125,7 +150,34 @@ def make_decode(s: DecodeShape, seed: int = 0, device="cpu") -> dict:
     k = _normal((s.B, s.L, s.Hkv, s.D), 1.0, dt, g, device)
     v = _normal((s.B, s.L, s.Hkv, s.D), 1.0, dt, g, device)
     lam = torch.randn((s.B, s.Hq // 2), generator=g, dtype=torch.float32, device=device)
-    return {"q": q, "k_cache": k, "v_cache": v, "lam": lam}
+    out = {"q": q, "k_cache": k, "v_cache": v, "lam": lam}
+    if s.varlen:
+        out["cache_lens"] = _lens(s.B, s.L, g, device)
+    return out
+
+
+def _lens(B: int, L: int, g, device) -> torch.Tensor:
+    return torch.randint(1, L + 1, (B,), generator=g, dtype=torch.int64, device=device).to(torch.int32)
+
+
+def make_v1_decode(s: V1DecodeShape, seed: int = 0, device="cpu") -> dict:
+    """q1, q2 (B,H,d); k1_cache, k2_cache (B,L,H,d); v_cache (B,L,H,2d);
+    lam_q1, lam_k1, lam_q2, lam_k2 (d,) fp32; cache_lens (B,) int32 if varlen."""
+    g = _gen(seed, device)
+    dt = _DT[s.dtype]
+    q1 = _normal((s.B, s.H, s.d), 1.0, dt, g, device)
+    q2 = _normal((s.B, s.H, s.d), 1.0, dt, g, device)
+    k1 = _normal((s.B, s.L, s.H, s.d), 1.0, dt, g, device)
+    k2 = _normal((s.B, s.L, s.H, s.d), 1.0, dt, g, device)
+    v = _normal((s.B, s.L, s.H, 2 * s.d), 1.0, dt, g, device)
+    lam = [torch.randn(s.d, generator=g, dtype=torch.float32, device=device) * 0.1
+           for _ in range(4)]
+    out = {"q1": q1, "q2": q2, "k1_cache": k1, "k2_cache": k2, "v_cache": v,
+           "lam_q1": lam[0], "lam_k1": lam[1], "lam_q2": lam[2], "lam_k2": lam[3],
+           "layer_index": s.layer_index}
+    if s.varlen:
+        out["cache_lens"] = _lens(s.B, s.L, g, device)
+    return out
 
 
 def make(shape, seed: int = 0, device="cpu") -> dict:
@@ -135,4 +187,6 @@ def make(shape, seed: int = 0, device="cpu") -> dict:
         return make_v2(shape, seed, device)
     if isinstance(shape, DecodeShape):
         return make_decode(shape, seed, device)
+    if isinstance(shape, V1DecodeShape):
+        return make_v1_decode(shape, seed, device)
     raise TypeError(type(shape))

@@ -18,6 +18,11 @@
  *   diffattn_v2_decode  same page, the decoding remark after DiffAttnV2: the V2
  *                       operation for one new query token per sequence against an
  *                       L-row KV cache (the token attends all L rows).
+ *   diffattn_v2_decode_varlen  the same with a cache length per sequence.
+ *   diffattn_v1_decode  DiffAttnV1 for one new query token per sequence against
+ *                       cached k1, k2, v rows (all L, or a length per sequence);
+ *                       the remark names V1 decoding as the case that needs
+ *                       custom kernels, because its v head is 2d wide.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
@@ -63,8 +68,10 @@ typedef enum {
     DA_ERR_CUDA = 7,              /* CUDA runtime / driver error                        */
     DA_ERR_BAD_DTYPE = 8,
     DA_ERR_DEVICE_TIMEOUT = 9,    /* reported by diffattn_device_error()               */
-    DA_ERR_SCRATCH_LIMIT = 10     /* the call needs more scratch than the library's     */
+    DA_ERR_SCRATCH_LIMIT = 10,    /* the call needs more scratch than the library's     */
                                   /* static buffer holds (diffattn_v2_decode_noalloc)  */
+    DA_ERR_BAD_LENGTH = 11        /* reported by diffattn_device_error(): a decode     */
+                                  /* cache length was outside 1..L (it was clamped)    */
 } da_status;
 
 typedef enum { DA_F32 = 0, DA_BF16 = 1 } da_dtype;
@@ -153,13 +160,56 @@ da_status diffattn_v2_decode_noalloc(const void *q, const void *k_cache, const v
                                      const float *lam, void *out, int B, int L, int Hq, int Hkv,
                                      int D, da_dtype dtype, cudaStream_t stream);
 
+/* DIFF V2 decode with a cache length per sequence: sequence b's new token
+ * attends cache rows 0 .. cache_lens[b]-1 (its own K/V already written at row
+ * cache_lens[b]-1); rows at and past that length are never used, whatever they
+ * hold.  The split-KV work is rebalanced over the SMs by the actual lengths.
+ *   cache_lens : DEVICE int32 array of B lengths, each in 1..L (L = rows
+ *                allocated per sequence, the cache's row stride).  A length
+ *                outside that range is clamped into it and recorded in the
+ *                device error word (diffattn_device_error -> DA_ERR_BAD_LENGTH).
+ *   workspace  : as diffattn_v2_decode (the same size function covers both).
+ *   Every other argument, layout and limit as diffattn_v2_decode.  dtype
+ *   DA_F32 runs the fp32 kernel, which takes no workspace.
+ */
+da_status diffattn_v2_decode_varlen(const void *q, const void *k_cache, const void *v_cache,
+                                    const float *lam, const int32_t *cache_lens, void *out,
+                                    void *workspace, size_t workspace_bytes, int B, int L, int Hq,
+                                    int Hkv, int D, da_dtype dtype, cudaStream_t stream);
+
+/* Bytes of device scratch that diffattn_v1_decode needs (either length mode)
+ * on the current device.  Returns 0 for invalid sizes or dtype DA_F32. */
+size_t diffattn_v1_decode_workspace_size(int B, int L, int H, int d, da_dtype dtype);
+
+/* DIFF V1 decode: the DiffAttnV1 operation for one new query token per
+ * sequence against a KV cache.
+ *   q1, q2          : (B, H, d) contiguous
+ *   k1_cache, k2_cache : (B, L, H, d) contiguous
+ *   v_cache         : (B, L, H, 2d) contiguous
+ *   lam_q1 .. lam_k2 : (d) fp32 lambda vectors; layer_index gives lam_init
+ *   cache_lens      : NULL (every sequence attends all L rows) or a DEVICE
+ *                     int32 array of B lengths in 1..L, as in
+ *                     diffattn_v2_decode_varlen
+ *   out             : (B, H, 2d) = (B, C), dtype as inputs
+ *   workspace       : DA_BF16 only; at least diffattn_v1_decode_workspace_size()
+ *                     bytes, 256-byte aligned, as in diffattn_v2_decode
+ *   Supported: d in {64, 128} for DA_BF16; d in {32, 64, 128} for DA_F32.
+ */
+da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cache,
+                             const void *k2_cache, const void *v_cache, const float *lam_q1,
+                             const float *lam_k1, const float *lam_q2, const float *lam_k2,
+                             const int32_t *cache_lens, void *out, void *workspace,
+                             size_t workspace_bytes, int B, int L, int H, int d, int layer_index,
+                             da_dtype dtype, cudaStream_t stream);
+
 /* Static string for a status code (never NULL). */
 const char *diffattn_status_string(da_status s);
 
 /* Synchronises the current device, reads and clears the device error word that
  * the kernels set when a bounded wait gives up.  *code receives the raw word
  * (0 = no error).  Returns DA_OK if the word was 0, DA_ERR_DEVICE_TIMEOUT if a
- * kernel recorded a give-up, DA_ERR_CUDA if the read itself failed. */
+ * kernel recorded a give-up, DA_ERR_BAD_LENGTH if the only record is a decode
+ * cache length outside 1..L, DA_ERR_CUDA if the read itself failed. */
 da_status diffattn_device_error(uint32_t *code);
 
 /* Number of kernel launches the last successful call on this host thread

@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("diffattn_v1_fwd", "diffattn_v2_fwd", "diffattn_v2_decode",
-              "diffattn_v2_decode_workspace_size", "diffattn_status_string", "diffattn_device_error"):
+              "diffattn_v2_decode_workspace_size", "diffattn_status_string", "diffattn_device_error",
+              "diffattn_v2_decode_varlen", "diffattn_v1_decode", "diffattn_v1_decode_workspace_size"):
         assert n in names
 
 
@@ -45,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     from differential_attention_causal_gb300 import binding
-    for code in range(10):
+    for code in range(12):
         s = binding.status_string(code)
         assert isinstance(s, str) and s
     assert binding.status_string(0) == "ok"
@@ -129,3 +130,39 @@ def test_oracle_is_not_imported_by_the_product():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
                 assert "diffattn_oracle" not in text, f
+
+
+def _v1dec(lib, **kw):
+    a = dict(q1=A, q2=A, k1=A, k2=A, v=A, lq1=A, lk1=A, lq2=A, lk2=A, lens=None, out=A, ws=A, wsb=1 << 20,
+             B=2, L=100, H=2, d=64, layer=0, dtype=1)
+    a.update(kw)
+    return lib.diffattn_v1_decode(a["q1"], a["q2"], a["k1"], a["k2"], a["v"], a["lq1"], a["lk1"], a["lq2"],
+                                  a["lk2"], a["lens"], a["out"], a["ws"], a["wsb"], a["B"], a["L"], a["H"],
+                                  a["d"], a["layer"], a["dtype"], None)
+
+
+def test_v1_decode_argument_checks(lib):
+    assert _v1dec(lib, k2=None) == 1
+    assert _v1dec(lib, lk1=None) == 1
+    assert _v1dec(lib, L=0) == 2
+    assert _v1dec(lib, layer=-3) == 2
+    assert _v1dec(lib, d=32) == 3          # bf16 decode needs d in {64, 128}
+    assert _v1dec(lib, d=96, dtype=0) == 3
+    assert _v1dec(lib, q2=A + 8) == 5
+    assert _v1dec(lib, lens=A + 2) == 5    # int32 lengths need 4-byte alignment
+    assert _v1dec(lib, dtype=5) == 8
+
+
+def test_v2_decode_varlen_argument_checks(lib):
+    def call(**kw):
+        a = dict(q=A, k=A, v=A, lam=A, lens=A, out=A, ws=A, wsb=1 << 20, B=2, L=100, Hq=8, Hkv=2, D=128, dtype=1)
+        a.update(kw)
+        return lib.diffattn_v2_decode_varlen(a["q"], a["k"], a["v"], a["lam"], a["lens"], a["out"], a["ws"],
+                                             a["wsb"], a["B"], a["L"], a["Hq"], a["Hkv"], a["D"], a["dtype"], None)
+    assert call(lens=None) == 1
+    assert call(lens=A + 1) == 5
+    assert call(B=0) == 2
+    assert call(Hq=6, Hkv=2) == 4          # odd group
+    assert call(D=96) == 3
+    assert call(k=A + 4) == 5
+    assert call(dtype=9) == 8

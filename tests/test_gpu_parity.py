@@ -235,9 +235,15 @@ def test_decode_workspace_checks():
     xd = to_dev(inputs.make_decode(s, seed=0))
     need = bd.decode_workspace_size(2, 100, 8, 2, 128)
     assert need > 0
+    # the size covers per-sequence lengths (the larger need): 16 bytes less fails that call
     small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    lens = torch.tensor([100, 3], dtype=torch.int32, device="cuda")
     with pytest.raises(bd.DiffAttnError) as e:
-        bd.v2_decode(xd["q"], xd["k_cache"], xd["v_cache"], xd["lam"], workspace=small)
+        bd.v2_decode_varlen(xd["q"], xd["k_cache"], xd["v_cache"], xd["lam"], lens, workspace=small)
+    assert e.value.code == 6
+    with pytest.raises(bd.DiffAttnError) as e:
+        bd.v2_decode(xd["q"], xd["k_cache"], xd["v_cache"], xd["lam"],
+                     workspace=torch.empty(64, dtype=torch.uint8, device="cuda"))
     assert e.value.code == 6
 
 

@@ -67,7 +67,7 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls(lib):
 
 def test_noalloc_refuses_sizes_beyond_its_scratch(lib):
     from differential_attention_causal_gb300 import binding
-    # many short sequences: one partial slot per (CTA, kv-head segment) overflows 8 MiB
+    # many short sequences: one partial slot per (b, kv head), plus one per CTA, overflows 8 MiB
     s = inputs.DecodeShape(300, 64, 16, 8, 128, "bf16")
     assert binding.decode_workspace_size(s.B, s.L, s.Hq, s.Hkv, s.D) > SCRATCH_LIMIT
     x = inputs.make_decode(s, seed=7, device="cuda")
