@@ -68,7 +68,7 @@ da_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DA_OK : DA_ERR_
 }  // namespace
 
 bool encode_map_4d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t d1, uint64_t d2, uint64_t d3,
-                   int64_t s1, int64_t s2, int64_t s3, uint32_t box_rows) {
+                   int64_t s1, int64_t s2, int64_t s3, uint32_t box_rows, int l2_promo_bytes) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {inner, d1, d2, d3};
@@ -79,7 +79,9 @@ bool encode_map_4d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t d1
     std::memset(m, 0, sizeof(*m));
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          l2_promo_bytes == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -332,10 +334,13 @@ da_status v2_decode_impl(const void *q, const void *k_cache, const void *v_cache
     if (G > 8) return DA_ERR_BAD_GROUP;
     DecodeMaps m;
     const int64_t st_row = static_cast<int64_t>(Hkv) * D;
+    // a decode unit reads D * 2 bytes of each cache row and the neighbouring
+    // bytes belong to another head: promote L2 fills no wider than a row
+    const int promo = D * 2 <= 128 ? 128 : 256;
     if (!encode_map_4d(&m.k, k_cache, D, Hkv, static_cast<uint64_t>(L), B, D, st_row, st_row * L,
-                       kDecodeKeysPerUnit) ||
+                       kDecodeKeysPerUnit, promo) ||
         !encode_map_4d(&m.v, v_cache, D, Hkv, static_cast<uint64_t>(L), B, D, st_row, st_row * L,
-                       kDecodeKeysPerUnit))
+                       kDecodeKeysPerUnit, promo))
         return DA_ERR_CUDA;
     m.k2 = m.k;
     DecodeParams p{};
@@ -410,8 +415,11 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
     }
     DecodeMaps m;
     const int64_t kr = static_cast<int64_t>(H) * d, vr = static_cast<int64_t>(H) * dv;
-    if (!encode_map_4d(&m.k, k1_cache, d, H, static_cast<uint64_t>(L), B, d, kr, kr * L, kDecodeKeysPerUnit) ||
-        !encode_map_4d(&m.k2, k2_cache, d, H, static_cast<uint64_t>(L), B, d, kr, kr * L, kDecodeKeysPerUnit) ||
+    const int kpromo = d * 2 <= 128 ? 128 : 256;   // as for the V2 cache maps
+    if (!encode_map_4d(&m.k, k1_cache, d, H, static_cast<uint64_t>(L), B, d, kr, kr * L, kDecodeKeysPerUnit,
+                       kpromo) ||
+        !encode_map_4d(&m.k2, k2_cache, d, H, static_cast<uint64_t>(L), B, d, kr, kr * L, kDecodeKeysPerUnit,
+                       kpromo) ||
         !encode_map_4d(&m.v, v_cache, dv, H, static_cast<uint64_t>(L), B, dv, vr, vr * L, kDecodeKeysPerUnit))
         return DA_ERR_CUDA;
     DecodeParams p{};

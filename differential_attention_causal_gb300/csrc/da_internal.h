@@ -102,7 +102,11 @@ constexpr int kDecodeKeysPerUnit = 64;
 
 // Tensor-map helper (da_api.cu): 4-D bf16 map over (inner, d1, d2, d3) with
 // element strides s1, s2, s3, box (64, 1, box_rows, 1), 128-byte swizzle.
+// l2_promo_bytes (128 or 256) is the L2 fetch granularity: a map whose rows
+// are 128 bytes apart from the next row it reads should not promote to 256,
+// or every row pulls in 128 bytes it does not use.
 bool encode_map_4d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t d1, uint64_t d2,
-                   uint64_t d3, int64_t s1, int64_t s2, int64_t s3, uint32_t box_rows);
+                   uint64_t d3, int64_t s1, int64_t s2, int64_t s3, uint32_t box_rows,
+                   int l2_promo_bytes = 256);
 
 }  // namespace da

@@ -41,7 +41,7 @@ namespace {
 template <int D>
 struct DecCfg {
     static constexpr int KEYS = kDecodeKeysPerUnit;   // keys per unit / stage
-    static constexpr int STAGES = D >= 256 ? 3 : 4;
+    static constexpr int STAGES = D >= 256 ? 3 : 4;    // D = 256: capped by shared memory
     static constexpr int NBOX = D / 64;                // 64-element boxes per row
     static constexpr int NBOX_LOG2 = NBOX == 1 ? 0 : (NBOX == 2 ? 1 : 2);
     static constexpr int BOX_BYTES = KEYS * 128;       // one 64 x 64 bf16 box
