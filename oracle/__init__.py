@@ -70,6 +70,12 @@ def _load():
             lib.oracle_v2_decode.restype = ctypes.c_int
             lib.oracle_v2_decode.argtypes = ([dp] * 4 + [ctypes.c_int, ctypes.c_int64] + [ctypes.c_int] * 3
                                              + [i64p, i64p, ctypes.c_int64, dp, ctypes.c_int])
+            lib.oracle_v1_bwd.restype = ctypes.c_int
+            lib.oracle_v1_bwd.argtypes = ([dp] * 10 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64] + [dp] * 6
+                                          + [ctypes.c_int])
+            lib.oracle_v2_bwd.restype = ctypes.c_int
+            lib.oracle_v2_bwd.argtypes = ([dp] * 5 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64] + [dp] * 4
+                                          + [ctypes.c_int])
             lib.oracle_v1_decode.restype = ctypes.c_int
             lib.oracle_v1_decode.argtypes = ([dp] * 9 + [ctypes.c_int, ctypes.c_int64] + [ctypes.c_int] * 3
                                              + [i64p, i64p, ctypes.c_int64, dp, ctypes.c_int])
@@ -225,6 +231,58 @@ def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, lq1, lk1, lq2, lk2, layer_ind
     if rc:
         raise RuntimeError(f"oracle_v1_decode failed ({rc})")
     return out if r is not None else out.reshape(B, H, 2 * d)
+
+
+def v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, layer_index: int, dout, heads=None,
+           nthreads: int | None = None) -> dict:
+    """Gradients of the DIFF V1 forward for upstream gradient dout (B, T, H, 2d).
+
+    Returns dq1, dq2, dk1, dk2 (B, T, H, d), dv (B, T, H, 2d) and dlam_q1,
+    dlam_k1, dlam_q2, dlam_k2 (d,).  heads: optional ids b*H + h; then only
+    those heads' gradients are filled (the rest stay 0) and the lambda-vector
+    gradients hold only those heads' share.
+    """
+    q1, q2, k1, k2, v, dout = (_f64(x) for x in (q1, q2, k1, k2, v, dout))
+    lq1, lk1, lq2, lk2 = (_f64(x) for x in (lq1, lk1, lq2, lk2))
+    B, T, H, d = q1.shape
+    assert q2.shape == k1.shape == k2.shape == (B, T, H, d)
+    assert v.shape == dout.shape == (B, T, H, 2 * d)
+    hs = None if heads is None else np.ascontiguousarray(np.asarray(heads, dtype=np.int64).reshape(-1))
+    hp = None if hs is None else hs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    g = {n: np.zeros(sh, dtype=np.float64) for n, sh in
+         (("dq1", q1.shape), ("dq2", q1.shape), ("dk1", q1.shape), ("dk2", q1.shape), ("dv", v.shape))}
+    dl = np.zeros(4 * d, dtype=np.float64)
+    rc = _load().oracle_v1_bwd(_ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v), _ptr(lq1), _ptr(lk1), _ptr(lq2),
+                               _ptr(lk2), _ptr(dout), B, T, H, d, int(layer_index), hp,
+                               0 if hs is None else hs.size, _ptr(g["dq1"]), _ptr(g["dq2"]), _ptr(g["dk1"]),
+                               _ptr(g["dk2"]), _ptr(g["dv"]), _ptr(dl), nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_v1_bwd failed ({rc})")
+    g.update(dlam_q1=dl[:d], dlam_k1=dl[d:2 * d], dlam_q2=dl[2 * d:3 * d], dlam_k2=dl[3 * d:])
+    return g
+
+
+def v2_bwd(q, k, v, lam, dout, groups=None, nthreads: int | None = None) -> dict:
+    """Gradients of the DIFF V2 prefill for upstream gradient dout (B, T, Hq/2, D).
+
+    Returns dq (B, T, Hq, D), dk, dv (B, T, Hkv, D), dlam (B, T, Hq/2).
+    groups: optional kv-group ids b*Hkv + g; then only those groups' heads,
+    kv rows and pairs are filled.
+    """
+    q, k, v, lam, dout = (_f64(x) for x in (q, k, v, lam, dout))
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == v.shape == (B, T, Hkv, D) and lam.shape == (B, T, Hq // 2)
+    assert dout.shape == (B, T, Hq // 2, D)
+    gs = None if groups is None else np.ascontiguousarray(np.asarray(groups, dtype=np.int64).reshape(-1))
+    gp = None if gs is None else gs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    g = {"dq": np.zeros(q.shape), "dk": np.zeros(k.shape), "dv": np.zeros(v.shape), "dlam": np.zeros(lam.shape)}
+    rc = _load().oracle_v2_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(lam), _ptr(dout), B, T, Hq, Hkv, D, gp,
+                               0 if gs is None else gs.size, _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                               _ptr(g["dlam"]), nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_v2_bwd failed ({rc})")
+    return g
 
 
 def decode_gather(q, k_cache, v_cache, lam, rows):

@@ -11,6 +11,9 @@
  * softmax, form the weighted sum of value rows, then apply the
  * differential combine.  No online softmax, no tiling, no fusion.
  * Rows are independent by definition; threads only split the list of rows.
+ * The gradients (end of file) follow the chain rule of the same definitions
+ * row by row; threads split the list of heads (V1) or kv groups (V2), whose
+ * gradients do not overlap.
  *
  * Sources (page titles as printed on the pages):
  *   "Differential Transformer V2", pseudo-code DiffAttnV1 / DiffAttnV2:
@@ -372,4 +375,302 @@ int oracle_v1_decode(const double *q1, const double *q2, const double *k1,
     J.nrows = rows ? nrows : (int64_t)B * H;
     J.out = out;
     return run_jobs(&J, nthreads);
+}
+
+/* ======================================================================
+ * Gradients (the backward of the same definitions).
+ *
+ * Written from the chain rule of the forward definitions above, with the
+ * softmax Jacobian taken as is (no flash-style shortcut):
+ *   one attention row a = sum_j p_j v_j, p = softmax(scale q.k_j), with
+ *   upstream gradient g = dL/da:
+ *     dL/dv_j += p_j g
+ *     dp_j     = g . v_j
+ *     ds_j     = p_j (dp_j - sum_l p_l dp_l)
+ *     dL/dq   += scale sum_j ds_j k_j
+ *     dL/dk_j += scale ds_j q
+ *   RMSNorm y_c = x_c r, r = (mean(x^2) + eps)^(-1/2):
+ *     dL/dx_c = r dy_c - r^3 x_c (sum_e dy_e x_e) / n
+ *   DiffAttnV1: out = (1 - lam_init) y, x = a1 - lam a2:
+ *     g1 = dL/dx, g2 = -lam dL/dx, dL/dlam = -sum (dL/dx . a2) over all rows;
+ *     lam = exp(lq1.lk1) - exp(lq2.lk2) + lam_init:
+ *     dlq1 = dlam exp(lq1.lk1) lk1, dlk1 = dlam exp(lq1.lk1) lq1,
+ *     dlq2 = -dlam exp(lq2.lk2) lk2, dlk2 = -dlam exp(lq2.lk2) lq2.
+ *   DiffAttnV2: out = a_e - sigmoid(l) a_o:
+ *     g_e = dout, g_o = -sigmoid(l) dout,
+ *     dL/dl = -sigmoid(l) (1 - sigmoid(l)) (dout . a_o).
+ * ==================================================================== */
+
+/* Backward of one attention row over keys 0..n-1.  g: upstream gradient
+ * [dv]; accumulates into dq [dqk], dk rows (stride k_stride) and dv rows
+ * (stride v_stride).  p, dp: scratch of n doubles each. */
+static void attend_row_bwd(const double *q, const double *k, int64_t k_stride,
+                           const double *v, int64_t v_stride, int64_t n,
+                           int dqk, int dvd, double scale, const double *g,
+                           double *p, double *dp, double *dq, double *dk,
+                           double *dv)
+{
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        const double *kj = k + j * k_stride;
+        double s = 0.0;
+        for (int c = 0; c < dqk; ++c)
+            s += q[c] * kj[c];
+        p[j] = s * scale;
+        if (p[j] > mx)
+            mx = p[j];
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        p[j] = exp(p[j] - mx);
+        sum += p[j];
+    }
+    double pdp = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        p[j] /= sum;
+        const double *vj = v + j * v_stride;
+        double t = 0.0;
+        for (int c = 0; c < dvd; ++c)
+            t += g[c] * vj[c];
+        dp[j] = t;
+        pdp += p[j] * t;
+    }
+    for (int64_t j = 0; j < n; ++j) {
+        const double ds = p[j] * (dp[j] - pdp);
+        const double *kj = k + j * k_stride;
+        double *dkj = dk + j * k_stride;
+        double *dvj = dv + j * v_stride;
+        for (int c = 0; c < dqk; ++c) {
+            dq[c] += scale * ds * kj[c];
+            dkj[c] += scale * ds * q[c];
+        }
+        for (int c = 0; c < dvd; ++c)
+            dvj[c] += p[j] * g[c];
+    }
+}
+
+typedef struct {
+    int kind;                 /* 1 = V1, 2 = V2 */
+    const double *q1, *q2, *k1, *k2, *v, *lam, *dout;
+    double lam_full, lam_init;
+    int B, T, H, dqk, dv, Hkv, G;
+    const int64_t *units;     /* V1: head ids b*H+h; V2: group ids b*Hkv+g */
+    int64_t nunits;
+    double *dq1, *dq2, *dk1, *dk2, *dvv, *dlam;   /* dlam: V1 one partial per unit, V2 (B,T,Hq/2) */
+    int tid, nthreads;
+} bjob_t;
+
+/* V1 head (b, h): every row t, both branches. */
+static void v1_head_bwd(const bjob_t *J, int64_t u, int64_t slot, double *p,
+                        double *dp, double *buf)
+{
+    const int H = J->H, T = J->T, d = J->dqk, dvd = J->dv;
+    const int h = (int)(u % H);
+    const int b = (int)(u / H);
+    const int64_t qk_row = (int64_t)H * d, v_row = (int64_t)H * dvd;
+    const double scale = 1.0 / sqrt((double)d);
+    double *a1 = buf, *a2 = buf + dvd, *x = buf + 2 * dvd, *dx = buf + 3 * dvd;
+    double *g2 = buf + 4 * dvd;
+    const int64_t kbase = (int64_t)b * T * H + h;
+    double dlam = 0.0;
+    for (int t = 0; t < T; ++t) {
+        const int64_t row = ((int64_t)b * T + t) * H + h;
+        const double *q1 = J->q1 + row * d, *q2 = J->q2 + row * d;
+        attend_row(q1, J->k1 + kbase * d, qk_row, J->v + kbase * dvd, v_row, (int64_t)t + 1, d, dvd, scale, p, a1);
+        attend_row(q2, J->k2 + kbase * d, qk_row, J->v + kbase * dvd, v_row, (int64_t)t + 1, d, dvd, scale, p, a2);
+        double ms = 0.0, xdy = 0.0;
+        const double *dout = J->dout + row * dvd;
+        for (int c = 0; c < dvd; ++c) {
+            x[c] = a1[c] - J->lam_full * a2[c];
+            ms += x[c] * x[c];
+            xdy += x[c] * (1.0 - J->lam_init) * dout[c];
+        }
+        ms /= (double)dvd;
+        const double r = 1.0 / sqrt(ms + 1e-5);
+        double xa2 = 0.0;
+        for (int c = 0; c < dvd; ++c) {
+            const double dy = (1.0 - J->lam_init) * dout[c];
+            dx[c] = r * dy - r * r * r * x[c] * xdy / (double)dvd;
+            g2[c] = -J->lam_full * dx[c];
+            xa2 += dx[c] * a2[c];
+        }
+        dlam -= xa2;
+        attend_row_bwd(q1, J->k1 + kbase * d, qk_row, J->v + kbase * dvd, v_row, (int64_t)t + 1, d, dvd, scale,
+                       dx, p, dp, J->dq1 + row * d, J->dk1 + kbase * d, J->dvv + kbase * dvd);
+        attend_row_bwd(q2, J->k2 + kbase * d, qk_row, J->v + kbase * dvd, v_row, (int64_t)t + 1, d, dvd, scale,
+                       g2, p, dp, J->dq2 + row * d, J->dk2 + kbase * d, J->dvv + kbase * dvd);
+    }
+    J->dlam[slot] = dlam;
+}
+
+/* V2 kv group (b, g): the pairs whose heads read kv head g, every row t. */
+static void v2_group_bwd(const bjob_t *J, int64_t u, double *p, double *dp,
+                         double *buf)
+{
+    const int Hkv = J->Hkv, T = J->T, D = J->dqk, G = J->G;
+    const int P = J->H, Hq = 2 * P;
+    const int g = (int)(u % Hkv);
+    const int b = (int)(u / Hkv);
+    const int64_t q_row = (int64_t)Hq * D, kv_row = (int64_t)Hkv * D;
+    const double scale = 1.0 / sqrt((double)D);
+    double *ae = buf, *ao = buf + D, *go = buf + 2 * D;
+    const double *k = J->k1 + ((int64_t)b * T * Hkv + g) * D;
+    const double *v = J->v + ((int64_t)b * T * Hkv + g) * D;
+    double *dk = J->dk1 + ((int64_t)b * T * Hkv + g) * D;
+    double *dv = J->dvv + ((int64_t)b * T * Hkv + g) * D;
+    for (int i = g * G / 2; i < (g + 1) * G / 2; ++i) {
+        const int he = 2 * i, ho = 2 * i + 1;
+        for (int t = 0; t < T; ++t) {
+            const int64_t tok = (int64_t)b * T + t;
+            const double *qe = J->q1 + (tok * Hq + he) * D;
+            const double *qo = J->q1 + (tok * Hq + ho) * D;
+            const double *dout = J->dout + (tok * P + i) * D;
+            attend_row(qe, k, kv_row, v, kv_row, (int64_t)t + 1, D, D, scale, p, ae);
+            attend_row(qo, k, kv_row, v, kv_row, (int64_t)t + 1, D, D, scale, p, ao);
+            const double sg = 1.0 / (1.0 + exp(-J->lam[tok * P + i]));
+            double da = 0.0;
+            for (int c = 0; c < D; ++c) {
+                go[c] = -sg * dout[c];
+                da += dout[c] * ao[c];
+            }
+            J->dlam[tok * P + i] = -sg * (1.0 - sg) * da;
+            attend_row_bwd(qe, k, kv_row, v, kv_row, (int64_t)t + 1, D, D, scale, dout, p, dp,
+                           J->dq1 + (tok * Hq + he) * D, dk, dv);
+            attend_row_bwd(qo, k, kv_row, v, kv_row, (int64_t)t + 1, D, D, scale, go, p, dp,
+                           J->dq1 + (tok * Hq + ho) * D, dk, dv);
+        }
+    }
+    (void)q_row;
+}
+
+static void *bwd_worker(void *arg)
+{
+    const bjob_t *J = (const bjob_t *)arg;
+    double *p = (double *)malloc(sizeof(double) * (size_t)J->T * 2);
+    double *buf = (double *)malloc(sizeof(double) * (size_t)J->dv * 6);
+    if (!p || !buf) {
+        free(p);
+        free(buf);
+        return (void *)1;
+    }
+    for (int64_t n = J->tid; n < J->nunits; n += J->nthreads) {
+        if (J->kind == 1)
+            v1_head_bwd(J, J->units[n], n, p, p + J->T, buf);
+        else
+            v2_group_bwd(J, J->units[n], p, p + J->T, buf);
+    }
+    free(p);
+    free(buf);
+    return NULL;
+}
+
+static int run_bwd_jobs(const bjob_t *proto, int nthreads)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    bjob_t jobs[256];
+    pthread_t th[256];
+    int started[256];
+    int rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = *proto;
+        jobs[i].tid = i;
+        jobs[i].nthreads = nthreads;
+        started[i] = pthread_create(&th[i], NULL, bwd_worker, &jobs[i]) == 0;
+        if (!started[i])
+            rc = 2;
+    }
+    for (int i = 0; i < nthreads; ++i) {
+        if (started[i]) {
+            void *ret = NULL;
+            pthread_join(th[i], &ret);
+            if (ret)
+                rc = 1;
+        }
+    }
+    return rc;
+}
+
+/* DIFF V1 backward.  Inputs as oracle_v1_fwd (contiguous), dout (B,T,H,2d).
+ * heads: ids b*H+h to differentiate (NULL = all); gradients are written for
+ * those heads only (dq1, dq2, dk1, dk2 (B,T,H,d), dv (B,T,H,2d), zeroed by
+ * the caller).  dlam_vec: 4*d doubles (dlq1, dlk1, dlq2, dlk2) from the
+ * listed heads' contribution to dL/dlam.  Returns 0 on success. */
+int oracle_v1_bwd(const double *q1, const double *q2, const double *k1,
+                  const double *k2, const double *v, const double *lq1,
+                  const double *lk1, const double *lq2, const double *lk2,
+                  const double *dout, int B, int T, int H, int d,
+                  int layer_index, const int64_t *heads, int64_t nheads,
+                  double *dq1, double *dq2, double *dk1, double *dk2,
+                  double *dv, double *dlam_vec, int nthreads)
+{
+    bjob_t J;
+    memset(&J, 0, sizeof(J));
+    J.kind = 1;
+    J.q1 = q1; J.q2 = q2; J.k1 = k1; J.k2 = k2; J.v = v; J.dout = dout;
+    J.B = B; J.T = T; J.H = H; J.dqk = d; J.dv = 2 * d;
+    J.lam_init = oracle_lambda_init(layer_index);
+    J.lam_full = oracle_lambda_full(lq1, lk1, lq2, lk2, d, J.lam_init);
+    J.dq1 = dq1; J.dq2 = dq2; J.dk1 = dk1; J.dk2 = dk2; J.dvv = dv;
+    const int64_t n = heads ? nheads : (int64_t)B * H;
+    int64_t *ids = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    double *part = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    if (!ids || !part) {
+        free(ids);
+        free(part);
+        return 3;
+    }
+    for (int64_t i = 0; i < n; ++i)
+        ids[i] = heads ? heads[i] : i;
+    J.units = ids; J.nunits = n; J.dlam = part;
+    const int rc = run_bwd_jobs(&J, nthreads);
+    double dlam = 0.0;
+    for (int64_t i = 0; i < n; ++i)
+        dlam += part[i];
+    double s1 = 0.0, s2 = 0.0;
+    for (int c = 0; c < d; ++c) {
+        s1 += lq1[c] * lk1[c];
+        s2 += lq2[c] * lk2[c];
+    }
+    for (int c = 0; c < d; ++c) {
+        dlam_vec[c] = dlam * exp(s1) * lk1[c];
+        dlam_vec[d + c] = dlam * exp(s1) * lq1[c];
+        dlam_vec[2 * d + c] = -dlam * exp(s2) * lk2[c];
+        dlam_vec[3 * d + c] = -dlam * exp(s2) * lq2[c];
+    }
+    free(ids);
+    free(part);
+    return rc;
+}
+
+/* DIFF V2 backward.  Inputs as oracle_v2_fwd (contiguous), dout (B,T,Hq/2,D).
+ * groups: ids b*Hkv+g (NULL = all); gradients for those kv groups only: dq
+ * (B,T,Hq,D) rows of the group's heads, dk, dv (B,T,Hkv,D), dlam (B,T,Hq/2)
+ * entries of the group's pairs; all zeroed by the caller. */
+int oracle_v2_bwd(const double *q, const double *k, const double *v,
+                  const double *lam, const double *dout, int B, int T, int Hq,
+                  int Hkv, int D, const int64_t *groups, int64_t ngroups,
+                  double *dq, double *dk, double *dv, double *dlam,
+                  int nthreads)
+{
+    if (Hq % Hkv != 0 || ((Hq / Hkv) & 1))
+        return 4;
+    bjob_t J;
+    memset(&J, 0, sizeof(J));
+    J.kind = 2;
+    J.q1 = q; J.k1 = k; J.v = v; J.lam = lam; J.dout = dout;
+    J.B = B; J.T = T; J.H = Hq / 2; J.dqk = D; J.dv = D; J.Hkv = Hkv; J.G = Hq / Hkv;
+    J.dq1 = dq; J.dk1 = dk; J.dvv = dv; J.dlam = dlam;
+    const int64_t n = groups ? ngroups : (int64_t)B * Hkv;
+    int64_t *ids = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    if (!ids)
+        return 3;
+    for (int64_t i = 0; i < n; ++i)
+        ids[i] = groups ? groups[i] : i;
+    J.units = ids; J.nunits = n;
+    const int rc = run_bwd_jobs(&J, nthreads);
+    free(ids);
+    return rc;
 }

@@ -11,6 +11,7 @@ import os
 
 import pytest
 
+import test_oracle_bwd_pins as bwd_pins
 import test_oracle_pins as pins
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -41,13 +42,24 @@ MUTANTS = {
     "V2 decode cache stride from the length": ("const double *k = J->k1 + ((int64_t)b * Lc * Hkv + g) * D;",
                                                "const double *k = J->k1 + ((int64_t)b * L * Hkv + g) * D;"),
     "V1 decode branch 2 reads k1": ("attend_row(q2, k2, (int64_t)H * d,", "attend_row(q2, k1, (int64_t)H * d,"),
+    "bwd: RMSNorm Jacobian without its r^3 term": (
+        "dx[c] = r * dy - r * r * r * x[c] * xdy / (double)dvd;", "dx[c] = r * dy;"),
+    "bwd: dlam sign": ("dlam -= xa2;", "dlam += xa2;"),
+    "bwd: dq without the score scale": ("dq[c] += scale * ds * kj[c];", "dq[c] += ds * kj[c];"),
+    "bwd: softmax Jacobian without its mean term": ("const double ds = p[j] * (dp[j] - pdp);",
+                                                    "const double ds = p[j] * dp[j];"),
+    "bwd: V2 odd-head gradient sign": ("go[c] = -sg * dout[c];", "go[c] = sg * dout[c];"),
+    "bwd: V2 dlam without (1 - sigmoid)": ("J->dlam[tok * P + i] = -sg * (1.0 - sg) * da;",
+                                           "J->dlam[tok * P + i] = -sg * da;"),
+    "bwd: V1 branch-2 gradient not scaled by lam": ("g2[c] = -J->lam_full * dx[c];", "g2[c] = -dx[c];"),
+    "bwd: dk from the key instead of the query": ("dkj[c] += scale * ds * q[c];", "dkj[c] += scale * ds * kj[c];"),
     "decode drops the last cache row": ("attend_row(qe, k, kv_row, v, kv_row, L, D, D, scale, scores, a1);",
                                         "attend_row(qe, k, kv_row, v, kv_row, L - 1, D, D, scale, scores, a1);"),
 }
 
 # mutants whose text stands at more than one site (every site is mutated:
-# the same mistake made in the prefill and the decode of one variant)
-SITES = {"scale 1/sqrt(2d) in V1": 2}
+# the same mistake made in the prefill, decode and backward of one variant)
+SITES = {"scale 1/sqrt(2d) in V1": 3, "V1 combine sign": 2}
 
 # pin checks that take only the oracle (parametrised ones get one case each)
 CHECKS = [
@@ -65,6 +77,11 @@ CHECKS = [
     pins.test_v1_decode_matches_library_and_last_prefill_row,
     pins.test_decode_lengths_read_only_each_sequence_rows,
     pins.test_causality_future_rows_do_not_matter,
+    lambda o: bwd_pins.test_v1_bwd_matches_autograd_of_library_forward(o, 1, 17, 2, 16, 0),
+    lambda o: bwd_pins.test_v2_bwd_matches_autograd_of_library_forward(o, 2, 19, 8, 2, 8),
+    bwd_pins.test_v1_bwd_finite_differences_of_the_forward,
+    bwd_pins.test_v2_bwd_finite_differences_of_the_forward,
+    bwd_pins.test_bwd_closed_forms,
 ]
 
 
