@@ -61,6 +61,22 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v1_decode.restype = i32
             L.diffattn_v1_decode.argtypes = ([vp] * 5 + [fp] * 4 + [vp, vp, vp, ctypes.c_size_t] + [i32] * 5
                                              + [i32, vp])
+            sz = ctypes.c_size_t
+            for n, k in (("diffattn_v1_train_saved_size", 4), ("diffattn_v1_bwd_workspace_size", 4),
+                         ("diffattn_v2_train_saved_size", 5), ("diffattn_v2_bwd_workspace_size", 5)):
+                getattr(L, n).restype = sz
+                getattr(L, n).argtypes = [i32] * k
+            L.diffattn_v1_fwd_train.restype = i32
+            L.diffattn_v1_fwd_train.argtypes = ([vp] * 5 + [fp] * 4 + [vp, vp, sz] + [i32] * 5 + [i64] * 12
+                                                + [i32, vp])
+            L.diffattn_v1_bwd.restype = i32
+            L.diffattn_v1_bwd.argtypes = ([vp] * 5 + [fp] * 4 + [vp, vp, sz] + [vp] * 5 + [fp] * 4 + [vp, sz]
+                                          + [i32] * 5 + [i64] * 12 + [i32, vp])
+            L.diffattn_v2_fwd_train.restype = i32
+            L.diffattn_v2_fwd_train.argtypes = [vp, vp, vp, fp, vp, vp, sz] + [i32] * 5 + [i32, vp]
+            L.diffattn_v2_bwd.restype = i32
+            L.diffattn_v2_bwd.argtypes = ([vp, vp, vp, fp, vp, vp, sz, vp, vp, vp, fp, vp, sz] + [i32] * 5
+                                          + [i32, vp])
             L.diffattn_status_string.restype = ctypes.c_char_p
             L.diffattn_status_string.argtypes = [i32]
             L.diffattn_device_error.restype = i32
@@ -299,3 +315,125 @@ def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, lam_q1, lam_k1, lam_q2, lam_k
                                   _stream(stream))
     _check("diffattn_v1_decode", rc)
     return out
+
+
+# ------------------------------------------------------------------ training
+
+def _v1_strides(q1, q2, k1, k2, v, t_out):
+    if q1.stride() != q2.stride() or k1.stride() != k2.stride():
+        raise ValueError("q1/q2 and k1/k2 must share strides")
+    for t in (q1, k1, v, t_out):
+        if t.stride(-1) != 1:
+            raise ValueError("head dimension must be contiguous")
+    qs, ks, vs, os_ = q1.stride(), k1.stride(), v.stride(), t_out.stride()
+    return [qs[0], qs[1], qs[2], ks[0], ks[1], ks[2], vs[0], vs[1], vs[2], os_[0], os_[1], os_[2]]
+
+
+def _lam_vecs(d, *xs):
+    out = [x.contiguous() for x in xs]
+    for x in out:
+        if x.dtype != torch.float32 or not x.is_cuda or x.numel() != d:
+            raise ValueError("lambda vectors must be fp32 CUDA tensors of length d")
+    return out
+
+
+def v1_fwd_train(q1, q2, k1, k2, v, lam_q1, lam_k1, lam_q2, lam_k2, layer_index: int, stream=None):
+    """DIFF V1 forward that also saves what the backward needs.
+
+    Arguments as v1_fwd.  Returns (out, saved): out (B, T, H, 2d) is the
+    forward output, saved an opaque uint8 CUDA tensor for v1_bwd.
+    """
+    for n, t in (("q1", q1), ("q2", q2), ("k1", k1), ("k2", k2), ("v", v)):
+        _cuda(t, n)
+    B, T, H, d = q1.shape
+    out = torch.empty((B, T, H, 2 * d), dtype=q1.dtype, device=q1.device)
+    strides = _v1_strides(q1, q2, k1, k2, v, out)
+    lams = _lam_vecs(d, lam_q1, lam_k1, lam_q2, lam_k2)
+    nbytes = int(lib().diffattn_v1_train_saved_size(B, T, H, d))
+    saved = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q1.device)
+    rc = lib().diffattn_v1_fwd_train(q1.data_ptr(), q2.data_ptr(), k1.data_ptr(), k2.data_ptr(), v.data_ptr(),
+                                     *[x.data_ptr() for x in lams], out.data_ptr(), saved.data_ptr(), saved.numel(),
+                                     B, T, H, d, int(layer_index), *strides, _dtype_code(q1), _stream(stream))
+    _check("diffattn_v1_fwd_train", rc)
+    return out, saved
+
+
+def v1_bwd(q1, q2, k1, k2, v, lam_q1, lam_k1, lam_q2, lam_k2, layer_index: int, dout, saved,
+           workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Gradients of DIFF V1 for upstream gradient dout (the output's shape).
+
+    Returns dq1, dq2 (q's layout: views of one (B, T, 2H, d) tensor when q1,
+    q2 are the interleaved views), dk1, dk2 (likewise for k), dv, and the fp32
+    lambda-vector gradients dlam_q1, dlam_k1, dlam_q2, dlam_k2.
+    """
+    B, T, H, d = q1.shape
+    if dout.shape != (B, T, H, 2 * d) or dout.dtype != q1.dtype:
+        raise ValueError("dout must match the output")
+    strides = _v1_strides(q1, q2, k1, k2, v, dout)
+    lams = _lam_vecs(d, lam_q1, lam_k1, lam_q2, lam_k2)
+
+    def like(t1, t2):
+        # gradients with the inputs' strides: a shared base when the inputs are views of one tensor
+        if t1.data_ptr() + t1.element_size() * d == t2.data_ptr() and t1.stride()[2] == 2 * d:
+            base = torch.empty((B, T, 2 * H, d), dtype=t1.dtype, device=t1.device)
+            return base[:, :, 0::2], base[:, :, 1::2]
+        if t1.is_contiguous() and t2.is_contiguous():
+            return torch.empty_like(t1), torch.empty_like(t2)
+        raise ValueError("q1/q2 (k1/k2) must be contiguous or the (2h, 2h+1) views of one tensor")
+    dq1, dq2 = like(q1, q2)
+    dk1, dk2 = like(k1, k2)
+    if dq1.stride() != q1.stride() or dk1.stride() != k1.stride():
+        raise ValueError("unsupported q / k layout")
+    dv = torch.empty_like(v)
+    if dv.stride() != v.stride():
+        raise ValueError("v must be contiguous")
+    dl = [torch.empty(d, dtype=torch.float32, device=q1.device) for _ in range(4)]
+    need = int(lib().diffattn_v1_bwd_workspace_size(B, T, H, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q1.device)
+    rc = lib().diffattn_v1_bwd(q1.data_ptr(), q2.data_ptr(), k1.data_ptr(), k2.data_ptr(), v.data_ptr(),
+                               *[x.data_ptr() for x in lams], dout.data_ptr(), saved.data_ptr(), saved.numel(),
+                               dq1.data_ptr(), dq2.data_ptr(), dk1.data_ptr(), dk2.data_ptr(), dv.data_ptr(),
+                               *[x.data_ptr() for x in dl], workspace.data_ptr(), workspace.numel(),
+                               B, T, H, d, int(layer_index), *strides, _dtype_code(q1), _stream(stream))
+    _check("diffattn_v1_bwd", rc)
+    return {"dq1": dq1, "dq2": dq2, "dk1": dk1, "dk2": dk2, "dv": dv,
+            "dlam_q1": dl[0], "dlam_k1": dl[1], "dlam_q2": dl[2], "dlam_k2": dl[3]}
+
+
+def v2_fwd_train(q, k, v, lam, stream=None):
+    """DIFF V2 forward that also saves what the backward needs: (out, saved)."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("lam", lam)):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    out = torch.empty((B, T, Hq // 2, D), dtype=q.dtype, device=q.device)
+    nbytes = int(lib().diffattn_v2_train_saved_size(B, T, Hq, Hkv, D))
+    saved = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    rc = lib().diffattn_v2_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), out.data_ptr(),
+                                     saved.data_ptr(), saved.numel(), B, T, Hq, Hkv, D, _dtype_code(q),
+                                     _stream(stream))
+    _check("diffattn_v2_fwd_train", rc)
+    return out, saved
+
+
+def v2_bwd(q, k, v, lam, dout, saved, workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """Gradients of DIFF V2 for upstream gradient dout (B, T, Hq/2, D):
+    dq, dk, dv (bf16, the inputs' shapes) and dlam (fp32, lam's shape)."""
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if dout.shape != (B, T, Hq // 2, D) or not dout.is_contiguous():
+        raise ValueError("dout must be a contiguous (B, T, Hq/2, D) tensor")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dlam = torch.empty_like(lam)
+    need = int(lib().diffattn_v2_bwd_workspace_size(B, T, Hq, Hkv, D))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = lib().diffattn_v2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), dout.data_ptr(),
+                               saved.data_ptr(), saved.numel(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                               dlam.data_ptr(), workspace.data_ptr(), workspace.numel(), B, T, Hq, Hkv, D,
+                               _dtype_code(q), _stream(stream))
+    _check("diffattn_v2_bwd", rc)
+    return {"dq": dq, "dk": dk, "dv": dv, "dlam": dlam}

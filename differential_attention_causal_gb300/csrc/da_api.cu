@@ -436,6 +436,289 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
 
 }  // extern "C"
 
+// ------------------------------------------------------------ training
+
+namespace {
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Saved-tensor layout of a training forward: two (B, T, H, DV) tensors
+// (V1: x and a2 in fp32; V2: a_e and a_o in bf16) | lse (fp32, (2, B, H, T)),
+// each part 256-byte aligned.
+struct SavedLayout {
+    size_t a_bytes, off_a2, off_lse, total;
+    SavedLayout(int B, int T, int H, int DV, int esize) {
+        a_bytes = round256(static_cast<size_t>(B) * T * H * DV * esize);
+        off_a2 = a_bytes;
+        off_lse = 2 * a_bytes;
+        total = off_lse + round256(static_cast<size_t>(2) * B * H * T * 4);
+    }
+};
+// Backward workspace: D (2, B, H, T) | c (B, H, T) | V1: dlam rows (B, T, H) | g (bf16, (B, T, H, DV))
+struct BwdWsLayout {
+    size_t off_c, off_rows, off_g, total;
+    BwdWsLayout(int B, int T, int H, int DV, bool v1) {
+        const size_t n = static_cast<size_t>(B) * H * T;
+        off_c = round256(2 * n * 4);
+        off_rows = off_c + round256(n * 4);
+        off_g = off_rows + (v1 ? round256(n * 4) : 0);
+        total = off_g + (v1 ? round256(n * DV * 2) : 0);
+    }
+};
+bool shape_ok_bytes(int B, int T, int H, int DV) {
+    return B >= 1 && T >= 1 && H >= 1 && static_cast<double>(B) * T * H * DV < 4.0e12;
+}
+}  // namespace
+
+extern "C" {
+
+size_t diffattn_v1_train_saved_size(int B, int T, int H, int d) {
+    if (!shape_ok_bytes(B, T, H, 2 * d) || !backward_supported(d, 2 * d, false)) return 0;
+    return SavedLayout(B, T, H, 2 * d, 4).total;
+}
+size_t diffattn_v2_train_saved_size(int B, int T, int Hq, int Hkv, int D) {
+    if (Hq < 2 || Hkv < 1 || !shape_ok_bytes(B, T, Hq / 2, D) || !backward_supported(D, D, true)) return 0;
+    return SavedLayout(B, T, Hq / 2, D, 2).total;
+}
+size_t diffattn_v1_bwd_workspace_size(int B, int T, int H, int d) {
+    if (!shape_ok_bytes(B, T, H, 2 * d) || !backward_supported(d, 2 * d, false)) return 0;
+    return BwdWsLayout(B, T, H, 2 * d, true).total;
+}
+size_t diffattn_v2_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D) {
+    if (Hq < 2 || Hkv < 1 || !shape_ok_bytes(B, T, Hq / 2, D) || !backward_supported(D, D, true)) return 0;
+    return BwdWsLayout(B, T, Hq / 2, D, false).total;
+}
+
+da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, const void *k2, const void *v,
+                                const float *lam_q1, const float *lam_k1, const float *lam_q2, const float *lam_k2,
+                                void *out, void *saved, size_t saved_bytes, int B, int T, int H, int d,
+                                int layer_index, int64_t q_sb, int64_t q_st, int64_t q_sh, int64_t k_sb,
+                                int64_t k_st, int64_t k_sh, int64_t v_sb, int64_t v_st, int64_t v_sh, int64_t o_sb,
+                                int64_t o_st, int64_t o_sh, da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q1 || !q2 || !k1 || !k2 || !v || !lam_q1 || !lam_k1 || !lam_q2 || !lam_k2 || !out || !saved)
+        return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
+    if (dtype != DA_BF16 || !backward_supported(d, 2 * d, false)) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q1, q2, k1, k2, v, static_cast<const void *>(out), static_cast<const void *>(saved)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    for (int64_t st : {q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh, o_sb, o_st, o_sh})
+        if (!stride_ok(st, 2)) return DA_ERR_MISALIGNED;
+    const SavedLayout sl(B, T, H, 2 * d, 4);
+    if (saved_bytes < sl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    t_last_launches = 0;
+    PrefillMaps m;
+    const uint64_t uT = static_cast<uint64_t>(T), uH = static_cast<uint64_t>(H), uB = static_cast<uint64_t>(B);
+    if (!encode_map_4d(&m.q1, q1, d, uH, uT, uB, q_sh, q_st, q_sb, 128) ||
+        !encode_map_4d(&m.q2, q2, d, uH, uT, uB, q_sh, q_st, q_sb, 128) ||
+        !encode_map_4d(&m.k1, k1, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
+        !encode_map_4d(&m.k2, k2, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
+        !encode_map_4d(&m.v, v, 2 * d, uH, uT, uB, v_sh, v_st, v_sb, 128) ||
+        !encode_map_4d(&m.out, out, 2 * d, uH, uT, uB, o_sh, o_st, o_sb, 128))
+        return DA_ERR_CUDA;
+    PrefillParams p{};
+    p.out = out; p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
+    p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+    p.layer_index = layer_index;
+    p.B = B; p.T = T; p.H = H; p.G = 1;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
+    p.err = err;
+    char *sv = static_cast<char *>(saved);
+    p.sa1 = sv;
+    p.sa2 = sv + sl.off_a2;
+    p.slse = reinterpret_cast<float *>(sv + sl.off_lse);
+    const da_status st = cuda_status(launch_prefill_train(m, p, d, 2 * d, false, stream));
+    if (st == DA_OK) t_last_launches = 1;
+    return st;
+}
+
+da_status diffattn_v2_fwd_train(const void *q, const void *k, const void *v, const float *lam, void *out,
+                                void *saved, size_t saved_bytes, int B, int T, int Hq, int Hkv, int D,
+                                da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q || !k || !v || !lam || !out || !saved) return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || Hq < 2 || Hkv < 1) return DA_ERR_BAD_SHAPE;
+    if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
+    if (dtype != DA_BF16 || !backward_supported(D, D, true)) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q, k, v, static_cast<const void *>(out), static_cast<const void *>(saved)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    const int P = Hq / 2, G = Hq / Hkv;
+    const SavedLayout sl(B, T, P, D, 2);
+    if (saved_bytes < sl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    t_last_launches = 0;
+    PrefillMaps m;
+    const uint64_t uT = static_cast<uint64_t>(T), uB = static_cast<uint64_t>(B);
+    const int64_t qst = static_cast<int64_t>(Hq) * D, kst = static_cast<int64_t>(Hkv) * D;
+    if (!encode_map_4d(&m.q1, q, D, Hq, uT, uB, D, qst, qst * T, 128) ||
+        !encode_map_4d(&m.k1, k, D, Hkv, uT, uB, D, kst, kst * T, 128) ||
+        !encode_map_4d(&m.v, v, D, Hkv, uT, uB, D, kst, kst * T, 128) ||
+        !encode_map_4d(&m.out, out, D, P, uT, uB, D, static_cast<int64_t>(P) * D, static_cast<int64_t>(P) * D * T, 128))
+        return DA_ERR_CUDA;
+    m.q2 = m.q1;
+    m.k2 = m.k1;
+    PrefillParams p{};
+    p.out = out;
+    p.o_sh = D; p.o_st = static_cast<int64_t>(P) * D; p.o_sb = p.o_st * T;
+    p.lam = lam;
+    p.B = B; p.T = T; p.H = P; p.G = G;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.err = err;
+    char *sv = static_cast<char *>(saved);
+    p.sa1 = sv;
+    p.sa2 = sv + sl.off_a2;
+    p.slse = reinterpret_cast<float *>(sv + sl.off_lse);
+    const da_status st = cuda_status(launch_prefill_train(m, p, D, D, true, stream));
+    if (st == DA_OK) t_last_launches = 1;
+    return st;
+}
+
+da_status diffattn_v1_bwd(const void *q1, const void *q2, const void *k1, const void *k2, const void *v,
+                          const float *lam_q1, const float *lam_k1, const float *lam_q2, const float *lam_k2,
+                          const void *dout, const void *saved, size_t saved_bytes, void *dq1, void *dq2, void *dk1,
+                          void *dk2, void *dv, float *dlam_q1, float *dlam_k1, float *dlam_q2, float *dlam_k2,
+                          void *workspace, size_t workspace_bytes, int B, int T, int H, int d, int layer_index,
+                          int64_t q_sb, int64_t q_st, int64_t q_sh, int64_t k_sb, int64_t k_st, int64_t k_sh,
+                          int64_t v_sb, int64_t v_st, int64_t v_sh, int64_t o_sb, int64_t o_st, int64_t o_sh,
+                          da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q1 || !q2 || !k1 || !k2 || !v || !lam_q1 || !lam_k1 || !lam_q2 || !lam_k2 || !dout || !saved || !dq1 ||
+        !dq2 || !dk1 || !dk2 || !dv || !dlam_q1 || !dlam_k1 || !dlam_q2 || !dlam_k2 || !workspace)
+        return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
+    if (dtype != DA_BF16 || !backward_supported(d, 2 * d, false)) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q1, q2, k1, k2, v, dout, saved, static_cast<const void *>(dq1),
+                            static_cast<const void *>(dq2), static_cast<const void *>(dk1),
+                            static_cast<const void *>(dk2), static_cast<const void *>(dv),
+                            static_cast<const void *>(workspace)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    for (int64_t st : {q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh, o_sb, o_st, o_sh})
+        if (!stride_ok(st, 2)) return DA_ERR_MISALIGNED;
+    const int DV = 2 * d;
+    const SavedLayout sl(B, T, H, DV, 4);
+    const BwdWsLayout wl(B, T, H, DV, true);
+    if (saved_bytes < sl.total || workspace_bytes < wl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    t_last_launches = 0;
+    char *ws = static_cast<char *>(workspace);
+    const char *sv = static_cast<const char *>(saved);
+    __nv_bfloat16 *g = reinterpret_cast<__nv_bfloat16 *>(ws + wl.off_g);
+    BwdMaps m;
+    const uint64_t uT = static_cast<uint64_t>(T), uH = static_cast<uint64_t>(H), uB = static_cast<uint64_t>(B);
+    const int64_t g_st = static_cast<int64_t>(H) * DV;
+    bool okm = true;
+    for (int rows : {128, 64}) {
+        const bool r = rows == 128;
+        okm = okm && encode_map_4d(r ? &m.q1r : &m.q1c, q1, d, uH, uT, uB, q_sh, q_st, q_sb, rows) &&
+              encode_map_4d(r ? &m.q2r : &m.q2c, q2, d, uH, uT, uB, q_sh, q_st, q_sb, rows) &&
+              encode_map_4d(r ? &m.k1r : &m.k1c, k1, d, uH, uT, uB, k_sh, k_st, k_sb, rows) &&
+              encode_map_4d(r ? &m.k2r : &m.k2c, k2, d, uH, uT, uB, k_sh, k_st, k_sb, rows) &&
+              encode_map_4d(r ? &m.vr : &m.vc, v, DV, uH, uT, uB, v_sh, v_st, v_sb, rows) &&
+              encode_map_4d(r ? &m.gr : &m.gc, g, DV, uH, uT, uB, DV, g_st, g_st * T, rows);
+    }
+    if (!okm) return DA_ERR_CUDA;
+    BwdPreParams pp{};
+    pp.sa1 = sv;
+    pp.sa2 = sv + sl.off_a2;
+    pp.dout = static_cast<const __nv_bfloat16 *>(dout);
+    pp.o_sb = o_sb; pp.o_st = o_st; pp.o_sh = o_sh;
+    pp.layer_index = layer_index;
+    pp.lq1 = lam_q1; pp.lk1 = lam_k1; pp.lq2 = lam_q2; pp.lk2 = lam_k2;
+    pp.dlq1 = dlam_q1; pp.dlk1 = dlam_k1; pp.dlq2 = dlam_q2; pp.dlk2 = dlam_k2;
+    pp.dlam_rows = reinterpret_cast<float *>(ws + wl.off_rows);
+    pp.g = g;
+    pp.dd = reinterpret_cast<float *>(ws);
+    pp.cv = reinterpret_cast<float *>(ws + wl.off_c);
+    pp.B = B; pp.T = T; pp.H = H; pp.d = d;
+    BwdParams p{};
+    p.dq1 = static_cast<__nv_bfloat16 *>(dq1); p.dq2 = static_cast<__nv_bfloat16 *>(dq2);
+    p.dk1 = static_cast<__nv_bfloat16 *>(dk1); p.dk2 = static_cast<__nv_bfloat16 *>(dk2);
+    p.dv = static_cast<__nv_bfloat16 *>(dv);
+    p.q_sb = q_sb; p.q_st = q_st; p.q_sh = q_sh;
+    p.k_sb = k_sb; p.k_st = k_st; p.k_sh = k_sh;
+    p.v_sb = v_sb; p.v_st = v_st; p.v_sh = v_sh;
+    p.lse = reinterpret_cast<const float *>(sv + sl.off_lse);
+    p.dd = pp.dd;
+    p.cv = pp.cv;
+    p.B = B; p.T = T; p.H = H; p.G = 1; p.Hkv = H;
+    p.scale = 1.f / sqrtf(static_cast<float>(d));
+    p.scale_log2 = 1.4426950408889634f * p.scale;
+    p.err = err;
+    const da_status st = cuda_status(launch_backward(m, p, pp, d, DV, false, stream));
+    if (st == DA_OK) t_last_launches = 4;
+    return st;
+}
+
+da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const float *lam, const void *dout,
+                          const void *saved, size_t saved_bytes, void *dq, void *dk, void *dv, float *dlam,
+                          void *workspace, size_t workspace_bytes, int B, int T, int Hq, int Hkv, int D,
+                          da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q || !k || !v || !lam || !dout || !saved || !dq || !dk || !dv || !dlam || !workspace)
+        return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || Hq < 2 || Hkv < 1) return DA_ERR_BAD_SHAPE;
+    if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
+    if (dtype != DA_BF16 || !backward_supported(D, D, true)) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q, k, v, dout, saved, static_cast<const void *>(dq), static_cast<const void *>(dk),
+                            static_cast<const void *>(dv), static_cast<const void *>(workspace)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    const int P = Hq / 2, G = Hq / Hkv;
+    const SavedLayout sl(B, T, P, D, 2);
+    const BwdWsLayout wl(B, T, P, D, false);
+    if (saved_bytes < sl.total || workspace_bytes < wl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    t_last_launches = 0;
+    char *ws = static_cast<char *>(workspace);
+    const char *sv = static_cast<const char *>(saved);
+    BwdMaps m;
+    const uint64_t uT = static_cast<uint64_t>(T), uB = static_cast<uint64_t>(B);
+    const int64_t qst = static_cast<int64_t>(Hq) * D, kst = static_cast<int64_t>(Hkv) * D;
+    const int64_t ost = static_cast<int64_t>(P) * D;
+    bool okm = true;
+    for (int rows : {128, 64}) {
+        const bool r = rows == 128;
+        okm = okm && encode_map_4d(r ? &m.q1r : &m.q1c, q, D, Hq, uT, uB, D, qst, qst * T, rows) &&
+              encode_map_4d(r ? &m.k1r : &m.k1c, k, D, Hkv, uT, uB, D, kst, kst * T, rows) &&
+              encode_map_4d(r ? &m.vr : &m.vc, v, D, Hkv, uT, uB, D, kst, kst * T, rows) &&
+              encode_map_4d(r ? &m.gr : &m.gc, dout, D, P, uT, uB, D, ost, ost * T, rows);
+    }
+    if (!okm) return DA_ERR_CUDA;
+    m.q2r = m.q1r; m.q2c = m.q1c; m.k2r = m.k1r; m.k2c = m.k1c;
+    BwdPreParams pp{};
+    pp.sa1 = sv;
+    pp.sa2 = sv + sl.off_a2;
+    pp.dout = static_cast<const __nv_bfloat16 *>(dout);
+    pp.o_sh = D; pp.o_st = ost; pp.o_sb = ost * T;
+    pp.lam = lam;
+    pp.dlam = dlam;
+    pp.dd = reinterpret_cast<float *>(ws);
+    pp.cv = reinterpret_cast<float *>(ws + wl.off_c);
+    pp.B = B; pp.T = T; pp.H = P; pp.d = D;
+    BwdParams p{};
+    p.dq1 = p.dq2 = static_cast<__nv_bfloat16 *>(dq);
+    p.dk1 = p.dk2 = static_cast<__nv_bfloat16 *>(dk);
+    p.dv = static_cast<__nv_bfloat16 *>(dv);
+    p.q_sh = D; p.q_st = qst; p.q_sb = qst * T;
+    p.k_sh = D; p.k_st = kst; p.k_sb = kst * T;
+    p.v_sh = D; p.v_st = kst; p.v_sb = kst * T;
+    p.lse = reinterpret_cast<const float *>(sv + sl.off_lse);
+    p.dd = pp.dd;
+    p.cv = pp.cv;
+    p.B = B; p.T = T; p.H = P; p.G = G; p.Hkv = Hkv;
+    p.scale = 1.f / sqrtf(static_cast<float>(D));
+    p.scale_log2 = 1.4426950408889634f * p.scale;
+    p.err = err;
+    const da_status st = cuda_status(launch_backward(m, p, pp, D, D, true, stream));
+    if (st == DA_OK) t_last_launches = 3;
+    return st;
+}
+
+}  // extern "C"
+
 // ---------------------------------------------------------------------------
 // Decode without allocation: the split-KV partials go to a buffer the library
 // owns, so a caller that may not allocate device memory passes only inputs

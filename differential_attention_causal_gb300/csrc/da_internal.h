@@ -50,6 +50,13 @@ struct PrefillParams {
     int B, T, H, G;
     float scale_log2;              // log2(e) / sqrt(dqk)
     uint32_t *err;
+    // training forward only ((B, T, H, DV) contiguous; NULL for the plain
+    // forward): V1 saves x = a1 - lam a2 (the RMSNorm input) and a2 in fp32,
+    // V2 saves a_e and a_o in bf16 (a_b = O_b / l_b); both save each branch's
+    // log-sum-exp in log2 units, lse_b = m + log2(l), so that
+    // P = 2^(s * scale_log2 - lse_b) (fp32, (2, B, H, T))
+    void *sa1, *sa2;
+    float *slse;
 };
 struct PrefillMaps {
     CUtensorMap q1, q2, k1, k2, v;
@@ -58,12 +65,52 @@ struct PrefillMaps {
 // dqk/dv in {64/128 (V1), 128/256 (V1 two-pass), 64/64, 128/128 (V2)}
 cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
                            cudaStream_t s);
+// The same kernel with the training epilogue (p.sa1, p.sa2, p.slse written).
+cudaError_t launch_prefill_train(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
+                                 cudaStream_t s);
 bool prefill_supported(int dqk, int dv, bool v2);
 // DIFF V1 in two passes over the keys (row statistics, then one combined PV);
 // dqk in {64, 128}, dv = 2 dqk.  The V tensor map's box has
 // prefill_v1_twopass_v_rows(dqk) rows (the Q/K maps 128).
 cudaError_t launch_prefill_v1_twopass(const PrefillMaps &m, const PrefillParams &p, int dqk, cudaStream_t s);
 int prefill_v1_twopass_v_rows(int dqk);
+
+// -------------------------------------------------------------- backward
+// Gradients of the V1 / V2 prefill (k_backward.cu).  H = diff heads (V1) or
+// pairs (V2); row vectors are (2, B, H, T) fp32 (branch-major).
+struct BwdParams {
+    __nv_bfloat16 *dq1, *dq2, *dk1, *dk2, *dv;   // V2: dq1 == dq2 (head 2i / 2i+1), dk1 == dk2
+    int64_t q_sb, q_st, q_sh;                    // element strides of q1/q2 and dq1/dq2
+    int64_t k_sb, k_st, k_sh;                    // of k1/k2 and dk1/dk2
+    int64_t v_sb, v_st, v_sh;                    // of v and dv
+    const float *lse;                            // forward log-sum-exp, log2 units
+    const float *dd;                             // D_b = g_b . a_b
+    const float *cv;                             // c (B, H, T): V1 -lam, V2 -sigmoid(lam[t])
+    int B, T, H, G, Hkv;
+    float scale_log2, scale;                     // log2(e) / sqrt(dqk), 1 / sqrt(dqk)
+    uint32_t *err;
+};
+struct BwdPreParams {
+    const void *sa1, *sa2;                       // saved: V1 x, a2 (fp32); V2 a_e, a_o (bf16)
+    const __nv_bfloat16 *dout;                   // upstream gradient, the output's layout
+    int64_t o_sb, o_st, o_sh;
+    const float *lam;                            // V2 logits (B, T, H)
+    int layer_index;                             // V1
+    const float *lq1, *lk1, *lq2, *lk2;          // V1 lambda vectors (d)
+    float *dlq1, *dlk1, *dlq2, *dlk2;            // V1 outputs (d)
+    float *dlam;                                 // V2 output (B, T, H)
+    float *dlam_rows;                            // V1 scratch (B, T, H)
+    __nv_bfloat16 *g;                            // V1 g_1 = dx, (B, T, H, DV) contiguous
+    float *dd, *cv;                              // outputs D (2, B, H, T); c (B, H, T)
+    int B, T, H, d;
+};
+struct BwdMaps {
+    CUtensorMap q1r, q2r, gr, k1c, k2c, vc;      // dQ kernel: 128-row Q / G boxes, 64-row K / V boxes
+    CUtensorMap k1r, k2r, vr, q1c, q2c, gc;      // dK dV kernel: 128-row K / V boxes, 64-row Q / G boxes
+};
+bool backward_supported(int dqk, int dv, bool v2);
+cudaError_t launch_backward(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, int dqk, int dv, bool v2,
+                            cudaStream_t s);
 
 // --------------------------------------------------------------- decode
 // One kernel family serves three decodes:

@@ -1,0 +1,783 @@
+// k_backward.cu -- backward of the causal differential attention on tcgen05
+// tensor cores (bf16 in, fp32 accumulate): DIFF V1 (d = 64, dv = 128) and
+// DIFF V2 (D = 64 / 128).
+//
+// "Differential Transformer V2", DiffAttnV1 / DiffAttnV2, differentiated.
+// Both operations are two softmax attentions a_b = softmax(S_b) V, b = 1, 2,
+// S_b = scale Q_b K_b^T (causal), combined per row.  With g_b = dL/da_b the
+// upstream gradient of branch b, each branch backward is
+//     dV += P_b^T g_b,   dP_b = g_b V^T,   dS_b = P_b o (dP_b - D_b),
+//     D_b[i] = sum_j P_b[i,j] dP_b[i,j] = g_b[i] . a_b[i],
+//     dQ_b = scale dS_b K_b,   dK_b = scale dS_b^T Q_b.
+// Here g_2 = c g_1 row by row (V1: g_1 = dx, c = -lam, dx the RMSNorm
+// backward of (1 - lam_init) dout; V2: g_1 = dout, c = -sigmoid(lam[t])), so
+//     dP_2 = c dP_1            (one dP product for both branches)
+//     dV  += (P_1 + c P_2)^T g_1   (one dV product for both branches).
+// P_b is recomputed from the scores and the forward's log-sum-exp.
+//
+// Three kernels (plus the row pre-pass in this file):
+//   bwd_pre     one warp per row: g_1 (V1: the RMSNorm backward), D_1, D_2,
+//               c, and the lambda gradient (V1: per-row share of dL/dlam;
+//               V2: dL/dlam[t] directly).
+//   bwd_dq      query-stationary: 128 query rows, 64-key sub-tiles.  TMEM:
+//               S1 | S2 | dP (64 columns each) | dQ1 | dQ2.
+//   bwd_dkdv    key-stationary: 128 key rows, 64-query sub-tiles (for V2 of
+//               every pair of the kv group).  TMEM: S1^T | S2^T | dP^T (64
+//               each) | dK1 (| dK2) | dV.
+// In both, warp 0 streams the sub-tiles with TMA, warp 1 issues the MMAs,
+// warps 4-7 own one TMEM lane (row) each and turn scores into P, dS.  The
+// bf16 results are written over columns the threads have already read
+// (dq: dS1 -> S1, dS2 -> S2; dkdv: P~ -> S1^T, dS1^T -> S2^T, dS2^T -> dP^T)
+// and feed TS MMAs (A from TMEM, B an MN-major shared-memory tile).
+#include "da_common.cuh"
+#include "da_internal.h"
+
+namespace da {
+namespace {
+
+template <int DQK, int DV, bool V2>
+struct BwdCfg {
+    static constexpr int BM = 128, BN = 64;
+    static constexpr int QB = DQK / 64, VB = DV / 64;   // 64-column boxes
+    static constexpr int RBOX = 128 * 128;              // 128 rows x 64 bf16
+    static constexpr int CBOX = 64 * 128;               // 64 rows x 64 bf16
+    static constexpr int NK = V2 ? 1 : 2;               // distinct K tiles (V1: K1, K2)
+    static constexpr int STAGES = 3;
+    static constexpr int COL_S1 = 0, COL_S2 = 64, COL_DP = 128, COL_ACC = 192;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false);
+    static constexpr uint32_t IDESC_QK = idesc_bf16(128, DQK, true);
+    static constexpr uint32_t IDESC_V = idesc_bf16(128, DV, true);
+    static constexpr int THREADS = 256;
+    static constexpr int MIN_SMEM = 120 * 1024;   // one CTA per SM (each takes all of TMEM)
+
+    // ---- dq kernel: resident Q1, Q2, G (128 rows); ring of K1 (, K2), V (64 rows)
+    static constexpr int DQ_OFF_Q1 = 0;
+    static constexpr int DQ_OFF_Q2 = QB * RBOX;
+    static constexpr int DQ_OFF_G = 2 * QB * RBOX;
+    static constexpr int DQ_OFF_RING = DQ_OFF_G + VB * RBOX;
+    static constexpr int DQ_STAGE = NK * QB * CBOX + VB * CBOX;
+    static constexpr int DQ_OFF_BAR = DQ_OFF_RING + STAGES * DQ_STAGE;
+    static constexpr int DQ_NBAR = 1 + 2 * STAGES + 4;   // res, full[S], empty[S], s, ds, done, drain
+    static constexpr int DQ_OFF_TSLOT = DQ_OFF_BAR + DQ_NBAR * 8;
+    static constexpr int DQ_SMEM_RAW = DQ_OFF_TSLOT + 8 + 1024;
+    static constexpr int DQ_SMEM = DQ_SMEM_RAW > MIN_SMEM ? DQ_SMEM_RAW : MIN_SMEM;
+    static constexpr int COL_DQ1 = COL_ACC, COL_DQ2 = COL_ACC + DQK;
+
+    // ---- dkdv kernel: resident K1 (, K2), V (128 rows); ring of Q1, Q2, G (64 rows) + row vectors
+    static constexpr int KV_OFF_K1 = 0;
+    static constexpr int KV_OFF_K2 = QB * RBOX;                    // V1 only
+    static constexpr int KV_OFF_V = NK * QB * RBOX;
+    static constexpr int KV_OFF_RING = KV_OFF_V + VB * RBOX;
+    static constexpr int KV_VEC = 5 * 64 * 4;                      // lse1, lse2, d1, d2, c
+    static constexpr int KV_STAGE_TMA = 2 * QB * CBOX + VB * CBOX;
+    static constexpr int KV_STAGE = KV_STAGE_TMA + 2048;           // vectors, padded to keep 1 KB alignment
+    static constexpr int KV_OFF_BAR = KV_OFF_RING + STAGES * KV_STAGE;
+    static constexpr int KV_NBAR = 1 + 2 * STAGES + 4;             // res, full[S], empty[S], s, p, done, drain
+    static constexpr int KV_OFF_TSLOT = KV_OFF_BAR + KV_NBAR * 8;
+    static constexpr int KV_SMEM_RAW = KV_OFF_TSLOT + 8 + 1024;
+    static constexpr int KV_SMEM = KV_SMEM_RAW > MIN_SMEM ? KV_SMEM_RAW : MIN_SMEM;
+    static constexpr int COL_DK1 = COL_ACC;
+    static constexpr int COL_DK2 = V2 ? COL_ACC : COL_ACC + DQK;   // V2: both branches hit one K
+    static constexpr int COL_DV = COL_ACC + NK * DQK;
+
+    static_assert(COL_DQ2 + DQK <= 512 && COL_DV + DV <= 512, "TMEM budget");
+    static_assert(DQ_SMEM <= 232448 && KV_SMEM <= 232448, "shared memory budget");
+    static_assert(KV_VEC <= 2048, "vector area");
+};
+
+// 16 bf16 pairs from 32 floats held as bit patterns
+__device__ __forceinline__ void pack32(const uint32_t *x, uint32_t *u) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) u[i] = pack_bf16(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+}
+
+// ===================================================================== dQ
+template <int DQK, int DV, bool V2>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dq(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
+           const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tk1,
+           const __grid_constant__ CUtensorMap tk2, const __grid_constant__ CUtensorMap tv, const BwdParams p) {
+    using C = BwdCfg<DQK, DV, V2>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // tile w -> query tile (heaviest first), head / pair, batch
+    const int n_qt = (p.T + C::BM - 1) / C::BM;
+    const int per_qt = p.H * p.B;
+    const int w = static_cast<int>(blockIdx.x);
+    const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
+    const int h = rest % p.H, b = rest / p.H;
+    const int n_kt = (p.T + C::BN - 1) / C::BN;
+    const int kend = (qt + 1) * (C::BM / C::BN);
+    const int n_kv = kend < n_kt ? kend : n_kt;   // 64-key sub-tiles at or before the diagonal
+    const int hq1 = V2 ? 2 * h : h, hq2 = V2 ? 2 * h + 1 : h;
+    const int hk = V2 ? (2 * h) / p.G : h;
+
+    const uint32_t bar_res = sbase + C::DQ_OFF_BAR;
+    const uint32_t bar_full = bar_res + 8;
+    const uint32_t bar_empty = bar_full + 8 * C::STAGES;
+    const uint32_t bar_s = bar_empty + 8 * C::STAGES;
+    const uint32_t bar_ds = bar_s + 8;
+    const uint32_t bar_done = bar_ds + 8;
+    const uint32_t bar_dr = bar_done + 8;
+    const uint32_t tslot = sbase + C::DQ_OFF_TSLOT;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_res, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_ds, 4);
+        mbar_init(bar_done, 1);
+        mbar_init(bar_dr, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::DQ_OFF_TSLOT);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            prefetch_tmap(&tq1);
+            prefetch_tmap(&tg);
+            prefetch_tmap(&tk1);
+            prefetch_tmap(&tv);
+            mbar_arrive_expect_tx(bar_res, 2 * C::QB * C::RBOX + C::VB * C::RBOX);
+#pragma unroll
+            for (int c = 0; c < C::QB; ++c) {
+                tma_load_4d(sbase + C::DQ_OFF_Q1 + c * C::RBOX, &tq1, bar_res, 64 * c, hq1, qt * C::BM, b);
+                tma_load_4d(sbase + C::DQ_OFF_Q2 + c * C::RBOX, &tq2, bar_res, 64 * c, hq2, qt * C::BM, b);
+            }
+#pragma unroll
+            for (int c = 0; c < C::VB; ++c)
+                tma_load_4d(sbase + C::DQ_OFF_G + c * C::RBOX, &tg, bar_res, 64 * c, h, qt * C::BM, b);
+            int j = 0;
+            for (; j < n_kv; ++j) {
+                const int st = j % C::STAGES;
+                if (j >= C::STAGES &&
+                    !mbar_wait(bar_empty + 8 * st, static_cast<uint32_t>((j / C::STAGES - 1) & 1), p.err))
+                    break;
+                const uint32_t dst = sbase + C::DQ_OFF_RING + st * C::DQ_STAGE;
+                mbar_arrive_expect_tx(bar_full + 8 * st, C::DQ_STAGE);
+#pragma unroll
+                for (int c = 0; c < C::QB; ++c) {
+                    tma_load_4d(dst + c * C::CBOX, &tk1, bar_full + 8 * st, 64 * c, hk, j * C::BN, b);
+                    if (!V2)
+                        tma_load_4d(dst + (C::QB + c) * C::CBOX, &tk2, bar_full + 8 * st, 64 * c, hk, j * C::BN, b);
+                }
+#pragma unroll
+                for (int c = 0; c < C::VB; ++c)
+                    tma_load_4d(dst + (C::NK * C::QB + c) * C::CBOX, &tv, bar_full + 8 * st, 64 * c, hk, j * C::BN,
+                                b);
+            }
+            // leave no copy in flight
+            mbar_wait(bar_res, 0, p.err);
+            for (int k = (j > C::STAGES ? j - C::STAGES : 0); k < j; ++k)
+                mbar_wait(bar_full + 8 * (k % C::STAGES), static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            const uint32_t sQ1 = sbase + C::DQ_OFF_Q1, sQ2 = sbase + C::DQ_OFF_Q2, sG = sbase + C::DQ_OFF_G;
+            bool ok = mbar_wait(bar_res, 0, p.err);
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int st = j % C::STAGES;
+                const uint32_t sK1 = sbase + C::DQ_OFF_RING + st * C::DQ_STAGE;
+                const uint32_t sK2 = V2 ? sK1 : sK1 + C::QB * C::CBOX;
+                const uint32_t sV = sK1 + C::NK * C::QB * C::CBOX;
+                ok = mbar_wait(bar_full + 8 * st, static_cast<uint32_t>((j / C::STAGES) & 1), p.err);
+                if (!ok) break;
+                tc_fence_after();
+                // S_b = Q_b K_b^T (N = 64 keys), dP = G V^T
+                {
+                    const uint64_t a1 = sdesc_sw128(sQ1, 16, 1024), a2 = sdesc_sw128(sQ2, 16, 1024);
+                    const uint64_t b1 = sdesc_sw128(sK1, 16, 1024), b2 = sdesc_sw128(sK2, 16, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < DQK / 16; ++ks) {
+                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                        mma_ss(tmem + C::COL_S1, a1 + oa, b1 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                        mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    }
+                    const uint64_t ag = sdesc_sw128(sG, 16, 1024), bv = sdesc_sw128(sV, 16, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < DV / 16; ++ks) {
+                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                        mma_ss(tmem + C::COL_DP, ag + oa, bv + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar_s);
+                ok = mbar_wait(bar_ds, static_cast<uint32_t>(j & 1), p.err);
+                if (!ok) break;
+                tc_fence_after();
+                // dQ_b += dS_b K_b: A = dS_b (bf16 in TMEM), B = K_b tile MN-major
+                {
+                    const uint64_t k1 = sdesc_sw128(sK1, C::CBOX, 1024), k2 = sdesc_sw128(sK2, C::CBOX, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < C::BN / 16; ++ks) {
+                        const uint32_t ob = (ks * 2048) >> 4;
+                        mma_ts(tmem + C::COL_DQ1, tmem + C::COL_S1 + ks * 8, k1 + ob, C::IDESC_QK,
+                               (j > 0 || ks > 0) ? 1u : 0u);
+                        mma_ts(tmem + C::COL_DQ2, tmem + C::COL_S2 + ks * 8, k2 + ob, C::IDESC_QK,
+                               (j > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar_empty + 8 * st);
+            }
+            mma_commit(bar_done);
+            // no MMA may be in flight when TMEM is released
+            mma_commit(bar_dr);
+            mbar_wait(bar_dr, 0, p.err);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ rows (query i)
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const int t = qt * C::BM + row;
+        const bool live = t < p.T;
+        const int64_t vi = (static_cast<int64_t>(b) * p.H + h) * p.T + t;
+        const int64_t vstride = static_cast<int64_t>(p.B) * p.H * p.T;
+        const float lse1 = live ? p.lse[vi] : 0.f, lse2 = live ? p.lse[vstride + vi] : 0.f;
+        const float d1 = live ? p.dd[vi] : 0.f, d2 = live ? p.dd[vstride + vi] : 0.f;
+        const float cc = live ? p.cv[vi] : 0.f;
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            ok = warp_wait(bar_s, static_cast<uint32_t>(j & 1), p.err, ok);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t s1[32], s2[32], dp[32];
+                    tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * hh, s1);
+                    tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * hh, s2);
+                    tmem_ld32(tmem + lane_off + C::COL_DP + 32 * hh, dp);
+                    tmem_wait_ld();
+                    const int key0 = j * C::BN + 32 * hh;
+                    // in place: s1 <- dS1, s2 <- dS2
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const bool valid = live && key0 + c <= t;
+                        const float dpv = __uint_as_float(dp[c]);
+                        const float p1 = valid ? ex2(__uint_as_float(s1[c]) * sl2 - lse1) : 0.f;
+                        const float p2 = valid ? ex2(__uint_as_float(s2[c]) * sl2 - lse2) : 0.f;
+                        s1[c] = __float_as_uint(p1 * (dpv - d1));
+                        s2[c] = __float_as_uint(p2 * (cc * dpv - d2));
+                    }
+                    uint32_t u[16];
+                    pack32(s1, u);
+                    tmem_st16(tmem + lane_off + C::COL_S1 + 16 * hh, u);
+                    pack32(s2, u);
+                    tmem_st16(tmem + lane_off + C::COL_S2 + 16 * hh, u);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ds);
+        }
+        // epilogue: dQ_b * scale -> bf16 rows
+        ok = warp_wait(bar_done, 0, p.err, ok);
+        tc_fence_after();
+        if (ok) {
+#pragma unroll
+            for (int br = 0; br < 2; ++br) {
+                __nv_bfloat16 *dst = (br ? p.dq2 : p.dq1) + b * p.q_sb + static_cast<int64_t>(t) * p.q_st +
+                                     static_cast<int64_t>(br ? hq2 : hq1) * p.q_sh;
+#pragma unroll
+                for (int c0 = 0; c0 < DQK; c0 += 32) {
+                    uint32_t a[32];
+                    tmem_ld32(tmem + lane_off + (br ? C::COL_DQ2 : C::COL_DQ1) + c0, a);
+                    tmem_wait_ld();
+                    if (live) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const uint32_t *aa = a + 8 * q8;
+                            d4[q8] = make_uint4(
+                                pack_bf16(__uint_as_float(aa[0]) * p.scale, __uint_as_float(aa[1]) * p.scale),
+                                pack_bf16(__uint_as_float(aa[2]) * p.scale, __uint_as_float(aa[3]) * p.scale),
+                                pack_bf16(__uint_as_float(aa[4]) * p.scale, __uint_as_float(aa[5]) * p.scale),
+                                pack_bf16(__uint_as_float(aa[6]) * p.scale, __uint_as_float(aa[7]) * p.scale));
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// =================================================================== dK dV
+template <int DQK, int DV, bool V2>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dkdv(const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
+             const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq1,
+             const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tg, const BwdParams p) {
+    using C = BwdCfg<DQK, DV, V2>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // tile w -> key tile (heaviest = earliest first), head (V1) / kv head (V2), batch
+    const int n_kt = (p.T + C::BM - 1) / C::BM;
+    const int nh = V2 ? p.Hkv : p.H;
+    const int per_kt = nh * p.B;
+    const int w = static_cast<int>(blockIdx.x);
+    const int kt = w / per_kt, rest = w % per_kt;
+    const int hk = rest % nh, b = rest / nh;
+    const int n_qs = (p.T + C::BN - 1) / C::BN;
+    const int i0 = kt * (C::BM / C::BN);
+    const int nq = n_qs - i0;                       // query sub-tiles at or after the diagonal
+    const int npairs = V2 ? p.G / 2 : 1;
+    const int n_items = npairs * nq;
+    // item -> (pair or head for the row vectors, query sub-tile)
+    auto item_head = [&](int it) { return V2 ? hk * (p.G / 2) + it / nq : hk; };
+    auto item_qs = [&](int it) { return i0 + it % nq; };
+
+    const uint32_t bar_res = sbase + C::KV_OFF_BAR;
+    const uint32_t bar_full = bar_res + 8;
+    const uint32_t bar_empty = bar_full + 8 * C::STAGES;
+    const uint32_t bar_s = bar_empty + 8 * C::STAGES;
+    const uint32_t bar_p = bar_s + 8;
+    const uint32_t bar_done = bar_p + 8;
+    const uint32_t bar_dr = bar_done + 8;
+    const uint32_t tslot = sbase + C::KV_OFF_TSLOT;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar_res, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1 + 32);   // TMA bytes + 32 lanes' row vectors
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_p, 4);
+        mbar_init(bar_done, 1);
+        mbar_init(bar_dr, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tslot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + C::KV_OFF_TSLOT);
+    const int64_t vstride = static_cast<int64_t>(p.B) * p.H * p.T;
+
+    if (warp == 0) {
+        // ------------------------------------------ TMA + row vectors (32 lanes)
+        if (lane == 0) {
+            prefetch_tmap(&tk1);
+            prefetch_tmap(&tv);
+            prefetch_tmap(&tq1);
+            prefetch_tmap(&tg);
+            mbar_arrive_expect_tx(bar_res, C::NK * C::QB * C::RBOX + C::VB * C::RBOX);
+#pragma unroll
+            for (int c = 0; c < C::QB; ++c) {
+                tma_load_4d(sbase + C::KV_OFF_K1 + c * C::RBOX, &tk1, bar_res, 64 * c, hk, kt * C::BM, b);
+                if (!V2) tma_load_4d(sbase + C::KV_OFF_K2 + c * C::RBOX, &tk2, bar_res, 64 * c, hk, kt * C::BM, b);
+            }
+#pragma unroll
+            for (int c = 0; c < C::VB; ++c)
+                tma_load_4d(sbase + C::KV_OFF_V + c * C::RBOX, &tv, bar_res, 64 * c, hk, kt * C::BM, b);
+        }
+        bool ok = true;
+        int it = 0;
+        for (; ok && it < n_items; ++it) {
+            const int st = it % C::STAGES;
+            if (it >= C::STAGES)
+                ok = warp_wait(bar_empty + 8 * st, static_cast<uint32_t>((it / C::STAGES - 1) & 1), p.err, ok);
+            if (!ok) break;
+            const int hp = item_head(it), qs = item_qs(it);
+            const uint32_t dst = sbase + C::KV_OFF_RING + st * C::KV_STAGE;
+            if (lane == 0) {
+                const int hq1 = V2 ? 2 * hp : hp, hq2 = V2 ? 2 * hp + 1 : hp;
+                mbar_arrive_expect_tx(bar_full + 8 * st, C::KV_STAGE_TMA);
+#pragma unroll
+                for (int c = 0; c < C::QB; ++c) {
+                    tma_load_4d(dst + c * C::CBOX, &tq1, bar_full + 8 * st, 64 * c, hq1, qs * C::BN, b);
+                    tma_load_4d(dst + (C::QB + c) * C::CBOX, &tq2, bar_full + 8 * st, 64 * c, hq2, qs * C::BN, b);
+                }
+#pragma unroll
+                for (int c = 0; c < C::VB; ++c)
+                    tma_load_4d(dst + (2 * C::QB + c) * C::CBOX, &tg, bar_full + 8 * st, 64 * c, hp, qs * C::BN, b);
+            }
+            // row vectors of the 64 query rows: lse (+inf past T so that P = 0), D, c
+            float *vec = reinterpret_cast<float *>(smem + (dst - sbase) + C::KV_STAGE_TMA);
+#pragma unroll
+            for (int r2 = 0; r2 < 2; ++r2) {
+                const int r = lane + 32 * r2;
+                const int tq = qs * C::BN + r;
+                const bool live = tq < p.T;
+                const int64_t vi = (static_cast<int64_t>(b) * p.H + hp) * p.T + tq;
+                vec[r] = live ? p.lse[vi] : INFINITY;
+                vec[64 + r] = live ? p.lse[vstride + vi] : INFINITY;
+                vec[128 + r] = live ? p.dd[vi] : 0.f;
+                vec[192 + r] = live ? p.dd[vstride + vi] : 0.f;
+                vec[256 + r] = live ? p.cv[vi] : 0.f;
+            }
+            mbar_arrive(bar_full + 8 * st);   // release: the vectors are visible to the waiters
+        }
+        // leave no copy in flight
+        if (lane == 0) {
+            mbar_wait(bar_res, 0, p.err);
+            for (int k = (it > C::STAGES ? it - C::STAGES : 0); k < it; ++k)
+                mbar_wait(bar_full + 8 * (k % C::STAGES), static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            const uint32_t sK1 = sbase + C::KV_OFF_K1, sK2 = V2 ? sK1 : sbase + C::KV_OFF_K2;
+            const uint32_t sV = sbase + C::KV_OFF_V;
+            bool ok = mbar_wait(bar_res, 0, p.err);
+            for (int it = 0; ok && it < n_items; ++it) {
+                const int st = it % C::STAGES;
+                const uint32_t sQ1 = sbase + C::KV_OFF_RING + st * C::KV_STAGE;
+                const uint32_t sQ2 = sQ1 + C::QB * C::CBOX, sG = sQ1 + 2 * C::QB * C::CBOX;
+                ok = mbar_wait(bar_full + 8 * st, static_cast<uint32_t>((it / C::STAGES) & 1), p.err);
+                if (!ok) break;
+                tc_fence_after();
+                // S_b^T = K_b Q_b^T (N = 64 queries), dP^T = V G^T
+                {
+                    const uint64_t a1 = sdesc_sw128(sK1, 16, 1024), a2 = sdesc_sw128(sK2, 16, 1024);
+                    const uint64_t b1 = sdesc_sw128(sQ1, 16, 1024), b2 = sdesc_sw128(sQ2, 16, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < DQK / 16; ++ks) {
+                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                        mma_ss(tmem + C::COL_S1, a1 + oa, b1 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                        mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    }
+                    const uint64_t av = sdesc_sw128(sV, 16, 1024), bg = sdesc_sw128(sG, 16, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < DV / 16; ++ks) {
+                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                        mma_ss(tmem + C::COL_DP, av + oa, bg + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar_s);
+                ok = mbar_wait(bar_p, static_cast<uint32_t>(it & 1), p.err);
+                if (!ok) break;
+                tc_fence_after();
+                // dV += P~^T G; dK_b += dS_b^T Q_b (A from TMEM, B MN-major over the 64 query rows)
+                {
+                    const uint64_t gdesc = sdesc_sw128(sG, C::CBOX, 1024);
+                    const uint64_t q1d = sdesc_sw128(sQ1, C::CBOX, 1024), q2d = sdesc_sw128(sQ2, C::CBOX, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < C::BN / 16; ++ks) {
+                        const uint32_t ob = (ks * 2048) >> 4;
+                        const uint32_t first = (it > 0 || ks > 0) ? 1u : 0u;
+                        mma_ts(tmem + C::COL_DV, tmem + C::COL_S1 + ks * 8, gdesc + ob, C::IDESC_V, first);
+                        mma_ts(tmem + C::COL_DK1, tmem + C::COL_S2 + ks * 8, q1d + ob, C::IDESC_QK, first);
+                        mma_ts(tmem + C::COL_DK2, tmem + C::COL_DP + ks * 8, q2d + ob, C::IDESC_QK,
+                               V2 ? 1u : first);
+                    }
+                }
+                mma_commit(bar_empty + 8 * st);
+            }
+            mma_commit(bar_done);
+            mma_commit(bar_dr);
+            mbar_wait(bar_dr, 0, p.err);
+        }
+    } else if (warp >= 4) {
+        // -------------------------------------------------- rows (key j)
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const int j = kt * C::BM + row;
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < n_items; ++it) {
+            const int st = it % C::STAGES;
+            ok = warp_wait(bar_s, static_cast<uint32_t>(it & 1), p.err, ok);
+            // the stage's row vectors were written by warp 0 before it arrived on
+            // the stage's full barrier: acquire them there (that phase is complete)
+            ok = warp_wait(bar_full + 8 * st, static_cast<uint32_t>((it / C::STAGES) & 1), p.err, ok);
+            if (ok) {
+                tc_fence_after();
+                const float *vec =
+                    reinterpret_cast<const float *>(smem + C::KV_OFF_RING + st * C::KV_STAGE + C::KV_STAGE_TMA);
+                const int q0 = item_qs(it) * C::BN;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t s1[32], s2[32], dp[32];
+                    tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * hh, s1);
+                    tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * hh, s2);
+                    tmem_ld32(tmem + lane_off + C::COL_DP + 32 * hh, dp);
+                    tmem_wait_ld();
+                    // in place: s1 <- P~ = P1 + c P2, s2 <- dS1, dp <- dS2
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int q = 32 * hh + c;
+                        const bool valid = q0 + q >= j;   // key j <= query q0 + q; rows past T carry lse = +inf
+                        const float dpv = __uint_as_float(dp[c]);
+                        const float cq = vec[256 + q];
+                        const float p1 = valid ? ex2(__uint_as_float(s1[c]) * sl2 - vec[q]) : 0.f;
+                        const float p2 = valid ? ex2(__uint_as_float(s2[c]) * sl2 - vec[64 + q]) : 0.f;
+                        s1[c] = __float_as_uint(fmaf(cq, p2, p1));
+                        s2[c] = __float_as_uint(p1 * (dpv - vec[128 + q]));
+                        dp[c] = __float_as_uint(p2 * (cq * dpv - vec[192 + q]));
+                    }
+                    uint32_t u[16];
+                    pack32(s1, u);
+                    tmem_st16(tmem + lane_off + C::COL_S1 + 16 * hh, u);
+                    pack32(s2, u);
+                    tmem_st16(tmem + lane_off + C::COL_S2 + 16 * hh, u);
+                    pack32(dp, u);
+                    tmem_st16(tmem + lane_off + C::COL_DP + 16 * hh, u);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p);
+        }
+        // epilogue: dK_b * scale, dV -> bf16 rows of key j
+        ok = warp_wait(bar_done, 0, p.err, ok);
+        tc_fence_after();
+        if (ok) {
+            const bool live = j < p.T;
+            auto store = [&](int col, int n, __nv_bfloat16 *dst, float f) {
+                for (int c0 = 0; c0 < n; c0 += 32) {
+                    uint32_t a[32];
+                    tmem_ld32(tmem + lane_off + col + c0, a);
+                    tmem_wait_ld();
+                    if (live) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const uint32_t *aa = a + 8 * q8;
+                            d4[q8] = make_uint4(pack_bf16(__uint_as_float(aa[0]) * f, __uint_as_float(aa[1]) * f),
+                                                pack_bf16(__uint_as_float(aa[2]) * f, __uint_as_float(aa[3]) * f),
+                                                pack_bf16(__uint_as_float(aa[4]) * f, __uint_as_float(aa[5]) * f),
+                                                pack_bf16(__uint_as_float(aa[6]) * f, __uint_as_float(aa[7]) * f));
+                        }
+                    }
+                }
+            };
+            const int64_t krow = b * p.k_sb + static_cast<int64_t>(j) * p.k_st + static_cast<int64_t>(hk) * p.k_sh;
+            store(C::COL_DK1, DQK, p.dk1 + krow, p.scale);
+            if (!V2) store(C::COL_DK2, DQK, p.dk2 + krow, p.scale);
+            store(C::COL_DV, DV, p.dv + b * p.v_sb + static_cast<int64_t>(j) * p.v_st + static_cast<int64_t>(hk) * p.v_sh,
+                  1.f);
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ================================================================ row pass
+// One warp per row: b, t, head (V1) / pair (V2).
+//   V1: x = a1 - lam a2 (saved by the forward), r = (mean(x^2) + 1e-5)^(-1/2), y = x r,
+//       dy = (1 - lam_init) dout, dx = r (dy - y mean(dy y));
+//       g = dx (bf16), D1 = dx . a1, D2 = -lam dx . a2, row share of
+//       dL/dlam = -dx . a2.
+//   V2: D1 = dout . a_e, D2 = -s dout . a_o, c = -s, dL/dlam = -s (1 - s)
+//       dout . a_o with s = sigmoid(lam[t]).
+template <int DV, bool V2>
+__global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
+    constexpr int PER = DV / 32;   // channels per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int64_t nrows = static_cast<int64_t>(p.B) * p.T * p.H;
+    if (r >= nrows) return;
+    const int h = static_cast<int>(r % p.H);
+    const int t = static_cast<int>((r / p.H) % p.T);
+    const int b = static_cast<int>(r / (static_cast<int64_t>(p.H) * p.T));
+    const __nv_bfloat16 *go = p.dout + b * p.o_sb + static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh;
+    // V2: x1, x2 = a_e, a_o (bf16 saved); V1: x1 = x (RMSNorm input), x2 = a2 (fp32 saved)
+    float x1[PER], x2[PER], dy[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int c = lane + 32 * i;
+        if (V2) {
+            x1[i] = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.sa1)[r * DV + c]);
+            x2[i] = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.sa2)[r * DV + c]);
+        } else {
+            x1[i] = static_cast<const float *>(p.sa1)[r * DV + c];
+            x2[i] = static_cast<const float *>(p.sa2)[r * DV + c];
+        }
+        dy[i] = __bfloat162float(go[c]);
+    }
+    const int64_t vi = (static_cast<int64_t>(b) * p.H + h) * p.T + t;
+    const int64_t vstride = nrows;
+    if (V2) {
+        float e = 0.f, o = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            e = fmaf(dy[i], x1[i], e);
+            o = fmaf(dy[i], x2[i], o);
+        }
+        e = warp_sum(e);
+        o = warp_sum(o);
+        if (lane == 0) {
+            const float s = 1.f / (1.f + expf(-p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h]));
+            p.dd[vi] = e;
+            p.dd[vstride + vi] = -s * o;
+            p.cv[vi] = -s;
+            p.dlam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] = -s * (1.f - s) * o;
+        }
+    } else {
+        // lam_init = 0.8 - 0.6 exp(-0.3 layer); lam = exp(lq1 . lk1) - exp(lq2 . lk2) + lam_init
+        float s1 = 0.f, s2 = 0.f;
+        for (int c = lane; c < p.d; c += 32) {
+            s1 = fmaf(p.lq1[c], p.lk1[c], s1);
+            s2 = fmaf(p.lq2[c], p.lk2[c], s2);
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        const float lam_init = 0.8f - 0.6f * expf(-0.3f * static_cast<float>(p.layer_index));
+        const float lam = expf(s1) - expf(s2) + lam_init;
+        // x as the forward normalised it; a1 = x + lam a2
+        float x[PER], ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            x[i] = x1[i];
+            x1[i] = fmaf(lam, x2[i], x[i]);
+            ss = fmaf(x[i], x[i], ss);
+            dy[i] *= (1.f - lam_init);
+        }
+        ss = warp_sum(ss);
+        const float rr = rsqrtf(ss / static_cast<float>(DV) + 1e-5f);
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) m = fmaf(dy[i], x[i] * rr, m);
+        m = warp_sum(m) / static_cast<float>(DV);
+        float d1 = 0.f, d2 = 0.f, dl = 0.f;
+        __nv_bfloat16 *g = p.g + r * DV;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const float dx = rr * (dy[i] - x[i] * rr * m);
+            // D is formed from the bf16 g that the dP product will use, so
+            // that dP - D cancels where it should (one key: dP = D exactly)
+            const __nv_bfloat16 gb = __float2bfloat16_rn(dx);
+            const float gr = __bfloat162float(gb);
+            d1 = fmaf(gr, x1[i], d1);
+            d2 = fmaf(gr, x2[i], d2);
+            dl = fmaf(dx, x2[i], dl);
+            g[lane + 32 * i] = gb;
+        }
+        d1 = warp_sum(d1);
+        d2 = warp_sum(d2);
+        dl = warp_sum(dl);
+        if (lane == 0) {
+            p.dd[vi] = d1;
+            p.dd[vstride + vi] = -lam * d2;
+            p.cv[vi] = -lam;
+            p.dlam_rows[r] = -dl;
+        }
+    }
+}
+
+// V1: dL/dlam = sum of the row shares (one CTA, fixed order), then the
+// lambda-vector gradients dlq1 = dlam e1 lk1, dlk1 = dlam e1 lq1,
+// dlq2 = -dlam e2 lk2, dlk2 = -dlam e2 lq2 with e_b = exp(lq_b . lk_b).
+__global__ void __launch_bounds__(1024) bwd_lambda(const BwdPreParams p) {
+    __shared__ float red[32];
+    const int64_t n = static_cast<int64_t>(p.B) * p.T * p.H;
+    float acc = 0.f;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) acc += p.dlam_rows[i];
+    acc = warp_sum(acc);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    float dlam = 0.f;
+    for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) dlam += red[k];
+    float s1 = 0.f, s2 = 0.f;
+    for (int c = 0; c < p.d; ++c) {
+        s1 = fmaf(p.lq1[c], p.lk1[c], s1);
+        s2 = fmaf(p.lq2[c], p.lk2[c], s2);
+    }
+    const float e1 = expf(s1), e2 = expf(s2);
+    for (int c = threadIdx.x; c < p.d; c += blockDim.x) {
+        p.dlq1[c] = dlam * e1 * p.lk1[c];
+        p.dlk1[c] = dlam * e1 * p.lq1[c];
+        p.dlq2[c] = -dlam * e2 * p.lk2[c];
+        p.dlk2[c] = -dlam * e2 * p.lq2[c];
+    }
+}
+
+template <int DQK, int DV, bool V2>
+cudaError_t launch_bwd_t(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, cudaStream_t s) {
+    using C = BwdCfg<DQK, DV, V2>;
+    static bool attr_set = false;   // per process; the attribute is per function
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_dq<DQK, DV, V2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::DQ_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bwd_dkdv<DQK, DV, V2>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KV_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int64_t rows = static_cast<int64_t>(pp.B) * pp.T * pp.H;
+    const int64_t pre_blocks = (rows + 7) / 8;
+    if (pre_blocks < 1 || pre_blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    bwd_pre<DV, V2><<<static_cast<unsigned>(pre_blocks), 256, 0, s>>>(pp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (!V2) {
+        bwd_lambda<<<1, 1024, 0, s>>>(pp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t dq_tiles = static_cast<int64_t>((p.T + C::BM - 1) / C::BM) * p.H * p.B;
+    const int64_t kv_tiles = static_cast<int64_t>((p.T + C::BM - 1) / C::BM) * (V2 ? p.Hkv : p.H) * p.B;
+    if (dq_tiles > 0x7fffffff || kv_tiles > 0x7fffffff) return cudaErrorInvalidValue;
+    bwd_dkdv<DQK, DV, V2><<<static_cast<unsigned>(kv_tiles), C::THREADS, C::KV_SMEM, s>>>(m.k1r, m.k2r, m.vr, m.q1c,
+                                                                                          m.q2c, m.gc, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dq<DQK, DV, V2><<<static_cast<unsigned>(dq_tiles), C::THREADS, C::DQ_SMEM, s>>>(m.q1r, m.q2r, m.gr, m.k1c,
+                                                                                       m.k2c, m.vc, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool backward_supported(int dqk, int dv, bool v2) {
+    if (v2) return (dqk == 128 && dv == 128) || (dqk == 64 && dv == 64);
+    return dqk == 64 && dv == 128;
+}
+
+cudaError_t launch_backward(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, int dqk, int dv, bool v2,
+                            cudaStream_t s) {
+    if (v2 && dqk == 128 && dv == 128) return launch_bwd_t<128, 128, true>(m, p, pp, s);
+    if (v2 && dqk == 64 && dv == 64) return launch_bwd_t<64, 64, true>(m, p, pp, s);
+    if (!v2 && dqk == 64 && dv == 128) return launch_bwd_t<64, 128, false>(m, p, pp, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace da

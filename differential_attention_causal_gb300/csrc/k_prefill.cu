@@ -118,7 +118,7 @@ __device__ __forceinline__ int snake_tile(int k, int c, int G, int NT) {
     return w < NT ? w : -1;
 }
 
-template <int DQK, int DV, bool V2>
+template <int DQK, int DV, bool V2, bool TRAIN>
 __global__ void __launch_bounds__(384, 1)
     prefill_onepass(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
                     const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
@@ -460,6 +460,8 @@ __global__ void __launch_bounds__(384, 1)
             // --------------------------------------------------- epilogue
             ok = warp_wait(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
             tc_fence_after();
+            if (TRAIN && t < p.T)   // this branch's log-sum-exp (log2 units) for the backward
+                p.slse[((static_cast<int64_t>(br) * p.B + b) * p.H + h) * p.T + t] = m_ref + __log2f(l);
             xch[br * 128 + row] = l;
             named_bar_sync(1, 256);   // both branches' final O are complete past this point
             tc_fence_after();
@@ -481,6 +483,39 @@ __global__ void __launch_bounds__(384, 1)
                     const float v = __uint_as_float(a[kk]) * c1 - __uint_as_float(bb[kk]) * c2;
                     x[cc + kk] = v;
                     ss = fmaf(v, v, ss);
+                }
+                if (TRAIN && !V2 && t < p.T) {
+                    // V1: x (the RMSNorm input) and a2 = O2 / l2 in fp32, channels col0 + cc .. + 31
+                    const float i2 = 1.f / l2;
+                    const int64_t off = ((static_cast<int64_t>(b) * p.T + t) * p.H + h) * DV + col0 + cc;
+                    float4 *d1 = reinterpret_cast<float4 *>(static_cast<float *>(p.sa1) + off);
+                    float4 *d2 = reinterpret_cast<float4 *>(static_cast<float *>(p.sa2) + off);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        d1[q4] = make_float4(x[cc + 4 * q4], x[cc + 4 * q4 + 1], x[cc + 4 * q4 + 2], x[cc + 4 * q4 + 3]);
+                        d2[q4] = make_float4(__uint_as_float(bb[4 * q4]) * i2, __uint_as_float(bb[4 * q4 + 1]) * i2,
+                                             __uint_as_float(bb[4 * q4 + 2]) * i2,
+                                             __uint_as_float(bb[4 * q4 + 3]) * i2);
+                    }
+                }
+                if (TRAIN && V2 && t < p.T) {
+                    // V2: a_b = O_b / l_b of this row's channels col0 + cc .. + 31, both heads, bf16
+                    const float i2 = 1.f / l2;
+                    const int64_t off = ((static_cast<int64_t>(b) * p.T + t) * p.H + h) * DV + col0 + cc;
+                    uint4 *d1 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.sa1) + off);
+                    uint4 *d2 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.sa2) + off);
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const uint32_t *aa = a + 8 * q8, *bq = bb + 8 * q8;
+                        d1[q8] = make_uint4(pack_bf16(__uint_as_float(aa[0]) * c1, __uint_as_float(aa[1]) * c1),
+                                            pack_bf16(__uint_as_float(aa[2]) * c1, __uint_as_float(aa[3]) * c1),
+                                            pack_bf16(__uint_as_float(aa[4]) * c1, __uint_as_float(aa[5]) * c1),
+                                            pack_bf16(__uint_as_float(aa[6]) * c1, __uint_as_float(aa[7]) * c1));
+                        d2[q8] = make_uint4(pack_bf16(__uint_as_float(bq[0]) * i2, __uint_as_float(bq[1]) * i2),
+                                            pack_bf16(__uint_as_float(bq[2]) * i2, __uint_as_float(bq[3]) * i2),
+                                            pack_bf16(__uint_as_float(bq[4]) * i2, __uint_as_float(bq[5]) * i2),
+                                            pack_bf16(__uint_as_float(bq[6]) * i2, __uint_as_float(bq[7]) * i2));
+                    }
                 }
             }
             // O has been read: the next tile's first PV may overwrite it
@@ -535,7 +570,7 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int DQK, int DV, bool V2>
+template <int DQK, int DV, bool V2, bool TRAIN>
 cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
     using C = PreCfg<DQK, DV, V2>;
     int dev = 0;
@@ -546,10 +581,10 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
         // grants (384 threads x registers per thread), or its increase would
         // never complete: refuse to launch otherwise.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_onepass<DQK, DV, V2>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_onepass<DQK, DV, V2, TRAIN>);
         if (e != cudaSuccess) return e;
         if (C::REG_SPLIT && fa.numRegs < C::REGS_NEEDED_AT_LAUNCH) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2, TRAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
@@ -567,7 +602,7 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
     }
     const int sms = dev < 64 ? num_sms[dev] : 1;
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    prefill_onepass<DQK, DV, V2><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, m.out, p);
+    prefill_onepass<DQK, DV, V2, TRAIN><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, m.out, p);
     return cudaGetLastError();
 }
 
@@ -580,9 +615,18 @@ bool prefill_supported(int dqk, int dv, bool v2) {
 
 cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
                            cudaStream_t s) {
-    if (v2 && dqk == 128 && dv == 128) return launch_t<128, 128, true>(m, p, s);
-    if (v2 && dqk == 64 && dv == 64) return launch_t<64, 64, true>(m, p, s);
-    if (!v2 && dqk == 64 && dv == 128) return launch_t<64, 128, false>(m, p, s);
+    if (v2 && dqk == 128 && dv == 128) return launch_t<128, 128, true, false>(m, p, s);
+    if (v2 && dqk == 64 && dv == 64) return launch_t<64, 64, true, false>(m, p, s);
+    if (!v2 && dqk == 64 && dv == 128) return launch_t<64, 128, false, false>(m, p, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_train(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
+                                 cudaStream_t s) {
+    if (!p.sa1 || !p.sa2 || !p.slse) return cudaErrorInvalidValue;
+    if (v2 && dqk == 128 && dv == 128) return launch_t<128, 128, true, true>(m, p, s);
+    if (v2 && dqk == 64 && dv == 64) return launch_t<64, 64, true, true>(m, p, s);
+    if (!v2 && dqk == 64 && dv == 128) return launch_t<64, 128, false, true>(m, p, s);
     return cudaErrorInvalidValue;
 }
 

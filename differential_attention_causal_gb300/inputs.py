@@ -180,6 +180,13 @@ def make_v1_decode(s: V1DecodeShape, seed: int = 0, device="cpu") -> dict:
     return out
 
 
+def make_grad_out(shape, dtype: str = "bf16", seed: int = 0, device="cpu") -> torch.Tensor:
+    """Upstream gradient dL/dout ~ N(0, 1) of the given output shape, drawn in
+    fp32 with its own generator (seed + 1000003) and rounded to dtype."""
+    g = _gen(int(seed) + 1000003, device)
+    return _normal(tuple(shape), 1.0, _DT[dtype], g, device)
+
+
 def make(shape, seed: int = 0, device="cpu") -> dict:
     if isinstance(shape, V1Shape):
         return make_v1(shape, seed, device)

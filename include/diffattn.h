@@ -19,6 +19,13 @@
  *                       operation for one new query token per sequence against an
  *                       L-row KV cache (the token attends all L rows).
  *   diffattn_v2_decode_varlen  the same with a cache length per sequence.
+ *   diffattn_v1_fwd_train / diffattn_v2_fwd_train, diffattn_v1_bwd /
+ *   diffattn_v2_bwd     the same forwards saving what their gradients need,
+ *                       and the gradients of DiffAttnV1 (q1, q2, k1, k2, v and
+ *                       the four lambda vectors) and DiffAttnV2 (q, k, v and
+ *                       the lambda logits) for an upstream gradient dout; the
+ *                       pages train these models, the backward is the chain
+ *                       rule of the same definitions.
  *   diffattn_v1_decode  DiffAttnV1 for one new query token per sequence against
  *                       cached k1, k2, v rows (all L, or a length per sequence);
  *                       the remark names V1 decoding as the case that needs
@@ -201,6 +208,63 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
                              const int32_t *cache_lens, void *out, void *workspace,
                              size_t workspace_bytes, int B, int L, int H, int d, int layer_index,
                              da_dtype dtype, cudaStream_t stream);
+
+/* ---- training: forward with saved tensors, and the backward -----------
+ * Supported: DA_BF16 only; V1 d = 64 (dv = 128), V2 D in {64, 128}; other
+ * combinations return DA_ERR_UNSUPPORTED_DIM.
+ *
+ * `saved` (DEVICE, caller-owned, at least *_train_saved_size() bytes,
+ * 16-byte aligned) receives each branch's normalised attention output a_b
+ * (bf16) and its log-sum-exp (fp32); its contents are private to this
+ * library: pass it unchanged to the matching *_bwd call.  The forward output
+ * is the same as the plain forward's.  `workspace` (DEVICE, at least
+ * *_bwd_workspace_size() bytes) is scratch for the backward; contents on
+ * entry are ignored.  Gradient outputs must not overlap any input; they are
+ * fully overwritten (not accumulated into).  Sizes functions return 0 for
+ * unsupported sizes. */
+size_t diffattn_v1_train_saved_size(int B, int T, int H, int d);
+size_t diffattn_v1_bwd_workspace_size(int B, int T, int H, int d);
+size_t diffattn_v2_train_saved_size(int B, int T, int Hq, int Hkv, int D);
+size_t diffattn_v2_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D);
+
+/* DIFF V1 training forward: arguments, layouts and strides as
+ * diffattn_v1_fwd, plus `saved`. */
+da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, const void *k2,
+                                const void *v, const float *lam_q1, const float *lam_k1,
+                                const float *lam_q2, const float *lam_k2, void *out, void *saved,
+                                size_t saved_bytes, int B, int T, int H, int d, int layer_index,
+                                int64_t q_sb, int64_t q_st, int64_t q_sh, int64_t k_sb,
+                                int64_t k_st, int64_t k_sh, int64_t v_sb, int64_t v_st,
+                                int64_t v_sh, int64_t o_sb, int64_t o_st, int64_t o_sh,
+                                da_dtype dtype, cudaStream_t stream);
+
+/* DIFF V1 backward.  Inputs as the training forward that filled `saved`;
+ * dout has the output's strides (o_*).  dq1, dq2 take q's strides, dk1, dk2
+ * k's, dv v's (bf16).  dlam_q1 .. dlam_k2: fp32 (d) gradients of the lambda
+ * vectors. */
+da_status diffattn_v1_bwd(const void *q1, const void *q2, const void *k1, const void *k2,
+                          const void *v, const float *lam_q1, const float *lam_k1,
+                          const float *lam_q2, const float *lam_k2, const void *dout,
+                          const void *saved, size_t saved_bytes, void *dq1, void *dq2, void *dk1,
+                          void *dk2, void *dv, float *dlam_q1, float *dlam_k1, float *dlam_q2,
+                          float *dlam_k2, void *workspace, size_t workspace_bytes, int B, int T,
+                          int H, int d, int layer_index, int64_t q_sb, int64_t q_st, int64_t q_sh,
+                          int64_t k_sb, int64_t k_st, int64_t k_sh, int64_t v_sb, int64_t v_st,
+                          int64_t v_sh, int64_t o_sb, int64_t o_st, int64_t o_sh, da_dtype dtype,
+                          cudaStream_t stream);
+
+/* DIFF V2 training forward: as diffattn_v2_fwd, plus `saved`. */
+da_status diffattn_v2_fwd_train(const void *q, const void *k, const void *v, const float *lam,
+                                void *out, void *saved, size_t saved_bytes, int B, int T, int Hq,
+                                int Hkv, int D, da_dtype dtype, cudaStream_t stream);
+
+/* DIFF V2 backward.  dout (B, T, Hq/2, D) contiguous; dq (B, T, Hq, D), dk, dv
+ * (B, T, Hkv, D) bf16 contiguous; dlam (B, T, Hq/2) fp32 gradient of the
+ * lambda logits. */
+da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const float *lam,
+                          const void *dout, const void *saved, size_t saved_bytes, void *dq,
+                          void *dk, void *dv, float *dlam, void *workspace, size_t workspace_bytes,
+                          int B, int T, int Hq, int Hkv, int D, da_dtype dtype, cudaStream_t stream);
 
 /* Static string for a status code (never NULL). */
 const char *diffattn_status_string(da_status s);

@@ -71,7 +71,7 @@ def _load():
             lib.oracle_v2_decode.argtypes = ([dp] * 4 + [ctypes.c_int, ctypes.c_int64] + [ctypes.c_int] * 3
                                              + [i64p, i64p, ctypes.c_int64, dp, ctypes.c_int])
             lib.oracle_v1_bwd.restype = ctypes.c_int
-            lib.oracle_v1_bwd.argtypes = ([dp] * 10 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64] + [dp] * 6
+            lib.oracle_v1_bwd.argtypes = ([dp] * 10 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64] + [dp] * 7
                                           + [ctypes.c_int])
             lib.oracle_v2_bwd.restype = ctypes.c_int
             lib.oracle_v2_bwd.argtypes = ([dp] * 5 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64] + [dp] * 4
@@ -237,8 +237,9 @@ def v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, layer_index: int, dout, heads=
            nthreads: int | None = None) -> dict:
     """Gradients of the DIFF V1 forward for upstream gradient dout (B, T, H, 2d).
 
-    Returns dq1, dq2, dk1, dk2 (B, T, H, d), dv (B, T, H, 2d) and dlam_q1,
-    dlam_k1, dlam_q2, dlam_k2 (d,).  heads: optional ids b*H + h; then only
+    Returns dq1, dq2, dk1, dk2 (B, T, H, d), dv (B, T, H, 2d), dlam_q1,
+    dlam_k1, dlam_q2, dlam_k2 (d,) and dlam_abs, the sum of |dx_c a2_c| over
+    the terms of dL/dlam = -sum dx_c a2_c (a scale for rounding errors).  heads: optional ids b*H + h; then only
     those heads' gradients are filled (the rest stay 0) and the lambda-vector
     gradients hold only those heads' share.
     """
@@ -252,13 +253,15 @@ def v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, layer_index: int, dout, heads=
     g = {n: np.zeros(sh, dtype=np.float64) for n, sh in
          (("dq1", q1.shape), ("dq2", q1.shape), ("dk1", q1.shape), ("dk2", q1.shape), ("dv", v.shape))}
     dl = np.zeros(4 * d, dtype=np.float64)
+    da = np.zeros(1, dtype=np.float64)
     rc = _load().oracle_v1_bwd(_ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v), _ptr(lq1), _ptr(lk1), _ptr(lq2),
                                _ptr(lk2), _ptr(dout), B, T, H, d, int(layer_index), hp,
                                0 if hs is None else hs.size, _ptr(g["dq1"]), _ptr(g["dq2"]), _ptr(g["dk1"]),
-                               _ptr(g["dk2"]), _ptr(g["dv"]), _ptr(dl), nthreads or default_threads())
+                               _ptr(g["dk2"]), _ptr(g["dv"]), _ptr(dl), _ptr(da), nthreads or default_threads())
     if rc:
         raise RuntimeError(f"oracle_v1_bwd failed ({rc})")
     g.update(dlam_q1=dl[:d], dlam_k1=dl[d:2 * d], dlam_q2=dl[2 * d:3 * d], dlam_k2=dl[3 * d:])
+    g["dlam_abs"] = float(da[0])   # sum |dx_c a2_c|: the scale of the terms cancelling in dL/dlam
     return g
 
 

@@ -457,6 +457,7 @@ typedef struct {
     const int64_t *units;     /* V1: head ids b*H+h; V2: group ids b*Hkv+g */
     int64_t nunits;
     double *dq1, *dq2, *dk1, *dk2, *dvv, *dlam;   /* dlam: V1 one partial per unit, V2 (B,T,Hq/2) */
+    double *dlam_abs;         /* V1: per unit, sum over rows and channels of |dx_c a2_c| */
     int tid, nthreads;
 } bjob_t;
 
@@ -472,7 +473,7 @@ static void v1_head_bwd(const bjob_t *J, int64_t u, int64_t slot, double *p,
     double *a1 = buf, *a2 = buf + dvd, *x = buf + 2 * dvd, *dx = buf + 3 * dvd;
     double *g2 = buf + 4 * dvd;
     const int64_t kbase = (int64_t)b * T * H + h;
-    double dlam = 0.0;
+    double dlam = 0.0, dlam_abs = 0.0;
     for (int t = 0; t < T; ++t) {
         const int64_t row = ((int64_t)b * T + t) * H + h;
         const double *q1 = J->q1 + row * d, *q2 = J->q2 + row * d;
@@ -493,6 +494,7 @@ static void v1_head_bwd(const bjob_t *J, int64_t u, int64_t slot, double *p,
             dx[c] = r * dy - r * r * r * x[c] * xdy / (double)dvd;
             g2[c] = -J->lam_full * dx[c];
             xa2 += dx[c] * a2[c];
+            dlam_abs += fabs(dx[c] * a2[c]);
         }
         dlam -= xa2;
         attend_row_bwd(q1, J->k1 + kbase * d, qk_row, J->v + kbase * dvd, v_row, (int64_t)t + 1, d, dvd, scale,
@@ -501,6 +503,7 @@ static void v1_head_bwd(const bjob_t *J, int64_t u, int64_t slot, double *p,
                        g2, p, dp, J->dq2 + row * d, J->dk2 + kbase * d, J->dvv + kbase * dvd);
     }
     J->dlam[slot] = dlam;
+    J->dlam_abs[slot] = dlam_abs;
 }
 
 /* V2 kv group (b, g): the pairs whose heads read kv head g, every row t. */
@@ -597,14 +600,18 @@ static int run_bwd_jobs(const bjob_t *proto, int nthreads)
  * heads: ids b*H+h to differentiate (NULL = all); gradients are written for
  * those heads only (dq1, dq2, dk1, dk2 (B,T,H,d), dv (B,T,H,2d), zeroed by
  * the caller).  dlam_vec: 4*d doubles (dlq1, dlk1, dlq2, dlk2) from the
- * listed heads' contribution to dL/dlam.  Returns 0 on success. */
+ * listed heads' contribution to dL/dlam.  dlam_abs_out: the sum of
+ * |dx_c a2_c| behind dL/dlam = -sum dx_c a2_c (the size of the terms that
+ * cancel in it, a scale for comparing a rounded result).  Returns 0 on
+ * success. */
 int oracle_v1_bwd(const double *q1, const double *q2, const double *k1,
                   const double *k2, const double *v, const double *lq1,
                   const double *lk1, const double *lq2, const double *lk2,
                   const double *dout, int B, int T, int H, int d,
                   int layer_index, const int64_t *heads, int64_t nheads,
                   double *dq1, double *dq2, double *dk1, double *dk2,
-                  double *dv, double *dlam_vec, int nthreads)
+                  double *dv, double *dlam_vec, double *dlam_abs_out,
+                  int nthreads)
 {
     bjob_t J;
     memset(&J, 0, sizeof(J));
@@ -616,7 +623,7 @@ int oracle_v1_bwd(const double *q1, const double *q2, const double *k1,
     J.dq1 = dq1; J.dq2 = dq2; J.dk1 = dk1; J.dk2 = dk2; J.dvv = dv;
     const int64_t n = heads ? nheads : (int64_t)B * H;
     int64_t *ids = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
-    double *part = (double *)calloc((size_t)(n > 0 ? n : 1), sizeof(double));
+    double *part = (double *)calloc((size_t)(n > 0 ? n : 1) * 2, sizeof(double));
     if (!ids || !part) {
         free(ids);
         free(part);
@@ -624,11 +631,14 @@ int oracle_v1_bwd(const double *q1, const double *q2, const double *k1,
     }
     for (int64_t i = 0; i < n; ++i)
         ids[i] = heads ? heads[i] : i;
-    J.units = ids; J.nunits = n; J.dlam = part;
+    J.units = ids; J.nunits = n; J.dlam = part; J.dlam_abs = part + n;
     const int rc = run_bwd_jobs(&J, nthreads);
-    double dlam = 0.0;
-    for (int64_t i = 0; i < n; ++i)
+    double dlam = 0.0, dlam_abs = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
         dlam += part[i];
+        dlam_abs += part[n + i];
+    }
+    *dlam_abs_out = dlam_abs;
     double s1 = 0.0, s2 = 0.0;
     for (int c = 0; c < d; ++c) {
         s1 += lq1[c] * lk1[c];

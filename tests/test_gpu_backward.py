@@ -1,0 +1,126 @@
+"""GPU parity of the backward (training) path through the C ABI against the
+fp64 oracle's gradients, on the same bf16-rounded inputs and upstream
+gradient.  Also: the training forward's output equals the plain forward's.
+
+Tolerance for bf16 gradients (per tensor, against the fp64 oracle):
+relative L2 <= 2e-2 and max abs <= 5e-2 * max|ref| (see the design notes for
+how the bound follows from the bf16 roundings on the path: P and dS fed to
+the tensor cores in bf16, the upstream gradient of branch 1 in bf16).  The
+V1 lambda-vector gradients are one scalar dL/dlam = -sum dx . a2 (times
+fixed vectors), a sum whose terms cancel: its error is bounded against the
+size of those terms, |err| <= 1e-2 * sum |dx_c a2_c| (the oracle reports that
+sum), carried through the same fixed factors.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from differential_attention_causal_gb300 import inputs
+
+from test_gpu_parity import binding, built, to_dev  # noqa: F401  (fixture)
+
+pytestmark = pytest.mark.gpu
+
+RL2, MAXREL = 2e-2, 5e-2
+
+
+def check_grad(name, got, ref, report=None):
+    got = got.detach().float().cpu().numpy().astype(np.float64).reshape(ref.shape)
+    assert np.isfinite(got).all(), name
+    scale = np.abs(ref).max()
+    err = np.abs(got - ref).max()
+    rl2 = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    if report is not None:
+        report[name] = (float(err / max(scale, 1e-30)), float(rl2))
+    assert rl2 <= RL2 and err <= MAXREL * scale, f"{name}: max abs {err:.3e} (ref max {scale:.3e}), rel L2 {rl2:.3e}"
+
+
+def check_lambda_vectors(g, ref, x, report):
+    """dlq1 = dlam e1 lk1, dlk1 = dlam e1 lq1, dlq2 = -dlam e2 lk2, dlk2 = -dlam e2 lq2
+    with e_b = exp(lq_b . lk_b): each element's error is bounded by
+    1e-2 * dlam_abs * e_b * |the fixed factor|."""
+    lv = {k: x[k].double().numpy() for k in ("lam_q1", "lam_k1", "lam_q2", "lam_k2")}
+    e1 = np.exp((lv["lam_q1"] * lv["lam_k1"]).sum())
+    e2 = np.exp((lv["lam_q2"] * lv["lam_k2"]).sum())
+    factors = {"dlam_q1": e1 * lv["lam_k1"], "dlam_k1": e1 * lv["lam_q1"],
+               "dlam_q2": e2 * lv["lam_k2"], "dlam_k2": e2 * lv["lam_q2"]}
+    for n, f in factors.items():
+        got = g[n].detach().double().cpu().numpy()
+        err = np.abs(got - ref[n])
+        bound = 1e-2 * ref["dlam_abs"] * np.abs(f) + 1e-7
+        report[n] = (float((err / bound).max()), float(np.linalg.norm(got - ref[n]) /
+                                                       max(np.linalg.norm(ref[n]), 1e-30)))
+        assert (err <= bound).all(), f"{n}: err / bound = {(err / bound).max():.3f}"
+
+
+def v1_case(B, T, H, seed, layer=12):
+    x = inputs.make_v1(inputs.V1Shape(B, T, H, 64, layer, "bf16"), seed=seed)
+    dout = inputs.make_grad_out((B, T, H, 128), "bf16", seed=seed)
+    return x, dout
+
+
+def run_v1(xd, dout_d, layer):
+    bd = binding()
+    out, saved = bd.v1_fwd_train(xd["q1"], xd["q2"], xd["k1"], xd["k2"], xd["v"], xd["lam_q1"], xd["lam_k1"],
+                                 xd["lam_q2"], xd["lam_k2"], layer)
+    g = bd.v1_bwd(xd["q1"], xd["q2"], xd["k1"], xd["k2"], xd["v"], xd["lam_q1"], xd["lam_k1"], xd["lam_q2"],
+                  xd["lam_k2"], layer, dout_d, saved)
+    return out, g
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 128, 1), (2, 200, 3), (1, 384, 2), (2, 64, 2), (1, 1, 1), (1, 700, 1)])
+def test_v1_backward(B, T, H):
+    x, dout = v1_case(B, T, H, seed=T + B)
+    xd, dd = to_dev(x), dout.cuda()
+    out, g = run_v1(xd, dd, 12)
+    assert binding().device_error() == 0
+    plain = binding().v1_fwd(xd["q1"], xd["q2"], xd["k1"], xd["k2"], xd["v"], xd["lam_q1"], xd["lam_k1"],
+                             xd["lam_q2"], xd["lam_k2"], 12)
+    # the same arithmetic; the training build of the kernel may contract a
+    # multiply-add differently, which can move a bf16 output by one unit
+    assert torch.allclose(out.float(), plain.float(), rtol=2 ** -7, atol=1e-6)
+    ref = oracle.v1_bwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"],
+                        x["lam_k2"], 12, dout)
+    rep = {}
+    for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
+        if T == 1 and n != "dv":
+            # one key: the scores carry no gradient, the oracle's are exactly 0
+            assert g[n].abs().max().item() <= 1e-6
+            continue
+        check_grad(n, g[n], ref[n], rep)
+    check_lambda_vectors(g, ref, x, rep)
+    print(f"V1 B{B} T{T} H{H}", {k: f"{a:.2e}/{b:.2e}" for k, (a, b) in rep.items()})
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,D", [(1, 128, 4, 2, 128), (2, 200, 8, 2, 128), (1, 300, 4, 1, 64),
+                                          (1, 256, 16, 2, 128), (2, 77, 4, 2, 64)])
+def test_v2_backward(B, T, Hq, Hkv, D):
+    s = inputs.V2Shape(B, T, Hq, Hkv, D, "bf16")
+    x = inputs.make_v2(s, seed=T + Hq)
+    dout = inputs.make_grad_out((B, T, Hq // 2, D), "bf16", seed=T)
+    xd, dd = to_dev(x), dout.cuda()
+    bd = binding()
+    out, saved = bd.v2_fwd_train(xd["q"], xd["k"], xd["v"], xd["lam"])
+    assert torch.allclose(out.float(), bd.v2_fwd(xd["q"], xd["k"], xd["v"], xd["lam"]).float(), rtol=2 ** -7,
+                          atol=1e-6)
+    g = bd.v2_bwd(xd["q"], xd["k"], xd["v"], xd["lam"], dd, saved)
+    assert bd.last_launch_count() == 3
+    assert bd.device_error() == 0
+    ref = oracle.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout)
+    rep = {}
+    for n in ("dq", "dk", "dv", "dlam"):
+        check_grad(n, g[n], ref[n], rep)
+    print(f"V2 B{B} T{T} Hq{Hq} Hkv{Hkv} D{D}", {k: f"{a:.2e}/{b:.2e}" for k, (a, b) in rep.items()})
+
+
+def test_backward_argument_checks():
+    bd = binding()
+    assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128) == 0      # d = 128: no backward kernel
+    assert bd.lib().diffattn_v2_bwd_workspace_size(1, 128, 6, 2, 128) > 0
+    x = to_dev(inputs.make_v2(inputs.V2Shape(1, 64, 4, 2, 128, "bf16"), seed=1))
+    out, saved = bd.v2_fwd_train(x["q"], x["k"], x["v"], x["lam"])
+    dout = torch.zeros_like(out)
+    with pytest.raises(bd.DiffAttnError) as e:
+        bd.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout, saved[:1024])
+    assert e.value.code == 6
