@@ -8,8 +8,9 @@ bf16 inputs drawn N(0,1) with a seeded generator.  The line also carries, as
 auxiliary measurements, DIFF V2 prefill (B=8, T=4096, Hq=32, Hkv=8, D=128,
 TFLOP/s), long-context DIFF V1 (B=1, T=32768, 12 heads, d=128, TFLOP/s),
 DIFF V2 decode (B=64, L=32768, Hq=64, Hkv=8, D=128, HBM GB/s), the same decode
-with per-sequence cache lengths uniform on 1..L, and DIFF V1 decode (B=32,
-L=16384, 12 heads, d=128, HBM GB/s).
+with per-sequence cache lengths uniform on 1..L, DIFF V1 decode (B=32,
+L=16384, 12 heads, d=128, HBM GB/s), and the backward (training) pass of the
+V1 headline and V2 prefill workloads (TFLOP/s).
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -61,6 +62,19 @@ def v1_flops(s) -> float:
 def v2_flops(s) -> float:
     """DIFF V2 prefill: per query head and causal pair 2D (QK) + 2D (PV)."""
     return float(s.B) * s.Hq * s.T * (s.T + 1) / 2 * 4 * s.D
+
+
+def v1_bwd_flops(s) -> float:
+    """Algorithmic FLOPs of the DIFF V1 backward: two attention backwards, each
+    per causal pair 2d (S recomputed) + 2*2d (dP) + 2*2d (dV) + 2d (dK) + 2d
+    (dQ) = 14d; 28d per pair."""
+    return float(s.B) * s.H * s.T * (s.T + 1) / 2 * 28 * s.d
+
+
+def v2_bwd_flops(s) -> float:
+    """DIFF V2 backward: per query head and causal pair 2D (S) + 2D (dP) + 2D
+    (dV) + 2D (dK) + 2D (dQ) = 10D."""
+    return float(s.B) * s.Hq * s.T * (s.T + 1) / 2 * 10 * s.D
 
 
 def decode_bytes(s) -> int:
@@ -372,6 +386,46 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                         "tokens_per_s": round(s.B / (ms * 1e-3)), "launches": 2, "peak_kind": peak_kind}
     del x, out, ws
     torch.cuda.empty_cache()
+    # backward (training): DIFF V1 on the headline workload, DIFF V2 on the prefill workload
+    s = inputs.WORKLOADS[HEADLINE]
+    x = inputs.make_v1(s, seed=args.seed, device=dev)
+    dout = inputs.make_grad_out((s.B, s.T, s.H, 2 * s.d), "bf16", seed=args.seed, device=dev)
+    a = (x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"],
+         s.layer_index)
+    _, saved = binding.v1_fwd_train(*a)
+    ws = torch.empty(binding.lib().diffattn_v1_bwd_workspace_size(s.B, s.T, s.H, s.d), dtype=torch.uint8,
+                     device=dev)
+    f = lambda: binding.v1_bwd(*a, dout, saved, workspace=ws)  # noqa: E731
+    for _ in range(3):
+        f()
+    ms = sum(t := time_steps(f, 10, flush)) / len(t)
+    ftr = lambda: binding.v1_fwd_train(*a)  # noqa: E731
+    ms_ft = sum(t := time_steps(ftr, 10, flush)) / len(t)
+    tf = v1_bwd_flops(s) / (ms * 1e-3) / 1e12
+    aux["v1_backward"] = {"workload": HEADLINE, "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                          "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                          "flop_count": "28d per causal pair (two attention backwards)",
+                          "fwd_train_ms": round(ms_ft, 4), "launches": 4, "peak_kind": peak_kind}
+    del x, dout, saved, ws
+    s = inputs.WORKLOADS["v2_bf16_B8_T4096_Hq32_Hkv8_D128"]
+    x = inputs.make_v2(s, seed=args.seed, device=dev)
+    dout = inputs.make_grad_out((s.B, s.T, s.Hq // 2, s.D), "bf16", seed=args.seed, device=dev)
+    _, saved = binding.v2_fwd_train(x["q"], x["k"], x["v"], x["lam"])
+    ws = torch.empty(binding.lib().diffattn_v2_bwd_workspace_size(s.B, s.T, s.Hq, s.Hkv, s.D), dtype=torch.uint8,
+                     device=dev)
+    f = lambda: binding.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout, saved, workspace=ws)  # noqa: E731
+    for _ in range(3):
+        f()
+    ms = sum(t := time_steps(f, 5, flush)) / len(t)
+    ftr = lambda: binding.v2_fwd_train(x["q"], x["k"], x["v"], x["lam"])  # noqa: E731
+    ms_ft = sum(t := time_steps(ftr, 5, flush)) / len(t)
+    tf = v2_bwd_flops(s) / (ms * 1e-3) / 1e12
+    aux["v2_backward"] = {"workload": "v2_bf16_B8_T4096_Hq32_Hkv8_D128", "ms": round(ms, 4),
+                          "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                          "flop_count": "10D per query head and causal pair", "fwd_train_ms": round(ms_ft, 4),
+                          "launches": 3, "peak_kind": peak_kind}
+    del x, dout, saved, ws
+    torch.cuda.empty_cache()
     if binding.device_error():
         raise RuntimeError("a kernel reported a device-side wait timeout")
     return aux
@@ -472,6 +526,9 @@ CASES = {
     "decode_b8": ("decode", None),
     "decode_varlen": ("decode_varlen", "v2_decode_varlen_bf16_B64_L32768_Hq64_Hkv8_D128"),
     "v1_decode": ("v1_decode", "v1_decode_bf16_B32_L16384_H12_d128"),
+    # backward of the headline V1 workload / a quarter of the V2 prefill workload (profiler-sized)
+    "v1_bwd": ("v1_bwd", "v1_bf16_B4_T2048_H16_d64"),
+    "v2_bwd_b2": ("v2_bwd", None),
 }
 
 
@@ -479,7 +536,12 @@ def run_case(name: str, launches: int):
     from differential_attention_causal_gb300 import binding
     kind, wl = CASES[name]
     dev = torch.device("cuda", 0)
-    s = inputs.WORKLOADS[wl] if wl else inputs.DecodeShape(8, 32768, 64, 8, 128, "bf16")
+    if wl:
+        s = inputs.WORKLOADS[wl]
+    elif kind == "v2_bwd":
+        s = inputs.V2Shape(2, 4096, 32, 8, 128, "bf16")
+    else:
+        s = inputs.DecodeShape(8, 32768, 64, 8, 128, "bf16")
     x = inputs.make(s, seed=0, device=dev)
     if kind == "v1":
         f = lambda: binding.v1_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"],  # noqa
@@ -489,6 +551,16 @@ def run_case(name: str, launches: int):
     elif kind == "decode_varlen":
         f = lambda: binding.v2_decode_varlen(x["q"], x["k_cache"], x["v_cache"], x["lam"],  # noqa: E731
                                              x["cache_lens"])
+    elif kind == "v1_bwd":
+        a = (x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"],
+             s.layer_index)
+        dout = inputs.make_grad_out((s.B, s.T, s.H, 2 * s.d), "bf16", seed=0, device=dev)
+        _, saved = binding.v1_fwd_train(*a)
+        f = lambda: binding.v1_bwd(*a, dout, saved)  # noqa: E731
+    elif kind == "v2_bwd":
+        dout = inputs.make_grad_out((s.B, s.T, s.Hq // 2, s.D), "bf16", seed=0, device=dev)
+        _, saved = binding.v2_fwd_train(x["q"], x["k"], x["v"], x["lam"])
+        f = lambda: binding.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout, saved)  # noqa: E731
     elif kind == "v1_decode":
         f = lambda: binding.v1_decode(x["q1"], x["q2"], x["k1_cache"], x["k2_cache"], x["v_cache"],  # noqa
                                       x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"], s.layer_index)

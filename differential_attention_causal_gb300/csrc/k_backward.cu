@@ -25,10 +25,11 @@
 //               every pair of the kv group).  TMEM: S1^T | S2^T | dP^T (64
 //               each) | dK1 (| dK2) | dV.
 // In both, warp 0 streams the sub-tiles with TMA, warp 1 issues the MMAs,
-// warps 4-7 own one TMEM lane (row) each and turn scores into P, dS.  The
-// bf16 results are written over columns the threads have already read
-// (dq: dS1 -> S1, dS2 -> S2; dkdv: P~ -> S1^T, dS1^T -> S2^T, dS2^T -> dP^T)
-// and feed TS MMAs (A from TMEM, B an MN-major shared-memory tile).
+// and two row warpgroups (warps 4-7, 8-11; thread = TMEM lane = row) each
+// turn 32 of a sub-tile's 64 columns of scores into P, dS.  The bf16 results
+// are written over columns the threads have already read (dq: dS1 -> S1,
+// dS2 -> S2; dkdv: P~ -> S1^T, dS1^T -> S2^T, dS2^T -> dP^T) and feed TS
+// MMAs (A from TMEM, B an MN-major shared-memory tile).
 #include "da_common.cuh"
 #include "da_internal.h"
 
@@ -48,7 +49,7 @@ struct BwdCfg {
     static constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false);
     static constexpr uint32_t IDESC_QK = idesc_bf16(128, DQK, true);
     static constexpr uint32_t IDESC_V = idesc_bf16(128, DV, true);
-    static constexpr int THREADS = 256;
+    static constexpr int THREADS = 384;   // warp 0 TMA, warp 1 MMA, warps 4-11 two row warpgroups
     static constexpr int MIN_SMEM = 120 * 1024;   // one CTA per SM (each takes all of TMEM)
 
     // ---- dq kernel: resident Q1, Q2, G (128 rows); ring of K1 (, K2), V (64 rows)
@@ -86,6 +87,12 @@ struct BwdCfg {
     static_assert(KV_VEC <= 2048, "vector area");
 };
 
+// The two row warpgroups each own 32 of a sub-tile's 64 columns and write
+// their bf16 results (16 packed columns) at column 32 * warpgroup of the
+// region they read: the TS MMA's K step ks (16 keys / queries, 8 columns)
+// therefore starts at column ts_col(ks).
+__device__ __forceinline__ uint32_t ts_col(int ks) { return (ks & 1) * 8 + (ks >> 1) * 32; }
+
 // 16 bf16 pairs from 32 floats held as bit patterns
 __device__ __forceinline__ void pack32(const uint32_t *x, uint32_t *u) {
 #pragma unroll
@@ -94,7 +101,7 @@ __device__ __forceinline__ void pack32(const uint32_t *x, uint32_t *u) {
 
 // ===================================================================== dQ
 template <int DQK, int DV, bool V2>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dq(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
            const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tk1,
            const __grid_constant__ CUtensorMap tk2, const __grid_constant__ CUtensorMap tv, const BwdParams p) {
@@ -133,7 +140,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_ds, 4);
+        mbar_init(bar_ds, 8);
         mbar_init(bar_done, 1);
         mbar_init(bar_dr, 1);
         fence_mbar_init();
@@ -229,9 +236,9 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int ks = 0; ks < C::BN / 16; ++ks) {
                         const uint32_t ob = (ks * 2048) >> 4;
-                        mma_ts(tmem + C::COL_DQ1, tmem + C::COL_S1 + ks * 8, k1 + ob, C::IDESC_QK,
+                        mma_ts(tmem + C::COL_DQ1, tmem + C::COL_S1 + ts_col(ks), k1 + ob, C::IDESC_QK,
                                (j > 0 || ks > 0) ? 1u : 0u);
-                        mma_ts(tmem + C::COL_DQ2, tmem + C::COL_S2 + ks * 8, k2 + ob, C::IDESC_QK,
+                        mma_ts(tmem + C::COL_DQ2, tmem + C::COL_S2 + ts_col(ks), k2 + ob, C::IDESC_QK,
                                (j > 0 || ks > 0) ? 1u : 0u);
                     }
                 }
@@ -244,7 +251,7 @@ __global__ void __launch_bounds__(256, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ rows (query i)
-        const int wq = warp & 3;
+        const int wq = warp & 3, wg = (warp - 4) >> 2;   // lane quadrant, key half
         const int row = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int t = qt * C::BM + row;
@@ -260,14 +267,13 @@ __global__ void __launch_bounds__(256, 1)
             ok = warp_wait(bar_s, static_cast<uint32_t>(j & 1), p.err, ok);
             if (ok) {
                 tc_fence_after();
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+                {
                     uint32_t s1[32], s2[32], dp[32];
-                    tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * hh, s1);
-                    tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * hh, s2);
-                    tmem_ld32(tmem + lane_off + C::COL_DP + 32 * hh, dp);
+                    tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * wg, s1);
+                    tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * wg, s2);
+                    tmem_ld32(tmem + lane_off + C::COL_DP + 32 * wg, dp);
                     tmem_wait_ld();
-                    const int key0 = j * C::BN + 32 * hh;
+                    const int key0 = j * C::BN + 32 * wg;
                     // in place: s1 <- dS1, s2 <- dS2
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
@@ -280,9 +286,9 @@ __global__ void __launch_bounds__(256, 1)
                     }
                     uint32_t u[16];
                     pack32(s1, u);
-                    tmem_st16(tmem + lane_off + C::COL_S1 + 16 * hh, u);
+                    tmem_st16(tmem + lane_off + C::COL_S1 + 32 * wg, u);
                     pack32(s2, u);
-                    tmem_st16(tmem + lane_off + C::COL_S2 + 16 * hh, u);
+                    tmem_st16(tmem + lane_off + C::COL_S2 + 32 * wg, u);
                 }
                 tmem_wait_st();
             }
@@ -290,12 +296,12 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_ds);
         }
-        // epilogue: dQ_b * scale -> bf16 rows
+        // epilogue: dQ_b * scale -> bf16 rows (warpgroup b takes branch b)
         ok = warp_wait(bar_done, 0, p.err, ok);
         tc_fence_after();
         if (ok) {
-#pragma unroll
-            for (int br = 0; br < 2; ++br) {
+            {
+                const int br = wg;
                 __nv_bfloat16 *dst = (br ? p.dq2 : p.dq1) + b * p.q_sb + static_cast<int64_t>(t) * p.q_st +
                                      static_cast<int64_t>(br ? hq2 : hq1) * p.q_sh;
 #pragma unroll
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(256, 1)
 
 // =================================================================== dK dV
 template <int DQK, int DV, bool V2>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dkdv(const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq1,
              const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tg, const BwdParams p) {
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_p, 4);
+        mbar_init(bar_p, 8);
         mbar_init(bar_done, 1);
         mbar_init(bar_dr, 1);
         fence_mbar_init();
@@ -494,9 +500,9 @@ __global__ void __launch_bounds__(256, 1)
                     for (int ks = 0; ks < C::BN / 16; ++ks) {
                         const uint32_t ob = (ks * 2048) >> 4;
                         const uint32_t first = (it > 0 || ks > 0) ? 1u : 0u;
-                        mma_ts(tmem + C::COL_DV, tmem + C::COL_S1 + ks * 8, gdesc + ob, C::IDESC_V, first);
-                        mma_ts(tmem + C::COL_DK1, tmem + C::COL_S2 + ks * 8, q1d + ob, C::IDESC_QK, first);
-                        mma_ts(tmem + C::COL_DK2, tmem + C::COL_DP + ks * 8, q2d + ob, C::IDESC_QK,
+                        mma_ts(tmem + C::COL_DV, tmem + C::COL_S1 + ts_col(ks), gdesc + ob, C::IDESC_V, first);
+                        mma_ts(tmem + C::COL_DK1, tmem + C::COL_S2 + ts_col(ks), q1d + ob, C::IDESC_QK, first);
+                        mma_ts(tmem + C::COL_DK2, tmem + C::COL_DP + ts_col(ks), q2d + ob, C::IDESC_QK,
                                V2 ? 1u : first);
                     }
                 }
@@ -508,7 +514,7 @@ __global__ void __launch_bounds__(256, 1)
         }
     } else if (warp >= 4) {
         // -------------------------------------------------- rows (key j)
-        const int wq = warp & 3;
+        const int wq = warp & 3, wg = (warp - 4) >> 2;   // lane quadrant, query half
         const int row = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int j = kt * C::BM + row;
@@ -525,8 +531,8 @@ __global__ void __launch_bounds__(256, 1)
                 const float *vec =
                     reinterpret_cast<const float *>(smem + C::KV_OFF_RING + st * C::KV_STAGE + C::KV_STAGE_TMA);
                 const int q0 = item_qs(it) * C::BN;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+                {
+                    const int hh = wg;
                     uint32_t s1[32], s2[32], dp[32];
                     tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * hh, s1);
                     tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * hh, s2);
@@ -547,11 +553,11 @@ __global__ void __launch_bounds__(256, 1)
                     }
                     uint32_t u[16];
                     pack32(s1, u);
-                    tmem_st16(tmem + lane_off + C::COL_S1 + 16 * hh, u);
+                    tmem_st16(tmem + lane_off + C::COL_S1 + 32 * hh, u);
                     pack32(s2, u);
-                    tmem_st16(tmem + lane_off + C::COL_S2 + 16 * hh, u);
+                    tmem_st16(tmem + lane_off + C::COL_S2 + 32 * hh, u);
                     pack32(dp, u);
-                    tmem_st16(tmem + lane_off + C::COL_DP + 16 * hh, u);
+                    tmem_st16(tmem + lane_off + C::COL_DP + 32 * hh, u);
                 }
                 tmem_wait_st();
             }
@@ -582,11 +588,15 @@ __global__ void __launch_bounds__(256, 1)
                     }
                 }
             };
+            // warpgroup 0 stores dK (both branches for V1), warpgroup 1 dV
             const int64_t krow = b * p.k_sb + static_cast<int64_t>(j) * p.k_st + static_cast<int64_t>(hk) * p.k_sh;
-            store(C::COL_DK1, DQK, p.dk1 + krow, p.scale);
-            if (!V2) store(C::COL_DK2, DQK, p.dk2 + krow, p.scale);
-            store(C::COL_DV, DV, p.dv + b * p.v_sb + static_cast<int64_t>(j) * p.v_st + static_cast<int64_t>(hk) * p.v_sh,
-                  1.f);
+            if (wg == 0) {
+                store(C::COL_DK1, DQK, p.dk1 + krow, p.scale);
+                if (!V2) store(C::COL_DK2, DQK, p.dk2 + krow, p.scale);
+            } else {
+                store(C::COL_DV, DV,
+                      p.dv + b * p.v_sb + static_cast<int64_t>(j) * p.v_st + static_cast<int64_t>(hk) * p.v_sh, 1.f);
+            }
         }
     }
 
@@ -709,8 +719,25 @@ __global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
 __global__ void __launch_bounds__(1024) bwd_lambda(const BwdPreParams p) {
     __shared__ float red[32];
     const int64_t n = static_cast<int64_t>(p.B) * p.T * p.H;
-    float acc = 0.f;
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) acc += p.dlam_rows[i];
+    // eight independent 16-byte loads in flight per thread (the partials sit
+    // at a 256-byte aligned workspace offset); fixed order, so deterministic
+    const float4 *r4 = reinterpret_cast<const float4 *>(p.dlam_rows);
+    const int64_t n4 = n / 4, nt = blockDim.x;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int64_t i = threadIdx.x;
+    for (; i + 7 * nt < n4; i += 8 * nt) {
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = r4[i + k * nt];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) a[k] += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+    }
+    for (; i < n4; i += nt) {
+        const float4 v = r4[i];
+        a[0] += (v.x + v.y) + (v.z + v.w);
+    }
+    for (int64_t j = n4 * 4 + threadIdx.x; j < n; j += nt) a[1] += p.dlam_rows[j];
+    float acc = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
     acc = warp_sum(acc);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
     __syncthreads();

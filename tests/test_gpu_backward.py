@@ -124,3 +124,37 @@ def test_backward_argument_checks():
     with pytest.raises(bd.DiffAttnError) as e:
         bd.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout, saved[:1024])
     assert e.value.code == 6
+
+
+@pytest.mark.slow
+def test_v1_backward_full_workload_sampled_heads():
+    """B=4, T=2048, 16 heads, d=64 (the bench's V1 workload and launch): gradients of
+    three sampled (b, h) heads against the oracle (heads are independent in V1;
+    the lambda-vector gradients need every head and are checked at small sizes)."""
+    s = inputs.WORKLOADS["v1_bf16_B4_T2048_H16_d64"]
+    x = inputs.make_v1(s, seed=0)
+    dout = inputs.make_grad_out((s.B, s.T, s.H, 2 * s.d), "bf16", seed=0)
+    xd, dd = to_dev(x), dout.cuda()
+    _, g = run_v1(xd, dd, s.layer_index)
+    heads = [0, 21, s.B * s.H - 1]
+    ref = oracle.v1_bwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"],
+                        x["lam_k2"], s.layer_index, dout, heads=heads)
+    for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
+        got = g[n].float().cpu().permute(0, 2, 1, 3).reshape(s.B * s.H, s.T, -1)[heads]
+        want = ref[n].transpose(0, 2, 1, 3).reshape(s.B * s.H, s.T, -1)[heads]
+        check_grad(n, got, want)
+
+
+@pytest.mark.slow
+def test_v2_backward_long_sequence():
+    """T=4096 (the V2 prefill workload's length), 4 query heads over 2 kv heads, D=128."""
+    s = inputs.V2Shape(1, 4096, 4, 2, 128, "bf16")
+    x = inputs.make_v2(s, seed=5)
+    dout = inputs.make_grad_out((s.B, s.T, s.Hq // 2, s.D), "bf16", seed=5)
+    xd, dd = to_dev(x), dout.cuda()
+    bd = binding()
+    _, saved = bd.v2_fwd_train(xd["q"], xd["k"], xd["v"], xd["lam"])
+    g = bd.v2_bwd(xd["q"], xd["k"], xd["v"], xd["lam"], dd, saved)
+    ref = oracle.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout)
+    for n in ("dq", "dk", "dv", "dlam"):
+        check_grad(n, g[n], ref[n])
