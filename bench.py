@@ -47,7 +47,7 @@ L2_FLUSH_BYTES = 256 << 20
 # it was taken on (sha256 of the .cu file, first 16 hex digits).
 TRAFFIC_RECORDS: dict = {
     # profiles/prefill_onepass_v1_B4_T2048_H16_d64.md: dram__bytes_read.sum + dram__bytes_write.sum
-    "prefill_v1_d64": {"src_sha": "b6bed68432e63926", "bytes_per_launch": 144667648 + 13954816},
+    "prefill_v1_d64": {"src_sha": "56af0a817adb1f81", "bytes_per_launch": 147878912 + 13930752},
 }
 
 
