@@ -15,7 +15,7 @@
 //     dV  += (P_1 + c P_2)^T g_1   (one dV product for both branches).
 // P_b is recomputed from the scores and the forward's log-sum-exp.
 //
-// Three kernels (plus the row pre-pass in this file):
+// Kernels (the row pre-pass and the lambda reduction at the end of the file):
 //   bwd_pre     one warp per row: g_1 (V1: the RMSNorm backward), D_1, D_2,
 //               c, and the lambda gradient (V1: per-row share of dL/dlam;
 //               V2: dL/dlam[t] directly).
@@ -26,10 +26,10 @@
 //               each) | dK1 (| dK2) | dV.
 // In both, warp 0 streams the sub-tiles with TMA, warp 1 issues the MMAs,
 // and two row warpgroups (warps 4-7, 8-11; thread = TMEM lane = row) each
-// turn 32 of a sub-tile's 64 columns of scores into P, dS.  The bf16 results
-// are written over columns the threads have already read (dq: dS1 -> S1,
-// dS2 -> S2; dkdv: P~ -> S1^T, dS1^T -> S2^T, dS2^T -> dP^T) and feed TS
-// MMAs (A from TMEM, B an MN-major shared-memory tile).
+// take 32 of a sub-tile's 64 columns.  The rows load S and dP, release that
+// TMEM at once (the next sub-tile's products start on the tensor cores),
+// form P, dS in fp32 and write them in bf16 to 128-byte-swizzled shared
+// tiles, the A operands of the accumulating MMAs (dV, dK_b or dQ_b).
 #include "da_common.cuh"
 #include "da_internal.h"
 
@@ -43,7 +43,6 @@ struct BwdCfg {
     static constexpr int RBOX = 128 * 128;              // 128 rows x 64 bf16
     static constexpr int CBOX = 64 * 128;               // 64 rows x 64 bf16
     static constexpr int NK = V2 ? 1 : 2;               // distinct K tiles (V1: K1, K2)
-    static constexpr int STAGES = 3;
     static constexpr int COL_S1 = 0, COL_S2 = 64, COL_DP = 128, COL_ACC = 192;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false);
@@ -52,29 +51,36 @@ struct BwdCfg {
     static constexpr int THREADS = 384;   // warp 0 TMA, warp 1 MMA, warps 4-11 two row warpgroups
     static constexpr int MIN_SMEM = 120 * 1024;   // one CTA per SM (each takes all of TMEM)
 
-    // ---- dq kernel: resident Q1, Q2, G (128 rows); ring of K1 (, K2), V (64 rows)
+    // ---- dq kernel: resident Q1, Q2, G (128 rows); ring of K1 (, K2), V (64 rows);
+    //      result tiles dS1, dS2 (128 x 64 bf16, the A operands of dQ += dS K)
+    static constexpr int DQ_STAGES = 3;
     static constexpr int DQ_OFF_Q1 = 0;
     static constexpr int DQ_OFF_Q2 = QB * RBOX;
     static constexpr int DQ_OFF_G = 2 * QB * RBOX;
-    static constexpr int DQ_OFF_RING = DQ_OFF_G + VB * RBOX;
+    static constexpr int DQ_OFF_RES = DQ_OFF_G + VB * RBOX;
+    static constexpr int DQ_OFF_RING = DQ_OFF_RES + 2 * RBOX;
     static constexpr int DQ_STAGE = NK * QB * CBOX + VB * CBOX;
-    static constexpr int DQ_OFF_BAR = DQ_OFF_RING + STAGES * DQ_STAGE;
-    static constexpr int DQ_NBAR = 1 + 2 * STAGES + 4;   // res, full[S], empty[S], s, ds, done, drain
+    static constexpr int DQ_OFF_BAR = DQ_OFF_RING + DQ_STAGES * DQ_STAGE;
+    // res, full[S], empty[S], s, sfree, rready, rfree, done, drain
+    static constexpr int DQ_NBAR = 1 + 2 * DQ_STAGES + 6;
     static constexpr int DQ_OFF_TSLOT = DQ_OFF_BAR + DQ_NBAR * 8;
     static constexpr int DQ_SMEM_RAW = DQ_OFF_TSLOT + 8 + 1024;
     static constexpr int DQ_SMEM = DQ_SMEM_RAW > MIN_SMEM ? DQ_SMEM_RAW : MIN_SMEM;
     static constexpr int COL_DQ1 = COL_ACC, COL_DQ2 = COL_ACC + DQK;
 
-    // ---- dkdv kernel: resident K1 (, K2), V (128 rows); ring of Q1, Q2, G (64 rows) + row vectors
+    // ---- dkdv kernel: resident K1 (, K2), V (128 rows); ring of Q1, Q2, G (64 rows) + row
+    //      vectors; result tiles P~^T, dS1^T, dS2^T (128 x 64 bf16, the A operands of dV, dK)
+    static constexpr int KV_STAGES = (V2 && DQK == 128) ? 2 : 3;   // shared memory
     static constexpr int KV_OFF_K1 = 0;
     static constexpr int KV_OFF_K2 = QB * RBOX;                    // V1 only
     static constexpr int KV_OFF_V = NK * QB * RBOX;
-    static constexpr int KV_OFF_RING = KV_OFF_V + VB * RBOX;
+    static constexpr int KV_OFF_RES = KV_OFF_V + VB * RBOX;
+    static constexpr int KV_OFF_RING = KV_OFF_RES + 3 * RBOX;
     static constexpr int KV_VEC = 5 * 64 * 4;                      // lse1, lse2, d1, d2, c
     static constexpr int KV_STAGE_TMA = 2 * QB * CBOX + VB * CBOX;
     static constexpr int KV_STAGE = KV_STAGE_TMA + 2048;           // vectors, padded to keep 1 KB alignment
-    static constexpr int KV_OFF_BAR = KV_OFF_RING + STAGES * KV_STAGE;
-    static constexpr int KV_NBAR = 1 + 2 * STAGES + 4;             // res, full[S], empty[S], s, p, done, drain
+    static constexpr int KV_OFF_BAR = KV_OFF_RING + KV_STAGES * KV_STAGE;
+    static constexpr int KV_NBAR = 1 + 2 * KV_STAGES + 6;
     static constexpr int KV_OFF_TSLOT = KV_OFF_BAR + KV_NBAR * 8;
     static constexpr int KV_SMEM_RAW = KV_OFF_TSLOT + 8 + 1024;
     static constexpr int KV_SMEM = KV_SMEM_RAW > MIN_SMEM ? KV_SMEM_RAW : MIN_SMEM;
@@ -87,25 +93,39 @@ struct BwdCfg {
     static_assert(KV_VEC <= 2048, "vector area");
 };
 
-// The two row warpgroups each own 32 of a sub-tile's 64 columns and write
-// their bf16 results (16 packed columns) at column 32 * warpgroup of the
-// region they read: the TS MMA's K step ks (16 keys / queries, 8 columns)
-// therefore starts at column ts_col(ks).
-__device__ __forceinline__ uint32_t ts_col(int ks) { return (ks & 1) * 8 + (ks >> 1) * 32; }
-
 // 16 bf16 pairs from 32 floats held as bit patterns
 __device__ __forceinline__ void pack32(const uint32_t *x, uint32_t *u) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) u[i] = pack_bf16(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
 }
 
+// Write 32 bf16 values (16 packed words) of one row into a 128-row x 64-col
+// K-major tile with 128-byte swizzle (the layout a TMA box of that shape
+// has), at 16-byte chunks 4 * half .. 4 * half + 3 of the row.
+__device__ __forceinline__ void store_row_half(uint8_t *tile, int row, int half, const uint32_t *u) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int ch = 4 * half + k;
+        *reinterpret_cast<uint4 *>(tile + row * 128 + ((ch ^ (row & 7)) << 4)) =
+            make_uint4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
+    }
+}
+
 // ===================================================================== dQ
+// Pipeline per 64-key sub-tile j (one MMA issuer, two row warpgroups):
+//   MMA:  S(j), dP(j) into TMEM once the rows have loaded S(j-1), dP(j-1)
+//         ("sfree"); then dQ += dS(j-1) K(j-1) from the shared-memory result
+//         tiles once the rows have written them ("rready").
+//   rows: load S(j), dP(j) -> sfree; compute dS; wait until dQ(j-1) has read
+//         the result tiles ("rfree"); write dS(j) -> rready.
+// So S(j+1) and dP(j+1) run on the tensor cores while the rows work on j.
 template <int DQK, int DV, bool V2>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
            const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tk1,
            const __grid_constant__ CUtensorMap tk2, const __grid_constant__ CUtensorMap tv, const BwdParams p) {
     using C = BwdCfg<DQK, DV, V2>;
+    constexpr int ST = C::DQ_STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -126,21 +146,25 @@ __global__ void __launch_bounds__(384, 1)
 
     const uint32_t bar_res = sbase + C::DQ_OFF_BAR;
     const uint32_t bar_full = bar_res + 8;
-    const uint32_t bar_empty = bar_full + 8 * C::STAGES;
-    const uint32_t bar_s = bar_empty + 8 * C::STAGES;
-    const uint32_t bar_ds = bar_s + 8;
-    const uint32_t bar_done = bar_ds + 8;
+    const uint32_t bar_empty = bar_full + 8 * ST;
+    const uint32_t bar_s = bar_empty + 8 * ST;
+    const uint32_t bar_sfree = bar_s + 8;
+    const uint32_t bar_rready = bar_sfree + 8;
+    const uint32_t bar_rfree = bar_rready + 8;
+    const uint32_t bar_done = bar_rfree + 8;
     const uint32_t bar_dr = bar_done + 8;
     const uint32_t tslot = sbase + C::DQ_OFF_TSLOT;
 
     if (threadIdx.x == 0) {
         mbar_init(bar_res, 1);
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < ST; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_ds, 8);
+        mbar_init(bar_sfree, 8);
+        mbar_init(bar_rready, 8);
+        mbar_init(bar_rfree, 1);
         mbar_init(bar_done, 1);
         mbar_init(bar_dr, 1);
         fence_mbar_init();
@@ -172,9 +196,8 @@ __global__ void __launch_bounds__(384, 1)
                 tma_load_4d(sbase + C::DQ_OFF_G + c * C::RBOX, &tg, bar_res, 64 * c, h, qt * C::BM, b);
             int j = 0;
             for (; j < n_kv; ++j) {
-                const int st = j % C::STAGES;
-                if (j >= C::STAGES &&
-                    !mbar_wait(bar_empty + 8 * st, static_cast<uint32_t>((j / C::STAGES - 1) & 1), p.err))
+                const int st = j % ST;
+                if (j >= ST && !mbar_wait(bar_empty + 8 * st, static_cast<uint32_t>((j / ST - 1) & 1), p.err))
                     break;
                 const uint32_t dst = sbase + C::DQ_OFF_RING + st * C::DQ_STAGE;
                 mbar_arrive_expect_tx(bar_full + 8 * st, C::DQ_STAGE);
@@ -191,20 +214,39 @@ __global__ void __launch_bounds__(384, 1)
             }
             // leave no copy in flight
             mbar_wait(bar_res, 0, p.err);
-            for (int k = (j > C::STAGES ? j - C::STAGES : 0); k < j; ++k)
-                mbar_wait(bar_full + 8 * (k % C::STAGES), static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
+            for (int k = (j > ST ? j - ST : 0); k < j; ++k)
+                mbar_wait(bar_full + 8 * (k % ST), static_cast<uint32_t>((k / ST) & 1), p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
             const uint32_t sQ1 = sbase + C::DQ_OFF_Q1, sQ2 = sbase + C::DQ_OFF_Q2, sG = sbase + C::DQ_OFF_G;
+            const uint32_t sR1 = sbase + C::DQ_OFF_RES, sR2 = sR1 + C::RBOX;
+            auto k1_at = [&](int j) { return sbase + C::DQ_OFF_RING + (j % ST) * C::DQ_STAGE; };
+            // dQ_b += dS_b K_b for sub-tile jj: A = dS_b (shared, K-major), B = K_b tile MN-major
+            auto acc = [&](int jj) {
+                const uint32_t sK1 = k1_at(jj), sK2 = V2 ? sK1 : sK1 + C::QB * C::CBOX;
+                const uint64_t a1 = sdesc_sw128(sR1, 16, 1024), a2 = sdesc_sw128(sR2, 16, 1024);
+                const uint64_t k1 = sdesc_sw128(sK1, C::CBOX, 1024), k2 = sdesc_sw128(sK2, C::CBOX, 1024);
+#pragma unroll
+                for (int ks = 0; ks < C::BN / 16; ++ks) {
+                    const uint32_t oa = (ks * 32) >> 4, ob = (ks * 2048) >> 4;
+                    const uint32_t first = (jj > 0 || ks > 0) ? 1u : 0u;
+                    mma_ss(tmem + C::COL_DQ1, a1 + oa, k1 + ob, C::IDESC_QK, first);
+                    mma_ss(tmem + C::COL_DQ2, a2 + oa, k2 + ob, C::IDESC_QK, first);
+                }
+                mma_commit(bar_empty + 8 * (jj % ST));   // K, V of jj no longer needed
+                mma_commit(bar_rfree);                    // result tiles read
+            };
             bool ok = mbar_wait(bar_res, 0, p.err);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int st = j % C::STAGES;
-                const uint32_t sK1 = sbase + C::DQ_OFF_RING + st * C::DQ_STAGE;
+            int j = 0;
+            for (; ok && j < n_kv; ++j) {
+                const int st = j % ST;
+                const uint32_t sK1 = k1_at(j);
                 const uint32_t sK2 = V2 ? sK1 : sK1 + C::QB * C::CBOX;
                 const uint32_t sV = sK1 + C::NK * C::QB * C::CBOX;
-                ok = mbar_wait(bar_full + 8 * st, static_cast<uint32_t>((j / C::STAGES) & 1), p.err);
+                ok = mbar_wait(bar_full + 8 * st, static_cast<uint32_t>((j / ST) & 1), p.err) &&
+                     (j == 0 || mbar_wait(bar_sfree, static_cast<uint32_t>((j - 1) & 1), p.err));
                 if (!ok) break;
                 tc_fence_after();
                 // S_b = Q_b K_b^T (N = 64 keys), dP = G V^T
@@ -227,23 +269,13 @@ __global__ void __launch_bounds__(384, 1)
                     }
                 }
                 mma_commit(bar_s);
-                ok = mbar_wait(bar_ds, static_cast<uint32_t>(j & 1), p.err);
-                if (!ok) break;
-                tc_fence_after();
-                // dQ_b += dS_b K_b: A = dS_b (bf16 in TMEM), B = K_b tile MN-major
-                {
-                    const uint64_t k1 = sdesc_sw128(sK1, C::CBOX, 1024), k2 = sdesc_sw128(sK2, C::CBOX, 1024);
-#pragma unroll
-                    for (int ks = 0; ks < C::BN / 16; ++ks) {
-                        const uint32_t ob = (ks * 2048) >> 4;
-                        mma_ts(tmem + C::COL_DQ1, tmem + C::COL_S1 + ts_col(ks), k1 + ob, C::IDESC_QK,
-                               (j > 0 || ks > 0) ? 1u : 0u);
-                        mma_ts(tmem + C::COL_DQ2, tmem + C::COL_S2 + ts_col(ks), k2 + ob, C::IDESC_QK,
-                               (j > 0 || ks > 0) ? 1u : 0u);
-                    }
+                if (j > 0) {
+                    ok = mbar_wait(bar_rready, static_cast<uint32_t>((j - 1) & 1), p.err);
+                    if (!ok) break;
+                    acc(j - 1);
                 }
-                mma_commit(bar_empty + 8 * st);
             }
+            if (ok && j == n_kv && mbar_wait(bar_rready, static_cast<uint32_t>((n_kv - 1) & 1), p.err)) acc(n_kv - 1);
             mma_commit(bar_done);
             // no MMA may be in flight when TMEM is released
             mma_commit(bar_dr);
@@ -262,64 +294,68 @@ __global__ void __launch_bounds__(384, 1)
         const float d1 = live ? p.dd[vi] : 0.f, d2 = live ? p.dd[vstride + vi] : 0.f;
         const float cc = live ? p.cv[vi] : 0.f;
         const float sl2 = p.scale_log2;
+        uint8_t *res1 = smem + C::DQ_OFF_RES, *res2 = res1 + C::RBOX;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             ok = warp_wait(bar_s, static_cast<uint32_t>(j & 1), p.err, ok);
+            uint32_t s1[32], s2[32], dp[32];
             if (ok) {
                 tc_fence_after();
-                {
-                    uint32_t s1[32], s2[32], dp[32];
-                    tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * wg, s1);
-                    tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * wg, s2);
-                    tmem_ld32(tmem + lane_off + C::COL_DP + 32 * wg, dp);
-                    tmem_wait_ld();
-                    const int key0 = j * C::BN + 32 * wg;
-                    // in place: s1 <- dS1, s2 <- dS2
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const bool valid = live && key0 + c <= t;
-                        const float dpv = __uint_as_float(dp[c]);
-                        const float p1 = valid ? ex2(__uint_as_float(s1[c]) * sl2 - lse1) : 0.f;
-                        const float p2 = valid ? ex2(__uint_as_float(s2[c]) * sl2 - lse2) : 0.f;
-                        s1[c] = __float_as_uint(p1 * (dpv - d1));
-                        s2[c] = __float_as_uint(p2 * (cc * dpv - d2));
-                    }
-                    uint32_t u[16];
-                    pack32(s1, u);
-                    tmem_st16(tmem + lane_off + C::COL_S1 + 32 * wg, u);
-                    pack32(s2, u);
-                    tmem_st16(tmem + lane_off + C::COL_S2 + 32 * wg, u);
-                }
-                tmem_wait_st();
+                tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * wg, s1);
+                tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * wg, s2);
+                tmem_ld32(tmem + lane_off + C::COL_DP + 32 * wg, dp);
+                tmem_wait_ld();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_ds);
+            if (lane == 0) mbar_arrive(bar_sfree);   // the next S, dP may overwrite TMEM
+            if (ok) {
+                const int key0 = j * C::BN + 32 * wg;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const bool valid = live && key0 + c <= t;
+                    const float dpv = __uint_as_float(dp[c]);
+                    const float p1 = valid ? ex2(__uint_as_float(s1[c]) * sl2 - lse1) : 0.f;
+                    const float p2 = valid ? ex2(__uint_as_float(s2[c]) * sl2 - lse2) : 0.f;
+                    s1[c] = __float_as_uint(p1 * (dpv - d1));
+                    s2[c] = __float_as_uint(p2 * (cc * dpv - d2));
+                }
+            }
+            // the previous dQ MMAs must have read the result tiles
+            if (j > 0) ok = warp_wait(bar_rfree, static_cast<uint32_t>((j - 1) & 1), p.err, ok);
+            if (ok) {
+                uint32_t u[16];
+                pack32(s1, u);
+                store_row_half(res1, row, wg, u);
+                pack32(s2, u);
+                store_row_half(res2, row, wg, u);
+                fence_async_smem();   // generic-proxy writes -> tensor core reads
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_rready);
         }
         // epilogue: dQ_b * scale -> bf16 rows (warpgroup b takes branch b)
         ok = warp_wait(bar_done, 0, p.err, ok);
         tc_fence_after();
         if (ok) {
-            {
-                const int br = wg;
-                __nv_bfloat16 *dst = (br ? p.dq2 : p.dq1) + b * p.q_sb + static_cast<int64_t>(t) * p.q_st +
-                                     static_cast<int64_t>(br ? hq2 : hq1) * p.q_sh;
+            const int br = wg;
+            __nv_bfloat16 *dst = (br ? p.dq2 : p.dq1) + b * p.q_sb + static_cast<int64_t>(t) * p.q_st +
+                                 static_cast<int64_t>(br ? hq2 : hq1) * p.q_sh;
 #pragma unroll
-                for (int c0 = 0; c0 < DQK; c0 += 32) {
-                    uint32_t a[32];
-                    tmem_ld32(tmem + lane_off + (br ? C::COL_DQ2 : C::COL_DQ1) + c0, a);
-                    tmem_wait_ld();
-                    if (live) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+            for (int c0 = 0; c0 < DQK; c0 += 32) {
+                uint32_t a[32];
+                tmem_ld32(tmem + lane_off + (br ? C::COL_DQ2 : C::COL_DQ1) + c0, a);
+                tmem_wait_ld();
+                if (live) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
 #pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-                            const uint32_t *aa = a + 8 * q8;
-                            d4[q8] = make_uint4(
-                                pack_bf16(__uint_as_float(aa[0]) * p.scale, __uint_as_float(aa[1]) * p.scale),
-                                pack_bf16(__uint_as_float(aa[2]) * p.scale, __uint_as_float(aa[3]) * p.scale),
-                                pack_bf16(__uint_as_float(aa[4]) * p.scale, __uint_as_float(aa[5]) * p.scale),
-                                pack_bf16(__uint_as_float(aa[6]) * p.scale, __uint_as_float(aa[7]) * p.scale));
-                        }
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        const uint32_t *aa = a + 8 * q8;
+                        d4[q8] = make_uint4(
+                            pack_bf16(__uint_as_float(aa[0]) * p.scale, __uint_as_float(aa[1]) * p.scale),
+                            pack_bf16(__uint_as_float(aa[2]) * p.scale, __uint_as_float(aa[3]) * p.scale),
+                            pack_bf16(__uint_as_float(aa[4]) * p.scale, __uint_as_float(aa[5]) * p.scale),
+                            pack_bf16(__uint_as_float(aa[6]) * p.scale, __uint_as_float(aa[7]) * p.scale));
                     }
                 }
             }
@@ -337,12 +373,17 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // =================================================================== dK dV
+// Same pipeline over 64-query sub-tiles (items; V2: of every pair of the kv
+// group): S1^T, S2^T, dP^T of item i run while the rows turn item i-1 into
+// P~^T = P1^T + c P2^T, dS1^T, dS2^T; dV += P~^T G, dK_b += dS_b^T Q_b read
+// those from shared memory.
 template <int DQK, int DV, bool V2>
 __global__ void __launch_bounds__(384, 1)
     bwd_dkdv(const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq1,
              const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tg, const BwdParams p) {
     using C = BwdCfg<DQK, DV, V2>;
+    constexpr int ST = C::KV_STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -367,21 +408,25 @@ __global__ void __launch_bounds__(384, 1)
 
     const uint32_t bar_res = sbase + C::KV_OFF_BAR;
     const uint32_t bar_full = bar_res + 8;
-    const uint32_t bar_empty = bar_full + 8 * C::STAGES;
-    const uint32_t bar_s = bar_empty + 8 * C::STAGES;
-    const uint32_t bar_p = bar_s + 8;
-    const uint32_t bar_done = bar_p + 8;
+    const uint32_t bar_empty = bar_full + 8 * ST;
+    const uint32_t bar_s = bar_empty + 8 * ST;
+    const uint32_t bar_sfree = bar_s + 8;
+    const uint32_t bar_rready = bar_sfree + 8;
+    const uint32_t bar_rfree = bar_rready + 8;
+    const uint32_t bar_done = bar_rfree + 8;
     const uint32_t bar_dr = bar_done + 8;
     const uint32_t tslot = sbase + C::KV_OFF_TSLOT;
 
     if (threadIdx.x == 0) {
         mbar_init(bar_res, 1);
-        for (int s = 0; s < C::STAGES; ++s) {
+        for (int s = 0; s < ST; ++s) {
             mbar_init(bar_full + 8 * s, 1 + 32);   // TMA bytes + 32 lanes' row vectors
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_p, 8);
+        mbar_init(bar_sfree, 8);
+        mbar_init(bar_rready, 8);
+        mbar_init(bar_rfree, 1);
         mbar_init(bar_done, 1);
         mbar_init(bar_dr, 1);
         fence_mbar_init();
@@ -416,9 +461,8 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         int it = 0;
         for (; ok && it < n_items; ++it) {
-            const int st = it % C::STAGES;
-            if (it >= C::STAGES)
-                ok = warp_wait(bar_empty + 8 * st, static_cast<uint32_t>((it / C::STAGES - 1) & 1), p.err, ok);
+            const int st = it % ST;
+            if (it >= ST) ok = warp_wait(bar_empty + 8 * st, static_cast<uint32_t>((it / ST - 1) & 1), p.err, ok);
             if (!ok) break;
             const int hp = item_head(it), qs = item_qs(it);
             const uint32_t dst = sbase + C::KV_OFF_RING + st * C::KV_STAGE;
@@ -453,20 +497,42 @@ __global__ void __launch_bounds__(384, 1)
         // leave no copy in flight
         if (lane == 0) {
             mbar_wait(bar_res, 0, p.err);
-            for (int k = (it > C::STAGES ? it - C::STAGES : 0); k < it; ++k)
-                mbar_wait(bar_full + 8 * (k % C::STAGES), static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
+            for (int k = (it > ST ? it - ST : 0); k < it; ++k)
+                mbar_wait(bar_full + 8 * (k % ST), static_cast<uint32_t>((k / ST) & 1), p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
             const uint32_t sK1 = sbase + C::KV_OFF_K1, sK2 = V2 ? sK1 : sbase + C::KV_OFF_K2;
             const uint32_t sV = sbase + C::KV_OFF_V;
+            const uint32_t sRP = sbase + C::KV_OFF_RES, sR1 = sRP + C::RBOX, sR2 = sR1 + C::RBOX;
+            auto q1_at = [&](int it) { return sbase + C::KV_OFF_RING + (it % ST) * C::KV_STAGE; };
+            // dV += P~^T G; dK_b += dS_b^T Q_b for item jj (A = result tiles, B = MN-major sub-tiles)
+            auto acc = [&](int jj) {
+                const uint32_t sQ1 = q1_at(jj), sQ2 = sQ1 + C::QB * C::CBOX, sG = sQ1 + 2 * C::QB * C::CBOX;
+                const uint64_t ap = sdesc_sw128(sRP, 16, 1024), a1 = sdesc_sw128(sR1, 16, 1024),
+                               a2 = sdesc_sw128(sR2, 16, 1024);
+                const uint64_t gdesc = sdesc_sw128(sG, C::CBOX, 1024);
+                const uint64_t q1d = sdesc_sw128(sQ1, C::CBOX, 1024), q2d = sdesc_sw128(sQ2, C::CBOX, 1024);
+#pragma unroll
+                for (int ks = 0; ks < C::BN / 16; ++ks) {
+                    const uint32_t oa = (ks * 32) >> 4, ob = (ks * 2048) >> 4;
+                    const uint32_t first = (jj > 0 || ks > 0) ? 1u : 0u;
+                    mma_ss(tmem + C::COL_DV, ap + oa, gdesc + ob, C::IDESC_V, first);
+                    mma_ss(tmem + C::COL_DK1, a1 + oa, q1d + ob, C::IDESC_QK, first);
+                    mma_ss(tmem + C::COL_DK2, a2 + oa, q2d + ob, C::IDESC_QK, V2 ? 1u : first);
+                }
+                mma_commit(bar_empty + 8 * (jj % ST));   // Q, G of jj no longer needed
+                mma_commit(bar_rfree);                    // result tiles read
+            };
             bool ok = mbar_wait(bar_res, 0, p.err);
-            for (int it = 0; ok && it < n_items; ++it) {
-                const int st = it % C::STAGES;
-                const uint32_t sQ1 = sbase + C::KV_OFF_RING + st * C::KV_STAGE;
+            int it = 0;
+            for (; ok && it < n_items; ++it) {
+                const int st = it % ST;
+                const uint32_t sQ1 = q1_at(it);
                 const uint32_t sQ2 = sQ1 + C::QB * C::CBOX, sG = sQ1 + 2 * C::QB * C::CBOX;
-                ok = mbar_wait(bar_full + 8 * st, static_cast<uint32_t>((it / C::STAGES) & 1), p.err);
+                ok = mbar_wait(bar_full + 8 * st, static_cast<uint32_t>((it / ST) & 1), p.err) &&
+                     (it == 0 || mbar_wait(bar_sfree, static_cast<uint32_t>((it - 1) & 1), p.err));
                 if (!ok) break;
                 tc_fence_after();
                 // S_b^T = K_b Q_b^T (N = 64 queries), dP^T = V G^T
@@ -489,25 +555,14 @@ __global__ void __launch_bounds__(384, 1)
                     }
                 }
                 mma_commit(bar_s);
-                ok = mbar_wait(bar_p, static_cast<uint32_t>(it & 1), p.err);
-                if (!ok) break;
-                tc_fence_after();
-                // dV += P~^T G; dK_b += dS_b^T Q_b (A from TMEM, B MN-major over the 64 query rows)
-                {
-                    const uint64_t gdesc = sdesc_sw128(sG, C::CBOX, 1024);
-                    const uint64_t q1d = sdesc_sw128(sQ1, C::CBOX, 1024), q2d = sdesc_sw128(sQ2, C::CBOX, 1024);
-#pragma unroll
-                    for (int ks = 0; ks < C::BN / 16; ++ks) {
-                        const uint32_t ob = (ks * 2048) >> 4;
-                        const uint32_t first = (it > 0 || ks > 0) ? 1u : 0u;
-                        mma_ts(tmem + C::COL_DV, tmem + C::COL_S1 + ts_col(ks), gdesc + ob, C::IDESC_V, first);
-                        mma_ts(tmem + C::COL_DK1, tmem + C::COL_S2 + ts_col(ks), q1d + ob, C::IDESC_QK, first);
-                        mma_ts(tmem + C::COL_DK2, tmem + C::COL_DP + ts_col(ks), q2d + ob, C::IDESC_QK,
-                               V2 ? 1u : first);
-                    }
+                if (it > 0) {
+                    ok = mbar_wait(bar_rready, static_cast<uint32_t>((it - 1) & 1), p.err);
+                    if (!ok) break;
+                    acc(it - 1);
                 }
-                mma_commit(bar_empty + 8 * st);
             }
+            if (ok && it == n_items && mbar_wait(bar_rready, static_cast<uint32_t>((n_items - 1) & 1), p.err))
+                acc(n_items - 1);
             mma_commit(bar_done);
             mma_commit(bar_dr);
             mbar_wait(bar_dr, 0, p.err);
@@ -519,51 +574,57 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int j = kt * C::BM + row;
         const float sl2 = p.scale_log2;
+        uint8_t *resP = smem + C::KV_OFF_RES, *res1 = resP + C::RBOX, *res2 = res1 + C::RBOX;
         bool ok = true;
         for (int it = 0; it < n_items; ++it) {
-            const int st = it % C::STAGES;
+            const int st = it % ST;
             ok = warp_wait(bar_s, static_cast<uint32_t>(it & 1), p.err, ok);
             // the stage's row vectors were written by warp 0 before it arrived on
             // the stage's full barrier: acquire them there (that phase is complete)
-            ok = warp_wait(bar_full + 8 * st, static_cast<uint32_t>((it / C::STAGES) & 1), p.err, ok);
+            ok = warp_wait(bar_full + 8 * st, static_cast<uint32_t>((it / ST) & 1), p.err, ok);
+            uint32_t s1[32], s2[32], dp[32];
             if (ok) {
                 tc_fence_after();
-                const float *vec =
-                    reinterpret_cast<const float *>(smem + C::KV_OFF_RING + st * C::KV_STAGE + C::KV_STAGE_TMA);
-                const int q0 = item_qs(it) * C::BN;
-                {
-                    const int hh = wg;
-                    uint32_t s1[32], s2[32], dp[32];
-                    tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * hh, s1);
-                    tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * hh, s2);
-                    tmem_ld32(tmem + lane_off + C::COL_DP + 32 * hh, dp);
-                    tmem_wait_ld();
-                    // in place: s1 <- P~ = P1 + c P2, s2 <- dS1, dp <- dS2
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int q = 32 * hh + c;
-                        const bool valid = q0 + q >= j;   // key j <= query q0 + q; rows past T carry lse = +inf
-                        const float dpv = __uint_as_float(dp[c]);
-                        const float cq = vec[256 + q];
-                        const float p1 = valid ? ex2(__uint_as_float(s1[c]) * sl2 - vec[q]) : 0.f;
-                        const float p2 = valid ? ex2(__uint_as_float(s2[c]) * sl2 - vec[64 + q]) : 0.f;
-                        s1[c] = __float_as_uint(fmaf(cq, p2, p1));
-                        s2[c] = __float_as_uint(p1 * (dpv - vec[128 + q]));
-                        dp[c] = __float_as_uint(p2 * (cq * dpv - vec[192 + q]));
-                    }
-                    uint32_t u[16];
-                    pack32(s1, u);
-                    tmem_st16(tmem + lane_off + C::COL_S1 + 32 * hh, u);
-                    pack32(s2, u);
-                    tmem_st16(tmem + lane_off + C::COL_S2 + 32 * hh, u);
-                    pack32(dp, u);
-                    tmem_st16(tmem + lane_off + C::COL_DP + 32 * hh, u);
-                }
-                tmem_wait_st();
+                tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * wg, s1);
+                tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * wg, s2);
+                tmem_ld32(tmem + lane_off + C::COL_DP + 32 * wg, dp);
+                tmem_wait_ld();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_p);
+            if (lane == 0) mbar_arrive(bar_sfree);   // the next S^T, dP^T may overwrite TMEM
+            if (ok) {
+                const float *vec =
+                    reinterpret_cast<const float *>(smem + C::KV_OFF_RING + st * C::KV_STAGE + C::KV_STAGE_TMA);
+                const int q0 = item_qs(it) * C::BN;
+                // in place: s1 <- P~ = P1 + c P2, s2 <- dS1, dp <- dS2
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int q = 32 * wg + c;
+                    const bool valid = q0 + q >= j;   // key j <= query q0 + q; rows past T carry lse = +inf
+                    const float dpv = __uint_as_float(dp[c]);
+                    const float cq = vec[256 + q];
+                    const float p1 = valid ? ex2(__uint_as_float(s1[c]) * sl2 - vec[q]) : 0.f;
+                    const float p2 = valid ? ex2(__uint_as_float(s2[c]) * sl2 - vec[64 + q]) : 0.f;
+                    s1[c] = __float_as_uint(fmaf(cq, p2, p1));
+                    s2[c] = __float_as_uint(p1 * (dpv - vec[128 + q]));
+                    dp[c] = __float_as_uint(p2 * (cq * dpv - vec[192 + q]));
+                }
+            }
+            // the previous item's dV / dK MMAs must have read the result tiles
+            if (it > 0) ok = warp_wait(bar_rfree, static_cast<uint32_t>((it - 1) & 1), p.err, ok);
+            if (ok) {
+                uint32_t u[16];
+                pack32(s1, u);
+                store_row_half(resP, row, wg, u);
+                pack32(s2, u);
+                store_row_half(res1, row, wg, u);
+                pack32(dp, u);
+                store_row_half(res2, row, wg, u);
+                fence_async_smem();   // generic-proxy writes -> tensor core reads
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_rready);
         }
         // epilogue: dK_b * scale, dV -> bf16 rows of key j
         ok = warp_wait(bar_done, 0, p.err, ok);
