@@ -311,14 +311,16 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) mbar_arrive(bar_sfree);   // the next S, dP may overwrite TMEM
             if (ok) {
                 const int key0 = j * C::BN + 32 * wg;
+                // every key of this half is at or before every query of the tile: no mask
+                const bool full = key0 + 31 <= qt * C::BM;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const bool valid = live && key0 + c <= t;
+                    const bool valid = live && (full || key0 + c <= t);
                     const float dpv = __uint_as_float(dp[c]);
-                    const float p1 = valid ? ex2(__uint_as_float(s1[c]) * sl2 - lse1) : 0.f;
-                    const float p2 = valid ? ex2(__uint_as_float(s2[c]) * sl2 - lse2) : 0.f;
+                    const float p1 = valid ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -lse1)) : 0.f;
+                    const float p2 = valid ? ex2(fmaf(__uint_as_float(s2[c]), sl2, -lse2)) : 0.f;
                     s1[c] = __float_as_uint(p1 * (dpv - d1));
-                    s2[c] = __float_as_uint(p2 * (cc * dpv - d2));
+                    s2[c] = __float_as_uint(p2 * fmaf(cc, dpv, -d2));
                 }
             }
             // the previous dQ MMAs must have read the result tiles
@@ -594,21 +596,32 @@ __global__ void __launch_bounds__(384, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_sfree);   // the next S^T, dP^T may overwrite TMEM
             if (ok) {
-                const float *vec =
-                    reinterpret_cast<const float *>(smem + C::KV_OFF_RING + st * C::KV_STAGE + C::KV_STAGE_TMA);
-                const int q0 = item_qs(it) * C::BN;
+                // this warpgroup's 32 query columns of the row vectors, 16 bytes at a time
+                const float4 *vec = reinterpret_cast<const float4 *>(smem + C::KV_OFF_RING + st * C::KV_STAGE +
+                                                                     C::KV_STAGE_TMA) + 8 * wg;
+                const int q0 = item_qs(it) * C::BN + 32 * wg;
+                // every query of this half is at or after every key of the tile: no mask
+                const bool full = q0 >= kt * C::BM + C::BM - 1;
                 // in place: s1 <- P~ = P1 + c P2, s2 <- dS1, dp <- dS2
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int q = 32 * wg + c;
-                    const bool valid = q0 + q >= j;   // key j <= query q0 + q; rows past T carry lse = +inf
-                    const float dpv = __uint_as_float(dp[c]);
-                    const float cq = vec[256 + q];
-                    const float p1 = valid ? ex2(__uint_as_float(s1[c]) * sl2 - vec[q]) : 0.f;
-                    const float p2 = valid ? ex2(__uint_as_float(s2[c]) * sl2 - vec[64 + q]) : 0.f;
-                    s1[c] = __float_as_uint(fmaf(cq, p2, p1));
-                    s2[c] = __float_as_uint(p1 * (dpv - vec[128 + q]));
-                    dp[c] = __float_as_uint(p2 * (cq * dpv - vec[192 + q]));
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 l1 = vec[c4], l2 = vec[16 + c4], e1 = vec[32 + c4], e2 = vec[48 + c4],
+                                 cv = vec[64 + c4];
+                    const float l1a[4] = {l1.x, l1.y, l1.z, l1.w}, l2a[4] = {l2.x, l2.y, l2.z, l2.w};
+                    const float e1a[4] = {e1.x, e1.y, e1.z, e1.w}, e2a[4] = {e2.x, e2.y, e2.z, e2.w};
+                    const float cva[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = 4 * c4 + k;
+                        // key j <= query q0 + c; rows past T carry lse = +inf
+                        const bool valid = full || q0 + c >= j;
+                        const float dpv = __uint_as_float(dp[c]);
+                        const float p1 = valid ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -l1a[k])) : 0.f;
+                        const float p2 = valid ? ex2(fmaf(__uint_as_float(s2[c]), sl2, -l2a[k])) : 0.f;
+                        s1[c] = __float_as_uint(fmaf(cva[k], p2, p1));
+                        s2[c] = __float_as_uint(p1 * (dpv - e1a[k]));
+                        dp[c] = __float_as_uint(p2 * fmaf(cva[k], dpv, -e2a[k]));
+                    }
                 }
             }
             // the previous item's dV / dK MMAs must have read the result tiles
@@ -690,20 +703,37 @@ __global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
     const int t = static_cast<int>((r / p.H) % p.T);
     const int b = static_cast<int>(r / (static_cast<int64_t>(p.H) * p.T));
     const __nv_bfloat16 *go = p.dout + b * p.o_sb + static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh;
-    // V2: x1, x2 = a_e, a_o (bf16 saved); V1: x1 = x (RMSNorm input), x2 = a2 (fp32 saved)
+    // V2: x1, x2 = a_e, a_o (bf16 saved); V1: x1 = x (RMSNorm input), x2 = a2 (fp32 saved).
+    // Lane l owns the PER consecutive channels l * PER .. (one vector load per tensor).
+    static_assert(PER == 2 || PER == 4, "row pass: DV of 64 or 128");
     float x1[PER], x2[PER], dy[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int c = lane + 32 * i;
-        if (V2) {
-            x1[i] = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.sa1)[r * DV + c]);
-            x2[i] = __bfloat162float(static_cast<const __nv_bfloat16 *>(p.sa2)[r * DV + c]);
+    const int64_t c0 = r * DV + lane * PER;
+    auto load_bf16 = [&](const __nv_bfloat16 *src, float *dst) {
+        if (PER == 4) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+            const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+            dst[0] = a.x; dst[1] = a.y; dst[2] = c.x; dst[3 % PER] = c.y;
         } else {
-            x1[i] = static_cast<const float *>(p.sa1)[r * DV + c];
-            x2[i] = static_cast<const float *>(p.sa2)[r * DV + c];
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(src));
+            dst[0] = a.x; dst[1 % PER] = a.y;
         }
-        dy[i] = __bfloat162float(go[c]);
+    };
+    if (V2) {
+        load_bf16(static_cast<const __nv_bfloat16 *>(p.sa1) + c0, x1);
+        load_bf16(static_cast<const __nv_bfloat16 *>(p.sa2) + c0, x2);
+    } else if (PER == 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.sa1) + c0);
+        const float4 c = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.sa2) + c0);
+        x1[0] = a.x; x1[1] = a.y; x1[2 % PER] = a.z; x1[3 % PER] = a.w;
+        x2[0] = c.x; x2[1] = c.y; x2[2 % PER] = c.z; x2[3 % PER] = c.w;
+    } else {
+        const float2 a = *reinterpret_cast<const float2 *>(static_cast<const float *>(p.sa1) + c0);
+        const float2 c = *reinterpret_cast<const float2 *>(static_cast<const float *>(p.sa2) + c0);
+        x1[0] = a.x; x1[1 % PER] = a.y;
+        x2[0] = c.x; x2[1 % PER] = c.y;
     }
+    load_bf16(go + lane * PER, dy);
     const int64_t vi = (static_cast<int64_t>(b) * p.H + h) * p.T + t;
     const int64_t vstride = nrows;
     if (V2) {
@@ -749,19 +779,22 @@ __global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
         for (int i = 0; i < PER; ++i) m = fmaf(dy[i], x[i] * rr, m);
         m = warp_sum(m) / static_cast<float>(DV);
         float d1 = 0.f, d2 = 0.f, dl = 0.f;
-        __nv_bfloat16 *g = p.g + r * DV;
+        __nv_bfloat16 gb[PER];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const float dx = rr * (dy[i] - x[i] * rr * m);
             // D is formed from the bf16 g that the dP product will use, so
             // that dP - D cancels where it should (one key: dP = D exactly)
-            const __nv_bfloat16 gb = __float2bfloat16_rn(dx);
-            const float gr = __bfloat162float(gb);
+            gb[i] = __float2bfloat16_rn(dx);
+            const float gr = __bfloat162float(gb[i]);
             d1 = fmaf(gr, x1[i], d1);
             d2 = fmaf(gr, x2[i], d2);
             dl = fmaf(dx, x2[i], dl);
-            g[lane + 32 * i] = gb;
         }
+        if (PER == 4)
+            *reinterpret_cast<uint2 *>(p.g + c0) = *reinterpret_cast<const uint2 *>(gb);
+        else
+            *reinterpret_cast<uint32_t *>(p.g + c0) = *reinterpret_cast<const uint32_t *>(gb);
         d1 = warp_sum(d1);
         d2 = warp_sum(d2);
         dl = warp_sum(dl);
