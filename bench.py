@@ -393,7 +393,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
     a = (x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"],
          s.layer_index)
     _, saved = binding.v1_fwd_train(*a)
-    ws = torch.empty(binding.lib().diffattn_v1_bwd_workspace_size(s.B, s.T, s.H, s.d), dtype=torch.uint8,
+    ws = torch.empty(binding.lib().diffattn_v1_bwd_workspace_size(s.B, s.T, s.H, s.d, 1), dtype=torch.uint8,
                      device=dev)
     f = lambda: binding.v1_bwd(*a, dout, saved, workspace=ws)  # noqa: E731
     for _ in range(3):
@@ -411,7 +411,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
     x = inputs.make_v2(s, seed=args.seed, device=dev)
     dout = inputs.make_grad_out((s.B, s.T, s.Hq // 2, s.D), "bf16", seed=args.seed, device=dev)
     _, saved = binding.v2_fwd_train(x["q"], x["k"], x["v"], x["lam"])
-    ws = torch.empty(binding.lib().diffattn_v2_bwd_workspace_size(s.B, s.T, s.Hq, s.Hkv, s.D), dtype=torch.uint8,
+    ws = torch.empty(binding.lib().diffattn_v2_bwd_workspace_size(s.B, s.T, s.Hq, s.Hkv, s.D, 1), dtype=torch.uint8,
                      device=dev)
     f = lambda: binding.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout, saved, workspace=ws)  # noqa: E731
     for _ in range(3):

@@ -62,8 +62,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v1_decode.argtypes = ([vp] * 5 + [fp] * 4 + [vp, vp, vp, ctypes.c_size_t] + [i32] * 5
                                              + [i32, vp])
             sz = ctypes.c_size_t
-            for n, k in (("diffattn_v1_train_saved_size", 4), ("diffattn_v1_bwd_workspace_size", 4),
-                         ("diffattn_v2_train_saved_size", 5), ("diffattn_v2_bwd_workspace_size", 5)):
+            for n, k in (("diffattn_v1_train_saved_size", 5), ("diffattn_v1_bwd_workspace_size", 5),
+                         ("diffattn_v2_train_saved_size", 6), ("diffattn_v2_bwd_workspace_size", 6)):
                 getattr(L, n).restype = sz
                 getattr(L, n).argtypes = [i32] * k
             L.diffattn_v1_fwd_train.restype = i32
@@ -349,7 +349,7 @@ def v1_fwd_train(q1, q2, k1, k2, v, lam_q1, lam_k1, lam_q2, lam_k2, layer_index:
     out = torch.empty((B, T, H, 2 * d), dtype=q1.dtype, device=q1.device)
     strides = _v1_strides(q1, q2, k1, k2, v, out)
     lams = _lam_vecs(d, lam_q1, lam_k1, lam_q2, lam_k2)
-    nbytes = int(lib().diffattn_v1_train_saved_size(B, T, H, d))
+    nbytes = int(lib().diffattn_v1_train_saved_size(B, T, H, d, _dtype_code(q1)))
     saved = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q1.device)
     rc = lib().diffattn_v1_fwd_train(q1.data_ptr(), q2.data_ptr(), k1.data_ptr(), k2.data_ptr(), v.data_ptr(),
                                      *[x.data_ptr() for x in lams], out.data_ptr(), saved.data_ptr(), saved.numel(),
@@ -387,8 +387,8 @@ def v1_bwd(q1, q2, k1, k2, v, lam_q1, lam_k1, lam_q2, lam_k2, layer_index: int, 
     dv = torch.empty_like(v)
     if dv.stride() != v.stride():
         raise ValueError("v must be contiguous")
-    dl = [torch.empty(d, dtype=torch.float32, device=q1.device) for _ in range(4)]
-    need = int(lib().diffattn_v1_bwd_workspace_size(B, T, H, d))
+    dl = [torch.empty(d, dtype=torch.float32, device=q1.device) for _ in range(4)]   # fp32 for both dtypes
+    need = int(lib().diffattn_v1_bwd_workspace_size(B, T, H, d, _dtype_code(q1)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q1.device)
     rc = lib().diffattn_v1_bwd(q1.data_ptr(), q2.data_ptr(), k1.data_ptr(), k2.data_ptr(), v.data_ptr(),
@@ -410,7 +410,7 @@ def v2_fwd_train(q, k, v, lam, stream=None):
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
     out = torch.empty((B, T, Hq // 2, D), dtype=q.dtype, device=q.device)
-    nbytes = int(lib().diffattn_v2_train_saved_size(B, T, Hq, Hkv, D))
+    nbytes = int(lib().diffattn_v2_train_saved_size(B, T, Hq, Hkv, D, _dtype_code(q)))
     saved = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     rc = lib().diffattn_v2_fwd_train(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), out.data_ptr(),
                                      saved.data_ptr(), saved.numel(), B, T, Hq, Hkv, D, _dtype_code(q),
@@ -428,7 +428,7 @@ def v2_bwd(q, k, v, lam, dout, saved, workspace: torch.Tensor | None = None, str
         raise ValueError("dout must be a contiguous (B, T, Hq/2, D) tensor")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dlam = torch.empty_like(lam)
-    need = int(lib().diffattn_v2_bwd_workspace_size(B, T, Hq, Hkv, D))
+    need = int(lib().diffattn_v2_bwd_workspace_size(B, T, Hq, Hkv, D, _dtype_code(q)))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     rc = lib().diffattn_v2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), dout.data_ptr(),

@@ -453,39 +453,47 @@ struct SavedLayout {
         total = off_lse + round256(static_cast<size_t>(2) * B * H * T * 4);
     }
 };
-// Backward workspace: D (2, B, H, T) | c (B, H, T) | V1: dlam rows (B, T, H) | g (bf16, (B, T, H, DV))
+// Backward workspace: D (2, B, H, T) | c (B, H, T) | V1: dlam rows (B, T, H) | g ((B, T, H, DV),
+// gsize bytes per element: bf16 on the tensor-core path, fp32 on the CUDA-core one)
 struct BwdWsLayout {
     size_t off_c, off_rows, off_g, total;
-    BwdWsLayout(int B, int T, int H, int DV, bool v1) {
+    BwdWsLayout(int B, int T, int H, int DV, bool v1, int gsize) {
         const size_t n = static_cast<size_t>(B) * H * T;
         off_c = round256(2 * n * 4);
         off_rows = off_c + round256(n * 4);
         off_g = off_rows + (v1 ? round256(n * 4) : 0);
-        total = off_g + (v1 ? round256(n * DV * 2) : 0);
+        total = off_g + (v1 ? round256(n * DV * gsize) : 0);
     }
 };
 bool shape_ok_bytes(int B, int T, int H, int DV) {
     return B >= 1 && T >= 1 && H >= 1 && static_cast<double>(B) * T * H * DV < 4.0e12;
 }
+// Training support: bf16 on the tcgen05 kernels, fp32 on the CUDA-core ones.
+bool train_supported(int dqk, bool v2, da_dtype dtype) {
+    if (dtype == DA_BF16) return backward_supported(dqk, v2 ? dqk : 2 * dqk, v2);
+    if (dtype == DA_F32) return v2 ? (dqk == 64 || dqk == 128) : (dqk == 32 || dqk == 64 || dqk == 128);
+    return false;
+}
+int saved_esize(bool v2, da_dtype dtype) { return (v2 && dtype == DA_BF16) ? 2 : 4; }
 }  // namespace
 
 extern "C" {
 
-size_t diffattn_v1_train_saved_size(int B, int T, int H, int d) {
-    if (!shape_ok_bytes(B, T, H, 2 * d) || !backward_supported(d, 2 * d, false)) return 0;
-    return SavedLayout(B, T, H, 2 * d, 4).total;
+size_t diffattn_v1_train_saved_size(int B, int T, int H, int d, da_dtype dtype) {
+    if (!shape_ok_bytes(B, T, H, 2 * d) || !train_supported(d, false, dtype)) return 0;
+    return SavedLayout(B, T, H, 2 * d, saved_esize(false, dtype)).total;
 }
-size_t diffattn_v2_train_saved_size(int B, int T, int Hq, int Hkv, int D) {
-    if (Hq < 2 || Hkv < 1 || !shape_ok_bytes(B, T, Hq / 2, D) || !backward_supported(D, D, true)) return 0;
-    return SavedLayout(B, T, Hq / 2, D, 2).total;
+size_t diffattn_v2_train_saved_size(int B, int T, int Hq, int Hkv, int D, da_dtype dtype) {
+    if (Hq < 2 || Hkv < 1 || !shape_ok_bytes(B, T, Hq / 2, D) || !train_supported(D, true, dtype)) return 0;
+    return SavedLayout(B, T, Hq / 2, D, saved_esize(true, dtype)).total;
 }
-size_t diffattn_v1_bwd_workspace_size(int B, int T, int H, int d) {
-    if (!shape_ok_bytes(B, T, H, 2 * d) || !backward_supported(d, 2 * d, false)) return 0;
-    return BwdWsLayout(B, T, H, 2 * d, true).total;
+size_t diffattn_v1_bwd_workspace_size(int B, int T, int H, int d, da_dtype dtype) {
+    if (!shape_ok_bytes(B, T, H, 2 * d) || !train_supported(d, false, dtype)) return 0;
+    return BwdWsLayout(B, T, H, 2 * d, true, dtype == DA_F32 ? 4 : 2).total;
 }
-size_t diffattn_v2_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D) {
-    if (Hq < 2 || Hkv < 1 || !shape_ok_bytes(B, T, Hq / 2, D) || !backward_supported(D, D, true)) return 0;
-    return BwdWsLayout(B, T, Hq / 2, D, false).total;
+size_t diffattn_v2_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, da_dtype dtype) {
+    if (Hq < 2 || Hkv < 1 || !shape_ok_bytes(B, T, Hq / 2, D) || !train_supported(D, true, dtype)) return 0;
+    return BwdWsLayout(B, T, Hq / 2, D, false, 4).total;
 }
 
 da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, const void *k2, const void *v,
@@ -498,16 +506,38 @@ da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, 
     if (!q1 || !q2 || !k1 || !k2 || !v || !lam_q1 || !lam_k1 || !lam_q2 || !lam_k2 || !out || !saved)
         return DA_ERR_NULL_PTR;
     if (B < 1 || T < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
-    if (dtype != DA_BF16 || !backward_supported(d, 2 * d, false)) return DA_ERR_UNSUPPORTED_DIM;
+    if (!train_supported(d, false, dtype)) return DA_ERR_UNSUPPORTED_DIM;
     for (const void *ptr : {q1, q2, k1, k2, v, static_cast<const void *>(out), static_cast<const void *>(saved)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
     for (int64_t st : {q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh, o_sb, o_st, o_sh})
-        if (!stride_ok(st, 2)) return DA_ERR_MISALIGNED;
-    const SavedLayout sl(B, T, H, 2 * d, 4);
+        if (!stride_ok(st, dtype == DA_F32 ? 4 : 2)) return DA_ERR_MISALIGNED;
+    const SavedLayout sl(B, T, H, 2 * d, saved_esize(false, dtype));
     if (saved_bytes < sl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     uint32_t *err = nullptr;
     if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
     t_last_launches = 0;
+    if (dtype == DA_F32) {
+        SimtParams p{};
+        p.q1 = static_cast<const float *>(q1); p.q2 = static_cast<const float *>(q2);
+        p.k1 = static_cast<const float *>(k1); p.k2 = static_cast<const float *>(k2);
+        p.v = static_cast<const float *>(v);
+        p.q_sb = q_sb; p.q_st = q_st; p.q_sh = q_sh;
+        p.k_sb = k_sb; p.k_st = k_st; p.k_sh = k_sh;
+        p.v_sb = v_sb; p.v_st = v_st; p.v_sh = v_sh;
+        p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
+        p.out = static_cast<float *>(out);
+        p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+        p.layer_index = layer_index;
+        p.B = B; p.Tq = T; p.Lk = T; p.H = H; p.G = 1; p.mode = 1;
+        p.err = err;
+        char *sv = static_cast<char *>(saved);
+        p.sa1 = reinterpret_cast<float *>(sv);
+        p.sa2 = reinterpret_cast<float *>(sv + sl.off_a2);
+        p.slse = reinterpret_cast<float *>(sv + sl.off_lse);
+        const da_status st = cuda_status(launch_simt(p, d, 2 * d, stream));
+        if (st == DA_OK) t_last_launches = 1;
+        return st;
+    }
     PrefillMaps m;
     const uint64_t uT = static_cast<uint64_t>(T), uH = static_cast<uint64_t>(H), uB = static_cast<uint64_t>(B);
     if (!encode_map_4d(&m.q1, q1, d, uH, uT, uB, q_sh, q_st, q_sb, 128) ||
@@ -540,15 +570,36 @@ da_status diffattn_v2_fwd_train(const void *q, const void *k, const void *v, con
     if (!q || !k || !v || !lam || !out || !saved) return DA_ERR_NULL_PTR;
     if (B < 1 || T < 1 || Hq < 2 || Hkv < 1) return DA_ERR_BAD_SHAPE;
     if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
-    if (dtype != DA_BF16 || !backward_supported(D, D, true)) return DA_ERR_UNSUPPORTED_DIM;
+    if (!train_supported(D, true, dtype)) return DA_ERR_UNSUPPORTED_DIM;
     for (const void *ptr : {q, k, v, static_cast<const void *>(out), static_cast<const void *>(saved)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
     const int P = Hq / 2, G = Hq / Hkv;
-    const SavedLayout sl(B, T, P, D, 2);
+    const SavedLayout sl(B, T, P, D, saved_esize(true, dtype));
     if (saved_bytes < sl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     uint32_t *err = nullptr;
     if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
     t_last_launches = 0;
+    if (dtype == DA_F32) {
+        SimtParams p{};
+        p.q1 = p.q2 = static_cast<const float *>(q);
+        p.k1 = p.k2 = static_cast<const float *>(k);
+        p.v = static_cast<const float *>(v);
+        p.q_sh = D; p.q_st = static_cast<int64_t>(Hq) * D; p.q_sb = p.q_st * T;
+        p.k_sh = D; p.k_st = static_cast<int64_t>(Hkv) * D; p.k_sb = p.k_st * T;
+        p.v_sh = p.k_sh; p.v_st = p.k_st; p.v_sb = p.k_sb;
+        p.o_sh = D; p.o_st = static_cast<int64_t>(P) * D; p.o_sb = p.o_st * T;
+        p.out = static_cast<float *>(out);
+        p.lam = lam; p.lam_st = P; p.lam_sb = static_cast<int64_t>(P) * T;
+        p.B = B; p.Tq = T; p.Lk = T; p.H = P; p.G = G; p.mode = 2;
+        p.err = err;
+        char *sv = static_cast<char *>(saved);
+        p.sa1 = reinterpret_cast<float *>(sv);
+        p.sa2 = reinterpret_cast<float *>(sv + sl.off_a2);
+        p.slse = reinterpret_cast<float *>(sv + sl.off_lse);
+        const da_status st = cuda_status(launch_simt(p, D, D, stream));
+        if (st == DA_OK) t_last_launches = 1;
+        return st;
+    }
     PrefillMaps m;
     const uint64_t uT = static_cast<uint64_t>(T), uB = static_cast<uint64_t>(B);
     const int64_t qst = static_cast<int64_t>(Hq) * D, kst = static_cast<int64_t>(Hkv) * D;
@@ -588,23 +639,55 @@ da_status diffattn_v1_bwd(const void *q1, const void *q2, const void *k1, const 
         !dq2 || !dk1 || !dk2 || !dv || !dlam_q1 || !dlam_k1 || !dlam_q2 || !dlam_k2 || !workspace)
         return DA_ERR_NULL_PTR;
     if (B < 1 || T < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
-    if (dtype != DA_BF16 || !backward_supported(d, 2 * d, false)) return DA_ERR_UNSUPPORTED_DIM;
+    if (!train_supported(d, false, dtype)) return DA_ERR_UNSUPPORTED_DIM;
     for (const void *ptr : {q1, q2, k1, k2, v, dout, saved, static_cast<const void *>(dq1),
                             static_cast<const void *>(dq2), static_cast<const void *>(dk1),
                             static_cast<const void *>(dk2), static_cast<const void *>(dv),
                             static_cast<const void *>(workspace)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    const bool f32 = dtype == DA_F32;
     for (int64_t st : {q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh, o_sb, o_st, o_sh})
-        if (!stride_ok(st, 2)) return DA_ERR_MISALIGNED;
+        if (!stride_ok(st, f32 ? 4 : 2)) return DA_ERR_MISALIGNED;
     const int DV = 2 * d;
-    const SavedLayout sl(B, T, H, DV, 4);
-    const BwdWsLayout wl(B, T, H, DV, true);
+    const SavedLayout sl(B, T, H, DV, saved_esize(false, dtype));
+    const BwdWsLayout wl(B, T, H, DV, true, f32 ? 4 : 2);
     if (saved_bytes < sl.total || workspace_bytes < wl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     uint32_t *err = nullptr;
     if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
     t_last_launches = 0;
     char *ws = static_cast<char *>(workspace);
     const char *sv = static_cast<const char *>(saved);
+    if (f32) {
+        SimtBwdParams p{};
+        p.q1 = static_cast<const float *>(q1); p.q2 = static_cast<const float *>(q2);
+        p.k1 = static_cast<const float *>(k1); p.k2 = static_cast<const float *>(k2);
+        p.v = static_cast<const float *>(v);
+        p.q_sb = q_sb; p.q_st = q_st; p.q_sh = q_sh;
+        p.k_sb = k_sb; p.k_st = k_st; p.k_sh = k_sh;
+        p.v_sb = v_sb; p.v_st = v_st; p.v_sh = v_sh;
+        p.dout = static_cast<const float *>(dout);
+        p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
+        p.sa1 = reinterpret_cast<const float *>(sv);
+        p.sa2 = reinterpret_cast<const float *>(sv + sl.off_a2);
+        p.slse = reinterpret_cast<const float *>(sv + sl.off_lse);
+        p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+        p.layer_index = layer_index;
+        p.dq1 = static_cast<float *>(dq1); p.dq2 = static_cast<float *>(dq2);
+        p.dk1 = static_cast<float *>(dk1); p.dk2 = static_cast<float *>(dk2);
+        p.dv = static_cast<float *>(dv);
+        p.dlq1 = dlam_q1; p.dlk1 = dlam_k1; p.dlq2 = dlam_q2; p.dlk2 = dlam_k2;
+        p.gw = reinterpret_cast<float *>(ws + wl.off_g);
+        p.g = p.gw;
+        p.g_sh = DV; p.g_st = static_cast<int64_t>(H) * DV; p.g_sb = p.g_st * T;
+        p.dd = reinterpret_cast<float *>(ws);
+        p.cv = reinterpret_cast<float *>(ws + wl.off_c);
+        p.dlam_rows = reinterpret_cast<float *>(ws + wl.off_rows);
+        p.B = B; p.T = T; p.H = H; p.G = 1; p.Hkv = H; p.mode = 1;
+        p.err = err;
+        const da_status st = cuda_status(launch_simt_backward(p, d, DV, stream));
+        if (st == DA_OK) t_last_launches = 4;
+        return st;
+    }
     __nv_bfloat16 *g = reinterpret_cast<__nv_bfloat16 *>(ws + wl.off_g);
     BwdMaps m;
     const uint64_t uT = static_cast<uint64_t>(T), uH = static_cast<uint64_t>(H), uB = static_cast<uint64_t>(B);
@@ -661,19 +744,49 @@ da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const flo
         return DA_ERR_NULL_PTR;
     if (B < 1 || T < 1 || Hq < 2 || Hkv < 1) return DA_ERR_BAD_SHAPE;
     if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
-    if (dtype != DA_BF16 || !backward_supported(D, D, true)) return DA_ERR_UNSUPPORTED_DIM;
+    if (!train_supported(D, true, dtype)) return DA_ERR_UNSUPPORTED_DIM;
     for (const void *ptr : {q, k, v, dout, saved, static_cast<const void *>(dq), static_cast<const void *>(dk),
                             static_cast<const void *>(dv), static_cast<const void *>(workspace)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
     const int P = Hq / 2, G = Hq / Hkv;
-    const SavedLayout sl(B, T, P, D, 2);
-    const BwdWsLayout wl(B, T, P, D, false);
+    const SavedLayout sl(B, T, P, D, saved_esize(true, dtype));
+    const BwdWsLayout wl(B, T, P, D, false, 4);
     if (saved_bytes < sl.total || workspace_bytes < wl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     uint32_t *err = nullptr;
     if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
     t_last_launches = 0;
     char *ws = static_cast<char *>(workspace);
     const char *sv = static_cast<const char *>(saved);
+    if (dtype == DA_F32) {
+        SimtBwdParams p{};
+        p.q1 = p.q2 = static_cast<const float *>(q);
+        p.k1 = p.k2 = static_cast<const float *>(k);
+        p.v = static_cast<const float *>(v);
+        const int64_t qst = static_cast<int64_t>(Hq) * D, kst = static_cast<int64_t>(Hkv) * D;
+        const int64_t ost = static_cast<int64_t>(P) * D;
+        p.q_sh = D; p.q_st = qst; p.q_sb = qst * T;
+        p.k_sh = D; p.k_st = kst; p.k_sb = kst * T;
+        p.v_sh = D; p.v_st = kst; p.v_sb = kst * T;
+        p.dout = static_cast<const float *>(dout);
+        p.o_sh = D; p.o_st = ost; p.o_sb = ost * T;
+        p.g = p.dout;
+        p.g_sh = D; p.g_st = ost; p.g_sb = ost * T;
+        p.sa1 = reinterpret_cast<const float *>(sv);
+        p.sa2 = reinterpret_cast<const float *>(sv + sl.off_a2);
+        p.slse = reinterpret_cast<const float *>(sv + sl.off_lse);
+        p.lam = lam;
+        p.dq1 = p.dq2 = static_cast<float *>(dq);
+        p.dk1 = p.dk2 = static_cast<float *>(dk);
+        p.dv = static_cast<float *>(dv);
+        p.dlam = dlam;
+        p.dd = reinterpret_cast<float *>(ws);
+        p.cv = reinterpret_cast<float *>(ws + wl.off_c);
+        p.B = B; p.T = T; p.H = P; p.G = G; p.Hkv = Hkv; p.mode = 2;
+        p.err = err;
+        const da_status st = cuda_status(launch_simt_backward(p, D, D, stream));
+        if (st == DA_OK) t_last_launches = 3;
+        return st;
+    }
     BwdMaps m;
     const uint64_t uT = static_cast<uint64_t>(T), uB = static_cast<uint64_t>(B);
     const int64_t qst = static_cast<int64_t>(Hq) * D, kst = static_cast<int64_t>(Hkv) * D;

@@ -35,6 +35,11 @@ struct SimtParams {
     int B, Tq, Lk, H, G, mode;
     const int *lens;               // decode (Tq == 1): keys per sequence, or NULL
     uint32_t *err;
+    // training forward (prefill) only, else NULL: per row (B, T, H, DV)
+    // contiguous fp32, V1 x = a1 - lam a2 and a2, V2 a_e and a_o; and each
+    // branch's log-sum-exp of the scaled scores in natural units,
+    // lse_b = m + log(l), P = exp(s * scale - lse_b) ((2, B, H, T) fp32)
+    float *sa1, *sa2, *slse;
 };
 cudaError_t launch_simt(const SimtParams &p, int dqk, int dv, cudaStream_t s);
 
@@ -109,6 +114,31 @@ struct BwdMaps {
     CUtensorMap k1r, k2r, vr, q1c, q2c, gc;      // dK dV kernel: 128-row K / V boxes, 64-row Q / G boxes
 };
 bool backward_supported(int dqk, int dv, bool v2);
+// dL/dlam summed from the per-row shares in pp.dlam_rows, then the four
+// lambda-vector gradients (one CTA; used by the bf16 and the fp32 backward).
+cudaError_t launch_bwd_lambda(const BwdPreParams &pp, cudaStream_t s);
+
+// fp32 backward on CUDA cores (k_simt_bwd.cu).  mode 1 = V1 (H diff heads),
+// mode 2 = V2 (H = pairs, query heads 2h / 2h+1, kv head 2h / G).
+struct SimtBwdParams {
+    const float *q1, *q2, *k1, *k2, *v;          // V2: q1 == q2, k1 == k2
+    int64_t q_sb, q_st, q_sh, k_sb, k_st, k_sh, v_sb, v_st, v_sh;   // elements
+    const float *dout;
+    int64_t o_sb, o_st, o_sh;
+    const float *sa1, *sa2, *slse;               // saved by the fp32 training forward
+    const float *lam;                            // V2 logits (B, T, H)
+    const float *lq1, *lk1, *lq2, *lk2;          // V1
+    int layer_index;
+    float *dq1, *dq2, *dk1, *dk2, *dv;           // outputs with the inputs' strides (V2: dq1 == dq2, dk1 == dk2)
+    float *dlam;                                 // V2 (B, T, H)
+    float *dlq1, *dlk1, *dlq2, *dlk2;            // V1 lambda-vector gradients (d)
+    const float *g;                              // upstream gradient of branch 1: V1 workspace, V2 dout
+    int64_t g_sb, g_st, g_sh;
+    float *gw, *dd, *cv, *dlam_rows;             // workspace: V1 g (B,T,H,DV); D (2,B,H,T); c (B,H,T); V1 rows
+    int B, T, H, G, Hkv, mode;
+    uint32_t *err;
+};
+cudaError_t launch_simt_backward(const SimtBwdParams &p, int dqk, int dv, cudaStream_t s);
 cudaError_t launch_backward(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, int dqk, int dv, bool v2,
                             cudaStream_t s);
 

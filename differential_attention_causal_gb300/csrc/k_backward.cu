@@ -888,6 +888,11 @@ cudaError_t launch_bwd_t(const BwdMaps &m, const BwdParams &p, const BwdPreParam
 
 }  // namespace
 
+cudaError_t launch_bwd_lambda(const BwdPreParams &pp, cudaStream_t s) {
+    bwd_lambda<<<1, 1024, 0, s>>>(pp);
+    return cudaGetLastError();
+}
+
 bool backward_supported(int dqk, int dv, bool v2) {
     if (v2) return (dqk == 128 && dv == 128) || (dqk == 64 && dv == 64);
     return dqk == 64 && dv == 128;

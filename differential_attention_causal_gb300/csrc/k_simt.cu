@@ -100,6 +100,14 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
     }
 
     float *out = p.out + b * p.o_sb + t * p.o_st + h * p.o_sh;
+    // training forward: saved tensors of this row for the backward
+    const bool train = p.sa1 != nullptr;
+    const int64_t srow = ((static_cast<int64_t>(b) * p.Tq + t) * p.H + h) * DV;
+    if (train && lane == 0) {
+        const int64_t li = (static_cast<int64_t>(b) * p.H + h) * p.Tq + t;
+        p.slse[li] = m1 + logf(l1);
+        p.slse[static_cast<int64_t>(p.B) * p.H * p.Tq + li] = m2 + logf(l2);
+    }
     if (p.mode == 1) {
         // lam = exp(lq1 . lk1) - exp(lq2 . lk2) + lam_init ; lam_init = 0.8 - 0.6 exp(-0.3 layer)
         float d1 = 0.f, d2 = 0.f;
@@ -119,6 +127,13 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
             ss = fmaf(x[i], x[i], ss);
         }
         ss = warp_sum(ss);
+        if (train) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                p.sa1[srow + lane + 32 * i] = x[i];
+                p.sa2[srow + lane + 32 * i] = o2[i] / l2;
+            }
+        }
         // RMSNorm over the DV channels, eps 1e-5, no weight; then (1 - lam_init)
         const float r = (1.f - lam_init) / sqrtf(ss / static_cast<float>(DV) + 1e-5f);
 #pragma unroll
@@ -129,6 +144,13 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
         const float i1 = 1.f / l1, i2 = sg / l2;
 #pragma unroll
         for (int i = 0; i < NV; ++i) out[lane + 32 * i] = o1[i] * i1 - o2[i] * i2;
+        if (train) {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                p.sa1[srow + lane + 32 * i] = o1[i] * i1;
+                p.sa2[srow + lane + 32 * i] = o2[i] / l2;
+            }
+        }
     }
 }
 

@@ -210,8 +210,10 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
                              da_dtype dtype, cudaStream_t stream);
 
 /* ---- training: forward with saved tensors, and the backward -----------
- * Supported: DA_BF16 only; V1 d = 64 (dv = 128), V2 D in {64, 128}; other
- * combinations return DA_ERR_UNSUPPORTED_DIM.
+ * Supported: DA_BF16 on the tensor cores: V1 d = 64 (dv = 128), V2 D in
+ * {64, 128}; DA_F32 on CUDA cores: V1 d in {32, 64, 128}, V2 D in {64, 128}
+ * (every tensor, dout and the gradients fp32).  Other combinations return
+ * DA_ERR_UNSUPPORTED_DIM.  The size functions take the same dtype.
  *
  * `saved` (DEVICE, caller-owned, at least *_train_saved_size() bytes,
  * 16-byte aligned) receives each branch's normalised attention output a_b
@@ -222,10 +224,10 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
  * entry are ignored.  Gradient outputs must not overlap any input; they are
  * fully overwritten (not accumulated into).  Sizes functions return 0 for
  * unsupported sizes. */
-size_t diffattn_v1_train_saved_size(int B, int T, int H, int d);
-size_t diffattn_v1_bwd_workspace_size(int B, int T, int H, int d);
-size_t diffattn_v2_train_saved_size(int B, int T, int Hq, int Hkv, int D);
-size_t diffattn_v2_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D);
+size_t diffattn_v1_train_saved_size(int B, int T, int H, int d, da_dtype dtype);
+size_t diffattn_v1_bwd_workspace_size(int B, int T, int H, int d, da_dtype dtype);
+size_t diffattn_v2_train_saved_size(int B, int T, int Hq, int Hkv, int D, da_dtype dtype);
+size_t diffattn_v2_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, da_dtype dtype);
 
 /* DIFF V1 training forward: arguments, layouts and strides as
  * diffattn_v1_fwd, plus `saved`. */

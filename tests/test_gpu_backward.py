@@ -116,8 +116,9 @@ def test_v2_backward(B, T, Hq, Hkv, D):
 
 def test_backward_argument_checks():
     bd = binding()
-    assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128) == 0      # d = 128: no backward kernel
-    assert bd.lib().diffattn_v2_bwd_workspace_size(1, 128, 6, 2, 128) > 0
+    assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128, 1) == 0   # bf16 d = 128: no backward kernel
+    assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128, 0) > 0    # fp32 d = 128: CUDA-core backward
+    assert bd.lib().diffattn_v2_bwd_workspace_size(1, 128, 6, 2, 128, 1) > 0
     x = to_dev(inputs.make_v2(inputs.V2Shape(1, 64, 4, 2, 128, "bf16"), seed=1))
     out, saved = bd.v2_fwd_train(x["q"], x["k"], x["v"], x["lam"])
     dout = torch.zeros_like(out)
@@ -158,3 +159,55 @@ def test_v2_backward_long_sequence():
     ref = oracle.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout)
     for n in ("dq", "dk", "dv", "dlam"):
         check_grad(n, g[n], ref[n])
+
+
+# ------------------------------------------------------------------ fp32 path
+# fp32 everywhere (CUDA cores, exact fp32 sums): the bound is the fp32 one of
+# the forward, max abs <= 1e-4, taken relative to the gradient's scale
+# (max abs <= 1e-4 * max(1, max|ref|)); the lambda-vector gradients against
+# the size of the terms that cancel in dL/dlam, as for bf16 but at 1e-4.
+
+def check_f32(name, got, ref):
+    got = got.detach().double().cpu().numpy().reshape(ref.shape)
+    err = np.abs(got - ref).max()
+    assert np.isfinite(got).all() and err <= 1e-4 * max(1.0, np.abs(ref).max()), f"{name}: max abs {err:.3e}"
+
+
+@pytest.mark.parametrize("B,T,H,d", [(2, 45, 2, 32), (1, 70, 3, 64), (1, 33, 2, 128)])
+def test_v1_backward_fp32(B, T, H, d):
+    x = inputs.make_v1(inputs.V1Shape(B, T, H, d, 3, "fp32"), seed=T)
+    dout = inputs.make_grad_out((B, T, H, 2 * d), "fp32", seed=T)
+    xd, dd = to_dev(x), dout.cuda()
+    out, g = run_v1(xd, dd, 3)
+    assert binding().last_launch_count() == 4
+    assert binding().device_error() == 0
+    plain = binding().v1_fwd(xd["q1"], xd["q2"], xd["k1"], xd["k2"], xd["v"], xd["lam_q1"], xd["lam_k1"],
+                             xd["lam_q2"], xd["lam_k2"], 3)
+    assert torch.equal(out, plain)
+    ref = oracle.v1_bwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"],
+                        x["lam_k2"], 3, dout)
+    for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
+        check_f32(n, g[n], ref[n])
+    lv = {k: x[k].double().numpy() for k in ("lam_q1", "lam_k1", "lam_q2", "lam_k2")}
+    e1 = np.exp((lv["lam_q1"] * lv["lam_k1"]).sum())
+    e2 = np.exp((lv["lam_q2"] * lv["lam_k2"]).sum())
+    for n, f in {"dlam_q1": e1 * lv["lam_k1"], "dlam_k1": e1 * lv["lam_q1"],
+                 "dlam_q2": e2 * lv["lam_k2"], "dlam_k2": e2 * lv["lam_q2"]}.items():
+        err = np.abs(g[n].double().cpu().numpy() - ref[n])
+        assert (err <= 1e-4 * ref["dlam_abs"] * np.abs(f) + 1e-7).all(), n
+
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,D", [(2, 40, 4, 2, 64), (1, 57, 8, 2, 128)])
+def test_v2_backward_fp32(B, T, Hq, Hkv, D):
+    x = inputs.make_v2(inputs.V2Shape(B, T, Hq, Hkv, D, "fp32"), seed=T)
+    dout = inputs.make_grad_out((B, T, Hq // 2, D), "fp32", seed=T)
+    xd, dd = to_dev(x), dout.cuda()
+    bd = binding()
+    out, saved = bd.v2_fwd_train(xd["q"], xd["k"], xd["v"], xd["lam"])
+    assert torch.equal(out, bd.v2_fwd(xd["q"], xd["k"], xd["v"], xd["lam"]))
+    g = bd.v2_bwd(xd["q"], xd["k"], xd["v"], xd["lam"], dd, saved)
+    assert bd.last_launch_count() == 3
+    assert bd.device_error() == 0
+    ref = oracle.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout)
+    for n in ("dq", "dk", "dv", "dlam"):
+        check_f32(n, g[n], ref[n])
