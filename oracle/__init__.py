@@ -76,6 +76,10 @@ def _load():
             lib.oracle_v2_bwd.restype = ctypes.c_int
             lib.oracle_v2_bwd.argtypes = ([dp] * 5 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64] + [dp] * 4
                                           + [ctypes.c_int])
+            lib.oracle_rope.restype = None
+            lib.oracle_rope.argtypes = [dp] + [ctypes.c_int] * 4 + [ctypes.c_int64, ctypes.c_double, dp]
+            lib.oracle_lambda_proj.restype = None
+            lib.oracle_lambda_proj.argtypes = [dp, dp, ctypes.c_int64, ctypes.c_int, ctypes.c_int, dp]
             lib.oracle_v1_decode.restype = ctypes.c_int
             lib.oracle_v1_decode.argtypes = ([dp] * 9 + [ctypes.c_int, ctypes.c_int64] + [ctypes.c_int] * 3
                                              + [i64p, i64p, ctypes.c_int64, dp, ctypes.c_int])
@@ -286,6 +290,29 @@ def v2_bwd(q, k, v, lam, dout, groups=None, nthreads: int | None = None) -> dict
     if rc:
         raise RuntimeError(f"oracle_v2_bwd failed ({rc})")
     return g
+
+
+def rope(x, pos0: int = 0, base: float = 10000.0) -> np.ndarray:
+    """Rotary position embedding (rotate-half form) of x (B, T, H, D) at
+    positions pos0 + t; returns fp64 (B, T, H, D)."""
+    x = _f64(x)
+    B, T, H, D = x.shape
+    assert D % 2 == 0
+    out = np.empty_like(x)
+    _load().oracle_rope(_ptr(x), B, T, H, D, int(pos0), float(base), _ptr(out))
+    return out
+
+
+def lambda_proj(x, w) -> np.ndarray:
+    """Projected lambda logits x @ w: x (..., C), w (C, P) -> (..., P) fp64."""
+    x, w = _f64(x), _f64(w)
+    C, P = w.shape
+    lead = x.shape[:-1]
+    assert x.shape[-1] == C
+    xf = np.ascontiguousarray(x.reshape(-1, C))
+    out = np.empty((xf.shape[0], P), dtype=np.float64)
+    _load().oracle_lambda_proj(_ptr(xf), _ptr(w), xf.shape[0], C, P, _ptr(out))
+    return out.reshape(*lead, P)
 
 
 def decode_gather(q, k_cache, v_cache, lam, rows):

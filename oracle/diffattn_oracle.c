@@ -684,3 +684,50 @@ int oracle_v2_bwd(const double *q, const double *k, const double *v,
     free(ids);
     return rc;
 }
+
+/* ======================================================================
+ * Neighbours of the attention call (the prologue).
+ *
+ * Rotary position embedding as the nanoGPT issue applies it to q and k
+ * before the attention (RotaryEmbedding(dim = head_dim) and
+ * apply_rotary_pos_emb; the class itself is not printed, so the plainest
+ * reading is taken: the rotate-half form with base 10000): for a row of
+ * head dim D at position p and each i < D/2, with theta = p * base^(-2i/D),
+ *   out[i]       = x[i] cos(theta) - x[i + D/2] sin(theta)
+ *   out[i + D/2] = x[i + D/2] cos(theta) + x[i] sin(theta).
+ * x: (B, T, H, D) contiguous, positions pos0 + t.
+ * ==================================================================== */
+void oracle_rope(const double *x, int B, int T, int H, int D, int64_t pos0,
+                 double base, double *out)
+{
+    const int half = D / 2;
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t) {
+            const double pos = (double)(pos0 + t);
+            for (int h = 0; h < H; ++h) {
+                const int64_t row = (((int64_t)b * T + t) * H + h) * D;
+                for (int i = 0; i < half; ++i) {
+                    const double theta = pos * pow(base, -2.0 * (double)i / (double)D);
+                    const double c = cos(theta), s = sin(theta);
+                    const double x1 = x[row + i], x2 = x[row + i + half];
+                    out[row + i] = x1 * c - x2 * s;
+                    out[row + i + half] = x2 * c + x1 * s;
+                }
+            }
+        }
+}
+
+/* DIFF V2's projected lambda ("a projected lambda for each token and each
+ * head"): lam[n, i] = sum_c x[n, c] w[c, i] for every token n; x (N, C),
+ * w (C, P), out (N, P). */
+void oracle_lambda_proj(const double *x, const double *w, int64_t N, int C,
+                        int P, double *out)
+{
+    for (int64_t n = 0; n < N; ++n)
+        for (int i = 0; i < P; ++i) {
+            double acc = 0.0;
+            for (int c = 0; c < C; ++c)
+                acc += x[n * C + c] * w[(int64_t)c * P + i];
+            out[n * P + i] = acc;
+        }
+}

@@ -13,6 +13,7 @@ import pytest
 
 import test_oracle_bwd_pins as bwd_pins
 import test_oracle_pins as pins
+import test_oracle_prologue_pins as pro_pins
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 ORACLE_DIR = os.path.join(ROOT, "oracle")
@@ -53,6 +54,12 @@ MUTANTS = {
                                            "J->dlam[tok * P + i] = -sg * da;"),
     "bwd: V1 branch-2 gradient not scaled by lam": ("g2[c] = -J->lam_full * dx[c];", "g2[c] = -dx[c];"),
     "bwd: dk from the key instead of the query": ("dkj[c] += scale * ds * q[c];", "dkj[c] += scale * ds * kj[c];"),
+    "rope: sign of the sine in the first half": ("out[row + i] = x1 * c - x2 * s;", "out[row + i] = x1 * c + x2 * s;"),
+    "rope: frequency exponent -i/D": ("pow(base, -2.0 * (double)i / (double)D)", "pow(base, -(double)i / (double)D)"),
+    "rope: pairs i with i + 1": ("const double x1 = x[row + i], x2 = x[row + i + half];",
+                                 "const double x1 = x[row + i], x2 = x[row + (i + 1) % D];"),
+    "lambda projection reads w transposed": ("acc += x[n * C + c] * w[(int64_t)c * P + i];",
+                                             "acc += x[n * C + c] * w[(int64_t)i * C + c];"),
     "decode drops the last cache row": ("attend_row(qe, k, kv_row, v, kv_row, L, D, D, scale, scores, a1);",
                                         "attend_row(qe, k, kv_row, v, kv_row, L - 1, D, D, scale, scores, a1);"),
 }
@@ -82,6 +89,10 @@ CHECKS = [
     bwd_pins.test_v1_bwd_finite_differences_of_the_forward,
     bwd_pins.test_v2_bwd_finite_differences_of_the_forward,
     bwd_pins.test_bwd_closed_forms,
+    pro_pins.test_rope_identity_norm_and_inverse,
+    pro_pins.test_rope_scores_depend_on_distance_only,
+    pro_pins.test_rope_complex_form_and_quarter_turn,
+    pro_pins.test_lambda_proj_one_hot_and_library,
 ]
 
 
