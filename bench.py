@@ -10,7 +10,8 @@ TFLOP/s), long-context DIFF V1 (B=1, T=32768, 12 heads, d=128, TFLOP/s),
 DIFF V2 decode (B=64, L=32768, Hq=64, Hkv=8, D=128, HBM GB/s), the same decode
 with per-sequence cache lengths uniform on 1..L, DIFF V1 decode (B=32,
 L=16384, 12 heads, d=128, HBM GB/s), and the backward (training) pass of the
-V1 headline and V2 prefill workloads (TFLOP/s).
+V1 headline and V2 prefill workloads (TFLOP/s), and the prologue (rotary q,
+k and the projected V2 lambda, HBM GB/s).
 
 Usage:
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -386,6 +387,23 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                         "tokens_per_s": round(s.B / (ms * 1e-3)), "launches": 2, "peak_kind": peak_kind}
     del x, out, ws
     torch.cuda.empty_cache()
+    # prologue (rotary q, k in place + projected lambda) on the V2 prefill workload
+    s = inputs.WORKLOADS["v2_bf16_B8_T4096_Hq32_Hkv8_D128"]
+    x = inputs.make_v2(s, seed=args.seed, device=dev)
+    C, P = (s.Hq // 2) * s.D, s.Hq // 2
+    lp = inputs.make_lambda_proj(s.B, s.T, C, P, "bf16", seed=args.seed, device=dev)
+    lam = torch.empty((s.B, s.T, P), dtype=torch.float32, device=dev)
+    f = lambda: binding.prologue(q=x["q"], k=x["k"], x=lp["x"], w_lam=lp["w_lam"], lam=lam)  # noqa: E731
+    for _ in range(3):
+        f()
+    ms = sum(t := time_steps(f, 10, flush)) / len(t)
+    nbytes = 2 * (x["q"].numel() + x["k"].numel()) * 2 + lp["x"].numel() * 2 + lp["w_lam"].numel() * 2 + lam.numel() * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    aux["prologue"] = {"workload": "v2_bf16_B8_T4096_Hq32_Hkv8_D128, x (B,T,2048), w (2048,16)", "ms": round(ms, 4),
+                       "GB/s": round(gbs, 1), "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                       "bytes": int(nbytes), "launches": 1, "peak_kind": peak_kind}
+    del x, lp, lam
+    torch.cuda.empty_cache()
     # backward (training): DIFF V1 on the headline workload, DIFF V2 on the prefill workload
     s = inputs.WORKLOADS[HEADLINE]
     x = inputs.make_v1(s, seed=args.seed, device=dev)
@@ -529,6 +547,7 @@ CASES = {
     # backward of the headline V1 workload / a quarter of the V2 prefill workload (profiler-sized)
     "v1_bwd": ("v1_bwd", "v1_bf16_B4_T2048_H16_d64"),
     "v2_bwd_b2": ("v2_bwd", None),
+    "prologue": ("prologue", "v2_bf16_B8_T4096_Hq32_Hkv8_D128"),
 }
 
 
@@ -551,6 +570,9 @@ def run_case(name: str, launches: int):
     elif kind == "decode_varlen":
         f = lambda: binding.v2_decode_varlen(x["q"], x["k_cache"], x["v_cache"], x["lam"],  # noqa: E731
                                              x["cache_lens"])
+    elif kind == "prologue":
+        lp = inputs.make_lambda_proj(s.B, s.T, (s.Hq // 2) * s.D, s.Hq // 2, "bf16", seed=0, device=dev)
+        f = lambda: binding.prologue(q=x["q"], k=x["k"], x=lp["x"], w_lam=lp["w_lam"])  # noqa: E731
     elif kind == "v1_bwd":
         a = (x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"],
              s.layer_index)

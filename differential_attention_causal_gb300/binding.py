@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v2_bwd.restype = i32
             L.diffattn_v2_bwd.argtypes = ([vp, vp, vp, fp, vp, vp, sz, vp, vp, vp, fp, vp, sz] + [i32] * 5
                                           + [i32, vp])
+            L.diffattn_prologue.restype = i32
+            L.diffattn_prologue.argtypes = ([vp, vp] + [i32] * 5 + [i64, ctypes.c_float, vp, vp, fp] + [i32] * 2
+                                            + [i32, vp])
             L.diffattn_status_string.restype = ctypes.c_char_p
             L.diffattn_status_string.argtypes = [i32]
             L.diffattn_device_error.restype = i32
@@ -437,3 +440,41 @@ def v2_bwd(q, k, v, lam, dout, saved, workspace: torch.Tensor | None = None, str
                                _dtype_code(q), _stream(stream))
     _check("diffattn_v2_bwd", rc)
     return {"dq": dq, "dk": dk, "dv": dv, "dlam": dlam}
+
+
+# ------------------------------------------------------------------ prologue
+
+def prologue(q=None, k=None, pos0: int = 0, base: float = 10000.0, x=None, w_lam=None, lam=None, stream=None):
+    """Rotary embedding of q (B, T, Hq, D) and k (B, T, Hk, D) in place and, if
+    x (B, T, C) and w_lam (C, P) are given, the V2 lambda logits x @ w_lam
+    (fp32 (B, T, P), written to lam or a new tensor), in one kernel.
+    Returns lam (or None)."""
+    ref = q if q is not None else (k if k is not None else x)
+    if ref is None:
+        raise ValueError("nothing to do")
+    for n, t in (("q", q), ("k", k), ("x", x), ("w_lam", w_lam)):
+        if t is not None:
+            _cuda(t, n)
+            if not t.is_contiguous():
+                raise ValueError(f"{n} must be contiguous")
+    shp = (q if q is not None else k).shape if (q is not None or k is not None) else None
+    if shp is not None:
+        B, T, _, D = shp
+    else:
+        B, T, _ = x.shape
+        D = 64
+    Hq = q.shape[2] if q is not None else 0
+    Hk = k.shape[2] if k is not None else 0
+    C = P = 0
+    if x is not None:
+        if w_lam is None:
+            raise ValueError("x needs w_lam")
+        C, P = w_lam.shape
+        if lam is None:
+            lam = torch.empty((B, T, P), dtype=torch.float32, device=x.device)
+    rc = lib().diffattn_prologue(None if q is None else q.data_ptr(), None if k is None else k.data_ptr(),
+                                 B, T, Hq, Hk, D, int(pos0), float(base),
+                                 None if x is None else x.data_ptr(), None if w_lam is None else w_lam.data_ptr(),
+                                 None if lam is None else lam.data_ptr(), C, P, _dtype_code(ref), _stream(stream))
+    _check("diffattn_prologue", rc)
+    return lam

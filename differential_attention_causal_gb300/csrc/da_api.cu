@@ -832,6 +832,36 @@ da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const flo
 
 }  // extern "C"
 
+// ------------------------------------------------------------ prologue
+
+extern "C" da_status diffattn_prologue(void *q, void *k, int B, int T, int Hq, int Hk, int D, int64_t pos0,
+                                       float base, const void *x, const void *w_lam, float *lam, int C, int P,
+                                       da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if ((Hq > 0 && !q) || (Hk > 0 && !k) || (x && (!w_lam || !lam))) return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || Hq < 0 || Hk < 0 || !(base > 0.f) || (x && (C < 1 || P < 1))) return DA_ERR_BAD_SHAPE;
+    if (!prologue_supported(D, x ? C : 0, x ? P : 0)) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {static_cast<const void *>(q), static_cast<const void *>(k), x, w_lam})
+        if (ptr && !aligned16(ptr)) return DA_ERR_MISALIGNED;
+    if (lam && !aligned16(lam)) return DA_ERR_MISALIGNED;
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    t_last_launches = 0;
+    if (Hq + Hk == 0 && !x) return DA_OK;   // nothing to do
+    PrologueParams p{};
+    p.q = Hq > 0 ? q : nullptr;
+    p.k = Hk > 0 ? k : nullptr;
+    p.Hq = Hq; p.Hk = Hk; p.D = D;
+    p.x = x; p.w = w_lam; p.lam = lam;
+    p.C = x ? C : 0; p.P = x ? P : 0;
+    p.B = B; p.T = T;
+    p.pos0 = pos0;
+    p.base = static_cast<double>(base);
+    const da_status st = cuda_status(launch_prologue(p, dtype == DA_BF16, stream));
+    if (st == DA_OK) t_last_launches = 1;
+    return st;
+}
+
 // ---------------------------------------------------------------------------
 // Decode without allocation: the split-KV partials go to a buffer the library
 // owns, so a caller that may not allocate device memory passes only inputs

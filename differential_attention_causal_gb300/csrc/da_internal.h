@@ -142,6 +142,21 @@ cudaError_t launch_simt_backward(const SimtBwdParams &p, int dqk, int dv, cudaSt
 cudaError_t launch_backward(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, int dqk, int dv, bool v2,
                             cudaStream_t s);
 
+// -------------------------------------------------------------- prologue
+// Rotary embedding of q, k in place and the V2 projected lambda (k_prologue.cu).
+struct PrologueParams {
+    void *q, *k;                   // (B, T, Hq, D), (B, T, Hk, D) contiguous; either may be NULL
+    int Hq, Hk, D;
+    const void *x, *w;             // (B, T, C), (C, P) contiguous; x NULL = no projection
+    float *lam;                    // (B, T, P) fp32
+    int C, P;
+    int B, T;
+    int64_t pos0;                  // position of token t is pos0 + t
+    double base;
+};
+bool prologue_supported(int D, int C, int P);
+cudaError_t launch_prologue(const PrologueParams &p, bool bf16, cudaStream_t s);
+
 // --------------------------------------------------------------- decode
 // One kernel family serves three decodes:
 //   V2      : kv head g of sequence b feeds the G query heads g*G .. g*G+G-1;

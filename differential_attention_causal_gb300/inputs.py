@@ -187,6 +187,16 @@ def make_grad_out(shape, dtype: str = "bf16", seed: int = 0, device="cpu") -> to
     return _normal(tuple(shape), 1.0, _DT[dtype], g, device)
 
 
+def make_lambda_proj(B: int, T: int, C: int, P: int, dtype: str = "bf16", seed: int = 0, device="cpu") -> dict:
+    """Inputs of DIFF V2's projected lambda: the layer input x (B, T, C) ~ N(0, 1)
+    and a random-init projection w (C, P) ~ N(0, 0.02^2) (no trained weights
+    exist here), drawn in that order with their own generator (seed + 2000003)."""
+    g = _gen(int(seed) + 2000003, device)
+    x = _normal((B, T, C), 1.0, _DT[dtype], g, device)
+    w = _normal((C, P), 0.02, _DT[dtype], g, device)
+    return {"x": x, "w_lam": w}
+
+
 def make(shape, seed: int = 0, device="cpu") -> dict:
     if isinstance(shape, V1Shape):
         return make_v1(shape, seed, device)

@@ -26,6 +26,8 @@
  *                       the lambda logits) for an upstream gradient dout; the
  *                       pages train these models, the backward is the chain
  *                       rule of the same definitions.
+ *   diffattn_prologue   the neighbours before the attention: rotary embedding of
+ *                       q and k, and V2's projected lambda logits.
  *   diffattn_v1_decode  DiffAttnV1 for one new query token per sequence against
  *                       cached k1, k2, v rows (all L, or a length per sequence);
  *                       the remark names V1 decoding as the case that needs
@@ -267,6 +269,24 @@ da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const flo
                           const void *dout, const void *saved, size_t saved_bytes, void *dq,
                           void *dk, void *dv, float *dlam, void *workspace, size_t workspace_bytes,
                           int B, int T, int Hq, int Hkv, int D, da_dtype dtype, cudaStream_t stream);
+
+/* Prologue of the attention call, in one pass over device memory:
+ *   - rotary position embedding of q (B, T, Hq, D) and k (B, T, Hk, D) in
+ *     place (contiguous, dtype as given), the rotate-half form: for the
+ *     token at position pos0 + t and i < D/2, theta = pos * base^(-2i/D),
+ *     (x_i, x_{i+D/2}) -> (x_i cos - x_{i+D/2} sin, x_{i+D/2} cos + x_i sin)
+ *     ("How best to implement a differential transformer?", the issue's
+ *     RotaryEmbedding / apply_rotary_pos_emb applied to q and k before the
+ *     attention; base 10000 there).  Hq or Hk may be 0 (that tensor is
+ *     skipped).  For DIFF V1 pass the interleaved (B, T, 2H, d) q and k.
+ *   - if x != NULL, DIFF V2's projected lambda ("Differential Transformer
+ *     V2": a projected lambda for each token and head): lam (B, T, P) fp32
+ *     = x (B, T, C) @ w_lam (C, P), x and w_lam in dtype, fp32 sums.
+ * Supported: D in {32, 64, 128}; C a multiple of 128; P a multiple of 8 in
+ * 8..64.  Pointers 16-byte aligned. */
+da_status diffattn_prologue(void *q, void *k, int B, int T, int Hq, int Hk, int D, int64_t pos0,
+                            float base, const void *x, const void *w_lam, float *lam, int C, int P,
+                            da_dtype dtype, cudaStream_t stream);
 
 /* Static string for a status code (never NULL). */
 const char *diffattn_status_string(da_status s);
