@@ -67,6 +67,8 @@ def _load():
             lib.oracle_v1_fwd.argtypes = [dp] * 9 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64, dp, ctypes.c_int]
             lib.oracle_v2_fwd.restype = ctypes.c_int
             lib.oracle_v2_fwd.argtypes = [dp] * 4 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64, dp, ctypes.c_int]
+            lib.oracle_paired_fwd.restype = ctypes.c_int
+            lib.oracle_paired_fwd.argtypes = [dp] * 3 + [ctypes.c_int] * 4 + [i64p, ctypes.c_int64, dp, ctypes.c_int]
             lib.oracle_v2_decode.restype = ctypes.c_int
             lib.oracle_v2_decode.argtypes = ([dp] * 4 + [ctypes.c_int, ctypes.c_int64] + [ctypes.c_int] * 3
                                              + [i64p, i64p, ctypes.c_int64, dp, ctypes.c_int])
@@ -178,6 +180,28 @@ def v2_fwd(q, k, v, lam, rows=None, nthreads: int | None = None) -> np.ndarray:
     if rc:
         raise RuntimeError(f"oracle_v2_fwd failed ({rc})")
     return out if r is not None else out.reshape(B, T, Hq // 2, D)
+
+
+def paired_fwd(q, k, v, rows=None, nthreads: int | None = None) -> np.ndarray:
+    """Paired Head Attention (modded-nanogpt pull request "New Record: Paired
+    Head Attention (-3.5s, -65 steps)", section "Updates in PR"): heads 2i and 2i+1
+    are interleaved into one causal sequence of length 2T (position 2t + e is
+    token t of head 2i + e) and attended with one softmax; outputs return to
+    (token, head).
+
+    q, k, v: (B, T, H, D), H even.  rows=None returns (B, T, H, D); otherwise
+    flat ids (b*T + t)*H + h.
+    """
+    q, k, v = (_f64(x) for x in (q, k, v))
+    B, T, H, D = q.shape
+    assert H % 2 == 0 and k.shape == q.shape and v.shape == q.shape
+    r, rp, n = _rows(rows)
+    out = np.empty(((n if r is not None else B * T * H), D), dtype=np.float64)
+    rc = _load().oracle_paired_fwd(_ptr(q), _ptr(k), _ptr(v), B, T, H, D, rp, n, _ptr(out),
+                                   nthreads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle_paired_fwd failed ({rc})")
+    return out if r is not None else out.reshape(B, T, H, D)
 
 
 def _lens(lens, B, L):

@@ -25,6 +25,10 @@
  *       first CausalSelfAttention: subln = RMSNorm(2*head_dim, eps=1e-5,
  *       no affine); second: scores scaled by 1/sqrt(k.size(-1)) and masked
  *       with a lower-triangular causal mask.
+ *   modded-nanogpt pull request "New Record: Paired Head Attention (-3.5s,
+ *       -65 steps)", section "Updates in PR": the k, q and v of two heads are
+ *       interleaved into one sequence twice as long, attended causally with
+ *       one softmax (paired_row below).
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - softmax scale is 1/sqrt(d), d = query/key head dim;
@@ -107,7 +111,7 @@ void oracle_rmsnorm(const double *x, int n, double eps, double *y)
 
 /* ---- work splitting over rows ----------------------------------------- */
 typedef struct {
-    int kind;                 /* 1 = V1, 2 = V2 prefill, 3 = V2 decode */
+    int kind;                 /* 1 = V1, 2 = V2 prefill, 3 = V2 decode, 4 = V1 decode, 5 = paired heads */
     const double *q1, *q2, *k1, *k2, *v, *lam;
     double lam_full, lam_init;
     int B, T, H, dqk, dv, Hkv, G;
@@ -231,10 +235,57 @@ static void v1dec_row(const job_t *J, int64_t r, double *scores, double *a1,
     v1_combine(J, a1, a2, x, y);
 }
 
+/* Paired Head Attention row id r = (b*T + t)*H + h (modded-nanogpt pull
+ * request "New Record: Paired Head Attention (-3.5s, -65 steps)", section
+ * "Updates in PR").  The k, q and v of heads 2i and 2i+1 are
+ * interleaved into one sequence of length 2T, position 2t + e holding token t
+ * of head 2i + e; plain causal softmax attention runs over that sequence and
+ * its outputs are de-interleaved back to (token, head).  So the query of
+ * token t, head 2i + e attends the interleaved positions 0 .. 2t + e: both
+ * heads' keys of tokens before t, head 2i's key of token t, and for e = 1
+ * also its own.  Layouts (contiguous): q, k, v (B,T,H,D); out row = D. */
+static void paired_row(const job_t *J, int64_t r, double *scores, double *a)
+{
+    const int H = J->H, T = J->T, D = J->dqk;
+    const int h = (int)(r % H);
+    const int t = (int)((r / H) % T);
+    const int b = (int)(r / ((int64_t)H * T));
+    const int i = h / 2, e = h % 2;
+    const double *q = J->q1 + (((int64_t)b * T + t) * H + h) * D;
+    const double scale = 1.0 / sqrt((double)D);
+    const int64_t n = 2 * (int64_t)t + e + 1;      /* interleaved positions 0 .. 2t+e */
+    double mx = -INFINITY;
+    for (int64_t s = 0; s < n; ++s) {
+        const int64_t ts = s / 2, hs = 2 * i + (int)(s % 2);
+        const double *ks = J->k1 + (((int64_t)b * T + ts) * H + hs) * D;
+        double x = 0.0;
+        for (int c = 0; c < D; ++c)
+            x += q[c] * ks[c];
+        x *= scale;
+        scores[s] = x;
+        if (x > mx)
+            mx = x;
+    }
+    double sum = 0.0;
+    for (int64_t s = 0; s < n; ++s) {
+        scores[s] = exp(scores[s] - mx);
+        sum += scores[s];
+    }
+    for (int c = 0; c < D; ++c)
+        a[c] = 0.0;
+    for (int64_t s = 0; s < n; ++s) {
+        const int64_t ts = s / 2, hs = 2 * i + (int)(s % 2);
+        const double *vs = J->v + (((int64_t)b * T + ts) * H + hs) * D;
+        const double w = scores[s] / sum;
+        for (int c = 0; c < D; ++c)
+            a[c] += w * vs[c];
+    }
+}
+
 static void *worker(void *arg)
 {
     const job_t *J = (const job_t *)arg;
-    const int64_t nkeys = (J->kind >= 3) ? J->L : (int64_t)J->T;
+    const int64_t nkeys = (J->kind == 5) ? 2 * (int64_t)J->T : (J->kind >= 3) ? J->L : (int64_t)J->T;
     const int dv = J->dv;
     double *scores = (double *)malloc(sizeof(double) * (size_t)(nkeys > 0 ? nkeys : 1));
     double *buf = (double *)malloc(sizeof(double) * (size_t)dv * 4);
@@ -253,6 +304,8 @@ static void *worker(void *arg)
             v2_row(J, r, scores, a1, a2, y);
         else if (J->kind == 3)
             dec_row(J, r, scores, a1, a2, y);
+        else if (J->kind == 5)
+            paired_row(J, r, scores, y);
         else
             v1dec_row(J, r, scores, a1, a2, x, y);
     }
@@ -327,6 +380,23 @@ int oracle_v2_fwd(const double *q, const double *k, const double *v,
     J.Hkv = Hkv; J.G = Hq / Hkv;
     J.rows = rows;
     J.nrows = rows ? nrows : (int64_t)B * T * (Hq / 2);
+    J.out = out;
+    return run_jobs(&J, nthreads);
+}
+
+/* Paired Head Attention forward: H heads (even), pairs (2i, 2i+1).
+ * rows: ids (b*T+t)*H+h, or NULL for all.  out: nrows x D. */
+int oracle_paired_fwd(const double *q, const double *k, const double *v,
+                      int B, int T, int H, int D, const int64_t *rows,
+                      int64_t nrows, double *out, int nthreads)
+{
+    job_t J;
+    memset(&J, 0, sizeof(J));
+    J.kind = 5;
+    J.q1 = q; J.k1 = k; J.v = v;
+    J.B = B; J.T = T; J.H = H; J.dqk = D; J.dv = D;
+    J.rows = rows;
+    J.nrows = rows ? nrows : (int64_t)B * T * H;
     J.out = out;
     return run_jobs(&J, nthreads);
 }

@@ -12,6 +12,7 @@ import os
 import pytest
 
 import test_oracle_bwd_pins as bwd_pins
+import test_oracle_paired_pins as paired_pins
 import test_oracle_pins as pins
 import test_oracle_prologue_pins as pro_pins
 
@@ -60,13 +61,21 @@ MUTANTS = {
                                  "const double x1 = x[row + i], x2 = x[row + (i + 1) % D];"),
     "lambda projection reads w transposed": ("acc += x[n * C + c] * w[(int64_t)c * P + i];",
                                              "acc += x[n * C + c] * w[(int64_t)i * C + c];"),
+    "paired: own position excluded": ("const int64_t n = 2 * (int64_t)t + e + 1;      /* interleaved positions 0 .. 2t+e */",
+                                      "const int64_t n = 2 * (int64_t)t + e + (t > 0 ? 0 : 1);"),
+    "paired: partner's key of the same token always visible": (
+        "const int64_t n = 2 * (int64_t)t + e + 1;      /* interleaved positions 0 .. 2t+e */",
+        "const int64_t n = 2 * (int64_t)t + 2;"),
+    "paired: heads swapped in the interleave": ("const int64_t ts = s / 2, hs = 2 * i + (int)(s % 2);",
+                                                "const int64_t ts = s / 2, hs = 2 * i + 1 - (int)(s % 2);"),
+    "paired: pairs (i, i + H/2)": ("const int i = h / 2, e = h % 2;", "const int i = h % (H / 2), e = h / (H / 2);"),
     "decode drops the last cache row": ("attend_row(qe, k, kv_row, v, kv_row, L, D, D, scale, scores, a1);",
                                         "attend_row(qe, k, kv_row, v, kv_row, L - 1, D, D, scale, scores, a1);"),
 }
 
 # mutants whose text stands at more than one site (every site is mutated:
 # the same mistake made in the prefill, decode and backward of one variant)
-SITES = {"scale 1/sqrt(2d) in V1": 3, "V1 combine sign": 2}
+SITES = {"scale 1/sqrt(2d) in V1": 3, "V1 combine sign": 2, "paired: heads swapped in the interleave": 2}
 
 # pin checks that take only the oracle (parametrised ones get one case each)
 CHECKS = [
@@ -93,6 +102,10 @@ CHECKS = [
     pro_pins.test_rope_scores_depend_on_distance_only,
     pro_pins.test_rope_complex_form_and_quarter_turn,
     pro_pins.test_lambda_proj_one_hot_and_library,
+    paired_pins.test_paired_page_interleave_order,
+    paired_pins.test_paired_page_visibility_example,
+    paired_pins.test_paired_matches_library_sdpa_on_interleaved,
+    paired_pins.test_paired_closed_forms,
 ]
 
 
