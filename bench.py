@@ -48,7 +48,7 @@ L2_FLUSH_BYTES = 256 << 20
 # it was taken on (sha256 of the .cu file, first 16 hex digits).
 TRAFFIC_RECORDS: dict = {
     # profiles/prefill_onepass_v1_B4_T2048_H16_d64.md: dram__bytes_read.sum + dram__bytes_write.sum
-    "prefill_v1_d64": {"src_sha": "56af0a817adb1f81", "bytes_per_launch": 147878912 + 13930752},
+    "prefill_v1_d64": {"src_sha": "24079bf3989c007f", "bytes_per_launch": 148169984 + 13982720},
 }
 
 
@@ -63,6 +63,13 @@ def v1_flops(s) -> float:
 def v2_flops(s) -> float:
     """DIFF V2 prefill: per query head and causal pair 2D (QK) + 2D (PV)."""
     return float(s.B) * s.Hq * s.T * (s.T + 1) / 2 * 4 * s.D
+
+
+def paired_flops(s) -> float:
+    """Paired Head Attention: one causal attention per head pair over the
+    interleaved 2T positions: per causal (query, key) position pair 2D (QK)
+    + 2D (PV); pairs per head pair = 2T (2T + 1) / 2."""
+    return float(s.B) * (s.H // 2) * (2 * s.T) * (2 * s.T + 1) / 2 * 4 * s.D
 
 
 def v1_bwd_flops(s) -> float:
@@ -404,6 +411,21 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                        "bytes": int(nbytes), "launches": 1, "peak_kind": peak_kind}
     del x, lp, lam
     torch.cuda.empty_cache()
+    # Paired Head Attention (interleaved head pairs, one causal softmax) on the V2 prefill's query heads
+    s = inputs.WORKLOADS["paired_bf16_B8_T4096_H32_D128"]
+    x = inputs.make_paired(s, seed=args.seed, device=dev)
+    out = torch.empty_like(x["q"])
+    f = lambda: binding.paired_fwd(x["q"], x["k"], x["v"], out=out)  # noqa: E731
+    for _ in range(3):
+        f()
+    ms = sum(t := time_steps(f, 10, flush)) / len(t)
+    tf = paired_flops(s) / (ms * 1e-3) / 1e12
+    aux["paired_prefill"] = {"workload": "paired_bf16_B8_T4096_H32_D128", "ms": round(ms, 4),
+                             "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                             "flop_count": "4D per head pair and causal pair of the 2T interleaved positions",
+                             "launches": 1, "peak_kind": peak_kind}
+    del x, out
+    torch.cuda.empty_cache()
     # backward (training): DIFF V1 on the headline workload, DIFF V2 on the prefill workload
     s = inputs.WORKLOADS[HEADLINE]
     x = inputs.make_v1(s, seed=args.seed, device=dev)
@@ -548,6 +570,9 @@ CASES = {
     "v1_bwd": ("v1_bwd", "v1_bf16_B4_T2048_H16_d64"),
     "v2_bwd_b2": ("v2_bwd", None),
     "prologue": ("prologue", "v2_bf16_B8_T4096_Hq32_Hkv8_D128"),
+    "paired": ("paired", "paired_bf16_B8_T4096_H32_D128"),
+    # a quarter of its batch, for multi-pass profiler captures
+    "paired_b2": ("paired", None),
 }
 
 
@@ -559,6 +584,8 @@ def run_case(name: str, launches: int):
         s = inputs.WORKLOADS[wl]
     elif kind == "v2_bwd":
         s = inputs.V2Shape(2, 4096, 32, 8, 128, "bf16")
+    elif kind == "paired":
+        s = inputs.PairedShape(2, 4096, 32, 128, "bf16")
     else:
         s = inputs.DecodeShape(8, 32768, 64, 8, 128, "bf16")
     x = inputs.make(s, seed=0, device=dev)
@@ -567,6 +594,8 @@ def run_case(name: str, launches: int):
                                    x["lam_q2"], x["lam_k2"], s.layer_index)
     elif kind == "v2":
         f = lambda: binding.v2_fwd(x["q"], x["k"], x["v"], x["lam"])  # noqa: E731
+    elif kind == "paired":
+        f = lambda: binding.paired_fwd(x["q"], x["k"], x["v"])  # noqa: E731
     elif kind == "decode_varlen":
         f = lambda: binding.v2_decode_varlen(x["q"], x["k_cache"], x["v_cache"], x["lam"],  # noqa: E731
                                              x["cache_lens"])

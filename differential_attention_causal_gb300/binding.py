@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v1_fwd.argtypes = ([vp] * 5 + [fp] * 4 + [vp] + [i32] * 5 + [i64] * 12 + [i32, vp])
             L.diffattn_v2_fwd.restype = i32
             L.diffattn_v2_fwd.argtypes = [vp, vp, vp, fp, vp] + [i32] * 5 + [i32, vp]
+            L.diffattn_paired_fwd.restype = i32
+            L.diffattn_paired_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 4 + [i32, vp]
             L.diffattn_v2_decode_workspace_size.restype = ctypes.c_size_t
             L.diffattn_v2_decode_workspace_size.argtypes = [i32] * 6
             L.diffattn_v2_decode.restype = i32
@@ -186,6 +188,29 @@ def v2_fwd(q, k, v, lam, out: torch.Tensor | None = None, stream=None) -> torch.
     rc = lib().diffattn_v2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), out.data_ptr(),
                                B, T, Hq, Hkv, D, _dtype_code(q), _stream(stream))
     _check("diffattn_v2_fwd", rc)
+    return out
+
+
+def paired_fwd(q, k, v, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Paired Head Attention, causal (modded-nanogpt pull request "New Record:
+    Paired Head Attention (-3.5s, -65 steps)"): heads 2i and 2i+1 interleaved
+    into one sequence of 2T positions with one softmax.
+
+    q, k, v: (B, T, H, D) contiguous bf16 CUDA tensors, H even, D in {64, 128}.
+    Returns out (B, T, H, D).
+    """
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape")
+    B, T, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib().diffattn_paired_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, T, H, D,
+                                   _dtype_code(q), _stream(stream))
+    _check("diffattn_paired_fwd", rc)
     return out
 
 

@@ -85,6 +85,20 @@ bool encode_map_4d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t d1
     return r == CUDA_SUCCESS;
 }
 
+bool encode_map_pairs(CUtensorMap *m, const void *base, uint64_t D, uint64_t H, uint64_t T, uint64_t B) {
+    auto fn = encode_fn();
+    if (!fn || (H & 1) || D % 64 != 0) return false;
+    cuuint64_t dims[5] = {D, 2, H / 2, T, B};
+    cuuint64_t strides[4] = {D * 2, 2 * D * 2, H * D * 2, T * H * D * 2};
+    cuuint32_t box[5] = {64, 2, 1, 64, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    std::memset(m, 0, sizeof(*m));
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace da
 
 using namespace da;
@@ -242,6 +256,37 @@ da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const flo
     const da_status st = cuda_status(launch_prefill(m, p, D, D, true, stream));
     if (st == DA_OK) t_last_launches = 1;
     return st;
+}
+
+da_status diffattn_paired_fwd(const void *q, const void *k, const void *v, void *out, int B, int T, int H, int D,
+                              da_dtype dtype, cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q || !k || !v || !out) return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || H < 2 || (H & 1)) return DA_ERR_BAD_SHAPE;
+    if (dtype != DA_BF16 || !paired_supported(D)) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q, k, v, static_cast<const void *>(out)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    t_last_launches = 0;
+    PrefillMaps m;
+    const uint64_t uT = static_cast<uint64_t>(T), uB = static_cast<uint64_t>(B), uH = static_cast<uint64_t>(H);
+    const int64_t st = static_cast<int64_t>(H) * D;
+    if (!encode_map_4d(&m.q1, q, D, uH, uT, uB, D, st, st * T, 128) ||
+        !encode_map_pairs(&m.k1, k, D, uH, uT, uB) || !encode_map_pairs(&m.v, v, D, uH, uT, uB))
+        return DA_ERR_CUDA;
+    m.q2 = m.q1;
+    m.k2 = m.k1;
+    m.out = m.q1;   // not read: the paired epilogue stores directly
+    PrefillParams p{};
+    p.out = out;
+    p.o_sh = D; p.o_st = st; p.o_sb = st * T;
+    p.B = B; p.T = T; p.H = H / 2; p.G = 2;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.err = err;
+    const da_status s = cuda_status(launch_paired(m, p, D, stream));
+    if (s == DA_OK) t_last_launches = 1;
+    return s;
 }
 
 size_t diffattn_v2_decode_workspace_size(int B, int L, int Hq, int Hkv, int D, da_dtype dtype) {

@@ -71,6 +71,15 @@ struct PrefillMaps {
 cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
                            cudaStream_t s);
 // The same kernel with the training epilogue (p.sa1, p.sa2, p.slse written).
+// Paired Head Attention forward on the one-pass kernel (bf16, D in {64, 128}):
+// m.q1 = m.q2 = a 4-D map of q, m.k1 = m.k2 and m.v 5-D interleaved maps of
+// k and v (encode_map_pairs); p.H = pairs, p.G = 2, p.out / p.o_* the output.
+bool paired_supported(int d);
+cudaError_t launch_paired(const PrefillMaps &m, const PrefillParams &p, int d, cudaStream_t s);
+// 5-D map over a contiguous (B, T, H, D) bf16 tensor read as {D, 2, H/2, T, B}
+// with boxes {64, 2, 1, 64, 1}: 64 tokens of both heads of one pair, in the
+// interleaved order (token, head) -- 128 rows of 128 bytes, 128-byte swizzle.
+bool encode_map_pairs(CUtensorMap *m, const void *base, uint64_t D, uint64_t H, uint64_t T, uint64_t B);
 cudaError_t launch_prefill_train(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
                                  cudaStream_t s);
 bool prefill_supported(int dqk, int dv, bool v2);

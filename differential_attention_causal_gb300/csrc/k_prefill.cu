@@ -36,6 +36,17 @@
 // sigmoid(lam[b,t,pair]) (V2); V1 then applies RMSNorm over the DV channels
 // (eps 1e-5) and the (1 - lam_init) scale; the bf16 tile is staged in shared
 // memory and written with TMA stores.
+//
+// Paired Head Attention (modded-nanogpt pull request "New Record: Paired Head
+// Attention (-3.5s, -65 steps)", section "Updates in PR") runs on the same
+// machinery (PAIRED, a V2-shaped instantiation): the keys and values of heads
+// 2i and 2i+1 form one interleaved sequence of 2T positions (position 2t + e
+// = token t of head 2i + e), which a 5-D tensor map reads directly as
+// 64 tokens x 2 heads per 128-row key tile.  Branch e takes the queries of
+// head 2i + e for 128 tokens, so both branches need the same key tiles
+// (0 .. 2 qt + 1) and differ only in the causal limit of the last two: row r
+// of branch e sees interleaved key columns c <= 2r + e - 128 (j - 2 qt).  The
+// epilogue writes O_e / l_e of each branch to its own head with direct stores.
 #include "da_common.cuh"
 #include "da_internal.h"
 
@@ -69,7 +80,7 @@ struct PreCfg {
     static constexpr int OFF_X = OFF_OUT;
     static constexpr int OFF_BAR = OFF_OUT + OUT_TILE;
     // qfull, qfree, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s[2], p[2][2], o[2], odrain, drain, lam
-    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 3;
+    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 5;
     static constexpr int OFF_LAM = OFF_BAR + NBAR * 8;        // 2 floats
     static constexpr int OFF_TSLOT = OFF_LAM + 8;
     static constexpr int SMEM = OFF_TSLOT + 8 + 1024;         // + alignment slack
@@ -118,13 +129,14 @@ __device__ __forceinline__ int snake_tile(int k, int c, int G, int NT) {
     return w < NT ? w : -1;
 }
 
-template <int DQK, int DV, bool V2, bool TRAIN>
+template <int DQK, int DV, bool V2, bool TRAIN, bool PAIRED>
 __global__ void __launch_bounds__(384, 1)
     prefill_onepass(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
                     const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tout,
                     const PrefillParams p) {
     using C = PreCfg<DQK, DV, V2>;
+    static_assert(!PAIRED || (V2 && !TRAIN && DQK == DV), "paired heads: V2-shaped forward only");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -135,6 +147,10 @@ __global__ void __launch_bounds__(384, 1)
     const int n_qt = (p.T + C::BM - 1) / C::BM;
     const int per_qt = p.H * p.B;
     const int NT = n_qt * per_qt;
+    // key tiles of query tile qt: the causal ones; for paired heads the keys are
+    // the interleaved sequence (two positions per token, 2T in all)
+    const int n_kt = PAIRED ? (2 * p.T + C::BN - 1) / C::BN : n_qt;
+    auto kv_tiles = [&](int qt) { return PAIRED ? min(2 * qt + 2, n_kt) : qt + 1; };
     const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
 
     const uint32_t bar_qf = sbase + C::OFF_BAR;
@@ -149,6 +165,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t bar_od = bar_o + 16;                // O read by the epilogue (8 warps)
     const uint32_t bar_dr = bar_od + 8;
     const uint32_t bar_lam = bar_dr + 8;
+    const uint32_t bar_stg = bar_lam + 8, bar_stf = bar_stg + 8;
     const uint32_t tslot = sbase + C::OFF_TSLOT;
     const uint32_t sQ1 = sbase + C::OFF_Q1, sQ2 = sbase + C::OFF_Q2;
     float *lam_smem = reinterpret_cast<float *>(smem + C::OFF_LAM);
@@ -173,6 +190,8 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(bar_od, 8);
         mbar_init(bar_dr, 1);
         mbar_init(bar_lam, 1);
+        mbar_init(bar_stg, 8);
+        mbar_init(bar_stf, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -206,7 +225,10 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_arrive_expect_tx(bar_kf + 8 * st, C::K_SLOT);
 #pragma unroll
                 for (int c = 0; c < C::QB; ++c) {
-                    tma_load_4d(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
+                    if (PAIRED)   // 64 tokens x both heads of pair hk, interleaved
+                        tma_load_5d(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, 0, hk, j * (C::BN / 2), b);
+                    else
+                        tma_load_4d(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
                     if (!V2)
                         tma_load_4d(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
                 }
@@ -221,8 +243,12 @@ __global__ void __launch_bounds__(384, 1)
                 const uint32_t dst = sbase + C::OFF_V + st * C::V_SLOT;
                 mbar_arrive_expect_tx(bar_vf + 8 * st, C::V_SLOT);
 #pragma unroll
-                for (int c = 0; c < C::VB; ++c)
-                    tma_load_4d(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b);
+                for (int c = 0; c < C::VB; ++c) {
+                    if (PAIRED)
+                        tma_load_5d(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, 0, hk, j * (C::BN / 2), b);
+                    else
+                        tma_load_4d(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b);
+                }
                 ++vc;
                 return true;
             };
@@ -230,7 +256,7 @@ __global__ void __launch_bounds__(384, 1)
                 const int w = snake_tile(k, cta, G, NT);
                 if (w < 0) break;
                 const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
-                const int h = rest % p.H, b = rest / p.H, n_kv = qt + 1;
+                const int h = rest % p.H, b = rest / p.H, n_kv = kv_tiles(qt);
                 const int hq1 = V2 ? 2 * h : h, hq2 = V2 ? 2 * h + 1 : h;
                 const int hk = V2 ? (2 * h) / p.G : h;
                 // Q of this tile once the previous tile's last QK has been issued
@@ -291,7 +317,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = 0; ok; ++k) {
                 const int w = snake_tile(k, cta, G, NT);
                 if (w < 0) break;
-                const int n_kv = n_qt - w / per_qt;
+                const int n_kv = kv_tiles(n_qt - 1 - w / per_qt);
                 ok = mbar_wait(bar_qf, static_cast<uint32_t>(tc & 1), p.err) && wait_k();
                 if (!ok) break;
                 tc_fence_after();
@@ -374,6 +400,25 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 3) {
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
+        if (lane == 0 && !PAIRED) {
+            bool ok = true;
+            for (int k = 0;; ++k) {
+                const int w = snake_tile(k, cta, G, NT);
+                if (w < 0) break;
+                const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
+                const int h = rest % p.H, b = rest / p.H;
+                ok = ok && mbar_wait(bar_stg, static_cast<uint32_t>(k & 1), p.err);
+                if (ok) {
+#pragma unroll
+                    for (int bx = 0; bx < C::VB; ++bx)
+                        tma_store_4d(&tout, sbase + C::OFF_OUT + bx * C::BOX, 64 * bx, h, qt * C::BM, b);
+                    bulk_commit();
+                }
+                bulk_wait_read_all();
+                mbar_arrive(bar_stf);
+            }
+            bulk_wait_all();
+        }
     } else {
         // -------------------------------------------------------- softmax
         if (C::REG_SPLIT) regs_increase<C::REGS_HIGH>();
@@ -400,10 +445,10 @@ __global__ void __launch_bounds__(384, 1)
             const int w = snake_tile(k, cta, G, NT);
             if (w < 0) break;
             const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
-            const int h = rest % p.H, b = rest / p.H, n_kv = qt + 1;
+            const int h = rest % p.H, b = rest / p.H, n_kv = kv_tiles(qt);
             const int t = qt * C::BM + row;   // query token of this thread's row
             // V2 gate logit of this row, fetched now and used in the epilogue
-            const float lg = (V2 && t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
+            const float lg = (V2 && !PAIRED && t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < n_kv; ++j, ++it) {
                 ok = warp_wait(my_s, static_cast<uint32_t>(it & 1), p.err, ok);
@@ -415,10 +460,11 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_ld32(tS + 64, s + 64);
                 tmem_ld32(tS + 96, s + 96);
                 tmem_wait_ld();
-                if (j == qt) {   // diagonal tile: keys past this row are masked
+                if (PAIRED ? j >= 2 * qt : j == qt) {   // diagonal tile(s): keys past this row are masked
+                    const int lim = PAIRED ? 2 * row + br - C::BN * (j - 2 * qt) : row;   // last visible column
 #pragma unroll
                     for (int c = 0; c < C::BN; ++c)
-                        if (c > row) s[c] = 0xff800000u;   // -inf
+                        if (c > lim) s[c] = 0xff800000u;   // -inf
                 }
                 const float m_new = fmaxf(m_ref, row_max128(s) * sl2);
                 float alpha = 1.f;
@@ -458,7 +504,37 @@ __global__ void __launch_bounds__(384, 1)
             }
 
             // --------------------------------------------------- epilogue
+            if constexpr (PAIRED) {
+                // each branch is one head of the pair: O_e / l_e to its rows, directly
+                ok = warp_wait(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
+                tc_fence_after();
+                const float il = 1.f / l;
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + static_cast<int64_t>(b) * p.o_sb +
+                                     static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(2 * h + br) * p.o_sh;
+#pragma unroll
+                for (int cc = 0; cc < DV; cc += 32) {
+                    uint32_t a[32];
+                    tmem_ld32(tO + cc, a);
+                    tmem_wait_ld();
+                    if (ok && t < p.T) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc);
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            const uint32_t *aa = a + 8 * q8;
+                            d4[q8] = make_uint4(pack_bf16(__uint_as_float(aa[0]) * il, __uint_as_float(aa[1]) * il),
+                                                pack_bf16(__uint_as_float(aa[2]) * il, __uint_as_float(aa[3]) * il),
+                                                pack_bf16(__uint_as_float(aa[4]) * il, __uint_as_float(aa[5]) * il),
+                                                pack_bf16(__uint_as_float(aa[6]) * il, __uint_as_float(aa[7]) * il));
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_od);   // O read: the next tile's first PV may overwrite it
+                continue;
+            }
             ok = warp_wait(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
+            if (k > 0) ok = warp_wait(bar_stf, static_cast<uint32_t>((k - 1) & 1), p.err, ok);
             tc_fence_after();
             if (TRAIN && t < p.T)   // this branch's log-sum-exp (log2 units) for the backward
                 p.slse[((static_cast<int64_t>(br) * p.B + b) * p.H + h) * p.T + t] = m_ref + __log2f(l);
@@ -546,21 +622,13 @@ __global__ void __launch_bounds__(384, 1)
                                            ((ch ^ (row & 7)) << 4)) = v;
             }
             fence_async_smem();
-            named_bar_sync(1, 256);
-            if (warp == 4 && lane == 0) {
-                if (ok) {
-#pragma unroll
-                    for (int bx = 0; bx < C::VB; ++bx)
-                        tma_store_4d(&tout, sbase + C::OFF_OUT + bx * C::BOX, 64 * bx, h, qt * C::BM, b);
-                    bulk_commit();
-                }
-                bulk_wait_read_all();   // staging tile (and exchange area) reusable
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_stg);
         }
     }
 
     // ------------------------------------------------------------ teardown
-    if (warp == 4 && lane == 0) bulk_wait_all();   // output stores complete before exit
+    if (warp == 3 && lane == 0) bulk_wait_all();   // output stores complete before exit
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -570,7 +638,7 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int DQK, int DV, bool V2, bool TRAIN>
+template <int DQK, int DV, bool V2, bool TRAIN, bool PAIRED = false>
 cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
     using C = PreCfg<DQK, DV, V2>;
     int dev = 0;
@@ -581,10 +649,10 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
         // grants (384 threads x registers per thread), or its increase would
         // never complete: refuse to launch otherwise.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_onepass<DQK, DV, V2, TRAIN>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_onepass<DQK, DV, V2, TRAIN, PAIRED>);
         if (e != cudaSuccess) return e;
         if (C::REG_SPLIT && fa.numRegs < C::REGS_NEEDED_AT_LAUNCH) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2, TRAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2, TRAIN, PAIRED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
@@ -602,7 +670,7 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
     }
     const int sms = dev < 64 ? num_sms[dev] : 1;
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
-    prefill_onepass<DQK, DV, V2, TRAIN><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, m.out, p);
+    prefill_onepass<DQK, DV, V2, TRAIN, PAIRED><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, m.out, p);
     return cudaGetLastError();
 }
 
@@ -618,6 +686,15 @@ cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk
     if (v2 && dqk == 128 && dv == 128) return launch_t<128, 128, true, false>(m, p, s);
     if (v2 && dqk == 64 && dv == 64) return launch_t<64, 64, true, false>(m, p, s);
     if (!v2 && dqk == 64 && dv == 128) return launch_t<64, 128, false, false>(m, p, s);
+    return cudaErrorInvalidValue;
+}
+
+bool paired_supported(int d) { return d == 64 || d == 128; }
+
+cudaError_t launch_paired(const PrefillMaps &m, const PrefillParams &p, int d, cudaStream_t s) {
+    if (p.G != 2) return cudaErrorInvalidValue;   // kv coordinate = pair index
+    if (d == 128) return launch_t<128, 128, true, false, true>(m, p, s);
+    if (d == 64) return launch_t<64, 64, true, false, true>(m, p, s);
     return cudaErrorInvalidValue;
 }
 

@@ -20,6 +20,9 @@ V1 q and k are drawn as one interleaved (B, T, 2H, d) tensor each, as the
 nanoGPT issue lays them out; q1 = q[:, :, 0::2], q2 = q[:, :, 1::2] (and the
 same for k) are strided views.  v is (B, T, H, 2d).
 
+Paired Head Attention inputs: q, k, v (B, T, H, D) ~ N(0, 1), drawn in that
+order (the pages give no workload; the shapes are the V2 prefill's query heads).
+
 Decode inputs: V2 q (B, Hq, D) and caches (B, L, Hkv, D); V1 q1, q2 (B, H, d),
 caches k1, k2 (B, L, H, d) and v (B, L, H, 2d), drawn in that order, each
 contiguous (a cache is written one row per token, so the two branches' keys
@@ -54,6 +57,16 @@ class V2Shape:
     T: int
     Hq: int
     Hkv: int
+    D: int
+    dtype: str = "bf16"
+
+
+@dataclass(frozen=True)
+class PairedShape:
+    """Paired Head Attention: H heads (H/2 interleaved pairs), head dim D."""
+    B: int
+    T: int
+    H: int
     D: int
     dtype: str = "bf16"
 
@@ -94,6 +107,8 @@ WORKLOADS = {
     # decode beyond the five: per-sequence lengths, and DIFF V1 decode
     "v2_decode_varlen_bf16_B64_L32768_Hq64_Hkv8_D128": DecodeShape(64, 32768, 64, 8, 128, "bf16", True),
     "v1_decode_bf16_B32_L16384_H12_d128": V1DecodeShape(32, 16384, 12, 128, 27, "bf16"),
+    # Paired Head Attention on the V2 prefill's query-head shapes
+    "paired_bf16_B8_T4096_H32_D128": PairedShape(8, 4096, 32, 128, "bf16"),
 }
 
 
@@ -140,6 +155,16 @@ def make_v2(s: V2Shape, seed: int = 0, device="cpu") -> dict:
     v = _normal((s.B, s.T, s.Hkv, s.D), 1.0, dt, g, device)
     lam = torch.randn((s.B, s.T, s.Hq // 2), generator=g, dtype=torch.float32, device=device)
     return {"q": q, "k": k, "v": v, "lam": lam}
+
+
+def make_paired(s: PairedShape, seed: int = 0, device="cpu") -> dict:
+    """q, k, v (B,T,H,D), drawn in that order."""
+    g = _gen(seed, device)
+    dt = _DT[s.dtype]
+    q = _normal((s.B, s.T, s.H, s.D), 1.0, dt, g, device)
+    k = _normal((s.B, s.T, s.H, s.D), 1.0, dt, g, device)
+    v = _normal((s.B, s.T, s.H, s.D), 1.0, dt, g, device)
+    return {"q": q, "k": k, "v": v}
 
 
 def make_decode(s: DecodeShape, seed: int = 0, device="cpu") -> dict:
@@ -206,4 +231,6 @@ def make(shape, seed: int = 0, device="cpu") -> dict:
         return make_decode(shape, seed, device)
     if isinstance(shape, V1DecodeShape):
         return make_v1_decode(shape, seed, device)
+    if isinstance(shape, PairedShape):
+        return make_paired(shape, seed, device)
     raise TypeError(type(shape))

@@ -28,6 +28,10 @@
  *                       rule of the same definitions.
  *   diffattn_prologue   the neighbours before the attention: rotary embedding of
  *                       q and k, and V2's projected lambda logits.
+ *   diffattn_paired_fwd modded-nanogpt pull request "New Record: Paired Head
+ *                       Attention (-3.5s, -65 steps)": heads 2i and 2i+1
+ *                       interleaved into one causal sequence of length 2T with
+ *                       one softmax (a second workload on the prefill kernel).
  *   diffattn_v1_decode  DiffAttnV1 for one new query token per sequence against
  *                       cached k1, k2, v rows (all L, or a length per sequence);
  *                       the remark names V1 decoding as the case that needs
@@ -120,6 +124,22 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
 da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const float *lam,
                           void *out, int B, int T, int Hq, int Hkv, int D,
                           da_dtype dtype, cudaStream_t stream);
+
+/* Paired Head Attention, causal (modded-nanogpt pull request "New Record:
+ * Paired Head Attention (-3.5s, -65 steps)", section "Updates in PR"): the k,
+ * q and v of heads 2i and 2i+1 are interleaved into one sequence of 2T
+ * positions (position 2t + e is token t of head 2i + e), attended with one
+ * causal softmax over it (scale 1/sqrt(D)), and the outputs are returned to
+ * their (token, head) places.  So the query of token t of head 2i + e sees
+ * both heads' keys of tokens < t, head 2i's key of token t, and for e = 1 its
+ * own.  Contiguous tensors:
+ *   q, k, v : (B, T, H, D)         H even, D in {64, 128}
+ *   out     : (B, T, H, D)
+ *   Supported: DA_BF16 only (tcgen05 one-pass kernel); DA_F32 returns
+ *   DA_ERR_UNSUPPORTED_DIM.  Errors as for the other entry points.
+ */
+da_status diffattn_paired_fwd(const void *q, const void *k, const void *v, void *out,
+                              int B, int T, int H, int D, da_dtype dtype, cudaStream_t stream);
 
 /* Bytes of device scratch that diffattn_v2_decode needs for these sizes on the
  * current device (depends on its SM count).  Returns 0 for invalid sizes. */

@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("diffattn_v1_fwd", "diffattn_v2_fwd", "diffattn_v2_decode",
               "diffattn_v2_decode_workspace_size", "diffattn_status_string", "diffattn_device_error",
-              "diffattn_v2_decode_varlen", "diffattn_v1_decode", "diffattn_v1_decode_workspace_size"):
+              "diffattn_v2_decode_varlen", "diffattn_v1_decode", "diffattn_v1_decode_workspace_size",
+              "diffattn_paired_fwd"):
         assert n in names
 
 
@@ -96,6 +97,22 @@ def test_v2_argument_checks(lib):
     assert _v2(lib, D=96) == 3
     assert _v2(lib, out=A + 2) == 5
     assert _v2(lib, dtype=2) == 8
+
+
+def _paired(lib, **kw):
+    a = dict(q=A, k=A, v=A, out=A, B=1, T=8, H=4, D=128, dtype=1)
+    a.update(kw)
+    return lib.diffattn_paired_fwd(a["q"], a["k"], a["v"], a["out"], a["B"], a["T"], a["H"], a["D"], a["dtype"], None)
+
+
+def test_paired_argument_checks(lib):
+    assert _paired(lib, v=None) == 1
+    assert _paired(lib, T=0) == 2
+    assert _paired(lib, H=3) == 2                      # heads come in pairs
+    assert _paired(lib, D=96) == 3
+    assert _paired(lib, dtype=0) == 3                  # fp32: no paired kernel
+    assert _paired(lib, out=A + 8) == 5
+    assert _paired(lib, dtype=5) == 8
 
 
 def _dec(lib, **kw):
