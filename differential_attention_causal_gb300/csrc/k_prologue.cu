@@ -18,7 +18,7 @@
 //      sine and cosine of the reduced angle in float;
 //   2. every (token, head, 8-pair chunk) of q and k: two 16-byte loads, the
 //      rotation in fp32, two stores;
-//   lambda, one CTA of 128 threads per 64 tokens:
+//   lambda, one CTA of 256 threads per 128 tokens:
 //   3. the logits of the CTA's 64 tokens: bf16 on the tensor cores
 //      (mma.sync, fp32 accumulators, x and w staged in shared memory 64
 //      channels at a time), fp32 on CUDA cores (one warp per token).
@@ -32,21 +32,32 @@
 namespace da {
 namespace {
 
-constexpr int TB = 64;          // tokens per lambda CTA (16 per warp, 4 warps)
-constexpr int LT = 128;         // threads of a lambda CTA
+constexpr int TB = 128;         // tokens per lambda CTA (16 per warp, 8 warps)
+constexpr int LT = 256;         // threads of a lambda CTA
 constexpr int TS = 32;          // tokens per rotary sub-block (one cos / sin table)
 constexpr int MAXP = 64;        // lambda logits per token
 // dynamic shared memory of the lambda kernel: LSTAGES x (TB x KC channels of
-// x + KC rows of padded w)
+// x + KC rows of w, each P logits padded by 16 bytes)
 constexpr int KC = 128;         // channels per stage of the lambda product
 constexpr int LSTAGES = 3;
-constexpr int LSTAGE = TB * KC * 2 + KC * (MAXP * 2 + 16);
-constexpr int SMEM = LSTAGES * LSTAGE;
+__host__ __device__ constexpr int lstage(int P) { return TB * KC * 2 + KC * (P * 2 + 16); }
+constexpr int SMEM_MAX = LSTAGES * lstage(MAXP);
 
 template <typename E>
 struct Vec8;                    // 8 elements <-> 8 floats
 template <>
 struct Vec8<__nv_bfloat16> {
+    using Raw = uint4;   // the 8 elements as loaded, unpacked only when used
+    static __device__ __forceinline__ Raw ld(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint4 *>(p); }
+    static __device__ __forceinline__ void unpack(const Raw &u, float *f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+            f[2 * i] = a.x;
+            f[2 * i + 1] = a.y;
+        }
+    }
     static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float *f) {
         const uint4 u = *reinterpret_cast<const uint4 *>(p);
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -64,6 +75,16 @@ struct Vec8<__nv_bfloat16> {
 };
 template <>
 struct Vec8<float> {
+    struct Raw {
+        float4 a, b;
+    };
+    static __device__ __forceinline__ Raw ld(const float *p) {
+        return Raw{*reinterpret_cast<const float4 *>(p), *reinterpret_cast<const float4 *>(p + 4)};
+    }
+    static __device__ __forceinline__ void unpack(const Raw &r, float *f) {
+        f[0] = r.a.x; f[1] = r.a.y; f[2] = r.a.z; f[3] = r.a.w;
+        f[4] = r.b.x; f[5] = r.b.y; f[6] = r.b.z; f[7] = r.b.w;
+    }
     static __device__ __forceinline__ void load(const float *p, float *f) {
         const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
         f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
@@ -82,9 +103,12 @@ struct Vec8<float> {
 // fma) and reduced modulo 2 pi against 2 pi split into three floats, each
 // step an fma (Cody and Waite's additive reduction); the reduced angle is
 // within a few 1e-7 rad of the exact one for any position below 2^24.
+// The cos / sin table of the block's TS tokens is stored [token][k][chunk]
+// (entry i = 8 chunk + k at (token * 8 + k) * CH + chunk), so that the lanes
+// of a warp, which take consecutive chunks, read consecutive entries.
 template <typename E, int D>
 __device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0, int h0, int h1,
-                                            float2 (*cs)[D / 2], const float *freq_hi, const float *freq_lo) {
+                                            float2 *cs, const float *freq_hi, const float *freq_lo) {
     constexpr int HALF = D / 2, CH = HALF / 8;
     constexpr double TWO_PI = 6.283185307179586476925286766559;
     constexpr float P1 = static_cast<float>(TWO_PI);
@@ -106,18 +130,20 @@ __device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0,
             r = fmaf(-k, P3, r) + lo;
             sincosf(r, &sn, &c);
         }
-        cs[tt][i] = make_float2(c, sn);
+        cs[(tt * 8 + i % 8) * CH + i / 8] = make_float2(c, sn);
     }
     __syncthreads();
     const int heads = h1 - h0;
     const int units = TS * heads * CH;
-    // U units per thread per round: all their loads are issued before the
-    // first rotation, so several 16-byte reads are in flight per thread
-    constexpr int U = 2;
+    // U units per thread per round: all their loads are issued (and kept
+    // packed) before the first rotation, so 2 U 16-byte reads are in flight
+    // per thread
+    constexpr int U = sizeof(E) == 2 ? 4 : 2;
+    using Raw = typename Vec8<E>::Raw;
     for (int u0 = threadIdx.x; u0 < units; u0 += U * blockDim.x) {
         E *row[U];
         int tt[U], ch[U];
-        float a[U][8], b[U][8];
+        Raw a[U], b[U];
 #pragma unroll
         for (int j = 0; j < U; ++j) {
             const int u = u0 + j * blockDim.x;
@@ -129,19 +155,21 @@ __device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0,
             if (u < units && n < ntok && (hh < p.Hq ? p.q != nullptr : p.k != nullptr)) {
                 row[j] = hh < p.Hq ? static_cast<E *>(p.q) + (n * p.Hq + hh) * D
                                    : static_cast<E *>(p.k) + (n * p.Hk + (hh - p.Hq)) * D;
-                Vec8<E>::load(row[j] + 8 * ch[j], a[j]);
-                Vec8<E>::load(row[j] + HALF + 8 * ch[j], b[j]);
+                a[j] = Vec8<E>::ld(row[j] + 8 * ch[j]);
+                b[j] = Vec8<E>::ld(row[j] + HALF + 8 * ch[j]);
             }
         }
 #pragma unroll
         for (int j = 0; j < U; ++j) {
             if (!row[j]) continue;
-            float ra[8], rb[8];
+            float fa[8], fb[8], ra[8], rb[8];
+            Vec8<E>::unpack(a[j], fa);
+            Vec8<E>::unpack(b[j], fb);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float2 t = cs[tt[j]][8 * ch[j] + k];
-                ra[k] = a[j][k] * t.x - b[j][k] * t.y;
-                rb[k] = b[j][k] * t.x + a[j][k] * t.y;
+                const float2 t = cs[(tt[j] * 8 + k) * CH + ch[j]];
+                ra[k] = fa[k] * t.x - fb[k] * t.y;
+                rb[k] = fb[k] * t.x + fa[k] * t.y;
             }
             Vec8<E>::store(row[j] + 8 * ch[j], ra);
             Vec8<E>::store(row[j] + HALF + 8 * ch[j], rb);
@@ -166,15 +194,16 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // LSTAGES-deep ring of shared-memory buffers filled with cp.async (x rows
 // 128-byte swizzled; w rows padded by 16 bytes so that ldmatrix reads them
 // without bank conflicts), so several chunks are in flight per CTA.  Warp w
-// owns tokens 16 w .. 16 w + 15 (4 warps); mma.sync m16n8k16 with fp32
+// owns tokens 16 w .. 16 w + 15 (8 warps); mma.sync m16n8k16 with fp32
 // accumulators.
 __device__ __forceinline__ void lambda_bf16(const PrologueParams &p, int64_t tok0, uint8_t *sm) {
     const int64_t ntok = static_cast<int64_t>(p.B) * p.T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wrow = p.P * 2 + 16;                         // padded w row, bytes
     const uint32_t sbase = smem_u32(sm);
-    auto xs = [&](int b) { return sbase + b * LSTAGE; };
-    auto ws = [&](int b) { return sbase + b * LSTAGE + TB * KC * 2; };
+    const int lst = lstage(p.P);
+    auto xs = [&](int b) { return sbase + b * lst; };
+    auto ws = [&](int b) { return sbase + b * lst + TB * KC * 2; };
     // x tile: rows of KC * 2 = 256 bytes, 16-byte chunk ch at
     // ((ch & 8) | ((ch & 7) ^ (row & 7))): ldmatrix's 8 rows hit 8 bank groups
     auto xoff = [](int row, int ch) { return row * (KC * 2) + (((ch & 8) | ((ch & 7) ^ (row & 7))) << 4); };
@@ -282,9 +311,9 @@ __device__ __forceinline__ void lambda_f32(const PrologueParams &p, int64_t tok0
 
 // Rotary embedding: one CTA per TS tokens (one cos / sin table), all heads.
 template <typename E, int D>
-__global__ void __launch_bounds__(256, 4) prologue_rope(const PrologueParams p) {
+__global__ void __launch_bounds__(256, 3) prologue_rope(const PrologueParams p) {
     constexpr int HALF = D / 2;
-    __shared__ float2 cs[TS][HALF];
+    __shared__ float2 cs[TS * HALF];
     __shared__ float freq_hi[HALF], freq_lo[HALF];
     // base^(-2i/D) in double, once per CTA, kept as a float pair
     for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
@@ -293,7 +322,10 @@ __global__ void __launch_bounds__(256, 4) prologue_rope(const PrologueParams p) 
         freq_lo[i] = static_cast<float>(f - static_cast<double>(freq_hi[i]));
     }
     __syncthreads();
-    rope_tokens<E, D>(p, static_cast<int64_t>(blockIdx.x) * TS, 0, p.Hq + p.Hk, cs, freq_hi, freq_lo);
+    // persistent: the grid fills the GPU once and walks the token blocks
+    const int64_t nblk = (static_cast<int64_t>(p.B) * p.T + TS - 1) / TS;
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x)
+        rope_tokens<E, D>(p, blk * TS, 0, p.Hq + p.Hk, cs, freq_hi, freq_lo);
 }
 
 // Lambda logits: one CTA per TB tokens.
@@ -311,9 +343,15 @@ cudaError_t launch_e(const PrologueParams &p, cudaStream_t s) {
     if (p.q || p.k) {
         const int64_t blocks = (ntok + TS - 1) / TS;
         if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
-        if (p.D == 32) prologue_rope<E, 32><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
-        else if (p.D == 64) prologue_rope<E, 64><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
-        else if (p.D == 128) prologue_rope<E, 128><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+        // three 256-thread CTAs per SM (the launch bound), one wave
+        int dev = 0, nsm = 0;
+        cudaError_t e0 = cudaGetDevice(&dev);
+        if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e0 != cudaSuccess) return e0;
+        const unsigned grid = static_cast<unsigned>(blocks < 3LL * nsm ? blocks : 3LL * nsm);
+        if (p.D == 32) prologue_rope<E, 32><<<grid, 256, 0, s>>>(p);
+        else if (p.D == 64) prologue_rope<E, 64><<<grid, 256, 0, s>>>(p);
+        else if (p.D == 128) prologue_rope<E, 128><<<grid, 256, 0, s>>>(p);
         else return cudaErrorInvalidValue;
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -322,13 +360,14 @@ cudaError_t launch_e(const PrologueParams &p, cudaStream_t s) {
         static bool attr_set = false;   // per process; the attribute is per function
         if (!attr_set) {
             const cudaError_t e =
-                cudaFuncSetAttribute(prologue_lambda<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+                cudaFuncSetAttribute(prologue_lambda<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
             if (e != cudaSuccess) return e;
             attr_set = true;
         }
         const int64_t blocks = (ntok + TB - 1) / TB;
         if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
-        prologue_lambda<E><<<static_cast<unsigned>(blocks), LT, SMEM, s>>>(p);
+        const int smem = sizeof(E) == 2 ? LSTAGES * lstage(p.P) : 0;   // the fp32 path stages nothing
+        prologue_lambda<E><<<static_cast<unsigned>(blocks), LT, smem, s>>>(p);
         return cudaGetLastError();
     }
     return cudaSuccess;
