@@ -253,23 +253,17 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
     traffic = tr["bytes_per_launch"] if tr and tr["src_sha"] == src_sha(
         "differential_attention_causal_gb300/csrc/k_prefill.cu") else None
 
-    # end to end through the public call with host buffers: pinned H2D of the
-    # step's inputs, the forward, D2H of the result, all inside the events.
+    # end to end through the C-ABI call on host buffers (diffattn_v1_fwd_host): the
+    # pinned H2D of the step's inputs, the forward and the D2H of the result, all
+    # inside the events; the call overlaps them chunk by chunk of batch entries.
     host = {k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()
             if k in ("q", "k", "v", "lam_q1", "lam_k1", "lam_q2", "lam_k2")}
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
-    dl = [torch.empty_like(x[n]) for n in ("lam_q1", "lam_k1", "lam_q2", "lam_k2")]
+    ws_host = torch.empty(binding.v1_fwd_host_workspace_size(s.B, s.T, s.H, s.d), dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        dq.copy_(host["q"], non_blocking=True)
-        dk.copy_(host["k"], non_blocking=True)
-        dv.copy_(host["v"], non_blocking=True)
-        for d_, n in zip(dl, ("lam_q1", "lam_k1", "lam_q2", "lam_k2")):
-            d_.copy_(host[n], non_blocking=True)
-        binding.v1_fwd(dq[:, :, 0::2], dq[:, :, 1::2], dk[:, :, 0::2], dk[:, :, 1::2], dv, *dl,
-                       s.layer_index, out=out)
-        hout.copy_(out, non_blocking=True)
+        binding.v1_fwd_host(host["q"], host["k"], host["v"], host["lam_q1"], host["lam_k1"], host["lam_q2"],
+                            host["lam_k2"], s.layer_index, hout, ws_host)
 
     for _ in range(3):
         e2e_step()

@@ -47,6 +47,11 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v1_fwd.argtypes = ([vp] * 5 + [fp] * 4 + [vp] + [i32] * 5 + [i64] * 12 + [i32, vp])
             L.diffattn_v2_fwd.restype = i32
             L.diffattn_v2_fwd.argtypes = [vp, vp, vp, fp, vp] + [i32] * 5 + [i32, vp]
+            L.diffattn_v1_fwd_host_workspace_size.restype = ctypes.c_size_t
+            L.diffattn_v1_fwd_host_workspace_size.argtypes = [i32] * 5
+            L.diffattn_v1_fwd_host.restype = i32
+            L.diffattn_v1_fwd_host.argtypes = ([vp, vp, vp, fp, fp, fp, fp, vp] + [i32] * 5
+                                               + [vp, ctypes.c_size_t, i32, vp])
             L.diffattn_paired_fwd.restype = i32
             L.diffattn_paired_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 4 + [i32, vp]
             L.diffattn_v2_decode_workspace_size.restype = ctypes.c_size_t
@@ -188,6 +193,37 @@ def v2_fwd(q, k, v, lam, out: torch.Tensor | None = None, stream=None) -> torch.
     rc = lib().diffattn_v2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), out.data_ptr(),
                                B, T, Hq, Hkv, D, _dtype_code(q), _stream(stream))
     _check("diffattn_v2_fwd", rc)
+    return out
+
+
+def v1_fwd_host_workspace_size(B: int, T: int, H: int, d: int, dtype=torch.bfloat16) -> int:
+    code = DA_BF16 if dtype == torch.bfloat16 else DA_F32
+    return int(lib().diffattn_v1_fwd_host_workspace_size(B, T, H, d, code))
+
+
+def v1_fwd_host(q, k, v, lam_q1, lam_k1, lam_q2, lam_k2, layer_index: int, out: torch.Tensor,
+                workspace: torch.Tensor, stream=None) -> torch.Tensor:
+    """DIFF V1 forward on HOST tensors (the end-to-end call): q, k (B, T, 2H, d)
+    interleaved and v (B, T, H, 2d) contiguous CPU tensors (pinned for the
+    copies to overlap), the four lambda vectors fp32 CPU tensors, `out`
+    (B, T, H, 2d) a CPU tensor, `workspace` a uint8 CUDA tensor of
+    v1_fwd_host_workspace_size() bytes.  Ordered on the current stream."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("lam_q1", lam_q1), ("lam_k1", lam_k1),
+                 ("lam_q2", lam_q2), ("lam_k2", lam_k2)):
+        if t.is_cuda:
+            raise ValueError(f"{n} must be a host tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _cuda(workspace, "workspace")
+    for t in (lam_q1, lam_k1, lam_q2, lam_k2):
+        if t.dtype != torch.float32:
+            raise ValueError("lambda vectors must be fp32")
+    B, T, H2, d = q.shape
+    rc = lib().diffattn_v1_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam_q1.data_ptr(),
+                                    lam_k1.data_ptr(), lam_q2.data_ptr(), lam_k2.data_ptr(), out.data_ptr(),
+                                    B, T, H2 // 2, d, layer_index, workspace.data_ptr(), workspace.numel(),
+                                    _dtype_code(q), _stream(stream))
+    _check("diffattn_v1_fwd_host", rc)
     return out
 
 

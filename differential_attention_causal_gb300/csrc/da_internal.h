@@ -80,6 +80,8 @@ cudaError_t launch_paired(const PrefillMaps &m, const PrefillParams &p, int d, c
 // with boxes {64, 2, 1, 64, 1}: 64 tokens of both heads of one pair, in the
 // interleaved order (token, head) -- 128 rows of 128 bytes, 128-byte swizzle.
 bool encode_map_pairs(CUtensorMap *m, const void *base, uint64_t D, uint64_t H, uint64_t T, uint64_t B);
+// The count diffattn_last_launch_count() reports for this thread's last call.
+void set_last_launches(int n);
 cudaError_t launch_prefill_train(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
                                  cudaStream_t s);
 bool prefill_supported(int dqk, int dv, bool v2);

@@ -28,6 +28,8 @@
  *                       rule of the same definitions.
  *   diffattn_prologue   the neighbours before the attention: rotary embedding of
  *                       q and k, and V2's projected lambda logits.
+ *   diffattn_v1_fwd_host  the same DiffAttnV1 forward on host buffers, copies
+ *                       overlapped with the forward (the end-to-end call).
  *   diffattn_paired_fwd modded-nanogpt pull request "New Record: Paired Head
  *                       Attention (-3.5s, -65 steps)": heads 2i and 2i+1
  *                       interleaved into one causal sequence of length 2T with
@@ -113,6 +115,32 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
                           int64_t v_sb, int64_t v_st, int64_t v_sh,
                           int64_t o_sb, int64_t o_st, int64_t o_sh,
                           da_dtype dtype, cudaStream_t stream);
+
+/* DIFF V1 forward from HOST buffers (the end-to-end call): the same operation
+ * as diffattn_v1_fwd on host-resident inputs and output, with the copies of
+ * the inputs in, the forward and the copy of the output back overlapped,
+ * chunk by chunk of batch entries (up to 8 chunks), on two copy streams of
+ * the library's own and `stream`.  The call is ordered on `stream`: work
+ * queued on it afterwards sees the output in host memory.  Layouts (host,
+ * contiguous; the nanoGPT issue's reshape(B, T, n_head, 2, d)):
+ *   q, k   : (B, T, 2H, d)   branch 1 of head h in channel block 2h, branch 2 in 2h + 1
+ *   v, out : (B, T, H, 2d)
+ *   lam_q1, lam_k1, lam_q2, lam_k2 : d fp32 each, host
+ *   workspace : device memory of diffattn_v1_fwd_host_workspace_size() bytes,
+ *               256-byte aligned, owned by the caller; holds the device copies.
+ * Host buffers should be pinned (page-locked) for the copies to run
+ * asynchronously and overlap.  Concurrent calls on one device are correct;
+ * they take the library's copy streams in turn.  Supported sizes as for
+ * diffattn_v1_fwd; errors as there, DA_ERR_WORKSPACE_TOO_SMALL for a short
+ * workspace.
+ */
+size_t diffattn_v1_fwd_host_workspace_size(int B, int T, int H, int d, da_dtype dtype);
+da_status diffattn_v1_fwd_host(const void *q, const void *k, const void *v,
+                               const float *lam_q1, const float *lam_k1,
+                               const float *lam_q2, const float *lam_k2,
+                               void *out, int B, int T, int H, int d, int layer_index,
+                               void *workspace, size_t workspace_bytes,
+                               da_dtype dtype, cudaStream_t stream);
 
 /* DIFF V2 causal prefill (contiguous tensors).
  *   q   : (B, T, Hq, D)        Hq even; G = Hq / Hkv must be an even integer

@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     for n in ("diffattn_v1_fwd", "diffattn_v2_fwd", "diffattn_v2_decode",
               "diffattn_v2_decode_workspace_size", "diffattn_status_string", "diffattn_device_error",
               "diffattn_v2_decode_varlen", "diffattn_v1_decode", "diffattn_v1_decode_workspace_size",
-              "diffattn_paired_fwd"):
+              "diffattn_paired_fwd", "diffattn_v1_fwd_host", "diffattn_v1_fwd_host_workspace_size"):
         assert n in names
 
 
@@ -113,6 +113,29 @@ def test_paired_argument_checks(lib):
     assert _paired(lib, dtype=0) == 3                  # fp32: no paired kernel
     assert _paired(lib, out=A + 8) == 5
     assert _paired(lib, dtype=5) == 8
+
+
+def _host(lib, **kw):
+    a = dict(q=A, k=A, v=A, l1=A, l2=A, l3=A, l4=A, out=A, B=2, T=8, H=2, d=64, layer=0, ws=A, wsb=1 << 30,
+             dtype=1)
+    a.update(kw)
+    return lib.diffattn_v1_fwd_host(a["q"], a["k"], a["v"], a["l1"], a["l2"], a["l3"], a["l4"], a["out"], a["B"],
+                                    a["T"], a["H"], a["d"], a["layer"], a["ws"], a["wsb"], a["dtype"], None)
+
+
+def test_v1_host_argument_checks(lib):
+    from differential_attention_causal_gb300 import binding
+    need = binding.v1_fwd_host_workspace_size(2, 8, 2, 64)
+    assert need >= 2 * 8 * 4 * 64 * 2 * 2 + 2 * 8 * 2 * 128 * 2 * 2   # q, k, v, out at least
+    assert _host(lib, out=None) == 1
+    assert _host(lib, ws=None) == 1
+    assert _host(lib, T=0) == 2
+    assert _host(lib, layer=-1) == 2
+    assert _host(lib, d=32) == 3                       # bf16 d = 32 unsupported
+    assert _host(lib, wsb=need - 1) == 6               # workspace too small
+    assert _host(lib, ws=A + 16) == 5                  # workspace not 256-byte aligned
+    assert _host(lib, dtype=3) == 8
+    assert binding.v1_fwd_host_workspace_size(0, 8, 2, 64) == 0
 
 
 def _dec(lib, **kw):
