@@ -565,6 +565,10 @@ CASES = {
     "v2_bwd_b2": ("v2_bwd", None),
     "prologue": ("prologue", "v2_bf16_B8_T4096_Hq32_Hkv8_D128"),
     "paired": ("paired", "paired_bf16_B8_T4096_H32_D128"),
+    # the V1 decode and the ragged-length decode workloads with 4 / 8 of their
+    # sequences (0.8 / 1.07 GB of cache: profiler-sized, still far larger than L2)
+    "v1_decode_b4": ("v1_decode", None),
+    "decode_varlen_b8": ("decode_varlen", None),
     # a quarter of its batch, for multi-pass profiler captures
     "paired_b2": ("paired", None),
 }
@@ -580,6 +584,10 @@ def run_case(name: str, launches: int):
         s = inputs.V2Shape(2, 4096, 32, 8, 128, "bf16")
     elif kind == "paired":
         s = inputs.PairedShape(2, 4096, 32, 128, "bf16")
+    elif kind == "v1_decode":
+        s = inputs.V1DecodeShape(4, 16384, 12, 128, 27, "bf16")
+    elif kind == "decode_varlen":
+        s = inputs.DecodeShape(8, 32768, 64, 8, 128, "bf16", True)
     else:
         s = inputs.DecodeShape(8, 32768, 64, 8, 128, "bf16")
     x = inputs.make(s, seed=0, device=dev)
