@@ -24,12 +24,17 @@
 //   bwd_dkdv    key-stationary: 128 key rows, 64-query sub-tiles (for V2 of
 //               every pair of the kv group).  TMEM: S1^T | S2^T | dP^T (64
 //               each) | dK1 (| dK2) | dV.
-// In both, warp 0 streams the sub-tiles with TMA, warp 1 issues the MMAs,
-// and two row warpgroups (warps 4-7, 8-11; thread = TMEM lane = row) each
-// take 32 of a sub-tile's 64 columns.  The rows load S and dP, release that
-// TMEM at once (the next sub-tile's products start on the tensor cores),
-// form P, dS in fp32 and write them in bf16 to 128-byte-swizzled shared
-// tiles, the A operands of the accumulating MMAs (dV, dK_b or dQ_b).
+// In both, warp 0 streams the sub-tiles with TMA, warp 1 issues the score
+// MMAs (S, dP), warp 2 the accumulating ones, and two row warpgroups (warps
+// 4-7, 8-11; thread = TMEM lane = row) each take 32 of a sub-tile's 64
+// columns.  The rows load S and dP, release that TMEM at once (the next
+// sub-tile's products start on the tensor cores), form P, dS in fp32 and
+// write them in bf16 to 128-byte-swizzled shared tiles, the A operands of
+// the accumulating MMAs (dV, dK_b or dQ_b).  Two issuing threads because a
+// thread's barrier wait returns only after the MMAs it issued before it
+// have drained: with one issuer every wait left the tensor pipe idle.
+#include <type_traits>
+
 #include "da_common.cuh"
 #include "da_internal.h"
 
@@ -48,12 +53,18 @@ struct BwdCfg {
     static constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false);
     static constexpr uint32_t IDESC_QK = idesc_bf16(128, DQK, true);
     static constexpr uint32_t IDESC_V = idesc_bf16(128, DV, true);
-    static constexpr int THREADS = 384;   // warp 0 TMA, warp 1 MMA, warps 4-11 two row warpgroups
+    // warp 0 TMA, warp 1 MMA, warps 4.. NRG row warpgroups, each taking RC of a sub-tile's 64 columns
+    static constexpr int NRG = 2, RC = BN / NRG;
+    static constexpr int THREADS = 128 + 128 * NRG;
+    // MMAs issued by two threads: warp 1 the score products (S, dP), warp 2 the
+    // accumulating ones; each thread's barrier waits then stall only its own
+    // stream while the other's MMAs keep the tensor pipe busy
+    static constexpr bool TWO_ISSUERS = true;
     static constexpr int MIN_SMEM = 120 * 1024;   // one CTA per SM (each takes all of TMEM)
 
     // ---- dq kernel: resident Q1, Q2, G (128 rows); ring of K1 (, K2), V (64 rows);
     //      result tiles dS1, dS2 (128 x 64 bf16, the A operands of dQ += dS K)
-    static constexpr int DQ_STAGES = 3;
+    static constexpr int DQ_STAGES = DQK == 64 ? 4 : 3;   // shared memory
     static constexpr int DQ_OFF_Q1 = 0;
     static constexpr int DQ_OFF_Q2 = QB * RBOX;
     static constexpr int DQ_OFF_G = 2 * QB * RBOX;
@@ -61,8 +72,8 @@ struct BwdCfg {
     static constexpr int DQ_OFF_RING = DQ_OFF_RES + 2 * RBOX;
     static constexpr int DQ_STAGE = NK * QB * CBOX + VB * CBOX;
     static constexpr int DQ_OFF_BAR = DQ_OFF_RING + DQ_STAGES * DQ_STAGE;
-    // res, full[S], empty[S], s, sfree, rready, rfree, done, drain
-    static constexpr int DQ_NBAR = 1 + 2 * DQ_STAGES + 6;
+    // res, full[S], empty[S], s, sfree, rready, rfree, done, drain, drain of the score issuer
+    static constexpr int DQ_NBAR = 1 + 2 * DQ_STAGES + 7;
     static constexpr int DQ_OFF_TSLOT = DQ_OFF_BAR + DQ_NBAR * 8;
     static constexpr int DQ_SMEM_RAW = DQ_OFF_TSLOT + 8 + 1024;
     static constexpr int DQ_SMEM = DQ_SMEM_RAW > MIN_SMEM ? DQ_SMEM_RAW : MIN_SMEM;
@@ -80,7 +91,7 @@ struct BwdCfg {
     static constexpr int KV_STAGE_TMA = 2 * QB * CBOX + VB * CBOX;
     static constexpr int KV_STAGE = KV_STAGE_TMA + 2048;           // vectors, padded to keep 1 KB alignment
     static constexpr int KV_OFF_BAR = KV_OFF_RING + KV_STAGES * KV_STAGE;
-    static constexpr int KV_NBAR = 1 + 2 * KV_STAGES + 6;
+    static constexpr int KV_NBAR = 1 + 2 * KV_STAGES + 7;
     static constexpr int KV_OFF_TSLOT = KV_OFF_BAR + KV_NBAR * 8;
     static constexpr int KV_SMEM_RAW = KV_OFF_TSLOT + 8 + 1024;
     static constexpr int KV_SMEM = KV_SMEM_RAW > MIN_SMEM ? KV_SMEM_RAW : MIN_SMEM;
@@ -93,19 +104,31 @@ struct BwdCfg {
     static_assert(KV_VEC <= 2048, "vector area");
 };
 
-// 16 bf16 pairs from 32 floats held as bit patterns
-__device__ __forceinline__ void pack32(const uint32_t *x, uint32_t *u) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) u[i] = pack_bf16(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+// RC consecutive fp32 columns of this thread's TMEM lane (RC = 16 or 32)
+template <int RC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t *r) {
+    static_assert(RC == 16 || RC == 32, "columns per row thread");
+    if constexpr (RC == 32)
+        tmem_ld32(taddr, r);
+    else
+        tmem_ld16(taddr, r);
 }
 
-// Write 32 bf16 values (16 packed words) of one row into a 128-row x 64-col
-// K-major tile with 128-byte swizzle (the layout a TMA box of that shape
-// has), at 16-byte chunks 4 * half .. 4 * half + 3 of the row.
-__device__ __forceinline__ void store_row_half(uint8_t *tile, int row, int half, const uint32_t *u) {
+// RC / 2 bf16 pairs from RC floats held as bit patterns
+template <int RC>
+__device__ __forceinline__ void pack_cols(const uint32_t *x, uint32_t *u) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int ch = 4 * half + k;
+    for (int i = 0; i < RC / 2; ++i) u[i] = pack_bf16(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+}
+
+// Write RC bf16 values (RC / 2 packed words) of one row into a 128-row x
+// 64-col K-major tile with 128-byte swizzle (the layout a TMA box of that
+// shape has), at the row's 16-byte chunks RC / 8 * part .. RC / 8 * part + RC / 8 - 1.
+template <int RC>
+__device__ __forceinline__ void store_row_part(uint8_t *tile, int row, int part, const uint32_t *u) {
+#pragma unroll
+    for (int k = 0; k < RC / 8; ++k) {
+        const int ch = RC / 8 * part + k;
         *reinterpret_cast<uint4 *>(tile + row * 128 + ((ch ^ (row & 7)) << 4)) =
             make_uint4(u[4 * k], u[4 * k + 1], u[4 * k + 2], u[4 * k + 3]);
     }
@@ -120,7 +143,7 @@ __device__ __forceinline__ void store_row_half(uint8_t *tile, int row, int half,
 //         the result tiles ("rfree"); write dS(j) -> rready.
 // So S(j+1) and dP(j+1) run on the tensor cores while the rows work on j.
 template <int DQK, int DV, bool V2>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
     bwd_dq(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
            const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tk1,
            const __grid_constant__ CUtensorMap tk2, const __grid_constant__ CUtensorMap tv, const BwdParams p) {
@@ -153,6 +176,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t bar_rfree = bar_rready + 8;
     const uint32_t bar_done = bar_rfree + 8;
     const uint32_t bar_dr = bar_done + 8;
+    const uint32_t bar_dra = bar_dr + 8;
     const uint32_t tslot = sbase + C::DQ_OFF_TSLOT;
 
     if (threadIdx.x == 0) {
@@ -162,11 +186,12 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_sfree, 8);
-        mbar_init(bar_rready, 8);
+        mbar_init(bar_sfree, 4 * C::NRG);   // one arrival per row warp
+        mbar_init(bar_rready, 4 * C::NRG);
         mbar_init(bar_rfree, 1);
         mbar_init(bar_done, 1);
         mbar_init(bar_dr, 1);
+        mbar_init(bar_dra, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -217,7 +242,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = (j > ST ? j - ST : 0); k < j; ++k)
                 mbar_wait(bar_full + 8 * (k % ST), static_cast<uint32_t>((k / ST) & 1), p.err);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (C::TWO_ISSUERS && warp == 2)) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
             const uint32_t sQ1 = sbase + C::DQ_OFF_Q1, sQ2 = sbase + C::DQ_OFF_Q2, sG = sbase + C::DQ_OFF_G;
@@ -238,52 +263,86 @@ __global__ void __launch_bounds__(384, 1)
                 mma_commit(bar_empty + 8 * (jj % ST));   // K, V of jj no longer needed
                 mma_commit(bar_rfree);                    // result tiles read
             };
-            bool ok = mbar_wait(bar_res, 0, p.err);
-            int j = 0;
-            for (; ok && j < n_kv; ++j) {
-                const int st = j % ST;
+            // S_b = Q_b K_b^T (N = 64 keys), dP = G V^T for sub-tile j
+            auto scores = [&](int j) {
                 const uint32_t sK1 = k1_at(j);
                 const uint32_t sK2 = V2 ? sK1 : sK1 + C::QB * C::CBOX;
                 const uint32_t sV = sK1 + C::NK * C::QB * C::CBOX;
-                ok = mbar_wait(bar_full + 8 * st, static_cast<uint32_t>((j / ST) & 1), p.err) &&
-                     (j == 0 || mbar_wait(bar_sfree, static_cast<uint32_t>((j - 1) & 1), p.err));
-                if (!ok) break;
-                tc_fence_after();
-                // S_b = Q_b K_b^T (N = 64 keys), dP = G V^T
-                {
-                    const uint64_t a1 = sdesc_sw128(sQ1, 16, 1024), a2 = sdesc_sw128(sQ2, 16, 1024);
-                    const uint64_t b1 = sdesc_sw128(sK1, 16, 1024), b2 = sdesc_sw128(sK2, 16, 1024);
+                const uint64_t a1 = sdesc_sw128(sQ1, 16, 1024), a2 = sdesc_sw128(sQ2, 16, 1024);
+                const uint64_t b1 = sdesc_sw128(sK1, 16, 1024), b2 = sdesc_sw128(sK2, 16, 1024);
 #pragma unroll
-                    for (int ks = 0; ks < DQK / 16; ++ks) {
-                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
-                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
-                        mma_ss(tmem + C::COL_S1, a1 + oa, b1 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
-                        mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
-                    }
-                    const uint64_t ag = sdesc_sw128(sG, 16, 1024), bv = sdesc_sw128(sV, 16, 1024);
+                for (int ks = 0; ks < DQK / 16; ++ks) {
+                    const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                    const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                    mma_ss(tmem + C::COL_S1, a1 + oa, b1 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                }
+                const uint64_t ag = sdesc_sw128(sG, 16, 1024), bv = sdesc_sw128(sV, 16, 1024);
 #pragma unroll
-                    for (int ks = 0; ks < DV / 16; ++ks) {
-                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
-                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
-                        mma_ss(tmem + C::COL_DP, ag + oa, bv + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
-                    }
+                for (int ks = 0; ks < DV / 16; ++ks) {
+                    const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                    const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                    mma_ss(tmem + C::COL_DP, ag + oa, bv + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_s);
-                if (j > 0) {
-                    ok = mbar_wait(bar_rready, static_cast<uint32_t>((j - 1) & 1), p.err);
+            };
+            // S(j) needs sub-tile j in the ring and the rows done loading S(j-1)
+            auto wait_scores = [&](int j) {
+                return mbar_wait(bar_full + 8 * (j % ST), static_cast<uint32_t>((j / ST) & 1), p.err) &&
+                       (j == 0 || mbar_wait(bar_sfree, static_cast<uint32_t>((j - 1) & 1), p.err));
+            };
+            if (C::TWO_ISSUERS && warp == 1) {
+                bool ok = mbar_wait(bar_res, 0, p.err);
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    ok = wait_scores(j);
                     if (!ok) break;
-                    acc(j - 1);
+                    tc_fence_after();
+                    scores(j);
                 }
+                // no MMA of this thread may be in flight when TMEM is released
+                mma_commit(bar_dra);
+                mbar_wait(bar_dra, 0, p.err);
+            } else if (C::TWO_ISSUERS) {
+                // dQ(j) waits for the rows' dS(j), which they form after S(j) completed
+                bool ok = true;
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    ok = mbar_wait(bar_rready, static_cast<uint32_t>(j & 1), p.err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    acc(j);
+                }
+                mma_commit(bar_done);
+                mma_commit(bar_dr);
+                mbar_wait(bar_dr, 0, p.err);
+            } else {
+                bool ok = mbar_wait(bar_res, 0, p.err);
+                int j = 0;
+                for (; ok && j < n_kv; ++j) {
+                    ok = wait_scores(j);
+                    if (!ok) break;
+                    tc_fence_after();
+                    scores(j);
+                    if (j > 0) {
+                        ok = mbar_wait(bar_rready, static_cast<uint32_t>((j - 1) & 1), p.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        acc(j - 1);
+                    }
+                }
+                if (ok && j == n_kv && mbar_wait(bar_rready, static_cast<uint32_t>((n_kv - 1) & 1), p.err)) {
+                    tc_fence_after();
+                    acc(n_kv - 1);
+                }
+                mma_commit(bar_done);
+                // no MMA may be in flight when TMEM is released
+                mma_commit(bar_dr);
+                mbar_wait(bar_dr, 0, p.err);
             }
-            if (ok && j == n_kv && mbar_wait(bar_rready, static_cast<uint32_t>((n_kv - 1) & 1), p.err)) acc(n_kv - 1);
-            mma_commit(bar_done);
-            // no MMA may be in flight when TMEM is released
-            mma_commit(bar_dr);
-            mbar_wait(bar_dr, 0, p.err);
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ rows (query i)
-        const int wq = warp & 3, wg = (warp - 4) >> 2;   // lane quadrant, key half
+        constexpr int RC = C::RC;
+        const int wq = warp & 3, wg = (warp - 4) >> 2;   // lane quadrant, key part
         const int row = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int t = qt * C::BM + row;
@@ -298,55 +357,64 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
             ok = warp_wait(bar_s, static_cast<uint32_t>(j & 1), p.err, ok);
-            uint32_t s1[32], s2[32], dp[32];
+            uint32_t s1[RC], s2[RC], dp[RC];
             if (ok) {
                 tc_fence_after();
-                tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * wg, s1);
-                tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * wg, s2);
-                tmem_ld32(tmem + lane_off + C::COL_DP + 32 * wg, dp);
+                tmem_ld_cols<RC>(tmem + lane_off + C::COL_S1 + RC * wg, s1);
+                tmem_ld_cols<RC>(tmem + lane_off + C::COL_S2 + RC * wg, s2);
+                tmem_ld_cols<RC>(tmem + lane_off + C::COL_DP + RC * wg, dp);
                 tmem_wait_ld();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_sfree);   // the next S, dP may overwrite TMEM
             if (ok) {
-                const int key0 = j * C::BN + 32 * wg;
-                // every key of this half is at or before every query of the tile: no mask
-                const bool full = key0 + 31 <= qt * C::BM;
+                const int key0 = j * C::BN + RC * wg;
+                // every key of this part is at or before every query of the tile: no mask
+                const bool full = key0 + RC - 1 <= qt * C::BM;
+                // two unrolled copies: without the per-element mask where it is all true
+                auto form = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const bool valid = live && (full || key0 + c <= t);
-                    const float dpv = __uint_as_float(dp[c]);
-                    const float p1 = valid ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -lse1)) : 0.f;
-                    const float p2 = valid ? ex2(fmaf(__uint_as_float(s2[c]), sl2, -lse2)) : 0.f;
-                    s1[c] = __float_as_uint(p1 * (dpv - d1));
-                    s2[c] = __float_as_uint(p2 * fmaf(cc, dpv, -d2));
-                }
+                    for (int c = 0; c < RC; ++c) {
+                        const bool valid = !decltype(masked)::value || (live && key0 + c <= t);
+                        const float dpv = __uint_as_float(dp[c]);
+                        const float p1 = valid ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -lse1)) : 0.f;
+                        const float p2 = valid ? ex2(fmaf(__uint_as_float(s2[c]), sl2, -lse2)) : 0.f;
+                        s1[c] = __float_as_uint(p1 * (dpv - d1));
+                        s2[c] = __float_as_uint(p2 * fmaf(cc, dpv, -d2));
+                    }
+                };
+                if (live && full)
+                    form(std::false_type{});
+                else
+                    form(std::true_type{});
             }
             // the previous dQ MMAs must have read the result tiles
             if (j > 0) ok = warp_wait(bar_rfree, static_cast<uint32_t>((j - 1) & 1), p.err, ok);
             if (ok) {
-                uint32_t u[16];
-                pack32(s1, u);
-                store_row_half(res1, row, wg, u);
-                pack32(s2, u);
-                store_row_half(res2, row, wg, u);
+                uint32_t u[RC / 2];
+                pack_cols<RC>(s1, u);
+                store_row_part<RC>(res1, row, wg, u);
+                pack_cols<RC>(s2, u);
+                store_row_part<RC>(res2, row, wg, u);
                 fence_async_smem();   // generic-proxy writes -> tensor core reads
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_rready);
         }
-        // epilogue: dQ_b * scale -> bf16 rows (warpgroup b takes branch b)
+        // epilogue: dQ_b * scale -> bf16 rows (warpgroup wg takes branch wg % 2,
+        // channels DQK / (NRG / 2) * (wg / 2) onwards)
         ok = warp_wait(bar_done, 0, p.err, ok);
         tc_fence_after();
         if (ok) {
-            const int br = wg;
+            constexpr int NCH = DQK / (C::NRG / 2);
+            const int br = wg & 1, ch0 = NCH * (wg >> 1);
             __nv_bfloat16 *dst = (br ? p.dq2 : p.dq1) + b * p.q_sb + static_cast<int64_t>(t) * p.q_st +
-                                 static_cast<int64_t>(br ? hq2 : hq1) * p.q_sh;
+                                 static_cast<int64_t>(br ? hq2 : hq1) * p.q_sh + ch0;
 #pragma unroll
-            for (int c0 = 0; c0 < DQK; c0 += 32) {
+            for (int c0 = 0; c0 < NCH; c0 += 32) {
                 uint32_t a[32];
-                tmem_ld32(tmem + lane_off + (br ? C::COL_DQ2 : C::COL_DQ1) + c0, a);
+                tmem_ld32(tmem + lane_off + (br ? C::COL_DQ2 : C::COL_DQ1) + ch0 + c0, a);
                 tmem_wait_ld();
                 if (live) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
@@ -380,7 +448,7 @@ __global__ void __launch_bounds__(384, 1)
 // P~^T = P1^T + c P2^T, dS1^T, dS2^T; dV += P~^T G, dK_b += dS_b^T Q_b read
 // those from shared memory.
 template <int DQK, int DV, bool V2>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
     bwd_dkdv(const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq1,
              const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tg, const BwdParams p) {
@@ -417,6 +485,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t bar_rfree = bar_rready + 8;
     const uint32_t bar_done = bar_rfree + 8;
     const uint32_t bar_dr = bar_done + 8;
+    const uint32_t bar_dra = bar_dr + 8;
     const uint32_t tslot = sbase + C::KV_OFF_TSLOT;
 
     if (threadIdx.x == 0) {
@@ -426,11 +495,12 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(bar_empty + 8 * s, 1);
         }
         mbar_init(bar_s, 1);
-        mbar_init(bar_sfree, 8);
-        mbar_init(bar_rready, 8);
+        mbar_init(bar_sfree, 4 * C::NRG);   // one arrival per row warp
+        mbar_init(bar_rready, 4 * C::NRG);
         mbar_init(bar_rfree, 1);
         mbar_init(bar_done, 1);
         mbar_init(bar_dr, 1);
+        mbar_init(bar_dra, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -502,7 +572,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = (it > ST ? it - ST : 0); k < it; ++k)
                 mbar_wait(bar_full + 8 * (k % ST), static_cast<uint32_t>((k / ST) & 1), p.err);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (C::TWO_ISSUERS && warp == 2)) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
             const uint32_t sK1 = sbase + C::KV_OFF_K1, sK2 = V2 ? sK1 : sbase + C::KV_OFF_K2;
@@ -527,51 +597,85 @@ __global__ void __launch_bounds__(384, 1)
                 mma_commit(bar_empty + 8 * (jj % ST));   // Q, G of jj no longer needed
                 mma_commit(bar_rfree);                    // result tiles read
             };
-            bool ok = mbar_wait(bar_res, 0, p.err);
-            int it = 0;
-            for (; ok && it < n_items; ++it) {
-                const int st = it % ST;
+            // S_b^T = K_b Q_b^T (N = 64 queries), dP^T = V G^T for item it
+            auto scores = [&](int it) {
                 const uint32_t sQ1 = q1_at(it);
                 const uint32_t sQ2 = sQ1 + C::QB * C::CBOX, sG = sQ1 + 2 * C::QB * C::CBOX;
-                ok = mbar_wait(bar_full + 8 * st, static_cast<uint32_t>((it / ST) & 1), p.err) &&
-                     (it == 0 || mbar_wait(bar_sfree, static_cast<uint32_t>((it - 1) & 1), p.err));
-                if (!ok) break;
-                tc_fence_after();
-                // S_b^T = K_b Q_b^T (N = 64 queries), dP^T = V G^T
-                {
-                    const uint64_t a1 = sdesc_sw128(sK1, 16, 1024), a2 = sdesc_sw128(sK2, 16, 1024);
-                    const uint64_t b1 = sdesc_sw128(sQ1, 16, 1024), b2 = sdesc_sw128(sQ2, 16, 1024);
+                const uint64_t a1 = sdesc_sw128(sK1, 16, 1024), a2 = sdesc_sw128(sK2, 16, 1024);
+                const uint64_t b1 = sdesc_sw128(sQ1, 16, 1024), b2 = sdesc_sw128(sQ2, 16, 1024);
 #pragma unroll
-                    for (int ks = 0; ks < DQK / 16; ++ks) {
-                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
-                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
-                        mma_ss(tmem + C::COL_S1, a1 + oa, b1 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
-                        mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
-                    }
-                    const uint64_t av = sdesc_sw128(sV, 16, 1024), bg = sdesc_sw128(sG, 16, 1024);
+                for (int ks = 0; ks < DQK / 16; ++ks) {
+                    const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                    const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                    mma_ss(tmem + C::COL_S1, a1 + oa, b1 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                }
+                const uint64_t av = sdesc_sw128(sV, 16, 1024), bg = sdesc_sw128(sG, 16, 1024);
 #pragma unroll
-                    for (int ks = 0; ks < DV / 16; ++ks) {
-                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
-                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
-                        mma_ss(tmem + C::COL_DP, av + oa, bg + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
-                    }
+                for (int ks = 0; ks < DV / 16; ++ks) {
+                    const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                    const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                    mma_ss(tmem + C::COL_DP, av + oa, bg + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_s);
-                if (it > 0) {
-                    ok = mbar_wait(bar_rready, static_cast<uint32_t>((it - 1) & 1), p.err);
+            };
+            // S(it) needs item it in the ring and the rows done loading S(it-1)
+            auto wait_scores = [&](int it) {
+                return mbar_wait(bar_full + 8 * (it % ST), static_cast<uint32_t>((it / ST) & 1), p.err) &&
+                       (it == 0 || mbar_wait(bar_sfree, static_cast<uint32_t>((it - 1) & 1), p.err));
+            };
+            if (C::TWO_ISSUERS && warp == 1) {
+                bool ok = mbar_wait(bar_res, 0, p.err);
+                for (int it = 0; ok && it < n_items; ++it) {
+                    ok = wait_scores(it);
                     if (!ok) break;
-                    acc(it - 1);
+                    tc_fence_after();
+                    scores(it);
                 }
+                // no MMA of this thread may be in flight when TMEM is released
+                mma_commit(bar_dra);
+                mbar_wait(bar_dra, 0, p.err);
+            } else if (C::TWO_ISSUERS) {
+                // dV, dK(it) wait for the rows' P~, dS(it), formed after S(it) completed
+                bool ok = true;
+                for (int it = 0; ok && it < n_items; ++it) {
+                    ok = mbar_wait(bar_rready, static_cast<uint32_t>(it & 1), p.err);
+                    if (!ok) break;
+                    tc_fence_after();
+                    acc(it);
+                }
+                mma_commit(bar_done);
+                mma_commit(bar_dr);
+                mbar_wait(bar_dr, 0, p.err);
+            } else {
+                bool ok = mbar_wait(bar_res, 0, p.err);
+                int it = 0;
+                for (; ok && it < n_items; ++it) {
+                    ok = wait_scores(it);
+                    if (!ok) break;
+                    tc_fence_after();
+                    scores(it);
+                    if (it > 0) {
+                        ok = mbar_wait(bar_rready, static_cast<uint32_t>((it - 1) & 1), p.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        acc(it - 1);
+                    }
+                }
+                if (ok && it == n_items &&
+                    mbar_wait(bar_rready, static_cast<uint32_t>((n_items - 1) & 1), p.err)) {
+                    tc_fence_after();
+                    acc(n_items - 1);
+                }
+                mma_commit(bar_done);
+                mma_commit(bar_dr);
+                mbar_wait(bar_dr, 0, p.err);
             }
-            if (ok && it == n_items && mbar_wait(bar_rready, static_cast<uint32_t>((n_items - 1) & 1), p.err))
-                acc(n_items - 1);
-            mma_commit(bar_done);
-            mma_commit(bar_dr);
-            mbar_wait(bar_dr, 0, p.err);
         }
     } else if (warp >= 4) {
         // -------------------------------------------------- rows (key j)
-        const int wq = warp & 3, wg = (warp - 4) >> 2;   // lane quadrant, query half
+        constexpr int RC = C::RC;
+        const int wq = warp & 3, wg = (warp - 4) >> 2;   // lane quadrant, query part
         const int row = wq * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const int j = kt * C::BM + row;
@@ -584,56 +688,63 @@ __global__ void __launch_bounds__(384, 1)
             // the stage's row vectors were written by warp 0 before it arrived on
             // the stage's full barrier: acquire them there (that phase is complete)
             ok = warp_wait(bar_full + 8 * st, static_cast<uint32_t>((it / ST) & 1), p.err, ok);
-            uint32_t s1[32], s2[32], dp[32];
+            uint32_t s1[RC], s2[RC], dp[RC];
             if (ok) {
                 tc_fence_after();
-                tmem_ld32(tmem + lane_off + C::COL_S1 + 32 * wg, s1);
-                tmem_ld32(tmem + lane_off + C::COL_S2 + 32 * wg, s2);
-                tmem_ld32(tmem + lane_off + C::COL_DP + 32 * wg, dp);
+                tmem_ld_cols<RC>(tmem + lane_off + C::COL_S1 + RC * wg, s1);
+                tmem_ld_cols<RC>(tmem + lane_off + C::COL_S2 + RC * wg, s2);
+                tmem_ld_cols<RC>(tmem + lane_off + C::COL_DP + RC * wg, dp);
                 tmem_wait_ld();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_sfree);   // the next S^T, dP^T may overwrite TMEM
             if (ok) {
-                // this warpgroup's 32 query columns of the row vectors, 16 bytes at a time
+                // this warpgroup's RC query columns of the row vectors, 16 bytes at a time
                 const float4 *vec = reinterpret_cast<const float4 *>(smem + C::KV_OFF_RING + st * C::KV_STAGE +
-                                                                     C::KV_STAGE_TMA) + 8 * wg;
-                const int q0 = item_qs(it) * C::BN + 32 * wg;
-                // every query of this half is at or after every key of the tile: no mask
+                                                                     C::KV_STAGE_TMA) + RC / 4 * wg;
+                const int q0 = item_qs(it) * C::BN + RC * wg;
+                // every query of this part is at or after every key of the tile: no mask
                 const bool full = q0 >= kt * C::BM + C::BM - 1;
-                // in place: s1 <- P~ = P1 + c P2, s2 <- dS1, dp <- dS2
+                // in place: s1 <- P~ = P1 + c P2, s2 <- dS1, dp <- dS2; two unrolled
+                // copies, without the per-element mask where it is all true
+                auto form = [&](auto masked) {
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    const float4 l1 = vec[c4], l2 = vec[16 + c4], e1 = vec[32 + c4], e2 = vec[48 + c4],
-                                 cv = vec[64 + c4];
-                    const float l1a[4] = {l1.x, l1.y, l1.z, l1.w}, l2a[4] = {l2.x, l2.y, l2.z, l2.w};
-                    const float e1a[4] = {e1.x, e1.y, e1.z, e1.w}, e2a[4] = {e2.x, e2.y, e2.z, e2.w};
-                    const float cva[4] = {cv.x, cv.y, cv.z, cv.w};
+                    for (int c4 = 0; c4 < RC / 4; ++c4) {
+                        const float4 l1 = vec[c4], l2 = vec[16 + c4], e1 = vec[32 + c4], e2 = vec[48 + c4],
+                                     cv = vec[64 + c4];
+                        const float l1a[4] = {l1.x, l1.y, l1.z, l1.w}, l2a[4] = {l2.x, l2.y, l2.z, l2.w};
+                        const float e1a[4] = {e1.x, e1.y, e1.z, e1.w}, e2a[4] = {e2.x, e2.y, e2.z, e2.w};
+                        const float cva[4] = {cv.x, cv.y, cv.z, cv.w};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = 4 * c4 + k;
-                        // key j <= query q0 + c; rows past T carry lse = +inf
-                        const bool valid = full || q0 + c >= j;
-                        const float dpv = __uint_as_float(dp[c]);
-                        const float p1 = valid ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -l1a[k])) : 0.f;
-                        const float p2 = valid ? ex2(fmaf(__uint_as_float(s2[c]), sl2, -l2a[k])) : 0.f;
-                        s1[c] = __float_as_uint(fmaf(cva[k], p2, p1));
-                        s2[c] = __float_as_uint(p1 * (dpv - e1a[k]));
-                        dp[c] = __float_as_uint(p2 * fmaf(cva[k], dpv, -e2a[k]));
+                        for (int k = 0; k < 4; ++k) {
+                            const int c = 4 * c4 + k;
+                            // key j <= query q0 + c; rows past T carry lse = +inf
+                            const bool valid = !decltype(masked)::value || q0 + c >= j;
+                            const float dpv = __uint_as_float(dp[c]);
+                            const float p1 = valid ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -l1a[k])) : 0.f;
+                            const float p2 = valid ? ex2(fmaf(__uint_as_float(s2[c]), sl2, -l2a[k])) : 0.f;
+                            s1[c] = __float_as_uint(fmaf(cva[k], p2, p1));
+                            s2[c] = __float_as_uint(p1 * (dpv - e1a[k]));
+                            dp[c] = __float_as_uint(p2 * fmaf(cva[k], dpv, -e2a[k]));
+                        }
                     }
-                }
+                };
+                if (full)
+                    form(std::false_type{});
+                else
+                    form(std::true_type{});
             }
             // the previous item's dV / dK MMAs must have read the result tiles
             if (it > 0) ok = warp_wait(bar_rfree, static_cast<uint32_t>((it - 1) & 1), p.err, ok);
             if (ok) {
-                uint32_t u[16];
-                pack32(s1, u);
-                store_row_half(resP, row, wg, u);
-                pack32(s2, u);
-                store_row_half(res1, row, wg, u);
-                pack32(dp, u);
-                store_row_half(res2, row, wg, u);
+                uint32_t u[RC / 2];
+                pack_cols<RC>(s1, u);
+                store_row_part<RC>(resP, row, wg, u);
+                pack_cols<RC>(s2, u);
+                store_row_part<RC>(res1, row, wg, u);
+                pack_cols<RC>(dp, u);
+                store_row_part<RC>(res2, row, wg, u);
                 fence_async_smem();   // generic-proxy writes -> tensor core reads
             }
             __syncwarp();
@@ -662,14 +773,21 @@ __global__ void __launch_bounds__(384, 1)
                     }
                 }
             };
-            // warpgroup 0 stores dK (both branches for V1), warpgroup 1 dV
+            // the first half of the warpgroups stores dK (both branches for V1), the
+            // second half dV, each warpgroup an equal share of the channels
+            constexpr int HG = C::NRG / 2;
+            const int part = wg % HG;
             const int64_t krow = b * p.k_sb + static_cast<int64_t>(j) * p.k_st + static_cast<int64_t>(hk) * p.k_sh;
-            if (wg == 0) {
-                store(C::COL_DK1, DQK, p.dk1 + krow, p.scale);
-                if (!V2) store(C::COL_DK2, DQK, p.dk2 + krow, p.scale);
+            if (wg < HG) {
+                constexpr int NK = DQK / HG;
+                store(C::COL_DK1 + NK * part, NK, p.dk1 + krow + NK * part, p.scale);
+                if (!V2) store(C::COL_DK2 + NK * part, NK, p.dk2 + krow + NK * part, p.scale);
             } else {
-                store(C::COL_DV, DV,
-                      p.dv + b * p.v_sb + static_cast<int64_t>(j) * p.v_st + static_cast<int64_t>(hk) * p.v_sh, 1.f);
+                constexpr int NV = DV / HG;
+                store(C::COL_DV + NV * part, NV,
+                      p.dv + b * p.v_sb + static_cast<int64_t>(j) * p.v_st + static_cast<int64_t>(hk) * p.v_sh +
+                          NV * part,
+                      1.f);
             }
         }
     }
