@@ -80,7 +80,7 @@ struct PreCfg {
     static constexpr int OFF_X = OFF_OUT;
     static constexpr int OFF_BAR = OFF_OUT + OUT_TILE;
     // qfull, qfree, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s[2], p[2][2], o[2], odrain, drain, lam
-    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 5;
+    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 6;
     static constexpr int OFF_LAM = OFF_BAR + NBAR * 8;        // 2 floats
     static constexpr int OFF_TSLOT = OFF_LAM + 8;
     static constexpr int SMEM = OFF_TSLOT + 8 + 1024;         // + alignment slack
@@ -90,6 +90,11 @@ struct PreCfg {
     // lambda, idle) give up registers, the two softmax warpgroups take them
     static constexpr uint32_t REGS_LOW = 88, REGS_HIGH = 192;
     static constexpr bool REG_SPLIT = !V2;                    // measured: helps V1, costs V2
+    // one MMA-issuing thread per branch (warp 1: S1, O1; warp 2: S2, O2) instead
+    // of one for both; measured on GB300 at the V1 d = 64 / V2 D = 128 prefill
+    // shapes: 13 % / 25 % slower, so off
+    static constexpr bool TWO_ISSUERS = false;
+    static constexpr uint32_t NISS = TWO_ISSUERS ? 2 : 1;     // arrivals on stage-release barriers
     static constexpr int REGS_NEEDED_AT_LAUNCH = (128 * REGS_LOW + 256 * REGS_HIGH + 383) / 384;
     static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, true);
@@ -166,20 +171,21 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t bar_dr = bar_od + 8;
     const uint32_t bar_lam = bar_dr + 8;
     const uint32_t bar_stg = bar_lam + 8, bar_stf = bar_stg + 8;
+    const uint32_t bar_dr2 = bar_stf + 8;              // drain of the second issuer
     const uint32_t tslot = sbase + C::OFF_TSLOT;
     const uint32_t sQ1 = sbase + C::OFF_Q1, sQ2 = sbase + C::OFF_Q2;
     float *lam_smem = reinterpret_cast<float *>(smem + C::OFF_LAM);
 
     if (threadIdx.x == 0) {
         mbar_init(bar_qf, 1);
-        mbar_init(bar_qe, 1);
+        mbar_init(bar_qe, C::NISS);
         for (int s = 0; s < C::KS; ++s) {
             mbar_init(bar_kf + 8 * s, 1);
-            mbar_init(bar_ke + 8 * s, 1);
+            mbar_init(bar_ke + 8 * s, C::NISS);
         }
         for (int s = 0; s < C::VS; ++s) {
             mbar_init(bar_vf + 8 * s, 1);
-            mbar_init(bar_ve + 8 * s, 1);
+            mbar_init(bar_ve + 8 * s, C::NISS);
         }
         for (int br = 0; br < 2; ++br) {
             mbar_init(bar_s + 8 * br, 1);
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(bar_lam, 1);
         mbar_init(bar_stg, 8);
         mbar_init(bar_stf, 1);
+        mbar_init(bar_dr2, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -282,10 +289,31 @@ __global__ void __launch_bounds__(384, 1)
             for (int k = (vc > C::VS ? vc - C::VS : 0); k < vc; ++k)
                 mbar_wait(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA
+    } else if (warp == 1 || warp == 2) {
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
-        if (lane == 0) {
+        if (warp == 2) {
+            // --------------------------------------------- lambda (V1 only)
+            if (!V2) {
+                // lam_init = 0.8 - 0.6 exp(-0.3 layer); lam = exp(lq1.lk1) - exp(lq2.lk2) + lam_init
+                float d1 = 0.f, d2 = 0.f;
+                for (int c = lane; c < DQK; c += 32) {
+                    d1 = fmaf(p.lq1[c], p.lk1[c], d1);
+                    d2 = fmaf(p.lq2[c], p.lk2[c], d2);
+                }
+                d1 = warp_sum(d1);
+                d2 = warp_sum(d2);
+                if (lane == 0) {
+                    const float lam_init = 0.8f - 0.6f * expf(-0.3f * static_cast<float>(p.layer_index));
+                    lam_smem[0] = expf(d1) - expf(d2) + lam_init;
+                    lam_smem[1] = lam_init;
+                    mbar_arrive(bar_lam);
+                }
+            }
+        }
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && (warp == 1 || C::TWO_ISSUERS)) {
+            // branches issued by this thread: both, or branch warp - 1
+            const int br0 = C::TWO_ISSUERS ? warp - 1 : 0, br1 = C::TWO_ISSUERS ? warp - 1 : 1;
             // Descriptors are built once per operand; a K step only moves the
             // start address field (bits 0-13, in 16-byte units), which never
             // carries for shared-memory addresses.
@@ -309,10 +337,20 @@ __global__ void __launch_bounds__(384, 1)
             };
             int kc = 0, vc = 0, tc = 0, it = 0;
             bool ok = true;
-            auto k1_at = [&]() { return sbase + C::OFF_K + (kc % C::KS) * C::K_SLOT; };
-            auto k2_at = [&]() { return k1_at() + (V2 ? 0 : C::K_TILE); };
+            auto k_at = [&](int br) {
+                return sbase + C::OFF_K + (kc % C::KS) * C::K_SLOT + ((br && !V2) ? C::K_TILE : 0);
+            };
             auto wait_k = [&]() {
                 return mbar_wait(bar_kf + 8 * (kc % C::KS), static_cast<uint32_t>((kc / C::KS) & 1), p.err);
+            };
+            // S_b = Q_b K_b^T for this thread's branches, then the K slot's release
+            auto scores = [&]() {
+                for (int br = br0; br <= br1; ++br) {
+                    issue_qk(br ? C::COL_S2 : C::COL_S1, br ? sQ2 : sQ1, k_at(br));
+                    mma_commit(bar_s + 8 * br);
+                }
+                mma_commit(bar_ke + 8 * (kc % C::KS));
+                ++kc;
             };
             for (int k = 0; ok; ++k) {
                 const int w = snake_tile(k, cta, G, NT);
@@ -321,82 +359,56 @@ __global__ void __launch_bounds__(384, 1)
                 ok = mbar_wait(bar_qf, static_cast<uint32_t>(tc & 1), p.err) && wait_k();
                 if (!ok) break;
                 tc_fence_after();
-                issue_qk(C::COL_S1, sQ1, k1_at());
-                mma_commit(bar_s);
-                issue_qk(C::COL_S2, sQ2, k2_at());
-                mma_commit(bar_s + 8);
-                mma_commit(bar_ke + 8 * (kc % C::KS));
-                ++kc;
+                scores();
                 if (n_kv == 1) mma_commit(bar_qe);
                 for (int j = 0; ok && j < n_kv; ++j, ++it) {
                     const uint32_t pj = static_cast<uint32_t>(it & 1);
                     const int vst = vc % C::VS;
                     const uint32_t sv = sbase + C::OFF_V + vst * C::V_SLOT;
-                    ok = mbar_wait(bar_vf + 8 * vst, static_cast<uint32_t>((vc / C::VS) & 1), p.err) &&
-                         mbar_wait(bar_p, pj, p.err);
+                    const bool more = j + 1 < n_kv;
+                    ok = mbar_wait(bar_vf + 8 * vst, static_cast<uint32_t>((vc / C::VS) & 1), p.err);
                     // the first PV of a tile overwrites O: the previous epilogue must have read it
                     if (ok && j == 0 && tc > 0) ok = mbar_wait(bar_od, static_cast<uint32_t>((tc - 1) & 1), p.err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv_half(C::COL_O1, C::COL_S1, sv, 0, j > 0);
-                    ok = mbar_wait(bar_p + 8, pj, p.err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv_half(C::COL_O1, C::COL_S1, sv, 1, j > 0);
-                    const bool more = j + 1 < n_kv;
-                    if (more) {
-                        ok = wait_k();
+                    // per branch: O_b += P_b V in two key halves as the softmax publishes them,
+                    // then S_b of the next key tile (in order after the PV that reads P_b)
+                    for (int br = br0; ok && br <= br1; ++br) {
+                        const uint32_t colS = br ? C::COL_S2 : C::COL_S1, colO = br ? C::COL_O2 : C::COL_O1;
+                        ok = mbar_wait(bar_p + 16 * br, pj, p.err);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_qk(C::COL_S1, sQ1, k1_at());
-                        mma_commit(bar_s);
-                    } else {
-                        mma_commit(bar_o);
-                    }
-                    ok = mbar_wait(bar_p + 16, pj, p.err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv_half(C::COL_O2, C::COL_S2, sv, 0, j > 0);
-                    ok = mbar_wait(bar_p + 24, pj, p.err);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv_half(C::COL_O2, C::COL_S2, sv, 1, j > 0);
-                    mma_commit(bar_ve + 8 * vst);
-                    ++vc;
-                    if (more) {
-                        issue_qk(C::COL_S2, sQ2, k2_at());
-                        mma_commit(bar_s + 8);
-                        mma_commit(bar_ke + 8 * (kc % C::KS));
-                        ++kc;
-                        if (j + 2 == n_kv) mma_commit(bar_qe);   // last QK of the tile issued
-                    } else {
-                        mma_commit(bar_o + 8);
+                        issue_pv_half(colO, colS, sv, 0, j > 0);
+                        ok = mbar_wait(bar_p + 16 * br + 8, pj, p.err);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv_half(colO, colS, sv, 1, j > 0);
+                        if (br == br1) {
+                            mma_commit(bar_ve + 8 * vst);
+                            ++vc;
+                        }
+                        if (more) {
+                            if (br == br0) {
+                                ok = wait_k();
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            issue_qk(colS, br ? sQ2 : sQ1, k_at(br));
+                            mma_commit(bar_s + 8 * br);
+                            if (br == br1) {
+                                mma_commit(bar_ke + 8 * (kc % C::KS));
+                                ++kc;
+                                if (j + 2 == n_kv) mma_commit(bar_qe);   // last QK of the tile issued
+                            }
+                        } else {
+                            mma_commit(bar_o + 8 * br);
+                        }
                     }
                 }
                 ++tc;
             }
             // no MMA may be in flight when TMEM is released
-            mma_commit(bar_dr);
-            mbar_wait(bar_dr, 0, p.err);
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------- lambda (V1 only)
-        if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
-        if (!V2) {
-            // lam_init = 0.8 - 0.6 exp(-0.3 layer); lam = exp(lq1.lk1) - exp(lq2.lk2) + lam_init
-            float d1 = 0.f, d2 = 0.f;
-            for (int c = lane; c < DQK; c += 32) {
-                d1 = fmaf(p.lq1[c], p.lk1[c], d1);
-                d2 = fmaf(p.lq2[c], p.lk2[c], d2);
-            }
-            d1 = warp_sum(d1);
-            d2 = warp_sum(d2);
-            if (lane == 0) {
-                const float lam_init = 0.8f - 0.6f * expf(-0.3f * static_cast<float>(p.layer_index));
-                lam_smem[0] = expf(d1) - expf(d2) + lam_init;
-                lam_smem[1] = lam_init;
-                mbar_arrive(bar_lam);
-            }
+            const uint32_t drain = warp == 1 ? bar_dr : bar_dr2;
+            mma_commit(drain);
+            mbar_wait(drain, 0, p.err);
         }
     } else if (warp == 3) {
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
