@@ -80,38 +80,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     }
 }
 
-// Non-blocking probe of a phase (acquire semantics, like try_wait).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// mbar_wait by polling with test_wait, for the thread that issues tcgen05.mma:
-// a blocking try_wait there stalls the tensor pipe longer, even on a phase
-// that has already completed (measured on GB300 between groups of MMAs: ~160
-// cycles of pipe time per try_wait, ~66 per test_wait).  Same bounds and
-// error reporting as mbar_wait.
-__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, uint32_t *err) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if ((ld_volatile_u32(err) & kErrFatal) != 0) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-                atomicOr(err, kErrWaitTimeout);
-                return false;
-            }
-        }
-    }
-}
-
 // Named barrier over `nthreads` threads (multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
