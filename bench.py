@@ -48,7 +48,7 @@ L2_FLUSH_BYTES = 256 << 20
 # it was taken on (sha256 of the .cu file, first 16 hex digits).
 TRAFFIC_RECORDS: dict = {
     # profiles/prefill_onepass_v1_B4_T2048_H16_d64.md: dram__bytes_read.sum + dram__bytes_write.sum
-    "prefill_v1_d64": {"src_sha": "24079bf3989c007f", "bytes_per_launch": 148169984 + 13982720},
+    "prefill_v1_d64": {"src_sha": "f49a9ba4f7304aec", "bytes_per_launch": 147988736 + 13867264},
 }
 
 
@@ -624,7 +624,12 @@ def run_case(name: str, launches: int):
     torch.cuda.synchronize()
     if binding.device_error():
         raise RuntimeError("a kernel reported a device-side wait timeout")
-    print(json.dumps({"case": name, "launches": launches, "ok": True}))
+    line = {"case": name, "launches": launches, "ok": True}
+    if kind == "decode_varlen":   # the lengths are drawn on the device: report what they sum to
+        line["alg_bytes_per_launch"] = decode_varlen_bytes(s, x["cache_lens"].tolist())
+    elif kind == "v1_decode":
+        line["alg_bytes_per_launch"] = v1_decode_bytes(s)
+    print(json.dumps(line))
 
 
 # -------------------------------------------------------------------- main
