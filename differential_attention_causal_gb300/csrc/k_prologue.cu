@@ -38,8 +38,8 @@ constexpr int TS = 32;          // tokens per rotary sub-block (one cos / sin ta
 constexpr int MAXP = 64;        // lambda logits per token
 // dynamic shared memory of the lambda kernel: LSTAGES x (TB x KC channels of
 // x + KC rows of w, each P logits padded by 16 bytes)
-constexpr int KC = 128;         // channels per stage of the lambda product
-constexpr int LSTAGES = 3;
+constexpr int KC = 64;          // channels per stage of the lambda product
+constexpr int LSTAGES = 4;   // 4 x 19.5 KB at P = 16: two CTAs per SM
 __host__ __device__ constexpr int lstage(int P) { return TB * KC * 2 + KC * (P * 2 + 16); }
 constexpr int SMEM_MAX = LSTAGES * lstage(MAXP);
 
@@ -204,7 +204,7 @@ __device__ __forceinline__ void lambda_bf16(const PrologueParams &p, int64_t tok
     const int lst = lstage(p.P);
     auto xs = [&](int b) { return sbase + b * lst; };
     auto ws = [&](int b) { return sbase + b * lst + TB * KC * 2; };
-    // x tile: rows of KC * 2 = 256 bytes, 16-byte chunk ch at
+    // x tile: rows of KC * 2 = 128 bytes, 16-byte chunk ch at
     // ((ch & 8) | ((ch & 7) ^ (row & 7))): ldmatrix's 8 rows hit 8 bank groups
     auto xoff = [](int row, int ch) { return row * (KC * 2) + (((ch & 8) | ((ch & 7) ^ (row & 7))) << 4); };
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(p.x);
@@ -377,7 +377,7 @@ cudaError_t launch_e(const PrologueParams &p, cudaStream_t s) {
 
 bool prologue_supported(int D, int C, int P) {
     const bool dim_ok = D == 32 || D == 64 || D == 128;
-    // the bf16 product takes the channels KC = 128 at a time
+    // the bf16 product takes the channels KC = 64 at a time
     const bool proj_ok = C == 0 || (C % KC == 0 && P >= 8 && P <= MAXP && P % 8 == 0);
     return dim_ok && proj_ok;
 }

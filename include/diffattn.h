@@ -330,7 +330,7 @@ da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const flo
  *   - if x != NULL, DIFF V2's projected lambda ("Differential Transformer
  *     V2": a projected lambda for each token and head): lam (B, T, P) fp32
  *     = x (B, T, C) @ w_lam (C, P), x and w_lam in dtype, fp32 sums.
- * Supported: D in {32, 64, 128}; C a multiple of 128; P a multiple of 8 in
+ * Supported: D in {32, 64, 128}; C a multiple of 64; P a multiple of 8 in
  * 8..64.  Pointers 16-byte aligned. */
 da_status diffattn_prologue(void *q, void *k, int B, int T, int Hq, int Hk, int D, int64_t pos0,
                             float base, const void *x, const void *w_lam, float *lam, int C, int P,

@@ -59,7 +59,7 @@ def test_rope_and_lambda_in_one_call(dtype):
     assert binding().device_error() == 0
 
 
-@pytest.mark.parametrize("C,P", [(128, 8), (2048, 64), (896, 24)])
+@pytest.mark.parametrize("C,P", [(128, 8), (2048, 64), (896, 24), (192, 16), (64, 8)])
 def test_lambda_only(C, P):
     lp = inputs.make_lambda_proj(3, 41, C, P, "bf16", seed=C)
     lam = binding().prologue(x=lp["x"].cuda(), w_lam=lp["w_lam"].cuda())
@@ -76,7 +76,7 @@ def test_prologue_argument_checks():
     assert f(x=A) == 1                         # x without w / lam
     assert f(D=96) == 3
     assert f(x=A, w=A, lam=A, C=64, P=12) == 3   # P not a multiple of 8
-    assert f(x=A, w=A, lam=A, C=96, P=16) == 3   # C not a multiple of 128
+    assert f(x=A, w=A, lam=A, C=96, P=16) == 3   # C not a multiple of 64
     assert f(q=A + 8) == 5
     assert f(base=0.0) == 2
     assert f(dtype=4) == 8
