@@ -11,7 +11,7 @@
 //
 // Two kernels of 256 threads (q, k and x are disjoint, so one pass over each
 // is all the fusion there is; the two need different shapes):
-//   rotary, one CTA per 32 tokens:
+//   rotary, persistent (three CTAs per SM), blocks of TS = 16 tokens:
 //   1. cos / sin of the block's positions: the angle is formed and reduced
 //      modulo 2 pi with an extra float of precision (positions reach 10^5,
 //      where a plain float product would already be off by ~1e-3 rad), the
@@ -34,7 +34,7 @@ namespace {
 
 constexpr int TB = 128;         // tokens per lambda CTA (16 per warp, 8 warps)
 constexpr int LT = 256;         // threads of a lambda CTA
-constexpr int TS = 32;          // tokens per rotary sub-block (one cos / sin table)
+constexpr int TS = 16;          // tokens per rotary sub-block (one cos / sin table)
 constexpr int MAXP = 64;        // lambda logits per token
 // dynamic shared memory of the lambda kernel: LSTAGES x (TB x KC channels of
 // x + KC rows of w, each P logits padded by 16 bytes)
