@@ -153,8 +153,10 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
         return DA_ERR_NULL_PTR;
     if (B < 1 || T < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
     const int es = dtype == DA_BF16 ? 2 : 4;
-    // bf16: d = 64 runs the one-pass kernel, d = 128 (dv = 256: two fp32
-    // accumulators would not fit in TMEM next to S) the two-pass kernel
+    // bf16: d = 64 runs the one-pass kernel, d = 32 the same kernel with q and
+    // k read through 64-column boxes whose upper half the copy fills with
+    // zeros (Q K^T unchanged), d = 128 (dv = 256: two fp32 accumulators would
+    // not fit in TMEM next to S) the two-pass kernel
     const bool twopass = dtype == DA_BF16 && d == 128;
     if (dtype == DA_BF16 ? !(twopass || prefill_supported(d, 2 * d, false)) : (d != 32 && d != 64 && d != 128))
         return DA_ERR_UNSUPPORTED_DIM;
@@ -198,6 +200,7 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
     p.out = out; p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
     p.lam = nullptr;
     p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+    p.dlam = d;
     p.layer_index = layer_index;
     p.B = B; p.T = T; p.H = H; p.G = 1;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
@@ -597,6 +600,7 @@ da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, 
     PrefillParams p{};
     p.out = out; p.o_sb = o_sb; p.o_st = o_st; p.o_sh = o_sh;
     p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
+    p.dlam = d;
     p.layer_index = layer_index;
     p.B = B; p.T = T; p.H = H; p.G = 1;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));

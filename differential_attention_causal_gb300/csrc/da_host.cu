@@ -83,7 +83,7 @@ da_status diffattn_v1_fwd_host(const void *q, const void *k, const void *v, cons
     if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
     if (!q || !k || !v || !lam_q1 || !lam_k1 || !lam_q2 || !lam_k2 || !out || !workspace) return DA_ERR_NULL_PTR;
     if (B < 1 || T < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
-    if (dtype == DA_BF16 ? (d != 64 && d != 128) : (d != 32 && d != 64 && d != 128)) return DA_ERR_UNSUPPORTED_DIM;
+    if (d != 32 && d != 64 && d != 128) return DA_ERR_UNSUPPORTED_DIM;
     const int es = dtype == DA_BF16 ? 2 : 4;
     const HostLayout L(B, T, H, d, es);
     if (workspace_bytes < L.total) return DA_ERR_WORKSPACE_TOO_SMALL;

@@ -51,6 +51,7 @@ struct PrefillParams {
     int64_t o_sb, o_st, o_sh;      // elements
     const float *lam;              // V2 logits (B, T, H) contiguous
     const float *lq1, *lk1, *lq2, *lk2;
+    int dlam;                      // V1: length d of the lambda vectors
     int layer_index;
     int B, T, H, G;
     float scale_log2;              // log2(e) / sqrt(dqk)
@@ -67,7 +68,7 @@ struct PrefillMaps {
     CUtensorMap q1, q2, k1, k2, v;
     CUtensorMap out;   // one-pass kernel: output tile stores (box 64 x 1 x 128 x 1)
 };
-// dqk/dv in {64/128 (V1), 128/256 (V1 two-pass), 64/64, 128/128 (V2)}
+// dqk/dv in {32/64, 64/128 (V1), 128/256 (V1 two-pass), 64/64, 128/128 (V2)}
 cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
                            cudaStream_t s);
 // The same kernel with the training epilogue (p.sa1, p.sa2, p.slse written).

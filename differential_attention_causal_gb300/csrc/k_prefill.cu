@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!V2) {
                 // lam_init = 0.8 - 0.6 exp(-0.3 layer); lam = exp(lq1.lk1) - exp(lq2.lk2) + lam_init
                 float d1 = 0.f, d2 = 0.f;
-                for (int c = lane; c < DQK; c += 32) {
+                for (int c = lane; c < p.dlam; c += 32) {
                     d1 = fmaf(p.lq1[c], p.lk1[c], d1);
                     d2 = fmaf(p.lq2[c], p.lk2[c], d2);
                 }
@@ -690,7 +690,7 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
 
 bool prefill_supported(int dqk, int dv, bool v2) {
     if (v2) return (dqk == 128 && dv == 128) || (dqk == 64 && dv == 64);
-    return dqk == 64 && dv == 128;
+    return (dqk == 64 && dv == 128) || (dqk == 32 && dv == 64);
 }
 
 cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk, int dv, bool v2,
@@ -698,6 +698,9 @@ cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk
     if (v2 && dqk == 128 && dv == 128) return launch_t<128, 128, true, false>(m, p, s);
     if (v2 && dqk == 64 && dv == 64) return launch_t<64, 64, true, false>(m, p, s);
     if (!v2 && dqk == 64 && dv == 128) return launch_t<64, 128, false, false>(m, p, s);
+    // d = 32: the q / k maps are 32 columns wide and their 64-column boxes are
+    // zero-filled past column 32, so the d = 64 kernel computes the same S
+    if (!v2 && dqk == 32 && dv == 64) return launch_t<64, 64, false, false>(m, p, s);
     return cudaErrorInvalidValue;
 }
 

@@ -102,7 +102,8 @@ typedef enum { DA_F32 = 0, DA_BF16 = 1 } da_dtype;
  *   lam_q1 .. lam_k2 : fp32 device vectors of length d.
  *   out            : (B, T, H, 2d), strides (o_sb, o_st, o_sh), dtype as inputs.
  *   layer_index    : >= 0, used as given (0-based) in lam_init.
- *   Supported: DA_BF16 with d in {64, 128};  DA_F32 with d in {32, 64, 128}.
+ *   Supported: d in {32, 64, 128} for both dtypes (DA_BF16 at d = 32 runs the
+ *   d = 64 tensor-core kernel on q / k boxes zero-filled past column 32).
  */
 da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const void *k2,
                           const void *v,

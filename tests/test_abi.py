@@ -73,7 +73,8 @@ def test_v1_argument_checks(lib):
     assert _v1(lib, lk2=None) == 1
     assert _v1(lib, T=0) == 2                           # bad shape
     assert _v1(lib, layer=-1) == 2
-    assert _v1(lib, d=32) == 3                          # bf16 d=32 unsupported
+    assert _v1(lib, d=48) == 3                          # bf16 d=48 unsupported
+    assert _v1(lib, d=32, v=A + 8) == 5                 # bf16 d=32 passes the dimension check
     assert _v1(lib, d=96) == 3
     assert _v1(lib, d=96, dtype=0) == 3                 # fp32 d=96 unsupported
     assert _v1(lib, v=A + 8) == 5                       # misaligned pointer
@@ -131,7 +132,7 @@ def test_v1_host_argument_checks(lib):
     assert _host(lib, ws=None) == 1
     assert _host(lib, T=0) == 2
     assert _host(lib, layer=-1) == 2
-    assert _host(lib, d=32) == 3                       # bf16 d = 32 unsupported
+    assert _host(lib, d=48) == 3                       # bf16 d = 48 unsupported
     assert _host(lib, wsb=need - 1) == 6               # workspace too small
     assert _host(lib, ws=A + 16) == 5                  # workspace not 256-byte aligned
     assert _host(lib, dtype=3) == 8

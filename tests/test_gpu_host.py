@@ -41,7 +41,8 @@ def host_call(x, s, stream=None):
 
 
 @pytest.mark.parametrize("B,T,H,d,layer,dtype", [(3, 200, 2, 64, 1, "bf16"), (9, 129, 2, 64, 0, "bf16"),
-                                                 (2, 300, 3, 128, 5, "bf16"), (2, 70, 2, 32, 2, "fp32")])
+                                                 (2, 300, 3, 128, 5, "bf16"), (2, 70, 2, 32, 2, "fp32"),
+                                                 (3, 65, 2, 32, 3, "bf16")])
 def test_v1_host_matches_device_call_and_oracle(B, T, H, d, layer, dtype):
     s = inputs.V1Shape(B, T, H, d, layer, dtype)
     x = inputs.make_v1(s, seed=B + T)

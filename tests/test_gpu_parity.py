@@ -88,6 +88,16 @@ def test_v1_bf16_d64(B, T, H, layer):
     assert_parity(y, oracle_v1(x, layer), "bf16")
 
 
+@pytest.mark.parametrize("B,T,H,layer", [(2, 77, 3, 5), (1, 1, 1, 0), (1, 129, 2, 12), (2, 300, 2, 27)])
+def test_v1_bf16_d32(B, T, H, layer):
+    # d = 32 (dv = 64) runs the d = 64 kernel on q / k boxes zero-filled past column 32
+    s = inputs.V1Shape(B, T, H, 32, layer, "bf16")
+    x = inputs.make_v1(s, seed=B * 1000 + T + 32)
+    y = run_v1(to_dev(x), layer)
+    assert_parity(y, oracle_v1(x, layer), "bf16")
+    assert binding().device_error() == 0
+
+
 def test_v1_bf16_lambda_zero_and_separate_tensors():
     """lam = 0 (lq1 = lk1 = 0, lq2.lk2 = ln(1 + lam_init)); q1/q2/k1/k2 as separate tensors
     and a strided output view."""
