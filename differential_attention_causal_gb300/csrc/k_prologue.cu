@@ -19,7 +19,7 @@
 //   2. every (token, head, 8-pair chunk) of q and k: two 16-byte loads, the
 //      rotation in fp32, two stores;
 //   lambda, one CTA of 256 threads per 128 tokens:
-//   3. the logits of the CTA's 64 tokens: bf16 on the tensor cores
+//   3. the logits of the CTA's 128 tokens: bf16 on the tensor cores
 //      (mma.sync, fp32 accumulators, x and w staged in shared memory 64
 //      channels at a time), fp32 on CUDA cores (one warp per token).
 // The work is HBM-bound (q and k read and written once, x read once); w
@@ -39,7 +39,7 @@ constexpr int MAXP = 64;        // lambda logits per token
 // dynamic shared memory of the lambda kernel: LSTAGES x (TB x KC channels of
 // x + KC rows of w, each P logits padded by 16 bytes)
 constexpr int KC = 64;          // channels per stage of the lambda product
-constexpr int LSTAGES = 4;   // 4 x 19.5 KB at P = 16: two CTAs per SM
+constexpr int LSTAGES = 4;      // 4 x 19.5 KB at P = 16: two CTAs per SM
 __host__ __device__ constexpr int lstage(int P) { return TB * KC * 2 + KC * (P * 2 + 16); }
 constexpr int SMEM_MAX = LSTAGES * lstage(MAXP);
 
