@@ -778,6 +778,7 @@ da_status diffattn_v1_bwd(const void *q1, const void *q2, const void *k1, const 
     p.dd = pp.dd;
     p.cv = pp.cv;
     p.B = B; p.T = T; p.H = H; p.G = 1; p.Hkv = H;
+    p.dqk_store = d;
     p.scale = 1.f / sqrtf(static_cast<float>(d));
     p.scale_log2 = 1.4426950408889634f * p.scale;
     p.err = err;
@@ -873,6 +874,7 @@ da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const flo
     p.dd = pp.dd;
     p.cv = pp.cv;
     p.B = B; p.T = T; p.H = P; p.G = G; p.Hkv = Hkv;
+    p.dqk_store = D;
     p.scale = 1.f / sqrtf(static_cast<float>(D));
     p.scale_log2 = 1.4426950408889634f * p.scale;
     p.err = err;

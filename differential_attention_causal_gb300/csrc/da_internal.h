@@ -104,6 +104,8 @@ struct BwdParams {
     const float *dd;                             // D_b = g_b . a_b
     const float *cv;                             // c (B, H, T): V1 -lam, V2 -sigmoid(lam[t])
     int B, T, H, G, Hkv;
+    int dqk_store;                               // channels of dq / dk stored (the real d; the
+                                                 // kernels may run on zero-padded q / k boxes)
     float scale_log2, scale;                     // log2(e) / sqrt(dqk), 1 / sqrt(dqk)
     uint32_t *err;
 };

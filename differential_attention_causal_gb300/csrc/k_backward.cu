@@ -413,6 +413,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                                  static_cast<int64_t>(br ? hq2 : hq1) * p.q_sh + ch0;
 #pragma unroll
             for (int c0 = 0; c0 < NCH; c0 += 32) {
+                if (ch0 + c0 >= p.dqk_store) break;   // zero-padded channels
                 uint32_t a[32];
                 tmem_ld32(tmem + lane_off + (br ? C::COL_DQ2 : C::COL_DQ1) + ch0 + c0, a);
                 tmem_wait_ld();
@@ -780,8 +781,10 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
             const int64_t krow = b * p.k_sb + static_cast<int64_t>(j) * p.k_st + static_cast<int64_t>(hk) * p.k_sh;
             if (wg < HG) {
                 constexpr int NK = DQK / HG;
-                store(C::COL_DK1 + NK * part, NK, p.dk1 + krow + NK * part, p.scale);
-                if (!V2) store(C::COL_DK2 + NK * part, NK, p.dk2 + krow + NK * part, p.scale);
+                // only the stored channels (the rest are zero padding)
+                const int nk = min(NK, p.dqk_store - NK * part);
+                store(C::COL_DK1 + NK * part, nk, p.dk1 + krow + NK * part, p.scale);
+                if (!V2) store(C::COL_DK2 + NK * part, nk, p.dk2 + krow + NK * part, p.scale);
             } else {
                 constexpr int NV = DV / HG;
                 store(C::COL_DV + NV * part, NV,
@@ -1013,7 +1016,7 @@ cudaError_t launch_bwd_lambda(const BwdPreParams &pp, cudaStream_t s) {
 
 bool backward_supported(int dqk, int dv, bool v2) {
     if (v2) return (dqk == 128 && dv == 128) || (dqk == 64 && dv == 64);
-    return dqk == 64 && dv == 128;
+    return (dqk == 64 && dv == 128) || (dqk == 32 && dv == 64);
 }
 
 cudaError_t launch_backward(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, int dqk, int dv, bool v2,
@@ -1021,6 +1024,10 @@ cudaError_t launch_backward(const BwdMaps &m, const BwdParams &p, const BwdPrePa
     if (v2 && dqk == 128 && dv == 128) return launch_bwd_t<128, 128, true>(m, p, pp, s);
     if (v2 && dqk == 64 && dv == 64) return launch_bwd_t<64, 64, true>(m, p, pp, s);
     if (!v2 && dqk == 64 && dv == 128) return launch_bwd_t<64, 128, false>(m, p, pp, s);
+    // d = 32: the q / k maps are 32 columns wide and their 64-column boxes are
+    // zero-filled, so the d = 64 kernels compute the same S; the padded halves
+    // of dq and dk come out zero and are not stored (p.dqk_store)
+    if (!v2 && dqk == 32 && dv == 64) return launch_bwd_t<64, 64, false>(m, p, pp, s);
     return cudaErrorInvalidValue;
 }
 

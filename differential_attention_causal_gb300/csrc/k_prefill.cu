@@ -719,6 +719,7 @@ cudaError_t launch_prefill_train(const PrefillMaps &m, const PrefillParams &p, i
     if (v2 && dqk == 128 && dv == 128) return launch_t<128, 128, true, true>(m, p, s);
     if (v2 && dqk == 64 && dv == 64) return launch_t<64, 64, true, true>(m, p, s);
     if (!v2 && dqk == 64 && dv == 128) return launch_t<64, 128, false, true>(m, p, s);
+    if (!v2 && dqk == 32 && dv == 64) return launch_t<64, 64, false, true>(m, p, s);   // zero-filled q / k boxes
     return cudaErrorInvalidValue;
 }
 

@@ -54,9 +54,9 @@ def check_lambda_vectors(g, ref, x, report):
         assert (err <= bound).all(), f"{n}: err / bound = {(err / bound).max():.3f}"
 
 
-def v1_case(B, T, H, seed, layer=12):
-    x = inputs.make_v1(inputs.V1Shape(B, T, H, 64, layer, "bf16"), seed=seed)
-    dout = inputs.make_grad_out((B, T, H, 128), "bf16", seed=seed)
+def v1_case(B, T, H, seed, layer=12, d=64):
+    x = inputs.make_v1(inputs.V1Shape(B, T, H, d, layer, "bf16"), seed=seed)
+    dout = inputs.make_grad_out((B, T, H, 2 * d), "bf16", seed=seed)
     return x, dout
 
 
@@ -71,7 +71,17 @@ def run_v1(xd, dout_d, layer):
 
 @pytest.mark.parametrize("B,T,H", [(1, 128, 1), (2, 200, 3), (1, 384, 2), (2, 64, 2), (1, 1, 1), (1, 700, 1)])
 def test_v1_backward(B, T, H):
-    x, dout = v1_case(B, T, H, seed=T + B)
+    check_v1_backward(B, T, H, 64)
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 128, 1), (2, 200, 3), (1, 1, 1), (1, 300, 2)])
+def test_v1_backward_d32(B, T, H):
+    # d = 32 runs the d = 64 kernels on zero-filled q / k boxes; dq, dk keep 32 channels
+    check_v1_backward(B, T, H, 32)
+
+
+def check_v1_backward(B, T, H, d):
+    x, dout = v1_case(B, T, H, seed=T + B + d, d=d)
     xd, dd = to_dev(x), dout.cuda()
     out, g = run_v1(xd, dd, 12)
     assert binding().device_error() == 0
@@ -90,7 +100,7 @@ def test_v1_backward(B, T, H):
             continue
         check_grad(n, g[n], ref[n], rep)
     check_lambda_vectors(g, ref, x, rep)
-    print(f"V1 B{B} T{T} H{H}", {k: f"{a:.2e}/{b:.2e}" for k, (a, b) in rep.items()})
+    print(f"V1 B{B} T{T} H{H} d{d}", {k: f"{a:.2e}/{b:.2e}" for k, (a, b) in rep.items()})
 
 
 @pytest.mark.parametrize("B,T,Hq,Hkv,D", [(1, 128, 4, 2, 128), (2, 200, 8, 2, 128), (1, 300, 4, 1, 64),
@@ -118,6 +128,7 @@ def test_backward_argument_checks():
     bd = binding()
     assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128, 1) == 0   # bf16 d = 128: no backward kernel
     assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128, 0) > 0    # fp32 d = 128: CUDA-core backward
+    assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 32, 1) > 0     # bf16 d = 32: the d = 64 kernels
     assert bd.lib().diffattn_v2_bwd_workspace_size(1, 128, 6, 2, 128, 1) > 0
     x = to_dev(inputs.make_v2(inputs.V2Shape(1, 64, 4, 2, 128, "bf16"), seed=1))
     out, saved = bd.v2_fwd_train(x["q"], x["k"], x["v"], x["lam"])
