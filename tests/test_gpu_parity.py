@@ -205,6 +205,43 @@ def test_v2_bf16_full_workload_sampled():
     assert_parity(y.reshape(-1, s.D)[torch.from_numpy(rows).cuda()], ref, "bf16")
 
 
+@pytest.mark.slow
+def test_v2_bf16_beyond_2_31_elements():
+    """B=2048, T=136 (a ragged last query tile), 64 query heads, 8 kv heads, D=128:
+    q holds 2^31 + 2^27 elements (4.6 GB), past what a 32-bit element offset
+    reaches; sampled rows of the first and last batch entries against the oracle
+    (inputs drawn on the device)."""
+    s = inputs.V2Shape(2048, 136, 64, 8, 128, "bf16")
+    assert s.B * s.T * s.Hq * s.D > 2 ** 31
+    xd = inputs.make_v2(s, seed=3, device="cuda")
+    y = binding().v2_fwd(xd["q"], xd["k"], xd["v"], xd["lam"])
+    assert binding().device_error() == 0
+    P = s.Hq // 2
+    rows = np.array([t * P + i for t in (0, 1, 127, 128, 135) for i in range(P)], dtype=np.int64)
+    for b in (0, 1, s.B - 2, s.B - 1):
+        xb = {n: xd[n][b:b + 1].contiguous().cpu() for n in ("q", "k", "v", "lam")}
+        ref = oracle.v2_fwd(xb["q"], xb["k"], xb["v"], xb["lam"], rows=rows)
+        assert_parity(y[b].reshape(-1, s.D)[torch.from_numpy(rows).cuda()], ref, "bf16")
+
+
+@pytest.mark.slow
+def test_v1_bf16_beyond_2_31_elements():
+    """B=2048, T=136, 64 diff heads, d=64: q, k (B, T, 2H, d) and v, out (B, T, H, 2d)
+    each hold 2^31 + 2^27 elements (4.6 GB); sampled rows of the first and last
+    batch entries against the oracle (inputs drawn on the device)."""
+    s = inputs.V1Shape(2048, 136, 64, 64, 5, "bf16")
+    assert s.B * s.T * 2 * s.H * s.d > 2 ** 31
+    xd = inputs.make_v1(s, seed=4, device="cuda")
+    y = run_v1(xd, s.layer_index)
+    assert binding().device_error() == 0
+    rows = np.array([t * s.H + h for t in (0, 1, 127, 128, 135) for h in range(s.H)], dtype=np.int64)
+    for b in (0, 1, s.B - 2, s.B - 1):
+        xb = {n: (xd[n][b:b + 1].contiguous().cpu() if n in ("q1", "q2", "k1", "k2", "v") else xd[n].cpu())
+              for n in ("q1", "q2", "k1", "k2", "v", "lam_q1", "lam_k1", "lam_q2", "lam_k2")}
+        ref = oracle_v1(xb, s.layer_index, rows=rows)
+        assert_parity(y[b].reshape(-1, 2 * s.d)[torch.from_numpy(rows).cuda()], ref, "bf16")
+
+
 # ------------------------------------------------------------ DIFF V2 decode
 
 @pytest.mark.parametrize("B,L,Hq,Hkv,D", [(3, 1000, 16, 2, 128), (1, 1, 8, 1, 128), (2, 63, 8, 2, 128),
