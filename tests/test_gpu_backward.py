@@ -139,6 +139,32 @@ def test_backward_argument_checks():
 
 
 @pytest.mark.slow
+def test_v1_backward_beyond_2_31_elements():
+    """B=2048, T=136 (ragged last tile), 64 heads, d=64: q, k, v, dout and every
+    gradient hold 2^31 + 2^27 elements, the saved fp32 tensors 9 GB each; two heads
+    of the first and of the last batch entry against the oracle (inputs drawn on
+    the device, one batch entry at a time copied back for the oracle)."""
+    s = inputs.V1Shape(2048, 136, 64, 64, 5, "bf16")
+    assert s.B * s.T * 2 * s.H * s.d > 2 ** 31
+    xd = inputs.make_v1(s, seed=6, device="cuda")
+    dd = inputs.make_grad_out((s.B, s.T, s.H, 2 * s.d), "bf16", seed=6, device="cuda")
+    _, g = run_v1(xd, dd, s.layer_index)
+    assert binding().device_error() == 0
+    heads = [0, s.H - 1]
+    for b in (0, s.B - 1):
+        xb = {n: xd[n][b:b + 1].contiguous().cpu() for n in ("q1", "q2", "k1", "k2", "v")}
+        ref = oracle.v1_bwd(xb["q1"], xb["q2"], xb["k1"], xb["k2"], xb["v"], xd["lam_q1"].cpu(),
+                            xd["lam_k1"].cpu(), xd["lam_q2"].cpu(), xd["lam_k2"].cpu(), s.layer_index,
+                            dd[b:b + 1].cpu(), heads=heads)
+        for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
+            got = g[n][b:b + 1].float().cpu().permute(0, 2, 1, 3).reshape(s.H, s.T, -1)[heads]
+            want = ref[n].transpose(0, 2, 1, 3).reshape(s.H, s.T, -1)[heads]
+            check_grad(n, got, want)
+    del g, xd, dd
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
 def test_v1_backward_full_workload_sampled_heads():
     """B=4, T=2048, 16 heads, d=64 (the bench's V1 workload and launch): gradients of
     three sampled (b, h) heads against the oracle (heads are independent in V1;
