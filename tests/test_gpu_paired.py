@@ -71,3 +71,20 @@ def test_paired_bf16_full_workload_sampled():
     rows = np.array(rows, dtype=np.int64)
     ref = oracle.paired_fwd(x["q"], x["k"], x["v"], rows=rows)
     assert_parity(y.reshape(-1, s.D)[torch.from_numpy(rows).cuda()], ref, "bf16")
+
+
+@pytest.mark.slow
+def test_paired_bf16_beyond_2_31_elements():
+    """B=4096, T=136, H=32 (16 pairs), D=128: q, k, v and out hold 2^31 + 2^27
+    elements each (4.6 GB); sampled rows of the first and last batch entries
+    against the oracle (inputs drawn on the device)."""
+    s = inputs.PairedShape(4096, 136, 32, 128, "bf16")
+    assert s.B * s.T * s.H * s.D > 2 ** 31
+    xd = inputs.make_paired(s, seed=7, device="cuda")
+    y = binding().paired_fwd(xd["q"], xd["k"], xd["v"])
+    assert binding().device_error() == 0
+    rows = np.array([t * s.H + h for t in (0, 1, 63, 64, 127, 128, 135) for h in range(s.H)], dtype=np.int64)
+    for b in (0, s.B - 1):
+        xb = {n: xd[n][b:b + 1].contiguous().cpu() for n in ("q", "k", "v")}
+        ref = oracle.paired_fwd(xb["q"], xb["k"], xb["v"], rows=rows)
+        assert_parity(y[b].reshape(-1, s.D)[torch.from_numpy(rows).cuda()], ref, "bf16")

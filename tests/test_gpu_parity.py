@@ -242,6 +242,24 @@ def test_v1_bf16_beyond_2_31_elements():
         assert_parity(y[b].reshape(-1, 2 * s.d)[torch.from_numpy(rows).cuda()], ref, "bf16")
 
 
+@pytest.mark.slow
+def test_v1_bf16_d128_beyond_2_31_elements():
+    """The two-pass kernel (d=128, dv=256) with B=2048, T=136, 32 heads: q, k
+    (B, T, 2H, d) and v, out (B, T, H, 2d) hold 2^31 + 2^27 elements each;
+    sampled rows of the first and last batch entries against the oracle."""
+    s = inputs.V1Shape(2048, 136, 32, 128, 27, "bf16")
+    assert s.B * s.T * 2 * s.H * s.d > 2 ** 31
+    xd = inputs.make_v1(s, seed=8, device="cuda")
+    y = run_v1(xd, s.layer_index)
+    assert binding().device_error() == 0
+    rows = np.array([t * s.H + h for t in (0, 1, 127, 128, 135) for h in range(s.H)], dtype=np.int64)
+    for b in (0, s.B - 1):
+        xb = {n: (xd[n][b:b + 1].contiguous().cpu() if n in ("q1", "q2", "k1", "k2", "v") else xd[n].cpu())
+              for n in ("q1", "q2", "k1", "k2", "v", "lam_q1", "lam_k1", "lam_q2", "lam_k2")}
+        ref = oracle_v1(xb, s.layer_index, rows=rows)
+        assert_parity(y[b].reshape(-1, 2 * s.d)[torch.from_numpy(rows).cuda()], ref, "bf16")
+
+
 # ------------------------------------------------------------ DIFF V2 decode
 
 @pytest.mark.parametrize("B,L,Hq,Hkv,D", [(3, 1000, 16, 2, 128), (1, 1, 8, 1, 128), (2, 63, 8, 2, 128),
