@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_status_string.argtypes = [i32]
             L.diffattn_device_error.restype = i32
             L.diffattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.diffattn_selftest_wait_limit.restype = i32
+            L.diffattn_selftest_wait_limit.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
             L.diffattn_last_launch_count.restype = i32
             L.diffattn_last_launch_count.argtypes = []
             _lib = L
@@ -104,6 +106,18 @@ def status_string(code: int) -> str:
 def last_launch_count() -> int:
     """Kernel launches enqueued by the last successful call on this thread."""
     return lib().diffattn_last_launch_count()
+
+
+def selftest_wait_limit(stream=None) -> int:
+    """Failure-path self-test (about 2 s): a kernel whose bounded wait nothing
+    completes must give up, record the timeout bit and leave the context usable.
+    Returns the raw error word it recorded (cleared again); raises if the wait
+    did not give up."""
+    code = ctypes.c_uint32(0)
+    rc = lib().diffattn_selftest_wait_limit(ctypes.byref(code), _stream(stream))
+    if rc != 0:
+        raise DiffAttnError("diffattn_selftest_wait_limit", rc)
+    return int(code.value)
 
 
 def device_error() -> int:

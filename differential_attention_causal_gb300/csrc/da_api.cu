@@ -142,6 +142,20 @@ da_status diffattn_device_error(uint32_t *code) {
     return v ? DA_ERR_DEVICE_TIMEOUT : DA_OK;
 }
 
+da_status diffattn_selftest_wait_limit(uint32_t *code, cudaStream_t stream) {
+    uint32_t *err = nullptr;
+    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    uint32_t before = 0;
+    if (diffattn_device_error(&before) == DA_ERR_CUDA) return DA_ERR_CUDA;   // start from a clear word
+    bool gave_up = false;
+    if (run_wait_selftest(err, &gave_up, stream) != cudaSuccess) return DA_ERR_CUDA;
+    uint32_t v = 0;
+    if (diffattn_device_error(&v) == DA_ERR_CUDA) return DA_ERR_CUDA;   // reads and clears the word
+    if (code) *code = v;
+    t_last_launches = 1;
+    return (gave_up && (v & kErrWaitTimeout) != 0) ? DA_OK : DA_ERR_CUDA;
+}
+
 da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const void *k2, const void *v,
                           const float *lam_q1, const float *lam_k1, const float *lam_q2, const float *lam_k2,
                           void *out, int B, int T, int H, int d, int layer_index,

@@ -128,6 +128,9 @@ struct BwdMaps {
     CUtensorMap k1r, k2r, vr, q1c, q2c, gc;      // dK dV kernel: 128-row K / V boxes, 64-row Q / G boxes
 };
 bool backward_supported(int dqk, int dv, bool v2);
+// One warp waits on an mbarrier phase nothing completes (the bounded-wait
+// failure path); *gave_up is true once the wait gave up as designed.
+cudaError_t run_wait_selftest(uint32_t *err, bool *gave_up, cudaStream_t s);
 // dL/dlam summed from the per-row shares in pp.dlam_rows, then the four
 // lambda-vector gradients (one CTA; used by the bf16 and the fp32 backward).
 cudaError_t launch_bwd_lambda(const BwdPreParams &pp, cudaStream_t s);

@@ -348,6 +348,16 @@ const char *diffattn_status_string(da_status s);
  * cache length outside 1..L, DA_ERR_CUDA if the read itself failed. */
 da_status diffattn_device_error(uint32_t *code);
 
+/* Failure-path self-test: one warp waits on an mbarrier phase that nothing
+ * completes.  Its bounded wait gives up after the library's limit (2 s of
+ * global time), records the timeout bit in the device error word and
+ * returns; the call then reads and clears that word (the raw value into
+ * *code, which may be NULL).  Returns DA_OK when the wait gave up and
+ * recorded the bit -- the context stays usable for the next call -- and
+ * DA_ERR_CUDA if a launch or copy failed or the wait did not give up.  Any
+ * error word set before the call is cleared first.  Takes about 2 s. */
+da_status diffattn_selftest_wait_limit(uint32_t *code, cudaStream_t stream);
+
 /* Number of kernel launches the last successful call on this host thread
  * enqueued (launch accounting for benchmarks). */
 int diffattn_last_launch_count(void);
