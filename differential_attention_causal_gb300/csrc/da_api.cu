@@ -324,14 +324,14 @@ size_t diffattn_v2_decode_workspace_size(int B, int L, int Hq, int Hkv, int D, d
 }
 
 size_t diffattn_v1_decode_workspace_size(int B, int L, int H, int d, da_dtype dtype) {
-    if (dtype != DA_BF16 || (d != 64 && d != 128)) return 0;
+    if (dtype != DA_BF16 || (d != 32 && d != 64 && d != 128)) return 0;
     uint32_t *err = nullptr;
     int nsm = 0;
     if (!device_state(&err, &nsm)) return 0;
     int grid, spb;
     int64_t units;
     size_t cum = 0, ws = 0;
-    if (!decode_plan(B, L, H, 2 * d, nsm, true, &grid, &units, &spb, &cum, &ws)) return 0;
+    if (!decode_plan(B, L, H, d == 32 ? 128 : 2 * d, nsm, true, &grid, &units, &spb, &cum, &ws)) return 0;
     return ws;
 }
 
@@ -446,7 +446,7 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
     if (!q1 || !q2 || !k1_cache || !k2_cache || !v_cache || !lam_q1 || !lam_k1 || !lam_q2 || !lam_k2 || !out)
         return DA_ERR_NULL_PTR;
     if (B < 1 || L < 1 || H < 1 || layer_index < 0) return DA_ERR_BAD_SHAPE;
-    if (dtype == DA_BF16 ? (d != 64 && d != 128) : (d != 32 && d != 64 && d != 128))
+    if (d != 32 && d != 64 && d != 128)
         return DA_ERR_UNSUPPORTED_DIM;
     for (const void *ptr : {q1, q2, k1_cache, k2_cache, v_cache, static_cast<const void *>(out)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
@@ -492,7 +492,11 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
     p.lq1 = lam_q1; p.lk1 = lam_k1; p.lq2 = lam_q2; p.lk2 = lam_k2;
     p.layer_index = layer_index;
     p.out = static_cast<__nv_bfloat16 *>(out);
-    p.B = B; p.L = L; p.Hq = H; p.Hkv = H; p.G = 2; p.D = dv;
+    // d = 32 runs the d = 64 configuration: the k maps are d wide and the v map
+    // 2d wide, their 64-column boxes zero-filled past that (q is zero-padded in
+    // the kernel), so the scores and the first 2d output channels are the same
+    p.B = B; p.L = L; p.Hq = H; p.Hkv = H; p.G = 2; p.D = d == 32 ? 128 : dv;
+    p.dq = d; p.dv = dv;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
     p.err = err;
     return decode_bf16(true, m, p, cache_lens, workspace, workspace_bytes, nsm, stream);

@@ -191,7 +191,9 @@ struct DecodeParams {
     float *ws;                     // partial slots: B * Hkv + grid - 1
     const int *lens;               // per-sequence rows (B), or NULL for all L
     int64_t *cum;                  // lens != NULL: units before sequence b (B + 1)
-    int B, L, Hq, Hkv, G, D;       // V1: Hq = Hkv = H, G = 2, D = 2d
+    int B, L, Hq, Hkv, G, D;       // V1: Hq = Hkv = H, G = 2, D = 2d (128 for d = 32)
+    int dq, dv;                    // V1: the real head dims d and 2d (D = 2d, or 128 for d = 32,
+                                   // which runs on k / v boxes zero-filled past d / 2d)
     int grid;                      // CTAs of the split kernel
     int64_t units;                 // lens == NULL: B * Hkv * spb
     int spb;                       // 64-key units per (b, kv head) at L rows

@@ -294,18 +294,20 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             if (V1) {
                 // column 0 = [q1 | 0], column 1 = [0 | q2]; q1, q2 rows at (b * H + h) * d
                 constexpr int DQ = D / 2;
-                const uint32_t *q1r = reinterpret_cast<const uint32_t *>(p.q + bg * DQ);
-                const uint32_t *q2r = reinterpret_cast<const uint32_t *>(p.q2 + bg * DQ);
+                // (d = p.dq may be less than DQ: the channels past it are zero, as in the
+                // zero-filled k boxes)
+                const uint32_t *q1r = reinterpret_cast<const uint32_t *>(p.q + bg * p.dq);
+                const uint32_t *q2r = reinterpret_cast<const uint32_t *>(p.q2 + bg * p.dq);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const int c0 = 16 * ks + 2 * t4;
                     const bool lo_half = 16 * ks < DQ;
                     if (g8 == 0 && lo_half) {
-                        bq[ks][0] = q1r[c0 >> 1];
-                        bq[ks][1] = q1r[(c0 + 8) >> 1];
+                        bq[ks][0] = c0 < p.dq ? q1r[c0 >> 1] : 0u;
+                        bq[ks][1] = c0 + 8 < p.dq ? q1r[(c0 + 8) >> 1] : 0u;
                     } else if (g8 == 1 && !lo_half) {
-                        bq[ks][0] = q2r[(c0 - DQ) >> 1];
-                        bq[ks][1] = q2r[(c0 - DQ + 8) >> 1];
+                        bq[ks][0] = c0 - DQ < p.dq ? q2r[(c0 - DQ) >> 1] : 0u;
+                        bq[ks][1] = c0 - DQ + 8 < p.dq ? q2r[(c0 - DQ + 8) >> 1] : 0u;
                     } else {
                         bq[ks][0] = bq[ks][1] = 0u;
                     }
@@ -474,20 +476,21 @@ __global__ void __launch_bounds__(D) decode_combine(const DecodeParams p) {
     float y;
     if (V1) {
         // lam = exp(lq1 . lk1) - exp(lq2 . lk2) + lam_init, lam_init = 0.8 - 0.6 exp(-0.3 layer)
-        constexpr int DQ = D / 2;
-        const float d1 = block_sum(dd < DQ ? p.lq1[dd] * p.lk1[dd] : 0.f, red);
-        const float d2 = block_sum(dd < DQ ? p.lq2[dd] * p.lk2[dd] : 0.f, red);
+        const float d1 = block_sum(dd < p.dq ? p.lq1[dd] * p.lk1[dd] : 0.f, red);
+        const float d2 = block_sum(dd < p.dq ? p.lq2[dd] * p.lk2[dd] : 0.f, red);
         const float lam_init = 0.8f - 0.6f * expf(-0.3f * static_cast<float>(p.layer_index));
         const float lam = expf(d1) - expf(d2) + lam_init;
         const float x = Oe / Le - lam * (Oo / Lo);
         const float ss = block_sum(x * x, red);
-        // RMSNorm over the 2d channels, eps 1e-5, no weight; then (1 - lam_init)
-        y = x * ((1.f - lam_init) / sqrtf(ss / static_cast<float>(D) + 1e-5f));
+        // RMSNorm over the 2d channels (those past p.dv are zero), eps 1e-5, no
+        // weight; then (1 - lam_init)
+        y = x * ((1.f - lam_init) / sqrtf(ss / static_cast<float>(p.dv) + 1e-5f));
+        if (dd < p.dv) p.out[static_cast<int64_t>(blockIdx.x) * p.dv + dd] = __float2bfloat16_rn(y);
     } else {
         const float sg = 1.f / (1.f + __expf(-p.lam[blockIdx.x]));
         y = Oe / Le - sg * (Oo / Lo);
+        p.out[static_cast<int64_t>(blockIdx.x) * D + dd] = __float2bfloat16_rn(y);
     }
-    p.out[static_cast<int64_t>(blockIdx.x) * D + dd] = __float2bfloat16_rn(y);
 }
 
 template <int D, bool V1>

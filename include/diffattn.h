@@ -251,7 +251,8 @@ size_t diffattn_v1_decode_workspace_size(int B, int L, int H, int d, da_dtype dt
  *   out             : (B, H, 2d) = (B, C), dtype as inputs
  *   workspace       : DA_BF16 only; at least diffattn_v1_decode_workspace_size()
  *                     bytes, 256-byte aligned, as in diffattn_v2_decode
- *   Supported: d in {64, 128} for DA_BF16; d in {32, 64, 128} for DA_F32.
+ *   Supported: d in {32, 64, 128} for both dtypes (DA_BF16 at d = 32 runs the
+ *   d = 64 kernels on k / v boxes zero-filled past d / 2d).
  */
 da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cache,
                              const void *k2_cache, const void *v_cache, const float *lam_q1,

@@ -187,7 +187,7 @@ def test_v1_decode_argument_checks(lib):
     assert _v1dec(lib, lk1=None) == 1
     assert _v1dec(lib, L=0) == 2
     assert _v1dec(lib, layer=-3) == 2
-    assert _v1dec(lib, d=32) == 3          # bf16 decode needs d in {64, 128}
+    assert _v1dec(lib, d=48) == 3          # bf16 decode needs d in {32, 64, 128}
     assert _v1dec(lib, d=96, dtype=0) == 3
     assert _v1dec(lib, q2=A + 8) == 5
     assert _v1dec(lib, lens=A + 2) == 5    # int32 lengths need 4-byte alignment

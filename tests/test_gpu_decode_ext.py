@@ -131,7 +131,7 @@ def oracle_v1_decode(x, lens=None, rows=None):
 
 @pytest.mark.parametrize("B,L,H,d,varlen", [(3, 1000, 4, 64, False), (2, 1, 2, 128, False), (1, 5000, 2, 128, False),
                                             (4, 777, 3, 128, True), (5, 130, 16, 64, True), (9, 64, 12, 128, True),
-                                            (2, 2049, 16, 64, False)])
+                                            (2, 2049, 16, 64, False), (3, 500, 4, 32, False), (4, 300, 3, 32, True)])
 def test_v1_decode_bf16(B, L, H, d, varlen):
     x = inputs.make_v1_decode(inputs.V1DecodeShape(B, L, H, d, 12, "bf16"), seed=B * 7 + L)
     lens = None
@@ -180,7 +180,8 @@ def test_v1_decode_argument_checks():
     bd = binding()
     xd = to_dev(inputs.make_v1_decode(inputs.V1DecodeShape(2, 100, 2, 64, 0, "bf16"), seed=0))
     assert bd.v1_decode_workspace_size(2, 100, 2, 64) > 0
-    assert bd.v1_decode_workspace_size(2, 100, 2, 32) == 0   # d = 32 runs on the fp32 kernel only
+    assert bd.v1_decode_workspace_size(2, 100, 2, 32) > 0    # d = 32: the d = 64 kernels on zero-filled boxes
+    assert bd.v1_decode_workspace_size(2, 100, 2, 48) == 0
     # the size covers per-sequence lengths (the larger need): 16 bytes less fails that call
     small = torch.empty(bd.v1_decode_workspace_size(2, 100, 2, 64) - 16, dtype=torch.uint8, device="cuda")
     lens = torch.tensor([100, 7], dtype=torch.int32, device="cuda")
