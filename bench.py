@@ -48,7 +48,7 @@ L2_FLUSH_BYTES = 256 << 20
 # it was taken on (sha256 of the .cu file, first 16 hex digits).
 TRAFFIC_RECORDS: dict = {
     # profiles/prefill_onepass_v1_B4_T2048_H16_d64.md: dram__bytes_read.sum + dram__bytes_write.sum
-    "prefill_v1_d64": {"src_sha": "f49a9ba4f7304aec", "bytes_per_launch": 147988736 + 13867264},
+    "prefill_v1_d64": {"src_sha": "50e13b0b703c8a85", "bytes_per_launch": 148303104 + 13934336},
 }
 
 
