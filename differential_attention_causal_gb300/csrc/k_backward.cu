@@ -375,15 +375,30 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                 // every key of this part is at or before every query of the tile: no mask
                 const bool full = key0 + RC - 1 <= qt * C::BM;
                 // two unrolled copies: without the per-element mask where it is all true
+                // two columns at a time on the packed fp32 pipe (the same roundings per element)
                 auto form = [&](auto masked) {
+                    const float2 sc2 = make_float2(sl2, sl2), cc2 = make_float2(cc, cc);
+                    const float2 nl1 = make_float2(-lse1, -lse1), nl2 = make_float2(-lse2, -lse2);
+                    const float2 nd1 = make_float2(-d1, -d1), nd2 = make_float2(-d2, -d2);
 #pragma unroll
-                    for (int c = 0; c < RC; ++c) {
-                        const bool valid = !decltype(masked)::value || (live && key0 + c <= t);
-                        const float dpv = __uint_as_float(dp[c]);
-                        const float p1 = valid ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -lse1)) : 0.f;
-                        const float p2 = valid ? ex2(fmaf(__uint_as_float(s2[c]), sl2, -lse2)) : 0.f;
-                        s1[c] = __float_as_uint(p1 * (dpv - d1));
-                        s2[c] = __float_as_uint(p2 * fmaf(cc, dpv, -d2));
+                    for (int c = 0; c < RC; c += 2) {
+                        const float2 dpv = make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1]));
+                        const float2 x1 =
+                            __ffma2_rn(make_float2(__uint_as_float(s1[c]), __uint_as_float(s1[c + 1])), sc2, nl1);
+                        const float2 x2 =
+                            __ffma2_rn(make_float2(__uint_as_float(s2[c]), __uint_as_float(s2[c + 1])), sc2, nl2);
+                        float2 p1 = make_float2(ex2(x1.x), ex2(x1.y)), p2 = make_float2(ex2(x2.x), ex2(x2.y));
+                        if (decltype(masked)::value) {
+                            const bool v0 = live && key0 + c <= t, v1 = live && key0 + c + 1 <= t;
+                            p1 = make_float2(v0 ? p1.x : 0.f, v1 ? p1.y : 0.f);
+                            p2 = make_float2(v0 ? p2.x : 0.f, v1 ? p2.y : 0.f);
+                        }
+                        const float2 r1 = __fmul2_rn(p1, __fadd2_rn(dpv, nd1));
+                        const float2 r2 = __fmul2_rn(p2, __ffma2_rn(cc2, dpv, nd2));
+                        s1[c] = __float_as_uint(r1.x);
+                        s1[c + 1] = __float_as_uint(r1.y);
+                        s2[c] = __float_as_uint(r2.x);
+                        s2[c + 1] = __float_as_uint(r2.y);
                     }
                 };
                 if (live && full)
@@ -719,17 +734,32 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                         const float l1a[4] = {l1.x, l1.y, l1.z, l1.w}, l2a[4] = {l2.x, l2.y, l2.z, l2.w};
                         const float e1a[4] = {e1.x, e1.y, e1.z, e1.w}, e2a[4] = {e2.x, e2.y, e2.z, e2.w};
                         const float cva[4] = {cv.x, cv.y, cv.z, cv.w};
+                        // two columns at a time on the packed fp32 pipe (the same roundings per element)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
+                        for (int k = 0; k < 4; k += 2) {
                             const int c = 4 * c4 + k;
-                            // key j <= query q0 + c; rows past T carry lse = +inf
-                            const bool valid = !decltype(masked)::value || q0 + c >= j;
-                            const float dpv = __uint_as_float(dp[c]);
-                            const float p1 = valid ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -l1a[k])) : 0.f;
-                            const float p2 = valid ? ex2(fmaf(__uint_as_float(s2[c]), sl2, -l2a[k])) : 0.f;
-                            s1[c] = __float_as_uint(fmaf(cva[k], p2, p1));
-                            s2[c] = __float_as_uint(p1 * (dpv - e1a[k]));
-                            dp[c] = __float_as_uint(p2 * fmaf(cva[k], dpv, -e2a[k]));
+                            const float2 sc2 = make_float2(sl2, sl2), cv2 = make_float2(cva[k], cva[k + 1]);
+                            const float2 dpv = make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1]));
+                            const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(s1[c]), __uint_as_float(s1[c + 1])),
+                                                         sc2, make_float2(-l1a[k], -l1a[k + 1]));
+                            const float2 x2 = __ffma2_rn(make_float2(__uint_as_float(s2[c]), __uint_as_float(s2[c + 1])),
+                                                         sc2, make_float2(-l2a[k], -l2a[k + 1]));
+                            float2 p1 = make_float2(ex2(x1.x), ex2(x1.y)), p2 = make_float2(ex2(x2.x), ex2(x2.y));
+                            if (decltype(masked)::value) {
+                                // key j <= query q0 + c; rows past T carry lse = +inf
+                                const bool v0 = q0 + c >= j, v1 = q0 + c + 1 >= j;
+                                p1 = make_float2(v0 ? p1.x : 0.f, v1 ? p1.y : 0.f);
+                                p2 = make_float2(v0 ? p2.x : 0.f, v1 ? p2.y : 0.f);
+                            }
+                            const float2 r0 = __ffma2_rn(cv2, p2, p1);
+                            const float2 r1 = __fmul2_rn(p1, __fadd2_rn(dpv, make_float2(-e1a[k], -e1a[k + 1])));
+                            const float2 r2 = __fmul2_rn(p2, __ffma2_rn(cv2, dpv, make_float2(-e2a[k], -e2a[k + 1])));
+                            s1[c] = __float_as_uint(r0.x);
+                            s1[c + 1] = __float_as_uint(r0.y);
+                            s2[c] = __float_as_uint(r1.x);
+                            s2[c + 1] = __float_as_uint(r1.y);
+                            dp[c] = __float_as_uint(r2.x);
+                            dp[c + 1] = __float_as_uint(r2.y);
                         }
                     }
                 };
