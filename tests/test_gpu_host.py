@@ -1,8 +1,9 @@
 """The end-to-end DIFF V1 call on host buffers (diffattn_v1_fwd_host): its
 output equals the device call's bit for bit (the chunked forwards compute the
 same tiles) and matches the fp64 oracle within the bf16 / fp32 tolerances;
-the chunking over batch entries covers uneven splits (B = 9 over 8 chunks)
-and the call is ordered on a caller's stream."""
+the chunking over batch entries covers uneven splits (B = 9 and B = 17 over
+8 chunks), single-entry calls and ragged last tiles, and the call is ordered
+on a caller's stream."""
 import numpy as np
 import pytest
 import torch
@@ -40,14 +41,21 @@ def host_call(x, s, stream=None):
     return out, bd.last_launch_count()
 
 
+def expected_launches(B, T, d, dtype):
+    """Chunks of the host call: runs of batch entries, at most 8."""
+    return min(B, 8)
+
+
 @pytest.mark.parametrize("B,T,H,d,layer,dtype", [(3, 200, 2, 64, 1, "bf16"), (9, 129, 2, 64, 0, "bf16"),
                                                  (2, 300, 3, 128, 5, "bf16"), (2, 70, 2, 32, 2, "fp32"),
-                                                 (3, 65, 2, 32, 3, "bf16")])
+                                                 (3, 65, 2, 32, 3, "bf16"), (1, 1000, 2, 64, 4, "bf16"),
+                                                 (2, 700, 2, 32, 6, "bf16"), (17, 130, 1, 64, 2, "bf16"),
+                                                 (4, 1024, 2, 64, 12, "bf16")])
 def test_v1_host_matches_device_call_and_oracle(B, T, H, d, layer, dtype):
     s = inputs.V1Shape(B, T, H, d, layer, dtype)
     x = inputs.make_v1(s, seed=B + T)
     got, launches = host_call(x, s)
-    assert launches == min(B, 8)
+    assert launches == expected_launches(B, T, d, dtype)
     dev = run_v1(to_dev(x), layer).cpu()
     assert torch.equal(got, dev)
     assert_parity(got, oracle_v1(x, layer), dtype)
