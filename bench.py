@@ -247,6 +247,8 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
     flops = v1_flops(s)
     value = job_throughput(flops, args.steps, world, total_ms)
     avg_ms = sum(times) / len(times)
+    med_ms, min_ms = statistics.median(times), min(times)
+    tokens_per_s = s.B * s.T * args.steps * world / (total_ms * 1e-3)
     achieved = flops / (avg_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     tr = TRAFFIC_RECORDS.get("prefill_v1_d64")
@@ -279,7 +281,9 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+        "ms_per_step_median": round(med_ms, 5), "ms_per_step_min": round(min_ms, 5),
+        "tokens_per_s": round(tokens_per_s), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.1) lambda vectors; seed + rank per rank)",
         "config": {"workload": HEADLINE, "B": s.B, "T": s.T, "H": s.H, "d": s.d, "dv": 2 * s.d,
@@ -296,13 +300,27 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
     if aux:
         line["aux"] = aux
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(x, s, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(x, s, out, dev, budget_s=args.cpu_seconds, seed=args.seed,
+                                            per_config=not args.no_aux)
     return line
 
 
 def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
     aux = {}
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # DIFF V1 fp32, the tiny parity workload: a latency figure (fp32 on CUDA cores), no roofline claim
+    s = inputs.WORKLOADS["v1_fp32_B1_T64_H2_d32"]
+    x = inputs.make_v1(s, seed=args.seed, device=dev)
+    out = torch.empty((s.B, s.T, s.H, 2 * s.d), dtype=torch.float32, device=dev)
+    f = lambda: binding.v1_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"],  # noqa
+                               x["lam_q2"], x["lam_k2"], s.layer_index, out=out)
+    for _ in range(10):
+        f()
+    t = time_steps(f, 100, None)
+    aux["v1_fp32_tiny"] = {"workload": "v1_fp32_B1_T64_H2_d32", "ms_median": round(statistics.median(t), 5),
+                           "ms_min": round(min(t), 5), "launches": 1,
+                           "note": "fp32 on CUDA cores; latency-bound, no roofline claim"}
+    del x, out
     # DIFF V2 prefill
     s = inputs.WORKLOADS["v2_bf16_B8_T4096_Hq32_Hkv8_D128"]
     x = inputs.make_v2(s, seed=args.seed, device=dev)
@@ -477,11 +495,16 @@ def _oracle_inputs(x) -> dict:
 
 
 def _oracle_rows_time(x_cpu, s, rows) -> float:
+    return _oracle_rows(x_cpu, s, rows)[0]
+
+
+def _oracle_rows(x_cpu, s, rows):
+    """(wall seconds, output rows) of the V1 oracle on the listed rows."""
     import oracle
     t0 = time.perf_counter()
-    oracle.v1_fwd(x_cpu["q1"], x_cpu["q2"], x_cpu["k1"], x_cpu["k2"], x_cpu["v"], x_cpu["lam_q1"],
-                  x_cpu["lam_k1"], x_cpu["lam_q2"], x_cpu["lam_k2"], s.layer_index, rows=rows)
-    return time.perf_counter() - t0
+    y = oracle.v1_fwd(x_cpu["q1"], x_cpu["q2"], x_cpu["k1"], x_cpu["k2"], x_cpu["v"], x_cpu["lam_q1"],
+                      x_cpu["lam_k1"], x_cpu["lam_q2"], x_cpu["lam_k2"], s.layer_index, rows=rows)
+    return time.perf_counter() - t0, y
 
 
 def _rows_flops(rows, s) -> float:
@@ -490,8 +513,11 @@ def _rows_flops(rows, s) -> float:
     return float(((t + 1) * 12 * s.d).sum())
 
 
-def cpu_baseline(x, s, budget_s: float = 15.0, seed: int = 0) -> dict:
-    """Time the fp64 oracle on a bounded random sample of the headline rows."""
+def cpu_baseline(x, s, out, dev, budget_s: float = 15.0, seed: int = 0, per_config: bool = True) -> dict:
+    """Time the fp64 oracle on a bounded random sample of the headline rows,
+    compare those rows with the timed GPU output, and time the oracle on the
+    other workloads (in full where it finishes in seconds, else on a stated
+    sample with the fraction of the causal work it covers)."""
     import numpy as np
     import oracle
     oracle.build()
@@ -503,11 +529,88 @@ def cpu_baseline(x, s, budget_s: float = 15.0, seed: int = 0) -> dict:
     per_row = dt / len(probe)          # random rows: their mean cost is the workload's mean
     n = int(min(nall, max(len(probe), budget_s / max(per_row, 1e-9))))
     rows = rng.choice(nall, size=n, replace=False)
-    dt = _oracle_rows_time(x_cpu, s, rows)
+    dt, ref = _oracle_rows(x_cpu, s, rows)
     val = _rows_flops(rows, s) / dt / 1e12
-    return {"value": val, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
-            "sample": f"{n} of {nall} output rows (b, t, head) of {HEADLINE}, uniform without replacement; "
-                      f"{dt:.1f} s wall; value = algorithmic 12d-per-pair FLOPs of the sample / wall time"}
+    got = out.reshape(-1, 2 * s.d)[torch.from_numpy(rows).to(out.device)].double().cpu().numpy()
+    err = float(np.abs(got - ref).max())
+    rl2 = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    res = {"value": val, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+           "sample": f"{n} of {nall} output rows (b, t, head) of {HEADLINE}, uniform without replacement; "
+                     f"{dt:.1f} s wall; value = algorithmic 12d-per-pair FLOPs of the sample / wall time",
+           "headline_parity": {"rows": n, "max_abs": err, "rel_l2": rl2, "bound": "max abs <= 2e-2, rel L2 <= 5e-3",
+                               "ok": bool(err <= 2e-2 and rl2 <= 5e-3),
+                               "what": "the timed step's output against the oracle on the sampled rows"}}
+    if per_config:
+        res["configs"] = oracle_per_config(dev, seed)
+    return res
+
+
+def oracle_per_config(dev, seed: int) -> dict:
+    """The fp64 oracle timed on the other workloads, on this host's cores."""
+    import numpy as np
+    import oracle
+    cores = oracle.default_threads()
+    res = {}
+    # DIFF V1 fp32 tiny workload: in full
+    s = inputs.WORKLOADS["v1_fp32_B1_T64_H2_d32"]
+    x = _oracle_inputs(inputs.make_v1(s, seed=seed))
+    t0 = time.perf_counter()
+    oracle.v1_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"],
+                  s.layer_index)
+    dt = time.perf_counter() - t0
+    res["v1_fp32_B1_T64_H2_d32"] = {"s": round(dt, 6), "covered": 1.0, "cores": cores,
+                                    "GFLOP/s": round(v1_flops(s) / dt / 1e9, 3)}
+    # DIFF V2 decode: in full, one batch entry per call (its cache copied out
+    # and widened to fp64 outside the timed calls)
+    s = inputs.WORKLOADS["v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128"]
+    xd = inputs.make_decode(s, seed=seed, device=dev)
+    tot = 0.0
+    for b in range(s.B):
+        xb = {k: xd[k][b:b + 1].double().cpu().numpy() for k in ("q", "k_cache", "v_cache", "lam")}
+        t0 = time.perf_counter()
+        oracle.v2_decode(xb["q"], xb["k_cache"], xb["v_cache"], xb["lam"])
+        tot += time.perf_counter() - t0
+    del xd, xb
+    torch.cuda.empty_cache()
+    res["v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128"] = {
+        "s": round(tot, 3), "covered": 1.0, "cores": cores, "GB/s": round(decode_bytes(s) / tot / 1e9, 3),
+        "note": "all B x Hq/2 rows, one batch entry per call"}
+    # DIFF V2 prefill and long-context DIFF V1: a sample of rows of batch entry 0
+    rng = np.random.default_rng(seed)
+    s = inputs.WORKLOADS["v2_bf16_B8_T4096_Hq32_Hkv8_D128"]
+    xd = inputs.make_v2(s, seed=seed, device=dev)
+    xb = {k: xd[k][0:1].double().cpu().numpy() for k in ("q", "k", "v", "lam")}
+    del xd
+    P = s.Hq // 2
+    rows = rng.choice(s.T * P, size=2048, replace=False)
+    t0 = time.perf_counter()
+    oracle.v2_fwd(xb["q"], xb["k"], xb["v"], xb["lam"], rows=rows)
+    dt = time.perf_counter() - t0
+    pairs = float(((rows // P) + 1).sum()) * 2          # two query heads per output row
+    frac = pairs / (s.B * s.Hq * s.T * (s.T + 1) / 2)
+    res["v2_bf16_B8_T4096_Hq32_Hkv8_D128"] = {
+        "s": round(dt, 3), "covered": frac, "cores": cores,
+        "TFLOP/s": round(pairs * 4 * s.D / dt / 1e12, 5),
+        "sample": "2048 random output rows (t, pair) of batch entry 0"}
+    s = inputs.WORKLOADS["v1_bf16_B1_T32768_H12_d128"]
+    xd = inputs.make_v1(s, seed=seed, device=dev)
+    xb = {k: (xd[k][:, :, 0:1].double().cpu().numpy() if k in ("q1", "q2", "k1", "k2", "v")
+              else xd[k].double().cpu().numpy()) for k in ("q1", "q2", "k1", "k2", "v", "lam_q1", "lam_k1",
+                                                           "lam_q2", "lam_k2")}
+    del xd
+    torch.cuda.empty_cache()
+    rows = rng.choice(s.T, size=256, replace=False)
+    t0 = time.perf_counter()
+    oracle.v1_fwd(xb["q1"], xb["q2"], xb["k1"], xb["k2"], xb["v"], xb["lam_q1"], xb["lam_k1"], xb["lam_q2"],
+                  xb["lam_k2"], s.layer_index, rows=rows)
+    dt = time.perf_counter() - t0
+    pairs = float((rows + 1).sum())
+    frac = pairs / (s.B * s.H * s.T * (s.T + 1) / 2)
+    res["v1_bf16_B1_T32768_H12_d128"] = {
+        "s": round(dt, 3), "covered": frac, "cores": cores,
+        "TFLOP/s": round(pairs * 12 * s.d / dt / 1e12, 5),
+        "sample": "256 random rows t of diff head 0"}
+    return res
 
 
 def run_reference(args, rank: int, world: int) -> dict | None:

@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_status_string.argtypes = [i32]
             L.diffattn_device_error.restype = i32
             L.diffattn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+            L.diffattn_stream_error.restype = i32
+            L.diffattn_stream_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
             L.diffattn_selftest_wait_limit.restype = i32
             L.diffattn_selftest_wait_limit.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
             L.diffattn_last_launch_count.restype = i32
@@ -121,11 +123,22 @@ def selftest_wait_limit(stream=None) -> int:
 
 
 def device_error() -> int:
-    """Synchronise, then read and clear the device error word (0 = no kernel gave up)."""
+    """Synchronise the device, then read and clear every stream's error word
+    (their OR; 0 = no kernel gave up)."""
     code = ctypes.c_uint32(0)
     rc = lib().diffattn_device_error(ctypes.byref(code))
     if rc not in (0, 9, 11):
         raise DiffAttnError("diffattn_device_error", rc)
+    return int(code.value)
+
+
+def stream_error(stream=None) -> int:
+    """Synchronise one stream (default: the current one), then read and clear
+    its error word (0 = no kernel on it gave up)."""
+    code = ctypes.c_uint32(0)
+    rc = lib().diffattn_stream_error(ctypes.byref(code), _stream(stream))
+    if rc not in (0, 9, 11):
+        raise DiffAttnError("diffattn_stream_error", rc)
     return int(code.value)
 
 

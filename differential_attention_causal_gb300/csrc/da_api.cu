@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include <cudaTypedefs.h>
 
@@ -15,34 +16,72 @@
 
 namespace da {
 
-// Sticky device error word, set by bounded waits that give up.
-__device__ uint32_t g_err_word;
+// Sticky device error words, set by bounded waits that give up.  Each stream
+// that calls the library gets a word of its own (slots handed out in order of
+// first use per device), so that an error on one stream neither stops the
+// kernels of another stream (a wait gives up at once when its word already
+// holds a fatal bit) nor shows up when another stream's word is read.  Past
+// kErrSlots streams on one device, later streams share words by hash.
+constexpr int kErrSlots = 256;
+__device__ uint32_t g_err_words[kErrSlots];
 
 namespace {
 
 thread_local int t_last_launches = 0;
 
+struct DeviceState {
+    uint32_t *words = nullptr;   // device address of this device's g_err_words
+    int num_sms = 0;
+    int used = 0;                // slots handed out so far
+    std::unordered_map<uintptr_t, int> slot;   // stream handle -> slot
+};
 std::mutex g_mu;
-uint32_t *g_err_ptr[64];   // per-device address of g_err_word
-int g_num_sms[64];
+DeviceState g_dev[64];
 
-// Address of this device's error word (looked up once per device, with that
-// device current).
-bool device_state(uint32_t **err, int *num_sms) {
+// Looks up (once per device, with that device current) the address of the
+// device's error words and its SM count; if err is not NULL, *err receives
+// the error word of `stream` on this device.
+bool device_state(cudaStream_t stream, uint32_t **err, int *num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_err_ptr[dev]) {
+    DeviceState &ds = g_dev[dev];
+    if (!ds.words) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess || !p) return false;
+        if (cudaGetSymbolAddress(&p, g_err_words) != cudaSuccess || !p) return false;
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             return false;
-        g_err_ptr[dev] = static_cast<uint32_t *>(p);
-        g_num_sms[dev] = n;
+        ds.words = static_cast<uint32_t *>(p);
+        ds.num_sms = n;
     }
-    *err = g_err_ptr[dev];
-    if (num_sms) *num_sms = g_num_sms[dev];
+    if (err) {
+        const uintptr_t key = reinterpret_cast<uintptr_t>(stream);
+        auto it = ds.slot.find(key);
+        int s;
+        if (it != ds.slot.end()) {
+            s = it->second;
+        } else if (ds.used < kErrSlots) {
+            s = ds.used++;
+            ds.slot.emplace(key, s);
+        } else {
+            s = static_cast<int>((key >> 4) % kErrSlots);
+        }
+        *err = ds.words + s;
+    }
+    if (num_sms) *num_sms = ds.num_sms;
+    return true;
+}
+
+// Error words of every slot handed out on the current device (for the
+// device-wide read).
+bool device_words(uint32_t **words, int *used) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (!device_state(nullptr, nullptr, nullptr)) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    *words = g_dev[dev].words;
+    *used = g_dev[dev].used;
     return true;
 }
 
@@ -129,28 +168,53 @@ const char *diffattn_status_string(da_status s) {
 
 int diffattn_last_launch_count(void) { return t_last_launches; }
 
+static da_status status_of_word(uint32_t v) {
+    if (v == 0) return DA_OK;
+    if (v == kErrBadLength) return DA_ERR_BAD_LENGTH;
+    return DA_ERR_DEVICE_TIMEOUT;
+}
+
 da_status diffattn_device_error(uint32_t *code) {
-    uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    uint32_t *words = nullptr;
+    int used = 0;
+    if (!device_words(&words, &used)) return DA_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
     uint32_t v = 0;
-    if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
-    if (v != 0 && cudaMemset(err, 0, sizeof(v)) != cudaSuccess) return DA_ERR_CUDA;
-    if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
+    if (used > 0) {
+        uint32_t w[kErrSlots];
+        if (cudaMemcpy(w, words, sizeof(uint32_t) * used, cudaMemcpyDeviceToHost) != cudaSuccess) return DA_ERR_CUDA;
+        for (int i = 0; i < used; ++i) v |= w[i];
+        if (v != 0 && cudaMemset(words, 0, sizeof(uint32_t) * used) != cudaSuccess) return DA_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return DA_ERR_CUDA;
+    }
     if (code) *code = v;
-    if (v == kErrBadLength) return DA_ERR_BAD_LENGTH;
-    return v ? DA_ERR_DEVICE_TIMEOUT : DA_OK;
+    return status_of_word(v);
+}
+
+da_status diffattn_stream_error(uint32_t *code, cudaStream_t stream) {
+    uint32_t *err = nullptr;
+    if (!device_state(stream, &err, nullptr)) return DA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DA_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, err, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return DA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DA_ERR_CUDA;
+    if (v != 0) {
+        if (cudaMemsetAsync(err, 0, sizeof(v), stream) != cudaSuccess) return DA_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return DA_ERR_CUDA;
+    }
+    if (code) *code = v;
+    return status_of_word(v);
 }
 
 da_status diffattn_selftest_wait_limit(uint32_t *code, cudaStream_t stream) {
     uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    if (!device_state(stream, &err, nullptr)) return DA_ERR_CUDA;
     uint32_t before = 0;
-    if (diffattn_device_error(&before) == DA_ERR_CUDA) return DA_ERR_CUDA;   // start from a clear word
+    if (diffattn_stream_error(&before, stream) == DA_ERR_CUDA) return DA_ERR_CUDA;   // start from a clear word
     bool gave_up = false;
     if (run_wait_selftest(err, &gave_up, stream) != cudaSuccess) return DA_ERR_CUDA;
     uint32_t v = 0;
-    if (diffattn_device_error(&v) == DA_ERR_CUDA) return DA_ERR_CUDA;   // reads and clears the word
+    if (diffattn_stream_error(&v, stream) == DA_ERR_CUDA) return DA_ERR_CUDA;   // reads and clears the word
     if (code) *code = v;
     t_last_launches = 1;
     return (gave_up && (v & kErrWaitTimeout) != 0) ? DA_OK : DA_ERR_CUDA;
@@ -180,7 +244,7 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
         if (!stride_ok(s, es)) return DA_ERR_MISALIGNED;
     uint32_t *err = nullptr;
     int nsm = 0;
-    if (!device_state(&err, &nsm)) return DA_ERR_CUDA;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     t_last_launches = 0;
     if (dtype == DA_F32) {
         SimtParams p{};
@@ -218,6 +282,7 @@ da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const 
     p.layer_index = layer_index;
     p.B = B; p.T = T; p.H = H; p.G = 1;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
+    p.num_sms = nsm;
     p.err = err;
     const da_status st = cuda_status(twopass ? launch_prefill_v1_twopass(m, p, d, stream)
                                              : launch_prefill(m, p, d, 2 * d, false, stream));
@@ -235,7 +300,8 @@ da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const flo
     for (const void *ptr : {q, k, v, static_cast<const void *>(out)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
     uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    int nsm = 0;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     const int P = Hq / 2, G = Hq / Hkv;
     t_last_launches = 0;
     if (dtype == DA_F32) {
@@ -271,6 +337,7 @@ da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const flo
     p.lam = lam;
     p.B = B; p.T = T; p.H = P; p.G = G;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.num_sms = nsm;
     p.err = err;
     const da_status st = cuda_status(launch_prefill(m, p, D, D, true, stream));
     if (st == DA_OK) t_last_launches = 1;
@@ -286,7 +353,8 @@ da_status diffattn_paired_fwd(const void *q, const void *k, const void *v, void 
     for (const void *ptr : {q, k, v, static_cast<const void *>(out)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
     uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    int nsm = 0;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     t_last_launches = 0;
     PrefillMaps m;
     const uint64_t uT = static_cast<uint64_t>(T), uB = static_cast<uint64_t>(B), uH = static_cast<uint64_t>(H);
@@ -302,6 +370,7 @@ da_status diffattn_paired_fwd(const void *q, const void *k, const void *v, void 
     p.o_sh = D; p.o_st = st; p.o_sb = st * T;
     p.B = B; p.T = T; p.H = H / 2; p.G = 2;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.num_sms = nsm;
     p.err = err;
     const da_status s = cuda_status(launch_paired(m, p, D, stream));
     if (s == DA_OK) t_last_launches = 1;
@@ -314,7 +383,7 @@ size_t diffattn_v2_decode_workspace_size(int B, int L, int Hq, int Hkv, int D, d
     if (D != 64 && D != 128) return 0;
     uint32_t *err = nullptr;
     int nsm = 0;
-    if (!device_state(&err, &nsm)) return 0;
+    if (!device_state(nullptr, nullptr, &nsm)) return 0;
     int grid, spb;
     int64_t units;
     size_t cum = 0, ws = 0;
@@ -327,7 +396,7 @@ size_t diffattn_v1_decode_workspace_size(int B, int L, int H, int d, da_dtype dt
     if (dtype != DA_BF16 || (d != 32 && d != 64 && d != 128)) return 0;
     uint32_t *err = nullptr;
     int nsm = 0;
-    if (!device_state(&err, &nsm)) return 0;
+    if (!device_state(nullptr, nullptr, &nsm)) return 0;
     int grid, spb;
     int64_t units;
     size_t cum = 0, ws = 0;
@@ -362,19 +431,32 @@ da_status decode_bf16(bool v1, const DecodeMaps &m, DecodeParams p, const int32_
     return st;
 }
 
-da_status v2_decode_impl(const void *q, const void *k_cache, const void *v_cache, const float *lam,
-                         const int32_t *lens, void *out, void *workspace, size_t workspace_bytes, int B, int L,
-                         int Hq, int Hkv, int D, da_dtype dtype, cudaStream_t stream) {
+}  // namespace
+
+// Argument checks of the V2 decode entry points (nothing enqueued on failure).
+static da_status v2_decode_check(const void *q, const void *k_cache, const void *v_cache, const float *lam,
+                                 const void *out, int B, int L, int Hq, int Hkv, int D, da_dtype dtype) {
     if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
     if (!q || !k_cache || !v_cache || !lam || !out) return DA_ERR_NULL_PTR;
     if (B < 1 || L < 1 || Hq < 2 || Hkv < 1) return DA_ERR_BAD_SHAPE;
     if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
     if (D != 64 && D != 128) return DA_ERR_UNSUPPORTED_DIM;
-    for (const void *ptr : {q, k_cache, v_cache, static_cast<const void *>(out)})
+    for (const void *ptr : {q, k_cache, v_cache, out})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    if (dtype == DA_BF16 && Hq / Hkv > 8) return DA_ERR_BAD_GROUP;
+    return DA_OK;
+}
+
+namespace {
+
+da_status v2_decode_impl(const void *q, const void *k_cache, const void *v_cache, const float *lam,
+                         const int32_t *lens, void *out, void *workspace, size_t workspace_bytes, int B, int L,
+                         int Hq, int Hkv, int D, da_dtype dtype, cudaStream_t stream) {
+    const da_status chk = v2_decode_check(q, k_cache, v_cache, lam, out, B, L, Hq, Hkv, D, dtype);
+    if (chk != DA_OK) return chk;
     uint32_t *err = nullptr;
     int nsm = 0;
-    if (!device_state(&err, &nsm)) return DA_ERR_CUDA;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     const int P = Hq / 2, G = Hq / Hkv;
     t_last_launches = 0;
     if (dtype == DA_F32) {
@@ -453,7 +535,7 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
     if (cache_lens && (reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0) return DA_ERR_MISALIGNED;
     uint32_t *err = nullptr;
     int nsm = 0;
-    if (!device_state(&err, &nsm)) return DA_ERR_CUDA;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     t_last_launches = 0;
     const int dv = 2 * d;
     if (dtype == DA_F32) {
@@ -582,7 +664,8 @@ da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, 
     const SavedLayout sl(B, T, H, 2 * d, saved_esize(false, dtype));
     if (saved_bytes < sl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    int nsm = 0;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     t_last_launches = 0;
     if (dtype == DA_F32) {
         SimtParams p{};
@@ -622,6 +705,7 @@ da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, 
     p.layer_index = layer_index;
     p.B = B; p.T = T; p.H = H; p.G = 1;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
+    p.num_sms = nsm;
     p.err = err;
     char *sv = static_cast<char *>(saved);
     p.sa1 = sv;
@@ -646,7 +730,8 @@ da_status diffattn_v2_fwd_train(const void *q, const void *k, const void *v, con
     const SavedLayout sl(B, T, P, D, saved_esize(true, dtype));
     if (saved_bytes < sl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    int nsm = 0;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     t_last_launches = 0;
     if (dtype == DA_F32) {
         SimtParams p{};
@@ -685,6 +770,7 @@ da_status diffattn_v2_fwd_train(const void *q, const void *k, const void *v, con
     p.lam = lam;
     p.B = B; p.T = T; p.H = P; p.G = G;
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.num_sms = nsm;
     p.err = err;
     char *sv = static_cast<char *>(saved);
     p.sa1 = sv;
@@ -722,7 +808,8 @@ da_status diffattn_v1_bwd(const void *q1, const void *q2, const void *k1, const 
     const BwdWsLayout wl(B, T, H, DV, true, f32 ? 4 : 2);
     if (saved_bytes < sl.total || workspace_bytes < wl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    int nsm = 0;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     t_last_launches = 0;
     char *ws = static_cast<char *>(workspace);
     const char *sv = static_cast<const char *>(saved);
@@ -823,7 +910,8 @@ da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const flo
     const BwdWsLayout wl(B, T, P, D, false, 4);
     if (saved_bytes < sl.total || workspace_bytes < wl.total) return DA_ERR_WORKSPACE_TOO_SMALL;
     uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    int nsm = 0;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     t_last_launches = 0;
     char *ws = static_cast<char *>(workspace);
     const char *sv = static_cast<const char *>(saved);
@@ -916,7 +1004,8 @@ extern "C" da_status diffattn_prologue(void *q, void *k, int B, int T, int Hq, i
         if (ptr && !aligned16(ptr)) return DA_ERR_MISALIGNED;
     if (lam && !aligned16(lam)) return DA_ERR_MISALIGNED;
     uint32_t *err = nullptr;
-    if (!device_state(&err, nullptr)) return DA_ERR_CUDA;
+    int nsm = 0;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
     t_last_launches = 0;
     if (Hq + Hk == 0 && !x) return DA_OK;   // nothing to do
     PrologueParams p{};
@@ -967,19 +1056,19 @@ bool noalloc_scratch(void **p) {
 extern "C" da_status diffattn_v2_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                                 const float *lam, void *out, int B, int L, int Hq, int Hkv,
                                                 int D, da_dtype dtype, cudaStream_t stream) {
-    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
-    if (!q || !k_cache || !v_cache || !lam || !out) return DA_ERR_NULL_PTR;
+    // every argument check of the workspace entry point first, so that an
+    // invalid call gets the same status there and here
+    const da_status chk = v2_decode_check(q, k_cache, v_cache, lam, out, B, L, Hq, Hkv, D, dtype);
+    if (chk != DA_OK) return chk;
     if (dtype == DA_F32)   // the fp32 kernel uses no scratch
         return diffattn_v2_decode(q, k_cache, v_cache, lam, out, nullptr, 0, B, L, Hq, Hkv, D, dtype, stream);
-    uint32_t *err = nullptr;
     int nsm = 0;
     int grid, spb;
     int64_t units;
     size_t cum = 0, need = 0;
-    if (B >= 1 && L >= 1 && Hq >= 2 && Hkv >= 1 && Hq % Hkv == 0 && (D == 64 || D == 128) &&
-        device_state(&err, &nsm) && decode_plan(B, L, Hkv, D, nsm, false, &grid, &units, &spb, &cum, &need) &&
-        need > kNoAllocScratchBytes)
-        return DA_ERR_SCRATCH_LIMIT;
+    if (!device_state(nullptr, nullptr, &nsm)) return DA_ERR_CUDA;
+    if (!decode_plan(B, L, Hkv, D, nsm, false, &grid, &units, &spb, &cum, &need)) return DA_ERR_BAD_SHAPE;
+    if (need > kNoAllocScratchBytes) return DA_ERR_SCRATCH_LIMIT;
     void *scratch = nullptr;
     if (!noalloc_scratch(&scratch)) return DA_ERR_CUDA;
     return diffattn_v2_decode(q, k_cache, v_cache, lam, out, scratch, kNoAllocScratchBytes, B, L, Hq, Hkv, D,

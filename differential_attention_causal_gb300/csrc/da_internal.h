@@ -17,6 +17,24 @@ enum : uint32_t {
     kErrFatal = kErrWaitTimeout | kErrAborted,   // bits after which kernels stop waiting
 };
 
+// Runs set() once per device and remembers success in one bit of *done.
+// Kernel attributes such as the dynamic shared-memory opt-in belong to the
+// current device's context, so a launcher that sets them must do so on every
+// device it launches on; the bitmask is read and updated atomically so that
+// host threads may launch concurrently (set() may then run more than once on
+// a device, which is harmless).  Devices past 63 run set() on every call.
+template <typename F>
+inline cudaError_t once_per_device(unsigned long long *done, F &&set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && bit) __atomic_fetch_or(done, bit, __ATOMIC_RELEASE);
+    return e;
+}
+
 // ---------------------------------------------------------------- SIMT fp32
 // One warp per output row.  mode 1 = DIFF V1, mode 2 = DIFF V2 (prefill or
 // decode).  Query t attends keys 0 .. t + (Lk - Tq): Lk == Tq is the causal
@@ -56,6 +74,7 @@ struct PrefillParams {
     int B, T, H, G;
     float scale_log2;              // log2(e) / sqrt(dqk)
     uint32_t *err;
+    int num_sms;                   // SMs of the device (the persistent grid)
     // training forward only ((B, T, H, DV) contiguous; NULL for the plain
     // forward): V1 saves x = a1 - lam a2 (the RMSNorm input) and a2 in fp32,
     // V2 saves a_e and a_o in bf16 (a_b = O_b / l_b); both save each branch's

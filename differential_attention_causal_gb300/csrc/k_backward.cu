@@ -1007,15 +1007,15 @@ __global__ void __launch_bounds__(1024) bwd_lambda(const BwdPreParams p) {
 template <int DQK, int DV, bool V2>
 cudaError_t launch_bwd_t(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, cudaStream_t s) {
     using C = BwdCfg<DQK, DV, V2>;
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
+    static unsigned long long attr_done = 0;   // one bit per device
+    cudaError_t ea = once_per_device(&attr_done, [] {
         cudaError_t e = cudaFuncSetAttribute(bwd_dq<DQK, DV, V2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::DQ_SMEM);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(bwd_dkdv<DQK, DV, V2>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KV_SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+        return e;
+    });
+    if (ea != cudaSuccess) return ea;
     const int64_t rows = static_cast<int64_t>(pp.B) * pp.T * pp.H;
     const int64_t pre_blocks = (rows + 7) / 8;
     if (pre_blocks < 1 || pre_blocks > 0x7fffffff) return cudaErrorInvalidValue;

@@ -496,13 +496,11 @@ __global__ void __launch_bounds__(D) decode_combine(const DecodeParams p) {
 template <int D, bool V1>
 cudaError_t launch_decode_t(const DecodeMaps &m, const DecodeParams &p, cudaStream_t s) {
     using C = DecCfg<D>;
-    static bool attr_set = false;   // per process; the attribute is per function
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split<D, V1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static unsigned long long attr_done = 0;   // one bit per device
+    cudaError_t ea = once_per_device(&attr_done, [] {
+        return cudaFuncSetAttribute(decode_split<D, V1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (ea != cudaSuccess) return ea;
     if (p.lens) {
         decode_prefix<<<1, 1024, 0, s>>>(p);
         cudaError_t e = cudaGetLastError();

@@ -653,10 +653,8 @@ __global__ void __launch_bounds__(384, 1)
 template <int DQK, int DV, bool V2, bool TRAIN, bool PAIRED = false>
 cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
     using C = PreCfg<DQK, DV, V2>;
-    int dev = 0;
-    cudaGetDevice(&dev);
     static unsigned long long attr_done = 0;   // one bit per device
-    if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    const cudaError_t ea = once_per_device(&attr_done, [] {
         // The register split inside the kernel must fit in what the launch
         // grants (384 threads x registers per thread), or its increase would
         // never complete: refuse to launch otherwise.
@@ -664,24 +662,16 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
         cudaError_t e = cudaFuncGetAttributes(&fa, prefill_onepass<DQK, DV, V2, TRAIN, PAIRED>);
         if (e != cudaSuccess) return e;
         if (C::REG_SPLIT && fa.numRegs < C::REGS_NEEDED_AT_LAUNCH) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2, TRAIN, PAIRED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM);
-        if (e != cudaSuccess) return e;
-        __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
-    }
+        return cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2, TRAIN, PAIRED>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (ea != cudaSuccess) return ea;
     const int n_qt = (p.T + C::BM - 1) / C::BM;
     const long long tiles = static_cast<long long>(n_qt) * p.H * p.B;
     if (tiles < 1 || tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     // persistent: one CTA per SM (shared memory and TMEM allow no more)
-    static int num_sms[64];
-    if (dev < 64 && num_sms[dev] == 0) {
-        int nsm = 0;
-        cudaError_t e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess || nsm < 1) return e != cudaSuccess ? e : cudaErrorInvalidValue;
-        num_sms[dev] = nsm;
-    }
-    const int sms = dev < 64 ? num_sms[dev] : 1;
-    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
+    if (p.num_sms < 1) return cudaErrorInvalidValue;
+    const unsigned grid = static_cast<unsigned>(tiles < p.num_sms ? tiles : p.num_sms);
     prefill_onepass<DQK, DV, V2, TRAIN, PAIRED><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, m.out, p);
     return cudaGetLastError();
 }

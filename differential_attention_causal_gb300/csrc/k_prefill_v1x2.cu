@@ -507,19 +507,16 @@ __global__ void __launch_bounds__(384, 1)
 template <int DQK>
 cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
     using C = V1x2Cfg<DQK>;
-    int dev = 0;
-    cudaGetDevice(&dev);
     static unsigned long long attr_done = 0;   // one bit per device
-    if (dev < 64 && !(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    const cudaError_t ea = once_per_device(&attr_done, [] {
         // the in-kernel register split must fit in the launch-time budget
         cudaFuncAttributes fa;
         cudaError_t e = cudaFuncGetAttributes(&fa, prefill_v1_twopass<DQK>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs < C::REGS_NEEDED_AT_LAUNCH) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(prefill_v1_twopass<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        __atomic_fetch_or(&attr_done, 1ull << dev, __ATOMIC_RELEASE);
-    }
+        return cudaFuncSetAttribute(prefill_v1_twopass<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    });
+    if (ea != cudaSuccess) return ea;
     const int n_qt = (p.T + C::BM - 1) / C::BM;
     const long long grid = static_cast<long long>(n_qt) * p.H * p.B;
     if (grid < 1 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;

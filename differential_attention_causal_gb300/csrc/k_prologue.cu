@@ -357,13 +357,11 @@ cudaError_t launch_e(const PrologueParams &p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     if (p.x) {
-        static bool attr_set = false;   // per process; the attribute is per function
-        if (!attr_set) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(prologue_lambda<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
-            if (e != cudaSuccess) return e;
-            attr_set = true;
-        }
+        static unsigned long long attr_done = 0;   // one bit per device
+        const cudaError_t ea = once_per_device(&attr_done, [] {
+            return cudaFuncSetAttribute(prologue_lambda<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
+        });
+        if (ea != cudaSuccess) return ea;
         const int64_t blocks = (ntok + TB - 1) / TB;
         if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
         const int smem = sizeof(E) == 2 ? LSTAGES * lstage(p.P) : 0;   // the fp32 path stages nothing

@@ -57,8 +57,11 @@
  *     launch error is returned as DA_ERR_CUDA.  Work is asynchronous on
  *     `stream` (NULL = legacy default stream).
  *   - Device-side waits are bounded: a kernel that gives up waiting records a
- *     code in a device error word and returns; read it with
- *     diffattn_device_error().
+ *     code in the error word of the stream it was launched on and returns;
+ *     read it with diffattn_stream_error() (that stream only) or
+ *     diffattn_device_error() (every stream of the device).  Each stream has
+ *     a word of its own, so an error on one stream neither cuts short the
+ *     kernels of another stream nor is reported to its caller.
  */
 #ifndef DIFFATTN_H
 #define DIFFATTN_H
@@ -342,21 +345,32 @@ da_status diffattn_prologue(void *q, void *k, int B, int T, int Hq, int Hk, int 
 /* Static string for a status code (never NULL). */
 const char *diffattn_status_string(da_status s);
 
-/* Synchronises the current device, reads and clears the device error word that
- * the kernels set when a bounded wait gives up.  *code receives the raw word
- * (0 = no error).  Returns DA_OK if the word was 0, DA_ERR_DEVICE_TIMEOUT if a
- * kernel recorded a give-up, DA_ERR_BAD_LENGTH if the only record is a decode
- * cache length outside 1..L, DA_ERR_CUDA if the read itself failed. */
+/* Error words.  The library keeps one 32-bit error word per stream that has
+ * called it (per device, handed out on a stream's first call; past 256
+ * streams on one device, further streams share words).  A kernel that gives
+ * up a bounded wait, or that meets a decode cache length outside 1..L, sets a
+ * bit in the word of the stream it runs on; the other kernels of that stream
+ * then give up their waits at once, those of other streams do not notice.
+ *
+ * diffattn_stream_error synchronises `stream` only, then reads and clears
+ * its word.  diffattn_device_error synchronises the whole current device,
+ * then reads and clears every stream's word and returns their OR.
+ * *code (may be NULL) receives the raw word (0 = no error).  Both return
+ * DA_OK if the word was 0, DA_ERR_DEVICE_TIMEOUT if a kernel recorded a
+ * give-up, DA_ERR_BAD_LENGTH if the only record is a decode cache length
+ * outside 1..L, DA_ERR_CUDA if the synchronisation or the read failed. */
+da_status diffattn_stream_error(uint32_t *code, cudaStream_t stream);
 da_status diffattn_device_error(uint32_t *code);
 
 /* Failure-path self-test: one warp waits on an mbarrier phase that nothing
  * completes.  Its bounded wait gives up after the library's limit (2 s of
- * global time), records the timeout bit in the device error word and
+ * global time), records the timeout bit in the error word of `stream` and
  * returns; the call then reads and clears that word (the raw value into
- * *code, which may be NULL).  Returns DA_OK when the wait gave up and
+ * *code, which may be NULL), synchronising `stream` only.  Returns DA_OK when the wait gave up and
  * recorded the bit -- the context stays usable for the next call -- and
  * DA_ERR_CUDA if a launch or copy failed or the wait did not give up.  Any
- * error word set before the call is cleared first.  Takes about 2 s. */
+ * error recorded on `stream` before the call is cleared first.  Takes about
+ * 2 s.  Run one self-test at a time per device. */
 da_status diffattn_selftest_wait_limit(uint32_t *code, cudaStream_t stream);
 
 /* Number of kernel launches the last successful call on this host thread

@@ -3,9 +3,13 @@ fp64 oracle's gradients, on the same bf16-rounded inputs and upstream
 gradient.  Also: the training forward's output equals the plain forward's.
 
 Tolerance for bf16 gradients (per tensor, against the fp64 oracle):
-relative L2 <= 2e-2 and max abs <= 5e-2 * max|ref| (see the design notes for
-how the bound follows from the bf16 roundings on the path: P and dS fed to
-the tensor cores in bf16, the upstream gradient of branch 1 in bf16).  The
+relative L2 <= 5e-3 and max abs <= 5e-2 * max|ref|.  Each gradient element
+is an fp32 sum of products carrying up to three bf16 roundings (P or dS fed
+to the tensor cores, the bf16 operand, the upstream gradient of branch 1):
+independent relative errors of 2^-9 each give about 3^(1/2) 2^-9 = 3.4e-3
+in L2, which the measured errors (2.3e-3 to 4e-3) match; the L2 bound is the
+forward's.  The max-abs term allows a single element the sum of the three
+worst-case roundings on a gradient whose terms partly cancel.  The
 V1 lambda-vector gradients are one scalar dL/dlam = -sum dx . a2 (times
 fixed vectors), a sum whose terms cancel: its error is bounded against the
 size of those terms, |err| <= 1e-2 * sum |dx_c a2_c| (the oracle reports that
@@ -22,7 +26,7 @@ from test_gpu_parity import binding, built, to_dev  # noqa: F401  (fixture)
 
 pytestmark = pytest.mark.gpu
 
-RL2, MAXREL = 2e-2, 5e-2
+RL2, MAXREL = 5e-3, 5e-2
 
 
 def check_grad(name, got, ref, report=None):
@@ -200,14 +204,14 @@ def test_v2_backward_long_sequence():
 
 # ------------------------------------------------------------------ fp32 path
 # fp32 everywhere (CUDA cores, exact fp32 sums): the bound is the fp32 one of
-# the forward, max abs <= 1e-4, taken relative to the gradient's scale
-# (max abs <= 1e-4 * max(1, max|ref|)); the lambda-vector gradients against
+# the forward, max abs <= 1e-4 absolute; the lambda-vector gradients against
 # the size of the terms that cancel in dL/dlam, as for bf16 but at 1e-4.
 
 def check_f32(name, got, ref):
     got = got.detach().double().cpu().numpy().reshape(ref.shape)
     err = np.abs(got - ref).max()
-    assert np.isfinite(got).all() and err <= 1e-4 * max(1.0, np.abs(ref).max()), f"{name}: max abs {err:.3e}"
+    print(f"fp32 {name}: max abs {err:.3e} (max |ref| {np.abs(ref).max():.3e})")
+    assert np.isfinite(got).all() and err <= 1e-4, f"{name}: max abs {err:.3e}"
 
 
 @pytest.mark.parametrize("B,T,H,d", [(2, 45, 2, 32), (1, 70, 3, 64), (1, 33, 2, 128)])

@@ -3,6 +3,7 @@ fault: a kernel waits on an mbarrier phase that nothing completes; its bounded
 wait must give up after the library's limit, report through the device error
 word, and leave the context usable for the next call (here a DIFF V1 forward
 checked against the oracle)."""
+import threading
 import time
 
 import pytest
@@ -38,3 +39,43 @@ def test_a_stale_error_word_is_cleared_before_the_self_test():
     assert bd.selftest_wait_limit() & 1        # a second run reports its own give-up again
     assert bd.device_error() == 0
     torch.cuda.synchronize()
+
+
+def test_an_error_on_one_stream_stays_on_that_stream():
+    """Each stream has its own error word: while the self-test's bounded wait
+    runs out on stream A (about 2 s), DIFF V1 forwards on stream B run to
+    parity and B's word reads 0 -- reading it synchronises B only, and A's
+    give-up neither cuts B's waits short nor is reported to B."""
+    bd = binding()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    s = inputs.V1Shape(1, 300, 2, 64, 4, "bf16")
+    x = inputs.make_v1(s, seed=21)
+    xd = to_dev(x)
+    ref = oracle_v1(x, s.layer_index)
+    torch.cuda.synchronize()
+    res = {}
+
+    def on_a():
+        try:
+            res["code"] = bd.selftest_wait_limit(sa)
+        except Exception as e:  # noqa: BLE001  (reported below)
+            res["exc"] = e
+
+    th = threading.Thread(target=on_a)
+    th.start()
+    outs, words = [], []
+    with torch.cuda.stream(sb):
+        t0 = time.monotonic()
+        while len(outs) < 4 or (th.is_alive() and time.monotonic() - t0 < 30.0):
+            outs.append(run_v1(xd, s.layer_index))
+            words.append(bd.stream_error(sb))
+            if len(outs) >= 64:
+                break
+    th.join(60.0)
+    assert not th.is_alive()
+    assert "exc" not in res, res.get("exc")
+    assert res["code"] & 1, res                  # A's own give-up, reported on A
+    assert words == [0] * len(words), words      # never on B
+    for y in outs:
+        assert_parity(y, ref, "bf16")
+    assert bd.device_error() == 0                # A's word was cleared by its reader

@@ -1,0 +1,209 @@
+"""GPU parity on inputs that take the online softmax's rare branches, and on
+the method's edge cases, against the fp64 oracle.
+
+The one-pass prefill (DIFF V1 d <= 64, DIFF V2, Paired Head Attention and
+the training forward) rescales its O accumulator in tensor memory only when
+a row's running maximum grows by more than 8 log2 units, and otherwise lets
+P = 2^(s - m_ref) grow up to 2^8 under a stale maximum.  The inputs of
+``rescale_cases`` plant a score level per key tile that steps past that
+threshold at some tiles and just below it at others; every test here first
+checks on the host, from the exact scores of the rounded inputs, that rows
+of the launch do take the rescale and do write P above 2^4 under a stale
+maximum, then compares the kernel's output with the oracle element by
+element at the bf16 bound (max abs <= 2e-2, relative L2 <= 5e-3).
+
+Edge cases of the definitions ("Differential Transformer V2", DiffAttnV1 /
+DiffAttnV2; the identical-branch remark on the Hacker News pages): identical
+branches (q1 = q2, k1 = k2 gives (1 - lam) A before the norm), lambda below
+0, near 1 and above 1 (x = a1 - lam a2 cancels in part and the RMSNorm
+scales the remainder up), and V2 gate logits far in either tail (sigmoid 0
+and 1, including logits whose exp overflows fp32).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rescale_cases as rc
+from differential_attention_causal_gb300 import inputs
+from test_gpu_parity import assert_parity, binding, built, oracle_v1, run_v1, to_dev  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+
+def assert_branches(resc, stale):
+    """Rows of the launch take the rescale, and write P above 2^4 under a stale maximum."""
+    assert (resc > 0).sum() >= 64, np.bincount(resc)
+    assert (stale > 4.0).sum() >= 64, stale.max()
+
+
+# ------------------------------------------------------------------- DIFF V1
+
+@pytest.mark.parametrize("B,T,H,d", [(1, 1024, 2, 64), (2, 1100, 3, 64), (1, 1300, 2, 32)])
+def test_v1_lazy_rescale(B, T, H, d):
+    x = inputs.make_v1(inputs.V1Shape(B, T, H, d, 12, "bf16"), seed=T + H)
+    rc.plant_v1(x, d)
+    for br in (0, 1):
+        assert_branches(*rc.v1_decisions(x, B - 1, H - 1, br))
+    y = run_v1(to_dev(x), 12)
+    assert_parity(y, oracle_v1(x, 12), "bf16")
+
+
+def test_v1_lazy_rescale_two_pass_d128():
+    # the d = 128 kernel takes exact row statistics in a first pass; the
+    # planted levels still test its exponent range
+    x = inputs.make_v1(inputs.V1Shape(1, 1024, 2, 128, 27, "bf16"), seed=5)
+    rc.plant_v1(x, 128)
+    y = run_v1(to_dev(x), 27)
+    assert_parity(y, oracle_v1(x, 27), "bf16")
+
+
+def test_v1_lazy_rescale_full_workload_sampled():
+    """B=4, T=2048, 16 diff heads, d=64 (the bench's V1 workload and launch) with
+    planted levels: sampled rows against the oracle."""
+    s = inputs.WORKLOADS["v1_bf16_B4_T2048_H16_d64"]
+    x = inputs.make_v1(s, seed=0)
+    rc.plant_v1(x, s.d)
+    assert_branches(*rc.v1_decisions(x, 3, 15, 0))
+    y = run_v1(to_dev(x), s.layer_index)
+    rng = np.random.default_rng(11)
+    ts = [0, 127, 128, 300, 1023, 1024, 2047]
+    rows = [(b * s.T + t) * s.H + h for b in range(s.B) for h in (0, 7, 15) for t in ts]
+    rows += list(rng.integers(0, s.B * s.T * s.H, 400))
+    rows = np.array(rows, dtype=np.int64)
+    ref = oracle_v1(x, s.layer_index, rows=rows)
+    assert_parity(y.reshape(-1, 2 * s.d)[torch.from_numpy(rows).cuda()], ref, "bf16")
+
+
+def lam_vectors_for(lam: float, layer: int, d: int) -> dict:
+    """Lambda vectors giving the scalar lam exactly in real arithmetic:
+    lq1 = lk1 = 0 so exp(lq1 . lk1) = 1, and lq2 . lk2 = ln(1 + lam_init - lam)."""
+    lam_init = oracle.lambda_init(layer)
+    c = 1.0 + lam_init - lam
+    assert c > 0
+    z = torch.zeros(d)
+    lq2 = torch.zeros(d)
+    lq2[0] = math.log(c)
+    lk2 = torch.zeros(d)
+    lk2[0] = 1.0
+    return {"lam_q1": z.clone(), "lam_k1": z.clone(), "lam_q2": lq2, "lam_k2": lk2}
+
+
+@pytest.mark.parametrize("lam", [-0.5, 0.95, 1.5])
+@pytest.mark.parametrize("d", [64, 128])
+def test_v1_lambda_outside_the_usual_range(lam, d):
+    layer = 12
+    x = inputs.make_v1(inputs.V1Shape(2, 700, 2, d, layer, "bf16"), seed=17)
+    x.update(lam_vectors_for(lam, layer, d))
+    assert abs(oracle.lambda_full(x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"], layer) - lam) < 1e-6
+    y = run_v1(to_dev(x), layer)
+    assert_parity(y, oracle_v1(x, layer), "bf16")
+
+
+@pytest.mark.parametrize("lam", [-0.5, 0.95, 1.5])
+@pytest.mark.parametrize("d", [64, 128])
+def test_v1_identical_branches(lam, d):
+    """q1 = q2 and k1 = k2: a1 = a2 = A and the output is (1 - lam_init)
+    RMSNorm((1 - lam) A), here with planted levels so that the rescale runs
+    on both (identical) branches."""
+    layer = 12
+    x = inputs.make_v1(inputs.V1Shape(1, 1024, 2, d, layer, "bf16"), seed=23)
+    rc.plant_v1(x, d)
+    x["q"][:, :, 1::2] = x["q"][:, :, 0::2]
+    x["k"][:, :, 1::2] = x["k"][:, :, 0::2]
+    x.update(lam_vectors_for(lam, layer, d))
+    y = run_v1(to_dev(x), layer)
+    ref = oracle_v1(x, layer)
+    assert_parity(y, ref, "bf16")
+
+
+# ------------------------------------------------------------------- DIFF V2
+
+@pytest.mark.parametrize("B,T,Hq,Hkv,D", [(1, 1024, 8, 2, 128), (2, 1100, 4, 1, 128), (1, 1200, 4, 2, 64)])
+def test_v2_lazy_rescale(B, T, Hq, Hkv, D):
+    x = inputs.make_v2(inputs.V2Shape(B, T, Hq, Hkv, D, "bf16"), seed=T + Hq)
+    rc.plant_v2(x, D)
+    G = Hq // Hkv
+    assert_branches(*rc.v2_decisions(x, B - 1, Hq - 1, G))
+    xd = to_dev(x)
+    y = binding().v2_fwd(xd["q"], xd["k"], xd["v"], xd["lam"])
+    assert_parity(y, oracle.v2_fwd(x["q"], x["k"], x["v"], x["lam"]), "bf16")
+
+
+def test_v2_gate_logits_in_both_tails():
+    """Logits of +-30, +-200 and +-1e4 (exp overflows fp32: sigmoid exactly 0
+    or 1) mixed with N(0, 1) ones, on planted levels."""
+    s = inputs.V2Shape(2, 1024, 8, 2, 128, "bf16")
+    x = inputs.make_v2(s, seed=31)
+    rc.plant_v2(x, s.D)
+    g = torch.Generator().manual_seed(31)
+    pick = torch.randint(0, 7, x["lam"].shape, generator=g)
+    table = torch.tensor([-1e4, -200.0, -30.0, 0.0, 30.0, 200.0, 1e4])
+    x["lam"] = torch.where(pick == 3, x["lam"], table[pick])
+    xd = to_dev(x)
+    y = binding().v2_fwd(xd["q"], xd["k"], xd["v"], xd["lam"])
+    assert_parity(y, oracle.v2_fwd(x["q"], x["k"], x["v"], x["lam"]), "bf16")
+
+
+# ------------------------------------------------------- Paired Head Attention
+
+@pytest.mark.parametrize("B,T,H,D", [(1, 1024, 4, 128), (2, 700, 2, 64)])
+def test_paired_lazy_rescale(B, T, H, D):
+    x = inputs.make_paired(inputs.PairedShape(B, T, H, D, "bf16"), seed=T)
+    rc.plant_paired(x, D)
+    assert_branches(*rc.paired_decisions(x, B - 1, H - 1))
+    xd = to_dev(x)
+    y = binding().paired_fwd(xd["q"], xd["k"], xd["v"])
+    assert_parity(y, oracle.paired_fwd(x["q"], x["k"], x["v"]), "bf16")
+
+
+# ------------------------------------------------------- training forward + backward
+
+def test_v1_train_lazy_rescale():
+    """The training forward (the same kernel with the training epilogue) on
+    planted levels: its output against the oracle's forward, and its saved
+    log-sum-exp through the gradients it feeds (every P of the backward is
+    rebuilt from it) against the oracle's gradients."""
+    from test_gpu_backward import check_grad, check_lambda_vectors
+    B, T, H, d, layer = 1, 1024, 2, 64, 12
+    x = inputs.make_v1(inputs.V1Shape(B, T, H, d, layer, "bf16"), seed=41)
+    rc.plant_v1(x, d)
+    assert_branches(*rc.v1_decisions(x, 0, 1, 1))
+    dout = inputs.make_grad_out((B, T, H, 2 * d), "bf16", seed=41)
+    xd, dd = to_dev(x), dout.cuda()
+    bd = binding()
+    a = (xd["q1"], xd["q2"], xd["k1"], xd["k2"], xd["v"], xd["lam_q1"], xd["lam_k1"], xd["lam_q2"], xd["lam_k2"],
+         layer)
+    out, saved = bd.v1_fwd_train(*a)
+    assert_parity(out, oracle_v1(x, layer), "bf16")
+    g = bd.v1_bwd(*a, dd, saved)
+    assert bd.device_error() == 0
+    ref = oracle.v1_bwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"],
+                        x["lam_k2"], layer, dout)
+    rep = {}
+    for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
+        check_grad(n, g[n], ref[n], rep)
+    check_lambda_vectors(g, ref, x, rep)
+    print("V1 train rescale", {k: f"{e:.2e}/{r:.2e}" for k, (e, r) in rep.items()})
+
+
+def test_v2_train_lazy_rescale():
+    from test_gpu_backward import check_grad
+    s = inputs.V2Shape(1, 1024, 4, 2, 128, "bf16")
+    x = inputs.make_v2(s, seed=43)
+    rc.plant_v2(x, s.D)
+    assert_branches(*rc.v2_decisions(x, 0, 1, 2))
+    dout = inputs.make_grad_out((s.B, s.T, s.Hq // 2, s.D), "bf16", seed=43)
+    xd, dd = to_dev(x), dout.cuda()
+    bd = binding()
+    out, saved = bd.v2_fwd_train(xd["q"], xd["k"], xd["v"], xd["lam"])
+    assert_parity(out, oracle.v2_fwd(x["q"], x["k"], x["v"], x["lam"]), "bf16")
+    g = bd.v2_bwd(xd["q"], xd["k"], xd["v"], xd["lam"], dd, saved)
+    assert bd.device_error() == 0
+    ref = oracle.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout)
+    rep = {}
+    for n in ("dq", "dk", "dv", "dlam"):
+        check_grad(n, g[n], ref[n], rep)
+    print("V2 train rescale", {k: f"{e:.2e}/{r:.2e}" for k, (e, r) in rep.items()})
