@@ -582,7 +582,7 @@ def oracle_per_config(dev, seed: int) -> dict:
     xb = {k: xd[k][0:1].double().cpu().numpy() for k in ("q", "k", "v", "lam")}
     del xd
     P = s.Hq // 2
-    rows = rng.choice(s.T * P, size=2048, replace=False)
+    rows = rng.choice(s.T * P, size=32768, replace=False)
     t0 = time.perf_counter()
     oracle.v2_fwd(xb["q"], xb["k"], xb["v"], xb["lam"], rows=rows)
     dt = time.perf_counter() - t0
@@ -591,7 +591,7 @@ def oracle_per_config(dev, seed: int) -> dict:
     res["v2_bf16_B8_T4096_Hq32_Hkv8_D128"] = {
         "s": round(dt, 3), "covered": frac, "cores": cores,
         "TFLOP/s": round(pairs * 4 * s.D / dt / 1e12, 5),
-        "sample": "2048 random output rows (t, pair) of batch entry 0"}
+        "sample": "32768 random output rows (t, pair) of batch entry 0"}
     s = inputs.WORKLOADS["v1_bf16_B1_T32768_H12_d128"]
     xd = inputs.make_v1(s, seed=seed, device=dev)
     xb = {k: (xd[k][:, :, 0:1].double().cpu().numpy() if k in ("q1", "q2", "k1", "k2", "v")
@@ -599,7 +599,7 @@ def oracle_per_config(dev, seed: int) -> dict:
                                                            "lam_q2", "lam_k2")}
     del xd
     torch.cuda.empty_cache()
-    rows = rng.choice(s.T, size=256, replace=False)
+    rows = rng.choice(s.T, size=4096, replace=False)
     t0 = time.perf_counter()
     oracle.v1_fwd(xb["q1"], xb["q2"], xb["k1"], xb["k2"], xb["v"], xb["lam_q1"], xb["lam_k1"], xb["lam_q2"],
                   xb["lam_k2"], s.layer_index, rows=rows)
@@ -609,7 +609,7 @@ def oracle_per_config(dev, seed: int) -> dict:
     res["v1_bf16_B1_T32768_H12_d128"] = {
         "s": round(dt, 3), "covered": frac, "cores": cores,
         "TFLOP/s": round(pairs * 12 * s.d / dt / 1e12, 5),
-        "sample": "256 random rows t of diff head 0"}
+        "sample": "4096 random rows t of diff head 0"}
     return res
 
 

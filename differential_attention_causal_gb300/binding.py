@@ -70,7 +70,8 @@ def lib() -> ctypes.CDLL:
                                              + [i32, vp])
             sz = ctypes.c_size_t
             for n, k in (("diffattn_v1_train_saved_size", 5), ("diffattn_v1_bwd_workspace_size", 5),
-                         ("diffattn_v2_train_saved_size", 6), ("diffattn_v2_bwd_workspace_size", 6)):
+                         ("diffattn_v2_train_saved_size", 6), ("diffattn_v2_bwd_workspace_size", 6),
+                         ("diffattn_v1_train_saved_lse_offset", 5), ("diffattn_v2_train_saved_lse_offset", 6)):
                 getattr(L, n).restype = sz
                 getattr(L, n).argtypes = [i32] * k
             L.diffattn_v1_fwd_train.restype = i32
@@ -447,6 +448,25 @@ def v1_fwd_train(q1, q2, k1, k2, v, lam_q1, lam_k1, lam_q2, lam_k2, layer_index:
                                      B, T, H, d, int(layer_index), *strides, _dtype_code(q1), _stream(stream))
     _check("diffattn_v1_fwd_train", rc)
     return out, saved
+
+
+def saved_lse(saved: torch.Tensor, B: int, T: int, H: int, d: int, dtype: torch.dtype,
+              v2: bool = False, Hkv: int = 1) -> torch.Tensor:
+    """View of the (2, B, H, T) fp32 row log-sum-exp inside a training
+    forward's `saved` (log2 units for bf16, natural for fp32).  V1: H diff
+    heads, d the q/k head dim; V2: H = Hq query heads, Hkv kv heads, d = D,
+    and the view is (2, B, Hq/2, T)."""
+    code = DA_BF16 if dtype == torch.bfloat16 else DA_F32
+    if v2:
+        off = int(lib().diffattn_v2_train_saved_lse_offset(B, T, H, Hkv, d, code))
+        rows = H // 2
+    else:
+        off = int(lib().diffattn_v1_train_saved_lse_offset(B, T, H, d, code))
+        rows = H
+    if off == 0:
+        raise ValueError("unsupported sizes")
+    n = 2 * B * rows * T
+    return saved[off:off + 4 * n].view(torch.float32).view(2, B, rows, T)
 
 
 def v1_bwd(q1, q2, k1, k2, v, lam_q1, lam_k1, lam_q2, lam_k2, layer_index: int, dout, saved,

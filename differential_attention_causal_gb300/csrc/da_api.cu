@@ -637,6 +637,14 @@ size_t diffattn_v2_train_saved_size(int B, int T, int Hq, int Hkv, int D, da_dty
     if (Hq < 2 || Hkv < 1 || !shape_ok_bytes(B, T, Hq / 2, D) || !train_supported(D, true, dtype)) return 0;
     return SavedLayout(B, T, Hq / 2, D, saved_esize(true, dtype)).total;
 }
+size_t diffattn_v1_train_saved_lse_offset(int B, int T, int H, int d, da_dtype dtype) {
+    if (!shape_ok_bytes(B, T, H, 2 * d) || !train_supported(d, false, dtype)) return 0;
+    return SavedLayout(B, T, H, 2 * d, saved_esize(false, dtype)).off_lse;
+}
+size_t diffattn_v2_train_saved_lse_offset(int B, int T, int Hq, int Hkv, int D, da_dtype dtype) {
+    if (Hq < 2 || Hkv < 1 || !shape_ok_bytes(B, T, Hq / 2, D) || !train_supported(D, true, dtype)) return 0;
+    return SavedLayout(B, T, Hq / 2, D, saved_esize(true, dtype)).off_lse;
+}
 size_t diffattn_v1_bwd_workspace_size(int B, int T, int H, int d, da_dtype dtype) {
     if (!shape_ok_bytes(B, T, H, 2 * d) || !train_supported(d, false, dtype)) return 0;
     return BwdWsLayout(B, T, H, 2 * d, true, dtype == DA_F32 ? 4 : 2).total;

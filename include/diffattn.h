@@ -285,6 +285,15 @@ size_t diffattn_v1_bwd_workspace_size(int B, int T, int H, int d, da_dtype dtype
 size_t diffattn_v2_train_saved_size(int B, int T, int Hq, int Hkv, int D, da_dtype dtype);
 size_t diffattn_v2_bwd_workspace_size(int B, int T, int Hq, int Hkv, int D, da_dtype dtype);
 
+/* Byte offset inside `saved` of each branch's row log-sum-exp: fp32
+ * (2, B, H, T) for V1 (branch 1, then branch 2) and (2, B, Hq/2, T) for V2
+ * (the even heads, then the odd heads), lse = log sum_j exp(q . k_j / sqrt(d))
+ * over the causal keys j <= t, in log2 units (times log2(e)) for DA_BF16 and
+ * natural units for DA_F32.  Arguments as the size functions; 0 for
+ * unsupported sizes.  The rest of `saved` stays private. */
+size_t diffattn_v1_train_saved_lse_offset(int B, int T, int H, int d, da_dtype dtype);
+size_t diffattn_v2_train_saved_lse_offset(int B, int T, int Hq, int Hkv, int D, da_dtype dtype);
+
 /* DIFF V1 training forward: arguments, layouts and strides as
  * diffattn_v1_fwd, plus `saved`. */
 da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, const void *k2,

@@ -78,6 +78,8 @@ def _load():
             lib.oracle_v2_bwd.restype = ctypes.c_int
             lib.oracle_v2_bwd.argtypes = ([dp] * 5 + [ctypes.c_int] * 5 + [i64p, ctypes.c_int64] + [dp] * 4
                                           + [ctypes.c_int])
+            lib.oracle_lse.restype = None
+            lib.oracle_lse.argtypes = [dp, dp] + [ctypes.c_int] * 5 + [dp]
             lib.oracle_rope.restype = None
             lib.oracle_rope.argtypes = [dp] + [ctypes.c_int] * 4 + [ctypes.c_int64, ctypes.c_double, dp]
             lib.oracle_lambda_proj.restype = None
@@ -314,6 +316,22 @@ def v2_bwd(q, k, v, lam, dout, groups=None, nthreads: int | None = None) -> dict
     if rc:
         raise RuntimeError(f"oracle_v2_bwd failed ({rc})")
     return g
+
+
+def lse(q, k) -> np.ndarray:
+    """Row log-sum-exp (natural log) of the causal scaled scores: for q
+    (B, T, Hq, d) and k (B, T, Hk, d), out[b, h, t] = log sum_{j <= t}
+    exp(q[b,t,h] . k[b,j,h/(Hq/Hk)] / sqrt(d)) -- the normaliser of each
+    row's softmax in "Differential Transformer V2" (DiffAttnV1 / DiffAttnV2,
+    each flash_attn_func call) and "How best to implement a differential
+    transformer?" (the masked, 1/sqrt(d)-scaled scores).  Returns (B, Hq, T)."""
+    q, k = _f64(q), _f64(k)
+    B, T, Hq, d = q.shape
+    Hk = k.shape[2]
+    assert k.shape == (B, T, Hk, d) and Hq % Hk == 0
+    out = np.empty((B, Hq, T), dtype=np.float64)
+    _load().oracle_lse(_ptr(q), _ptr(k), B, T, Hq, Hk, d, _ptr(out))
+    return out
 
 
 def rope(x, pos0: int = 0, base: float = 10000.0) -> np.ndarray:

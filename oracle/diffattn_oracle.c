@@ -44,6 +44,41 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* ---- row log-sum-exp of the causal scores ---------------------------- */
+/* For every batch entry b, query head h and row t: the log-sum-exp (natural
+ * log) of the scaled scores that row's softmax normalises,
+ *   lse = log sum_{j <= t} exp(q_t . k_j / sqrt(d)),
+ * taken as max + log(sum exp(s - max)).  q (B, T, Hq, d), k (B, T, Hk, d)
+ * contiguous, query head h reads key head h / (Hq / Hk); out (B, Hq, T). */
+void oracle_lse(const double *q, const double *k, int B, int T, int Hq, int Hk,
+                int d, double *out)
+{
+    const double scale = 1.0 / sqrt((double)d);
+    const int G = Hq / Hk;
+    double *s = (double *)malloc(sizeof(double) * (size_t)T);
+    if (!s) return;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < Hq; ++h)
+            for (int t = 0; t < T; ++t) {
+                const double *qt = q + (((int64_t)b * T + t) * Hq + h) * d;
+                const int n = t + 1;   /* causal: keys 0 .. t */
+                double mx = -INFINITY;
+                for (int j = 0; j < n; ++j) {
+                    const double *kj = k + (((int64_t)b * T + j) * Hk + h / G) * d;
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c)
+                        acc += qt[c] * kj[c];
+                    s[j] = acc * scale;
+                    if (s[j] > mx) mx = s[j];
+                }
+                double sum = 0.0;
+                for (int j = 0; j < n; ++j)
+                    sum += exp(s[j] - mx);
+                out[((int64_t)b * Hq + h) * T + t] = mx + log(sum);
+            }
+    free(s);
+}
+
 /* ---- one causal softmax-attention row -------------------------------- */
 /* q: [dqk]; keys row j at k + j*k_stride; values row j at v + j*v_stride.
  * Attends keys 0..n-1.  Writes a[dv] = sum_j softmax(q.k_j * scale)_j v_j.

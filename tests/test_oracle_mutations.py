@@ -69,13 +69,17 @@ MUTANTS = {
     "paired: heads swapped in the interleave": ("const int64_t ts = s / 2, hs = 2 * i + (int)(s % 2);",
                                                 "const int64_t ts = s / 2, hs = 2 * i + 1 - (int)(s % 2);"),
     "paired: pairs (i, i + H/2)": ("const int i = h / 2, e = h % 2;", "const int i = h % (H / 2), e = h / (H / 2);"),
+    "lse: key head h % Hk": ("const double *kj = k + (((int64_t)b * T + j) * Hk + h / G) * d;",
+                             "const double *kj = k + (((int64_t)b * T + j) * Hk + h % Hk) * d;"),
+    "lse: one future key": ("const int n = t + 1;   /* causal: keys 0 .. t */",
+                            "const int n = t + 1 < T ? t + 2 : t + 1;"),
     "decode drops the last cache row": ("attend_row(qe, k, kv_row, v, kv_row, L, D, D, scale, scores, a1);",
                                         "attend_row(qe, k, kv_row, v, kv_row, L - 1, D, D, scale, scores, a1);"),
 }
 
 # mutants whose text stands at more than one site (every site is mutated:
 # the same mistake made in the prefill, decode and backward of one variant)
-SITES = {"scale 1/sqrt(2d) in V1": 3, "V1 combine sign": 2, "paired: heads swapped in the interleave": 2}
+SITES = {"scale 1/sqrt(2d) in V1": 4, "V1 combine sign": 2, "paired: heads swapped in the interleave": 2}
 
 # pin checks that take only the oracle (parametrised ones get one case each)
 CHECKS = [
@@ -106,6 +110,8 @@ CHECKS = [
     paired_pins.test_paired_page_visibility_example,
     paired_pins.test_paired_matches_library_sdpa_on_interleaved,
     paired_pins.test_paired_closed_forms,
+    pins.test_lse_closed_forms,
+    lambda o: pins.test_lse_matches_library_logsumexp(o, 8, 2),
 ]
 
 

@@ -408,3 +408,38 @@ def test_thread_count_does_not_change_result(oracle):
     a = oracle.v1_fwd(q1, q2, k1, k2, v, *lam, 2, nthreads=1)
     b = oracle.v1_fwd(q1, q2, k1, k2, v, *lam, 2, nthreads=7)
     np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------ row log-sum-exp
+
+def test_lse_closed_forms(oracle):
+    """q = 0: every visible score is 0, so row t normalises t + 1 ones and
+    lse = log(t + 1) exactly; T = 1: lse = q0 . k0 / sqrt(d)."""
+    rng = np.random.default_rng(40)
+    q = np.zeros((2, 9, 4, 8))
+    k = rng.standard_normal((2, 9, 2, 8))
+    got = oracle.lse(q, k)
+    want = np.broadcast_to(np.log(np.arange(1, 10, dtype=np.float64)), got.shape)
+    assert np.abs(got - want).max() < 1e-14
+    q1 = rng.standard_normal((1, 1, 2, 16))
+    k1 = rng.standard_normal((1, 1, 2, 16))
+    got = oracle.lse(q1, k1)[0, :, 0]
+    want = (q1[0, 0] * k1[0, 0]).sum(-1) / 4.0
+    assert np.abs(got - want).max() < 1e-14
+
+
+@pytest.mark.parametrize("Hq,Hk", [(3, 3), (8, 2)])
+def test_lse_matches_library_logsumexp(oracle, Hq, Hk):
+    """Against torch.logsumexp of the causally masked, 1/sqrt(d)-scaled fp64
+    scores, query head h reading key head h / (Hq / Hk)."""
+    rng = np.random.default_rng(41 + Hq)
+    B, T, d = 2, 23, 16
+    q = rng.standard_normal((B, T, Hq, d)) * 2.0
+    k = rng.standard_normal((B, T, Hk, d))
+    qt = torch.from_numpy(q).permute(0, 2, 1, 3)                          # (B, Hq, T, d)
+    kt = torch.from_numpy(k).permute(0, 2, 1, 3).repeat_interleave(Hq // Hk, dim=1)
+    s = qt @ kt.transpose(-1, -2) / np.sqrt(d)
+    mask = torch.ones(T, T, dtype=torch.bool).tril()
+    want = torch.logsumexp(s.masked_fill(~mask, float("-inf")), dim=-1).numpy()
+    got = oracle.lse(q, k)
+    assert np.abs(got - want).max() < 1e-12
