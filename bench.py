@@ -43,6 +43,7 @@ METRIC = "fused diff-attn fwd TFLOP/s (% bf16 TC peak); V2 decode HBM GB/s (% pe
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+SPINUP_S = 0.3
 
 # DRAM traffic per launch from an ncu capture, valid only for the kernel source
 # it was taken on (sha256 of the .cu file, first 16 hex digits).
@@ -222,15 +223,38 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
     out = torch.empty((s.B, s.T, s.H, 2 * s.d), dtype=torch.bfloat16, device=dev)
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def step():
+    def launch():
         binding.v1_fwd(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"],
                        x["lam_k2"], s.layer_index, out=out)
 
+    # The step is one C-ABI call; it is captured once into a CUDA graph and
+    # replayed, so that the host-side argument checks and tensor-map encoding
+    # of the call (tens of microseconds against a ~0.1 ms kernel) never leave
+    # the GPU idle inside a timed step.  The graph holds exactly the call's
+    # one kernel launch.
+    launch()                       # first call: per-device set-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launch()
+    launches_per_step = binding.last_launch_count()
+
+    def step():
+        graph.replay()
+
+    # Clock spin-up: an idle GPU starts below its maximum SM clock and takes a
+    # fraction of a second under load to reach it; the step runs untimed for
+    # SPINUP_S seconds before the W warm-up steps so that the K timed steps
+    # see steady clocks (recorded in config).
+    t_end = time.perf_counter() + SPINUP_S
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
     for _ in range(args.warmup):
         flush.add_(1)
         step()
     torch.cuda.synchronize()
-    launches_per_step = binding.last_launch_count()
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     if world > 1:
@@ -289,6 +313,8 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
         "config": {"workload": HEADLINE, "B": s.B, "T": s.T, "H": s.H, "d": s.d, "dv": 2 * s.d,
                    "layer_index": s.layer_index, "causal": True,
                    "l2": "256 MiB buffer written between timed steps (flush)",
+                   "spinup": f"the step run untimed for {SPINUP_S} s before the warm-up steps (clock ramp)",
+                   "launch": "the C-ABI call captured once into a CUDA graph (one kernel) and replayed per step",
                    "flop_count": "12d per causal pair (two QK, two PV)"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

@@ -90,6 +90,10 @@ struct PreCfg {
     // lambda, idle) give up registers, the two softmax warpgroups take them
     static constexpr uint32_t REGS_LOW = 88, REGS_HIGH = 192;
     static constexpr bool REG_SPLIT = !V2;                    // measured: helps V1, costs V2
+    // V1: the row max of keys 0-63 is taken while keys 64-127 are still being
+    // read out of TMEM (off the diagonal); measured on GB300: V1 d = 64 1-2 %
+    // faster, V2 D = 128 1 % slower, so V1 only
+    static constexpr bool LD_SPLIT = !V2;
     // one MMA-issuing thread per branch (warp 1: S1, O1; warp 2: S2, O2) instead
     // of one for both; measured on GB300 at the V1 d = 64 / V2 D = 128 prefill
     // shapes: 13 % / 25 % slower, so off
@@ -469,16 +473,39 @@ __global__ void __launch_bounds__(384, 1)
                 uint32_t s[C::BN];
                 tmem_ld32(tS + 0, s);
                 tmem_ld32(tS + 32, s + 32);
+                if (C::LD_SPLIT) tmem_wait_ld();
                 tmem_ld32(tS + 64, s + 64);
                 tmem_ld32(tS + 96, s + 96);
-                tmem_wait_ld();
-                if (PAIRED ? j >= 2 * qt : j == qt) {   // diagonal tile(s): keys past this row are masked
-                    const int lim = PAIRED ? 2 * row + br - C::BN * (j - 2 * qt) : row;   // last visible column
+                const bool diag = PAIRED ? j >= 2 * qt : j == qt;
+                float rmax;
+                if (!C::LD_SPLIT || diag) {
+                    tmem_wait_ld();
+                    if (diag) {   // diagonal tile(s): keys past this row are masked
+                        const int lim = PAIRED ? 2 * row + br - C::BN * (j - 2 * qt) : row;   // last visible column
 #pragma unroll
-                    for (int c = 0; c < C::BN; ++c)
-                        if (c > lim) s[c] = 0xff800000u;   // -inf
+                        for (int c = 0; c < C::BN; ++c)
+                            if (c > lim) s[c] = 0xff800000u;   // -inf
+                    }
+                    rmax = row_max128(s);
+                } else {
+                    // max of keys 0-63 while keys 64-127 are still coming out of TMEM
+                    float a[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) a[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
+#pragma unroll
+                    for (int k2 = 8; k2 < 64; k2 += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            a[i] = fmax3(a[i], __uint_as_float(s[k2 + 2 * i]), __uint_as_float(s[k2 + 2 * i + 1]));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k2 = 64; k2 < 128; k2 += 8)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            a[i] = fmax3(a[i], __uint_as_float(s[k2 + 2 * i]), __uint_as_float(s[k2 + 2 * i + 1]));
+                    rmax = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
                 }
-                const float m_new = fmaxf(m_ref, row_max128(s) * sl2);
+                const float m_new = fmaxf(m_ref, rmax * sl2);
                 float alpha = 1.f;
                 const bool resc = m_new > m_ref + 8.f;
                 if (resc) {
