@@ -485,6 +485,28 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                           "flop_count": "28d per causal pair (two attention backwards)",
                           "fwd_train_ms": round(ms_ft, 4), "launches": 4, "peak_kind": peak_kind}
     del x, dout, saved, ws
+    # backward of the long-context DIFF V1 workload (d = 128, dv = 256: split kernels)
+    s = inputs.WORKLOADS["v1_bf16_B1_T32768_H12_d128"]
+    x = inputs.make_v1(s, seed=args.seed, device=dev)
+    dout = inputs.make_grad_out((s.B, s.T, s.H, 2 * s.d), "bf16", seed=args.seed, device=dev)
+    a = (x["q1"], x["q2"], x["k1"], x["k2"], x["v"], x["lam_q1"], x["lam_k1"], x["lam_q2"], x["lam_k2"],
+         s.layer_index)
+    _, saved = binding.v1_fwd_train(*a)
+    ws = torch.empty(binding.lib().diffattn_v1_bwd_workspace_size(s.B, s.T, s.H, s.d, 1), dtype=torch.uint8,
+                     device=dev)
+    f = lambda: binding.v1_bwd(*a, dout, saved, workspace=ws)  # noqa: E731
+    for _ in range(2):
+        f()
+    ms = sum(t := time_steps(f, 3, flush)) / len(t)
+    ftr = lambda: binding.v1_fwd_train(*a)  # noqa: E731
+    ms_ft = sum(t := time_steps(ftr, 3, flush)) / len(t)
+    tf = v1_bwd_flops(s) / (ms * 1e-3) / 1e12
+    aux["v1_long_backward"] = {"workload": "v1_bf16_B1_T32768_H12_d128", "ms": round(ms, 3), "TFLOP/s": round(tf, 1),
+                               "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                               "flop_count": "28d per causal pair (two attention backwards)",
+                               "fwd_train_ms": round(ms_ft, 3), "launches": 5, "peak_kind": peak_kind}
+    del x, dout, saved, ws
+    torch.cuda.empty_cache()
     s = inputs.WORKLOADS["v2_bf16_B8_T4096_Hq32_Hkv8_D128"]
     x = inputs.make_v2(s, seed=args.seed, device=dev)
     dout = inputs.make_grad_out((s.B, s.T, s.Hq // 2, s.D), "bf16", seed=args.seed, device=dev)
@@ -692,6 +714,8 @@ CASES = {
     # backward of the headline V1 workload / a quarter of the V2 prefill workload (profiler-sized)
     "v1_bwd": ("v1_bwd", "v1_bf16_B4_T2048_H16_d64"),
     "v2_bwd_b2": ("v2_bwd", None),
+    # the long-context V1 backward (d = 128) on a quarter of its length, profiler-sized
+    "v1_long_bwd_t8k": ("v1_bwd", None),
     "prologue": ("prologue", "v2_bf16_B8_T4096_Hq32_Hkv8_D128"),
     "paired": ("paired", "paired_bf16_B8_T4096_H32_D128"),
     # the V1 decode and the ragged-length decode workloads with 4 / 8 of their
@@ -711,6 +735,8 @@ def run_case(name: str, launches: int):
         s = inputs.WORKLOADS[wl]
     elif kind == "v2_bwd":
         s = inputs.V2Shape(2, 4096, 32, 8, 128, "bf16")
+    elif kind == "v1_bwd":
+        s = inputs.V1Shape(1, 8192, 12, 128, 27, "bf16")
     elif kind == "paired":
         s = inputs.PairedShape(2, 4096, 32, 128, "bf16")
     elif kind == "v1_decode":

@@ -699,11 +699,14 @@ da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, 
     }
     PrefillMaps m;
     const uint64_t uT = static_cast<uint64_t>(T), uH = static_cast<uint64_t>(H), uB = static_cast<uint64_t>(B);
+    // d = 128: the two-pass kernel (its V map has the item-sized box)
+    const bool twopass = d == 128;
     if (!encode_map_4d(&m.q1, q1, d, uH, uT, uB, q_sh, q_st, q_sb, 128) ||
         !encode_map_4d(&m.q2, q2, d, uH, uT, uB, q_sh, q_st, q_sb, 128) ||
         !encode_map_4d(&m.k1, k1, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
         !encode_map_4d(&m.k2, k2, d, uH, uT, uB, k_sh, k_st, k_sb, 128) ||
-        !encode_map_4d(&m.v, v, 2 * d, uH, uT, uB, v_sh, v_st, v_sb, 128) ||
+        !encode_map_4d(&m.v, v, 2 * d, uH, uT, uB, v_sh, v_st, v_sb,
+                       twopass ? static_cast<uint32_t>(prefill_v1_twopass_v_rows(d)) : 128u) ||
         !encode_map_4d(&m.out, out, 2 * d, uH, uT, uB, o_sh, o_st, o_sb, 128))
         return DA_ERR_CUDA;
     PrefillParams p{};
@@ -719,8 +722,9 @@ da_status diffattn_v1_fwd_train(const void *q1, const void *q2, const void *k1, 
     p.sa1 = sv;
     p.sa2 = sv + sl.off_a2;
     p.slse = reinterpret_cast<float *>(sv + sl.off_lse);
-    const da_status st = cuda_status(launch_prefill_train(m, p, d, 2 * d, false, stream));
-    if (st == DA_OK) t_last_launches = 1;
+    const da_status st = cuda_status(twopass ? launch_prefill_v1_twopass_train(m, p, stream)
+                                             : launch_prefill_train(m, p, d, 2 * d, false, stream));
+    if (st == DA_OK) t_last_launches = twopass ? 2 : 1;
     return st;
 }
 
@@ -896,7 +900,7 @@ da_status diffattn_v1_bwd(const void *q1, const void *q2, const void *k1, const 
     p.scale_log2 = 1.4426950408889634f * p.scale;
     p.err = err;
     const da_status st = cuda_status(launch_backward(m, p, pp, d, DV, false, stream));
-    if (st == DA_OK) t_last_launches = 4;
+    if (st == DA_OK) t_last_launches = d == 128 ? 5 : 4;
     return st;
 }
 

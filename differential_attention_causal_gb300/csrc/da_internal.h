@@ -82,6 +82,7 @@ struct PrefillParams {
     // P = 2^(s * scale_log2 - lse_b) (fp32, (2, B, H, T))
     void *sa1, *sa2;
     float *slse;
+    int train_run;                 // DIFF V1 two-pass training forward: 1 = x and lse, 2 = a2
 };
 struct PrefillMaps {
     CUtensorMap q1, q2, k1, k2, v;
@@ -109,6 +110,10 @@ bool prefill_supported(int dqk, int dv, bool v2);
 // dqk in {64, 128}, dv = 2 dqk.  The V tensor map's box has
 // prefill_v1_twopass_v_rows(dqk) rows (the Q/K maps 128).
 cudaError_t launch_prefill_v1_twopass(const PrefillMaps &m, const PrefillParams &p, int dqk, cudaStream_t s);
+// Its training forward at dqk = 128 (two launches): the output, x = a1 - lam a2
+// (p.sa1, fp32), a2 (p.sa2, fp32) and each branch's log-sum-exp (p.slse, log2
+// units), the layout the V1 backward reads.
+cudaError_t launch_prefill_v1_twopass_train(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s);
 int prefill_v1_twopass_v_rows(int dqk);
 
 // -------------------------------------------------------------- backward

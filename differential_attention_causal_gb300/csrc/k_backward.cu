@@ -41,13 +41,22 @@
 namespace da {
 namespace {
 
-template <int DQK, int DV, bool V2>
+// MODE 0: both branches in one kernel (dq: dQ1 and dQ2; dkdv: dK1, dK2 and dV).
+// MODE 1: one branch per CTA, the branch = work index & 1 (dq: dQ_b; dkdv: dK_b).
+// MODE 2: dkdv kernel computing dV only.
+// DIFF V1 at d = 128 (dv = 256) runs MODE 1 dq, MODE 1 dkdv and MODE 2 dkdv:
+// with both branches, dK1 | dK2 | dV (512 fp32 columns) next to S1 | S2 | dP
+// would not fit in TMEM, nor the resident tiles in shared memory.
+template <int DQK, int DV, bool V2, int MODE = 0>
 struct BwdCfg {
     static constexpr int BM = 128, BN = 64;
     static constexpr int QB = DQK / 64, VB = DV / 64;   // 64-column boxes
     static constexpr int RBOX = 128 * 128;              // 128 rows x 64 bf16
     static constexpr int CBOX = 64 * 128;               // 64 rows x 64 bf16
     static constexpr int NK = V2 ? 1 : 2;               // distinct K tiles (V1: K1, K2)
+    static constexpr int NQ = MODE == 1 ? 1 : 2;        // Q tiles a CTA reads (both branches, or its own)
+    static constexpr int NKT = MODE == 1 ? 1 : NK;      // K tiles a CTA reads
+    static constexpr bool HAS_DP = MODE != 2;           // dP = G V^T is formed (and V read)
     static constexpr int COL_S1 = 0, COL_S2 = 64, COL_DP = 128, COL_ACC = 192;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t IDESC_S = idesc_bf16(128, 64, false);
@@ -64,15 +73,16 @@ struct BwdCfg {
     static constexpr bool TWO_ISSUERS = true;
     static constexpr int MIN_SMEM = 120 * 1024;   // one CTA per SM (each takes all of TMEM)
 
-    // ---- dq kernel: resident Q1, Q2, G (128 rows); ring of K1 (, K2), V (64 rows);
-    //      result tiles dS1, dS2 (128 x 64 bf16, the A operands of dQ += dS K)
-    static constexpr int DQ_STAGES = DQK == 64 ? 4 : 3;   // shared memory
+    // ---- dq kernel: resident Q1 (, Q2), G (128 rows); ring of K1 (, K2), V (64 rows);
+    //      result tiles dS1 (, dS2) (128 x 64 bf16, the A operands of dQ += dS K)
+    static constexpr int DQ_NRES = MODE == 1 ? 1 : 2;
+    static constexpr int DQ_STAGES = MODE == 1 ? 2 : (DQK == 64 ? 4 : 3);   // shared memory
     static constexpr int DQ_OFF_Q1 = 0;
     static constexpr int DQ_OFF_Q2 = QB * RBOX;
-    static constexpr int DQ_OFF_G = 2 * QB * RBOX;
+    static constexpr int DQ_OFF_G = NQ * QB * RBOX;
     static constexpr int DQ_OFF_RES = DQ_OFF_G + VB * RBOX;
-    static constexpr int DQ_OFF_RING = DQ_OFF_RES + 2 * RBOX;
-    static constexpr int DQ_STAGE = NK * QB * CBOX + VB * CBOX;
+    static constexpr int DQ_OFF_RING = DQ_OFF_RES + DQ_NRES * RBOX;
+    static constexpr int DQ_STAGE = NKT * QB * CBOX + VB * CBOX;
     static constexpr int DQ_OFF_BAR = DQ_OFF_RING + DQ_STAGES * DQ_STAGE;
     // res, full[S], empty[S], s, sfree, rready, rfree, done, drain, drain of the score issuer
     static constexpr int DQ_NBAR = 1 + 2 * DQ_STAGES + 7;
@@ -81,16 +91,18 @@ struct BwdCfg {
     static constexpr int DQ_SMEM = DQ_SMEM_RAW > MIN_SMEM ? DQ_SMEM_RAW : MIN_SMEM;
     static constexpr int COL_DQ1 = COL_ACC, COL_DQ2 = COL_ACC + DQK;
 
-    // ---- dkdv kernel: resident K1 (, K2), V (128 rows); ring of Q1, Q2, G (64 rows) + row
-    //      vectors; result tiles P~^T, dS1^T, dS2^T (128 x 64 bf16, the A operands of dV, dK)
-    static constexpr int KV_STAGES = (V2 && DQK == 128) ? 2 : 3;   // shared memory
+    // ---- dkdv kernel: resident K1 (, K2) (, V) (128 rows); ring of Q1 (, Q2), G (64 rows)
+    //      + row vectors; result tiles (P~^T,) dS1^T (, dS2^T) or P~^T alone (128 x 64
+    //      bf16, the A operands of dV, dK)
+    static constexpr int KV_NRES = MODE == 0 ? 3 : 1;
+    static constexpr int KV_STAGES = MODE != 0 ? 2 : ((V2 && DQK == 128) ? 2 : 3);   // shared memory
     static constexpr int KV_OFF_K1 = 0;
-    static constexpr int KV_OFF_K2 = QB * RBOX;                    // V1 only
-    static constexpr int KV_OFF_V = NK * QB * RBOX;
-    static constexpr int KV_OFF_RES = KV_OFF_V + VB * RBOX;
-    static constexpr int KV_OFF_RING = KV_OFF_RES + 3 * RBOX;
+    static constexpr int KV_OFF_K2 = QB * RBOX;                    // V1, MODE 0 / 2
+    static constexpr int KV_OFF_V = NKT * QB * RBOX;
+    static constexpr int KV_OFF_RES = KV_OFF_V + (HAS_DP ? VB * RBOX : 0);
+    static constexpr int KV_OFF_RING = KV_OFF_RES + KV_NRES * RBOX;
     static constexpr int KV_VEC = 5 * 64 * 4;                      // lse1, lse2, d1, d2, c
-    static constexpr int KV_STAGE_TMA = 2 * QB * CBOX + VB * CBOX;
+    static constexpr int KV_STAGE_TMA = NQ * QB * CBOX + VB * CBOX;
     static constexpr int KV_STAGE = KV_STAGE_TMA + 2048;           // vectors, padded to keep 1 KB alignment
     static constexpr int KV_OFF_BAR = KV_OFF_RING + KV_STAGES * KV_STAGE;
     static constexpr int KV_NBAR = 1 + 2 * KV_STAGES + 7;
@@ -99,10 +111,12 @@ struct BwdCfg {
     static constexpr int KV_SMEM = KV_SMEM_RAW > MIN_SMEM ? KV_SMEM_RAW : MIN_SMEM;
     static constexpr int COL_DK1 = COL_ACC;
     static constexpr int COL_DK2 = V2 ? COL_ACC : COL_ACC + DQK;   // V2: both branches hit one K
-    static constexpr int COL_DV = COL_ACC + NK * DQK;
+    static constexpr int COL_DV = MODE == 2 ? COL_ACC : COL_ACC + NK * DQK;
 
-    static_assert(COL_DQ2 + DQK <= 512 && COL_DV + DV <= 512, "TMEM budget");
-    static_assert(DQ_SMEM <= 232448 && KV_SMEM <= 232448, "shared memory budget");
+    static_assert(MODE == 0 || (!V2 && DQK == 128 && DV == 256), "split modes: V1 at d = 128");
+    static_assert((MODE == 1 ? COL_DQ1 + DQK : COL_DQ2 + DQK) <= 512, "TMEM budget (dq)");
+    static_assert((MODE == 1 ? COL_DK1 + DQK : COL_DV + DV) <= 512, "TMEM budget (dkdv)");
+    static_assert((MODE == 2 || DQ_SMEM <= 232448) && KV_SMEM <= 232448, "shared memory budget");
     static_assert(KV_VEC <= 2048, "vector area");
 };
 
@@ -144,12 +158,13 @@ __device__ __forceinline__ void store_row_part(uint8_t *tile, int row, int part,
 //   rows: load S(j), dP(j) -> sfree; compute dS; wait until dQ(j-1) has read
 //         the result tiles ("rfree"); write dS(j) -> rready.
 // So S(j+1) and dP(j+1) run on the tensor cores while the rows work on j.
-template <int DQK, int DV, bool V2>
-__global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
+template <int DQK, int DV, bool V2, int MODE = 0>
+__global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
     bwd_dq(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
            const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tk1,
            const __grid_constant__ CUtensorMap tk2, const __grid_constant__ CUtensorMap tv, const BwdParams p) {
-    using C = BwdCfg<DQK, DV, V2>;
+    using C = BwdCfg<DQK, DV, V2, MODE>;
+    static_assert(MODE != 2, "dq kernel: MODE 0 or 1");
     constexpr int ST = C::DQ_STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -157,10 +172,12 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
     uint8_t *smem = smem_raw + (sbase - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // tile w -> query tile (heaviest first), head / pair, batch
+    // tile w -> query tile (heaviest first), head / pair, batch; MODE 1: the two
+    // branches of a tile are neighbouring CTAs, branch = index & 1
     const int n_qt = (p.T + C::BM - 1) / C::BM;
     const int per_qt = p.H * p.B;
-    const int w = static_cast<int>(blockIdx.x);
+    const int w = static_cast<int>(blockIdx.x) >> (MODE == 1 ? 1 : 0);
+    const int brc = MODE == 1 ? static_cast<int>(blockIdx.x & 1u) : 0;   // this CTA's branch (MODE 1)
     const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
     const int h = rest % p.H, b = rest / p.H;
     const int n_kt = (p.T + C::BN - 1) / C::BN;
@@ -208,15 +225,20 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            prefetch_tmap(&tq1);
+            // MODE 1: only this branch's Q and K
+            const CUtensorMap *mq = (MODE == 1 && brc) ? &tq2 : &tq1;
+            const CUtensorMap *mk = (MODE == 1 && brc) ? &tk2 : &tk1;
+            prefetch_tmap(mq);
             prefetch_tmap(&tg);
-            prefetch_tmap(&tk1);
+            prefetch_tmap(mk);
             prefetch_tmap(&tv);
-            mbar_arrive_expect_tx(bar_res, 2 * C::QB * C::RBOX + C::VB * C::RBOX);
+            mbar_arrive_expect_tx(bar_res, C::NQ * C::QB * C::RBOX + C::VB * C::RBOX);
 #pragma unroll
             for (int c = 0; c < C::QB; ++c) {
-                tma_load_4d(sbase + C::DQ_OFF_Q1 + c * C::RBOX, &tq1, bar_res, 64 * c, hq1, qt * C::BM, b);
-                tma_load_4d(sbase + C::DQ_OFF_Q2 + c * C::RBOX, &tq2, bar_res, 64 * c, hq2, qt * C::BM, b);
+                tma_load_4d(sbase + C::DQ_OFF_Q1 + c * C::RBOX, mq, bar_res, 64 * c, (MODE == 1 && brc) ? hq2 : hq1,
+                            qt * C::BM, b);
+                if (MODE == 0)
+                    tma_load_4d(sbase + C::DQ_OFF_Q2 + c * C::RBOX, &tq2, bar_res, 64 * c, hq2, qt * C::BM, b);
             }
 #pragma unroll
             for (int c = 0; c < C::VB; ++c)
@@ -230,13 +252,13 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                 mbar_arrive_expect_tx(bar_full + 8 * st, C::DQ_STAGE);
 #pragma unroll
                 for (int c = 0; c < C::QB; ++c) {
-                    tma_load_4d(dst + c * C::CBOX, &tk1, bar_full + 8 * st, 64 * c, hk, j * C::BN, b);
-                    if (!V2)
+                    tma_load_4d(dst + c * C::CBOX, mk, bar_full + 8 * st, 64 * c, hk, j * C::BN, b);
+                    if (!V2 && MODE == 0)
                         tma_load_4d(dst + (C::QB + c) * C::CBOX, &tk2, bar_full + 8 * st, 64 * c, hk, j * C::BN, b);
                 }
 #pragma unroll
                 for (int c = 0; c < C::VB; ++c)
-                    tma_load_4d(dst + (C::NK * C::QB + c) * C::CBOX, &tv, bar_full + 8 * st, 64 * c, hk, j * C::BN,
+                    tma_load_4d(dst + (C::NKT * C::QB + c) * C::CBOX, &tv, bar_full + 8 * st, 64 * c, hk, j * C::BN,
                                 b);
             }
             // leave no copy in flight
@@ -252,7 +274,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
             auto k1_at = [&](int j) { return sbase + C::DQ_OFF_RING + (j % ST) * C::DQ_STAGE; };
             // dQ_b += dS_b K_b for sub-tile jj: A = dS_b (shared, K-major), B = K_b tile MN-major
             auto acc = [&](int jj) {
-                const uint32_t sK1 = k1_at(jj), sK2 = V2 ? sK1 : sK1 + C::QB * C::CBOX;
+                const uint32_t sK1 = k1_at(jj), sK2 = (V2 || MODE == 1) ? sK1 : sK1 + C::QB * C::CBOX;
                 const uint64_t a1 = sdesc_sw128(sR1, 16, 1024), a2 = sdesc_sw128(sR2, 16, 1024);
                 const uint64_t k1 = sdesc_sw128(sK1, C::CBOX, 1024), k2 = sdesc_sw128(sK2, C::CBOX, 1024);
 #pragma unroll
@@ -260,7 +282,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                     const uint32_t oa = (ks * 32) >> 4, ob = (ks * 2048) >> 4;
                     const uint32_t first = (jj > 0 || ks > 0) ? 1u : 0u;
                     mma_ss(tmem + C::COL_DQ1, a1 + oa, k1 + ob, C::IDESC_QK, first);
-                    mma_ss(tmem + C::COL_DQ2, a2 + oa, k2 + ob, C::IDESC_QK, first);
+                    if (MODE == 0) mma_ss(tmem + C::COL_DQ2, a2 + oa, k2 + ob, C::IDESC_QK, first);
                 }
                 mma_commit(bar_empty + 8 * (jj % ST));   // K, V of jj no longer needed
                 mma_commit(bar_rfree);                    // result tiles read
@@ -268,8 +290,8 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
             // S_b = Q_b K_b^T (N = 64 keys), dP = G V^T for sub-tile j
             auto scores = [&](int j) {
                 const uint32_t sK1 = k1_at(j);
-                const uint32_t sK2 = V2 ? sK1 : sK1 + C::QB * C::CBOX;
-                const uint32_t sV = sK1 + C::NK * C::QB * C::CBOX;
+                const uint32_t sK2 = (V2 || MODE == 1) ? sK1 : sK1 + C::QB * C::CBOX;
+                const uint32_t sV = sK1 + C::NKT * C::QB * C::CBOX;
                 const uint64_t a1 = sdesc_sw128(sQ1, 16, 1024), a2 = sdesc_sw128(sQ2, 16, 1024);
                 const uint64_t b1 = sdesc_sw128(sK1, 16, 1024), b2 = sdesc_sw128(sK2, 16, 1024);
 #pragma unroll
@@ -277,7 +299,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                     const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
                     const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
                     mma_ss(tmem + C::COL_S1, a1 + oa, b1 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
-                    mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    if (MODE == 0) mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
                 }
                 const uint64_t ag = sdesc_sw128(sG, 16, 1024), bv = sdesc_sw128(sV, 16, 1024);
 #pragma unroll
@@ -351,9 +373,13 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
         const bool live = t < p.T;
         const int64_t vi = (static_cast<int64_t>(b) * p.H + h) * p.T + t;
         const int64_t vstride = static_cast<int64_t>(p.B) * p.H * p.T;
-        const float lse1 = live ? p.lse[vi] : 0.f, lse2 = live ? p.lse[vstride + vi] : 0.f;
-        const float d1 = live ? p.dd[vi] : 0.f, d2 = live ? p.dd[vstride + vi] : 0.f;
+        // MODE 1: branch 2's values sit in the first pair (lse1, d1): one formula below
+        const int64_t v1i = vi + (MODE == 1 && brc ? vstride : 0);
+        const float lse1 = live ? p.lse[v1i] : 0.f, lse2 = live && MODE == 0 ? p.lse[vstride + vi] : 0.f;
+        const float d1 = live ? p.dd[v1i] : 0.f, d2 = live && MODE == 0 ? p.dd[vstride + vi] : 0.f;
         const float cc = live ? p.cv[vi] : 0.f;
+        // dS_b = P_b (cb dP - D_b): cb = 1 for branch 1, c for branch 2
+        const float cb1 = (MODE == 1 && brc) ? cc : 1.f;
         const float sl2 = p.scale_log2;
         uint8_t *res1 = smem + C::DQ_OFF_RES, *res2 = res1 + C::RBOX;
         bool ok = true;
@@ -363,7 +389,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
             if (ok) {
                 tc_fence_after();
                 tmem_ld_cols<RC>(tmem + lane_off + C::COL_S1 + RC * wg, s1);
-                tmem_ld_cols<RC>(tmem + lane_off + C::COL_S2 + RC * wg, s2);
+                if (MODE == 0) tmem_ld_cols<RC>(tmem + lane_off + C::COL_S2 + RC * wg, s2);
                 tmem_ld_cols<RC>(tmem + lane_off + C::COL_DP + RC * wg, dp);
                 tmem_wait_ld();
             }
@@ -380,25 +406,37 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                     const float2 sc2 = make_float2(sl2, sl2), cc2 = make_float2(cc, cc);
                     const float2 nl1 = make_float2(-lse1, -lse1), nl2 = make_float2(-lse2, -lse2);
                     const float2 nd1 = make_float2(-d1, -d1), nd2 = make_float2(-d2, -d2);
+                    const float2 cb2 = make_float2(cb1, cb1);
 #pragma unroll
                     for (int c = 0; c < RC; c += 2) {
                         const float2 dpv = make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1]));
                         const float2 x1 =
                             __ffma2_rn(make_float2(__uint_as_float(s1[c]), __uint_as_float(s1[c + 1])), sc2, nl1);
-                        const float2 x2 =
-                            __ffma2_rn(make_float2(__uint_as_float(s2[c]), __uint_as_float(s2[c + 1])), sc2, nl2);
-                        float2 p1 = make_float2(ex2(x1.x), ex2(x1.y)), p2 = make_float2(ex2(x2.x), ex2(x2.y));
+                        float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
                         if (decltype(masked)::value) {
                             const bool v0 = live && key0 + c <= t, v1 = live && key0 + c + 1 <= t;
                             p1 = make_float2(v0 ? p1.x : 0.f, v1 ? p1.y : 0.f);
-                            p2 = make_float2(v0 ? p2.x : 0.f, v1 ? p2.y : 0.f);
                         }
-                        const float2 r1 = __fmul2_rn(p1, __fadd2_rn(dpv, nd1));
-                        const float2 r2 = __fmul2_rn(p2, __ffma2_rn(cc2, dpv, nd2));
-                        s1[c] = __float_as_uint(r1.x);
-                        s1[c + 1] = __float_as_uint(r1.y);
-                        s2[c] = __float_as_uint(r2.x);
-                        s2[c + 1] = __float_as_uint(r2.y);
+                        if constexpr (MODE == 1) {
+                            // one branch: dS = P (cb dP - D)
+                            const float2 r1 = __fmul2_rn(p1, __ffma2_rn(cb2, dpv, nd1));
+                            s1[c] = __float_as_uint(r1.x);
+                            s1[c + 1] = __float_as_uint(r1.y);
+                        } else {
+                            const float2 x2 =
+                                __ffma2_rn(make_float2(__uint_as_float(s2[c]), __uint_as_float(s2[c + 1])), sc2, nl2);
+                            float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+                            if (decltype(masked)::value) {
+                                const bool v0 = live && key0 + c <= t, v1 = live && key0 + c + 1 <= t;
+                                p2 = make_float2(v0 ? p2.x : 0.f, v1 ? p2.y : 0.f);
+                            }
+                            const float2 r1 = __fmul2_rn(p1, __fadd2_rn(dpv, nd1));
+                            const float2 r2 = __fmul2_rn(p2, __ffma2_rn(cc2, dpv, nd2));
+                            s1[c] = __float_as_uint(r1.x);
+                            s1[c + 1] = __float_as_uint(r1.y);
+                            s2[c] = __float_as_uint(r2.x);
+                            s2[c + 1] = __float_as_uint(r2.y);
+                        }
                     }
                 };
                 if (live && full)
@@ -412,27 +450,31 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                 uint32_t u[RC / 2];
                 pack_cols<RC>(s1, u);
                 store_row_part<RC>(res1, row, wg, u);
-                pack_cols<RC>(s2, u);
-                store_row_part<RC>(res2, row, wg, u);
+                if (MODE == 0) {
+                    pack_cols<RC>(s2, u);
+                    store_row_part<RC>(res2, row, wg, u);
+                }
                 fence_async_smem();   // generic-proxy writes -> tensor core reads
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_rready);
         }
-        // epilogue: dQ_b * scale -> bf16 rows (warpgroup wg takes branch wg % 2,
-        // channels DQK / (NRG / 2) * (wg / 2) onwards)
+        // epilogue: dQ_b * scale -> bf16 rows (MODE 0: warpgroup wg takes branch
+        // wg % 2, channels DQK / (NRG / 2) * (wg / 2) onwards; MODE 1: this CTA's
+        // branch, channels DQK / NRG * wg onwards, from the first accumulator)
         ok = warp_wait(bar_done, 0, p.err, ok);
         tc_fence_after();
         if (ok) {
-            constexpr int NCH = DQK / (C::NRG / 2);
-            const int br = wg & 1, ch0 = NCH * (wg >> 1);
+            constexpr int NCH = MODE == 1 ? DQK / C::NRG : DQK / (C::NRG / 2);
+            const int br = MODE == 1 ? brc : (wg & 1), ch0 = MODE == 1 ? NCH * wg : NCH * (wg >> 1);
+            const int acol = (MODE == 0 && br) ? C::COL_DQ2 : C::COL_DQ1;
             __nv_bfloat16 *dst = (br ? p.dq2 : p.dq1) + b * p.q_sb + static_cast<int64_t>(t) * p.q_st +
                                  static_cast<int64_t>(br ? hq2 : hq1) * p.q_sh + ch0;
 #pragma unroll
             for (int c0 = 0; c0 < NCH; c0 += 32) {
                 if (ch0 + c0 >= p.dqk_store) break;   // zero-padded channels
                 uint32_t a[32];
-                tmem_ld32(tmem + lane_off + (br ? C::COL_DQ2 : C::COL_DQ1) + ch0 + c0, a);
+                tmem_ld32(tmem + lane_off + acol + ch0 + c0, a);
                 tmem_wait_ld();
                 if (live) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
@@ -465,12 +507,12 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
 // group): S1^T, S2^T, dP^T of item i run while the rows turn item i-1 into
 // P~^T = P1^T + c P2^T, dS1^T, dS2^T; dV += P~^T G, dK_b += dS_b^T Q_b read
 // those from shared memory.
-template <int DQK, int DV, bool V2>
-__global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
+template <int DQK, int DV, bool V2, int MODE = 0>
+__global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
     bwd_dkdv(const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq1,
              const __grid_constant__ CUtensorMap tq2, const __grid_constant__ CUtensorMap tg, const BwdParams p) {
-    using C = BwdCfg<DQK, DV, V2>;
+    using C = BwdCfg<DQK, DV, V2, MODE>;
     constexpr int ST = C::KV_STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -482,7 +524,9 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
     const int n_kt = (p.T + C::BM - 1) / C::BM;
     const int nh = V2 ? p.Hkv : p.H;
     const int per_kt = nh * p.B;
-    const int w = static_cast<int>(blockIdx.x);
+    // MODE 1: the two branches of a key tile are neighbouring CTAs, branch = index & 1
+    const int w = static_cast<int>(blockIdx.x) >> (MODE == 1 ? 1 : 0);
+    const int brc = MODE == 1 ? static_cast<int>(blockIdx.x & 1u) : 0;
     const int kt = w / per_kt, rest = w % per_kt;
     const int hk = rest % nh, b = rest / nh;
     const int n_qs = (p.T + C::BN - 1) / C::BN;
@@ -533,20 +577,26 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
 
     if (warp == 0) {
         // ------------------------------------------ TMA + row vectors (32 lanes)
+        // MODE 1: only this branch's K and Q
+        const CUtensorMap *mk = (MODE == 1 && brc) ? &tk2 : &tk1;
+        const CUtensorMap *mq = (MODE == 1 && brc) ? &tq2 : &tq1;
         if (lane == 0) {
-            prefetch_tmap(&tk1);
+            prefetch_tmap(mk);
             prefetch_tmap(&tv);
-            prefetch_tmap(&tq1);
+            prefetch_tmap(mq);
             prefetch_tmap(&tg);
-            mbar_arrive_expect_tx(bar_res, C::NK * C::QB * C::RBOX + C::VB * C::RBOX);
+            mbar_arrive_expect_tx(bar_res, C::NKT * C::QB * C::RBOX + (C::HAS_DP ? C::VB * C::RBOX : 0));
 #pragma unroll
             for (int c = 0; c < C::QB; ++c) {
-                tma_load_4d(sbase + C::KV_OFF_K1 + c * C::RBOX, &tk1, bar_res, 64 * c, hk, kt * C::BM, b);
-                if (!V2) tma_load_4d(sbase + C::KV_OFF_K2 + c * C::RBOX, &tk2, bar_res, 64 * c, hk, kt * C::BM, b);
+                tma_load_4d(sbase + C::KV_OFF_K1 + c * C::RBOX, mk, bar_res, 64 * c, hk, kt * C::BM, b);
+                if (!V2 && MODE != 1)
+                    tma_load_4d(sbase + C::KV_OFF_K2 + c * C::RBOX, &tk2, bar_res, 64 * c, hk, kt * C::BM, b);
             }
+            if (C::HAS_DP) {
 #pragma unroll
-            for (int c = 0; c < C::VB; ++c)
-                tma_load_4d(sbase + C::KV_OFF_V + c * C::RBOX, &tv, bar_res, 64 * c, hk, kt * C::BM, b);
+                for (int c = 0; c < C::VB; ++c)
+                    tma_load_4d(sbase + C::KV_OFF_V + c * C::RBOX, &tv, bar_res, 64 * c, hk, kt * C::BM, b);
+            }
         }
         bool ok = true;
         int it = 0;
@@ -561,12 +611,15 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                 mbar_arrive_expect_tx(bar_full + 8 * st, C::KV_STAGE_TMA);
 #pragma unroll
                 for (int c = 0; c < C::QB; ++c) {
-                    tma_load_4d(dst + c * C::CBOX, &tq1, bar_full + 8 * st, 64 * c, hq1, qs * C::BN, b);
-                    tma_load_4d(dst + (C::QB + c) * C::CBOX, &tq2, bar_full + 8 * st, 64 * c, hq2, qs * C::BN, b);
+                    tma_load_4d(dst + c * C::CBOX, mq, bar_full + 8 * st, 64 * c, (MODE == 1 && brc) ? hq2 : hq1,
+                                qs * C::BN, b);
+                    if (MODE != 1)
+                        tma_load_4d(dst + (C::QB + c) * C::CBOX, &tq2, bar_full + 8 * st, 64 * c, hq2, qs * C::BN, b);
                 }
 #pragma unroll
                 for (int c = 0; c < C::VB; ++c)
-                    tma_load_4d(dst + (2 * C::QB + c) * C::CBOX, &tg, bar_full + 8 * st, 64 * c, hp, qs * C::BN, b);
+                    tma_load_4d(dst + (C::NQ * C::QB + c) * C::CBOX, &tg, bar_full + 8 * st, 64 * c, hp, qs * C::BN,
+                                b);
             }
             // row vectors of the 64 query rows: lse (+inf past T so that P = 0), D, c
             float *vec = reinterpret_cast<float *>(smem + (dst - sbase) + C::KV_STAGE_TMA);
@@ -593,13 +646,13 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
     } else if (warp == 1 || (C::TWO_ISSUERS && warp == 2)) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
-            const uint32_t sK1 = sbase + C::KV_OFF_K1, sK2 = V2 ? sK1 : sbase + C::KV_OFF_K2;
+            const uint32_t sK1 = sbase + C::KV_OFF_K1, sK2 = (V2 || MODE == 1) ? sK1 : sbase + C::KV_OFF_K2;
             const uint32_t sV = sbase + C::KV_OFF_V;
             const uint32_t sRP = sbase + C::KV_OFF_RES, sR1 = sRP + C::RBOX, sR2 = sR1 + C::RBOX;
             auto q1_at = [&](int it) { return sbase + C::KV_OFF_RING + (it % ST) * C::KV_STAGE; };
             // dV += P~^T G; dK_b += dS_b^T Q_b for item jj (A = result tiles, B = MN-major sub-tiles)
             auto acc = [&](int jj) {
-                const uint32_t sQ1 = q1_at(jj), sQ2 = sQ1 + C::QB * C::CBOX, sG = sQ1 + 2 * C::QB * C::CBOX;
+                const uint32_t sQ1 = q1_at(jj), sQ2 = sQ1 + C::QB * C::CBOX, sG = sQ1 + C::NQ * C::QB * C::CBOX;
                 const uint64_t ap = sdesc_sw128(sRP, 16, 1024), a1 = sdesc_sw128(sR1, 16, 1024),
                                a2 = sdesc_sw128(sR2, 16, 1024);
                 const uint64_t gdesc = sdesc_sw128(sG, C::CBOX, 1024);
@@ -608,9 +661,16 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                 for (int ks = 0; ks < C::BN / 16; ++ks) {
                     const uint32_t oa = (ks * 32) >> 4, ob = (ks * 2048) >> 4;
                     const uint32_t first = (jj > 0 || ks > 0) ? 1u : 0u;
-                    mma_ss(tmem + C::COL_DV, ap + oa, gdesc + ob, C::IDESC_V, first);
-                    mma_ss(tmem + C::COL_DK1, a1 + oa, q1d + ob, C::IDESC_QK, first);
-                    mma_ss(tmem + C::COL_DK2, a2 + oa, q2d + ob, C::IDESC_QK, V2 ? 1u : first);
+                    if constexpr (MODE == 1) {
+                        // dK_b += dS_b^T Q_b: the one result tile sits first
+                        mma_ss(tmem + C::COL_DK1, ap + oa, q1d + ob, C::IDESC_QK, first);
+                    } else if constexpr (MODE == 2) {
+                        mma_ss(tmem + C::COL_DV, ap + oa, gdesc + ob, C::IDESC_V, first);
+                    } else {
+                        mma_ss(tmem + C::COL_DV, ap + oa, gdesc + ob, C::IDESC_V, first);
+                        mma_ss(tmem + C::COL_DK1, a1 + oa, q1d + ob, C::IDESC_QK, first);
+                        mma_ss(tmem + C::COL_DK2, a2 + oa, q2d + ob, C::IDESC_QK, V2 ? 1u : first);
+                    }
                 }
                 mma_commit(bar_empty + 8 * (jj % ST));   // Q, G of jj no longer needed
                 mma_commit(bar_rfree);                    // result tiles read
@@ -618,7 +678,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
             // S_b^T = K_b Q_b^T (N = 64 queries), dP^T = V G^T for item it
             auto scores = [&](int it) {
                 const uint32_t sQ1 = q1_at(it);
-                const uint32_t sQ2 = sQ1 + C::QB * C::CBOX, sG = sQ1 + 2 * C::QB * C::CBOX;
+                const uint32_t sQ2 = sQ1 + C::QB * C::CBOX, sG = sQ1 + C::NQ * C::QB * C::CBOX;
                 const uint64_t a1 = sdesc_sw128(sK1, 16, 1024), a2 = sdesc_sw128(sK2, 16, 1024);
                 const uint64_t b1 = sdesc_sw128(sQ1, 16, 1024), b2 = sdesc_sw128(sQ2, 16, 1024);
 #pragma unroll
@@ -626,14 +686,16 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                     const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
                     const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
                     mma_ss(tmem + C::COL_S1, a1 + oa, b1 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
-                    mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    if (MODE != 1) mma_ss(tmem + C::COL_S2, a2 + oa, b2 + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
                 }
-                const uint64_t av = sdesc_sw128(sV, 16, 1024), bg = sdesc_sw128(sG, 16, 1024);
+                if (C::HAS_DP) {
+                    const uint64_t av = sdesc_sw128(sV, 16, 1024), bg = sdesc_sw128(sG, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < DV / 16; ++ks) {
-                    const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
-                    const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
-                    mma_ss(tmem + C::COL_DP, av + oa, bg + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < DV / 16; ++ks) {
+                        const uint32_t oa = ((ks >> 2) * C::RBOX + (ks & 3) * 32) >> 4;
+                        const uint32_t ob = ((ks >> 2) * C::CBOX + (ks & 3) * 32) >> 4;
+                        mma_ss(tmem + C::COL_DP, av + oa, bg + ob, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    }
                 }
                 mma_commit(bar_s);
             };
@@ -710,8 +772,8 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
             if (ok) {
                 tc_fence_after();
                 tmem_ld_cols<RC>(tmem + lane_off + C::COL_S1 + RC * wg, s1);
-                tmem_ld_cols<RC>(tmem + lane_off + C::COL_S2 + RC * wg, s2);
-                tmem_ld_cols<RC>(tmem + lane_off + C::COL_DP + RC * wg, dp);
+                if (MODE != 1) tmem_ld_cols<RC>(tmem + lane_off + C::COL_S2 + RC * wg, s2);
+                if (C::HAS_DP) tmem_ld_cols<RC>(tmem + lane_off + C::COL_DP + RC * wg, dp);
                 tmem_wait_ld();
             }
             tc_fence_before();
@@ -724,13 +786,15 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                 const int q0 = item_qs(it) * C::BN + RC * wg;
                 // every query of this part is at or after every key of the tile: no mask
                 const bool full = q0 >= kt * C::BM + C::BM - 1;
-                // in place: s1 <- P~ = P1 + c P2, s2 <- dS1, dp <- dS2; two unrolled
-                // copies, without the per-element mask where it is all true
+                // in place: s1 <- P~ = P1 + c P2, s2 <- dS1, dp <- dS2 (MODE 1: s1 <- dS_b;
+                // MODE 2: s1 <- P~); two unrolled copies, without the per-element mask
+                // where it is all true
                 auto form = [&](auto masked) {
 #pragma unroll
                     for (int c4 = 0; c4 < RC / 4; ++c4) {
-                        const float4 l1 = vec[c4], l2 = vec[16 + c4], e1 = vec[32 + c4], e2 = vec[48 + c4],
-                                     cv = vec[64 + c4];
+                        // MODE 1, branch 2: its lse and D in the place of branch 1's
+                        const float4 l1 = vec[(MODE == 1 && brc ? 16 : 0) + c4], l2 = vec[16 + c4],
+                                     e1 = vec[(MODE == 1 && brc ? 48 : 32) + c4], e2 = vec[48 + c4], cv = vec[64 + c4];
                         const float l1a[4] = {l1.x, l1.y, l1.z, l1.w}, l2a[4] = {l2.x, l2.y, l2.z, l2.w};
                         const float e1a[4] = {e1.x, e1.y, e1.z, e1.w}, e2a[4] = {e2.x, e2.y, e2.z, e2.w};
                         const float cva[4] = {cv.x, cv.y, cv.z, cv.w};
@@ -751,15 +815,28 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                                 p1 = make_float2(v0 ? p1.x : 0.f, v1 ? p1.y : 0.f);
                                 p2 = make_float2(v0 ? p2.x : 0.f, v1 ? p2.y : 0.f);
                             }
-                            const float2 r0 = __ffma2_rn(cv2, p2, p1);
-                            const float2 r1 = __fmul2_rn(p1, __fadd2_rn(dpv, make_float2(-e1a[k], -e1a[k + 1])));
-                            const float2 r2 = __fmul2_rn(p2, __ffma2_rn(cv2, dpv, make_float2(-e2a[k], -e2a[k + 1])));
-                            s1[c] = __float_as_uint(r0.x);
-                            s1[c + 1] = __float_as_uint(r0.y);
-                            s2[c] = __float_as_uint(r1.x);
-                            s2[c + 1] = __float_as_uint(r1.y);
-                            dp[c] = __float_as_uint(r2.x);
-                            dp[c + 1] = __float_as_uint(r2.y);
+                            if constexpr (MODE == 1) {
+                                // dS_b = P_b (cb dP - D_b), cb = 1 (branch 1) or c (branch 2)
+                                const float2 cb2 = brc ? cv2 : make_float2(1.f, 1.f);
+                                const float2 r1 = __fmul2_rn(p1, __ffma2_rn(cb2, dpv, make_float2(-e1a[k], -e1a[k + 1])));
+                                s1[c] = __float_as_uint(r1.x);
+                                s1[c + 1] = __float_as_uint(r1.y);
+                            } else if constexpr (MODE == 2) {
+                                const float2 r0 = __ffma2_rn(cv2, p2, p1);
+                                s1[c] = __float_as_uint(r0.x);
+                                s1[c + 1] = __float_as_uint(r0.y);
+                            } else {
+                                const float2 r0 = __ffma2_rn(cv2, p2, p1);
+                                const float2 r1 = __fmul2_rn(p1, __fadd2_rn(dpv, make_float2(-e1a[k], -e1a[k + 1])));
+                                const float2 r2 =
+                                    __fmul2_rn(p2, __ffma2_rn(cv2, dpv, make_float2(-e2a[k], -e2a[k + 1])));
+                                s1[c] = __float_as_uint(r0.x);
+                                s1[c + 1] = __float_as_uint(r0.y);
+                                s2[c] = __float_as_uint(r1.x);
+                                s2[c + 1] = __float_as_uint(r1.y);
+                                dp[c] = __float_as_uint(r2.x);
+                                dp[c + 1] = __float_as_uint(r2.y);
+                            }
                         }
                     }
                 };
@@ -774,10 +851,12 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                 uint32_t u[RC / 2];
                 pack_cols<RC>(s1, u);
                 store_row_part<RC>(resP, row, wg, u);
-                pack_cols<RC>(s2, u);
-                store_row_part<RC>(res1, row, wg, u);
-                pack_cols<RC>(dp, u);
-                store_row_part<RC>(res2, row, wg, u);
+                if (MODE == 0) {
+                    pack_cols<RC>(s2, u);
+                    store_row_part<RC>(res1, row, wg, u);
+                    pack_cols<RC>(dp, u);
+                    store_row_part<RC>(res2, row, wg, u);
+                }
                 fence_async_smem();   // generic-proxy writes -> tensor core reads
             }
             __syncwarp();
@@ -806,12 +885,23 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2>::THREADS, 1)
                     }
                 }
             };
-            // the first half of the warpgroups stores dK (both branches for V1), the
-            // second half dV, each warpgroup an equal share of the channels
+            // MODE 0: the first half of the warpgroups stores dK (both branches for V1),
+            // the second half dV, each warpgroup an equal share of the channels;
+            // MODE 1 / 2: every warpgroup an equal share of dK_b / dV
             constexpr int HG = C::NRG / 2;
             const int part = wg % HG;
             const int64_t krow = b * p.k_sb + static_cast<int64_t>(j) * p.k_st + static_cast<int64_t>(hk) * p.k_sh;
-            if (wg < HG) {
+            if constexpr (MODE == 1) {
+                constexpr int NK = DQK / C::NRG;
+                const int nk = min(NK, p.dqk_store - NK * wg);
+                if (nk > 0) store(C::COL_DK1 + NK * wg, nk, (brc ? p.dk2 : p.dk1) + krow + NK * wg, p.scale);
+            } else if constexpr (MODE == 2) {
+                constexpr int NV = DV / C::NRG;
+                store(C::COL_DV + NV * wg, NV,
+                      p.dv + b * p.v_sb + static_cast<int64_t>(j) * p.v_st + static_cast<int64_t>(hk) * p.v_sh +
+                          NV * wg,
+                      1.f);
+            } else if (wg < HG) {
                 constexpr int NK = DQK / HG;
                 // only the stored channels (the rest are zero padding)
                 const int nk = min(NK, p.dqk_store - NK * part);
@@ -858,11 +948,20 @@ __global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
     const __nv_bfloat16 *go = p.dout + b * p.o_sb + static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh;
     // V2: x1, x2 = a_e, a_o (bf16 saved); V1: x1 = x (RMSNorm input), x2 = a2 (fp32 saved).
     // Lane l owns the PER consecutive channels l * PER .. (one vector load per tensor).
-    static_assert(PER == 2 || PER == 4, "row pass: DV of 64 or 128");
+    static_assert(PER == 2 || PER == 4 || PER == 8, "row pass: DV of 64, 128 or 256");
     float x1[PER], x2[PER], dy[PER];
     const int64_t c0 = r * DV + lane * PER;
     auto load_bf16 = [&](const __nv_bfloat16 *src, float *dst) {
-        if (PER == 4) {
+        if constexpr (PER == 8) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(src);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[k]));
+                dst[2 * k] = a.x;
+                dst[2 * k + 1] = a.y;
+            }
+        } else if (PER == 4) {
             const uint2 u = *reinterpret_cast<const uint2 *>(src);
             const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
             const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
@@ -875,6 +974,14 @@ __global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
     if (V2) {
         load_bf16(static_cast<const __nv_bfloat16 *>(p.sa1) + c0, x1);
         load_bf16(static_cast<const __nv_bfloat16 *>(p.sa2) + c0, x2);
+    } else if constexpr (PER == 8) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const float4 a = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.sa1) + c0 + 4 * k);
+            const float4 c = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.sa2) + c0 + 4 * k);
+            x1[4 * k] = a.x; x1[4 * k + 1] = a.y; x1[4 * k + 2] = a.z; x1[4 * k + 3] = a.w;
+            x2[4 * k] = c.x; x2[4 * k + 1] = c.y; x2[4 * k + 2] = c.z; x2[4 * k + 3] = c.w;
+        }
     } else if (PER == 4) {
         const float4 a = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.sa1) + c0);
         const float4 c = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.sa2) + c0);
@@ -932,7 +1039,7 @@ __global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
         for (int i = 0; i < PER; ++i) m = fmaf(dy[i], x[i] * rr, m);
         m = warp_sum(m) / static_cast<float>(DV);
         float d1 = 0.f, d2 = 0.f, dl = 0.f;
-        __nv_bfloat16 gb[PER];
+        alignas(16) __nv_bfloat16 gb[PER];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const float dx = rr * (dy[i] - x[i] * rr * m);
@@ -944,7 +1051,9 @@ __global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
             d2 = fmaf(gr, x2[i], d2);
             dl = fmaf(dx, x2[i], dl);
         }
-        if (PER == 4)
+        if constexpr (PER == 8)
+            *reinterpret_cast<uint4 *>(p.g + c0) = *reinterpret_cast<const uint4 *>(gb);
+        else if (PER == 4)
             *reinterpret_cast<uint2 *>(p.g + c0) = *reinterpret_cast<const uint2 *>(gb);
         else
             *reinterpret_cast<uint32_t *>(p.g + c0) = *reinterpret_cast<const uint32_t *>(gb);
@@ -1046,9 +1155,52 @@ cudaError_t launch_bwd_lambda(const BwdPreParams &pp, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// DIFF V1 at d = 128 (dv = 256): per-branch dQ and dK kernels (two CTAs per
+// tile) and a dV kernel, after the row pass and the lambda reduction.
+cudaError_t launch_bwd_v1_d128(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, cudaStream_t s) {
+    using CQ = BwdCfg<128, 256, false, 1>;
+    using CK = BwdCfg<128, 256, false, 1>;
+    using CV = BwdCfg<128, 256, false, 2>;
+    static unsigned long long attr_done = 0;   // one bit per device
+    cudaError_t ea = once_per_device(&attr_done, [] {
+        cudaError_t e = cudaFuncSetAttribute(bwd_dq<128, 256, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             CQ::DQ_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bwd_dkdv<128, 256, false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     CK::KV_SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bwd_dkdv<128, 256, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     CV::KV_SMEM);
+        return e;
+    });
+    if (ea != cudaSuccess) return ea;
+    const int64_t rows = static_cast<int64_t>(pp.B) * pp.T * pp.H;
+    const int64_t pre_blocks = (rows + 7) / 8;
+    if (pre_blocks < 1 || pre_blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    bwd_pre<256, false><<<static_cast<unsigned>(pre_blocks), 256, 0, s>>>(pp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_lambda<<<1, 1024, 0, s>>>(pp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = static_cast<int64_t>((p.T + 127) / 128) * p.H * p.B;
+    if (2 * tiles > 0x7fffffff) return cudaErrorInvalidValue;
+    bwd_dkdv<128, 256, false, 1><<<static_cast<unsigned>(2 * tiles), CK::THREADS, CK::KV_SMEM, s>>>(
+        m.k1r, m.k2r, m.vr, m.q1c, m.q2c, m.gc, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dkdv<128, 256, false, 2><<<static_cast<unsigned>(tiles), CV::THREADS, CV::KV_SMEM, s>>>(
+        m.k1r, m.k2r, m.vr, m.q1c, m.q2c, m.gc, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dq<128, 256, false, 1><<<static_cast<unsigned>(2 * tiles), CQ::THREADS, CQ::DQ_SMEM, s>>>(
+        m.q1r, m.q2r, m.gr, m.k1c, m.k2c, m.vc, p);
+    return cudaGetLastError();
+}
+
 bool backward_supported(int dqk, int dv, bool v2) {
     if (v2) return (dqk == 128 && dv == 128) || (dqk == 64 && dv == 64);
-    return (dqk == 64 && dv == 128) || (dqk == 32 && dv == 64);
+    return (dqk == 64 && dv == 128) || (dqk == 32 && dv == 64) || (dqk == 128 && dv == 256);
 }
 
 cudaError_t launch_backward(const BwdMaps &m, const BwdParams &p, const BwdPreParams &pp, int dqk, int dv, bool v2,
@@ -1060,6 +1212,7 @@ cudaError_t launch_backward(const BwdMaps &m, const BwdParams &p, const BwdPrePa
     // zero-filled, so the d = 64 kernels compute the same S; the padded halves
     // of dq and dk come out zero and are not stored (p.dqk_store)
     if (!v2 && dqk == 32 && dv == 64) return launch_bwd_t<64, 64, false>(m, p, pp, s);
+    if (!v2 && dqk == 128 && dv == 256) return launch_bwd_v1_d128(m, p, pp, s);
     return cudaErrorInvalidValue;
 }
 

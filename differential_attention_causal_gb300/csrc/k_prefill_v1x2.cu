@@ -103,7 +103,11 @@ __device__ __forceinline__ float sum_exp128(const uint32_t *s, float scale, floa
     return t.x + t.y;
 }
 
-template <int DQK>
+// TRAIN (the training forward, DQK = 128): run 1 saves each branch's row
+// log-sum-exp (log2 units, m + log2 l of pass A) and x = a1 - lam a2 (fp32,
+// the RMSNorm input) besides the output; run 2 forms P = e2 / l2 alone in
+// pass B and saves a2 (fp32), writing no output.
+template <int DQK, bool TRAIN = false>
 __global__ void __launch_bounds__(384, 1)
     prefill_v1_twopass(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
                        const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
@@ -411,7 +415,11 @@ __global__ void __launch_bounds__(384, 1)
         const float m2 = xch[256 + row], l2 = xch[384 + row];
         ok = warp_wait(bar_lam, 0, p.err, ok);
         const float lam = lam_smem[0], lam_init = lam_smem[1];
-        const float c1 = 1.f / l1, c2 = lam / l2;
+        const bool a2_run = TRAIN && p.train_run == 2;
+        if (TRAIN && !a2_run && t < p.T)   // this branch's log-sum-exp for the backward
+            p.slse[((static_cast<int64_t>(br) * p.B + b) * p.H + h) * p.T + t] = m + __log2f(l);
+        // P = c1 e1 - c2 e2: x = a1 - lam a2, or a2 alone (c1 = 0, c2 = -1 / l2)
+        const float c1 = a2_run ? 0.f : 1.f / l1, c2 = a2_run ? -1.f / l2 : lam / l2;
 
         // pass B: keys 64*br .. 64*br+63 of each tile
         for (int j = 0; j < n; ++j) {
@@ -475,12 +483,19 @@ __global__ void __launch_bounds__(384, 1)
                 ss = fmaf(x[cc0 + k], x[cc0 + k], ss);
             }
         }
+        if (TRAIN && ok && t < p.T) {
+            // x (run 1) or a2 (run 2), fp32, this warpgroup's half of the channels
+            float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(a2_run ? p.sa2 : p.sa1) +
+                                                    ((static_cast<int64_t>(b) * p.T + t) * p.H + h) * C::DV + col0);
+#pragma unroll
+            for (int k = 0; k < HALF; k += 4) d4[k / 4] = make_float4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+        }
         // the statistics area is free again: both warpgroups read it before pass B
         xch[br * 128 + row] = ss;
         named_bar_sync(1, 256);
         const float ms = (xch[row] + xch[128 + row]) * (1.f / static_cast<float>(C::DV));
         const float r = (1.f - lam_init) * rsqrtf(ms + 1e-5f);
-        if (ok && t < p.T) {
+        if (ok && t < p.T && !a2_run) {
             __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + static_cast<int64_t>(b) * p.o_sb +
                                  static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh + col0;
 #pragma unroll
@@ -504,23 +519,25 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int DQK>
+template <int DQK, bool TRAIN = false>
 cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
     using C = V1x2Cfg<DQK>;
     static unsigned long long attr_done = 0;   // one bit per device
     const cudaError_t ea = once_per_device(&attr_done, [] {
         // the in-kernel register split must fit in the launch-time budget
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_v1_twopass<DQK>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_v1_twopass<DQK, TRAIN>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs < C::REGS_NEEDED_AT_LAUNCH) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(prefill_v1_twopass<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        return cudaFuncSetAttribute(prefill_v1_twopass<DQK, TRAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::SMEM);
     });
     if (ea != cudaSuccess) return ea;
     const int n_qt = (p.T + C::BM - 1) / C::BM;
     const long long grid = static_cast<long long>(n_qt) * p.H * p.B;
     if (grid < 1 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    prefill_v1_twopass<DQK><<<static_cast<unsigned>(grid), 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, p);
+    prefill_v1_twopass<DQK, TRAIN><<<static_cast<unsigned>(grid), 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v,
+                                                                                     p);
     return cudaGetLastError();
 }
 
@@ -532,6 +549,16 @@ cudaError_t launch_prefill_v1_twopass(const PrefillMaps &m, const PrefillParams 
     if (dqk == 128) return launch_t<128>(m, p, s);
     if (dqk == 64) return launch_t<64>(m, p, s);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_v1_twopass_train(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
+    if (!p.sa1 || !p.sa2 || !p.slse) return cudaErrorInvalidValue;
+    PrefillParams q = p;
+    q.train_run = 1;   // output, x and the log-sum-exp
+    cudaError_t e = launch_t<128, true>(m, q, s);
+    if (e != cudaSuccess) return e;
+    q.train_run = 2;   // a2
+    return launch_t<128, true>(m, q, s);
 }
 
 }  // namespace da

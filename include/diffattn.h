@@ -265,9 +265,11 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
                              da_dtype dtype, cudaStream_t stream);
 
 /* ---- training: forward with saved tensors, and the backward -----------
- * Supported: DA_BF16 on the tensor cores: V1 d in {32, 64} (d = 32 on the
- * d = 64 kernels with zero-filled q / k boxes), V2 D in {64, 128}; DA_F32 on
- * CUDA cores: V1 d in {32, 64, 128}, V2 D in {64, 128}
+ * Supported: DA_BF16 on the tensor cores: V1 d in {32, 64, 128} (d = 32 on
+ * the d = 64 kernels with zero-filled q / k boxes; d = 128, dv = 256, with a
+ * training forward of two launches and a backward of five: a row pass, the
+ * lambda reduction, dK per branch, dV, dQ per branch), V2 D in {64, 128};
+ * DA_F32 on CUDA cores: V1 d in {32, 64, 128}, V2 D in {64, 128}
  * (every tensor, dout and the gradients fp32).  Other combinations return
  * DA_ERR_UNSUPPORTED_DIM.  The size functions take the same dtype.
  *

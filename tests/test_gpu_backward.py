@@ -79,6 +79,14 @@ def test_v1_backward(B, T, H):
     check_v1_backward(B, T, H, 64)
 
 
+@pytest.mark.parametrize("B,T,H", [(1, 128, 1), (2, 200, 3), (1, 1, 1), (1, 384, 2), (1, 700, 1), (1, 1300, 2)])
+def test_v1_backward_d128(B, T, H):
+    # d = 128, dv = 256: the two-pass training forward (two launches: output, x and
+    # the log-sum-exp; then a2) and the split backward (row pass, lambda, per-branch
+    # dK, dV, per-branch dQ: five launches)
+    check_v1_backward(B, T, H, 128)
+
+
 @pytest.mark.parametrize("B,T,H", [(1, 128, 1), (2, 200, 3), (1, 1, 1), (1, 300, 2)])
 def test_v1_backward_d32(B, T, H):
     # d = 32 runs the d = 64 kernels on zero-filled q / k boxes; dq, dk keep 32 channels
@@ -89,6 +97,7 @@ def check_v1_backward(B, T, H, d):
     x, dout = v1_case(B, T, H, seed=T + B + d, d=d)
     xd, dd = to_dev(x), dout.cuda()
     out, g = run_v1(xd, dd, 12)
+    assert binding().last_launch_count() == (5 if d == 128 else 4)
     assert binding().device_error() == 0
     plain = binding().v1_fwd(xd["q1"], xd["q2"], xd["k1"], xd["k2"], xd["v"], xd["lam_q1"], xd["lam_k1"],
                              xd["lam_q2"], xd["lam_k2"], 12)
@@ -100,8 +109,12 @@ def check_v1_backward(B, T, H, d):
     rep = {}
     for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
         if T == 1 and n != "dv":
-            # one key: the scores carry no gradient, the oracle's are exactly 0
-            assert g[n].abs().max().item() <= 1e-6
+            # one key: the scores carry no gradient, the oracle's are exactly 0.  At
+            # d = 128 the saved x is the two-pass forward's, formed from the combined
+            # P = e1 / l1 - lam e2 / l2 rounded to bf16, so a1 = x + lam a2 and with it
+            # D1 = g . a1 differ from g . v by that rounding: dP - D leaves a residue
+            # of the order of 2^-9 |D| scaled by |k| / sqrt(d) (measured 2.4e-6)
+            assert g[n].abs().max().item() <= (1e-5 if d == 128 else 1e-6)
             continue
         check_grad(n, g[n], ref[n], rep)
     check_lambda_vectors(g, ref, x, rep)
@@ -131,7 +144,7 @@ def test_v2_backward(B, T, Hq, Hkv, D):
 
 def test_backward_argument_checks():
     bd = binding()
-    assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128, 1) == 0   # bf16 d = 128: no backward kernel
+    assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128, 1) > 0    # bf16 d = 128: the split backward
     assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 128, 0) > 0    # fp32 d = 128: CUDA-core backward
     assert bd.lib().diffattn_v1_train_saved_size(1, 128, 2, 32, 1) > 0     # bf16 d = 32: the d = 64 kernels
     assert bd.lib().diffattn_v2_bwd_workspace_size(1, 128, 6, 2, 128, 1) > 0
@@ -253,3 +266,33 @@ def test_v2_backward_fp32(B, T, Hq, Hkv, D):
     ref = oracle.v2_bwd(x["q"], x["k"], x["v"], x["lam"], dout)
     for n in ("dq", "dk", "dv", "dlam"):
         check_f32(n, g[n], ref[n])
+
+
+def test_v1_backward_d128_long_context_workload():
+    """B=1, T=32768, 12 diff heads, d=128, dv=256, layer_index=27 (the long-context
+    V1 workload), in the launch the bench times.  Row i's dq1, dq2 depend only on
+    tokens 0..i (its keys, values and its own upstream gradient), so the first
+    T0 = 1024 rows of two heads are checked element by element against the
+    oracle's gradients of the same inputs cut at T0.  dK and dV of every key
+    depend on all later rows; for them the full-size property checked is that
+    each head's keys' dk sum to zero (sum_j dS_ij = 0 for every row), bounded
+    by the sum of |dk| times the bf16 rounding scale."""
+    s = inputs.WORKLOADS["v1_bf16_B1_T32768_H12_d128"]
+    xd = inputs.make_v1(s, seed=2, device="cuda")
+    dd = inputs.make_grad_out((s.B, s.T, s.H, 2 * s.d), "bf16", seed=2, device="cuda")
+    _, g = run_v1(xd, dd, s.layer_index)
+    assert binding().device_error() == 0
+    T0, heads = 1024, [0, s.H - 1]
+    xc = {n: xd[n][:, :T0, heads].contiguous().cpu() for n in ("q1", "q2", "k1", "k2", "v")}
+    ref = oracle.v1_bwd(xc["q1"], xc["q2"], xc["k1"], xc["k2"], xc["v"], xd["lam_q1"].cpu(), xd["lam_k1"].cpu(),
+                        xd["lam_q2"].cpu(), xd["lam_k2"].cpu(), s.layer_index, dd[:, :T0, heads].cpu())
+    for n in ("dq1", "dq2"):
+        check_grad(n, g[n][:, :T0, heads], ref[n])
+    for n in ("dk1", "dk2"):
+        gk = g[n].float()
+        tot = gk.sum(dim=1).abs()                     # (B, H, d): sum over keys
+        scale = gk.abs().sum(dim=1)
+        assert bool((tot <= 1e-2 * scale + 1e-3).all()), (n, float((tot / (scale + 1e-30)).max()))
+    assert torch.isfinite(g["dv"].float()).all()
+    del g, xd, dd
+    torch.cuda.empty_cache()
