@@ -49,7 +49,7 @@ SPINUP_S = 0.3
 # it was taken on (sha256 of the .cu file, first 16 hex digits).
 TRAFFIC_RECORDS: dict = {
     # profiles/prefill_onepass_v1_B4_T2048_H16_d64.md: dram__bytes_read.sum + dram__bytes_write.sum
-    "prefill_v1_d64": {"src_sha": "50e13b0b703c8a85", "bytes_per_launch": 148303104 + 13934336},
+    "prefill_v1_d64": {"src_sha": "b6ee62431a599eb7", "bytes_per_launch": 145358592 + 14034176},
 }
 
 
