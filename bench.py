@@ -724,11 +724,70 @@ CASES = {
     "decode_varlen_b8": ("decode_varlen", None),
     # a quarter of its batch, for multi-pass profiler captures
     "paired_b2": ("paired", None),
+    # pinned host <-> device copy rates per NUMA node (the end-to-end figure's link)
+    "host_link": ("host_link", None),
 }
+
+
+def host_link(launches: int):
+    """Pinned host <-> device copy rates behind the end-to-end figure, with the
+    host buffer first touched by a process bound to each NUMA node's CPUs."""
+    def read(path):
+        try:
+            with open(path) as f:
+                return f.read().strip()
+        except OSError:
+            return None
+    nodes = {}
+    base = "/sys/devices/system/node"
+    for n in sorted(os.listdir(base)) if os.path.isdir(base) else []:
+        if n.startswith("node") and n[4:].isdigit():
+            nodes[n] = read(os.path.join(base, n, "cpulist"))
+    bus = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader"], capture_output=True,
+                         text=True).stdout.strip().splitlines()
+    gpu_node = read(f"/sys/bus/pci/devices/{bus[0].strip().lower()}/numa_node") if bus else None
+    code = r"""
+import os, sys, torch
+cpus = sys.argv[1]
+if cpus != "all":
+    sel = set()
+    for part in cpus.split(","):
+        a, _, b = part.partition("-")
+        sel.update(range(int(a), int(b or a) + 1))
+    os.sched_setaffinity(0, sel)
+n = 256 << 20
+h = torch.empty(n, dtype=torch.uint8).pin_memory()
+h.fill_(1)
+d = torch.empty(n, dtype=torch.uint8, device="cuda")
+def rate(fn, k):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(k):
+        fn()
+    b.record()
+    b.synchronize()
+    return n * k / (a.elapsed_time(b) * 1e-3) / 1e9
+print(rate(lambda: d.copy_(h, non_blocking=True), int(sys.argv[2])),
+      rate(lambda: h.copy_(d, non_blocking=True), int(sys.argv[2])))
+"""
+    res = {}
+    for name, cpus in [("all", "all")] + list(nodes.items()):
+        r = subprocess.run([sys.executable, "-c", code, cpus or "all", str(max(3, launches))], capture_output=True,
+                           text=True)
+        v = r.stdout.split()
+        res[name] = {"cpus": cpus, "h2d_GBps": round(float(v[0]), 1), "d2h_GBps": round(float(v[1]), 1)} \
+            if len(v) == 2 else {"cpus": cpus, "error": r.stderr[-300:]}
+    print(json.dumps({"case": "host_link", "numa_nodes": nodes, "gpu_numa_node": gpu_node, "copies": res}))
 
 
 def run_case(name: str, launches: int):
     from differential_attention_causal_gb300 import binding
+    if name == "host_link":
+        host_link(launches)
+        return
     kind, wl = CASES[name]
     dev = torch.device("cuda", 0)
     if wl:
