@@ -446,8 +446,37 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
     gbs = nbytes / (ms * 1e-3) / 1e9
     aux["prologue"] = {"workload": "v2_bf16_B8_T4096_Hq32_Hkv8_D128, x (B,T,2048), w (2048,16)", "ms": round(ms, 4),
                        "GB/s": round(gbs, 1), "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
-                       "bytes": int(nbytes), "launches": 1, "peak_kind": peak_kind}
-    del x, lp, lam
+                       "bytes": int(nbytes), "launches": 2, "peak_kind": peak_kind}
+    # the V2 attention call with its prologue, two ways: rotary q, k + lambda
+    # logits, then the prefill (3 launches), against lambda logits, then the
+    # prefill with q rotated tile by tile inside it (k + table, prefill: 3 launches)
+    out = torch.empty((s.B, s.T, s.Hq // 2, s.D), dtype=torch.bfloat16, device=dev)
+    cs = torch.empty(s.T * s.D, dtype=torch.float32, device=dev)
+
+    def two_call():
+        binding.prologue(q=x["q"], k=x["k"], x=lp["x"], w_lam=lp["w_lam"], lam=lam)
+        binding.v2_fwd(x["q"], x["k"], x["v"], lam, out=out)
+
+    def fused():
+        binding.prologue(x=lp["x"], w_lam=lp["w_lam"], lam=lam)
+        binding.v2_fwd_rope(x["q"], x["k"], x["v"], lam, out=out, cs=cs)
+
+    res = {}
+    for name, fn in (("two_call", two_call), ("fused", fused)):
+        for _ in range(3):
+            fn()
+        t = time_steps(fn, 10, flush)
+        res[name] = (sum(t) / len(t), statistics.median(t))
+    tf = v2_flops(s) / (res["fused"][1] * 1e-3) / 1e12
+    aux["v2_prefill_with_prologue"] = {
+        "workload": "v2_bf16_B8_T4096_Hq32_Hkv8_D128, x (B,T,2048), w (2048,16)",
+        "two_call_ms": round(res["two_call"][0], 4), "two_call_ms_median": round(res["two_call"][1], 4),
+        "fused_ms": round(res["fused"][0], 4), "fused_ms_median": round(res["fused"][1], 4),
+        "saved_ms_median": round(res["two_call"][1] - res["fused"][1], 4),
+        "fused_attention_TFLOP/s_incl_prologue": round(tf, 1), "launches": 3,
+        "note": "two_call: prologue (rotary q, k; lambda logits) + v2_fwd; fused: lambda logits + "
+                "v2_fwd_rope (k and the cos/sin table, then the prefill rotating each Q tile in shared memory)"}
+    del x, lp, lam, out, cs
     torch.cuda.empty_cache()
     # Paired Head Attention (interleaved head pairs, one causal softmax) on the V2 prefill's query heads
     s = inputs.WORKLOADS["paired_bf16_B8_T4096_H32_D128"]

@@ -52,6 +52,9 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v1_fwd_host.restype = i32
             L.diffattn_v1_fwd_host.argtypes = ([vp, vp, vp, fp, fp, fp, fp, vp] + [i32] * 5
                                                + [vp, ctypes.c_size_t, i32, vp])
+            L.diffattn_v2_fwd_rope.restype = i32
+            L.diffattn_v2_fwd_rope.argtypes = ([vp, vp, vp, fp, vp] + [i32] * 5 + [i64, ctypes.c_float, fp]
+                                               + [i32, vp])
             L.diffattn_paired_fwd.restype = i32
             L.diffattn_paired_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 4 + [i32, vp]
             L.diffattn_v2_decode_workspace_size.restype = ctypes.c_size_t
@@ -221,6 +224,35 @@ def v2_fwd(q, k, v, lam, out: torch.Tensor | None = None, stream=None) -> torch.
     rc = lib().diffattn_v2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), out.data_ptr(),
                                B, T, Hq, Hkv, D, _dtype_code(q), _stream(stream))
     _check("diffattn_v2_fwd", rc)
+    return out
+
+
+def v2_fwd_rope(q, k, v, lam, pos0: int = 0, base: float = 10000.0, out: torch.Tensor | None = None,
+                cs: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """DIFF V2 causal prefill of rotary-embedded q and k: the same result as
+    prologue(q, k, pos0, base) followed by v2_fwd, with q left unchanged (its
+    tiles are rotated inside the prefill kernel) and k rotated in place.
+
+    Shapes as for v2_fwd (bf16); cs is an optional fp32 workspace of T * D
+    elements (allocated here if None).  Returns out."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("lam", lam)):
+        _cuda(t, n)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    if lam.dtype != torch.float32:
+        raise ValueError("lam must be fp32")
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty((B, T, Hq // 2, D), dtype=q.dtype, device=q.device)
+    if cs is None:
+        cs = torch.empty(T * D, dtype=torch.float32, device=q.device)
+    elif cs.dtype != torch.float32 or cs.numel() < T * D or not cs.is_contiguous():
+        raise ValueError("cs must be a contiguous fp32 tensor of at least T * D elements")
+    rc = lib().diffattn_v2_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), out.data_ptr(),
+                                    B, T, Hq, Hkv, D, int(pos0), float(base), cs.data_ptr(),
+                                    _dtype_code(q), _stream(stream))
+    _check("diffattn_v2_fwd_rope", rc)
     return out
 
 
@@ -555,7 +587,8 @@ def v2_bwd(q, k, v, lam, dout, saved, workspace: torch.Tensor | None = None, str
 def prologue(q=None, k=None, pos0: int = 0, base: float = 10000.0, x=None, w_lam=None, lam=None, stream=None):
     """Rotary embedding of q (B, T, Hq, D) and k (B, T, Hk, D) in place and, if
     x (B, T, C) and w_lam (C, P) are given, the V2 lambda logits x @ w_lam
-    (fp32 (B, T, P), written to lam or a new tensor), in one kernel.
+    (fp32 (B, T, P), written to lam or a new tensor): one pass over each
+    tensor, one kernel for the rotation and one for the logits.
     Returns lam (or None)."""
     ref = q if q is not None else (k if k is not None else x)
     if ref is None:

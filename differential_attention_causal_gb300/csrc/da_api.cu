@@ -344,6 +344,57 @@ da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const flo
     return st;
 }
 
+da_status diffattn_v2_fwd_rope(const void *q, void *k, const void *v, const float *lam, void *out, int B, int T,
+                               int Hq, int Hkv, int D, int64_t pos0, float base, float *cs, da_dtype dtype,
+                               cudaStream_t stream) {
+    if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
+    if (!q || !k || !v || !lam || !out || !cs) return DA_ERR_NULL_PTR;
+    if (B < 1 || T < 1 || Hq < 2 || Hkv < 1 || !(base > 0.f)) return DA_ERR_BAD_SHAPE;
+    if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
+    if (dtype != DA_BF16 || (D != 64 && D != 128)) return DA_ERR_UNSUPPORTED_DIM;
+    for (const void *ptr : {q, static_cast<const void *>(k), v, static_cast<const void *>(out),
+                            static_cast<const void *>(cs)})
+        if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
+    uint32_t *err = nullptr;
+    int nsm = 0;
+    if (!device_state(stream, &err, &nsm)) return DA_ERR_CUDA;
+    const int P = Hq / 2, G = Hq / Hkv;
+    t_last_launches = 0;
+    PrefillMaps m;
+    const uint64_t uT = static_cast<uint64_t>(T), uB = static_cast<uint64_t>(B);
+    const int64_t qst = static_cast<int64_t>(Hq) * D, kst = static_cast<int64_t>(Hkv) * D;
+    if (!encode_map_4d(&m.q1, q, D, Hq, uT, uB, D, qst, qst * T, 128) ||
+        !encode_map_4d(&m.k1, k, D, Hkv, uT, uB, D, kst, kst * T, 128) ||
+        !encode_map_4d(&m.v, v, D, Hkv, uT, uB, D, kst, kst * T, 128) ||
+        !encode_map_4d(&m.out, out, D, P, uT, uB, D, static_cast<int64_t>(P) * D, static_cast<int64_t>(P) * D * T, 128))
+        return DA_ERR_CUDA;
+    m.q2 = m.q1;
+    m.k2 = m.k1;
+    // k rotated in place and the cos / sin table written in one pass
+    PrologueParams r{};
+    r.k = k;
+    r.Hq = 0; r.Hk = Hkv; r.D = D;
+    r.B = B; r.T = T;
+    r.pos0 = pos0;
+    r.base = static_cast<double>(base);
+    r.cs_out = reinterpret_cast<float2 *>(cs);
+    da_status st = cuda_status(launch_prologue(r, true, stream));
+    if (st != DA_OK) return st;
+    t_last_launches = 1;
+    PrefillParams p{};
+    p.out = out;
+    p.o_sh = D; p.o_st = static_cast<int64_t>(P) * D; p.o_sb = p.o_st * T;
+    p.lam = lam;
+    p.B = B; p.T = T; p.H = P; p.G = G;
+    p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
+    p.num_sms = nsm;
+    p.err = err;
+    p.rope_cs = reinterpret_cast<const float4 *>(cs);
+    st = cuda_status(launch_prefill_v2_rope(m, p, D, stream));
+    if (st == DA_OK) t_last_launches = 2;
+    return st;
+}
+
 da_status diffattn_paired_fwd(const void *q, const void *k, const void *v, void *out, int B, int T, int H, int D,
                               da_dtype dtype, cudaStream_t stream) {
     if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
@@ -1030,7 +1081,7 @@ extern "C" da_status diffattn_prologue(void *q, void *k, int B, int T, int Hq, i
     p.pos0 = pos0;
     p.base = static_cast<double>(base);
     const da_status st = cuda_status(launch_prologue(p, dtype == DA_BF16, stream));
-    if (st == DA_OK) t_last_launches = 1;
+    if (st == DA_OK) t_last_launches = (Hq + Hk > 0 ? 1 : 0) + (x ? 1 : 0);
     return st;
 }
 

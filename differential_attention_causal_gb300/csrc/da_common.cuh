@@ -315,6 +315,20 @@ __device__ __forceinline__ float row_max128(const uint32_t *s) {
     return fmaxf(fmax3(a[0], a[1], a[2]), fmax3(fmax3(a[3], a[4], a[5]), a[6], a[7]));
 }
 
+// Rotary embedding of one pair (a = x_i, b = x_{i + D/2}) by the angle whose
+// cosine and sine are c, s: (a c - b s, b c + a s), each an fma over a
+// rounded product, so that every kernel that rotates gets the same bits.
+__device__ __forceinline__ void rope_rotate(float a, float b, float c, float s, float &ra, float &rb) {
+    ra = fmaf(a, c, -(b * s));
+    rb = fmaf(b, c, a * s);
+}
+// The same for two pairs at once on the paired fp32 units (same bits per lane).
+__device__ __forceinline__ void rope_rotate2(float2 a, float2 b, float2 c, float2 s, float2 &ra, float2 &rb) {
+    const float2 bs = __fmul2_rn(b, s);
+    ra = __ffma2_rn(a, c, make_float2(-bs.x, -bs.y));
+    rb = __ffma2_rn(b, c, __fmul2_rn(a, s));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);

@@ -83,6 +83,9 @@ struct PrefillParams {
     void *sa1, *sa2;
     float *slse;
     int train_run;                 // DIFF V1 two-pass training forward: 1 = x and lse, 2 = a2
+    const float4 *rope_cs;         // V2 with rotary embedding: the cos / sin table, entry j * T + t
+                                   // = (cos, sin) of pairs 2j and 2j + 1 at token t; q rotated in
+                                   // shared memory as each Q tile lands
 };
 struct PrefillMaps {
     CUtensorMap q1, q2, k1, k2, v;
@@ -95,6 +98,9 @@ cudaError_t launch_prefill(const PrefillMaps &m, const PrefillParams &p, int dqk
 // Paired Head Attention forward on the one-pass kernel (bf16, D in {64, 128}):
 // m.q1 = m.q2 = a 4-D map of q, m.k1 = m.k2 and m.v 5-D interleaved maps of
 // k and v (encode_map_pairs); p.H = pairs, p.G = 2, p.out / p.o_* the output.
+// V2 prefill whose Q tiles are rotated (rotary embedding, table p.rope_cs) in
+// shared memory before their first product; D in {64, 128}, bf16.
+cudaError_t launch_prefill_v2_rope(const PrefillMaps &m, const PrefillParams &p, int d, cudaStream_t s);
 bool paired_supported(int d);
 cudaError_t launch_paired(const PrefillMaps &m, const PrefillParams &p, int d, cudaStream_t s);
 // 5-D map over a contiguous (B, T, H, D) bf16 tensor read as {D, 2, H/2, T, B}
@@ -194,6 +200,10 @@ struct PrologueParams {
     int B, T;
     int64_t pos0;                  // position of token t is pos0 + t
     double base;
+    float2 *cs_out;                // optional: the (cos, sin) the rotation applies at token t to
+                                   // pair i, at cs_out[((i / 2) * T + t) * 2 + i % 2], so that
+                                   // pairs 2j, 2j + 1 of a token are one 16-byte entry (batch 0
+                                   // writes it)
 };
 bool prologue_supported(int D, int C, int P);
 cudaError_t launch_prologue(const PrologueParams &p, bool bf16, cudaStream_t s);

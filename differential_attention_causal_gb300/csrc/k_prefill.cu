@@ -79,8 +79,9 @@ struct PreCfg {
     // the output staging tile, used before the tile is written
     static constexpr int OFF_X = OFF_OUT;
     static constexpr int OFF_BAR = OFF_OUT + OUT_TILE;
-    // qfull, qfree, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s[2], p[2][2], o[2], odrain, drain, lam
-    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 6;
+    // qfull, qfree, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s[2], p[2][2], o[2], odrain, drain, lam,
+    // staged, store-free, drain2, q rotated
+    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 7;
     static constexpr int OFF_LAM = OFF_BAR + NBAR * 8;        // 2 floats
     static constexpr int OFF_TSLOT = OFF_LAM + 8;
     static constexpr int SMEM = OFF_TSLOT + 8 + 1024;         // + alignment slack
@@ -138,7 +139,63 @@ __device__ __forceinline__ int snake_tile(int k, int c, int G, int NT) {
     return w < NT ? w : -1;
 }
 
-template <int DQK, int DV, bool V2, bool TRAIN, bool PAIRED>
+// Rotary embedding of one query row of both Q tiles in shared memory (each
+// DQK channels as DQK / 64 boxes of 128 rows x 128 bytes, 128-byte swizzle),
+// the pairs (i, i + DQK/2) for i in this thread's half of the pairs (half 0:
+// i < DQK/4, half 1: the rest), turned by the angles of cs[(i / 2) * ld]
+// (a (cos, sin, cos, sin) entry per two pairs), every value rounded back to
+// bf16.  8-channel chunk c of the first half pairs with chunk c + DQK/16 at
+// the same place in its group.  The two branches' threads of one row take
+// the two halves, so each table entry is read once per row.
+template <int DQK>
+struct RopeTab {
+    static constexpr int MY = DQK / 32;    // 8-channel chunks of this thread per tile
+    float4 t[MY][4];
+};
+
+template <int DQK>
+__device__ __forceinline__ void rope_tab_load(RopeTab<DQK> &tab, int half, const float4 *cs, int ld) {
+    constexpr int MY = RopeTab<DQK>::MY;
+#pragma unroll
+    for (int c = 0; c < MY; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            tab.t[c][e] = __ldg(cs + static_cast<int64_t>(4 * (half * MY + c) + e) * ld);
+}
+
+template <int DQK>
+__device__ __forceinline__ void rope_q_row(uint8_t *q1, uint8_t *q2, int row, int half, const RopeTab<DQK> &tab) {
+    constexpr int NCH = DQK / 16;          // 8-channel chunks per half of the channels
+    constexpr int MY = RopeTab<DQK>::MY;
+    constexpr int BOX = 128 * 128;
+    auto at = [&](uint8_t *q, int c) { return q + (c >> 3) * BOX + row * 128 + (((c & 7) ^ (row & 7)) << 4); };
+    const int c0 = half * MY;
+#pragma unroll
+    for (int tile = 0; tile < 2; ++tile) {
+#pragma unroll
+        for (int c = 0; c < MY; ++c) {
+            uint4 *pa = reinterpret_cast<uint4 *>(at(tile ? q2 : q1, c0 + c));
+            uint4 *pb = reinterpret_cast<uint4 *>(at(tile ? q2 : q1, c0 + c + NCH));
+            const uint4 ua = *pa, ub = *pb;
+            const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+            uint32_t ra[4], rb[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wa[k]));
+                const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wb[k]));
+                const float4 cs4 = tab.t[c][k];
+                float2 xa, xb;
+                rope_rotate2(a, b, make_float2(cs4.x, cs4.z), make_float2(cs4.y, cs4.w), xa, xb);
+                ra[k] = pack_bf16(xa.x, xa.y);
+                rb[k] = pack_bf16(xb.x, xb.y);
+            }
+            *pa = make_uint4(ra[0], ra[1], ra[2], ra[3]);
+            *pb = make_uint4(rb[0], rb[1], rb[2], rb[3]);
+        }
+    }
+}
+
+template <int DQK, int DV, bool V2, bool TRAIN, bool PAIRED, bool ROPE>
 __global__ void __launch_bounds__(384, 1)
     prefill_onepass(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
                     const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
@@ -146,6 +203,7 @@ __global__ void __launch_bounds__(384, 1)
                     const PrefillParams p) {
     using C = PreCfg<DQK, DV, V2>;
     static_assert(!PAIRED || (V2 && !TRAIN && DQK == DV), "paired heads: V2-shaped forward only");
+    static_assert(!ROPE || (V2 && !TRAIN && !PAIRED), "rotated Q tiles: V2 forward only");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -176,6 +234,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t bar_lam = bar_dr + 8;
     const uint32_t bar_stg = bar_lam + 8, bar_stf = bar_stg + 8;
     const uint32_t bar_dr2 = bar_stf + 8;              // drain of the second issuer
+    const uint32_t bar_qr = bar_dr2 + 8;               // Q tiles rotated (8 softmax warps)
     const uint32_t tslot = sbase + C::OFF_TSLOT;
     const uint32_t sQ1 = sbase + C::OFF_Q1, sQ2 = sbase + C::OFF_Q2;
     float *lam_smem = reinterpret_cast<float *>(smem + C::OFF_LAM);
@@ -203,6 +262,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(bar_stg, 8);
         mbar_init(bar_stf, 1);
         mbar_init(bar_dr2, 1);
+        mbar_init(bar_qr, 8);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -360,7 +420,8 @@ __global__ void __launch_bounds__(384, 1)
                 const int w = snake_tile(k, cta, G, NT);
                 if (w < 0) break;
                 const int n_kv = kv_tiles(n_qt - 1 - w / per_qt);
-                ok = mbar_wait(bar_qf, static_cast<uint32_t>(tc & 1), p.err) && wait_k();
+                // Q of this tile landed (and, with the rotary embedding, rotated in place)
+                ok = mbar_wait(ROPE ? bar_qr : bar_qf, static_cast<uint32_t>(tc & 1), p.err) && wait_k();
                 if (!ok) break;
                 tc_fence_after();
                 scores();
@@ -455,6 +516,30 @@ __global__ void __launch_bounds__(384, 1)
             lam_init = lam_smem[1];
         }
         int it = 0;
+        // Rotary embedding: the two softmax threads of a row turn half of the
+        // row's channel pairs each, in both Q tiles of work tile kk (query
+        // tile of work w), once the tiles have landed; the MMA thread issues
+        // the tile's first QK after all 8 warps have arrived.  Tile 0 is rotated before the first key tile,
+        // tile kk + 1 right after the last P of tile kk (its Q load was issued
+        // when the last QK of tile kk was), while the last PV runs.
+        auto rotate_q = [&](int kk, int w) {
+            if constexpr (ROPE) {
+                const int tq = (n_qt - 1 - w / per_qt) * C::BM + row;
+                ok = warp_wait(bar_qf, static_cast<uint32_t>(kk & 1), p.err, ok);
+                if (ok && tq < p.T) {
+                    RopeTab<DQK> tab;
+                    rope_tab_load<DQK>(tab, br, p.rope_cs + tq, p.T);
+                    rope_q_row<DQK>(smem + C::OFF_Q1, smem + C::OFF_Q2, row, br, tab);
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_qr);
+            }
+        };
+        if (ROPE) {
+            const int w0 = snake_tile(0, cta, G, NT);
+            if (w0 >= 0) rotate_q(0, w0);
+        }
         // Every softmax warp walks the same tile list and reaches the same
         // named barriers, also after an error (then it skips waits and work).
         for (int k = 0;; ++k) {
@@ -540,6 +625,10 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(my_p + 8);
+            }
+            if (ROPE) {
+                const int wn = snake_tile(k + 1, cta, G, NT);
+                if (wn >= 0) rotate_q(k + 1, wn);
             }
 
             // --------------------------------------------------- epilogue
@@ -677,7 +766,7 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int DQK, int DV, bool V2, bool TRAIN, bool PAIRED = false>
+template <int DQK, int DV, bool V2, bool TRAIN, bool PAIRED = false, bool ROPE = false>
 cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
     using C = PreCfg<DQK, DV, V2>;
     static unsigned long long attr_done = 0;   // one bit per device
@@ -686,10 +775,10 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
         // grants (384 threads x registers per thread), or its increase would
         // never complete: refuse to launch otherwise.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_onepass<DQK, DV, V2, TRAIN, PAIRED>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_onepass<DQK, DV, V2, TRAIN, PAIRED, ROPE>);
         if (e != cudaSuccess) return e;
         if (C::REG_SPLIT && fa.numRegs < C::REGS_NEEDED_AT_LAUNCH) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2, TRAIN, PAIRED>,
+        return cudaFuncSetAttribute(prefill_onepass<DQK, DV, V2, TRAIN, PAIRED, ROPE>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     });
     if (ea != cudaSuccess) return ea;
@@ -699,7 +788,7 @@ cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t 
     // persistent: one CTA per SM (shared memory and TMEM allow no more)
     if (p.num_sms < 1) return cudaErrorInvalidValue;
     const unsigned grid = static_cast<unsigned>(tiles < p.num_sms ? tiles : p.num_sms);
-    prefill_onepass<DQK, DV, V2, TRAIN, PAIRED><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, m.out, p);
+    prefill_onepass<DQK, DV, V2, TRAIN, PAIRED, ROPE><<<grid, 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v, m.out, p);
     return cudaGetLastError();
 }
 
@@ -727,6 +816,13 @@ cudaError_t launch_paired(const PrefillMaps &m, const PrefillParams &p, int d, c
     if (p.G != 2) return cudaErrorInvalidValue;   // kv coordinate = pair index
     if (d == 128) return launch_t<128, 128, true, false, true>(m, p, s);
     if (d == 64) return launch_t<64, 64, true, false, true>(m, p, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_v2_rope(const PrefillMaps &m, const PrefillParams &p, int d, cudaStream_t s) {
+    if (!p.rope_cs) return cudaErrorInvalidValue;
+    if (d == 128) return launch_t<128, 128, true, false, false, true>(m, p, s);
+    if (d == 64) return launch_t<64, 64, true, false, false, true>(m, p, s);
     return cudaErrorInvalidValue;
 }
 

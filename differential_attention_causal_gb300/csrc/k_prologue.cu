@@ -96,41 +96,57 @@ struct Vec8<float> {
     }
 };
 
-// Rotate every (token, head, 8-pair chunk) of q and k in tokens [t0, t0 + TS)
-// for heads [h0, h1) of the Hq + Hk (q heads first, then k heads).
-// freq_hi + freq_lo = base^(-2i/D) as two floats.  The angle pos * freq is
-// carried as a float pair (the product's rounding error recovered with an
-// fma) and reduced modulo 2 pi against 2 pi split into three floats, each
-// step an fma (Cody and Waite's additive reduction); the reduced angle is
-// within a few 1e-7 rad of the exact one for any position below 2^24.
-// The cos / sin table of the block's TS tokens is stored [token][k][chunk]
-// (entry i = 8 chunk + k at (token * 8 + k) * CH + chunk), so that the lanes
-// of a warp, which take consecutive chunks, read consecutive entries.
-template <typename E, int D>
-__device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0, int h0, int h1,
-                                            float2 *cs, const float *freq_hi, const float *freq_lo) {
-    constexpr int HALF = D / 2, CH = HALF / 8;
+// cos and sin of pos * (fhi + flo), fhi + flo = base^(-2i/D) as two floats.
+// The angle is carried as a float pair (the product's rounding error
+// recovered with an fma) and reduced modulo 2 pi against 2 pi split into
+// three floats, each step an fma (Cody and Waite's additive reduction); the
+// reduced angle is within a few 1e-7 rad of the exact one for any position
+// below 2^24.
+__device__ __forceinline__ float2 rope_cs(float pos, float fhi, float flo) {
     constexpr double TWO_PI = 6.283185307179586476925286766559;
     constexpr float P1 = static_cast<float>(TWO_PI);
     constexpr float P2 = static_cast<float>(TWO_PI - static_cast<double>(P1));
     constexpr float P3 = static_cast<float>(TWO_PI - static_cast<double>(P1) - static_cast<double>(P2));
     constexpr float INV_2PI = static_cast<float>(1.0 / TWO_PI);
+    const float hi = pos * fhi;
+    const float lo = fmaf(pos, flo, fmaf(pos, fhi, -hi));
+    const float k = rintf(hi * INV_2PI);
+    float r = fmaf(-k, P1, hi);
+    r = fmaf(-k, P2, r);
+    r = fmaf(-k, P3, r) + lo;
+    float c, sn;
+    sincosf(r, &sn, &c);
+    return make_float2(c, sn);
+}
+
+// base^(-2i/D) in double, kept as a float pair (i < D/2), into shared memory
+template <int D>
+__device__ __forceinline__ void rope_freqs(double base, float *freq_hi, float *freq_lo) {
+    for (int i = threadIdx.x; i < D / 2; i += blockDim.x) {
+        const double f = exp(-2.0 * static_cast<double>(i) / static_cast<double>(D) * log(base));
+        freq_hi[i] = static_cast<float>(f);
+        freq_lo[i] = static_cast<float>(f - static_cast<double>(freq_hi[i]));
+    }
+}
+
+// Rotate every (token, head, 8-pair chunk) of q and k in tokens [t0, t0 + TS)
+// for heads [h0, h1) of the Hq + Hk (q heads first, then k heads).  The cos /
+// sin table of the block's TS tokens is stored [token][k][chunk] (entry
+// i = 8 chunk + k at (token * 8 + k) * CH + chunk), so that the lanes of a
+// warp, which take consecutive chunks, read consecutive entries.
+template <typename E, int D>
+__device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0, int h0, int h1,
+                                            float2 *cs, const float *freq_hi, const float *freq_lo) {
+    constexpr int HALF = D / 2, CH = HALF / 8;
     const int64_t ntok = static_cast<int64_t>(p.B) * p.T;
     for (int e = threadIdx.x; e < TS * HALF; e += blockDim.x) {
         const int tt = e / HALF, i = e % HALF;
         const int64_t n = t0 + tt;
-        float c = 1.f, sn = 0.f;
-        if (n < ntok) {
-            const float pos = static_cast<float>(p.pos0 + n % p.T);
-            const float hi = pos * freq_hi[i];
-            const float lo = fmaf(pos, freq_lo[i], fmaf(pos, freq_hi[i], -hi));
-            const float k = rintf(hi * INV_2PI);
-            float r = fmaf(-k, P1, hi);
-            r = fmaf(-k, P2, r);
-            r = fmaf(-k, P3, r) + lo;
-            sincosf(r, &sn, &c);
-        }
-        cs[(tt * 8 + i % 8) * CH + i / 8] = make_float2(c, sn);
+        float2 csv = make_float2(1.f, 0.f);
+        if (n < ntok) csv = rope_cs(static_cast<float>(p.pos0 + n % p.T), freq_hi[i], freq_lo[i]);
+        cs[(tt * 8 + i % 8) * CH + i / 8] = csv;
+        if (p.cs_out && n < p.T)   // batch 0 writes the table
+            p.cs_out[(static_cast<int64_t>(i >> 1) * p.T + n) * 2 + (i & 1)] = csv;
     }
     __syncthreads();
     const int heads = h1 - h0;
@@ -168,8 +184,7 @@ __device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0,
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const float2 t = cs[(tt[j] * 8 + k) * CH + ch[j]];
-                ra[k] = fa[k] * t.x - fb[k] * t.y;
-                rb[k] = fb[k] * t.x + fa[k] * t.y;
+                rope_rotate(fa[k], fb[k], t.x, t.y, ra[k], rb[k]);
             }
             Vec8<E>::store(row[j] + 8 * ch[j], ra);
             Vec8<E>::store(row[j] + HALF + 8 * ch[j], rb);
@@ -315,12 +330,7 @@ __global__ void __launch_bounds__(256, 3) prologue_rope(const PrologueParams p) 
     constexpr int HALF = D / 2;
     __shared__ float2 cs[TS * HALF];
     __shared__ float freq_hi[HALF], freq_lo[HALF];
-    // base^(-2i/D) in double, once per CTA, kept as a float pair
-    for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-        const double f = exp(-2.0 * static_cast<double>(i) / static_cast<double>(D) * log(p.base));
-        freq_hi[i] = static_cast<float>(f);
-        freq_lo[i] = static_cast<float>(f - static_cast<double>(freq_hi[i]));
-    }
+    rope_freqs<D>(p.base, freq_hi, freq_lo);   // once per CTA
     __syncthreads();
     // persistent: the grid fills the GPU once and walks the token blocks
     const int64_t nblk = (static_cast<int64_t>(p.B) * p.T + TS - 1) / TS;
@@ -340,7 +350,7 @@ __global__ void __launch_bounds__(LT) prologue_lambda(const PrologueParams p) {
 template <typename E>
 cudaError_t launch_e(const PrologueParams &p, cudaStream_t s) {
     const int64_t ntok = static_cast<int64_t>(p.B) * p.T;
-    if (p.q || p.k) {
+    if (p.q || p.k || p.cs_out) {
         const int64_t blocks = (ntok + TS - 1) / TS;
         if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
         // three 256-thread CTAs per SM (the launch bound), one wave
@@ -383,5 +393,6 @@ bool prologue_supported(int D, int C, int P) {
 cudaError_t launch_prologue(const PrologueParams &p, bool bf16, cudaStream_t s) {
     return bf16 ? launch_e<__nv_bfloat16>(p, s) : launch_e<float>(p, s);
 }
+
 
 }  // namespace da

@@ -28,6 +28,8 @@
  *                       rule of the same definitions.
  *   diffattn_prologue   the neighbours before the attention: rotary embedding of
  *                       q and k, and V2's projected lambda logits.
+ *   diffattn_v2_fwd_rope  diffattn_v2_fwd with the rotary embedding folded in:
+ *                       q is rotated tile by tile inside the prefill kernel.
  *   diffattn_v1_fwd_host  the same DiffAttnV1 forward on host buffers, copies
  *                       overlapped with the forward (the end-to-end call).
  *   diffattn_paired_fwd modded-nanogpt pull request "New Record: Paired Head
@@ -156,6 +158,27 @@ da_status diffattn_v1_fwd_host(const void *q, const void *k, const void *v,
 da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const float *lam,
                           void *out, int B, int T, int Hq, int Hkv, int D,
                           da_dtype dtype, cudaStream_t stream);
+
+/* DIFF V2 forward with the rotary embedding of q and k folded in: the result
+ * of diffattn_prologue(q, k, ..., pos0, base) (rotate-half form, see there)
+ * followed by diffattn_v2_fwd, bit for bit, with q left as it is.
+ *   - k is rotated in place, as diffattn_prologue does, in a first launch that
+ *     also writes the cos / sin table `cs`;
+ *   - q is read once per query tile by the prefill kernel and each tile is
+ *     rotated in shared memory before its first product, so q is never
+ *     written back (the tile is loaded once per query tile, so this repeats
+ *     no work).
+ * Arguments as for diffattn_v2_fwd, plus
+ *   pos0, base : position of token t is pos0 + t; theta = pos * base^(-2i/D)
+ *   cs         : caller-owned device workspace of T * D floats (fp32), 16-byte
+ *                aligned; overwritten (the (cos, sin) pairs for the T positions),
+ *                read by the second launch, free once the call's work is done.
+ * Supported: DA_BF16, D in {64, 128} (DA_F32 returns DA_ERR_UNSUPPORTED_DIM).
+ * Errors as for the other entry points. */
+da_status diffattn_v2_fwd_rope(const void *q, void *k, const void *v, const float *lam,
+                               void *out, int B, int T, int Hq, int Hkv, int D,
+                               int64_t pos0, float base, float *cs,
+                               da_dtype dtype, cudaStream_t stream);
 
 /* Paired Head Attention, causal (modded-nanogpt pull request "New Record:
  * Paired Head Attention (-3.5s, -65 steps)", section "Updates in PR"): the k,
