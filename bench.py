@@ -197,16 +197,29 @@ def rank_seed(seed: int, rank: int) -> int:
     return seed + rank
 
 
+# NVTX: every timed step runs inside a range named after the measurement it
+# belongs to (set with section()), so a timeline profiler shows which launches
+# each number covers.  Without a profiler attached the ranges cost nothing.
+_SECTION = "bench"
+
+
+def section(name: str) -> None:
+    global _SECTION
+    _SECTION = name
+
+
 def time_steps(step, steps: int, flush: torch.Tensor | None):
     """Per-step device time (ms) with CUDA events on the current stream; the
     L2 flush (if any) runs between steps, outside the events."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b in evs:
+    for i, (a, b) in enumerate(evs):
         if flush is not None:
             flush.add_(1)
+        torch.cuda.nvtx.range_push(f"{_SECTION}: timed step {i}")
         a.record()
         step()
         b.record()
+        torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in evs]
 
@@ -260,6 +273,7 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    section(f"headline {HEADLINE}")
     times = time_steps(step, args.steps, flush)
     torch.cuda.synchronize()
     if world > 1:
@@ -295,6 +309,7 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
         e2e_step()
     torch.cuda.synchronize()
     e2e_steps = max(5, min(args.steps, 50))
+    section("e2e diffattn_v1_fwd_host")
     et = time_steps(e2e_step, e2e_steps, flush)
     h2d = sum(host[n].numel() * host[n].element_size() for n in host)
     d2h = hout.numel() * hout.element_size()
@@ -334,6 +349,7 @@ def run_ours(args, rank: int, world: int, dev: torch.device) -> dict | None:
 def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
     aux = {}
     flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    section("aux v1_fp32_tiny")
     # DIFF V1 fp32, the tiny parity workload: a latency figure (fp32 on CUDA cores), no roofline claim
     s = inputs.WORKLOADS["v1_fp32_B1_T64_H2_d32"]
     x = inputs.make_v1(s, seed=args.seed, device=dev)
@@ -347,6 +363,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                            "ms_min": round(min(t), 5), "launches": 1,
                            "note": "fp32 on CUDA cores; latency-bound, no roofline claim"}
     del x, out
+    section("aux v2_prefill")
     # DIFF V2 prefill
     s = inputs.WORKLOADS["v2_bf16_B8_T4096_Hq32_Hkv8_D128"]
     x = inputs.make_v2(s, seed=args.seed, device=dev)
@@ -361,6 +378,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                          "TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
                          "tokens_per_s": round(s.B * s.T / (ms * 1e-3)), "peak_kind": peak_kind}
     del x, out
+    section("aux v1_long")
     # DIFF V1 long context, d = 128 / dv = 256 (two-pass kernel)
     s = inputs.WORKLOADS["v1_bf16_B1_T32768_H12_d128"]
     x = inputs.make_v1(s, seed=args.seed, device=dev)
@@ -377,6 +395,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                       "tokens_per_s": round(s.B * s.T / (ms * 1e-3)), "kernel": "prefill_v1_twopass<128>",
                       "peak_kind": peak_kind}
     del x, out
+    section("aux v2_decode")
     # DIFF V2 decode (8.6 GB cache >> L2: no flush needed)
     s = inputs.WORKLOADS["v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128"]
     x = inputs.make_decode(s, seed=args.seed, device=dev)
@@ -394,6 +413,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                         "launches": 2, "peak_kind": peak_kind}
     del x, out, ws
     torch.cuda.empty_cache()
+    section("aux v2_decode_varlen")
     # DIFF V2 decode, per-sequence lengths uniform on 1..L (the same cache allocation)
     s = inputs.WORKLOADS["v2_decode_varlen_bf16_B64_L32768_Hq64_Hkv8_D128"]
     x = inputs.make_decode(s, seed=args.seed, device=dev)
@@ -414,6 +434,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                                "peak_kind": peak_kind}
     del x, out, ws
     torch.cuda.empty_cache()
+    section("aux v1_decode")
     # DIFF V1 decode, d = 128 (6.4 GB of k1, k2, v cache >> L2)
     s = inputs.WORKLOADS["v1_decode_bf16_B32_L16384_H12_d128"]
     x = inputs.make_v1_decode(s, seed=args.seed, device=dev)
@@ -432,6 +453,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                         "tokens_per_s": round(s.B / (ms * 1e-3)), "launches": 2, "peak_kind": peak_kind}
     del x, out, ws
     torch.cuda.empty_cache()
+    section("aux prologue")
     # prologue (rotary q, k in place + projected lambda) on the V2 prefill workload
     s = inputs.WORKLOADS["v2_bf16_B8_T4096_Hq32_Hkv8_D128"]
     x = inputs.make_v2(s, seed=args.seed, device=dev)
@@ -447,6 +469,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
     aux["prologue"] = {"workload": "v2_bf16_B8_T4096_Hq32_Hkv8_D128, x (B,T,2048), w (2048,16)", "ms": round(ms, 4),
                        "GB/s": round(gbs, 1), "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
                        "bytes": int(nbytes), "launches": 2, "peak_kind": peak_kind}
+    section("aux v2_prefill_with_prologue")
     # the V2 attention call with its prologue, two ways: rotary q, k + lambda
     # logits, then the prefill (3 launches), against lambda logits, then the
     # prefill with q rotated tile by tile inside it (k + table, prefill: 3 launches)
@@ -478,6 +501,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                 "v2_fwd_rope (k and the cos/sin table, then the prefill rotating each Q tile in shared memory)"}
     del x, lp, lam, out, cs
     torch.cuda.empty_cache()
+    section("aux paired_prefill")
     # Paired Head Attention (interleaved head pairs, one causal softmax) on the V2 prefill's query heads
     s = inputs.WORKLOADS["paired_bf16_B8_T4096_H32_D128"]
     x = inputs.make_paired(s, seed=args.seed, device=dev)
@@ -493,6 +517,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                              "launches": 1, "peak_kind": peak_kind}
     del x, out
     torch.cuda.empty_cache()
+    section("aux backward")
     # backward (training): DIFF V1 on the headline workload, DIFF V2 on the prefill workload
     s = inputs.WORKLOADS[HEADLINE]
     x = inputs.make_v1(s, seed=args.seed, device=dev)
@@ -514,6 +539,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
                           "flop_count": "28d per causal pair (two attention backwards)",
                           "fwd_train_ms": round(ms_ft, 4), "launches": 4, "peak_kind": peak_kind}
     del x, dout, saved, ws
+    section("aux v1_long_backward")
     # backward of the long-context DIFF V1 workload (d = 128, dv = 256: split kernels)
     s = inputs.WORKLOADS["v1_bf16_B1_T32768_H12_d128"]
     x = inputs.make_v1(s, seed=args.seed, device=dev)

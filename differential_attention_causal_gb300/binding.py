@@ -15,12 +15,14 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdiffattn.so")
+LIB_DEBUG_PATH = os.path.join(_HERE, "libdiffattn_debug.so")
 
 DA_F32, DA_BF16 = 0, 1
 STATUS = {
     0: "DA_OK", 1: "DA_ERR_NULL_PTR", 2: "DA_ERR_BAD_SHAPE", 3: "DA_ERR_UNSUPPORTED_DIM",
     4: "DA_ERR_BAD_GROUP", 5: "DA_ERR_MISALIGNED", 6: "DA_ERR_WORKSPACE_TOO_SMALL",
     7: "DA_ERR_CUDA", 8: "DA_ERR_BAD_DTYPE", 9: "DA_ERR_DEVICE_TIMEOUT", 10: "DA_ERR_SCRATCH_LIMIT",
+    11: "DA_ERR_BAD_LENGTH", 12: "DA_ERR_DEVICE_BOUNDS",
 }
 _lock = threading.Lock()
 _lib = None
@@ -101,8 +103,43 @@ def lib() -> ctypes.CDLL:
             L.diffattn_selftest_wait_limit.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
             L.diffattn_last_launch_count.restype = i32
             L.diffattn_last_launch_count.argtypes = []
+            L.diffattn_debug_checks.restype = i32
+            L.diffattn_debug_checks.argtypes = []
+            L.diffattn_selftest_bounds.restype = i32
+            L.diffattn_selftest_bounds.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
             _lib = L
     return _lib
+
+
+def use_library(debug: bool) -> str:
+    """Route the calls of this module to libdiffattn_debug.so (debug=True: the
+    kernels check the indices they write through, failures are reported as
+    DA_ERR_DEVICE_BOUNDS by the error-word calls) or to the release library.
+    Each library keeps its own error words.  Returns the path now in use."""
+    global _lib, LIB_PATH
+    with _lock:
+        path = LIB_DEBUG_PATH if debug else os.path.join(_HERE, "libdiffattn.so")
+        if path != LIB_PATH:
+            LIB_PATH = path
+            _lib = None
+    return LIB_PATH
+
+
+def debug_checks() -> bool:
+    """True if the library in use was built with the bounds checks."""
+    return bool(lib().diffattn_debug_checks())
+
+
+def selftest_bounds(stream=None) -> int:
+    """A warp tests an index past the end of a buffer through the kernels'
+    bounds check (the write is skipped in both builds).  Returns the raw error
+    word it left (debug build: the bounds bit; release: 0), cleared again;
+    raises if the result is not the one of the build."""
+    code = ctypes.c_uint32(0)
+    rc = lib().diffattn_selftest_bounds(ctypes.byref(code), _stream(stream))
+    if rc != 0:
+        raise DiffAttnError("diffattn_selftest_bounds", rc)
+    return int(code.value)
 
 
 def status_string(code: int) -> str:
@@ -128,10 +165,10 @@ def selftest_wait_limit(stream=None) -> int:
 
 def device_error() -> int:
     """Synchronise the device, then read and clear every stream's error word
-    (their OR; 0 = no kernel gave up)."""
+    (their OR; 0 = no kernel recorded anything)."""
     code = ctypes.c_uint32(0)
     rc = lib().diffattn_device_error(ctypes.byref(code))
-    if rc not in (0, 9, 11):
+    if rc not in (0, 9, 11, 12):
         raise DiffAttnError("diffattn_device_error", rc)
     return int(code.value)
 
@@ -141,7 +178,7 @@ def stream_error(stream=None) -> int:
     its error word (0 = no kernel on it gave up)."""
     code = ctypes.c_uint32(0)
     rc = lib().diffattn_stream_error(ctypes.byref(code), _stream(stream))
-    if rc not in (0, 9, 11):
+    if rc not in (0, 9, 11, 12):
         raise DiffAttnError("diffattn_stream_error", rc)
     return int(code.value)
 

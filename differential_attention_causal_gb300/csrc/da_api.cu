@@ -162,6 +162,7 @@ const char *diffattn_status_string(da_status s) {
             return "sizes need more decode scratch than the library's static 8 MiB buffer; "
                    "use diffattn_v2_decode with a workspace";
         case DA_ERR_BAD_LENGTH: return "a decode cache length was outside 1..L and was clamped";
+        case DA_ERR_DEVICE_BOUNDS: return "a bounds check of the debug build failed (the access was skipped)";
     }
     return "unknown status";
 }
@@ -170,7 +171,9 @@ int diffattn_last_launch_count(void) { return t_last_launches; }
 
 static da_status status_of_word(uint32_t v) {
     if (v == 0) return DA_OK;
-    if (v == kErrBadLength) return DA_ERR_BAD_LENGTH;
+    if (v & kErrFatal) return DA_ERR_DEVICE_TIMEOUT;
+    if (v & kErrBounds) return DA_ERR_DEVICE_BOUNDS;
+    if (v & kErrBadLength) return DA_ERR_BAD_LENGTH;
     return DA_ERR_DEVICE_TIMEOUT;
 }
 
@@ -218,6 +221,23 @@ da_status diffattn_selftest_wait_limit(uint32_t *code, cudaStream_t stream) {
     if (code) *code = v;
     t_last_launches = 1;
     return (gave_up && (v & kErrWaitTimeout) != 0) ? DA_OK : DA_ERR_CUDA;
+}
+
+int diffattn_debug_checks(void) { return kDebugChecks ? 1 : 0; }
+
+da_status diffattn_selftest_bounds(uint32_t *code, cudaStream_t stream) {
+    uint32_t *err = nullptr;
+    if (!device_state(stream, &err, nullptr)) return DA_ERR_CUDA;
+    uint32_t before = 0;
+    if (diffattn_stream_error(&before, stream) == DA_ERR_CUDA) return DA_ERR_CUDA;   // start from a clear word
+    bool wrote = true;
+    if (run_bounds_selftest(err, &wrote, stream) != cudaSuccess) return DA_ERR_CUDA;
+    uint32_t v = 0;
+    if (diffattn_stream_error(&v, stream) == DA_ERR_CUDA) return DA_ERR_CUDA;   // reads and clears the word
+    if (code) *code = v;
+    t_last_launches = 1;
+    if (wrote) return DA_ERR_CUDA;   // the write past the end must be skipped in both builds
+    return (kDebugChecks ? v == kErrBounds : v == 0) ? DA_OK : DA_ERR_CUDA;
 }
 
 da_status diffattn_v1_fwd(const void *q1, const void *q2, const void *k1, const void *k2, const void *v,
@@ -378,6 +398,7 @@ da_status diffattn_v2_fwd_rope(const void *q, void *k, const void *v, const floa
     r.pos0 = pos0;
     r.base = static_cast<double>(base);
     r.cs_out = reinterpret_cast<float2 *>(cs);
+    r.err = err;
     da_status st = cuda_status(launch_prologue(r, true, stream));
     if (st != DA_OK) return st;
     t_last_launches = 1;
@@ -935,6 +956,7 @@ da_status diffattn_v1_bwd(const void *q1, const void *q2, const void *k1, const 
     pp.dd = reinterpret_cast<float *>(ws);
     pp.cv = reinterpret_cast<float *>(ws + wl.off_c);
     pp.B = B; pp.T = T; pp.H = H; pp.d = d;
+    pp.err = err;
     BwdParams p{};
     p.dq1 = static_cast<__nv_bfloat16 *>(dq1); p.dq2 = static_cast<__nv_bfloat16 *>(dq2);
     p.dk1 = static_cast<__nv_bfloat16 *>(dk1); p.dk2 = static_cast<__nv_bfloat16 *>(dk2);
@@ -1032,6 +1054,7 @@ da_status diffattn_v2_bwd(const void *q, const void *k, const void *v, const flo
     pp.dd = reinterpret_cast<float *>(ws);
     pp.cv = reinterpret_cast<float *>(ws + wl.off_c);
     pp.B = B; pp.T = T; pp.H = P; pp.d = D;
+    pp.err = err;
     BwdParams p{};
     p.dq1 = p.dq2 = static_cast<__nv_bfloat16 *>(dq);
     p.dk1 = p.dk2 = static_cast<__nv_bfloat16 *>(dk);
@@ -1080,6 +1103,7 @@ extern "C" da_status diffattn_prologue(void *q, void *k, int B, int T, int Hq, i
     p.B = B; p.T = T;
     p.pos0 = pos0;
     p.base = static_cast<double>(base);
+    p.err = err;
     const da_status st = cuda_status(launch_prologue(p, dtype == DA_BF16, stream));
     if (st == DA_OK) t_last_launches = (Hq + Hk > 0 ? 1 : 0) + (x ? 1 : 0);
     return st;

@@ -20,6 +20,22 @@ namespace da {
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s of global time
 
+// Bounds checks of the debug build (compiled with -DDA_DEBUG_CHECKS): at the
+// places where a kernel writes memory through a computed index, DA_CHECK(cond,
+// err) tests the index against the extent of its tensor or tile; a failed
+// test records kErrBounds in the error word and yields false, and the caller
+// skips the access.  Nothing traps.  In the release build DA_CHECK is the
+// constant true and the test is not compiled.
+#ifdef DA_DEBUG_CHECKS
+__device__ __forceinline__ bool da_check(bool c, uint32_t *err) {
+    if (!c && err) atomicOr(err, kErrBounds);
+    return c;
+}
+#define DA_CHECK(cond, err) ::da::da_check((cond), (err))
+#else
+#define DA_CHECK(cond, err) true
+#endif
+
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -14,8 +14,16 @@ enum : uint32_t {
     kErrWaitTimeout = 1u,      // a bounded mbarrier wait gave up
     kErrAborted = 2u,          // a kernel saw an earlier error and returned early
     kErrBadLength = 4u,        // a decode cache length outside 1 .. L (clamped)
+    kErrBounds = 8u,           // debug builds: an index failed its bounds check (access skipped)
     kErrFatal = kErrWaitTimeout | kErrAborted,   // bits after which kernels stop waiting
 };
+
+// Built with the debug bounds checks (-DDA_DEBUG_CHECKS, libdiffattn_debug.so).
+#ifdef DA_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
 
 // Runs set() once per device and remembers success in one bit of *done.
 // Kernel attributes such as the dynamic shared-memory opt-in belong to the
@@ -152,6 +160,7 @@ struct BwdPreParams {
     __nv_bfloat16 *g;                            // V1 g_1 = dx, (B, T, H, DV) contiguous
     float *dd, *cv;                              // outputs D (2, B, H, T); c (B, H, T)
     int B, T, H, d;
+    uint32_t *err;                               // error word (debug bounds checks)
 };
 struct BwdMaps {
     CUtensorMap q1r, q2r, gr, k1c, k2c, vc;      // dQ kernel: 128-row Q / G boxes, 64-row K / V boxes
@@ -161,6 +170,9 @@ bool backward_supported(int dqk, int dv, bool v2);
 // One warp waits on an mbarrier phase nothing completes (the bounded-wait
 // failure path); *gave_up is true once the wait gave up as designed.
 cudaError_t run_wait_selftest(uint32_t *err, bool *gave_up, cudaStream_t s);
+// One warp tests index 32 of a 32-entry buffer through DA_CHECK; *wrote says
+// whether any write reached the buffer (it must not, in either build).
+cudaError_t run_bounds_selftest(uint32_t *err, bool *wrote, cudaStream_t s);
 // dL/dlam summed from the per-row shares in pp.dlam_rows, then the four
 // lambda-vector gradients (one CTA; used by the bf16 and the fp32 backward).
 cudaError_t launch_bwd_lambda(const BwdPreParams &pp, cudaStream_t s);
@@ -200,6 +212,7 @@ struct PrologueParams {
     int B, T;
     int64_t pos0;                  // position of token t is pos0 + t
     double base;
+    uint32_t *err;                 // error word (debug bounds checks)
     float2 *cs_out;                // optional: the (cos, sin) the rotation applies at token t to
                                    // pair i, at cs_out[((i / 2) * T + t) * 2 + i % 2], so that
                                    // pairs 2j, 2j + 1 of a token are one 16-byte entry (batch 0

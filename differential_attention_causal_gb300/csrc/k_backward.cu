@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 uint32_t a[32];
                 tmem_ld32(tmem + lane_off + acol + ch0 + c0, a);
                 tmem_wait_ld();
-                if (live) {
+                if (live && DA_CHECK(b < p.B && ch0 + c0 + 32 <= DQK, p.err)) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
 #pragma unroll
                     for (int q8 = 0; q8 < 4; ++q8) {
@@ -872,7 +872,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                     uint32_t a[32];
                     tmem_ld32(tmem + lane_off + col + c0, a);
                     tmem_wait_ld();
-                    if (live) {
+                    if (live && DA_CHECK(b < p.B && col + c0 + 32 <= static_cast<int>(C::TMEM_COLS), p.err)) {
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
 #pragma unroll
                         for (int q8 = 0; q8 < 4; ++q8) {
@@ -945,6 +945,7 @@ __global__ void __launch_bounds__(256) bwd_pre(const BwdPreParams p) {
     const int h = static_cast<int>(r % p.H);
     const int t = static_cast<int>((r / p.H) % p.T);
     const int b = static_cast<int>(r / (static_cast<int64_t>(p.H) * p.T));
+    if (!DA_CHECK(b < p.B && t < p.T && h < p.H, p.err)) return;   // warp-uniform
     const __nv_bfloat16 *go = p.dout + b * p.o_sb + static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh;
     // V2: x1, x2 = a_e, a_o (bf16 saved); V1: x1 = x (RMSNorm input), x2 = a2 (fp32 saved).
     // Lane l owns the PER consecutive channels l * PER .. (one vector load per tensor).

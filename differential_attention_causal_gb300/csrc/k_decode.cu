@@ -247,7 +247,9 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         named_bar_sync(1, 32 * C::NCW);
         const int tid = w * 32 + lane;
         float *dst = p.ws + (bg + blockIdx.x) * C::SLOT;
-        for (int e = tid; e < D * 8; e += 32 * C::NCW) {
+        // the partial slots: B * Hkv + grid - 1
+        const bool in_ws = DA_CHECK(bg + blockIdx.x < static_cast<int64_t>(p.B) * p.Hkv + p.grid - 1, p.err);
+        for (int e = tid; in_ws && e < D * 8; e += 32 * C::NCW) {
             const int n = e & 7, dd = e >> 3;
             float M = -INFINITY;
 #pragma unroll
@@ -261,7 +263,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             }
             dst[n * D + dd] = acc;
         }
-        if (tid < 8) {
+        if (tid < 8 && in_ws) {
             float M = -INFINITY;
 #pragma unroll
             for (int ww = 0; ww < C::NCW; ++ww) M = fmaxf(M, xw[ww * (C::XW / 4) + D * 8 + tid]);
@@ -485,11 +487,13 @@ __global__ void __launch_bounds__(D) decode_combine(const DecodeParams p) {
         // RMSNorm over the 2d channels (those past p.dv are zero), eps 1e-5, no
         // weight; then (1 - lam_init)
         y = x * ((1.f - lam_init) / sqrtf(ss / static_cast<float>(p.dv) + 1e-5f));
-        if (dd < p.dv) p.out[static_cast<int64_t>(blockIdx.x) * p.dv + dd] = __float2bfloat16_rn(y);
+        if (dd < p.dv && DA_CHECK(blockIdx.x < static_cast<int64_t>(p.B) * p.Hq, p.err))
+            p.out[static_cast<int64_t>(blockIdx.x) * p.dv + dd] = __float2bfloat16_rn(y);
     } else {
         const float sg = 1.f / (1.f + __expf(-p.lam[blockIdx.x]));
         y = Oe / Le - sg * (Oo / Lo);
-        p.out[static_cast<int64_t>(blockIdx.x) * D + dd] = __float2bfloat16_rn(y);
+        if (DA_CHECK(blockIdx.x < static_cast<int64_t>(p.B) * (p.Hq / 2), p.err))
+            p.out[static_cast<int64_t>(blockIdx.x) * D + dd] = __float2bfloat16_rn(y);
     }
 }
 

@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(384, 1)
                 const int qt = n_qt - 1 - w / per_qt, rest = w % per_qt;
                 const int h = rest % p.H, b = rest / p.H;
                 ok = ok && mbar_wait(bar_stg, static_cast<uint32_t>(k & 1), p.err);
-                if (ok) {
+                if (ok && DA_CHECK(qt * C::BM < p.T && h < p.H && b < p.B, p.err)) {
 #pragma unroll
                     for (int bx = 0; bx < C::VB; ++bx)
                         tma_store_4d(&tout, sbase + C::OFF_OUT + bx * C::BOX, 64 * bx, h, qt * C::BM, b);
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(384, 1)
             if constexpr (ROPE) {
                 const int tq = (n_qt - 1 - w / per_qt) * C::BM + row;
                 ok = warp_wait(bar_qf, static_cast<uint32_t>(kk & 1), p.err, ok);
-                if (ok && tq < p.T) {
+                if (ok && tq < p.T && DA_CHECK(row < C::BM, p.err)) {
                     RopeTab<DQK> tab;
                     rope_tab_load<DQK>(tab, br, p.rope_cs + tq, p.T);
                     rope_q_row<DQK>(smem + C::OFF_Q1, smem + C::OFF_Q2, row, br, tab);
@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(384, 1)
                     uint32_t a[32];
                     tmem_ld32(tO + cc, a);
                     tmem_wait_ld();
-                    if (ok && t < p.T) {
+                    if (ok && t < p.T && DA_CHECK(2 * h + br < 2 * p.H && b < p.B && cc + 32 <= DV, p.err)) {
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc);
 #pragma unroll
                         for (int q8 = 0; q8 < 4; ++q8) {
@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(384, 1)
             ok = warp_wait(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
             if (k > 0) ok = warp_wait(bar_stf, static_cast<uint32_t>((k - 1) & 1), p.err, ok);
             tc_fence_after();
-            if (TRAIN && t < p.T)   // this branch's log-sum-exp (log2 units) for the backward
+            if (TRAIN && t < p.T && DA_CHECK(b < p.B && h < p.H, p.err))   // this branch's log-sum-exp (log2 units) for the backward
                 p.slse[((static_cast<int64_t>(br) * p.B + b) * p.H + h) * p.T + t] = m_ref + __log2f(l);
             xch[br * 128 + row] = l;
             named_bar_sync(1, 256);   // both branches' final O are complete past this point
@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(384, 1)
                     x[cc + kk] = v;
                     ss = fmaf(v, v, ss);
                 }
-                if (TRAIN && !V2 && t < p.T) {
+                if (TRAIN && !V2 && t < p.T && DA_CHECK(b < p.B && h < p.H && col0 + cc + 32 <= DV, p.err)) {
                     // V1: x (the RMSNorm input) and a2 = O2 / l2 in fp32, channels col0 + cc .. + 31
                     const float i2 = 1.f / l2;
                     const int64_t off = ((static_cast<int64_t>(b) * p.T + t) * p.H + h) * DV + col0 + cc;
@@ -702,7 +702,7 @@ __global__ void __launch_bounds__(384, 1)
                                              __uint_as_float(bb[4 * q4 + 3]) * i2);
                     }
                 }
-                if (TRAIN && V2 && t < p.T) {
+                if (TRAIN && V2 && t < p.T && DA_CHECK(b < p.B && h < p.H && col0 + cc + 32 <= DV, p.err)) {
                     // V2: a_b = O_b / l_b of this row's channels col0 + cc .. + 31, both heads, bf16
                     const float i2 = 1.f / l2;
                     const int64_t off = ((static_cast<int64_t>(b) * p.T + t) * p.H + h) * DV + col0 + cc;
@@ -741,6 +741,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int kk = 0; kk < HALF; kk += 8) {
                 const int col = col0 + kk, ch = (col & 63) >> 3;
+                if (!DA_CHECK((col >> 6) * C::BOX + row * 128 + 16 * ch + 16 <= C::OUT_TILE, p.err)) continue;
                 uint4 v;
                 v.x = pack_bf16(x[kk], x[kk + 1]);
                 v.y = pack_bf16(x[kk + 2], x[kk + 3]);

@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(384, 1)
         ok = warp_wait(bar_lam, 0, p.err, ok);
         const float lam = lam_smem[0], lam_init = lam_smem[1];
         const bool a2_run = TRAIN && p.train_run == 2;
-        if (TRAIN && !a2_run && t < p.T)   // this branch's log-sum-exp for the backward
+        if (TRAIN && !a2_run && t < p.T && DA_CHECK(b < p.B && h < p.H, p.err))   // this branch's log-sum-exp
             p.slse[((static_cast<int64_t>(br) * p.B + b) * p.H + h) * p.T + t] = m + __log2f(l);
         // P = c1 e1 - c2 e2: x = a1 - lam a2, or a2 alone (c1 = 0, c2 = -1 / l2)
         const float c1 = a2_run ? 0.f : 1.f / l1, c2 = a2_run ? -1.f / l2 : lam / l2;
@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(384, 1)
                 ss = fmaf(x[cc0 + k], x[cc0 + k], ss);
             }
         }
-        if (TRAIN && ok && t < p.T) {
+        if (TRAIN && ok && t < p.T && DA_CHECK(b < p.B && h < p.H && col0 + HALF <= C::DV, p.err)) {
             // x (run 1) or a2 (run 2), fp32, this warpgroup's half of the channels
             float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(a2_run ? p.sa2 : p.sa1) +
                                                     ((static_cast<int64_t>(b) * p.T + t) * p.H + h) * C::DV + col0);
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(384, 1)
         named_bar_sync(1, 256);
         const float ms = (xch[row] + xch[128 + row]) * (1.f / static_cast<float>(C::DV));
         const float r = (1.f - lam_init) * rsqrtf(ms + 1e-5f);
-        if (ok && t < p.T && !a2_run) {
+        if (ok && t < p.T && !a2_run && DA_CHECK(b < p.B && h < p.H && col0 + HALF <= C::DV, p.err)) {
             __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + static_cast<int64_t>(b) * p.o_sb +
                                  static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh + col0;
 #pragma unroll

@@ -145,7 +145,7 @@ __device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0,
         float2 csv = make_float2(1.f, 0.f);
         if (n < ntok) csv = rope_cs(static_cast<float>(p.pos0 + n % p.T), freq_hi[i], freq_lo[i]);
         cs[(tt * 8 + i % 8) * CH + i / 8] = csv;
-        if (p.cs_out && n < p.T)   // batch 0 writes the table
+        if (p.cs_out && n < p.T && DA_CHECK(i < HALF, p.err))   // batch 0 writes the table
             p.cs_out[(static_cast<int64_t>(i >> 1) * p.T + n) * 2 + (i & 1)] = csv;
     }
     __syncthreads();
@@ -168,7 +168,8 @@ __device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0,
             const int hh = h0 + (u / CH) % heads;
             tt[j] = u / (CH * heads);
             const int64_t n = t0 + tt[j];
-            if (u < units && n < ntok && (hh < p.Hq ? p.q != nullptr : p.k != nullptr)) {
+            if (u < units && n < ntok && (hh < p.Hq ? p.q != nullptr : p.k != nullptr) &&
+                DA_CHECK(hh < p.Hq + p.Hk && 8 * ch[j] + 8 <= HALF, p.err)) {
                 row[j] = hh < p.Hq ? static_cast<E *>(p.q) + (n * p.Hq + hh) * D
                                    : static_cast<E *>(p.k) + (n * p.Hk + (hh - p.Hq)) * D;
                 a[j] = Vec8<E>::ld(row[j] + 8 * ch[j]);
@@ -279,6 +280,7 @@ __device__ __forceinline__ void lambda_bf16(const PrologueParams &p, int64_t tok
         if (8 * j < p.P) {
             const int col = 8 * j + 2 * t4;
             const int64_t n0 = tok0 + 16 * warp + g, n1 = n0 + 8;
+            if (!DA_CHECK(col + 2 <= p.P, p.err)) continue;
             if (n0 < ntok) *reinterpret_cast<float2 *>(p.lam + n0 * p.P + col) = make_float2(acc[j][0], acc[j][1]);
             if (n1 < ntok) *reinterpret_cast<float2 *>(p.lam + n1 * p.P + col) = make_float2(acc[j][2], acc[j][3]);
         }

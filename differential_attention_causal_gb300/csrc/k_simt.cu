@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
     const int h = static_cast<int>(row % p.H);
     const int t = static_cast<int>((row / p.H) % p.Tq);
     const int b = static_cast<int>(row / (static_cast<int64_t>(p.H) * p.Tq));
+    if (!DA_CHECK(b < p.B && t < p.Tq && h < p.H, p.err)) return;
 
     // Head selection: V1 diff head h reads q1/k1 and q2/k2 at head h and v at
     // head h; V2 pair h reads query heads 2h (kept) and 2h+1 (subtracted) and

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(128) bwd_simt_pre(const SimtBwdParams p) {
     const int h = static_cast<int>(r % p.H);
     const int t = static_cast<int>((r / p.H) % p.T);
     const int b = static_cast<int>(r / (static_cast<int64_t>(p.H) * p.T));
+    if (!DA_CHECK(b < p.B && t < p.T && h < p.H, p.err)) return;
     const float *go = p.dout + b * p.o_sb + static_cast<int64_t>(t) * p.o_st + static_cast<int64_t>(h) * p.o_sh;
     const int64_t vi = (static_cast<int64_t>(b) * p.H + h) * p.T + t;
     float x1[NV], x2[NV], dy[NV];
@@ -116,6 +117,7 @@ __global__ void __launch_bounds__(128) bwd_simt_dq(const SimtBwdParams p) {
     const int h = static_cast<int>(r % p.H);
     const int t = static_cast<int>((r / p.H) % p.T);
     const int b = static_cast<int>(r / (static_cast<int64_t>(p.H) * p.T));
+    if (!DA_CHECK(b < p.B && t < p.T && h < p.H, p.err)) return;
     const bool v2 = p.mode == 2;
     const int hq1 = v2 ? 2 * h : h, hq2 = v2 ? 2 * h + 1 : h, hk = v2 ? (2 * h) / p.G : h;
     const float scale = rsqrtf(static_cast<float>(DQK));
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(128) bwd_simt_dkdv(const SimtBwdParams p) {
     const int hk = static_cast<int>(r % nh);
     const int j = static_cast<int>((r / nh) % p.T);
     const int b = static_cast<int>(r / (static_cast<int64_t>(nh) * p.T));
+    if (!DA_CHECK(b < p.B && j < p.T && hk < nh, p.err)) return;
     const float scale = rsqrtf(static_cast<float>(DQK));
     const int64_t vrows = static_cast<int64_t>(p.B) * p.H * p.T;
     const float *kj1 = p.k1 + b * p.k_sb + static_cast<int64_t>(j) * p.k_st + static_cast<int64_t>(hk) * p.k_sh;

@@ -90,8 +90,10 @@ typedef enum {
     DA_ERR_DEVICE_TIMEOUT = 9,    /* reported by diffattn_device_error()               */
     DA_ERR_SCRATCH_LIMIT = 10,    /* the call needs more scratch than the library's     */
                                   /* static buffer holds (diffattn_v2_decode_noalloc)  */
-    DA_ERR_BAD_LENGTH = 11        /* reported by diffattn_device_error(): a decode     */
+    DA_ERR_BAD_LENGTH = 11,       /* reported by diffattn_device_error(): a decode     */
                                   /* cache length was outside 1..L (it was clamped)    */
+    DA_ERR_DEVICE_BOUNDS = 12     /* reported by the error-word calls of the debug     */
+                                  /* build: an index failed its bounds check            */
 } da_status;
 
 typedef enum { DA_F32 = 0, DA_BF16 = 1 } da_dtype;
@@ -391,8 +393,9 @@ const char *diffattn_status_string(da_status s);
  * then reads and clears every stream's word and returns their OR.
  * *code (may be NULL) receives the raw word (0 = no error).  Both return
  * DA_OK if the word was 0, DA_ERR_DEVICE_TIMEOUT if a kernel recorded a
- * give-up, DA_ERR_BAD_LENGTH if the only record is a decode cache length
- * outside 1..L, DA_ERR_CUDA if the synchronisation or the read failed. */
+ * give-up, else DA_ERR_DEVICE_BOUNDS if a bounds check of the debug build
+ * failed, else DA_ERR_BAD_LENGTH if the record is a decode cache length
+ * outside 1..L; DA_ERR_CUDA if the synchronisation or the read failed. */
 da_status diffattn_stream_error(uint32_t *code, cudaStream_t stream);
 da_status diffattn_device_error(uint32_t *code);
 
@@ -406,6 +409,27 @@ da_status diffattn_device_error(uint32_t *code);
  * error recorded on `stream` before the call is cleared first.  Takes about
  * 2 s.  Run one self-test at a time per device. */
 da_status diffattn_selftest_wait_limit(uint32_t *code, cudaStream_t stream);
+
+/* Debug build.  libdiffattn_debug.so is the same library compiled with
+ * DA_DEBUG_CHECKS: every kernel tests the indices through which it writes
+ * memory (output rows, channels, heads and batch entries against the call's
+ * sizes; partial slots against the workspace; shared-memory staging offsets
+ * against the tile; TMEM columns against the allocation) before the access.
+ * A failed test skips the access and records a bit in the stream's error
+ * word, which diffattn_stream_error / diffattn_device_error report as
+ * DA_ERR_DEVICE_BOUNDS; nothing traps.  (No tool of the image checks device
+ * memory accesses on this system, so this build stands in for one.)
+ *
+ * diffattn_debug_checks returns 1 in the debug build and 0 in the release
+ * build.  diffattn_selftest_bounds launches one warp that tests an index one
+ * past the end of a 32-entry buffer through the same check (the write is
+ * skipped), then reads and clears the error word of `stream` (raw value into
+ * *code, may be NULL).  Debug build: DA_OK when the bit was recorded.
+ * Release build: DA_OK with a zero word (the check is compiled out).
+ * DA_ERR_CUDA if a launch or copy failed or the result is not the one of
+ * the build. */
+int diffattn_debug_checks(void);
+da_status diffattn_selftest_bounds(uint32_t *code, cudaStream_t stream);
 
 /* Number of kernel launches the last successful call on this host thread
  * enqueued (launch accounting for benchmarks). */

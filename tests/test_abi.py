@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     from differential_attention_causal_gb300 import binding
-    for code in range(12):
+    for code in range(13):
         s = binding.status_string(code)
         assert isinstance(s, str) and s
     assert binding.status_string(0) == "ok"
@@ -207,3 +207,21 @@ def test_v2_decode_varlen_argument_checks(lib):
     assert call(D=96) == 3
     assert call(k=A + 4) == 5
     assert call(dtype=9) == 8
+
+
+def test_debug_library_builds_and_exports_the_same_symbols(lib):
+    """The debug build (-DDA_DEBUG_CHECKS: bounds checks in every kernel that
+    writes through a computed index) links, exports every declared symbol and
+    says which build it is; the release build says it has no checks.  Both
+    answers are plain host calls, no GPU needed."""
+    from differential_attention_causal_gb300 import build as b
+    path = b.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (diffattn_\w+)", out))
+    for n in declared_functions():
+        assert n in exported, n
+    dbg = ctypes.CDLL(path)
+    assert dbg.diffattn_debug_checks() == 1
+    assert lib.diffattn_debug_checks() == 0
+    dbg.diffattn_status_string.restype = ctypes.c_char_p
+    assert b"bounds" in dbg.diffattn_status_string(12)
