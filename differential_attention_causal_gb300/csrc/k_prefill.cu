@@ -287,6 +287,9 @@ __global__ void __launch_bounds__(384, 1)
             }
             int kc = 0, vc = 0, tc = 0;   // ring and tile counters (the MMA warp keeps the same)
             bool ok = true;
+            // Q tiles are read once; K and V tiles are read again by the other
+            // query tiles of their head (from L2, if they are kept there)
+            const uint64_t pol_once = l2_evict_first(), pol_reuse = l2_evict_last();
             auto load_k = [&](int j, int hk, int b) -> bool {
                 const int st = kc % C::KS;
                 if (kc >= C::KS &&
@@ -299,9 +302,10 @@ __global__ void __launch_bounds__(384, 1)
                     if (PAIRED)   // 64 tokens x both heads of pair hk, interleaved
                         tma_load_5d(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, 0, hk, j * (C::BN / 2), b);
                     else
-                        tma_load_4d(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
+                        tma_load_4d_hint(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b, pol_reuse);
                     if (!V2)
-                        tma_load_4d(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b);
+                        tma_load_4d_hint(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b,
+                                         pol_reuse);
                 }
                 ++kc;
                 return true;
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(384, 1)
                     if (PAIRED)
                         tma_load_5d(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, 0, hk, j * (C::BN / 2), b);
                     else
-                        tma_load_4d(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b);
+                        tma_load_4d_hint(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b, pol_reuse);
                 }
                 ++vc;
                 return true;
@@ -335,8 +339,8 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_arrive_expect_tx(bar_qf, 2 * C::Q_TILE);
 #pragma unroll
                 for (int c = 0; c < C::QB; ++c) {
-                    tma_load_4d(sQ1 + c * C::BOX, &tq1, bar_qf, 64 * c, hq1, qt * C::BM, b);
-                    tma_load_4d(sQ2 + c * C::BOX, &tq2, bar_qf, 64 * c, hq2, qt * C::BM, b);
+                    tma_load_4d_hint(sQ1 + c * C::BOX, &tq1, bar_qf, 64 * c, hq1, qt * C::BM, b, pol_once);
+                    tma_load_4d_hint(sQ2 + c * C::BOX, &tq2, bar_qf, 64 * c, hq2, qt * C::BM, b, pol_once);
                 }
                 ++tc;
                 // consumption order: K0, (V_j, K_j+1) ...
@@ -479,6 +483,7 @@ __global__ void __launch_bounds__(384, 1)
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
         if (lane == 0 && !PAIRED) {
             bool ok = true;
+            const uint64_t pol_once = l2_evict_first();   // the output is written once
             for (int k = 0;; ++k) {
                 const int w = snake_tile(k, cta, G, NT);
                 if (w < 0) break;
@@ -488,7 +493,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (ok && DA_CHECK(qt * C::BM < p.T && h < p.H && b < p.B, p.err)) {
 #pragma unroll
                     for (int bx = 0; bx < C::VB; ++bx)
-                        tma_store_4d(&tout, sbase + C::OFF_OUT + bx * C::BOX, 64 * bx, h, qt * C::BM, b);
+                        tma_store_4d_hint(&tout, sbase + C::OFF_OUT + bx * C::BOX, 64 * bx, h, qt * C::BM, b, pol_once);
                     bulk_commit();
                 }
                 bulk_wait_read_all();
