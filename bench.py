@@ -474,7 +474,6 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
     # logits, then the prefill (3 launches), against lambda logits, then the
     # prefill with q rotated tile by tile inside it (k + table, prefill: 3 launches)
     out = torch.empty((s.B, s.T, s.Hq // 2, s.D), dtype=torch.bfloat16, device=dev)
-    cs = torch.empty(s.T * s.D, dtype=torch.float32, device=dev)
 
     def two_call():
         binding.prologue(q=x["q"], k=x["k"], x=lp["x"], w_lam=lp["w_lam"], lam=lam)
@@ -482,7 +481,7 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
 
     def fused():
         binding.prologue(x=lp["x"], w_lam=lp["w_lam"], lam=lam)
-        binding.v2_fwd_rope(x["q"], x["k"], x["v"], lam, out=out, cs=cs)
+        binding.v2_fwd_rope(x["q"], x["k"], x["v"], lam, out=out)
 
     res = {}
     for name, fn in (("two_call", two_call), ("fused", fused)):
@@ -498,8 +497,8 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
         "saved_ms_median": round(res["two_call"][1] - res["fused"][1], 4),
         "fused_attention_TFLOP/s_incl_prologue": round(tf, 1), "launches": 3,
         "note": "two_call: prologue (rotary q, k; lambda logits) + v2_fwd; fused: lambda logits + "
-                "v2_fwd_rope (k and the cos/sin table, then the prefill rotating each Q tile in shared memory)"}
-    del x, lp, lam, out, cs
+                "v2_fwd_rope (rotary k, then the prefill rotating each Q tile in shared memory)"}
+    del x, lp, lam, out
     torch.cuda.empty_cache()
     section("aux paired_prefill")
     # Paired Head Attention (interleaved head pairs, one causal softmax) on the V2 prefill's query heads
@@ -760,6 +759,9 @@ CASES = {
     "v1": ("v1", "v1_bf16_B4_T2048_H16_d64"),
     "v1_long": ("v1", "v1_bf16_B1_T32768_H12_d128"),
     "v2": ("v2", "v2_bf16_B8_T4096_Hq32_Hkv8_D128"),
+    # the V2 forward with the rotary embedding folded in, on a quarter of the
+    # prefill batch (profiler-sized): rotary k, then the prefill
+    "v2_rope_b2": ("v2_rope", None),
     "decode": ("decode", "v2_decode_bf16_B64_L32768_Hq64_Hkv8_D128"),
     # the decode workload with 8 of its 64 sequences: 1.07 GB of cache, small
     # enough for multi-pass profiler captures, still far larger than L2
@@ -847,7 +849,7 @@ def run_case(name: str, launches: int):
     dev = torch.device("cuda", 0)
     if wl:
         s = inputs.WORKLOADS[wl]
-    elif kind == "v2_bwd":
+    elif kind in ("v2_bwd", "v2_rope"):
         s = inputs.V2Shape(2, 4096, 32, 8, 128, "bf16")
     elif kind == "v1_bwd":
         s = inputs.V1Shape(1, 8192, 12, 128, 27, "bf16")
@@ -865,6 +867,8 @@ def run_case(name: str, launches: int):
                                    x["lam_q2"], x["lam_k2"], s.layer_index)
     elif kind == "v2":
         f = lambda: binding.v2_fwd(x["q"], x["k"], x["v"], x["lam"])  # noqa: E731
+    elif kind == "v2_rope":
+        f = lambda: binding.v2_fwd_rope(x["q"], x["k"], x["v"], x["lam"])  # noqa: E731
     elif kind == "paired":
         f = lambda: binding.paired_fwd(x["q"], x["k"], x["v"])  # noqa: E731
     elif kind == "decode_varlen":

@@ -55,7 +55,7 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v1_fwd_host.argtypes = ([vp, vp, vp, fp, fp, fp, fp, vp] + [i32] * 5
                                                + [vp, ctypes.c_size_t, i32, vp])
             L.diffattn_v2_fwd_rope.restype = i32
-            L.diffattn_v2_fwd_rope.argtypes = ([vp, vp, vp, fp, vp] + [i32] * 5 + [i64, ctypes.c_float, fp]
+            L.diffattn_v2_fwd_rope.argtypes = ([vp, vp, vp, fp, vp] + [i32] * 5 + [i64, ctypes.c_float]
                                                + [i32, vp])
             L.diffattn_paired_fwd.restype = i32
             L.diffattn_paired_fwd.argtypes = [vp, vp, vp, vp] + [i32] * 4 + [i32, vp]
@@ -265,13 +265,12 @@ def v2_fwd(q, k, v, lam, out: torch.Tensor | None = None, stream=None) -> torch.
 
 
 def v2_fwd_rope(q, k, v, lam, pos0: int = 0, base: float = 10000.0, out: torch.Tensor | None = None,
-                cs: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                stream=None) -> torch.Tensor:
     """DIFF V2 causal prefill of rotary-embedded q and k: the same result as
     prologue(q, k, pos0, base) followed by v2_fwd, with q left unchanged (its
     tiles are rotated inside the prefill kernel) and k rotated in place.
 
-    Shapes as for v2_fwd (bf16); cs is an optional fp32 workspace of T * D
-    elements (allocated here if None).  Returns out."""
+    Shapes as for v2_fwd (bf16).  Returns out."""
     for n, t in (("q", q), ("k", k), ("v", v), ("lam", lam)):
         _cuda(t, n)
         if not t.is_contiguous():
@@ -282,13 +281,8 @@ def v2_fwd_rope(q, k, v, lam, pos0: int = 0, base: float = 10000.0, out: torch.T
     Hkv = k.shape[2]
     if out is None:
         out = torch.empty((B, T, Hq // 2, D), dtype=q.dtype, device=q.device)
-    if cs is None:
-        cs = torch.empty(T * D, dtype=torch.float32, device=q.device)
-    elif cs.dtype != torch.float32 or cs.numel() < T * D or not cs.is_contiguous():
-        raise ValueError("cs must be a contiguous fp32 tensor of at least T * D elements")
     rc = lib().diffattn_v2_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), lam.data_ptr(), out.data_ptr(),
-                                    B, T, Hq, Hkv, D, int(pos0), float(base), cs.data_ptr(),
-                                    _dtype_code(q), _stream(stream))
+                                    B, T, Hq, Hkv, D, int(pos0), float(base), _dtype_code(q), _stream(stream))
     _check("diffattn_v2_fwd_rope", rc)
     return out
 

@@ -365,15 +365,14 @@ da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const flo
 }
 
 da_status diffattn_v2_fwd_rope(const void *q, void *k, const void *v, const float *lam, void *out, int B, int T,
-                               int Hq, int Hkv, int D, int64_t pos0, float base, float *cs, da_dtype dtype,
+                               int Hq, int Hkv, int D, int64_t pos0, float base, da_dtype dtype,
                                cudaStream_t stream) {
     if (dtype != DA_F32 && dtype != DA_BF16) return DA_ERR_BAD_DTYPE;
-    if (!q || !k || !v || !lam || !out || !cs) return DA_ERR_NULL_PTR;
+    if (!q || !k || !v || !lam || !out) return DA_ERR_NULL_PTR;
     if (B < 1 || T < 1 || Hq < 2 || Hkv < 1 || !(base > 0.f)) return DA_ERR_BAD_SHAPE;
     if (Hq % Hkv != 0 || ((Hq / Hkv) & 1)) return DA_ERR_BAD_GROUP;
     if (dtype != DA_BF16 || (D != 64 && D != 128)) return DA_ERR_UNSUPPORTED_DIM;
-    for (const void *ptr : {q, static_cast<const void *>(k), v, static_cast<const void *>(out),
-                            static_cast<const void *>(cs)})
+    for (const void *ptr : {q, static_cast<const void *>(k), v, static_cast<const void *>(out)})
         if (!aligned16(ptr)) return DA_ERR_MISALIGNED;
     uint32_t *err = nullptr;
     int nsm = 0;
@@ -390,14 +389,13 @@ da_status diffattn_v2_fwd_rope(const void *q, void *k, const void *v, const floa
         return DA_ERR_CUDA;
     m.q2 = m.q1;
     m.k2 = m.k1;
-    // k rotated in place and the cos / sin table written in one pass
+    // k rotated in place
     PrologueParams r{};
     r.k = k;
     r.Hq = 0; r.Hk = Hkv; r.D = D;
     r.B = B; r.T = T;
     r.pos0 = pos0;
     r.base = static_cast<double>(base);
-    r.cs_out = reinterpret_cast<float2 *>(cs);
     r.err = err;
     da_status st = cuda_status(launch_prologue(r, true, stream));
     if (st != DA_OK) return st;
@@ -410,7 +408,8 @@ da_status diffattn_v2_fwd_rope(const void *q, void *k, const void *v, const floa
     p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
     p.num_sms = nsm;
     p.err = err;
-    p.rope_cs = reinterpret_cast<const float4 *>(cs);
+    p.rope_pos0 = pos0;
+    p.rope_base = static_cast<double>(base);
     st = cuda_status(launch_prefill_v2_rope(m, p, D, stream));
     if (st == DA_OK) t_last_launches = 2;
     return st;

@@ -363,6 +363,37 @@ __device__ __forceinline__ float row_max128(const uint32_t *s) {
     return fmaxf(fmax3(a[0], a[1], a[2]), fmax3(fmax3(a[3], a[4], a[5]), a[6], a[7]));
 }
 
+// Rotary embedding: f_i = base^(-2i/D) for pair i < D/2, in double, kept as
+// the float pair fhi + flo.
+__device__ __forceinline__ void rope_freq(double base, int i, int D, float &fhi, float &flo) {
+    const double f = exp(-2.0 * static_cast<double>(i) / static_cast<double>(D) * log(base));
+    fhi = static_cast<float>(f);
+    flo = static_cast<float>(f - static_cast<double>(fhi));
+}
+// cos and sin of the angle pos * (fhi + flo).  The product is carried as a
+// float pair (its rounding error recovered with an fma) and reduced modulo
+// 2 pi against 2 pi split into three floats, each step an fma (Cody and
+// Waite's additive reduction): the reduced angle, in [-pi, pi], is within a
+// few 1e-7 rad of the exact one for any position below 2^24.  Its cosine and
+// sine come from the hardware approximations __cosf / __sinf, whose absolute
+// error on [-pi, pi] is below 2^-21.4.  Every kernel that rotates calls this
+// one function, so the prologue and the prefill's in-place Q rotation apply
+// the same bits.
+__device__ __forceinline__ float2 rope_cs(float pos, float fhi, float flo) {
+    constexpr double TWO_PI = 6.283185307179586476925286766559;
+    constexpr float P1 = static_cast<float>(TWO_PI);
+    constexpr float P2 = static_cast<float>(TWO_PI - static_cast<double>(P1));
+    constexpr float P3 = static_cast<float>(TWO_PI - static_cast<double>(P1) - static_cast<double>(P2));
+    constexpr float INV_2PI = static_cast<float>(1.0 / TWO_PI);
+    const float hi = pos * fhi;
+    const float lo = fmaf(pos, flo, fmaf(pos, fhi, -hi));
+    const float k = rintf(hi * INV_2PI);
+    float r = fmaf(-k, P1, hi);
+    r = fmaf(-k, P2, r);
+    r = fmaf(-k, P3, r) + lo;
+    return make_float2(__cosf(r), __sinf(r));
+}
+
 // Rotary embedding of one pair (a = x_i, b = x_{i + D/2}) by the angle whose
 // cosine and sine are c, s: (a c - b s, b c + a s), each an fma over a
 // rounded product, so that every kernel that rotates gets the same bits.

@@ -91,9 +91,8 @@ struct PrefillParams {
     void *sa1, *sa2;
     float *slse;
     int train_run;                 // DIFF V1 two-pass training forward: 1 = x and lse, 2 = a2
-    const float4 *rope_cs;         // V2 with rotary embedding: the cos / sin table, entry j * T + t
-                                   // = (cos, sin) of pairs 2j and 2j + 1 at token t; q rotated in
-                                   // shared memory as each Q tile lands
+    int64_t rope_pos0;             // V2 with rotary embedding (q rotated in shared memory as each
+    double rope_base;              // Q tile lands): position of token t = rope_pos0 + t, base
 };
 struct PrefillMaps {
     CUtensorMap q1, q2, k1, k2, v;
@@ -213,10 +212,6 @@ struct PrologueParams {
     int64_t pos0;                  // position of token t is pos0 + t
     double base;
     uint32_t *err;                 // error word (debug bounds checks)
-    float2 *cs_out;                // optional: the (cos, sin) the rotation applies at token t to
-                                   // pair i, at cs_out[((i / 2) * T + t) * 2 + i % 2], so that
-                                   // pairs 2j, 2j + 1 of a token are one 16-byte entry (batch 0
-                                   // writes it)
 };
 bool prologue_supported(int D, int C, int P);
 cudaError_t launch_prologue(const PrologueParams &p, bool bf16, cudaStream_t s);

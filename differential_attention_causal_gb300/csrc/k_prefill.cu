@@ -84,7 +84,8 @@ struct PreCfg {
     static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 4 + 2 + 7;
     static constexpr int OFF_LAM = OFF_BAR + NBAR * 8;        // 2 floats
     static constexpr int OFF_TSLOT = OFF_LAM + 8;
-    static constexpr int SMEM = OFF_TSLOT + 8 + 1024;         // + alignment slack
+    static constexpr int OFF_FREQ = OFF_TSLOT + 8;            // rotary f_i as float pairs (DQK / 2 x 2)
+    static constexpr int SMEM = OFF_FREQ + DQK * 4 + 1024;    // + alignment slack
     static constexpr int COL_S1 = 0, COL_S2 = BN, COL_O1 = 2 * BN, COL_O2 = 2 * BN + DV;
     static constexpr uint32_t TMEM_COLS = 512;
     // registers per thread after the split: warps 0-3 (producer, MMA,
@@ -139,43 +140,30 @@ __device__ __forceinline__ int snake_tile(int k, int c, int G, int NT) {
     return w < NT ? w : -1;
 }
 
-// Rotary embedding of one query row of both Q tiles in shared memory (each
-// DQK channels as DQK / 64 boxes of 128 rows x 128 bytes, 128-byte swizzle),
-// the pairs (i, i + DQK/2) for i in this thread's half of the pairs (half 0:
-// i < DQK/4, half 1: the rest), turned by the angles of cs[(i / 2) * ld]
-// (a (cos, sin, cos, sin) entry per two pairs), every value rounded back to
-// bf16.  8-channel chunk c of the first half pairs with chunk c + DQK/16 at
-// the same place in its group.  The two branches' threads of one row take
-// the two halves, so each table entry is read once per row.
+// Rotary embedding of one query row (position pos) of both Q tiles in shared
+// memory (each DQK channels as DQK / 64 boxes of 128 rows x 128 bytes,
+// 128-byte swizzle): the pairs (i, i + DQK/2) for i in this thread's half of
+// the pairs (half 0: i < DQK/4, half 1: the rest), turned by the angle
+// pos * f_i (f_i = fhi[i] + flo[i]), every value rounded back to bf16.
+// 8-channel chunk c of the first half pairs with chunk c + DQK/16 at the same
+// place in its group.  The two branches' threads of one row take the two
+// halves, so each (cos, sin) is formed once per row and applied to both tiles.
 template <int DQK>
-struct RopeTab {
-    static constexpr int MY = DQK / 32;    // 8-channel chunks of this thread per tile
-    float4 t[MY][4];
-};
-
-template <int DQK>
-__device__ __forceinline__ void rope_tab_load(RopeTab<DQK> &tab, int half, const float4 *cs, int ld) {
-    constexpr int MY = RopeTab<DQK>::MY;
-#pragma unroll
-    for (int c = 0; c < MY; ++c)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            tab.t[c][e] = __ldg(cs + static_cast<int64_t>(4 * (half * MY + c) + e) * ld);
-}
-
-template <int DQK>
-__device__ __forceinline__ void rope_q_row(uint8_t *q1, uint8_t *q2, int row, int half, const RopeTab<DQK> &tab) {
+__device__ __forceinline__ void rope_q_row(uint8_t *q1, uint8_t *q2, int row, int half, float pos,
+                                           const float *fhi, const float *flo) {
     constexpr int NCH = DQK / 16;          // 8-channel chunks per half of the channels
-    constexpr int MY = RopeTab<DQK>::MY;
+    constexpr int MY = DQK / 32;           // chunks of this thread per tile
     constexpr int BOX = 128 * 128;
     auto at = [&](uint8_t *q, int c) { return q + (c >> 3) * BOX + row * 128 + (((c & 7) ^ (row & 7)) << 4); };
-    const int c0 = half * MY;
+#pragma unroll 1
+    for (int c = half * MY; c < half * MY + MY; ++c) {
+        float2 cs[8];
 #pragma unroll
-    for (int tile = 0; tile < 2; ++tile) {
+        for (int e = 0; e < 8; ++e) cs[e] = rope_cs(pos, fhi[8 * c + e], flo[8 * c + e]);
 #pragma unroll
-        for (int c = 0; c < MY; ++c) {
-            uint4 *pa = reinterpret_cast<uint4 *>(at(tile ? q2 : q1, c0 + c));
-            uint4 *pb = reinterpret_cast<uint4 *>(at(tile ? q2 : q1, c0 + c + NCH));
+        for (int tile = 0; tile < 2; ++tile) {
+            uint4 *pa = reinterpret_cast<uint4 *>(at(tile ? q2 : q1, c));
+            uint4 *pb = reinterpret_cast<uint4 *>(at(tile ? q2 : q1, c + NCH));
             const uint4 ua = *pa, ub = *pb;
             const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
             uint32_t ra[4], rb[4];
@@ -183,9 +171,9 @@ __device__ __forceinline__ void rope_q_row(uint8_t *q1, uint8_t *q2, int row, in
             for (int k = 0; k < 4; ++k) {
                 const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wa[k]));
                 const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wb[k]));
-                const float4 cs4 = tab.t[c][k];
                 float2 xa, xb;
-                rope_rotate2(a, b, make_float2(cs4.x, cs4.z), make_float2(cs4.y, cs4.w), xa, xb);
+                rope_rotate2(a, b, make_float2(cs[2 * k].x, cs[2 * k + 1].x), make_float2(cs[2 * k].y, cs[2 * k + 1].y),
+                             xa, xb);
                 ra[k] = pack_bf16(xa.x, xa.y);
                 rb[k] = pack_bf16(xb.x, xb.y);
             }
@@ -513,6 +501,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t my_s = bar_s + 8 * br, my_p = bar_p + 16 * br, my_o = bar_o + 8 * br;
         const float sl2 = p.scale_log2;
         float *xch = reinterpret_cast<float *>(smem + C::OFF_X);
+        float *freq = reinterpret_cast<float *>(smem + C::OFF_FREQ);
         bool ok = true;
         float lam = 0.f, lam_init = 0.f;
         if (!V2) {
@@ -523,25 +512,27 @@ __global__ void __launch_bounds__(384, 1)
         int it = 0;
         // Rotary embedding: the two softmax threads of a row turn half of the
         // row's channel pairs each, in both Q tiles of work tile kk (query
-        // tile of work w), once the tiles have landed; the MMA thread issues
-        // the tile's first QK after all 8 warps have arrived.  Tile 0 is rotated before the first key tile,
+        // tile of work w), once the tiles have landed (cos and sin formed in
+        // registers, no table); the MMA thread issues the tile's first QK
+        // after all 8 warps have arrived.  Tile 0 is rotated before the first key tile,
         // tile kk + 1 right after the last P of tile kk (its Q load was issued
         // when the last QK of tile kk was), while the last PV runs.
         auto rotate_q = [&](int kk, int w) {
             if constexpr (ROPE) {
                 const int tq = (n_qt - 1 - w / per_qt) * C::BM + row;
                 ok = warp_wait(bar_qf, static_cast<uint32_t>(kk & 1), p.err, ok);
-                if (ok && tq < p.T && DA_CHECK(row < C::BM, p.err)) {
-                    RopeTab<DQK> tab;
-                    rope_tab_load<DQK>(tab, br, p.rope_cs + tq, p.T);
-                    rope_q_row<DQK>(smem + C::OFF_Q1, smem + C::OFF_Q2, row, br, tab);
-                }
+                if (ok && tq < p.T && DA_CHECK(row < C::BM, p.err))
+                    rope_q_row<DQK>(smem + C::OFF_Q1, smem + C::OFF_Q2, row, br, static_cast<float>(p.rope_pos0 + tq),
+                                    freq, freq + DQK / 2);
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_qr);
             }
         };
         if (ROPE) {
+            // f_i of the rotary embedding, once per CTA
+            for (int i = (warp - 4) * 32 + lane; i < DQK / 2; i += 256) rope_freq(p.rope_base, i, DQK, freq[i], freq[DQK / 2 + i]);
+            named_bar_sync(1, 256);
             const int w0 = snake_tile(0, cta, G, NT);
             if (w0 >= 0) rotate_q(0, w0);
         }
@@ -826,7 +817,7 @@ cudaError_t launch_paired(const PrefillMaps &m, const PrefillParams &p, int d, c
 }
 
 cudaError_t launch_prefill_v2_rope(const PrefillMaps &m, const PrefillParams &p, int d, cudaStream_t s) {
-    if (!p.rope_cs) return cudaErrorInvalidValue;
+    if (!(p.rope_base > 0.0)) return cudaErrorInvalidValue;
     if (d == 128) return launch_t<128, 128, true, false, false, true>(m, p, s);
     if (d == 64) return launch_t<64, 64, true, false, false, true>(m, p, s);
     return cudaErrorInvalidValue;

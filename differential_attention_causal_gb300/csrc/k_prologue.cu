@@ -96,37 +96,10 @@ struct Vec8<float> {
     }
 };
 
-// cos and sin of pos * (fhi + flo), fhi + flo = base^(-2i/D) as two floats.
-// The angle is carried as a float pair (the product's rounding error
-// recovered with an fma) and reduced modulo 2 pi against 2 pi split into
-// three floats, each step an fma (Cody and Waite's additive reduction); the
-// reduced angle is within a few 1e-7 rad of the exact one for any position
-// below 2^24.
-__device__ __forceinline__ float2 rope_cs(float pos, float fhi, float flo) {
-    constexpr double TWO_PI = 6.283185307179586476925286766559;
-    constexpr float P1 = static_cast<float>(TWO_PI);
-    constexpr float P2 = static_cast<float>(TWO_PI - static_cast<double>(P1));
-    constexpr float P3 = static_cast<float>(TWO_PI - static_cast<double>(P1) - static_cast<double>(P2));
-    constexpr float INV_2PI = static_cast<float>(1.0 / TWO_PI);
-    const float hi = pos * fhi;
-    const float lo = fmaf(pos, flo, fmaf(pos, fhi, -hi));
-    const float k = rintf(hi * INV_2PI);
-    float r = fmaf(-k, P1, hi);
-    r = fmaf(-k, P2, r);
-    r = fmaf(-k, P3, r) + lo;
-    float c, sn;
-    sincosf(r, &sn, &c);
-    return make_float2(c, sn);
-}
-
-// base^(-2i/D) in double, kept as a float pair (i < D/2), into shared memory
+// base^(-2i/D) for the D/2 pairs, once per CTA, into shared memory
 template <int D>
 __device__ __forceinline__ void rope_freqs(double base, float *freq_hi, float *freq_lo) {
-    for (int i = threadIdx.x; i < D / 2; i += blockDim.x) {
-        const double f = exp(-2.0 * static_cast<double>(i) / static_cast<double>(D) * log(base));
-        freq_hi[i] = static_cast<float>(f);
-        freq_lo[i] = static_cast<float>(f - static_cast<double>(freq_hi[i]));
-    }
+    for (int i = threadIdx.x; i < D / 2; i += blockDim.x) rope_freq(base, i, D, freq_hi[i], freq_lo[i]);
 }
 
 // Rotate every (token, head, 8-pair chunk) of q and k in tokens [t0, t0 + TS)
@@ -145,8 +118,6 @@ __device__ __forceinline__ void rope_tokens(const PrologueParams &p, int64_t t0,
         float2 csv = make_float2(1.f, 0.f);
         if (n < ntok) csv = rope_cs(static_cast<float>(p.pos0 + n % p.T), freq_hi[i], freq_lo[i]);
         cs[(tt * 8 + i % 8) * CH + i / 8] = csv;
-        if (p.cs_out && n < p.T && DA_CHECK(i < HALF, p.err))   // batch 0 writes the table
-            p.cs_out[(static_cast<int64_t>(i >> 1) * p.T + n) * 2 + (i & 1)] = csv;
     }
     __syncthreads();
     const int heads = h1 - h0;
@@ -352,7 +323,7 @@ __global__ void __launch_bounds__(LT) prologue_lambda(const PrologueParams p) {
 template <typename E>
 cudaError_t launch_e(const PrologueParams &p, cudaStream_t s) {
     const int64_t ntok = static_cast<int64_t>(p.B) * p.T;
-    if (p.q || p.k || p.cs_out) {
+    if (p.q || p.k) {
         const int64_t blocks = (ntok + TS - 1) / TS;
         if (blocks < 1 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
         // three 256-thread CTAs per SM (the launch bound), one wave

@@ -164,23 +164,19 @@ da_status diffattn_v2_fwd(const void *q, const void *k, const void *v, const flo
 /* DIFF V2 forward with the rotary embedding of q and k folded in: the result
  * of diffattn_prologue(q, k, ..., pos0, base) (rotate-half form, see there)
  * followed by diffattn_v2_fwd, bit for bit, with q left as it is.
- *   - k is rotated in place, as diffattn_prologue does, in a first launch that
- *     also writes the cos / sin table `cs`;
+ *   - k is rotated in place, as diffattn_prologue does (first launch);
  *   - q is read once per query tile by the prefill kernel and each tile is
- *     rotated in shared memory before its first product, so q is never
- *     written back (the tile is loaded once per query tile, so this repeats
- *     no work).
- * Arguments as for diffattn_v2_fwd, plus
- *   pos0, base : position of token t is pos0 + t; theta = pos * base^(-2i/D)
- *   cs         : caller-owned device workspace of T * D floats (fp32), 16-byte
- *                aligned; overwritten (the (cos, sin) pairs for the T positions),
- *                read by the second launch, free once the call's work is done.
+ *     rotated in shared memory before its first product (cos and sin formed
+ *     in registers with the same arithmetic as the prologue), so q is never
+ *     written back; the tile is loaded once per query tile, so this repeats
+ *     no work.
+ * Arguments as for diffattn_v2_fwd, plus pos0, base: the position of token t
+ * is pos0 + t, theta = pos * base^(-2i/D).  No workspace.
  * Supported: DA_BF16, D in {64, 128} (DA_F32 returns DA_ERR_UNSUPPORTED_DIM).
  * Errors as for the other entry points. */
 da_status diffattn_v2_fwd_rope(const void *q, void *k, const void *v, const float *lam,
                                void *out, int B, int T, int Hq, int Hkv, int D,
-                               int64_t pos0, float base, float *cs,
-                               da_dtype dtype, cudaStream_t stream);
+                               int64_t pos0, float base, da_dtype dtype, cudaStream_t stream);
 
 /* Paired Head Attention, causal (modded-nanogpt pull request "New Record:
  * Paired Head Attention (-3.5s, -65 steps)", section "Updates in PR"): the k,

@@ -4,9 +4,9 @@ by tile inside the prefill kernel.
 
 Two kinds of check:
   * bit equality with the two-call path it replaces (diffattn_prologue on q
-    and k, then diffattn_v2_fwd): both apply the same cos / sin values with
-    the same fma form and round the rotated values to bf16 the same way, so
-    the outputs and the rotated k must be identical, and q must be untouched;
+    and k, then diffattn_v2_fwd): both form cos / sin with one shared function
+    and rotate with the same fma form, rounding to bf16 the same way, so the
+    outputs and the rotated k must be identical, and q must be untouched;
   * parity with the fp64 oracle: oracle.v2_fwd on oracle.rope(q), oracle.rope(k)
     (rotary embedding of "How best to implement a differential transformer?",
     the issue's apply_rotary_pos_emb before the attention; DiffAttnV2 of
@@ -68,25 +68,22 @@ def test_fused_rope_vs_oracle(B, T, Hq, Hkv, D, pos0):
     assert_parity(out, ref, "bf16")
 
 
-def test_fused_rope_workspace_reuse_and_caller_table():
-    """The cos / sin workspace is the caller's: one buffer serves calls of
-    different T and position offsets, and after a call it holds the table of
-    that call's positions (checked against the oracle's angles)."""
+def test_fused_rope_positions_and_repeat_calls():
+    """Large position offsets (angles of ~10^5 rad, reduced modulo 2 pi in
+    float arithmetic) and calls of different T in a row: still equal to the
+    two-call path, and repeated calls give the same bits."""
     D = 128
-    cs = torch.empty(700 * D, dtype=torch.float32, device="cuda")
-    for T, pos0 in ((700, 0), (300, 90000), (1, 5)):
+    for T, pos0 in ((700, 0), (300, 90000), (1, 5), (129, 16000000)):
         x = _inputs(1, T, 4, 2, D, seed=T)
         xd = {n: v.cuda() for n, v in x.items()}
-        ref_out, _ = _two_call(xd, pos0)
-        out = binding().v2_fwd_rope(xd["q"], xd["k"], xd["v"], xd["lam"], pos0=pos0, cs=cs)
-        assert torch.equal(out, ref_out)
-        # entry (j, t) holds (cos, sin) of pairs 2j and 2j + 1
-        tab = cs[:T * D].view(D // 4, T, 2, 2).permute(0, 2, 1, 3).reshape(D // 2, T, 2).double().cpu().numpy()
-        pos = pos0 + np.arange(T, dtype=np.float64)
-        inv = 10000.0 ** (-2.0 * np.arange(D // 2, dtype=np.float64) / D)
-        ang = inv[:, None] * pos[None, :]
-        assert np.abs(tab[..., 0] - np.cos(ang)).max() < 2e-6
-        assert np.abs(tab[..., 1] - np.sin(ang)).max() < 2e-6
+        ref_out, ref_k = _two_call(xd, pos0)
+        outs = []
+        for _ in range(2):
+            k = xd["k"].clone()
+            outs.append(binding().v2_fwd_rope(xd["q"], k, xd["v"], xd["lam"], pos0=pos0))
+            assert torch.equal(k, ref_k)
+        assert torch.equal(outs[0], ref_out) and torch.equal(outs[1], ref_out)
+    assert binding().device_error() == 0
 
 
 def test_fused_rope_argument_checks():
@@ -94,15 +91,15 @@ def test_fused_rope_argument_checks():
     A = 0x10000
     f = lambda **kw: lib.diffattn_v2_fwd_rope(*[kw.get(n, dv) for n, dv in (  # noqa: E731
         ("q", A), ("k", A), ("v", A), ("lam", A), ("out", A), ("B", 1), ("T", 8), ("Hq", 4), ("Hkv", 2),
-        ("D", 128), ("pos0", 0), ("base", 1e4), ("cs", A), ("dtype", 1), ("stream", None))])
-    assert f(cs=None) == 1
+        ("D", 128), ("pos0", 0), ("base", 1e4), ("dtype", 1), ("stream", None))])
+    assert f(out=None) == 1
     assert f(q=None) == 1
     assert f(T=0) == 2
     assert f(base=0.0) == 2
     assert f(Hkv=3) == 4                       # Hq not a multiple of Hkv
     assert f(D=32) == 3
     assert f(dtype=0) == 3                     # fp32 not supported here
-    assert f(cs=A + 4) == 5
+    assert f(k=A + 4) == 5
     assert f(dtype=4) == 8
 
 
