@@ -12,10 +12,11 @@
 // Two kernels of 256 threads (q, k and x are disjoint, so one pass over each
 // is all the fusion there is; the two need different shapes):
 //   rotary, persistent (three CTAs per SM), blocks of TS = 16 tokens:
-//   1. cos / sin of the block's positions: the angle is formed and reduced
-//      modulo 2 pi with an extra float of precision (positions reach 10^5,
-//      where a plain float product would already be off by ~1e-3 rad), the
-//      sine and cosine of the reduced angle in float;
+//   1. cos / sin of the block's positions (rope_cs, shared with the prefill's
+//      in-place Q rotation): the angle is formed and reduced modulo 2 pi with
+//      an extra float of precision (positions reach 10^5, where a plain float
+//      product would already be off by ~1e-3 rad), the sine and cosine of
+//      the reduced angle from the hardware approximations;
 //   2. every (token, head, 8-pair chunk) of q and k: two 16-byte loads, the
 //      rotation in fp32, two stores;
 //   lambda, one CTA of 256 threads per 128 tokens:
