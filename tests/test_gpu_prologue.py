@@ -59,7 +59,7 @@ def test_rope_and_lambda_in_one_call(dtype):
     assert binding().device_error() == 0
 
 
-@pytest.mark.parametrize("C,P", [(128, 8), (2048, 64), (896, 24), (192, 16), (64, 8)])
+@pytest.mark.parametrize("C,P", [(128, 8), (2048, 64), (896, 24), (192, 16), (64, 8), (1024, 64), (2048, 16)])
 def test_lambda_only(C, P):
     lp = inputs.make_lambda_proj(3, 41, C, P, "bf16", seed=C)
     lam = binding().prologue(x=lp["x"].cuda(), w_lam=lp["w_lam"].cuda())
