@@ -155,7 +155,9 @@ struct BwdPreParams {
     const float *lq1, *lk1, *lq2, *lk2;          // V1 lambda vectors (d)
     float *dlq1, *dlk1, *dlq2, *dlk2;            // V1 outputs (d)
     float *dlam;                                 // V2 output (B, T, H)
-    float *dlam_rows;                            // V1 scratch (B, T, H)
+    float *dlam_rows;                            // V1 scratch: shares of dL/dlam (n_shares of them)
+    int64_t n_shares;                            // set by the launchers: one per row-pass block (tensor-core
+                                                 // path) or one per row (fp32 path)
     __nv_bfloat16 *g;                            // V1 g_1 = dx, (B, T, H, DV) contiguous
     float *dd, *cv;                              // outputs D (2, B, H, T); c (B, H, T)
     int B, T, H, d;

@@ -274,6 +274,8 @@ cudaError_t launch_t(const SimtBwdParams &p, cudaStream_t s) {
         pp.lq1 = p.lq1; pp.lk1 = p.lk1; pp.lq2 = p.lq2; pp.lk2 = p.lk2;
         pp.dlq1 = p.dlq1; pp.dlk1 = p.dlk1; pp.dlq2 = p.dlq2; pp.dlk2 = p.dlk2;
         pp.B = p.B; pp.T = p.T; pp.H = p.H; pp.d = DQK;
+        pp.n_shares = rows;
+        pp.err = p.err;
         e = launch_bwd_lambda(pp, s);
         if (e != cudaSuccess) return e;
     }
