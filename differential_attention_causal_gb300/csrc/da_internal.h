@@ -32,15 +32,19 @@ constexpr bool kDebugChecks = false;
 // host threads may launch concurrently (set() may then run more than once on
 // a device, which is harmless).  Devices past 63 run set() on every call.
 template <typename F>
-inline cudaError_t once_per_device(unsigned long long *done, F &&set) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+inline cudaError_t once_on_device(unsigned long long *done, int dev, F &&set) {
     const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
     if (bit && (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
-    e = set();
+    const cudaError_t e = set();
     if (e == cudaSuccess && bit) __atomic_fetch_or(done, bit, __ATOMIC_RELEASE);
     return e;
+}
+template <typename F>
+inline cudaError_t once_per_device(unsigned long long *done, F &&set) {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return once_on_device(done, dev, static_cast<F &&>(set));
 }
 
 // ---------------------------------------------------------------- SIMT fp32
