@@ -18,6 +18,7 @@ import pytest
 import torch
 
 import oracle
+import rescale_cases as rc
 from differential_attention_causal_gb300 import inputs
 
 from test_gpu_parity import assert_parity, binding, built  # noqa: F401  (fixture)
@@ -84,6 +85,46 @@ def test_fused_rope_positions_and_repeat_calls():
             assert torch.equal(k, ref_k)
         assert torch.equal(outs[0], ref_out) and torch.equal(outs[1], ref_out)
     assert binding().device_error() == 0
+
+
+def test_fused_rope_lazy_rescale():
+    """Planted per-key-tile score levels (as in rescale_cases) through the
+    Q-rotating kernel.  The planted components sit in channel pair
+    (D/2 - 1, D - 1), the slowest rotary frequency, with channel D - 1 of q
+    and k set to 0, and the rotary base is 1e30, so that this pair turns by
+    less than 1e-25 rad and keeps its values exactly (the planted keys are
+    large: a rotation would round them to bf16 differently than the fp64
+    oracle's exact rotation, a difference of the input's precision, not of
+    the kernel); the other pairs turn by up to pos rad as usual.  The
+    branches are checked on the host from the rotated bf16 q, k that the
+    two-call path produces (the same bits the kernel rotates to), then the
+    fused output must equal the two-call output and match the oracle."""
+    B, T, Hq, Hkv, D = 1, 1024, 4, 2, 128
+    G = Hq // Hkv
+    x = _inputs(B, T, Hq, Hkv, D, seed=11)
+    c = D // 2 - 1
+    lv = rc.key_channel0(T, D, rc.targets((T + 127) // 128)).to(x["k"].dtype)
+    x["q"][:, :, :, c] = rc.A
+    x["q"][:, :, :, D - 1] = 0
+    x["k"][:, :, :, c] = lv[None, :, None]
+    x["k"][:, :, :, D - 1] = 0
+    xd = {n: v.cuda() for n, v in x.items()}
+    base = 1e30
+    q2, ref_k = xd["q"].clone(), xd["k"].clone()
+    binding().prologue(q=q2, k=ref_k, base=base)
+    ref_out = binding().v2_fwd(q2, ref_k, xd["v"], xd["lam"])
+    qr = q2
+    rot = {"q": qr.cpu(), "k": ref_k.cpu()}
+    for head in (0, Hq - 1):
+        resc, stale = rc.v2_decisions(rot, 0, head, G)
+        assert (resc > 0).sum() >= 64, np.bincount(resc)
+        assert (stale > 4.0).sum() >= 64, stale.max()
+    k = xd["k"].clone()
+    out = binding().v2_fwd_rope(xd["q"], k, xd["v"], xd["lam"], base=base)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(k, ref_k)
+    ref = oracle.v2_fwd(oracle.rope(x["q"], base=base), oracle.rope(x["k"], base=base), x["v"], x["lam"])
+    assert_parity(out, ref, "bf16")
 
 
 def test_fused_rope_argument_checks():
