@@ -47,6 +47,16 @@
 // (0 .. 2 qt + 1) and differ only in the causal limit of the last two: row r
 // of branch e sees interleaved key columns c <= 2r + e - 128 (j - 2 qt).  The
 // epilogue writes O_e / l_e of each branch to its own head with direct stores.
+//
+// Rotary embedding (ROPE, V2): when a work tile's Q tiles land, the two
+// softmax threads of each row turn half of the row's channel pairs each, in
+// shared memory, before the tile's first QK (see rope_q_row); the MMA thread
+// then waits on a "Q rotated" barrier instead of "Q landed".
+//
+// L2: the Q tiles and the output are copied with an evict-first policy (read
+// or written once), K and V with evict-last (every later query tile of the
+// head reads them again), which keeps a head's K / V in L2 across its query
+// tiles: the headline workload's DRAM traffic equals its algorithmic bytes.
 #include "da_common.cuh"
 #include "da_internal.h"
 
