@@ -94,7 +94,6 @@ struct PrefillParams {
     // P = 2^(s * scale_log2 - lse_b) (fp32, (2, B, H, T))
     void *sa1, *sa2;
     float *slse;
-    int train_run;                 // DIFF V1 two-pass training forward: 1 = x and lse, 2 = a2
     int64_t rope_pos0;             // V2 with rotary embedding (q rotated in shared memory as each
     double rope_base;              // Q tile lands): position of token t = rope_pos0 + t, base
 };

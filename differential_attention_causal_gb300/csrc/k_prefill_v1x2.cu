@@ -105,14 +105,18 @@ __device__ __forceinline__ float sum_exp128(const uint32_t *s, float scale, floa
 
 // TRAIN (the training forward, DQK = 128): run 1 saves each branch's row
 // log-sum-exp (log2 units, m + log2 l of pass A) and x = a1 - lam a2 (fp32,
-// the RMSNorm input) besides the output; run 2 forms P = e2 / l2 alone in
-// pass B and saves a2 (fp32), writing no output.
-template <int DQK, bool TRAIN = false>
+// the RMSNorm input) besides the output; run 2 (A2) saves a2 (fp32) and
+// writes no output: with branch 2's log-sum-exp known from run 1 it needs
+// neither pass A nor branch 1, so it loads Q2, K2 and V only and computes
+// S2 and P = 2^(s2 scale - lse2) = e2 / l2 once per key (half the products
+// and a quarter of the exponentials of run 1).
+template <int DQK, bool TRAIN = false, bool A2 = false>
 __global__ void __launch_bounds__(384, 1)
     prefill_v1_twopass(const __grid_constant__ CUtensorMap tq1, const __grid_constant__ CUtensorMap tq2,
                        const __grid_constant__ CUtensorMap tk1, const __grid_constant__ CUtensorMap tk2,
                        const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
     using C = V1x2Cfg<DQK>;
+    static_assert(!A2 || (TRAIN && DQK == 128), "the a2 run: training forward, d = 128");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -186,10 +190,10 @@ __global__ void __launch_bounds__(384, 1)
             prefetch_tmap(&tk1);
             prefetch_tmap(&tk2);
             prefetch_tmap(&tv);
-            mbar_arrive_expect_tx(bar_q, 2 * C::Q_TILE);
+            mbar_arrive_expect_tx(bar_q, (A2 ? 1 : 2) * C::Q_TILE);
 #pragma unroll
             for (int c = 0; c < C::QB; ++c) {
-                tma_load_4d(sQ1 + c * C::BOX, &tq1, bar_q, 64 * c, h, q0, b);
+                if (!A2) tma_load_4d(sQ1 + c * C::BOX, &tq1, bar_q, 64 * c, h, q0, b);
                 tma_load_4d(sQ2 + c * C::BOX, &tq2, bar_q, 64 * c, h, q0, b);
             }
             int ki = 0, vi = 0;
@@ -229,16 +233,16 @@ __global__ void __launch_bounds__(384, 1)
                 ++vi;
                 return true;
             };
-            // pass A: K tiles in order
-            for (int j = 0; ok && j < n; ++j) ok = load_tile_k(j);
-            // pass B, in the order the MMA warp consumes the items
-            if (ok) ok = load_tile_k(0);
+            // pass A: K tiles in order (none for the a2 run)
+            for (int j = 0; !A2 && ok && j < n; ++j) ok = load_tile_k(j);
+            // pass B, in the order the MMA warp consumes the items (the a2 run: K2 items only)
+            if (ok) ok = A2 ? load_k(0, 1) : load_tile_k(0);
             for (int j = 0; ok && j < n; ++j) {
                 if (C::BIG) {
                     // K2 of the next tile first: its S2 is computed before this tile's PV
                     if (j + 1 < n) ok = load_k(j + 1, 1);
                     for (int it = 0; ok && it < C::V_ITEMS; ++it) ok = load_v(j, it);
-                    if (ok && j + 1 < n) ok = load_k(j + 1, 0);
+                    if (!A2 && ok && j + 1 < n) ok = load_k(j + 1, 0);
                 } else {
                     if (j + 1 < n) ok = load_tile_k(j + 1);
                     if (ok) ok = load_v(j, 0);
@@ -320,18 +324,31 @@ __global__ void __launch_bounds__(384, 1)
                 return true;
             };
             bool ok = mbar_wait(bar_q, 0, p.err);
+            if constexpr (A2) {
+                // S2 only; S2(j+1) as soon as S2(j) has been read, P(j) (over the
+                // S1 columns) read by PV(j); "S ready" is committed after PV(j),
+                // so that the softmax writes P(j+1) only once P(j) has been read.
+                if (ok) ok = qk_one(C::COL_S2, sQ2, 0);
+                if (ok) mma_commit(bar_sbf);
+                for (int j = 0; ok && j < n; ++j) {
+                    if (j + 1 < n)
+                        ok = mbar_wait(bar_sbe, static_cast<uint32_t>(j & 1), p.err) && qk_one(C::COL_S2, sQ2, 0);
+                    for (int it = 0; ok && it < C::V_ITEMS; ++it) ok = pv_item(j, it);
+                    if (ok && j + 1 < n) mma_commit(bar_sbf);
+                }
+            }
             // ------------------------------------------------------ pass A
-            for (int j = 0; ok && j < n; ++j) {
+            for (int j = 0; !A2 && ok && j < n; ++j) {
                 const int buf = j & 1;
                 if (j >= 2) ok = mbar_wait(bar_sae + 8 * buf, static_cast<uint32_t>(((j >> 1) - 1) & 1), p.err);
                 if (ok) ok = qk_pair(256 * buf, 256 * buf + 128, bar_saf + 16 * buf, bar_saf + 16 * buf + 8);
             }
             // pass B overwrites TMEM that pass A used: wait until both tiles' S were read
-            for (int j = (n > 2 ? n - 2 : 0); ok && j < n; ++j)
+            for (int j = (n > 2 ? n - 2 : 0); !A2 && ok && j < n; ++j)
                 ok = mbar_wait(bar_sae + 8 * (j & 1), static_cast<uint32_t>((j >> 1) & 1), p.err);
             // ------------------------------------------------------ pass B
-            if (ok) ok = qk_pair(C::COL_S1, C::COL_S2, 0, bar_sbf);
-            for (int j = 0; ok && j < n; ++j) {
+            if (!A2 && ok) ok = qk_pair(C::COL_S1, C::COL_S2, 0, bar_sbf);
+            for (int j = 0; !A2 && ok && j < n; ++j) {
                 if (C::BIG) {
                     // P(j) lies over S1 only: S2 of the next tile goes first, once
                     // this tile's S has been read, then the PV, then S1.
@@ -382,9 +399,9 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         uint32_t s[128];
 
-        // pass A: exact online row max / sum of branch br
+        // pass A: exact online row max / sum of branch br (not in the a2 run)
         float m = -INFINITY, l = 0.f;
-        for (int j = 0; j < n; ++j) {
+        for (int j = 0; !A2 && j < n; ++j) {
             const int buf = j & 1;
             ok = warp_wait(bar_saf + 16 * buf + 8 * br, static_cast<uint32_t>((j >> 1) & 1), p.err, ok);
             if (!ok) break;
@@ -415,14 +432,49 @@ __global__ void __launch_bounds__(384, 1)
         const float m2 = xch[256 + row], l2 = xch[384 + row];
         ok = warp_wait(bar_lam, 0, p.err, ok);
         const float lam = lam_smem[0], lam_init = lam_smem[1];
-        const bool a2_run = TRAIN && p.train_run == 2;
+        constexpr bool a2_run = A2;
         if (TRAIN && !a2_run && t < p.T && DA_CHECK(b < p.B && h < p.H, p.err))   // this branch's log-sum-exp
             p.slse[((static_cast<int64_t>(br) * p.B + b) * p.H + h) * p.T + t] = m + __log2f(l);
-        // P = c1 e1 - c2 e2: x = a1 - lam a2, or a2 alone (c1 = 0, c2 = -1 / l2)
-        const float c1 = a2_run ? 0.f : 1.f / l1, c2 = a2_run ? -1.f / l2 : lam / l2;
+        // P = c1 e1 - c2 e2: x = a1 - lam a2
+        const float c1 = 1.f / l1, c2 = lam / l2;
+
+        // the a2 run: P = 2^(s2 scale - lse2) from branch 2's saved log-sum-exp
+        if constexpr (A2) {
+            const float lse2 = (t < p.T && DA_CHECK(b < p.B && h < p.H, p.err))
+                                   ? p.slse[((static_cast<int64_t>(p.B) + b) * p.H + h) * p.T + t]
+                                   : 0.f;
+            for (int j = 0; j < n; ++j) {
+                ok = warp_wait(bar_sbf, static_cast<uint32_t>(j & 1), p.err, ok);
+                if (!ok) break;
+                tc_fence_after();
+                tmem_ld32(tmem + lane_off + C::COL_S2 + 64 * br, s);
+                tmem_ld32(tmem + lane_off + C::COL_S2 + 64 * br + 32, s + 32);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sbe);   // this tile's S2 has been read
+                if (j == qt) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (64 * br + c > row) s[c] = 0xff800000u;
+                }
+                const float2 sc2 = make_float2(sl2, sl2), nl2 = make_float2(-lse2, -lse2);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
+                                                sc2, nl2);
+                    s[c] = pack_bf16(ex2(x.x), ex2(x.y));
+                }
+                tmem_st32(tmem + lane_off + C::p_col(j, br), s);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_pb + 8 * br);
+            }
+        }
 
         // pass B: keys 64*br .. 64*br+63 of each tile
-        for (int j = 0; j < n; ++j) {
+        for (int j = 0; !A2 && j < n; ++j) {
             ok = warp_wait(bar_sbf, static_cast<uint32_t>(j & 1), p.err, ok);
             if (!ok) break;
             tc_fence_after();
@@ -519,24 +571,24 @@ __global__ void __launch_bounds__(384, 1)
     }
 }
 
-template <int DQK, bool TRAIN = false>
+template <int DQK, bool TRAIN = false, bool A2 = false>
 cudaError_t launch_t(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
     using C = V1x2Cfg<DQK>;
     static unsigned long long attr_done = 0;   // one bit per device
     const cudaError_t ea = once_per_device(&attr_done, [] {
         // the in-kernel register split must fit in the launch-time budget
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_v1_twopass<DQK, TRAIN>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, prefill_v1_twopass<DQK, TRAIN, A2>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs < C::REGS_NEEDED_AT_LAUNCH) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(prefill_v1_twopass<DQK, TRAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(prefill_v1_twopass<DQK, TRAIN, A2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::SMEM);
     });
     if (ea != cudaSuccess) return ea;
     const int n_qt = (p.T + C::BM - 1) / C::BM;
     const long long grid = static_cast<long long>(n_qt) * p.H * p.B;
     if (grid < 1 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    prefill_v1_twopass<DQK, TRAIN><<<static_cast<unsigned>(grid), 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v,
+    prefill_v1_twopass<DQK, TRAIN, A2><<<static_cast<unsigned>(grid), 384, C::SMEM, s>>>(m.q1, m.q2, m.k1, m.k2, m.v,
                                                                                      p);
     return cudaGetLastError();
 }
@@ -553,12 +605,10 @@ cudaError_t launch_prefill_v1_twopass(const PrefillMaps &m, const PrefillParams 
 
 cudaError_t launch_prefill_v1_twopass_train(const PrefillMaps &m, const PrefillParams &p, cudaStream_t s) {
     if (!p.sa1 || !p.sa2 || !p.slse) return cudaErrorInvalidValue;
-    PrefillParams q = p;
-    q.train_run = 1;   // output, x and the log-sum-exp
-    cudaError_t e = launch_t<128, true>(m, q, s);
+    // run 1: output, x and the log-sum-exp; run 2: a2, from branch 2's log-sum-exp
+    cudaError_t e = launch_t<128, true, false>(m, p, s);
     if (e != cudaSuccess) return e;
-    q.train_run = 2;   // a2
-    return launch_t<128, true>(m, q, s);
+    return launch_t<128, true, true>(m, p, s);
 }
 
 }  // namespace da
