@@ -295,9 +295,11 @@ da_status diffattn_v1_decode(const void *q1, const void *q2, const void *k1_cach
  * DA_ERR_UNSUPPORTED_DIM.  The size functions take the same dtype.
  *
  * `saved` (DEVICE, caller-owned, at least *_train_saved_size() bytes,
- * 16-byte aligned) receives each branch's normalised attention output a_b
- * (bf16) and its log-sum-exp (fp32); its contents are private to this
- * library: pass it unchanged to the matching *_bwd call.  The forward output
+ * 16-byte aligned) receives what the backward needs -- V2: each branch's
+ * normalised attention output a_b (bf16); V1: x = a1 - lam a2, the RMSNorm
+ * input, and a2 (fp32) -- and each branch's row log-sum-exp (fp32); its
+ * contents are private to this library: pass it unchanged to the matching
+ * *_bwd call.  The forward output
  * is the same as the plain forward's.  `workspace` (DEVICE, at least
  * *_bwd_workspace_size() bytes) is scratch for the backward; contents on
  * entry are ignored.  Gradient outputs must not overlap any input; they are
