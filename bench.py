@@ -359,9 +359,20 @@ def run_aux(args, dev, peaks, peak_kind, binding) -> dict:
     for _ in range(10):
         f()
     t = time_steps(f, 100, None)
+    # the same call captured in a CUDA graph: the kernel without the host-side call overhead
+    f()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        f()
+    for _ in range(10):
+        graph.replay()
+    tg = time_steps(graph.replay, 100, None)
     aux["v1_fp32_tiny"] = {"workload": "v1_fp32_B1_T64_H2_d32", "ms_median": round(statistics.median(t), 5),
-                           "ms_min": round(min(t), 5), "launches": 1,
-                           "note": "fp32 on CUDA cores; latency-bound, no roofline claim"}
+                           "ms_min": round(min(t), 5), "kernel_ms_median": round(statistics.median(tg), 5),
+                           "launches": 1,
+                           "note": "fp32 on CUDA cores; ms_*: the C-ABI call (host checks included), "
+                                   "kernel_ms: replayed from a CUDA graph; latency-bound, no roofline claim"}
     del x, out
     section("aux v2_prefill")
     # DIFF V2 prefill

@@ -4,12 +4,14 @@
 // plain causal softmax attentions; V1 combines them as
 // RMSNorm(a1 - lam a2) (1 - lam_init), V2 as a1 - sigmoid(lam) a2.
 //
-// One warp owns one output row.  Lanes split the head dimension; every key
-// costs one warp-wide dot-product reduction per branch and an exact online
-// softmax update (running max m, running sum l, rescaled accumulator).  This
-// path exists for fp32 accuracy (the tf32 tensor-core rate would not hold a
-// 1e-4 bound after the RMSNorm) and for the small fp32 workloads; it is not
-// the throughput path.
+// One warp owns one output row and walks the keys 32 at a time: lane j forms
+// the scores of key j0 + j (its own dot products, q from shared memory), the
+// chunk's max and sum are two warp reductions per branch, and the exact online
+// softmax update (running max m, running sum l, rescaled accumulator) then
+// adds the chunk's P V with lanes over the value channels (p_j broadcast by a
+// shuffle).  This path exists for fp32 accuracy (the tf32 tensor-core rate
+// would not hold a 1e-4 bound after the RMSNorm) and for the small fp32
+// workloads; it is not the throughput path.
 #include "da_common.cuh"
 #include "da_internal.h"
 
@@ -21,6 +23,11 @@ __device__ __forceinline__ float warp_sum(float x) {
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
 
 template <int DQK, int DV>
 __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
@@ -30,7 +37,8 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
     const int64_t nrows = static_cast<int64_t>(p.B) * p.Tq * p.H;
     if (row >= nrows) return;
-    if ((ld_volatile_u32(p.err) & kErrFatal) != 0) {   // an earlier kernel gave up: do not compute
+    // an earlier kernel gave up: do not compute (decided for the whole warp)
+    if (__any_sync(0xffffffffu, (ld_volatile_u32(p.err) & kErrFatal) != 0)) {
         if (lane == 0) atomicOr(p.err, kErrAborted);
         return;
     }
@@ -52,9 +60,17 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
     const float *k2 = p.k2 + b * p.k_sb + hk * p.k_sh;
     const float *vv = p.v + b * p.v_sb + hk * p.v_sh;
 
-    float qa[NQ], qb[NQ];
+    // this row's q1, q2 in shared memory: every lane reads all channels
+    __shared__ __align__(16) float qsh[4][2][DQK];
+    const int w = threadIdx.x >> 5;
 #pragma unroll
-    for (int i = 0; i < NQ; ++i) { qa[i] = q1[lane + 32 * i]; qb[i] = q2[lane + 32 * i]; }
+    for (int i = 0; i < NQ; ++i) {
+        qsh[w][0][lane + 32 * i] = q1[lane + 32 * i];
+        qsh[w][1][lane + 32 * i] = q2[lane + 32 * i];
+    }
+    __syncwarp();
+    const float4 *qa4 = reinterpret_cast<const float4 *>(qsh[w][0]);
+    const float4 *qb4 = reinterpret_cast<const float4 *>(qsh[w][1]);
     const float scale = rsqrtf(static_cast<float>(DQK));
     float m1 = -INFINITY, m2 = -INFINITY, l1 = 0.f, l2 = 0.f;
     float o1[NV], o2[NV];
@@ -73,30 +89,57 @@ __global__ void __launch_bounds__(128) simt_fwd(SimtParams p) {
             nkeys = n;
         }
     }
-    for (int j = 0; j < nkeys; ++j) {
-        const float *kj1 = k1 + j * p.k_st;
-        const float *kj2 = k2 + j * p.k_st;
-        float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-            s1 = fmaf(qa[i], kj1[lane + 32 * i], s1);
-            s2 = fmaf(qb[i], kj2[lane + 32 * i], s2);
+    for (int j0 = 0; j0 < nkeys; j0 += 32) {
+        // scores of keys j0 .. j0 + 31, one per lane (past the last key: -inf)
+        const int j = j0 + lane;
+        float s1 = -INFINITY, s2 = -INFINITY;
+        if (j < nkeys) {
+            const float4 *kj1 = reinterpret_cast<const float4 *>(k1 + static_cast<int64_t>(j) * p.k_st);
+            const float4 *kj2 = reinterpret_cast<const float4 *>(k2 + static_cast<int64_t>(j) * p.k_st);
+            float d1 = 0.f, d2 = 0.f;
+#pragma unroll 8
+            for (int c4 = 0; c4 < DQK / 4; ++c4) {
+                const float4 x = kj1[c4], y = kj2[c4], qa = qa4[c4], qb = qb4[c4];
+                d1 = fmaf(qa.x, x.x, d1); d1 = fmaf(qa.y, x.y, d1); d1 = fmaf(qa.z, x.z, d1); d1 = fmaf(qa.w, x.w, d1);
+                d2 = fmaf(qb.x, y.x, d2); d2 = fmaf(qb.y, y.y, d2); d2 = fmaf(qb.z, y.z, d2); d2 = fmaf(qb.w, y.w, d2);
+            }
+            s1 = d1 * scale;
+            s2 = d2 * scale;
         }
-        s1 = warp_sum(s1) * scale;
-        s2 = warp_sum(s2) * scale;
-        const float n1 = fmaxf(m1, s1), n2 = fmaxf(m2, s2);
-        const float a1 = expf(m1 - n1), a2 = expf(m2 - n2);   // 0 on the first key
-        const float p1 = expf(s1 - n1), p2 = expf(s2 - n2);
-        l1 = l1 * a1 + p1;
-        l2 = l2 * a2 + p2;
+        const float n1 = fmaxf(m1, warp_max(s1)), n2 = fmaxf(m2, warp_max(s2));
+        const float a1 = expf(m1 - n1), a2 = expf(m2 - n2);   // 0 on the first chunk
+        const float p1 = j < nkeys ? expf(s1 - n1) : 0.f, p2 = j < nkeys ? expf(s2 - n2) : 0.f;
+        l1 = l1 * a1 + warp_sum(p1);
+        l2 = l2 * a2 + warp_sum(p2);
         m1 = n1;
         m2 = n2;
-        const float *vj = vv + j * p.v_st;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
-            const float x = vj[lane + 32 * i];
-            o1[i] = fmaf(p1, x, o1[i] * a1);
-            o2[i] = fmaf(p2, x, o2[i] * a2);
+            o1[i] *= a1;
+            o2[i] *= a2;
+        }
+        // O_b += sum_j p_j v_j over the chunk's keys, lanes over the channels;
+        // eight keys' value rows are loaded before they are used, so that
+        // their loads are in flight together
+        const int jn = nkeys - j0 < 32 ? nkeys - j0 : 32;
+        for (int g = 0; g < jn; g += 8) {
+            float vx[8][NV];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float *vj = vv + static_cast<int64_t>(j0 + g + u) * p.v_st;
+#pragma unroll
+                for (int i = 0; i < NV; ++i) vx[u][i] = g + u < jn ? vj[lane + 32 * i] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                // keys past the chunk's last have p = 0 and v = 0: adding them changes nothing
+                const float pa = __shfl_sync(0xffffffffu, p1, g + u), pb = __shfl_sync(0xffffffffu, p2, g + u);
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    o1[i] = fmaf(pa, vx[u][i], o1[i]);
+                    o2[i] = fmaf(pb, vx[u][i], o2[i]);
+                }
+            }
         }
     }
 
