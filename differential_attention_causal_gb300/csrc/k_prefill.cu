@@ -26,7 +26,9 @@
 // Per KV tile j the MMA warp issues   PV1(j) S1(j+1) ... PV2(j) S2(j+1):
 //   S_b = Q_b K_b^T      (SS MMA, K-major operands, 128-byte swizzle)
 //   P_b (bf16) is written by the softmax threads over the first 64 columns
-//   of S_b, and O_b += P_b V is a TS MMA (A = P from TMEM, B = V MN-major).
+//   of S_b in two key halves, and O_b += P_b V is a TS MMA (A = P from
+//   TMEM, B = V MN-major), per half as it is published (V1) or once both
+//   are (V2).
 // While branch 1's threads exponentiate, the tensor core runs branch 2's
 // products and vice versa.  The online softmax keeps a per-row reference
 // max and rescales O only when the running max grows by more than 2^8; P
@@ -106,6 +108,11 @@ struct PreCfg {
     // read out of TMEM (off the diagonal); measured on GB300: V1 d = 64 1-2 %
     // faster, V2 D = 128 1 % slower, so V1 only
     static constexpr bool LD_SPLIT = !V2;
+    // PV issued per key half as the softmax publishes each (P_HALVES) or once
+    // both halves are published; measured on GB300: halves keep V1 d = 64 1-2 %
+    // faster, the single wait makes V2 D = 128 and Paired Head Attention 2 %
+    // faster (one barrier wait fewer per branch and key tile in the MMA thread)
+    static constexpr bool P_HALVES = !V2;
     // one MMA-issuing thread per branch (warp 1: S1, O1; warp 2: S2, O2) instead
     // of one for both; measured on GB300 at the V1 d = 64 / V2 D = 128 prefill
     // shapes: 13 % / 25 % slower, so off
@@ -440,13 +447,16 @@ __global__ void __launch_bounds__(384, 1)
                     // then S_b of the next key tile (in order after the PV that reads P_b)
                     for (int br = br0; ok && br <= br1; ++br) {
                         const uint32_t colS = br ? C::COL_S2 : C::COL_S1, colO = br ? C::COL_O2 : C::COL_O1;
-                        ok = mbar_wait(bar_p + 16 * br, pj, p.err);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv_half(colO, colS, sv, 0, j > 0);
+                        if (C::P_HALVES) {
+                            ok = mbar_wait(bar_p + 16 * br, pj, p.err);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_pv_half(colO, colS, sv, 0, j > 0);
+                        }
                         ok = mbar_wait(bar_p + 16 * br + 8, pj, p.err);
                         if (!ok) break;
                         tc_fence_after();
+                        if (!C::P_HALVES) issue_pv_half(colO, colS, sv, 0, j > 0);
                         issue_pv_half(colO, colS, sv, 1, j > 0);
                         if (br == br1) {
                             mma_commit(bar_ve + 8 * vst);
@@ -617,8 +627,11 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     tmem_wait_st();
                 }
-                // P in two halves: the tensor core starts O += P V on keys 0-63
-                // while keys 64-127 are still being exponentiated.
+                // P in two halves: with P_HALVES the tensor core starts O += P V
+                // on keys 0-63 while keys 64-127 are still being exponentiated;
+                // without, the MMA thread waits for the second half only (the
+                // first half's store wait is kept: measured, dropping it costs V2
+                // the 2 % that the single wait gains).
                 l += exp_pack64(s, sl2, m_ref);
                 tmem_st32(tS + 0, s);
                 tmem_wait_st();
