@@ -17,7 +17,8 @@
 //               tile's last QK has been issued); K tiles (K1 and K2 for V1)
 //               into a KS-deep ring and V tiles into a VS-deep ring, causal
 //               tiles only, in the order the MMAs consume them.
-//   warp 1      TMEM owner and single-thread MMA issuer.
+//   warp 1      TMEM owner and MMA issuer (lane 0, or for V1 the converged
+//               warp with one elected lane issuing).
 //   warp 2      V1: the lambda scalar (lam_init and the two exp terms) into
 //               shared memory while the main loop runs.
 //   warps 4-7   softmax for branch 1 (thread = query row = TMEM lane)
@@ -117,6 +118,10 @@ struct PreCfg {
     // of one for both; measured on GB300 at the V1 d = 64 / V2 D = 128 prefill
     // shapes: 13 % / 25 % slower, so off
     static constexpr bool TWO_ISSUERS = false;
+    // the MMA issue loop run by all of warp 1, converged, each MMA and commit
+    // issued by one lane chosen with elect.sync, instead of by lane 0 alone;
+    // measured on GB300: V1 d = 64 2 % faster, V2 D = 128 8 % slower
+    static constexpr bool ELECT_ISSUE = !V2;
     static constexpr uint32_t NISS = TWO_ISSUERS ? 2 : 1;     // arrivals on stage-release barriers
     static constexpr int REGS_NEEDED_AT_LAUNCH = (128 * REGS_LOW + 256 * REGS_HIGH + 383) / 384;
     static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
@@ -384,7 +389,24 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
         // ------------------------------------------------------------ MMA
-        if (lane == 0 && (warp == 1 || C::TWO_ISSUERS)) {
+        if ((C::ELECT_ISSUE || lane == 0) && (warp == 1 || C::TWO_ISSUERS)) {
+            // issue primitives of this thread (lane 0) or of the converged warp
+            auto wait_i = [&](uint32_t bar, uint32_t parity, uint32_t *err) -> bool {
+                if constexpr (C::ELECT_ISSUE) return warp_wait(bar, parity, err, true);
+                else return mbar_wait(bar, parity, err);
+            };
+            auto ss_i = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+                if constexpr (C::ELECT_ISSUE) mma_ss_elect(d, a, b, idesc, acc);
+                else mma_ss(d, a, b, idesc, acc);
+            };
+            auto ts_i = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+                if constexpr (C::ELECT_ISSUE) mma_ts_elect(d, a, b, idesc, acc);
+                else mma_ts(d, a, b, idesc, acc);
+            };
+            auto commit_i = [&](uint32_t bar) {
+                if constexpr (C::ELECT_ISSUE) mma_commit_elect(bar);
+                else mma_commit(bar);
+            };
             // branches issued by this thread: both, or branch warp - 1
             const int br0 = C::TWO_ISSUERS ? warp - 1 : 0, br1 = C::TWO_ISSUERS ? warp - 1 : 1;
             // Descriptors are built once per operand; a K step only moves the
@@ -395,7 +417,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int ks = 0; ks < DQK / 16; ++ks) {
                     const uint32_t off = ((ks >> 2) * C::BOX + (ks & 3) * 32) >> 4;
-                    mma_ss(tmem + dcol, da + off, db + off, C::IDESC_QK, ks > 0 ? 1u : 0u);
+                    ss_i(tmem + dcol, da + off, db + off, C::IDESC_QK, ks > 0 ? 1u : 0u);
                 }
             };
             // O += P V over one half of the key tile (64 keys = 4 K-steps).
@@ -404,7 +426,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int k = 0; k < C::BN / 32; ++k) {
                     const int ks = half * (C::BN / 32) + k;
-                    mma_ts(tmem + dcol, tmem + pcol + ks * 8, dv + ((ks * 2048) >> 4), C::IDESC_PV,
+                    ts_i(tmem + dcol, tmem + pcol + ks * 8, dv + ((ks * 2048) >> 4), C::IDESC_PV,
                            (acc || ks > 0) ? 1u : 0u);
                 }
             };
@@ -414,15 +436,15 @@ __global__ void __launch_bounds__(384, 1)
                 return sbase + C::OFF_K + (kc % C::KS) * C::K_SLOT + ((br && !V2) ? C::K_TILE : 0);
             };
             auto wait_k = [&]() {
-                return mbar_wait(bar_kf + 8 * (kc % C::KS), static_cast<uint32_t>((kc / C::KS) & 1), p.err);
+                return wait_i(bar_kf + 8 * (kc % C::KS), static_cast<uint32_t>((kc / C::KS) & 1), p.err);
             };
             // S_b = Q_b K_b^T for this thread's branches, then the K slot's release
             auto scores = [&]() {
                 for (int br = br0; br <= br1; ++br) {
                     issue_qk(br ? C::COL_S2 : C::COL_S1, br ? sQ2 : sQ1, k_at(br));
-                    mma_commit(bar_s + 8 * br);
+                    commit_i(bar_s + 8 * br);
                 }
-                mma_commit(bar_ke + 8 * (kc % C::KS));
+                commit_i(bar_ke + 8 * (kc % C::KS));
                 ++kc;
             };
             for (int k = 0; ok; ++k) {
@@ -430,36 +452,36 @@ __global__ void __launch_bounds__(384, 1)
                 if (w < 0) break;
                 const int n_kv = kv_tiles(n_qt - 1 - w / per_qt);
                 // Q of this tile landed (and, with the rotary embedding, rotated in place)
-                ok = mbar_wait(ROPE ? bar_qr : bar_qf, static_cast<uint32_t>(tc & 1), p.err) && wait_k();
+                ok = wait_i(ROPE ? bar_qr : bar_qf, static_cast<uint32_t>(tc & 1), p.err) && wait_k();
                 if (!ok) break;
                 tc_fence_after();
                 scores();
-                if (n_kv == 1) mma_commit(bar_qe);
+                if (n_kv == 1) commit_i(bar_qe);
                 for (int j = 0; ok && j < n_kv; ++j, ++it) {
                     const uint32_t pj = static_cast<uint32_t>(it & 1);
                     const int vst = vc % C::VS;
                     const uint32_t sv = sbase + C::OFF_V + vst * C::V_SLOT;
                     const bool more = j + 1 < n_kv;
-                    ok = mbar_wait(bar_vf + 8 * vst, static_cast<uint32_t>((vc / C::VS) & 1), p.err);
+                    ok = wait_i(bar_vf + 8 * vst, static_cast<uint32_t>((vc / C::VS) & 1), p.err);
                     // the first PV of a tile overwrites O: the previous epilogue must have read it
-                    if (ok && j == 0 && tc > 0) ok = mbar_wait(bar_od, static_cast<uint32_t>((tc - 1) & 1), p.err);
+                    if (ok && j == 0 && tc > 0) ok = wait_i(bar_od, static_cast<uint32_t>((tc - 1) & 1), p.err);
                     // per branch: O_b += P_b V in two key halves as the softmax publishes them,
                     // then S_b of the next key tile (in order after the PV that reads P_b)
                     for (int br = br0; ok && br <= br1; ++br) {
                         const uint32_t colS = br ? C::COL_S2 : C::COL_S1, colO = br ? C::COL_O2 : C::COL_O1;
                         if (C::P_HALVES) {
-                            ok = mbar_wait(bar_p + 16 * br, pj, p.err);
+                            ok = wait_i(bar_p + 16 * br, pj, p.err);
                             if (!ok) break;
                             tc_fence_after();
                             issue_pv_half(colO, colS, sv, 0, j > 0);
                         }
-                        ok = mbar_wait(bar_p + 16 * br + 8, pj, p.err);
+                        ok = wait_i(bar_p + 16 * br + 8, pj, p.err);
                         if (!ok) break;
                         tc_fence_after();
                         if (!C::P_HALVES) issue_pv_half(colO, colS, sv, 0, j > 0);
                         issue_pv_half(colO, colS, sv, 1, j > 0);
                         if (br == br1) {
-                            mma_commit(bar_ve + 8 * vst);
+                            commit_i(bar_ve + 8 * vst);
                             ++vc;
                         }
                         if (more) {
@@ -469,14 +491,14 @@ __global__ void __launch_bounds__(384, 1)
                                 tc_fence_after();
                             }
                             issue_qk(colS, br ? sQ2 : sQ1, k_at(br));
-                            mma_commit(bar_s + 8 * br);
+                            commit_i(bar_s + 8 * br);
                             if (br == br1) {
-                                mma_commit(bar_ke + 8 * (kc % C::KS));
+                                commit_i(bar_ke + 8 * (kc % C::KS));
                                 ++kc;
-                                if (j + 2 == n_kv) mma_commit(bar_qe);   // last QK of the tile issued
+                                if (j + 2 == n_kv) commit_i(bar_qe);   // last QK of the tile issued
                             }
                         } else {
-                            mma_commit(bar_o + 8 * br);
+                            commit_i(bar_o + 8 * br);
                         }
                     }
                 }
@@ -484,8 +506,8 @@ __global__ void __launch_bounds__(384, 1)
             }
             // no MMA may be in flight when TMEM is released
             const uint32_t drain = warp == 1 ? bar_dr : bar_dr2;
-            mma_commit(drain);
-            mbar_wait(drain, 0, p.err);
+            commit_i(drain);
+            wait_i(drain, 0, p.err);
         }
     } else if (warp == 3) {
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
