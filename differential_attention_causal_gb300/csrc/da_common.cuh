@@ -151,6 +151,22 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(pol)
         : "memory");
 }
+// Warp-converged forms of the above: every lane executes them, one lane
+// chosen by elect.sync issues.
+__device__ __forceinline__ void tma_load_4d_hint_elect(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                                       int c0, int c1, int c2, int c3, uint64_t pol) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
 // tma_store_4d with an L2 cache policy.
 __device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2, int c3,
                                                   uint64_t pol) {

@@ -119,9 +119,12 @@ struct PreCfg {
     // shapes: 13 % / 25 % slower, so off
     static constexpr bool TWO_ISSUERS = false;
     // the MMA issue loop run by all of warp 1, converged, each MMA and commit
-    // issued by one lane chosen with elect.sync, instead of by lane 0 alone;
-    // measured on GB300: V1 d = 64 2 % faster, V2 D = 128 8 % slower
+    // issued by one lane chosen with elect.sync, instead of by lane 0 alone
+    // (whose loop runs divergent from the rest of its warp); measured on
+    // GB300: V1 d = 64 2 % faster, V2 D = 128 1 % slower
     static constexpr bool ELECT_ISSUE = !V2;
+    // the same for the TMA producer (warp 0): V1 d = 64 another 0.8 % faster
+    static constexpr bool ELECT_LOAD = !V2;
     static constexpr uint32_t NISS = TWO_ISSUERS ? 2 : 1;     // arrivals on stage-release barriers
     static constexpr int REGS_NEEDED_AT_LAUNCH = (128 * REGS_LOW + 256 * REGS_HIGH + 383) / 384;
     static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
@@ -287,7 +290,21 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
-        if (lane == 0) {
+        if (C::ELECT_LOAD || lane == 0) {
+            // load primitives of this thread (lane 0) or of the converged warp
+            auto wait_p = [&](uint32_t bar, uint32_t parity, uint32_t *err) -> bool {
+                if constexpr (C::ELECT_LOAD) return warp_wait(bar, parity, err, true);
+                else return mbar_wait(bar, parity, err);
+            };
+            auto expect_p = [&](uint32_t bar, uint32_t bytes) {
+                if constexpr (C::ELECT_LOAD) mbar_arrive_expect_tx_elect(bar, bytes);
+                else mbar_arrive_expect_tx(bar, bytes);
+            };
+            auto load4_p = [&](uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2, int c3,
+                               uint64_t pol) {
+                if constexpr (C::ELECT_LOAD) tma_load_4d_hint_elect(dst, m, bar, c0, c1, c2, c3, pol);
+                else tma_load_4d_hint(dst, m, bar, c0, c1, c2, c3, pol);
+            };
             prefetch_tmap(&tq1);
             prefetch_tmap(&tk1);
             prefetch_tmap(&tv);
@@ -303,18 +320,18 @@ __global__ void __launch_bounds__(384, 1)
             auto load_k = [&](int j, int hk, int b) -> bool {
                 const int st = kc % C::KS;
                 if (kc >= C::KS &&
-                    !mbar_wait(bar_ke + 8 * st, static_cast<uint32_t>((kc / C::KS - 1) & 1), p.err))
+                    !wait_p(bar_ke + 8 * st, static_cast<uint32_t>((kc / C::KS - 1) & 1), p.err))
                     return false;
                 const uint32_t dst = sbase + C::OFF_K + st * C::K_SLOT;
-                mbar_arrive_expect_tx(bar_kf + 8 * st, C::K_SLOT);
+                expect_p(bar_kf + 8 * st, C::K_SLOT);
 #pragma unroll
                 for (int c = 0; c < C::QB; ++c) {
                     if (PAIRED)   // 64 tokens x both heads of pair hk, interleaved
                         tma_load_5d(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, 0, hk, j * (C::BN / 2), b);
                     else
-                        tma_load_4d_hint(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b, pol_reuse);
+                        load4_p(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b, pol_reuse);
                     if (!V2)
-                        tma_load_4d_hint(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b,
+                        load4_p(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, hk, j * C::BN, b,
                                          pol_reuse);
                 }
                 ++kc;
@@ -323,16 +340,16 @@ __global__ void __launch_bounds__(384, 1)
             auto load_v = [&](int j, int hk, int b) -> bool {
                 const int st = vc % C::VS;
                 if (vc >= C::VS &&
-                    !mbar_wait(bar_ve + 8 * st, static_cast<uint32_t>((vc / C::VS - 1) & 1), p.err))
+                    !wait_p(bar_ve + 8 * st, static_cast<uint32_t>((vc / C::VS - 1) & 1), p.err))
                     return false;
                 const uint32_t dst = sbase + C::OFF_V + st * C::V_SLOT;
-                mbar_arrive_expect_tx(bar_vf + 8 * st, C::V_SLOT);
+                expect_p(bar_vf + 8 * st, C::V_SLOT);
 #pragma unroll
                 for (int c = 0; c < C::VB; ++c) {
                     if (PAIRED)
                         tma_load_5d(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, 0, hk, j * (C::BN / 2), b);
                     else
-                        tma_load_4d_hint(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b, pol_reuse);
+                        load4_p(dst + c * C::BOX, &tv, bar_vf + 8 * st, 64 * c, hk, j * C::BN, b, pol_reuse);
                 }
                 ++vc;
                 return true;
@@ -345,12 +362,12 @@ __global__ void __launch_bounds__(384, 1)
                 const int hq1 = V2 ? 2 * h : h, hq2 = V2 ? 2 * h + 1 : h;
                 const int hk = V2 ? (2 * h) / p.G : h;
                 // Q of this tile once the previous tile's last QK has been issued
-                if (tc > 0 && !mbar_wait(bar_qe, static_cast<uint32_t>((tc - 1) & 1), p.err)) break;
-                mbar_arrive_expect_tx(bar_qf, 2 * C::Q_TILE);
+                if (tc > 0 && !wait_p(bar_qe, static_cast<uint32_t>((tc - 1) & 1), p.err)) break;
+                expect_p(bar_qf, 2 * C::Q_TILE);
 #pragma unroll
                 for (int c = 0; c < C::QB; ++c) {
-                    tma_load_4d_hint(sQ1 + c * C::BOX, &tq1, bar_qf, 64 * c, hq1, qt * C::BM, b, pol_once);
-                    tma_load_4d_hint(sQ2 + c * C::BOX, &tq2, bar_qf, 64 * c, hq2, qt * C::BM, b, pol_once);
+                    load4_p(sQ1 + c * C::BOX, &tq1, bar_qf, 64 * c, hq1, qt * C::BM, b, pol_once);
+                    load4_p(sQ2 + c * C::BOX, &tq2, bar_qf, 64 * c, hq2, qt * C::BM, b, pol_once);
                 }
                 ++tc;
                 // consumption order: K0, (V_j, K_j+1) ...
@@ -361,11 +378,11 @@ __global__ void __launch_bounds__(384, 1)
                 }
             }
             // leave no copy in flight
-            if (tc > 0) mbar_wait(bar_qf, static_cast<uint32_t>((tc - 1) & 1), p.err);
+            if (tc > 0) wait_p(bar_qf, static_cast<uint32_t>((tc - 1) & 1), p.err);
             for (int k = (kc > C::KS ? kc - C::KS : 0); k < kc; ++k)
-                mbar_wait(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
+                wait_p(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
             for (int k = (vc > C::VS ? vc - C::VS : 0); k < vc; ++k)
-                mbar_wait(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
+                wait_p(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
         }
     } else if (warp == 1 || warp == 2) {
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
