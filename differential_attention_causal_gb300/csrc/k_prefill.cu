@@ -13,12 +13,16 @@
 // tiles, heaviest (most key tiles) first, so that every CTA gets the same
 // amount of causal work and one tile's epilogue overlaps the next tile's
 // loads and first products.
-//   warp 0      TMA producer: Q1, Q2 per work tile (as soon as the previous
+//   warp 0      TMA producer (converged, elected lane; lane 0 alone for
+//               Paired Head Attention): Q1, Q2 per work tile (as soon as the previous
 //               tile's last QK has been issued); K tiles (K1 and K2 for V1)
 //               into a KS-deep ring and V tiles into a VS-deep ring, causal
 //               tiles only, in the order the MMAs consume them.
-//   warp 1      TMEM owner and MMA issuer (lane 0, or for V1 the converged
-//               warp with one elected lane issuing).
+//   warp 1      TMEM owner and MMA issuer (the whole warp runs the issue
+//               loop converged; one lane chosen by elect.sync issues each
+//               MMA and commit).
+// The waits of these two roles and of the softmax warps are warp-uniform
+// vote loops (warp_wait_vote), so those warps never run a divergent branch.
 //   warp 2      V1: the lambda scalar (lam_init and the two exp terms) into
 //               shared memory while the main loop runs.
 //   warps 4-7   softmax for branch 1 (thread = query row = TMEM lane)
@@ -120,11 +124,12 @@ struct PreCfg {
     static constexpr bool TWO_ISSUERS = false;
     // the MMA issue loop run by all of warp 1, converged, each MMA and commit
     // issued by one lane chosen with elect.sync, instead of by lane 0 alone
-    // (whose loop runs divergent from the rest of its warp); measured on
-    // GB300: V1 d = 64 2 % faster, V2 D = 128 1 % slower
-    static constexpr bool ELECT_ISSUE = !V2;
-    // the same for the TMA producer (warp 0): V1 d = 64 another 0.8 % faster
-    static constexpr bool ELECT_LOAD = !V2;
+    // (whose loop runs divergent from the rest of its warp), and the same for
+    // the TMA producer (warp 0; not for Paired Head Attention, whose 5-D key
+    // loads stay on lane 0).  Measured on GB300 with the vote-based waits:
+    // V1 d = 64 2.7 % faster, V2 D = 128 0.7 % faster.
+    static constexpr bool ELECT_ISSUE = true;
+    static constexpr bool ELECT_LOAD = true;
     static constexpr uint32_t NISS = TWO_ISSUERS ? 2 : 1;     // arrivals on stage-release barriers
     static constexpr int REGS_NEEDED_AT_LAUNCH = (128 * REGS_LOW + 256 * REGS_HIGH + 383) / 384;
     static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false);
@@ -290,19 +295,20 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
-        if (C::ELECT_LOAD || lane == 0) {
+        constexpr bool kElectLoad = C::ELECT_LOAD && !PAIRED;
+        if (kElectLoad || lane == 0) {
             // load primitives of this thread (lane 0) or of the converged warp
             auto wait_p = [&](uint32_t bar, uint32_t parity, uint32_t *err) -> bool {
-                if constexpr (C::ELECT_LOAD) return warp_wait(bar, parity, err, true);
+                if constexpr (kElectLoad) return warp_wait_vote(bar, parity, err, true);
                 else return mbar_wait(bar, parity, err);
             };
             auto expect_p = [&](uint32_t bar, uint32_t bytes) {
-                if constexpr (C::ELECT_LOAD) mbar_arrive_expect_tx_elect(bar, bytes);
+                if constexpr (kElectLoad) mbar_arrive_expect_tx_elect(bar, bytes);
                 else mbar_arrive_expect_tx(bar, bytes);
             };
             auto load4_p = [&](uint32_t dst, const CUtensorMap *m, uint32_t bar, int c0, int c1, int c2, int c3,
                                uint64_t pol) {
-                if constexpr (C::ELECT_LOAD) tma_load_4d_hint_elect(dst, m, bar, c0, c1, c2, c3, pol);
+                if constexpr (kElectLoad) tma_load_4d_hint_elect(dst, m, bar, c0, c1, c2, c3, pol);
                 else tma_load_4d_hint(dst, m, bar, c0, c1, c2, c3, pol);
             };
             prefetch_tmap(&tq1);
@@ -409,7 +415,7 @@ __global__ void __launch_bounds__(384, 1)
         if ((C::ELECT_ISSUE || lane == 0) && (warp == 1 || C::TWO_ISSUERS)) {
             // issue primitives of this thread (lane 0) or of the converged warp
             auto wait_i = [&](uint32_t bar, uint32_t parity, uint32_t *err) -> bool {
-                if constexpr (C::ELECT_ISSUE) return warp_wait(bar, parity, err, true);
+                if constexpr (C::ELECT_ISSUE) return warp_wait_vote(bar, parity, err, true);
                 else return mbar_wait(bar, parity, err);
             };
             auto ss_i = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -564,7 +570,7 @@ __global__ void __launch_bounds__(384, 1)
         bool ok = true;
         float lam = 0.f, lam_init = 0.f;
         if (!V2) {
-            ok = warp_wait(bar_lam, 0, p.err, ok);
+            ok = warp_wait_vote(bar_lam, 0, p.err, ok);
             lam = lam_smem[0];
             lam_init = lam_smem[1];
         }
@@ -579,7 +585,7 @@ __global__ void __launch_bounds__(384, 1)
         auto rotate_q = [&](int kk, int w) {
             if constexpr (ROPE) {
                 const int tq = (n_qt - 1 - w / per_qt) * C::BM + row;
-                ok = warp_wait(bar_qf, static_cast<uint32_t>(kk & 1), p.err, ok);
+                ok = warp_wait_vote(bar_qf, static_cast<uint32_t>(kk & 1), p.err, ok);
                 if (ok && tq < p.T && DA_CHECK(row < C::BM, p.err))
                     rope_q_row<DQK>(smem + C::OFF_Q1, smem + C::OFF_Q2, row, br, static_cast<float>(p.rope_pos0 + tq),
                                     freq, freq + DQK / 2);
@@ -607,7 +613,7 @@ __global__ void __launch_bounds__(384, 1)
             const float lg = (V2 && !PAIRED && t < p.T) ? p.lam[(static_cast<int64_t>(b) * p.T + t) * p.H + h] : 0.f;
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < n_kv; ++j, ++it) {
-                ok = warp_wait(my_s, static_cast<uint32_t>(it & 1), p.err, ok);
+                ok = warp_wait_vote(my_s, static_cast<uint32_t>(it & 1), p.err, ok);
                 if (!ok) continue;
                 tc_fence_after();
                 uint32_t s[C::BN];
@@ -692,7 +698,7 @@ __global__ void __launch_bounds__(384, 1)
             // --------------------------------------------------- epilogue
             if constexpr (PAIRED) {
                 // each branch is one head of the pair: O_e / l_e to its rows, directly
-                ok = warp_wait(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
+                ok = warp_wait_vote(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
                 tc_fence_after();
                 const float il = 1.f / l;
                 __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + static_cast<int64_t>(b) * p.o_sb +
@@ -719,8 +725,8 @@ __global__ void __launch_bounds__(384, 1)
                 if (lane == 0) mbar_arrive(bar_od);   // O read: the next tile's first PV may overwrite it
                 continue;
             }
-            ok = warp_wait(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
-            if (k > 0) ok = warp_wait(bar_stf, static_cast<uint32_t>((k - 1) & 1), p.err, ok);
+            ok = warp_wait_vote(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
+            if (k > 0) ok = warp_wait_vote(bar_stf, static_cast<uint32_t>((k - 1) & 1), p.err, ok);
             tc_fence_after();
             if (TRAIN && t < p.T && DA_CHECK(b < p.B && h < p.H, p.err))   // this branch's log-sum-exp (log2 units) for the backward
                 p.slse[((static_cast<int64_t>(br) * p.B + b) * p.H + h) * p.T + t] = m_ref + __log2f(l);
