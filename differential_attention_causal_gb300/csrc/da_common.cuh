@@ -189,6 +189,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32
                  "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+__device__ __forceinline__ void tma_load_4d_elect(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                                  int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
 // tma_store_4d with an L2 cache policy.
 __device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2, int c3,
                                                   uint64_t pol) {

@@ -27,6 +27,12 @@
 // the PV and only the next S1 follows it.
 // With dv = 256 a key tile of V is 64 KB, so V streams in 32-key items.
 //
+// Roles: warp 0 TMA producer and warp 1 MMA issuer, each run by the whole
+// warp converged with one lane chosen by elect.sync issuing (measured on
+// GB300: 3 % faster at B1 T32768 H12 than lane 0 alone); warp 2 the lambda
+// scalar; warps 4-11 two softmax warpgroups.  All waits of the converged
+// warps are warp-uniform vote loops (warp_wait_vote).
+//
 // Executed work per causal (query, key) pair: 2d (S1) + 2d (S2) in each pass
 // and 2 dv for the single PV = 12d, the same as two attentions with separate
 // PV products; exponentials: 2 per pass.
@@ -184,34 +190,38 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         regs_decrease<C::REGS_LOW>();
-        if (lane == 0) {
+        {
+            // the whole warp, converged; one elected lane issues each copy
+            auto wait_p = [&](uint32_t bar, uint32_t parity, uint32_t *err) {
+                return warp_wait_vote(bar, parity, err, true);
+            };
             prefetch_tmap(&tq1);
             prefetch_tmap(&tq2);
             prefetch_tmap(&tk1);
             prefetch_tmap(&tk2);
             prefetch_tmap(&tv);
-            mbar_arrive_expect_tx(bar_q, (A2 ? 1 : 2) * C::Q_TILE);
+            mbar_arrive_expect_tx_elect(bar_q, (A2 ? 1 : 2) * C::Q_TILE);
 #pragma unroll
             for (int c = 0; c < C::QB; ++c) {
-                if (!A2) tma_load_4d(sQ1 + c * C::BOX, &tq1, bar_q, 64 * c, h, q0, b);
-                tma_load_4d(sQ2 + c * C::BOX, &tq2, bar_q, 64 * c, h, q0, b);
+                if (!A2) tma_load_4d_elect(sQ1 + c * C::BOX, &tq1, bar_q, 64 * c, h, q0, b);
+                tma_load_4d_elect(sQ2 + c * C::BOX, &tq2, bar_q, 64 * c, h, q0, b);
             }
             int ki = 0, vi = 0;
             bool ok = true;
             // K ring item for tile j; `which` selects K1 / K2 when an item holds one of them
             auto load_k = [&](int j, int which) {
                 const int st = ki % C::KS;
-                if (ki >= C::KS && !mbar_wait(bar_ke + 8 * st, static_cast<uint32_t>((ki / C::KS - 1) & 1), p.err))
+                if (ki >= C::KS && !wait_p(bar_ke + 8 * st, static_cast<uint32_t>((ki / C::KS - 1) & 1), p.err))
                     return false;
                 const uint32_t dst = sbase + C::OFF_K + st * C::K_SLOT;
-                mbar_arrive_expect_tx(bar_kf + 8 * st, C::K_SLOT);
+                mbar_arrive_expect_tx_elect(bar_kf + 8 * st, C::K_SLOT);
 #pragma unroll
                 for (int c = 0; c < C::QB; ++c) {
                     if (C::BIG) {
-                        tma_load_4d(dst + c * C::BOX, which ? &tk2 : &tk1, bar_kf + 8 * st, 64 * c, h, j * C::BN, b);
+                        tma_load_4d_elect(dst + c * C::BOX, which ? &tk2 : &tk1, bar_kf + 8 * st, 64 * c, h, j * C::BN, b);
                     } else {
-                        tma_load_4d(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, h, j * C::BN, b);
-                        tma_load_4d(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, h, j * C::BN, b);
+                        tma_load_4d_elect(dst + c * C::BOX, &tk1, bar_kf + 8 * st, 64 * c, h, j * C::BN, b);
+                        tma_load_4d_elect(dst + C::K_TILE + c * C::BOX, &tk2, bar_kf + 8 * st, 64 * c, h, j * C::BN, b);
                     }
                 }
                 ++ki;
@@ -223,13 +233,13 @@ __global__ void __launch_bounds__(384, 1)
             };
             auto load_v = [&](int j, int item) {
                 const int st = vi % C::VS;
-                if (vi >= C::VS && !mbar_wait(bar_ve + 8 * st, static_cast<uint32_t>((vi / C::VS - 1) & 1), p.err))
+                if (vi >= C::VS && !wait_p(bar_ve + 8 * st, static_cast<uint32_t>((vi / C::VS - 1) & 1), p.err))
                     return false;
                 const uint32_t dst = sbase + C::OFF_V + st * C::V_SLOT;
-                mbar_arrive_expect_tx(bar_vf + 8 * st, C::V_SLOT);
+                mbar_arrive_expect_tx_elect(bar_vf + 8 * st, C::V_SLOT);
 #pragma unroll
                 for (int c = 0; c < C::VB; ++c)
-                    tma_load_4d(dst + c * C::V_BOX, &tv, bar_vf + 8 * st, 64 * c, h, j * C::BN + item * C::V_ROWS, b);
+                    tma_load_4d_elect(dst + c * C::V_BOX, &tv, bar_vf + 8 * st, 64 * c, h, j * C::BN + item * C::V_ROWS, b);
                 ++vi;
                 return true;
             };
@@ -249,19 +259,23 @@ __global__ void __launch_bounds__(384, 1)
                 }
             }
             // leave no copy in flight
-            mbar_wait(bar_q, 0, p.err);
+            wait_p(bar_q, 0, p.err);
             for (int k = (ki > C::KS ? ki - C::KS : 0); k < ki; ++k)
-                mbar_wait(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
+                wait_p(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
             for (int k = (vi > C::VS ? vi - C::VS : 0); k < vi; ++k)
-                mbar_wait(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
+                wait_p(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
         regs_decrease<C::REGS_LOW>();
-        if (lane == 0) {
+        {
+            // the whole warp, converged; one elected lane issues each MMA and commit
+            auto wait_i = [&](uint32_t bar, uint32_t parity, uint32_t *err) {
+                return warp_wait_vote(bar, parity, err, true);
+            };
             int ki = 0, vi = 0;
             auto wait_k = [&]() {
-                return mbar_wait(bar_kf + 8 * (ki % C::KS), static_cast<uint32_t>((ki / C::KS) & 1), p.err);
+                return wait_i(bar_kf + 8 * (ki % C::KS), static_cast<uint32_t>((ki / C::KS) & 1), p.err);
             };
             auto k_at = [&]() { return sbase + C::OFF_K + (ki % C::KS) * C::K_SLOT; };
             auto issue_qk = [&](uint32_t dcol, uint32_t sq, uint32_t sk) {
@@ -269,7 +283,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int ks = 0; ks < DQK / 16; ++ks) {
                     const uint32_t off = ((ks >> 2) * C::BOX + (ks & 3) * 32) >> 4;
-                    mma_ss(tmem + dcol, da + off, db + off, C::IDESC_QK, ks > 0 ? 1u : 0u);
+                    mma_ss_elect(tmem + dcol, da + off, db + off, C::IDESC_QK, ks > 0 ? 1u : 0u);
                 }
             };
             // S1 -> col1, S2 -> col2 for the next tile's K items; commits the K slots.
@@ -278,9 +292,9 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_after();
                 const uint32_t sk = k_at();
                 issue_qk(col1, sQ1, sk);
-                if (bar1) mma_commit(bar1);
+                if (bar1) mma_commit_elect(bar1);
                 if (C::BIG) {
-                    mma_commit(bar_ke + 8 * (ki % C::KS));
+                    mma_commit_elect(bar_ke + 8 * (ki % C::KS));
                     ++ki;
                     if (!wait_k()) return false;
                     tc_fence_after();
@@ -288,8 +302,8 @@ __global__ void __launch_bounds__(384, 1)
                 } else {
                     issue_qk(col2, sQ2, sk + C::K_TILE);
                 }
-                mma_commit(bar2);
-                mma_commit(bar_ke + 8 * (ki % C::KS));
+                mma_commit_elect(bar2);
+                mma_commit_elect(bar_ke + 8 * (ki % C::KS));
                 ++ki;
                 return true;
             };
@@ -298,8 +312,8 @@ __global__ void __launch_bounds__(384, 1)
                 if (!wait_k()) return false;
                 tc_fence_after();
                 issue_qk(col, sq, k_at());
-                if (bar) mma_commit(bar);
-                mma_commit(bar_ke + 8 * (ki % C::KS));
+                if (bar) mma_commit_elect(bar);
+                mma_commit_elect(bar_ke + 8 * (ki % C::KS));
                 ++ki;
                 return true;
             };
@@ -307,45 +321,45 @@ __global__ void __launch_bounds__(384, 1)
             // (64 keys) is waited for before its first K step.
             auto pv_item = [&](int j, int item) {
                 const int st = vi % C::VS;
-                if (!mbar_wait(bar_vf + 8 * st, static_cast<uint32_t>((vi / C::VS) & 1), p.err)) return false;
+                if (!wait_i(bar_vf + 8 * st, static_cast<uint32_t>((vi / C::VS) & 1), p.err)) return false;
                 const uint64_t dv = sdesc_sw128(sbase + C::OFF_V + st * C::V_SLOT, C::V_BOX, 1024);
 #pragma unroll
                 for (int ks = 0; ks < C::V_ROWS / 16; ++ks) {
                     const int g = item * (C::V_ROWS / 16) + ks;   // K step within the tile (16 keys)
                     if ((g & 3) == 0) {
-                        if (!mbar_wait(bar_pb + 8 * (g >> 2), static_cast<uint32_t>(j & 1), p.err)) return false;
+                        if (!wait_i(bar_pb + 8 * (g >> 2), static_cast<uint32_t>(j & 1), p.err)) return false;
                         tc_fence_after();
                     }
-                    mma_ts(tmem + C::COL_O, tmem + C::p_col(j, g >> 2) + 8 * (g & 3), dv + ((ks * 2048) >> 4),
+                    mma_ts_elect(tmem + C::COL_O, tmem + C::p_col(j, g >> 2) + 8 * (g & 3), dv + ((ks * 2048) >> 4),
                            C::IDESC_PV, (j > 0 || g > 0) ? 1u : 0u);
                 }
-                mma_commit(bar_ve + 8 * st);
+                mma_commit_elect(bar_ve + 8 * st);
                 ++vi;
                 return true;
             };
-            bool ok = mbar_wait(bar_q, 0, p.err);
+            bool ok = wait_i(bar_q, 0, p.err);
             if constexpr (A2) {
                 // S2 only; S2(j+1) as soon as S2(j) has been read, P(j) (over the
                 // S1 columns) read by PV(j); "S ready" is committed after PV(j),
                 // so that the softmax writes P(j+1) only once P(j) has been read.
                 if (ok) ok = qk_one(C::COL_S2, sQ2, 0);
-                if (ok) mma_commit(bar_sbf);
+                if (ok) mma_commit_elect(bar_sbf);
                 for (int j = 0; ok && j < n; ++j) {
                     if (j + 1 < n)
-                        ok = mbar_wait(bar_sbe, static_cast<uint32_t>(j & 1), p.err) && qk_one(C::COL_S2, sQ2, 0);
+                        ok = wait_i(bar_sbe, static_cast<uint32_t>(j & 1), p.err) && qk_one(C::COL_S2, sQ2, 0);
                     for (int it = 0; ok && it < C::V_ITEMS; ++it) ok = pv_item(j, it);
-                    if (ok && j + 1 < n) mma_commit(bar_sbf);
+                    if (ok && j + 1 < n) mma_commit_elect(bar_sbf);
                 }
             }
             // ------------------------------------------------------ pass A
             for (int j = 0; !A2 && ok && j < n; ++j) {
                 const int buf = j & 1;
-                if (j >= 2) ok = mbar_wait(bar_sae + 8 * buf, static_cast<uint32_t>(((j >> 1) - 1) & 1), p.err);
+                if (j >= 2) ok = wait_i(bar_sae + 8 * buf, static_cast<uint32_t>(((j >> 1) - 1) & 1), p.err);
                 if (ok) ok = qk_pair(256 * buf, 256 * buf + 128, bar_saf + 16 * buf, bar_saf + 16 * buf + 8);
             }
             // pass B overwrites TMEM that pass A used: wait until both tiles' S were read
             for (int j = (n > 2 ? n - 2 : 0); !A2 && ok && j < n; ++j)
-                ok = mbar_wait(bar_sae + 8 * (j & 1), static_cast<uint32_t>((j >> 1) & 1), p.err);
+                ok = wait_i(bar_sae + 8 * (j & 1), static_cast<uint32_t>((j >> 1) & 1), p.err);
             // ------------------------------------------------------ pass B
             if (!A2 && ok) ok = qk_pair(C::COL_S1, C::COL_S2, 0, bar_sbf);
             for (int j = 0; !A2 && ok && j < n; ++j) {
@@ -353,21 +367,21 @@ __global__ void __launch_bounds__(384, 1)
                     // P(j) lies over S1 only: S2 of the next tile goes first, once
                     // this tile's S has been read, then the PV, then S1.
                     if (j + 1 < n)
-                        ok = mbar_wait(bar_sbe, static_cast<uint32_t>(j & 1), p.err) && qk_one(C::COL_S2, sQ2, 0);
+                        ok = wait_i(bar_sbe, static_cast<uint32_t>(j & 1), p.err) && qk_one(C::COL_S2, sQ2, 0);
                     for (int it = 0; ok && it < C::V_ITEMS; ++it) ok = pv_item(j, it);
                     if (ok && j + 1 < n) ok = qk_one(C::COL_S1, sQ1, bar_sbf);
                 } else {
                     if (j + 1 < n) {
-                        ok = mbar_wait(bar_sbe, static_cast<uint32_t>(j & 1), p.err) &&
+                        ok = wait_i(bar_sbe, static_cast<uint32_t>(j & 1), p.err) &&
                              qk_pair(C::COL_S1, C::COL_S2, 0, bar_sbf);
                     }
                     if (ok) ok = pv_item(j, 0);
-                    if (ok) mma_commit(bar_pfree + 8 * (j & 1));
+                    if (ok) mma_commit_elect(bar_pfree + 8 * (j & 1));
                 }
             }
-            if (ok) mma_commit(bar_o);
-            mma_commit(bar_dr);
-            mbar_wait(bar_dr, 0, p.err);
+            if (ok) mma_commit_elect(bar_o);
+            mma_commit_elect(bar_dr);
+            wait_i(bar_dr, 0, p.err);
         }
     } else if (warp == 2) {
         regs_decrease<C::REGS_LOW>();
@@ -403,7 +417,7 @@ __global__ void __launch_bounds__(384, 1)
         float m = -INFINITY, l = 0.f;
         for (int j = 0; !A2 && j < n; ++j) {
             const int buf = j & 1;
-            ok = warp_wait(bar_saf + 16 * buf + 8 * br, static_cast<uint32_t>((j >> 1) & 1), p.err, ok);
+            ok = warp_wait_vote(bar_saf + 16 * buf + 8 * br, static_cast<uint32_t>((j >> 1) & 1), p.err, ok);
             if (!ok) break;
             tc_fence_after();
             const uint32_t ts = tmem + lane_off + 256 * buf + 128 * br;
@@ -430,7 +444,7 @@ __global__ void __launch_bounds__(384, 1)
         named_bar_sync(1, 256);
         const float m1 = xch[row], l1 = xch[128 + row];
         const float m2 = xch[256 + row], l2 = xch[384 + row];
-        ok = warp_wait(bar_lam, 0, p.err, ok);
+        ok = warp_wait_vote(bar_lam, 0, p.err, ok);
         const float lam = lam_smem[0], lam_init = lam_smem[1];
         constexpr bool a2_run = A2;
         if (TRAIN && !a2_run && t < p.T && DA_CHECK(b < p.B && h < p.H, p.err))   // this branch's log-sum-exp
@@ -444,7 +458,7 @@ __global__ void __launch_bounds__(384, 1)
                                    ? p.slse[((static_cast<int64_t>(p.B) + b) * p.H + h) * p.T + t]
                                    : 0.f;
             for (int j = 0; j < n; ++j) {
-                ok = warp_wait(bar_sbf, static_cast<uint32_t>(j & 1), p.err, ok);
+                ok = warp_wait_vote(bar_sbf, static_cast<uint32_t>(j & 1), p.err, ok);
                 if (!ok) break;
                 tc_fence_after();
                 tmem_ld32(tmem + lane_off + C::COL_S2 + 64 * br, s);
@@ -475,7 +489,7 @@ __global__ void __launch_bounds__(384, 1)
 
         // pass B: keys 64*br .. 64*br+63 of each tile
         for (int j = 0; !A2 && j < n; ++j) {
-            ok = warp_wait(bar_sbf, static_cast<uint32_t>(j & 1), p.err, ok);
+            ok = warp_wait_vote(bar_sbf, static_cast<uint32_t>(j & 1), p.err, ok);
             if (!ok) break;
             tc_fence_after();
             tmem_ld32(tmem + lane_off + C::COL_S1 + 64 * br, s);
@@ -509,7 +523,7 @@ __global__ void __launch_bounds__(384, 1)
                 s[c] = pack_bf16(pv[0], pv[1]);
             }
             if (!C::BIG && j >= 2)
-                ok = warp_wait(bar_pfree + 8 * (j & 1), static_cast<uint32_t>(((j >> 1) - 1) & 1), p.err, ok);
+                ok = warp_wait_vote(bar_pfree + 8 * (j & 1), static_cast<uint32_t>(((j >> 1) - 1) & 1), p.err, ok);
             tmem_st32(tmem + lane_off + C::p_col(j, br), s);
             tmem_wait_st();
             tc_fence_before();
@@ -518,7 +532,7 @@ __global__ void __launch_bounds__(384, 1)
         }
 
         // -------------------------------------------- epilogue: RMSNorm, scale
-        ok = warp_wait(bar_o, 0, p.err, ok);
+        ok = warp_wait_vote(bar_o, 0, p.err, ok);
         tc_fence_after();
         constexpr int HALF = C::DV / 2;
         const int col0 = br * HALF;
