@@ -591,7 +591,7 @@ __global__ void __launch_bounds__(384, 1)
                                     freq, freq + DQK / 2);
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_qr);
+                mbar_arrive_elect(bar_qr);
             }
         };
         if (ROPE) {
@@ -652,13 +652,10 @@ __global__ void __launch_bounds__(384, 1)
                     rmax = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
                 }
                 const float m_new = fmaxf(m_ref, rmax * sl2);
-                float alpha = 1.f;
                 const bool resc = m_new > m_ref + 8.f;
-                if (resc) {
-                    alpha = ex2(m_ref - m_new);
-                    l *= alpha;
-                    m_ref = m_new;
-                }
+                const float alpha = resc ? ex2(m_ref - m_new) : 1.f;
+                l *= alpha;
+                m_ref = resc ? m_new : m_ref;
                 if (j > 0 && __any_sync(0xffffffffu, resc)) {
                     // O_b is quiescent: PV_b(j-1) completed before S_b(j) was signalled.
 #pragma unroll 1
@@ -682,13 +679,13 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(my_p);
+                mbar_arrive_elect(my_p);
                 l += exp_pack64(s + 64, sl2, m_ref);
                 tmem_st32(tS + 32, s + 64);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(my_p + 8);
+                mbar_arrive_elect(my_p + 8);
             }
             if (ROPE) {
                 const int wn = snake_tile(k + 1, cta, G, NT);
@@ -722,7 +719,7 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_od);   // O read: the next tile's first PV may overwrite it
+                mbar_arrive_elect(bar_od);   // O read: the next tile's first PV may overwrite it
                 continue;
             }
             ok = warp_wait_vote(my_o, static_cast<uint32_t>(k & 1), p.err, ok);
@@ -789,7 +786,7 @@ __global__ void __launch_bounds__(384, 1)
             // O has been read: the next tile's first PV may overwrite it
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_od);
+            mbar_arrive_elect(bar_od);
             if (!V2) {
                 xch[256 + br * 128 + row] = ss;
                 named_bar_sync(1, 256);
@@ -816,7 +813,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_stg);
+            mbar_arrive_elect(bar_stg);
         }
     }
 
