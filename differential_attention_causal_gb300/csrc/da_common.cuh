@@ -135,6 +135,32 @@ __device__ __forceinline__ bool warp_wait_vote(uint32_t bar, uint32_t parity, ui
     }
 }
 
+// Waits for copies or MMAs that this CTA issued itself, before it exits or
+// frees TMEM: bounded by the time limit only, and not cut short when another
+// CTA has recorded an error, because shared memory and TMEM must not be
+// released under an asynchronous write.  Such phases always complete (the
+// copy or MMA was issued), so these return at once in practice.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint32_t *err) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitTimeoutNs) {
+            atomicOr(err, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool warp_wait_drain(uint32_t bar, uint32_t parity, uint32_t *err) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if ((i & 63u) == 63u && __any_sync(0xffffffffu, global_timer_ns() - t0 > kWaitTimeoutNs)) {
+            if ((threadIdx.x & 31) == 0) atomicOr(err, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

@@ -268,9 +268,9 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                                 b);
             }
             // leave no copy in flight
-            wait_c(bar_res, 0, p.err);
+            warp_wait_drain(bar_res, 0, p.err);
             for (int k = (j > ST ? j - ST : 0); k < j; ++k)
-                wait_c(bar_full + 8 * (k % ST), static_cast<uint32_t>((k / ST) & 1), p.err);
+                warp_wait_drain(bar_full + 8 * (k % ST), static_cast<uint32_t>((k / ST) & 1), p.err);
         }
     } else if (warp == 1 || (C::TWO_ISSUERS && warp == 2)) {
         // ------------------------------------------------------------ MMA
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 }
                 // no MMA of this thread may be in flight when TMEM is released
                 mma_commit_elect(bar_dra);
-                wait_c(bar_dra, 0, p.err);
+                warp_wait_drain(bar_dra, 0, p.err);
             } else if (C::TWO_ISSUERS) {
                 // dQ(j) waits for the rows' dS(j), which they form after S(j) completed
                 bool ok = true;
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 }
                 mma_commit_elect(bar_done);
                 mma_commit_elect(bar_dr);
-                wait_c(bar_dr, 0, p.err);
+                warp_wait_drain(bar_dr, 0, p.err);
             } else {
                 bool ok = wait_c(bar_res, 0, p.err);
                 int j = 0;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 mma_commit_elect(bar_done);
                 // no MMA may be in flight when TMEM is released
                 mma_commit_elect(bar_dr);
-                wait_c(bar_dr, 0, p.err);
+                warp_wait_drain(bar_dr, 0, p.err);
             }
         }
     } else if (warp >= 4) {
@@ -651,9 +651,9 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
         }
         // leave no copy in flight
         {
-            wait_c(bar_res, 0, p.err);
+            warp_wait_drain(bar_res, 0, p.err);
             for (int k = (it > ST ? it - ST : 0); k < it; ++k)
-                wait_c(bar_full + 8 * (k % ST), static_cast<uint32_t>((k / ST) & 1), p.err);
+                warp_wait_drain(bar_full + 8 * (k % ST), static_cast<uint32_t>((k / ST) & 1), p.err);
         }
     } else if (warp == 1 || (C::TWO_ISSUERS && warp == 2)) {
         // ------------------------------------------------------------ MMA
@@ -729,7 +729,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 }
                 // no MMA of this thread may be in flight when TMEM is released
                 mma_commit_elect(bar_dra);
-                wait_c(bar_dra, 0, p.err);
+                warp_wait_drain(bar_dra, 0, p.err);
             } else if (C::TWO_ISSUERS) {
                 // dV, dK(it) wait for the rows' P~, dS(it), formed after S(it) completed
                 bool ok = true;
@@ -741,7 +741,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 }
                 mma_commit_elect(bar_done);
                 mma_commit_elect(bar_dr);
-                wait_c(bar_dr, 0, p.err);
+                warp_wait_drain(bar_dr, 0, p.err);
             } else {
                 bool ok = wait_c(bar_res, 0, p.err);
                 int it = 0;
@@ -764,7 +764,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 }
                 mma_commit_elect(bar_done);
                 mma_commit_elect(bar_dr);
-                wait_c(bar_dr, 0, p.err);
+                warp_wait_drain(bar_dr, 0, p.err);
             }
         }
     } else if (warp >= 4) {

@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
             // Leave no copy in flight: wait for the last fills issued.
             const int64_t first = i > C::STAGES ? i - C::STAGES : 0;
             for (int64_t k = first; k < i; ++k)
-                mbar_wait(bar_full + 8 * static_cast<int>(k % C::STAGES),
-                          static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
+                mbar_wait_drain(bar_full + 8 * static_cast<int>(k % C::STAGES),
+                                static_cast<uint32_t>((k / C::STAGES) & 1), p.err);
         }
         return;
     }

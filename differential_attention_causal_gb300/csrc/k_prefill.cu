@@ -384,11 +384,15 @@ __global__ void __launch_bounds__(384, 1)
                 }
             }
             // leave no copy in flight
-            if (tc > 0) wait_p(bar_qf, static_cast<uint32_t>((tc - 1) & 1), p.err);
+            auto drain_p = [&](uint32_t bar, uint32_t parity) {
+                if constexpr (kElectLoad) warp_wait_drain(bar, parity, p.err);
+                else mbar_wait_drain(bar, parity, p.err);
+            };
+            if (tc > 0) drain_p(bar_qf, static_cast<uint32_t>((tc - 1) & 1));
             for (int k = (kc > C::KS ? kc - C::KS : 0); k < kc; ++k)
-                wait_p(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
+                drain_p(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1));
             for (int k = (vc > C::VS ? vc - C::VS : 0); k < vc; ++k)
-                wait_p(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
+                drain_p(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1));
         }
     } else if (warp == 1 || warp == 2) {
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();
@@ -530,7 +534,8 @@ __global__ void __launch_bounds__(384, 1)
             // no MMA may be in flight when TMEM is released
             const uint32_t drain = warp == 1 ? bar_dr : bar_dr2;
             commit_i(drain);
-            wait_i(drain, 0, p.err);
+            if constexpr (C::ELECT_ISSUE) warp_wait_drain(drain, 0, p.err);
+            else mbar_wait_drain(drain, 0, p.err);
         }
     } else if (warp == 3) {
         if (C::REG_SPLIT) regs_decrease<C::REGS_LOW>();

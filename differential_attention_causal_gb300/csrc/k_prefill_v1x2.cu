@@ -259,11 +259,11 @@ __global__ void __launch_bounds__(384, 1)
                 }
             }
             // leave no copy in flight
-            wait_p(bar_q, 0, p.err);
+            warp_wait_drain(bar_q, 0, p.err);
             for (int k = (ki > C::KS ? ki - C::KS : 0); k < ki; ++k)
-                wait_p(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
+                warp_wait_drain(bar_kf + 8 * (k % C::KS), static_cast<uint32_t>((k / C::KS) & 1), p.err);
             for (int k = (vi > C::VS ? vi - C::VS : 0); k < vi; ++k)
-                wait_p(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
+                warp_wait_drain(bar_vf + 8 * (k % C::VS), static_cast<uint32_t>((k / C::VS) & 1), p.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (ok) mma_commit_elect(bar_o);
             mma_commit_elect(bar_dr);
-            wait_i(bar_dr, 0, p.err);
+            warp_wait_drain(bar_dr, 0, p.err);
         }
     } else if (warp == 2) {
         regs_decrease<C::REGS_LOW>();
