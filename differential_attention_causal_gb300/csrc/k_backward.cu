@@ -35,7 +35,10 @@
 // have drained: with one issuer every wait left the tensor pipe idle.
 // The TMA warp and the two issuing warps run converged (one lane chosen by
 // elect.sync issues each copy, MMA and commit; their waits are warp-vote
-// loops), which measured 0.7 % faster on GB300 than lane 0 alone.
+// loops), which measured 0.7 % faster on GB300 than lane 0 alone.  The row
+// warps arrive on barriers through elect.sync as well (V2 2 % faster), but
+// keep the per-lane polling wait (warp_wait): the vote-based one costs the
+// V1 backward 4-5 %.
 #include <type_traits>
 
 #include "da_common.cuh"
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_sfree);   // the next S, dP may overwrite TMEM
+            mbar_arrive_elect(bar_sfree);   // the next S, dP may overwrite TMEM
             if (ok) {
                 const int key0 = j * C::BN + RC * wg;
                 // every key of this part is at or before every query of the tile: no mask
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 fence_async_smem();   // generic-proxy writes -> tensor core reads
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_rready);
+            mbar_arrive_elect(bar_rready);
         }
         // epilogue: dQ_b * scale -> bf16 rows (MODE 0: warpgroup wg takes branch
         // wg % 2, channels DQK / (NRG / 2) * (wg / 2) onwards; MODE 1: this CTA's
@@ -793,7 +796,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_sfree);   // the next S^T, dP^T may overwrite TMEM
+            mbar_arrive_elect(bar_sfree);   // the next S^T, dP^T may overwrite TMEM
             if (ok) {
                 // this warpgroup's RC query columns of the row vectors, 16 bytes at a time
                 const float4 *vec = reinterpret_cast<const float4 *>(smem + C::KV_OFF_RING + st * C::KV_STAGE +
@@ -875,7 +878,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
                 fence_async_smem();   // generic-proxy writes -> tensor core reads
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_rready);
+            mbar_arrive_elect(bar_rready);
         }
         // epilogue: dK_b * scale, dV -> bf16 rows of key j
         ok = warp_wait(bar_done, 0, p.err, ok);
