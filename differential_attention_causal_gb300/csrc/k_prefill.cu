@@ -108,11 +108,13 @@ struct PreCfg {
     // registers per thread after the split: warps 0-3 (producer, MMA,
     // lambda, idle) give up registers, the two softmax warpgroups take them
     static constexpr uint32_t REGS_LOW = 88, REGS_HIGH = 192;
-    static constexpr bool REG_SPLIT = !V2;                    // measured: helps V1, costs V2
-    // V1: the row max of keys 0-63 is taken while keys 64-127 are still being
-    // read out of TMEM (off the diagonal); measured on GB300: V1 d = 64 1-2 %
-    // faster, V2 D = 128 1 % slower, so V1 only
-    static constexpr bool LD_SPLIT = !V2;
+    // measured on GB300 with the converged issuing warps: V1 and V2 both
+    // faster with the split (V2 D = 128 4.7 %; before that change it cost V2)
+    static constexpr bool REG_SPLIT = true;
+    // the row max of keys 0-63 taken while keys 64-127 are still being read
+    // out of TMEM (off the diagonal): measured on GB300 with the converged
+    // issuing warps, V1 d = 64 1 % slower, V2 D = 128 2 % slower, so off
+    static constexpr bool LD_SPLIT = false;
     // PV issued per key half as the softmax publishes each (P_HALVES) or once
     // both halves are published; measured on GB300: halves keep V1 d = 64 1-2 %
     // faster, the single wait makes V2 D = 128 and Paired Head Attention 2 %
