@@ -82,11 +82,12 @@ struct PreCfg {
     static constexpr int K_SLOT = NK * K_TILE;
     static constexpr int V_SLOT = VB * BOX;
     static constexpr int OUT_TILE = VB * BOX;          // bf16 output tile staged for TMA stores
-    // Ring depths.  V(j) is needed one K-tile later than K(j) is freed, so
-    // when shared memory is short the V ring keeps the deeper ring (V1).
+    // Ring depths when shared memory is short: V2 D = 128 2 / 2; V1 d = 64
+    // K 3 / V 2 (measured on GB300 with the converged issuing warps: 0.4 %
+    // faster than K 2 / V 3).
     static constexpr bool ROOMY = 2 * Q_TILE + 3 * (K_SLOT + V_SLOT) + OUT_TILE + 2048 <= 232448;
-    static constexpr int KS = ROOMY ? 3 : 2;
-    static constexpr int VS = ROOMY ? 3 : (V2 ? 2 : 3);
+    static constexpr int KS = ROOMY ? 3 : (V2 ? 2 : 3);
+    static constexpr int VS = ROOMY ? 3 : 2;
     static constexpr int OFF_Q1 = 0;
     static constexpr int OFF_Q2 = Q_TILE;
     static constexpr int OFF_K = 2 * Q_TILE;
