@@ -49,7 +49,7 @@ SPINUP_S = 0.3
 # it was taken on (sha256 of the .cu file, first 16 hex digits).
 TRAFFIC_RECORDS: dict = {
     # profiles/prefill_onepass_v1_B4_T2048_H16_d64.md: dram__bytes_read.sum + dram__bytes_write.sum
-    "prefill_v1_d64": {"src_sha": "33460cedf5fc4813", "bytes_per_launch": 127620608 + 10393600},
+    "prefill_v1_d64": {"src_sha": "9d7bf7215e00e1fe", "bytes_per_launch": 127620608 + 10393600},
 }
 
 

@@ -61,13 +61,14 @@
 //
 // Rotary embedding (ROPE, V2): when a work tile's Q tiles land, the two
 // softmax threads of each row turn half of the row's channel pairs each, in
-// shared memory, before the tile's first QK (see rope_q_row); the MMA thread
+// shared memory, before the tile's first QK (see rope_q_row); the MMA warp
 // then waits on a "Q rotated" barrier instead of "Q landed".
 //
 // L2: the Q tiles and the output are copied with an evict-first policy (read
 // or written once), K and V with evict-last (every later query tile of the
 // head reads them again), which keeps a head's K / V in L2 across its query
-// tiles: the headline workload's DRAM traffic equals its algorithmic bytes.
+// tiles: the headline workload's DRAM traffic is within 3 % of its
+// algorithmic bytes.
 #include "da_common.cuh"
 #include "da_internal.h"
 
@@ -122,12 +123,13 @@ struct PreCfg {
     static constexpr bool LD_SPLIT = false;
     // PV issued per key half as the softmax publishes each (P_HALVES) or once
     // both halves are published; measured on GB300: halves keep V1 d = 64 1-2 %
-    // faster, the single wait makes V2 D = 128 and Paired Head Attention 2 %
-    // faster (one barrier wait fewer per branch and key tile in the MMA thread)
+    // faster, the single wait makes V2 D = 128 and Paired Head Attention 2-4 %
+    // faster (one barrier wait fewer per branch and key tile in the MMA warp)
     static constexpr bool P_HALVES = !V2;
-    // one MMA-issuing thread per branch (warp 1: S1, O1; warp 2: S2, O2) instead
+    // one MMA-issuing warp per branch (warp 1: S1, O1; warp 2: S2, O2) instead
     // of one for both; measured on GB300 at the V1 d = 64 / V2 D = 128 prefill
-    // shapes: 13 % / 25 % slower, so off
+    // shapes: 13 % / 25 % slower with lane-0 issuers, 19 % / 20 % slower with
+    // converged ones, so off
     static constexpr bool TWO_ISSUERS = false;
     // the MMA issue loop run by all of warp 1, converged, each MMA and commit
     // issued by one lane chosen with elect.sync, instead of by lane 0 alone
