@@ -35,7 +35,8 @@
 // have drained: with one issuer every wait left the tensor pipe idle.
 // The TMA warp and the two issuing warps run converged (one lane chosen by
 // elect.sync issues each copy, MMA and commit; their waits are warp-vote
-// loops), which measured 0.7 % faster on GB300 than lane 0 alone.  The row
+// loops), which measured 0.7 % faster on GB300 than lane 0 alone at d = 64
+// (the d = 128 split kernels 1.5-3 % slower, kept the same for one code path).  The row
 // warps arrive on barriers through elect.sync as well (V2 2 % faster), but
 // keep the per-lane polling wait (warp_wait): the vote-based one costs the
 // V1 backward 4-5 %.
