@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         {
+            // the whole warp, converged; one elected lane issues each copy
             auto wait_c = [&](uint32_t bar, uint32_t parity, uint32_t *err) {
                 return warp_wait_vote(bar, parity, err, true);
             };
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
     } else if (warp == 1 || (C::TWO_ISSUERS && warp == 2)) {
         // ------------------------------------------------------------ MMA
         {
+            // the whole warp, converged; one elected lane issues each MMA and commit
             auto wait_c = [&](uint32_t bar, uint32_t parity, uint32_t *err) {
                 return warp_wait_vote(bar, parity, err, true);
             };
@@ -662,6 +664,7 @@ __global__ void __launch_bounds__(BwdCfg<DQK, DV, V2, MODE>::THREADS, 1)
     } else if (warp == 1 || (C::TWO_ISSUERS && warp == 2)) {
         // ------------------------------------------------------------ MMA
         {
+            // the whole warp, converged; one elected lane issues each MMA and commit
             auto wait_c = [&](uint32_t bar, uint32_t parity, uint32_t *err) {
                 return warp_wait_vote(bar, parity, err, true);
             };
